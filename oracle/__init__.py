@@ -1,0 +1,18 @@
+"""fp64 CPU oracle for exact attention.
+
+TEST INFRASTRUCTURE ONLY: imported by the tests, by the smoke check and by the
+benchmark's CPU-baseline / reference arm.  The product path never imports it.
+"""
+from .attention_ref import (  # noqa: F401
+    attn_fwd_ref,
+    attn_fwd_ref_rows,
+    attn_bwd_ref,
+    bwd_preprocess_ref,
+    online_softmax_scalar,
+    online_softmax_blocks,
+    merge_two_blocks,
+    attn_fwd_tiled_ref,
+    max_abs_err,
+    rel_fro_err,
+    lse_max_abs_err,
+)

@@ -1,0 +1,146 @@
+/*
+ * fa.h -- C ABI of libfa.so: exact scaled-dot-product attention on one
+ * NVIDIA GB300 (sm_103a), forward and backward, computed tile by tile with
+ * running softmax statistics so that no N x N matrix is ever written to HBM.
+ *
+ * Sources (cited by page title and section):
+ *   [TRITON-IO]  "FlashAttention的Triton实现：IO-aware注意力机制底层原理"
+ *   [WHY-FAST]   "为什么Flash Attention能将注意力计算提速数倍而不损失精度"
+ *   [KERNEL-101] "GPU Kernel 入门：Triton / FlashAttention"
+ *
+ * Conventions shared by every entry point
+ *   - Tensors are row-major, contiguous, [B, H, N, d] bf16 (d innermost);
+ *     row statistics (LSE, D) are [B, H, N] fp32.  Q, K, V share one N.
+ *   - d must be 64 or 128, else FA_ERR_UNSUPPORTED.  N >= 0; N == 0 is a
+ *     no-op that returns FA_OK.  B, H >= 1.  B*H*ceil(N/128) must fit in
+ *     2^31 - 1.
+ *   - Every device pointer must be 16-byte aligned (fp32 vectors: 4-byte),
+ *     outputs must not overlap inputs or each other; otherwise
+ *     FA_ERR_INVALID_ARG.  The library never writes its inputs.
+ *   - scale is the softmax scale applied to Q K^T; it must be finite and > 0
+ *     (FA_ERR_INVALID_ARG otherwise).  The pages never write the scale; the
+ *     usual choice is 1/sqrt(d).
+ *   - causal != 0 keeps key j only for query rows i >= j.
+ *   - Ownership: the caller allocates and frees every buffer, including the
+ *     backward workspace.  The library holds no device allocation between
+ *     calls and keeps no pointer after a call returns.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t / CUstream; NULL
+ *     is the legacy default stream).  The return value reports argument
+ *     checks and launch errors (FA_ERR_CUDA: the launch failed; the CUDA
+ *     error is left in the runtime's last-error slot).  Faults inside a
+ *     kernel surface at the caller's next synchronisation.
+ *   - No exception ever crosses this interface.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t and CUstream are both `struct CUstream_st *` */
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,  /* null/misaligned/overlapping pointer, bad size or scale */
+  FA_ERR_UNSUPPORTED = 2,  /* head dim other than 64/128, or sizes beyond the limits */
+  FA_ERR_CUDA = 3,         /* a CUDA runtime/driver call or a launch failed */
+  FA_ERR_WORKSPACE = 4,    /* workspace missing, misaligned or too small */
+  FA_ERR_TIMEOUT = 5       /* a kernel gave up on a wait (see fa_debug_status) */
+} fa_status;
+
+/*
+ * Forward pass: O = softmax(scale * Q K^T [+ causal mask]) V, and
+ * LSE_i = log(sum_j exp(scale * q_i . k_j)) over the unmasked keys (natural
+ * log, fp32).  The pages' "exact attention": tiling plus the online softmax
+ * reach the plain result up to rounding ([WHY-FAST] "分块计算（Tiling）",
+ * "在线Softmax技巧"; [KERNEL-101] "FlashAttention 与在线 softmax：难点与解法").
+ * LSE replaces the pages' separately saved (m, l) ([WHY-FAST] "分块计算（Tiling）"
+ * saves both): LSE = m + ln l.
+ *   q, k, v  in : bf16 [B, H, N, d]
+ *   o        out: bf16 [B, H, N, d]
+ *   lse      out: fp32 [B, H, N]
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int B, int H, int N, int d, float scale, int causal,
+                 struct CUstream_st* stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs: the fp32 row term D [B, H, N],
+ * rounded up to 256 bytes.  Returns 0 for N <= 0 or invalid sizes.
+ */
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
+
+/*
+ * Backward pass of L(q, k, v) with upstream gradient dO = dL/dO, recomputing
+ * the probabilities from the saved LSE instead of storing them
+ * ([WHY-FAST] "反向传播中的重计算策略").  The gradients are the calculus of
+ * the forward definition (the pages give none):
+ *   dV = P^T dO, dP = dO V^T, D_i = sum_c dO_ic O_ic,
+ *   dS = P o (dP - D), dQ = scale dS K, dK = scale dS^T Q.
+ * Runs fa_bwd_preprocess, fa_bwd_dkdv and fa_bwd_dq in that order on `stream`.
+ *   q, k, v, o, dO in : bf16 [B, H, N, d]; o and lse from fa_fwd
+ *   lse            in : fp32 [B, H, N]
+ *   dq, dk, dv     out: bf16 [B, H, N, d]
+ *   workspace      scratch, >= fa_bwd_workspace_bytes(B, H, N, d) bytes,
+ *                  16-byte aligned, owned by the caller; its contents on
+ *                  return are the row term D (fp32 [B, H, N]).
+ */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                 const void* dO, void* dq, void* dk, void* dv,
+                 int B, int H, int N, int d, float scale, int causal,
+                 void* workspace, size_t workspace_bytes, struct CUstream_st* stream);
+
+/*
+ * Backward step 1: D_i = sum_c dO_ic O_ic (fp32 [B, H, N]), the row term of
+ * the softmax Jacobian (derived; not on the pages).  Memory-bound.
+ */
+fa_status fa_bwd_preprocess(const void* o, const void* dO, float* Dvec,
+                            int B, int H, int N, int d, struct CUstream_st* stream);
+
+/*
+ * Backward step 2: dK and dV.  For each 128-key tile, loops over the query
+ * tiles, recomputing P^T = exp(scale K Q^T - LSE) on chip.
+ *   Dvec in: fp32 [B, H, N] from fa_bwd_preprocess.
+ */
+fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const float* lse,
+                      const void* dO, const float* Dvec, void* dk, void* dv,
+                      int B, int H, int N, int d, float scale, int causal,
+                      struct CUstream_st* stream);
+
+/*
+ * Backward step 3: dQ.  For each 128-query tile, loops over the key tiles,
+ * recomputing P = exp(scale Q K^T - LSE) on chip.
+ */
+fa_status fa_bwd_dq(const void* q, const void* k, const void* v, const float* lse,
+                    const void* dO, const float* Dvec, void* dq,
+                    int B, int H, int N, int d, float scale, int causal,
+                    struct CUstream_st* stream);
+
+/* Static description of a status code (never NULL). */
+const char* fa_status_string(fa_status s);
+
+/*
+ * Device-side status of the kernels: FA_OK, or FA_ERR_TIMEOUT if some kernel
+ * gave up on a pipeline wait (a deadlock guard; each wait is bounded and the
+ * kernel unwinds instead of hanging).  Synchronous: reads device memory.
+ * reset != 0 clears the recorded state.  FA_ERR_CUDA if the read fails.
+ */
+fa_status fa_debug_status(int reset);
+
+/* Site code of the first recorded timeout (0 if none); valid after fa_debug_status. */
+unsigned int fa_debug_site(void);
+
+/*
+ * Text describing the last FA_ERR_CUDA returned on the calling thread: which
+ * call failed and the CUDA error string.  Static storage, never NULL.
+ */
+const char* fa_last_error_detail(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

@@ -1,0 +1,456 @@
+// Forward pass of exact attention on sm_103a: tiled over 128-row query tiles
+// and 128-key tiles with running softmax statistics, so the N x N score and
+// probability matrices never leave the SM.
+//
+// Method (cited by page title and section):
+//   * tiling with the query tile held on chip and K/V tiles streamed in the
+//     inner loop: "FlashAttention的Triton实现：IO-aware注意力机制底层原理",
+//     sections "分块策略：SRAM容量限制下的精打细算" and "FA1 vs FA2：循环顺序的工程权衡";
+//   * the running (m, l, acc) update and final division by l:
+//     "为什么Flash Attention能将注意力计算提速数倍而不损失精度", section
+//     "在线Softmax技巧" (two-block merge), and "GPU Kernel 入门：Triton /
+//     FlashAttention", section "FlashAttention 与在线 softmax：难点与解法";
+//   * one fused kernel (scores -> mask -> softmax -> PV, one read of Q/K/V, one
+//     write of O): same page, section "核函数融合（Kernel Fusion）";
+//   * asynchronous tensor cores fed by TMA with a producer/consumer pipeline
+//     and two query tiles whose softmax alternates with the other tile's
+//     matrix products: same page, section "Flash Attention 3：拥抱Hopper架构".
+//
+// GB300 design (one CTA per SM, 384 threads = 3 warpgroups):
+//   warps 0-3  softmax for query tile 0 (thread = query row = TMEM lane)
+//   warps 4-7  softmax for query tile 1
+//   warp  8    TMA producer: Q0/Q1 once, then K_j, V_j through a ring of slots
+//   warp  9    TMEM owner and single-thread tcgen05.mma issuer
+//   warps 10-11 idle
+// The third warpgroup gives registers to the softmax warpgroups (setmaxnreg):
+// each softmax thread holds a full 128-score row in registers.
+// TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+d) O1 [256+d,256+2d).
+// P (bf16) overwrites the first 64 columns of its S tile and feeds O += P V
+// straight from TMEM.  Scores live in base-2 units: x = s * scale * log2(e).
+//
+// Lazy rescaling: the merge identity holds for any common reference value, so
+// a row keeps its reference max until a new block exceeds it by more than
+// 2^8; P values stay <= 256, and O is rescaled in TMEM only when some row of
+// the warp moved its reference.  The final O = acc / l is unchanged.
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+
+#include <cmath>
+
+namespace fa {
+namespace {
+
+__device__ unsigned int g_status_fwd = 0;
+
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <int D>
+struct FwdCfg {
+  static_assert(D == 64 || D == 128, "head dim");
+  static constexpr int kBoxes = D / 64;                     // 128-byte boxes per row
+  static constexpr uint32_t kBoxBytes = 128u * 128u;        // 128 rows x 128 B
+  static constexpr uint32_t kTileBytes = kBoxes * kBoxBytes;
+  static constexpr int kSlots = (D == 128) ? 4 : 8;         // K/V ring
+  static constexpr uint32_t kQOff = 0;
+  static constexpr uint32_t kSlotOff = 2 * kTileBytes;
+  static constexpr uint32_t kBarOff = kSlotOff + kSlots * kTileBytes;
+  // full[S], empty[S], q_full, s_full[2], p_full[2], o_done[2], drain, staged[2]
+  static constexpr int kBars = 2 * kSlots + 10;
+  static constexpr uint32_t kMiscOff = kBarOff + kBars * 8;
+  static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;  // + alignment slack
+  static constexpr int kThreads = 384;
+  static constexpr uint32_t kRegsSoftmax = 216;  // per thread, warpgroups 0-1
+  static constexpr uint32_t kRegsOther = 56;     // per thread, warpgroup 2
+  static constexpr uint32_t kRegsNeeded = 256 * kRegsSoftmax + 128 * kRegsOther;
+  __host__ __device__ static constexpr uint32_t col_s(int tile) { return tile ? 128u : 0u; }
+  __host__ __device__ static constexpr uint32_t col_o(int tile) { return tile ? 256u + D : 256u; }
+};
+
+struct FwdWork {
+  int bh, qt0, n0, n1, n;
+};
+
+__device__ __forceinline__ FwdWork fwd_work(int N, int n_pairs, bool causal) {
+  FwdWork w;
+  w.bh = blockIdx.x / n_pairs;
+  const int pair = n_pairs - 1 - static_cast<int>(blockIdx.x % n_pairs);  // heavy tiles first
+  const int n_qt = (N + 127) / 128;
+  w.qt0 = 2 * pair;
+  const int qt1 = w.qt0 + 1;
+  w.n0 = causal ? min(w.qt0 + 1, n_qt) : n_qt;
+  w.n1 = qt1 < n_qt ? (causal ? min(qt1 + 1, n_qt) : n_qt) : 0;
+  w.n = max(w.n0, w.n1);
+  return w;
+}
+
+template <int D>
+__device__ __forceinline__ void fwd_producer(const FwdWork& w, uint8_t* smem, uint64_t* full, uint64_t* empty,
+                                             uint64_t* q_full, const CUtensorMap* tmQ, const CUtensorMap* tmK,
+                                             const CUtensorMap* tmV, const CtaGuard& g) {
+  using C = FwdCfg<D>;
+  mbar_arrive_expect_tx(q_full, (w.n1 > 0 ? 2u : 1u) * C::kTileBytes);
+#pragma unroll
+  for (int b = 0; b < C::kBoxes; ++b)
+    tma_load_3d(smem + C::kQOff + b * C::kBoxBytes, tmQ, q_full, 64 * b, 128 * w.qt0, w.bh);
+  if (w.n1 > 0) {
+#pragma unroll
+    for (int b = 0; b < C::kBoxes; ++b)
+      tma_load_3d(smem + C::kQOff + C::kTileBytes + b * C::kBoxBytes, tmQ, q_full, 64 * b, 128 * (w.qt0 + 1),
+                  w.bh);
+  }
+  int issued = 0;
+  bool ok = true;
+  for (int j = 0; j < w.n && ok; ++j) {
+    for (int kind = 0; kind < 2; ++kind) {
+      const int idx = 2 * j + kind;
+      const int slot = idx % C::kSlots;
+      const uint32_t ph = (idx / C::kSlots) & 1;
+      if (!mbar_wait(&empty[slot], ph ^ 1u, g, kSiteFwd | 1u)) {
+        ok = false;
+        break;
+      }
+      mbar_arrive_expect_tx(&full[slot], C::kTileBytes);
+      uint8_t* dst = smem + C::kSlotOff + slot * C::kTileBytes;
+#pragma unroll
+      for (int b = 0; b < C::kBoxes; ++b)
+        tma_load_3d(dst + b * C::kBoxBytes, kind ? tmV : tmK, &full[slot], 64 * b, 128 * j, w.bh);
+      issued = idx + 1;
+    }
+  }
+  if (!ok) {  // unwinding: let copies already issued land before smem is released
+    mbar_drain(q_full, 0);
+    for (int idx = max(0, issued - C::kSlots); idx < issued; ++idx)
+      mbar_drain(&full[idx % C::kSlots], (idx / C::kSlots) & 1);
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void fwd_issue_s(uint32_t tmem_d, uint32_t q_addr, uint32_t k_addr) {
+  using C = FwdCfg<D>;
+  constexpr uint32_t idesc = idesc_bf16(128, 128, false, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk / 4) * C::kBoxBytes + (kk % 4) * 32;
+    tc_mma_ss(tmem_d, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024), idesc,
+              kk > 0 ? 1u : 0u);
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void fwd_issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_addr, bool acc) {
+  using C = FwdCfg<D>;
+  constexpr uint32_t idesc = idesc_bf16(128, D, false, true);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {  // 128 keys, 16 per MMA; P packs 2 keys per column
+    tc_mma_ts(tmem_o, tmem_p + kk * 8, sdesc_sw128(v_addr + kk * 2048, C::kBoxBytes, 1024), idesc,
+              (acc || kk > 0) ? 1u : 0u);
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void fwd_mma(const FwdWork& w, uint32_t tmem, uint32_t smem_base, uint64_t* full,
+                                        uint64_t* empty, uint64_t* q_full, uint64_t* s_full, uint64_t* p_full,
+                                        uint64_t* o_done, const CtaGuard& g) {
+  using C = FwdCfg<D>;
+  const uint32_t q_addr[2] = {smem_base + C::kQOff, smem_base + C::kQOff + C::kTileBytes};
+  auto slot_addr = [&](int idx) { return smem_base + C::kSlotOff + (idx % C::kSlots) * C::kTileBytes; };
+  auto slot_wait = [&](int idx) {
+    return mbar_wait(&full[idx % C::kSlots], (idx / C::kSlots) & 1, g, kSiteFwd | 2u);
+  };
+  if (!mbar_wait(q_full, 0, g, kSiteFwd | 3u)) return;
+  if (!slot_wait(0)) return;
+  if (w.n0 > 0) {
+    fwd_issue_s<D>(tmem + C::col_s(0), q_addr[0], slot_addr(0));
+    tc_commit(&s_full[0]);
+  }
+  if (w.n1 > 0) {
+    fwd_issue_s<D>(tmem + C::col_s(1), q_addr[1], slot_addr(0));
+    tc_commit(&s_full[1]);
+  }
+  tc_commit(&empty[0]);
+  for (int j = 0; j < w.n; ++j) {
+    const int iv = 2 * j + 1, ik = 2 * j + 2;
+    const bool next = j + 1 < w.n;
+    if (!slot_wait(iv)) return;
+    if (j < w.n0) {
+      if (!mbar_wait(&p_full[0], j & 1, g, kSiteFwd | 4u)) return;
+      tc_fence_after();
+      fwd_issue_pv<D>(tmem + C::col_o(0), tmem + C::col_s(0), slot_addr(iv), j > 0);
+      if (j == w.n0 - 1) tc_commit(&o_done[0]);
+    }
+    if (next) {
+      if (!slot_wait(ik)) return;
+      if (j + 1 < w.n0) {
+        fwd_issue_s<D>(tmem + C::col_s(0), q_addr[0], slot_addr(ik));
+        tc_commit(&s_full[0]);
+      }
+    }
+    if (j < w.n1) {
+      if (!mbar_wait(&p_full[1], j & 1, g, kSiteFwd | 5u)) return;
+      tc_fence_after();
+      fwd_issue_pv<D>(tmem + C::col_o(1), tmem + C::col_s(1), slot_addr(iv), j > 0);
+      if (j == w.n1 - 1) tc_commit(&o_done[1]);
+    }
+    tc_commit(&empty[iv % C::kSlots]);
+    if (next) {
+      if (j + 1 < w.n1) {
+        fwd_issue_s<D>(tmem + C::col_s(1), q_addr[1], slot_addr(ik));
+        tc_commit(&s_full[1]);
+      }
+      tc_commit(&empty[ik % C::kSlots]);
+    }
+  }
+}
+
+template <int D, bool CAUSAL>
+__device__ __forceinline__ void fwd_softmax(const FwdWork& w, int tile, uint32_t tmem, uint8_t* smem,
+                                            uint64_t* s_full, uint64_t* p_full, uint64_t* o_done,
+                                            uint64_t* staged, const CUtensorMap* tmO, float* __restrict__ lse, int N,
+                                            float scale_log2, const CtaGuard& g) {
+  using C = FwdCfg<D>;
+  const int n_i = tile ? w.n1 : w.n0;
+  if (n_i == 0) return;
+  const int r = threadIdx.x & 127;                 // row within the tile = TMEM lane
+  const int qt = w.qt0 + tile;
+  const int row = qt * 128 + r;
+  const uint32_t lane_base = static_cast<uint32_t>((threadIdx.x >> 5) & 3) * 32u << 16;
+  const uint32_t tS = tmem + lane_base + C::col_s(tile);
+  const uint32_t tO = tmem + lane_base + C::col_o(tile);
+
+  float m_use = -INFINITY;  // reference max, base-2 units
+  float l = 0.f;
+  for (int j = 0; j < n_i; ++j) {
+    if (!mbar_wait(&s_full[tile], j & 1, g, kSiteFwd | 6u)) return;
+    __syncwarp();
+    tc_fence_after();
+    uint32_t s[4][32];
+    tmem_ld32(tS + 0, s[0]);
+    tmem_ld32(tS + 32, s[1]);
+    tmem_ld32(tS + 64, s[2]);
+    tmem_ld32(tS + 96, s[3]);
+    tmem_ld_wait(s[0]);
+    tmem_ld_fence(s[1]);
+    tmem_ld_fence(s[2]);
+    tmem_ld_fence(s[3]);
+
+    // keys kv0 .. kv0+lim-1 are visible to this row
+    const int kv0 = j * 128;
+    int lim = N - kv0;
+    if (CAUSAL) lim = min(lim, row - kv0 + 1);
+    if (lim < 128) {
+#pragma unroll
+      for (int c = 0; c < 128; ++c)
+        if (c >= lim) s[c / 32][c % 32] = __float_as_uint(-INFINITY);
+    }
+    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+    for (int c = 0; c < 128; ++c) mx[c % 4] = fmaxf(mx[c % 4], __uint_as_float(s[c / 32][c % 32]));
+    const float row_max = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * scale_log2;
+
+    if (j == 0) {
+      m_use = row_max;  // O is overwritten by the first P V product
+    } else {
+      const bool need = row_max > m_use + kRescaleThreshold;
+      if (__any_sync(0xffffffffu, need)) {
+        const float m_new = need ? row_max : m_use;
+        const float corr = (m_use == -INFINITY) ? 0.f : ex2_approx(m_use - m_new);
+        l *= corr;
+        m_use = m_new;
+#pragma unroll
+        for (int c = 0; c < D; c += 32) {
+          uint32_t o[32];
+          tmem_ld32(tO + c, o);
+          tmem_ld_wait(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
+          tmem_st32(tO + c, o);
+        }
+      }
+    }
+    __syncwarp();
+    const float m_off = (m_use == -INFINITY) ? 0.f : m_use;
+    float sum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {  // keys [64h, 64h+64) -> P columns [32h, 32h+32)
+      uint32_t pk[32];
+#pragma unroll
+      for (int c = 64 * h; c < 64 * h + 64; c += 2) {
+        const float p0 = ex2_approx(fmaf(__uint_as_float(s[c / 32][c % 32]), scale_log2, -m_off));
+        const float p1 = ex2_approx(fmaf(__uint_as_float(s[(c + 1) / 32][(c + 1) % 32]), scale_log2, -m_off));
+        sum[(c / 2) % 4] += p0 + p1;
+        pk[(c / 2) % 32] = pack_bf16x2(p0, p1);
+      }
+      tmem_st32(tS + 32 * h, pk);
+    }
+    l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
+    tmem_st_wait();
+    tc_fence_before();
+    mbar_arrive(&p_full[tile]);
+  }
+
+  // epilogue: O = acc / l -> bf16 -> swizzled staging (this tile's Q buffer) -> TMA store
+  if (!mbar_wait(&o_done[tile], 0, g, kSiteFwd | 7u)) return;
+  __syncwarp();
+  tc_fence_after();
+  const float inv_l = l > 0.f ? 1.f / l : 0.f;
+  const uint32_t stage = smem_u32(smem + C::kQOff + tile * C::kTileBytes);
+#pragma unroll
+  for (int c = 0; c < D; c += 32) {
+    uint32_t o[32];
+    tmem_ld32(tO + c, o);
+    tmem_ld_wait(o);
+    const uint32_t box = stage + (c / 64) * C::kBoxBytes + r * 128;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int chunk = (c % 64) / 8 + q;
+      float f[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(o[8 * q + e]) * inv_l;
+      st_shared_v4(box + ((chunk ^ (r & 7)) << 4), pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                   pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+    }
+  }
+  fence_proxy_async_smem();
+  mbar_arrive(&staged[tile]);
+  if (r == 0 && mbar_wait(&staged[tile], 0, g, kSiteFwd | 8u)) {
+#pragma unroll
+    for (int b = 0; b < C::kBoxes; ++b)
+      tma_store_3d(tmO, smem + C::kQOff + tile * C::kTileBytes + b * C::kBoxBytes, 64 * b, qt * 128, w.bh);
+    tma_store_commit();
+    tma_store_wait_read_all();
+  }
+  if (row < N) lse[static_cast<size_t>(w.bh) * N + row] = l > 0.f ? (m_use + __log2f(l)) * kLn2 : -INFINITY;
+}
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(384, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                  float* __restrict__ lse, int N, int n_pairs, float scale_log2) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + C::kSlots;
+  uint64_t* q_full = bars + 2 * C::kSlots;
+  uint64_t* s_full = q_full + 1;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* o_done = p_full + 2;
+  uint64_t* drain = o_done + 2;
+  uint64_t* staged = drain + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kMiscOff + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const FwdWork w = fwd_work(N, n_pairs, CAUSAL);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kSlots; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 128);
+      mbar_init(&o_done[i], 1);
+      mbar_init(&staged[i], 128);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_holder, 512);
+    tmem_relinquish();
+  }
+  if (warp == 8 && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmO);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const CtaGuard g{abort_flag, &g_status_fwd};
+
+  // Roles.  Each branch ends the kernel on its own (no shared tail), so the
+  // register budget set by setmaxnreg holds for the whole branch.  The MMA
+  // warp frees TMEM after every TMEM user has passed the end barrier.
+  if (warp >= 8) {
+    regs_dec<C::kRegsOther>();
+    if (warp == 8) {
+      if (lane == 0) fwd_producer<D>(w, smem, full, empty, q_full, &tmQ, &tmK, &tmV, g);
+    } else if (warp == 9) {
+      if (lane == 0) {
+        fwd_mma<D>(w, tmem, smem_u32(smem), full, empty, q_full, s_full, p_full, o_done, g);
+        tc_commit(drain);  // every MMA issued above has finished before TMEM is released
+        mbar_drain(drain, 0);
+      }
+      __syncwarp();
+      tc_fence_before();
+      named_bar_sync(1, 288);
+      tc_fence_after();
+      tmem_dealloc(tmem, 512);
+    }
+  } else {
+    regs_inc<C::kRegsSoftmax>();
+    fwd_softmax<D, CAUSAL>(w, warp >> 2, tmem, smem, s_full, p_full, o_done, staged, &tmO, lse, N, scale_log2,
+                           g);
+    __syncwarp();
+    tc_fence_before();
+    named_bar_sync(1, 288);
+  }
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const CUtensorMap& to, float* lse, const Shape& s, cudaStream_t st) {
+  using C = FwdCfg<D>;
+  auto kern = fa_fwd_kernel<D, CAUSAL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  // The warpgroups' register split must fit the launch allocation, or the
+  // softmax warpgroups would wait forever in setmaxnreg.inc.
+  cudaFuncAttributes attr;
+  e = cudaFuncGetAttributes(&attr, kern);
+  if (e != cudaSuccess) return e;
+  if (static_cast<uint32_t>(attr.numRegs) * C::kThreads < C::kRegsNeeded) return cudaErrorInvalidConfiguration;
+  const int n_qt = (s.N + 127) / 128;
+  const int n_pairs = (n_qt + 1) / 2;
+  const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
+  const dim3 grid(static_cast<unsigned>(s.B) * s.H * n_pairs);
+  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, to, lse, s.N, n_pairs, scale_log2);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& to, float* lse, const Shape& s, cudaStream_t st) {
+  if (s.d == 128) {
+    return s.causal ? launch_fwd_t<128, true>(tq, tk, tv, to, lse, s, st)
+                    : launch_fwd_t<128, false>(tq, tk, tv, to, lse, s, st);
+  }
+  return s.causal ? launch_fwd_t<64, true>(tq, tk, tv, to, lse, s, st)
+                  : launch_fwd_t<64, false>(tq, tk, tv, to, lse, s, st);
+}
+
+cudaError_t fwd_status(uint32_t* out, bool reset) {
+  unsigned int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_status_fwd, sizeof(v));
+  if (e != cudaSuccess) return e;
+  *out = v;
+  if (reset && v != 0) {
+    const unsigned int z = 0;
+    e = cudaMemcpyToSymbol(g_status_fwd, &z, sizeof(z));
+  }
+  return e;
+}
+
+}  // namespace fa

@@ -1,0 +1,218 @@
+"""Thin ctypes binding over libfa.so (argument marshalling only).
+
+The same names as the C ABI in ``include/fa.h``.  Tensors are torch CUDA
+tensors used only as device memory; every step of the computation runs in the
+library's kernels.  There is no fallback: a missing library, a missing GPU or
+a non-zero status raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional, Tuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfa.so")
+
+FA_OK = 0
+STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_CUDA",
+                4: "FA_ERR_WORKSPACE", 5: "FA_ERR_TIMEOUT"}
+
+_lib = None
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+_SZ = ctypes.c_size_t
+
+SIGNATURES = {
+    "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
+    "fa_bwd_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
+    "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
+    "fa_bwd_preprocess": (_I, [_P, _P, _P, _I, _I, _I, _I, _P]),
+    "fa_bwd_dkdv": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
+    "fa_bwd_dq": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
+    "fa_status_string": (ctypes.c_char_p, [_I]),
+    "fa_debug_status": (_I, [_I]),
+    "fa_debug_site": (ctypes.c_uint, []),
+    "fa_last_error_detail": (ctypes.c_char_p, []),
+}
+
+
+class FAError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        msg = f"{fn} failed: {status_string(status)}"
+        if status == 3:
+            try:
+                msg += f" [{load().fa_last_error_detail().decode()}]"
+            except Exception:
+                pass
+        super().__init__(msg)
+
+
+def load(path: str = LIB_PATH):
+    """Load libfa.so (once) and declare its signatures.  Raises if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is not built: run `python -c \"import __graft_entry__ as g; g.build()\"`")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load().fa_status_string(int(status)).decode()
+    except Exception:
+        return STATUS_NAMES.get(int(status), f"status {status}")
+
+
+def _check(fn: str, status: int):
+    if status != FA_OK:
+        raise FAError(fn, status)
+
+
+def _stream_ptr(stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _bhnd(t: torch.Tensor, name: str) -> Tuple[int, int, int, int]:
+    if not isinstance(t, torch.Tensor) or t.dim() != 4:
+        raise ValueError(f"{name} must be a 4-D [B, H, N, d] tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (device memory)")
+    if t.dtype != torch.bfloat16:
+        raise ValueError(f"{name} must be bfloat16")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return tuple(t.shape)
+
+
+def _same(shape, t: torch.Tensor, name: str):
+    if _bhnd(t, name) != shape:
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {shape}")
+
+
+def _vec(t: torch.Tensor, shape, name: str):
+    if not (t.is_cuda and t.dtype == torch.float32 and t.is_contiguous() and tuple(t.shape) == tuple(shape[:3])):
+        raise ValueError(f"{name} must be a contiguous fp32 CUDA tensor of shape {tuple(shape[:3])}")
+
+
+def default_scale(d: int) -> float:
+    return 1.0 / math.sqrt(d)
+
+
+# ---------------------------------------------------------------------------
+# Calls
+# ---------------------------------------------------------------------------
+
+def fa_fwd(q, k, v, scale: Optional[float] = None, causal: bool = False, out=None, lse=None, stream=None):
+    """O, LSE = attention(q, k, v): bf16 [B, H, N, d] in, O bf16 and LSE fp32 [B, H, N] out."""
+    shape = _bhnd(q, "q")
+    _same(shape, k, "k")
+    _same(shape, v, "v")
+    B, H, N, d = shape
+    scale = default_scale(d) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _same(shape, out, "out")
+    _vec(lse, shape, "lse")
+    st = load().fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                       B, H, N, d, scale, int(bool(causal)), _stream_ptr(stream))
+    _check("fa_fwd", st)
+    return out, lse
+
+
+def fa_bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(load().fa_bwd_workspace_bytes(B, H, N, d))
+
+
+def fa_bwd(q, k, v, o, lse, do, scale: Optional[float] = None, causal: bool = False,
+           dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """dQ, dK, dV for upstream gradient `do`, recomputing P from `lse`."""
+    shape = _bhnd(q, "q")
+    for t, n in ((k, "k"), (v, "v"), (o, "o"), (do, "do")):
+        _same(shape, t, n)
+    _vec(lse, shape, "lse")
+    B, H, N, d = shape
+    scale = default_scale(d) if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _same(shape, t, n)
+    need = fa_bwd_workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    st = load().fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), do.data_ptr(),
+                       dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, scale, int(bool(causal)),
+                       workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    _check("fa_bwd", st)
+    return dq, dk, dv
+
+
+def fa_bwd_preprocess(o, do, Dvec=None, stream=None):
+    shape = _bhnd(o, "o")
+    _same(shape, do, "do")
+    B, H, N, d = shape
+    if Dvec is None:
+        Dvec = torch.empty((B, H, N), dtype=torch.float32, device=o.device)
+    _vec(Dvec, shape, "Dvec")
+    _check("fa_bwd_preprocess", load().fa_bwd_preprocess(o.data_ptr(), do.data_ptr(), Dvec.data_ptr(),
+                                                          B, H, N, d, _stream_ptr(stream)))
+    return Dvec
+
+
+def fa_bwd_dkdv(q, k, v, lse, do, Dvec, scale: Optional[float] = None, causal: bool = False,
+                dk=None, dv=None, stream=None):
+    shape = _bhnd(q, "q")
+    for t, n in ((k, "k"), (v, "v"), (do, "do")):
+        _same(shape, t, n)
+    _vec(lse, shape, "lse")
+    _vec(Dvec, shape, "Dvec")
+    B, H, N, d = shape
+    scale = default_scale(d) if scale is None else float(scale)
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    _check("fa_bwd_dkdv", load().fa_bwd_dkdv(q.data_ptr(), k.data_ptr(), v.data_ptr(), lse.data_ptr(),
+                                              do.data_ptr(), Dvec.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                              B, H, N, d, scale, int(bool(causal)), _stream_ptr(stream)))
+    return dk, dv
+
+
+def fa_bwd_dq(q, k, v, lse, do, Dvec, scale: Optional[float] = None, causal: bool = False, dq=None,
+              stream=None):
+    shape = _bhnd(q, "q")
+    for t, n in ((k, "k"), (v, "v"), (do, "do")):
+        _same(shape, t, n)
+    _vec(lse, shape, "lse")
+    _vec(Dvec, shape, "Dvec")
+    B, H, N, d = shape
+    scale = default_scale(d) if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    _check("fa_bwd_dq", load().fa_bwd_dq(q.data_ptr(), k.data_ptr(), v.data_ptr(), lse.data_ptr(),
+                                          do.data_ptr(), Dvec.data_ptr(), dq.data_ptr(),
+                                          B, H, N, d, scale, int(bool(causal)), _stream_ptr(stream)))
+    return dq
+
+
+def fa_debug_status(reset: bool = False) -> int:
+    """FA_OK, or FA_ERR_TIMEOUT when a kernel gave up on a wait (synchronous)."""
+    return int(load().fa_debug_status(int(bool(reset))))
+
+
+def fa_debug_site() -> int:
+    return int(load().fa_debug_site())

@@ -1,0 +1,103 @@
+"""The C-ABI library: it builds, loads, exports what include/fa.h declares, and
+rejects bad arguments before touching a device (CPU only, no compute calls)."""
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+        pytest.skip("nvcc not available")
+    from io_aware_exact_14_gb300 import build, fa
+    build.build()
+    return fa.load()
+
+
+def declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for want in ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_status_string", "fa_debug_status"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from io_aware_exact_14_gb300 import fa
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in fa.SIGNATURES, f"binding lacks {name}"
+
+
+FAKE = 0x10000  # never dereferenced: every call below fails validation first
+BAD_ALIGN = FAKE + 8
+
+
+def fwd(lib, q=FAKE, k=FAKE + 0x100000, v=FAKE + 0x200000, o=FAKE + 0x300000, lse=FAKE + 0x400000,
+        B=1, H=1, N=128, d=64, scale=0.125, causal=0):
+    return lib.fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, None)
+
+
+def test_fwd_argument_checks(lib):
+    assert fwd(lib, d=96) == 2            # FA_ERR_UNSUPPORTED
+    assert fwd(lib, d=256) == 2
+    assert fwd(lib, N=0, q=0, k=0, v=0, o=0, lse=0) == 0  # empty problem is a no-op
+    assert fwd(lib, q=0) == 1             # FA_ERR_INVALID_ARG: null
+    assert fwd(lib, lse=0) == 1
+    assert fwd(lib, v=BAD_ALIGN) == 1     # misaligned tensor
+    assert fwd(lib, lse=FAKE + 0x400002) == 1
+    assert fwd(lib, B=0) == 1
+    assert fwd(lib, N=-1) == 1
+    assert fwd(lib, scale=0.0) == 1
+    assert fwd(lib, scale=float("nan")) == 1
+    assert fwd(lib, scale=-0.125) == 1
+    assert fwd(lib, o=FAKE) == 1          # output aliases q
+    assert fwd(lib, lse=FAKE + 0x300000 + 64) == 1  # lse overlaps o
+    assert fwd(lib, B=1 << 16, H=1 << 16) == 2      # beyond the grid limit
+
+
+def test_bwd_argument_checks(lib):
+    p = [FAKE + i * 0x100000 for i in range(12)]
+    ws = lib.fa_bwd_workspace_bytes(1, 1, 128, 64)
+    assert ws == 512  # 128 fp32 row terms, 256-byte rounded
+    assert lib.fa_bwd_workspace_bytes(2, 3, 100, 128) == ((2 * 3 * 100 * 4 + 255) // 256) * 256
+    assert lib.fa_bwd_workspace_bytes(1, 1, 0, 64) == 0
+    assert lib.fa_bwd_workspace_bytes(1, 1, 128, 96) == 0
+
+    def bwd(**kw):
+        a = dict(q=p[0], k=p[1], v=p[2], o=p[3], lse=p[4], do=p[5], dq=p[6], dk=p[7], dv=p[8],
+                 B=1, H=1, N=128, d=64, scale=0.125, causal=1, ws=p[9], wsb=ws)
+        a.update(kw)
+        return lib.fa_bwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["do"], a["dq"], a["dk"], a["dv"],
+                          a["B"], a["H"], a["N"], a["d"], a["scale"], a["causal"], a["ws"], a["wsb"], None)
+
+    assert bwd(d=80) == 2
+    assert bwd(N=0, q=0) == 0
+    assert bwd(dq=0) == 1
+    assert bwd(do=BAD_ALIGN) == 1
+    assert bwd(ws=0) == 4                 # FA_ERR_WORKSPACE
+    assert bwd(wsb=ws - 4) == 4
+    assert bwd(ws=p[9] + 4) == 4
+    assert bwd(dk=p[0]) == 1              # output aliases an input
+    assert bwd(dv=p[6]) == 1              # two outputs alias
+    assert bwd(ws=p[4]) == 1              # workspace aliases lse
+    assert lib.fa_bwd_preprocess(p[3], p[5], 0, 1, 1, 128, 64, None) == 1
+    assert lib.fa_bwd_dkdv(p[0], p[1], p[2], p[4], p[5], p[10], p[7], p[0], 1, 1, 128, 64, 0.1, 0, None) == 1
+    assert lib.fa_bwd_dq(p[0], p[1], p[2], p[4], p[5], p[10], p[6], 1, 1, 128, 64, 0.0, 0, None) == 1
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        text = lib.fa_status_string(s).decode()
+        assert text.startswith("FA_")
+    assert lib.fa_status_string(99).decode() == "unknown fa_status"

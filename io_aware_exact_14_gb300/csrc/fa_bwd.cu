@@ -78,7 +78,589 @@ __global__ void __launch_bounds__(kPreThreads) fa_bwd_preprocess_kernel(const ui
   }
 }
 
+// ---------------------------------------------------------------------------
+// Steps 2 and 3: the two tensor-core kernels.
+//
+// Shared layout: one CTA per SM, 384 threads.
+//   warps 0-3  compute warpgroup 0: columns [0, 64) of each 128 x 128 tile
+//   warps 4-7  compute warpgroup 1: columns [64, 128)
+//   warp  8    producer (TMA tiles; the whole warp gathers the row vectors)
+//   warp  9    TMEM owner and single-thread tcgen05.mma issuer
+//   warps 10-11 idle
+// TMEM (512 columns): T0 [0,128) scores, T1 [128,256) dP, then accumulators.
+// bf16 operands made by the compute warps (P^T, dS^T, dS) overwrite the first
+// 32 columns of their own half of T0 / T1 and feed the next MMA from TMEM.
+// ---------------------------------------------------------------------------
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct BwdCfg {
+  static_assert(D == 64 || D == 128, "head dim");
+  static constexpr int kBoxes = D / 64;
+  static constexpr uint32_t kBoxBytes = 128u * 128u;
+  static constexpr uint32_t kTileBytes = kBoxes * kBoxBytes;
+  static constexpr int kStages = 2;
+  // resident tiles R0, R1; each stage: tiles X, Y and two fp32[128] vectors
+  static constexpr uint32_t kResOff = 0;
+  static constexpr uint32_t kStageOff = 2 * kTileBytes;
+  static constexpr uint32_t kStageBytes = 2 * kTileBytes + 1024;
+  static constexpr uint32_t kBarOff = kStageOff + kStages * kStageBytes;
+  // res_full, full[S], empty[S], s_full, s_free, dp_full, p_full, ds_full, acc_done, drain, staged[2]
+  static constexpr int kBars = 1 + 2 * kStages + 10;
+  static constexpr uint32_t kMiscOff = kBarOff + kBars * 8;
+  static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;
+  static constexpr int kThreads = 384;
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColAcc0 = 256, kColAcc1 = 256 + D;
+  __host__ __device__ static constexpr uint32_t x_off(int st) { return kStageOff + st * kStageBytes; }
+  __host__ __device__ static constexpr uint32_t y_off(int st) { return x_off(st) + kTileBytes; }
+  __host__ __device__ static constexpr uint32_t vec_off(int st) { return x_off(st) + 2 * kTileBytes; }
+};
+
+struct BwdBars {
+  uint64_t *res_full, *full, *empty, *s_full, *s_free, *dp_full, *p_full, *ds_full, *acc_done, *drain, *staged;
+  uint32_t* tmem_holder;
+  volatile uint32_t* abort_flag;
+};
+
+template <int D>
+__device__ __forceinline__ BwdBars bwd_bars(uint8_t* smem) {
+  using C = BwdCfg<D>;
+  uint64_t* b = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+  BwdBars r;
+  r.res_full = b;
+  r.full = b + 1;
+  r.empty = b + 1 + C::kStages;
+  uint64_t* m = b + 1 + 2 * C::kStages;
+  r.s_full = m;
+  r.s_free = m + 1;
+  r.dp_full = m + 2;
+  r.p_full = m + 3;
+  r.ds_full = m + 4;
+  r.acc_done = m + 5;
+  r.drain = m + 6;
+  r.staged = m + 7;  // two
+  r.tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
+  r.abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kMiscOff + 4);
+  return r;
+}
+
+template <int D>
+__device__ __forceinline__ void bwd_init(const BwdBars& b, uint32_t staged_count) {
+  using C = BwdCfg<D>;
+  mbar_init(b.res_full, 1);
+  for (int i = 0; i < C::kStages; ++i) {
+    mbar_init(&b.full[i], 2);   // TMA bytes + the producer warp's vector writes
+    mbar_init(&b.empty[i], 1);
+  }
+  mbar_init(b.s_full, 1);
+  mbar_init(b.s_free, 256);
+  mbar_init(b.dp_full, 1);
+  mbar_init(b.p_full, 256);
+  mbar_init(b.ds_full, 256);
+  mbar_init(b.acc_done, 1);
+  mbar_init(b.drain, 1);
+  mbar_init(&b.staged[0], staged_count);
+  mbar_init(&b.staged[1], staged_count);
+  *b.abort_flag = 0u;
+  fence_mbar_init();
+}
+
+// S-like product: D(128 x 128) = A(128 x d) * B(128 x d)^T, both K-major tiles.
+template <int D>
+__device__ __forceinline__ void mma_nt(uint32_t tmem_d, uint32_t a_addr, uint32_t b_addr) {
+  using C = BwdCfg<D>;
+  constexpr uint32_t idesc = idesc_bf16(128, 128, false, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk / 4) * C::kBoxBytes + (kk % 4) * 32;
+    tc_mma_ss(tmem_d, sdesc_sw128(a_addr + off, 16, 1024), sdesc_sw128(b_addr + off, 16, 1024), idesc,
+              kk > 0 ? 1u : 0u);
+  }
+}
+
+// Accumulating product: D(128 x d) += A(128 x 128, TMEM bf16) * B(128 x d, MN-major tile).
+// A's 128 K columns live as two 64-wide halves at a_tmem and a_tmem + 64.
+template <int D>
+__device__ __forceinline__ void mma_tn_acc(uint32_t tmem_d, uint32_t a_tmem, uint32_t b_addr, bool acc) {
+  using C = BwdCfg<D>;
+  constexpr uint32_t idesc = idesc_bf16(128, D, false, true);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint32_t a = a_tmem + (kk / 4) * 64 + (kk % 4) * 8;
+    tc_mma_ts(tmem_d, a, sdesc_sw128(b_addr + kk * 2048, C::kBoxBytes, 1024), idesc, (acc || kk > 0) ? 1u : 0u);
+  }
+}
+
+// Pack 32 fp32 values (in two 16-value halves) into 16 bf16x2 words and store
+// them to 16 TMEM columns.
+__device__ __forceinline__ void st_bf16_16cols(uint32_t taddr, const float* v) {
+  uint32_t w[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+  tmem_st16(taddr, w);
+}
+
+// Epilogue for one 128 x d accumulator: TMEM -> * mult -> bf16 -> swizzled
+// staging -> TMA store (rows past N clipped).  `c0, c1` bound the columns this
+// warpgroup writes; the TMA store is issued by `leader` once `staged` fills.
+template <int D>
+__device__ __forceinline__ void bwd_store_acc(uint32_t tacc, uint8_t* stage, int c0, int c1, float mult, int r,
+                                              uint64_t* staged, bool leader, const CUtensorMap* map, int row0,
+                                              int bh, const CtaGuard& g, uint32_t site) {
+  using C = BwdCfg<D>;
+  const uint32_t st = smem_u32(stage);
+  for (int c = c0; c < c1; c += 32) {
+    uint32_t o[32];
+    tmem_ld32(tacc + c, o);
+    tmem_ld_wait(o);
+    const uint32_t box = st + (c / 64) * C::kBoxBytes + r * 128;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int chunk = (c % 64) / 8 + q;
+      float f[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(o[8 * q + e]) * mult;
+      st_shared_v4(box + ((chunk ^ (r & 7)) << 4), pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                   pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+    }
+  }
+  fence_proxy_async_smem();
+  mbar_arrive(staged);
+  if (leader && mbar_wait(staged, 0, g, site)) {
+#pragma unroll
+    for (int b = 0; b < C::kBoxes; ++b) tma_store_3d(map, stage + b * C::kBoxBytes, 64 * b, row0, bh);
+    tma_store_commit();
+    tma_store_wait_read_all();
+  }
+}
+
+// Row vectors for a query tile: lse2 = lse * log2(e) (+inf past N, so P = 0
+// there) and D (0 past N).  The whole producer warp writes them.
+__device__ __forceinline__ void load_row_vectors(float* lse2, float* dvec, const float* __restrict__ lse,
+                                                 const float* __restrict__ Dg, size_t row_base, int q0, int N,
+                                                 int lane) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int c = lane + 32 * k;
+    const int q = q0 + c;
+    float a = INFINITY, d = 0.f;
+    if (q < N) {
+      const float l = lse[row_base + q];
+      a = (l == -INFINITY) ? INFINITY : l * kLog2e;
+      d = Dg[row_base + q];
+    }
+    lse2[c] = a;
+    dvec[c] = d;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// dK / dV: one CTA per (b, h, 128-key tile j); loop over query tiles i.
+//   S^T = K_j Q_i^T, P^T = exp2(S^T * scale * log2e - lse2_i)
+//   dP^T = V_j dO_i^T, dS^T = P^T o (dP^T - D_i)
+//   dV_j += P^T dO_i,  dK_j += dS^T Q_i,  finally dK_j *= scale
+// MMA order S(i) dP(i) dV(i) S(i+1) dK(i) dP(i+1) ...: the exponentials of tile i
+// run under dP(i), the dS products under dV(i) and S(i+1).
+// TMEM: T0 = S^T, T1 = dP^T, acc0 = dV, acc1 = dK.
+// ---------------------------------------------------------------------------
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(384, 1)
+    fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                       const __grid_constant__ CUtensorMap tmDK, const __grid_constant__ CUtensorMap tmDV,
+                       const float* __restrict__ lse, const float* __restrict__ Dg, int N, int n_tiles,
+                       float scale, float scale_log2) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const BwdBars bb = bwd_bars<D>(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int bh = blockIdx.x / n_tiles;
+  const int kt = static_cast<int>(blockIdx.x % n_tiles);       // key tile; causal: small kt is heavy
+  const int i0 = CAUSAL ? kt : 0;                               // first query tile
+  const int cnt = n_tiles - i0;                                 // query tiles visited (>= 1)
+  const size_t row_base = static_cast<size_t>(bh) * N;
+
+  if (threadIdx.x == 0) bwd_init<D>(bb, 128);
+  if (warp == 9) {
+    tmem_alloc(bb.tmem_holder, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *bb.tmem_holder;
+  const CtaGuard g{bb.abort_flag, &g_status_bwd};
+  const uint32_t sbase = smem_u32(smem);
+
+  if (warp >= 8) {
+    if (warp == 8) {  // producer
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bb.res_full, 2 * C::kTileBytes);
+        for (int b = 0; b < C::kBoxes; ++b) {
+          tma_load_3d(smem + C::kResOff + b * C::kBoxBytes, &tmK, bb.res_full, 64 * b, 128 * kt, bh);
+          tma_load_3d(smem + C::kResOff + C::kTileBytes + b * C::kBoxBytes, &tmV, bb.res_full, 64 * b, 128 * kt,
+                      bh);
+        }
+      }
+      for (int it = 0; it < cnt; ++it) {
+        const int st = it % C::kStages;
+        const uint32_t ph = (it / C::kStages) & 1;
+        int ok = 1;
+        if (lane == 0) ok = mbar_wait(&bb.empty[st], ph ^ 1u, g, kSiteDkdv | 1u);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;   // the whole warp follows lane 0
+        const int qt = i0 + it;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bb.full[st], 2 * C::kTileBytes);
+          for (int b = 0; b < C::kBoxes; ++b) {
+            tma_load_3d(smem + C::x_off(st) + b * C::kBoxBytes, &tmQ, &bb.full[st], 64 * b, 128 * qt, bh);
+            tma_load_3d(smem + C::y_off(st) + b * C::kBoxBytes, &tmDO, &bb.full[st], 64 * b, 128 * qt, bh);
+          }
+        }
+        float* vec = reinterpret_cast<float*>(smem + C::vec_off(st));
+        load_row_vectors(vec, vec + 128, lse, Dg, row_base, 128 * qt, N, lane);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bb.full[st]);
+      }
+    } else if (warp == 9) {  // MMA issuer
+      if (lane == 0) {
+        const uint32_t tS = tmem + C::kColS, tDP = tmem + C::kColDP;
+        const uint32_t tDV = tmem + C::kColAcc0, tDK = tmem + C::kColAcc1;
+        const uint32_t aK = sbase + C::kResOff, aV = sbase + C::kResOff + C::kTileBytes;
+        bool ok = mbar_wait(bb.res_full, 0, g, kSiteDkdv | 2u) && mbar_wait(&bb.full[0], 0, g, kSiteDkdv | 3u);
+        if (ok) {
+          mma_nt<D>(tS, aK, sbase + C::x_off(0));
+          tc_commit(bb.s_full);
+          mma_nt<D>(tDP, aV, sbase + C::y_off(0));
+          tc_commit(bb.dp_full);
+        }
+        for (int it = 0; ok && it < cnt; ++it) {
+          const int st = it % C::kStages;
+          const uint32_t par = it & 1;
+          const bool next = it + 1 < cnt;
+          const int st1 = (it + 1) % C::kStages;
+          if (!(ok = mbar_wait(bb.p_full, par, g, kSiteDkdv | 4u))) break;
+          tc_fence_after();
+          mma_tn_acc<D>(tDV, tS, sbase + C::y_off(st), it > 0);          // dV += P^T dO_i
+          if (next) {
+            if (!(ok = mbar_wait(&bb.full[st1], ((it + 1) / C::kStages) & 1, g, kSiteDkdv | 5u))) break;
+            mma_nt<D>(tS, aK, sbase + C::x_off(st1));                     // S^T(i+1)
+            tc_commit(bb.s_full);
+          }
+          if (!(ok = mbar_wait(bb.ds_full, par, g, kSiteDkdv | 6u))) break;
+          tc_fence_after();
+          mma_tn_acc<D>(tDK, tDP, sbase + C::x_off(st), it > 0);         // dK += dS^T Q_i
+          tc_commit(&bb.empty[st]);
+          if (next) {
+            mma_nt<D>(tDP, aV, sbase + C::y_off(st1));                    // dP^T(i+1)
+            tc_commit(bb.dp_full);
+          }
+        }
+        if (ok) tc_commit(bb.acc_done);
+        tc_commit(bb.drain);
+        mbar_drain(bb.drain, 0);
+      }
+      __syncwarp();
+      tc_fence_before();
+      named_bar_sync(1, 288);
+      tc_fence_after();
+      tmem_dealloc(tmem, 512);
+    }
+    return;
+  }
+
+  // compute warpgroups: key row t = TMEM lane; half h owns query columns [64h, 64h+64)
+  const int h = warp >> 2;
+  const int t = threadIdx.x & 127;
+  const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+  const uint32_t tS = tmem + lane_base + C::kColS + 64 * h;
+  const uint32_t tDP = tmem + lane_base + C::kColDP + 64 * h;
+  bool ok = true;
+  for (int it = 0; ok && it < cnt; ++it) {
+    const int st = it % C::kStages;
+    const uint32_t par = it & 1;
+    const int qt = i0 + it;
+    const float* lse2 = reinterpret_cast<const float*>(smem + C::vec_off(st)) + 64 * h;
+    const float* dv = lse2 + 128;
+    // the row vectors were written by the producer before it arrived on full[st]
+    if (!(ok = mbar_wait(&bb.full[st], (it / C::kStages) & 1, g, kSiteDkdv | 7u))) break;
+    if (!(ok = mbar_wait(bb.s_full, par, g, kSiteDkdv | 8u))) break;
+    __syncwarp();
+    tc_fence_after();
+    uint32_t sr[2][32];
+    tmem_ld32(tS, sr[0]);
+    tmem_ld32(tS + 32, sr[1]);
+    tmem_ld_wait(sr[0]);
+    tmem_ld_fence(sr[1]);
+    float p[64];
+    // diagonal tile: query column 64h + c is masked when it precedes key t
+    const int lim = (CAUSAL && qt == kt) ? t - 64 * h : -1;
+#pragma unroll
+    for (int c = 0; c < 64; ++c) {
+      const float x = fmaf(__uint_as_float(sr[c / 32][c % 32]), scale_log2, -lse2[c]);
+      p[c] = (c < lim) ? 0.f : ex2_approx(x);
+    }
+#pragma unroll
+    for (int c = 0; c < 64; c += 32) {
+      st_bf16_16cols(tS + c / 2, p + c);
+    }
+    tmem_st_wait();
+    tc_fence_before();
+    mbar_arrive(bb.p_full);
+
+    if (!(ok = mbar_wait(bb.dp_full, par, g, kSiteDkdv | 9u))) break;
+    __syncwarp();
+    tc_fence_after();
+    uint32_t dr[2][32];
+    tmem_ld32(tDP, dr[0]);
+    tmem_ld32(tDP + 32, dr[1]);
+    tmem_ld_wait(dr[0]);
+    tmem_ld_fence(dr[1]);
+#pragma unroll
+    for (int c = 0; c < 64; ++c) p[c] = p[c] * (__uint_as_float(dr[c / 32][c % 32]) - dv[c]);
+#pragma unroll
+    for (int c = 0; c < 64; c += 32) st_bf16_16cols(tDP + c / 2, p + c);
+    tmem_st_wait();
+    tc_fence_before();
+    mbar_arrive(bb.ds_full);
+  }
+  if (ok && mbar_wait(bb.acc_done, 0, g, kSiteDkdv | 10u)) {
+    __syncwarp();
+    tc_fence_after();
+    // warpgroup 0 writes dV (staged in stage 0's X tile), warpgroup 1 writes dK (stage 0's Y tile)
+    const uint32_t tacc = tmem + lane_base + (h ? C::kColAcc1 : C::kColAcc0);
+    uint8_t* stage = smem + (h ? C::y_off(0) : C::x_off(0));
+    bwd_store_acc<D>(tacc, stage, 0, D, h ? scale : 1.f, t, &bb.staged[h], t == 0, h ? &tmDK : &tmDV, 128 * kt,
+                     bh, g, kSiteDkdv | 11u);
+  }
+  __syncwarp();
+  tc_fence_before();
+  named_bar_sync(1, 288);
+}
+
+// ---------------------------------------------------------------------------
+// dQ: one CTA per (b, h, 128-query tile i); loop over key tiles j.
+//   S = Q_i K_j^T, P = exp2(S * scale * log2e - lse2_row)
+//   dP = dO_i V_j^T, dS = P o (dP - D_row),  dQ_i += dS K_j,  finally dQ_i *= scale
+// MMA order S(j) dP(j) S(j+1) dQ(j) dP(j+1) ...: the exponentials of tile j run
+// under dP(j), the dS products under S(j+1).
+// TMEM: T0 = S, T1 = dP, acc0 = dQ.
+// ---------------------------------------------------------------------------
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(384, 1)
+    fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                     const __grid_constant__ CUtensorMap tmDQ, const float* __restrict__ lse,
+                     const float* __restrict__ Dg, int N, int n_tiles, float scale, float scale_log2) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const BwdBars bb = bwd_bars<D>(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int bh = blockIdx.x / n_tiles;
+  const int qt = n_tiles - 1 - static_cast<int>(blockIdx.x % n_tiles);  // causal: large qt is heavy
+  const int cnt = CAUSAL ? qt + 1 : n_tiles;                             // key tiles visited
+  const size_t row_base = static_cast<size_t>(bh) * N;
+
+  if (threadIdx.x == 0) bwd_init<D>(bb, 256);
+  if (warp == 9) {
+    tmem_alloc(bb.tmem_holder, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *bb.tmem_holder;
+  const CtaGuard g{bb.abort_flag, &g_status_bwd};
+  const uint32_t sbase = smem_u32(smem);
+
+  if (warp >= 8) {
+    if (warp == 8) {  // producer: Q_i, dO_i once; K_j, V_j per stage
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bb.res_full, 2 * C::kTileBytes);
+        for (int b = 0; b < C::kBoxes; ++b) {
+          tma_load_3d(smem + C::kResOff + b * C::kBoxBytes, &tmQ, bb.res_full, 64 * b, 128 * qt, bh);
+          tma_load_3d(smem + C::kResOff + C::kTileBytes + b * C::kBoxBytes, &tmDO, bb.res_full, 64 * b,
+                      128 * qt, bh);
+        }
+        for (int it = 0; it < cnt; ++it) {
+          const int st = it % C::kStages;
+          const uint32_t ph = (it / C::kStages) & 1;
+          if (!mbar_wait(&bb.empty[st], ph ^ 1u, g, kSiteDq | 1u)) break;
+          mbar_arrive_expect_tx(&bb.full[st], 2 * C::kTileBytes);
+          for (int b = 0; b < C::kBoxes; ++b) {
+            tma_load_3d(smem + C::x_off(st) + b * C::kBoxBytes, &tmK, &bb.full[st], 64 * b, 128 * it, bh);
+            tma_load_3d(smem + C::y_off(st) + b * C::kBoxBytes, &tmV, &bb.full[st], 64 * b, 128 * it, bh);
+          }
+          mbar_arrive(&bb.full[st]);  // no row vectors here: second arrival of the two expected
+        }
+      }
+    } else if (warp == 9) {  // MMA issuer
+      if (lane == 0) {
+        const uint32_t tS = tmem + C::kColS, tDP = tmem + C::kColDP, tDQ = tmem + C::kColAcc0;
+        const uint32_t aQ = sbase + C::kResOff, aDO = sbase + C::kResOff + C::kTileBytes;
+        bool ok = mbar_wait(bb.res_full, 0, g, kSiteDq | 2u) && mbar_wait(&bb.full[0], 0, g, kSiteDq | 3u);
+        if (ok) {
+          mma_nt<D>(tS, aQ, sbase + C::x_off(0));
+          tc_commit(bb.s_full);
+          mma_nt<D>(tDP, aDO, sbase + C::y_off(0));
+          tc_commit(bb.dp_full);
+        }
+        for (int it = 0; ok && it < cnt; ++it) {
+          const int st = it % C::kStages;
+          const uint32_t par = it & 1;
+          const bool next = it + 1 < cnt;
+          const int st1 = (it + 1) % C::kStages;
+          if (next) {
+            if (!(ok = mbar_wait(&bb.full[st1], ((it + 1) / C::kStages) & 1, g, kSiteDq | 4u))) break;
+            if (!(ok = mbar_wait(bb.s_free, par, g, kSiteDq | 5u))) break;
+            tc_fence_after();
+            mma_nt<D>(tS, aQ, sbase + C::x_off(st1));                 // S(j+1)
+            tc_commit(bb.s_full);
+          }
+          if (!(ok = mbar_wait(bb.ds_full, par, g, kSiteDq | 6u))) break;
+          tc_fence_after();
+          mma_tn_acc<D>(tDQ, tDP, sbase + C::x_off(st), it > 0);     // dQ += dS K_j
+          tc_commit(&bb.empty[st]);
+          if (next) {
+            mma_nt<D>(tDP, aDO, sbase + C::y_off(st1));               // dP(j+1)
+            tc_commit(bb.dp_full);
+          }
+        }
+        if (ok) tc_commit(bb.acc_done);
+        tc_commit(bb.drain);
+        mbar_drain(bb.drain, 0);
+      }
+      __syncwarp();
+      tc_fence_before();
+      named_bar_sync(1, 288);
+      tc_fence_after();
+      tmem_dealloc(tmem, 512);
+    }
+    return;
+  }
+
+  // compute warpgroups: query row r = TMEM lane; half h owns key columns [64h, 64h+64)
+  const int h = warp >> 2;
+  const int r = threadIdx.x & 127;
+  const int row = 128 * qt + r;
+  const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+  const uint32_t tS = tmem + lane_base + C::kColS + 64 * h;
+  const uint32_t tDP = tmem + lane_base + C::kColDP + 64 * h;
+  float lse2 = INFINITY, drow = 0.f;
+  if (row < N) {
+    const float l = lse[row_base + row];
+    lse2 = (l == -INFINITY) ? INFINITY : l * kLog2e;
+    drow = Dg[row_base + row];
+  }
+  bool ok = true;
+  for (int it = 0; ok && it < cnt; ++it) {
+    const uint32_t par = it & 1;
+    if (!(ok = mbar_wait(bb.s_full, par, g, kSiteDq | 7u))) break;
+    __syncwarp();
+    tc_fence_after();
+    uint32_t sr[2][32];
+    tmem_ld32(tS, sr[0]);
+    tmem_ld32(tS + 32, sr[1]);
+    tmem_ld_wait(sr[0]);
+    tmem_ld_fence(sr[1]);
+    tc_fence_before();
+    mbar_arrive(bb.s_free);   // S(j) is in registers: the tensor core may overwrite it
+    // keys k0 .. k0+lim-1 of this half are visible to the row
+    const int k0 = 128 * it + 64 * h;
+    int lim = N - k0;
+    if (CAUSAL) lim = min(lim, row - k0 + 1);
+    float p[64];
+#pragma unroll
+    for (int c = 0; c < 64; ++c) {
+      const float x = fmaf(__uint_as_float(sr[c / 32][c % 32]), scale_log2, -lse2);
+      p[c] = (c < lim) ? ex2_approx(x) : 0.f;
+    }
+    if (!(ok = mbar_wait(bb.dp_full, par, g, kSiteDq | 8u))) break;
+    __syncwarp();
+    tc_fence_after();
+    uint32_t dr[2][32];
+    tmem_ld32(tDP, dr[0]);
+    tmem_ld32(tDP + 32, dr[1]);
+    tmem_ld_wait(dr[0]);
+    tmem_ld_fence(dr[1]);
+#pragma unroll
+    for (int c = 0; c < 64; ++c) p[c] = p[c] * (__uint_as_float(dr[c / 32][c % 32]) - drow);
+#pragma unroll
+    for (int c = 0; c < 64; c += 32) st_bf16_16cols(tDP + c / 2, p + c);
+    tmem_st_wait();
+    tc_fence_before();
+    mbar_arrive(bb.ds_full);
+  }
+  if (ok && mbar_wait(bb.acc_done, 0, g, kSiteDq | 9u)) {
+    __syncwarp();
+    tc_fence_after();
+    // both warpgroups stage dQ into the (now idle) Q tile; thread 0 stores it
+    bwd_store_acc<D>(tmem + lane_base + C::kColAcc0, smem + C::kResOff, h * (D / 2), (h + 1) * (D / 2), scale, r,
+                     &bb.staged[0], threadIdx.x == 0, &tmDQ, 128 * qt, bh, g, kSiteDq | 10u);
+  }
+  __syncwarp();
+  tc_fence_before();
+  named_bar_sync(1, 288);
+}
+template <int D, bool CAUSAL>
+cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv, const float* lse,
+                          const float* Dvec, const Shape& s, cudaStream_t st) {
+  using C = BwdCfg<D>;
+  auto kern = fa_bwd_dkdv_kernel<D, CAUSAL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int n_tiles = (s.N + 127) / 128;
+  const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
+  const dim3 grid(static_cast<unsigned>(s.B) * s.H * n_tiles);
+  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s.N, n_tiles, s.scale,
+                                                 scale_log2);
+  return cudaGetLastError();
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                        const CUtensorMap& tdo, const CUtensorMap& tdq, const float* lse, const float* Dvec,
+                        const Shape& s, cudaStream_t st) {
+  using C = BwdCfg<D>;
+  auto kern = fa_bwd_dq_kernel<D, CAUSAL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int n_tiles = (s.N + 127) / 128;
+  const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
+  const dim3 grid(static_cast<unsigned>(s.B) * s.H * n_tiles);
+  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, tdq, lse, Dvec, s.N, n_tiles, s.scale,
+                                                 scale_log2);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_bwd_dkdv(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
+                            const float* lse, const float* Dvec, const Shape& s, cudaStream_t st) {
+  if (s.d == 128)
+    return s.causal ? launch_dkdv_t<128, true>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s, st)
+                    : launch_dkdv_t<128, false>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s, st);
+  return s.causal ? launch_dkdv_t<64, true>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s, st)
+                  : launch_dkdv_t<64, false>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s, st);
+}
+
+cudaError_t launch_bwd_dq(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const CUtensorMap& tdo, const CUtensorMap& tdq, const float* lse, const float* Dvec,
+                          const Shape& s, cudaStream_t st) {
+  if (s.d == 128)
+    return s.causal ? launch_dq_t<128, true>(tq, tk, tv, tdo, tdq, lse, Dvec, s, st)
+                    : launch_dq_t<128, false>(tq, tk, tv, tdo, tdq, lse, Dvec, s, st);
+  return s.causal ? launch_dq_t<64, true>(tq, tk, tv, tdo, tdq, lse, Dvec, s, st)
+                  : launch_dq_t<64, false>(tq, tk, tv, tdo, tdq, lse, Dvec, s, st);
+}
 
 cudaError_t launch_bwd_preprocess(const void* o, const void* dO, float* Dvec, const Shape& s, cudaStream_t st) {
   const long long rows = static_cast<long long>(s.B) * s.H * s.N;
@@ -97,17 +679,6 @@ cudaError_t launch_bwd_preprocess(const void* o, const void* dO, float* Dvec, co
     fa_bwd_preprocess_kernel<64><<<grid, kPreThreads, 0, st>>>(static_cast<const uint8_t*>(o),
                                                                 static_cast<const uint8_t*>(dO), Dvec, rows);
   return cudaGetLastError();
-}
-
-cudaError_t launch_bwd_dkdv(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                            const CUtensorMap&, const CUtensorMap&, const float*, const float*, const Shape&,
-                            cudaStream_t) {
-  return cudaErrorNotSupported;
-}
-
-cudaError_t launch_bwd_dq(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                          const CUtensorMap&, const float*, const float*, const Shape&, cudaStream_t) {
-  return cudaErrorNotSupported;
 }
 
 cudaError_t bwd_status(uint32_t* out, bool reset) {

@@ -1,0 +1,446 @@
+#!/usr/bin/env python3
+"""Benchmark: one training step of exact attention (forward + backward) on GB300.
+
+A step is the whole hot path over one batch of synthetic input: the forward
+kernel (O, LSE), then the backward's row-term preprocess, dK/dV kernel and dQ
+kernel.  Default workload: B=8, H=16, N=4096, d=128, causal, bf16 (the
+training-shaped workload at N >= 4096, d = 128).  Prints ONE JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 (torchrun), every rank runs the same workload on its own GPU with no
+data exchange (the path shards by (batch, head); ranks are replicas), timing is
+the max over ranks and `value` counts the work of all ranks.
+
+--impl reference times the fp64 CPU oracle (the only other implementation of
+the method here) on the host cores, a bounded sample of the workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from io_aware_exact_14_gb300 import counts  # noqa: E402
+from io_aware_exact_14_gb300.workloads import WORKLOADS, make_inputs  # noqa: E402
+
+METRIC = "attention fwd/bwd TFLOP/s (bf16, 1xGB300) and % of dense BF16 tensor peak"
+UNIT = "TFLOP/s"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=5, choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU-baseline time budget")
+    ap.add_argument("--batch", type=int, default=None, help="override B (smaller cases for profiler captures)")
+    return ap.parse_args()
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return p, "measured"
+    except Exception:
+        return FALLBACK_PEAKS, "fallback"
+
+
+def step_flops(w, causal):
+    return counts.attn_flops(w.B, w.H, w.N, w.d, causal, "fwd") + counts.attn_flops(w.B, w.H, w.N, w.d, causal, "bwd")
+
+
+# ---------------------------------------------------------------------------
+# distributed helpers (replicas: barrier + max-reduce of the timing only)
+# ---------------------------------------------------------------------------
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+
+    def init(self, backend):
+        if self.world > 1:
+            import torch.distributed as dist
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if self.pg is None:
+            return x
+        import torch
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# clocks (nvidia-smi sampled during the timed region)
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.lines = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        t0 = time.time()
+        while not self.lines and time.time() - t0 < 5:
+            time.sleep(0.02)
+        self.lines.clear()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in list(self.lines):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names[1:], parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def traffic_for(kernel: str, source_files):
+    """Per-launch DRAM bytes from the committed ncu summary, if the kernel source is unchanged."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)[kernel]
+    except Exception:
+        return None
+    h = hashlib.sha256()
+    for p in source_files:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    if rec.get("source_sha256") != h.hexdigest():
+        return None
+    return rec.get("bytes_per_launch")
+
+
+def run_ours(args, dist: Dist):
+    import torch
+    from io_aware_exact_14_gb300 import fa
+
+    torch.cuda.set_device(dist.local)
+    dist.init("nccl")
+    dev = torch.device("cuda", dist.local)
+    w = WORKLOADS[args.workload]
+    if args.batch is not None:
+        import dataclasses
+        w = dataclasses.replace(w, B=args.batch, name=f"{w.name}@B={args.batch}")
+    causal = w.causal[-1]
+    B, H, N, d = w.shape
+    scale = w.scale
+    x = make_inputs(B, H, N, d, w.seed + 100 * dist.rank, w.qk_mult, with_grad=True)
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    Dv = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    stream = torch.cuda.current_stream(dev)
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        fa.fa_fwd(q, k, v, scale, causal, out=o, lse=lse)
+        if evs:
+            evs[1].record(stream)
+        fa.fa_bwd_preprocess(o, do, Dv)
+        if evs:
+            evs[2].record(stream)
+        fa.fa_bwd_dkdv(q, k, v, lse, do, Dv, scale, causal, dk=dk, dv=dv)
+        if evs:
+            evs[3].record(stream)
+        fa.fa_bwd_dq(q, k, v, lse, do, Dv, scale, causal, dq=dq)
+        if evs:
+            evs[4].record(stream)
+
+    clocks = ClockSampler(dist.local)
+    clocks.start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    dist.barrier()
+    torch.cuda.synchronize()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    clk = clocks.stop()
+    if fa.fa_debug_status(reset=True) != fa.FA_OK:
+        raise RuntimeError(f"kernel pipeline timeout at site {fa.fa_debug_site():#x}")
+    total_ms = dist.max(t_start.elapsed_time(t_end))
+    per = [[e[j].elapsed_time(e[j + 1]) for j in range(4)] for e in evs]
+    kern_ms = [sum(p[j] for p in per) / args.steps for j in range(4)]
+    ms_step = total_ms / args.steps
+
+    flops_step = step_flops(w, causal)
+    value = flops_step * dist.world * args.steps / (total_ms * 1e-3) / 1e12
+
+    peaks, peak_src = load_peaks()
+    burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    names = ["fa_fwd_kernel", "fa_bwd_preprocess_kernel", "fa_bwd_dkdv_kernel", "fa_bwd_dq_kernel"]
+    work = [counts.attn_flops(B, H, N, d, causal, "fwd"), counts.preprocess_bytes(B, H, N, d),
+            counts.dkdv_flops(B, H, N, d, causal), counts.dq_flops(B, H, N, d, causal)]
+    kernels = {}
+    for nm, ms, wk in zip(names, kern_ms, work):
+        if nm == "fa_bwd_preprocess_kernel":
+            kernels[nm] = {"ms": round(ms, 4), "GB/s": round(wk / ms / 1e6, 1), "frac_hbm": round(wk / ms / 1e6 / hbm, 3)}
+        else:
+            kernels[nm] = {"ms": round(ms, 4), "TFLOP/s": round(wk / ms / 1e9, 1),
+                           "frac_bf16": round(wk / ms / 1e9 / burst, 3)}
+    dom = max(range(4), key=lambda j: kern_ms[j])
+    src = {"fa_fwd_kernel": ["io_aware_exact_14_gb300/csrc/fa_fwd.cu", "io_aware_exact_14_gb300/csrc/fa_ptx.cuh"],
+           "fa_bwd_preprocess_kernel": ["io_aware_exact_14_gb300/csrc/fa_bwd.cu"],
+           "fa_bwd_dkdv_kernel": ["io_aware_exact_14_gb300/csrc/fa_bwd.cu", "io_aware_exact_14_gb300/csrc/fa_ptx.cuh"],
+           "fa_bwd_dq_kernel": ["io_aware_exact_14_gb300/csrc/fa_bwd.cu", "io_aware_exact_14_gb300/csrc/fa_ptx.cuh"]}
+    if names[dom] == "fa_bwd_preprocess_kernel":
+        ach = work[dom] / kern_ms[dom] / 1e6
+        roof = {"kernel": names[dom], "bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(ach / hbm, 3)}
+    else:
+        ach = work[dom] / kern_ms[dom] / 1e9
+        roof = {"kernel": names[dom], "bound": "tensor", "achieved": round(ach, 1), "peak": burst, "unit": "TFLOP/s",
+                "frac": round(ach / burst, 3)}
+    roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json bf16 burst / hbm copy)"
+    roof["work_per_launch"] = work[dom]
+    roof["traffic"] = traffic_for(names[dom], src[names[dom]])
+
+    fwd_fl = counts.attn_flops(B, H, N, d, causal, "fwd")
+    bwd_fl = counts.attn_flops(B, H, N, d, causal, "bwd")
+    bwd_ms = kern_ms[1] + kern_ms[2] + kern_ms[3]
+    passes = {"fwd": {"ms": round(kern_ms[0], 4), "TFLOP/s": round(fwd_fl / kern_ms[0] / 1e9, 1),
+                      "frac_bf16": round(fwd_fl / kern_ms[0] / 1e9 / burst, 3)},
+              "bwd": {"ms": round(bwd_ms, 4), "TFLOP/s": round(bwd_fl / bwd_ms / 1e9, 1),
+                      "frac_bf16": round(bwd_fl / bwd_ms / 1e9 / burst, 3)}}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, w, causal, x, dev, dist, flops_step)
+
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16 q, k, v, dO)",
+        "config": {"workload": w.name, "B": B, "H": H, "N": N, "d": d, "causal": causal, "scale": scale,
+                   "step": "fa_fwd + fa_bwd_preprocess + fa_bwd_dkdv + fa_bwd_dq",
+                   "l2": "inputs larger than L2: q, k, v, o, dO are 134 MB each (L2 129 MB)",
+                   "parallelism": "replicas" if dist.world > 1 else "single GPU"},
+        "frac_of_peak": round(value / dist.world / burst, 3),
+        "passes": passes, "kernels": kernels, "roofline": roof,
+        "gpu_launches": 4 * args.steps, "clocks": clk,
+    }
+    if e2e is not None:
+        out["e2e"] = e2e
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(w, causal, args.cpu_seconds)
+    dist.close()
+    if dist.rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def run_e2e(args, w, causal, x, dev, dist, flops_step):
+    """Same step through the public API with host buffers: pinned H2D copies of
+    q, k, v, dO and D2H copies of O, LSE, dQ, dK, dV inside the timed region."""
+    import torch
+    from io_aware_exact_14_gb300 import fa
+    B, H, N, d = w.shape
+    h_in = [x[n].pin_memory() for n in ("q", "k", "v", "do")]
+    d_in = [torch.empty_like(t, device=dev) for t in h_in]
+    h_out = [torch.empty((B, H, N, d), dtype=torch.bfloat16).pin_memory() for _ in range(4)]
+    h_lse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
+    o = torch.empty_like(d_in[0])
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    g = [torch.empty_like(d_in[0]) for _ in range(3)]
+
+    def step():
+        for hd, dd in zip(h_in, d_in):
+            dd.copy_(hd, non_blocking=True)
+        fa.fa_fwd(d_in[0], d_in[1], d_in[2], w.scale, causal, out=o, lse=lse)
+        fa.fa_bwd(d_in[0], d_in[1], d_in[2], o, lse, d_in[3], w.scale, causal, dq=g[0], dk=g[1], dv=g[2],
+                  workspace=ws)
+        for hd, dd in zip(h_out, [o] + g):
+            hd.copy_(dd, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+
+    steps = max(1, min(args.steps, 10))
+    for _ in range(max(1, min(args.warmup, 3))):
+        step()
+    torch.cuda.synchronize()
+    dist.barrier()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        step()
+    e.record()
+    torch.cuda.synchronize()
+    ms = dist.max(s.elapsed_time(e))
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = sum(t.numel() * t.element_size() for t in h_out) + h_lse.numel() * 4
+    return {"value": round(flops_step * dist.world * steps / (ms * 1e-3) / 1e12, 2), "unit": UNIT,
+            "steps": steps, "ms_per_step": round(ms / steps, 4), "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline leg and reference arm)
+# ---------------------------------------------------------------------------
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var):
+            return int(os.environ[var])
+    return os.cpu_count()
+
+
+def oracle_slice_step(w, causal, x, b, h):
+    """Forward + backward of one (b, h) slice in fp64 with the oracle as it stands."""
+    import oracle
+    from io_aware_exact_14_gb300.workloads import to_f64
+    sl = [to_f64(x[n][b:b + 1, h:h + 1]) for n in ("q", "k", "v", "do")]
+    oracle.attn_fwd_ref(sl[0], sl[1], sl[2], w.scale, causal)
+    oracle.attn_bwd_ref(sl[0], sl[1], sl[2], sl[3], w.scale, causal)
+
+
+def slice_flops(w, causal):
+    return (counts.attn_flops(1, 1, w.N, w.d, causal, "fwd") + counts.attn_flops(1, 1, w.N, w.d, causal, "bwd"))
+
+
+def cpu_baseline(w, causal, budget_s):
+    x = make_inputs(1, min(w.H, 4), w.N, w.d, w.seed, w.qk_mult, with_grad=True)
+    done, t0 = 0, time.time()
+    while True:
+        oracle_slice_step(w, causal, x, 0, done % x["q"].shape[1])
+        done += 1
+        if time.time() - t0 >= budget_s:
+            break
+    dt = time.time() - t0
+    return {"value": round(slice_flops(w, causal) * done / dt / 1e12, 6), "unit": UNIT, "cores": blas_threads(),
+            "kind": "oracle",
+            "sample": f"{done} (batch, head) slices of the workload (N={w.N}, d={w.d}, causal={causal}), "
+                      f"forward + backward in fp64 NumPy, {dt:.1f} s"}
+
+
+def run_reference(args, dist: Dist):
+    """The fp64 oracle timed on host cores: each step is one (b, h) slice of the workload."""
+    if dist.world > 1 and dist.rank != 0:
+        return
+    w = WORKLOADS[args.workload]
+    causal = w.causal[-1]
+    x = make_inputs(1, min(w.H, 4), w.N, w.d, w.seed, w.qk_mult, with_grad=True)
+    H = x["q"].shape[1]
+    for i in range(args.warmup):
+        oracle_slice_step(w, causal, x, 0, i % H)
+    t0 = time.time()
+    for i in range(args.steps):
+        oracle_slice_step(w, causal, x, 0, i % H)
+    dt = time.time() - t0
+    value = slice_flops(w, causal) * args.steps / dt / 1e12
+    sample = (f"one (batch, head) slice per step (N={w.N}, d={w.d}, causal={causal}), forward + backward "
+              f"in fp64 NumPy")
+    out = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) bf16 q, k, v, dO, upcast to fp64)",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": causal,
+                   "sample": "one (b, h) slice per step"},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    args = parse()
+    dist = Dist()
+    if args.impl == "reference":
+        run_reference(args, dist)
+    else:
+        run_ours(args, dist)
+
+
+if __name__ == "__main__":
+    main()

@@ -119,6 +119,31 @@ fa_status fa_bwd_dq(const void* q, const void* k, const void* v, const float* ls
                     int B, int H, int N, int d, float scale, int causal,
                     struct CUstream_st* stream);
 
+/*
+ * fa_bwd without a workspace argument, for callers that cannot allocate
+ * device memory themselves: code whose device memory belongs to a framework
+ * allocator or to a fixed budget (where a raw cudaMalloc may fail or break the
+ * owner's accounting), and code on latency-critical paths that cannot accept
+ * cudaMalloc's implicit device synchronisation.  The pages have no
+ * counterpart: this is a deployment convenience of this library.
+ *
+ * Same arguments, results and rules as fa_bwd.  The row term D is kept in a
+ * scratch array built into the library (8 MiB of device memory, reserved on
+ * every GPU that loads the library until the process exits), so
+ * B*H*N may be at most 2^21 = 2097152 rows; larger problems return
+ * FA_ERR_WORKSPACE (see fa_last_error_detail) and must use fa_bwd.  This entry
+ * point allocates nothing and calls no allocating routine.
+ *   - The first call with a given device current looks up the scratch's
+ *     device address; make that first call before any stream capture.
+ *   - All calls share the one scratch array: two calls whose kernels overlap
+ *     on the GPU (for example on different streams) race on it.  Calls
+ *     ordered on one stream are safe; each call overwrites the rows it uses.
+ */
+fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                         const void* dO, void* dq, void* dk, void* dv,
+                         int B, int H, int N, int d, float scale, int causal,
+                         struct CUstream_st* stream);
+
 /* Static description of a status code (never NULL). */
 const char* fa_status_string(fa_status s);
 

@@ -221,6 +221,29 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   return dq_checked(q, k, v, lse, dO, Dvec, dq, s, stream);
 }
 
+fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                         const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
+                         int causal, struct CUstream_st* stream) {
+  FA_TRY(check_sizes(B, H, N, d));
+  if (N == 0) return FA_OK;
+  FA_TRY(check_ptrs({q, k, v, o, dO, dq, dk, dv}, {lse}));
+  FA_TRY(check_scale(scale));
+  const Shape s{B, H, N, d, scale, causal ? 1 : 0};
+  if (static_cast<size_t>(B) * H * N > fa::kNoAllocRows) {
+    std::snprintf(g_detail, sizeof(g_detail),
+                  "fa_bwd_noalloc: B*H*N = %lld rows exceeds the built-in scratch of %zu rows; use fa_bwd",
+                  static_cast<long long>(B) * H * N, fa::kNoAllocRows);
+    return FA_ERR_WORKSPACE;
+  }
+  const size_t tb = tensor_bytes(s), vb = vec_bytes(s);
+  FA_TRY(check_disjoint({{dq, tb}, {dk, tb}, {dv, tb}}, {{q, tb}, {k, tb}, {v, tb}, {o, tb}, {dO, tb}, {lse, vb}}));
+  float* Dvec = nullptr;
+  FA_TRY(cuda_status(fa::noalloc_scratch(&Dvec), "locating the built-in scratch (cudaGetSymbolAddress)"));
+  FA_TRY(cuda_status(fa::launch_bwd_preprocess(o, dO, Dvec, s, stream), "preprocess kernel launch"));
+  FA_TRY(dkdv_checked(q, k, v, lse, dO, Dvec, dk, dv, s, stream));
+  return dq_checked(q, k, v, lse, dO, Dvec, dq, s, stream);
+}
+
 const char* fa_status_string(fa_status s) {
   switch (s) {
     case FA_OK: return "FA_OK: success";

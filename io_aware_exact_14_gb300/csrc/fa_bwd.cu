@@ -11,11 +11,13 @@
 #include "fa_ptx.cuh"
 
 #include <cmath>
+#include <mutex>
 
 namespace fa {
 namespace {
 
 __device__ unsigned int g_status_bwd = 0;
+constexpr int kMaxDevices = 64;
 
 // ---------------------------------------------------------------------------
 // Step 1: D_i = sum_c dO_ic O_ic.  HBM-bound: 16-byte loads, d/8 threads per
@@ -679,6 +681,30 @@ cudaError_t launch_bwd_preprocess(const void* o, const void* dO, float* Dvec, co
     fa_bwd_preprocess_kernel<64><<<grid, kPreThreads, 0, st>>>(static_cast<const uint8_t*>(o),
                                                                 static_cast<const uint8_t*>(dO), Dvec, rows);
   return cudaGetLastError();
+}
+
+// Scratch for fa_bwd_noalloc: the row term D lives here instead of in a
+// caller-provided workspace.  Every GPU that loads the library holds these
+// 8 MiB until the process exits; all calls share them.
+static __device__ __align__(256) float g_noalloc_rows[kNoAllocRows];
+
+cudaError_t noalloc_scratch(float** out) {
+  static std::mutex mu;
+  static float* addr[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    // a symbol's host-side name is not a device address: ask the runtime for it
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_rows);
+    if (e != cudaSuccess) return e;
+    addr[dev] = static_cast<float*>(p);
+  }
+  *out = addr[dev];
+  return cudaSuccess;
 }
 
 cudaError_t bwd_status(uint32_t* out, bool reset) {

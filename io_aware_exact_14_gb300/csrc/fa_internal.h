@@ -34,6 +34,13 @@ cudaError_t launch_bwd_dq(const CUtensorMap& tq, const CUtensorMap& tk, const CU
                           const CUtensorMap& tdo, const CUtensorMap& tdq, const float* lse,
                           const float* Dvec, const Shape& s, cudaStream_t st);
 
+// Fixed device scratch for callers that cannot allocate: room for the fp32
+// row term of up to kNoAllocRows rows (B*H*N), in a file-scope device array of
+// fa_bwd.cu.  Returns its device address for the current device, looking it up
+// (cudaGetSymbolAddress) on the first call made with that device current.
+constexpr size_t kNoAllocRows = size_t(1) << 21;  // 8 MiB of fp32
+cudaError_t noalloc_scratch(float** out);
+
 // Device status words (0 = no kernel gave up on a wait).  `reset` clears them.
 // Synchronous: copies from the device.
 cudaError_t fwd_status(uint32_t* out, bool reset);

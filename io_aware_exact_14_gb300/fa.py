@@ -32,6 +32,7 @@ SIGNATURES = {
     "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
     "fa_bwd_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
+    "fa_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
     "fa_bwd_preprocess": (_I, [_P, _P, _P, _I, _I, _I, _I, _P]),
     "fa_bwd_dkdv": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
     "fa_bwd_dq": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
@@ -161,6 +162,28 @@ def fa_bwd(q, k, v, o, lse, do, scale: Optional[float] = None, causal: bool = Fa
                        dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, scale, int(bool(causal)),
                        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_ptr(stream))
     _check("fa_bwd", st)
+    return dq, dk, dv
+
+
+def fa_bwd_noalloc(q, k, v, o, lse, do, scale: Optional[float] = None, causal: bool = False,
+                   dq=None, dk=None, dv=None, stream=None):
+    """fa_bwd for callers that cannot allocate: the library's built-in scratch holds
+    the row term, so only the gradients are caller memory (B*H*N <= 2^21)."""
+    shape = _bhnd(q, "q")
+    for t, n in ((k, "k"), (v, "v"), (o, "o"), (do, "do")):
+        _same(shape, t, n)
+    _vec(lse, shape, "lse")
+    B, H, N, d = shape
+    scale = default_scale(d) if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _same(shape, t, n)
+    st = load().fa_bwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                               do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, scale,
+                               int(bool(causal)), _stream_ptr(stream))
+    _check("fa_bwd_noalloc", st)
     return dq, dk, dv
 
 

@@ -96,6 +96,14 @@ def test_bwd_argument_checks(lib):
     assert lib.fa_bwd_dq(p[0], p[1], p[2], p[4], p[5], p[10], p[6], 1, 1, 128, 64, 0.0, 0, None) == 1
 
 
+def test_noalloc_rejects_oversized_problem_without_a_device(lib):
+    p = [FAKE + i * 0x100000 for i in range(9)]
+    assert lib.fa_bwd_noalloc(*p, 1, 64, 32769, 64, 0.125, 0, None) == 4   # 2^21 + 64 rows
+    assert b"exceeds the built-in scratch" in lib.fa_last_error_detail()
+    assert lib.fa_bwd_noalloc(*p, 1, 1, 128, 96, 0.125, 0, None) == 2
+    assert lib.fa_bwd_noalloc(0, *p[1:], 1, 1, 128, 64, 0.125, 0, None) == 1
+
+
 def test_status_strings(lib):
     for s in range(6):
         text = lib.fa_status_string(s).decode()

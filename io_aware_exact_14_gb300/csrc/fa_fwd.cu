@@ -125,47 +125,58 @@ __device__ __forceinline__ void fwd_producer(const FwdWork& w, uint8_t* smem, ui
   }
 }
 
+// Descriptor arithmetic: the start-address field is the low 14 bits of a
+// descriptor (address >> 4), so advancing an operand inside shared memory is a
+// plain add on the descriptor; every call site below adds compile-time
+// constants to a base descriptor, keeping the issuing thread's work per MMA
+// to a few instructions (the tensor core's queue is shallow, so a slow issuer
+// starves it).
 template <int D>
-__device__ __forceinline__ void fwd_issue_s(uint32_t tmem_d, uint32_t q_addr, uint32_t k_addr) {
+__device__ __forceinline__ void fwd_issue_s(uint32_t tmem_d, uint64_t q_desc, uint64_t k_desc) {
   using C = FwdCfg<D>;
   constexpr uint32_t idesc = idesc_bf16(128, 128, false, false);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = (kk / 4) * C::kBoxBytes + (kk % 4) * 32;
-    tc_mma_ss(tmem_d, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024), idesc,
-              kk > 0 ? 1u : 0u);
+    const uint64_t off = ((kk / 4) * C::kBoxBytes + (kk % 4) * 32) >> 4;
+    tc_mma_ss(tmem_d, q_desc + off, k_desc + off, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
 template <int D>
-__device__ __forceinline__ void fwd_issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_addr, bool acc) {
-  using C = FwdCfg<D>;
+__device__ __forceinline__ void fwd_issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint64_t v_desc, bool acc) {
   constexpr uint32_t idesc = idesc_bf16(128, D, false, true);
 #pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {  // 128 keys, 16 per MMA; P packs 2 keys per column
-    tc_mma_ts(tmem_o, tmem_p + kk * 8, sdesc_sw128(v_addr + kk * 2048, C::kBoxBytes, 1024), idesc,
-              (acc || kk > 0) ? 1u : 0u);
-  }
+  for (int kk = 0; kk < 8; ++kk)  // 128 keys, 16 per MMA; P packs 2 keys per TMEM column
+    tc_mma_ts(tmem_o, tmem_p + kk * 8, v_desc + ((kk * 2048) >> 4), idesc, (acc || kk > 0) ? 1u : 0u);
 }
 
+// Issue order S0(0) S1(0) | PV0(0) S0(1) PV1(0) S1(1) | PV0(1) ...: while one
+// tile's softmax runs, the tensor core works on the other tile.  All slot
+// waits of an iteration happen before the first P wait, so once P is ready a
+// PV product and the next S product go out back to back.
 template <int D>
 __device__ __forceinline__ void fwd_mma(const FwdWork& w, uint32_t tmem, uint32_t smem_base, uint64_t* full,
                                         uint64_t* empty, uint64_t* q_full, uint64_t* s_full, uint64_t* p_full,
                                         uint64_t* o_done, const CtaGuard& g) {
   using C = FwdCfg<D>;
-  const uint32_t q_addr[2] = {smem_base + C::kQOff, smem_base + C::kQOff + C::kTileBytes};
-  auto slot_addr = [&](int idx) { return smem_base + C::kSlotOff + (idx % C::kSlots) * C::kTileBytes; };
+  const uint64_t q_desc[2] = {sdesc_sw128(smem_base + C::kQOff, 16, 1024),
+                              sdesc_sw128(smem_base + C::kQOff + C::kTileBytes, 16, 1024)};
+  // K-major (S = Q K^T) and MN-major (O += P V) descriptors of ring slot 0;
+  // slot s is `s * kTileBytes` further on
+  const uint64_t k_desc0 = sdesc_sw128(smem_base + C::kSlotOff, 16, 1024);
+  const uint64_t v_desc0 = sdesc_sw128(smem_base + C::kSlotOff, C::kBoxBytes, 1024);
+  auto slot_off = [&](int idx) { return static_cast<uint64_t>((idx % C::kSlots) * (C::kTileBytes >> 4)); };
   auto slot_wait = [&](int idx) {
     return mbar_wait(&full[idx % C::kSlots], (idx / C::kSlots) & 1, g, kSiteFwd | 2u);
   };
   if (!mbar_wait(q_full, 0, g, kSiteFwd | 3u)) return;
   if (!slot_wait(0)) return;
   if (w.n0 > 0) {
-    fwd_issue_s<D>(tmem + C::col_s(0), q_addr[0], slot_addr(0));
+    fwd_issue_s<D>(tmem + C::col_s(0), q_desc[0], k_desc0 + slot_off(0));
     tc_commit(&s_full[0]);
   }
   if (w.n1 > 0) {
-    fwd_issue_s<D>(tmem + C::col_s(1), q_addr[1], slot_addr(0));
+    fwd_issue_s<D>(tmem + C::col_s(1), q_desc[1], k_desc0 + slot_off(0));
     tc_commit(&s_full[1]);
   }
   tc_commit(&empty[0]);
@@ -173,33 +184,26 @@ __device__ __forceinline__ void fwd_mma(const FwdWork& w, uint32_t tmem, uint32_
     const int iv = 2 * j + 1, ik = 2 * j + 2;
     const bool next = j + 1 < w.n;
     if (!slot_wait(iv)) return;
+    if (next && !slot_wait(ik)) return;
+    const uint64_t vd = v_desc0 + slot_off(iv), kd = k_desc0 + slot_off(ik);
     if (j < w.n0) {
       if (!mbar_wait(&p_full[0], j & 1, g, kSiteFwd | 4u)) return;
       tc_fence_after();
-      fwd_issue_pv<D>(tmem + C::col_o(0), tmem + C::col_s(0), slot_addr(iv), j > 0);
+      fwd_issue_pv<D>(tmem + C::col_o(0), tmem + C::col_s(0), vd, j > 0);
+      if (next && j + 1 < w.n0) fwd_issue_s<D>(tmem + C::col_s(0), q_desc[0], kd);
       if (j == w.n0 - 1) tc_commit(&o_done[0]);
-    }
-    if (next) {
-      if (!slot_wait(ik)) return;
-      if (j + 1 < w.n0) {
-        fwd_issue_s<D>(tmem + C::col_s(0), q_addr[0], slot_addr(ik));
-        tc_commit(&s_full[0]);
-      }
+      if (next && j + 1 < w.n0) tc_commit(&s_full[0]);
     }
     if (j < w.n1) {
       if (!mbar_wait(&p_full[1], j & 1, g, kSiteFwd | 5u)) return;
       tc_fence_after();
-      fwd_issue_pv<D>(tmem + C::col_o(1), tmem + C::col_s(1), slot_addr(iv), j > 0);
+      fwd_issue_pv<D>(tmem + C::col_o(1), tmem + C::col_s(1), vd, j > 0);
+      if (next && j + 1 < w.n1) fwd_issue_s<D>(tmem + C::col_s(1), q_desc[1], kd);
       if (j == w.n1 - 1) tc_commit(&o_done[1]);
+      if (next && j + 1 < w.n1) tc_commit(&s_full[1]);
     }
     tc_commit(&empty[iv % C::kSlots]);
-    if (next) {
-      if (j + 1 < w.n1) {
-        fwd_issue_s<D>(tmem + C::col_s(1), q_addr[1], slot_addr(ik));
-        tc_commit(&s_full[1]);
-      }
-      tc_commit(&empty[ik % C::kSlots]);
-    }
+    if (next) tc_commit(&empty[ik % C::kSlots]);
   }
 }
 

@@ -170,29 +170,33 @@ __device__ __forceinline__ void bwd_init(const BwdBars& b, uint32_t staged_count
 
 // S-like product: D(128 x 128) = A(128 x d) * B(128 x d)^T, both K-major tiles.
 template <int D>
-__device__ __forceinline__ void mma_nt(uint32_t tmem_d, uint32_t a_addr, uint32_t b_addr) {
+__device__ __forceinline__ void mma_nt(uint32_t tmem_d, uint64_t a_desc, uint64_t b_desc) {
   using C = BwdCfg<D>;
   constexpr uint32_t idesc = idesc_bf16(128, 128, false, false);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = (kk / 4) * C::kBoxBytes + (kk % 4) * 32;
-    tc_mma_ss(tmem_d, sdesc_sw128(a_addr + off, 16, 1024), sdesc_sw128(b_addr + off, 16, 1024), idesc,
-              kk > 0 ? 1u : 0u);
+    const uint64_t off = ((kk / 4) * C::kBoxBytes + (kk % 4) * 32) >> 4;   // descriptor address units
+    tc_mma_ss(tmem_d, a_desc + off, b_desc + off, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
 // Accumulating product: D(128 x d) += A(128 x 128, TMEM bf16) * B(128 x d, MN-major tile).
 // A's 128 K columns live as two 64-wide halves at a_tmem and a_tmem + 64.
 template <int D>
-__device__ __forceinline__ void mma_tn_acc(uint32_t tmem_d, uint32_t a_tmem, uint32_t b_addr, bool acc) {
-  using C = BwdCfg<D>;
+__device__ __forceinline__ void mma_tn_acc(uint32_t tmem_d, uint32_t a_tmem, uint64_t b_desc, bool acc) {
   constexpr uint32_t idesc = idesc_bf16(128, D, false, true);
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
     const uint32_t a = a_tmem + (kk / 4) * 64 + (kk % 4) * 8;
-    tc_mma_ts(tmem_d, a, sdesc_sw128(b_addr + kk * 2048, C::kBoxBytes, 1024), idesc, (acc || kk > 0) ? 1u : 0u);
+    tc_mma_ts(tmem_d, a, b_desc + ((kk * 2048) >> 4), idesc, (acc || kk > 0) ? 1u : 0u);
   }
 }
+
+// K-major (kmaj) and MN-major (mnmaj) descriptors of a 128-row tile at `addr`.
+template <int D>
+__device__ __forceinline__ uint64_t kmaj(uint32_t addr) { return sdesc_sw128(addr, 16, 1024); }
+template <int D>
+__device__ __forceinline__ uint64_t mnmaj(uint32_t addr) { return sdesc_sw128(addr, BwdCfg<D>::kBoxBytes, 1024); }
 
 // Pack 32 fp32 values (in two 16-value halves) into 16 bf16x2 words and store
 // them to 16 TMEM columns.
@@ -331,12 +335,21 @@ __global__ void __launch_bounds__(384, 1)
       if (lane == 0) {
         const uint32_t tS = tmem + C::kColS, tDP = tmem + C::kColDP;
         const uint32_t tDV = tmem + C::kColAcc0, tDK = tmem + C::kColAcc1;
-        const uint32_t aK = sbase + C::kResOff, aV = sbase + C::kResOff + C::kTileBytes;
+        const uint64_t kK = kmaj<D>(sbase + C::kResOff), kV = kmaj<D>(sbase + C::kResOff + C::kTileBytes);
+        // stage st: Q and dO as K-major B operands (S^T, dP^T) and as MN-major
+        // B operands (dK, dV); stages are kStageBytes apart
+        const uint64_t kQ0 = kmaj<D>(sbase + C::x_off(0)), kDO0 = kmaj<D>(sbase + C::y_off(0));
+        const uint64_t mQ0 = mnmaj<D>(sbase + C::x_off(0)), mDO0 = mnmaj<D>(sbase + C::y_off(0));
+        auto stg = [](int st) { return static_cast<uint64_t>(st) * (C::kStageBytes >> 4); };
+        auto kQ = [&](int st) { return kQ0 + stg(st); };
+        auto kDO = [&](int st) { return kDO0 + stg(st); };
+        auto mQ = [&](int st) { return mQ0 + stg(st); };
+        auto mDO = [&](int st) { return mDO0 + stg(st); };
         bool ok = mbar_wait(bb.res_full, 0, g, kSiteDkdv | 2u) && mbar_wait(&bb.full[0], 0, g, kSiteDkdv | 3u);
         if (ok) {
-          mma_nt<D>(tS, aK, sbase + C::x_off(0));
+          mma_nt<D>(tS, kK, kQ(0));
           tc_commit(bb.s_full);
-          mma_nt<D>(tDP, aV, sbase + C::y_off(0));
+          mma_nt<D>(tDP, kV, kDO(0));
           tc_commit(bb.dp_full);
         }
         for (int it = 0; ok && it < cnt; ++it) {
@@ -346,18 +359,20 @@ __global__ void __launch_bounds__(384, 1)
           const int st1 = (it + 1) % C::kStages;
           if (!(ok = mbar_wait(bb.p_full, par, g, kSiteDkdv | 4u))) break;
           tc_fence_after();
-          mma_tn_acc<D>(tDV, tS, sbase + C::y_off(st), it > 0);          // dV += P^T dO_i
+          mma_tn_acc<D>(tDV, tS, mDO(st), it > 0);          // dV += P^T dO_i
           if (next) {
+            // with two stages the next query tile is still loading when dV(i) can
+            // start, so it is awaited only here
             if (!(ok = mbar_wait(&bb.full[st1], ((it + 1) / C::kStages) & 1, g, kSiteDkdv | 5u))) break;
-            mma_nt<D>(tS, aK, sbase + C::x_off(st1));                     // S^T(i+1)
+            mma_nt<D>(tS, kK, kQ(st1));                     // S^T(i+1)
             tc_commit(bb.s_full);
           }
           if (!(ok = mbar_wait(bb.ds_full, par, g, kSiteDkdv | 6u))) break;
           tc_fence_after();
-          mma_tn_acc<D>(tDK, tDP, sbase + C::x_off(st), it > 0);         // dK += dS^T Q_i
+          mma_tn_acc<D>(tDK, tDP, mQ(st), it > 0);          // dK += dS^T Q_i
           tc_commit(&bb.empty[st]);
           if (next) {
-            mma_nt<D>(tDP, aV, sbase + C::y_off(st1));                    // dP^T(i+1)
+            mma_nt<D>(tDP, kV, kDO(st1));                   // dP^T(i+1)
             tc_commit(bb.dp_full);
           }
         }
@@ -398,12 +413,23 @@ __global__ void __launch_bounds__(384, 1)
     tmem_ld_wait(sr[0]);
     tmem_ld_fence(sr[1]);
     float p[64];
-    // diagonal tile: query column 64h + c is masked when it precedes key t
-    const int lim = (CAUSAL && qt == kt) ? t - 64 * h : -1;
+    const float4* lse4 = reinterpret_cast<const float4*>(lse2);
 #pragma unroll
-    for (int c = 0; c < 64; ++c) {
-      const float x = fmaf(__uint_as_float(sr[c / 32][c % 32]), scale_log2, -lse2[c]);
-      p[c] = (c < lim) ? 0.f : ex2_approx(x);
+    for (int c4 = 0; c4 < 16; ++c4) {  // one 16-byte broadcast load per four columns
+      const float4 l4 = lse4[c4];
+      const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int c = 4 * c4 + e;
+        p[c] = ex2_approx(fmaf(__uint_as_float(sr[c / 32][c % 32]), scale_log2, -lv[e]));
+      }
+    }
+    if (CAUSAL && qt == kt) {
+      // diagonal tile: query column 64h + c precedes key t (and is masked) when c < t - 64h
+      const int lim = t - 64 * h;
+#pragma unroll
+      for (int c = 0; c < 64; ++c)
+        if (c < lim) p[c] = 0.f;
     }
 #pragma unroll
     for (int c = 0; c < 64; c += 32) {
@@ -421,8 +447,17 @@ __global__ void __launch_bounds__(384, 1)
     tmem_ld32(tDP + 32, dr[1]);
     tmem_ld_wait(dr[0]);
     tmem_ld_fence(dr[1]);
+    const float4* dv4 = reinterpret_cast<const float4*>(dv);
 #pragma unroll
-    for (int c = 0; c < 64; ++c) p[c] = p[c] * (__uint_as_float(dr[c / 32][c % 32]) - dv[c]);
+    for (int c4 = 0; c4 < 16; ++c4) {
+      const float4 d4 = dv4[c4];
+      const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int c = 4 * c4 + e;
+        p[c] = p[c] * (__uint_as_float(dr[c / 32][c % 32]) - dd[e]);
+      }
+    }
 #pragma unroll
     for (int c = 0; c < 64; c += 32) st_bf16_16cols(tDP + c / 2, p + c);
     tmem_st_wait();
@@ -505,12 +540,20 @@ __global__ void __launch_bounds__(384, 1)
     } else if (warp == 9) {  // MMA issuer
       if (lane == 0) {
         const uint32_t tS = tmem + C::kColS, tDP = tmem + C::kColDP, tDQ = tmem + C::kColAcc0;
-        const uint32_t aQ = sbase + C::kResOff, aDO = sbase + C::kResOff + C::kTileBytes;
+        const uint64_t kQ = kmaj<D>(sbase + C::kResOff), kDO = kmaj<D>(sbase + C::kResOff + C::kTileBytes);
+        // stage st: K, V as K-major B operands (S, dP) and K as the MN-major B
+        // operand of dQ; stages are kStageBytes apart
+        const uint64_t kK0 = kmaj<D>(sbase + C::x_off(0)), kV0 = kmaj<D>(sbase + C::y_off(0));
+        const uint64_t mK0 = mnmaj<D>(sbase + C::x_off(0));
+        auto stg = [](int st) { return static_cast<uint64_t>(st) * (C::kStageBytes >> 4); };
+        auto kK = [&](int st) { return kK0 + stg(st); };
+        auto kV = [&](int st) { return kV0 + stg(st); };
+        auto mK = [&](int st) { return mK0 + stg(st); };
         bool ok = mbar_wait(bb.res_full, 0, g, kSiteDq | 2u) && mbar_wait(&bb.full[0], 0, g, kSiteDq | 3u);
         if (ok) {
-          mma_nt<D>(tS, aQ, sbase + C::x_off(0));
+          mma_nt<D>(tS, kQ, kK(0));
           tc_commit(bb.s_full);
-          mma_nt<D>(tDP, aDO, sbase + C::y_off(0));
+          mma_nt<D>(tDP, kDO, kV(0));
           tc_commit(bb.dp_full);
         }
         for (int it = 0; ok && it < cnt; ++it) {
@@ -522,15 +565,15 @@ __global__ void __launch_bounds__(384, 1)
             if (!(ok = mbar_wait(&bb.full[st1], ((it + 1) / C::kStages) & 1, g, kSiteDq | 4u))) break;
             if (!(ok = mbar_wait(bb.s_free, par, g, kSiteDq | 5u))) break;
             tc_fence_after();
-            mma_nt<D>(tS, aQ, sbase + C::x_off(st1));                 // S(j+1)
+            mma_nt<D>(tS, kQ, kK(st1));                 // S(j+1)
             tc_commit(bb.s_full);
           }
           if (!(ok = mbar_wait(bb.ds_full, par, g, kSiteDq | 6u))) break;
           tc_fence_after();
-          mma_tn_acc<D>(tDQ, tDP, sbase + C::x_off(st), it > 0);     // dQ += dS K_j
+          mma_tn_acc<D>(tDQ, tDP, mK(st), it > 0);     // dQ += dS K_j
           tc_commit(&bb.empty[st]);
           if (next) {
-            mma_nt<D>(tDP, aDO, sbase + C::y_off(st1));               // dP(j+1)
+            mma_nt<D>(tDP, kDO, kV(st1));               // dP(j+1)
             tc_commit(bb.dp_full);
           }
         }
@@ -579,9 +622,11 @@ __global__ void __launch_bounds__(384, 1)
     if (CAUSAL) lim = min(lim, row - k0 + 1);
     float p[64];
 #pragma unroll
-    for (int c = 0; c < 64; ++c) {
-      const float x = fmaf(__uint_as_float(sr[c / 32][c % 32]), scale_log2, -lse2);
-      p[c] = (c < lim) ? ex2_approx(x) : 0.f;
+    for (int c = 0; c < 64; ++c) p[c] = ex2_approx(fmaf(__uint_as_float(sr[c / 32][c % 32]), scale_log2, -lse2));
+    if (lim < 64) {  // diagonal or ragged-tail tile only
+#pragma unroll
+      for (int c = 0; c < 64; ++c)
+        if (c >= lim) p[c] = 0.f;
     }
     if (!(ok = mbar_wait(bb.dp_full, par, g, kSiteDq | 8u))) break;
     __syncwarp();

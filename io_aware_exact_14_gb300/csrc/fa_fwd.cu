@@ -247,10 +247,16 @@ __device__ __forceinline__ void fwd_softmax(const FwdWork& w, int tile, uint32_t
       for (int c = 0; c < 128; ++c)
         if (c >= lim) s[c / 32][c % 32] = __float_as_uint(-INFINITY);
     }
-    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    // row max: 3-input maxes over 8 independent chains
+    float mx[8];
 #pragma unroll
-    for (int c = 0; c < 128; ++c) mx[c % 4] = fmaxf(mx[c % 4], __uint_as_float(s[c / 32][c % 32]));
-    const float row_max = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * scale_log2;
+    for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < 128; c += 2)
+      mx[(c / 2) % 8] = max3f(mx[(c / 2) % 8], __uint_as_float(s[c / 32][c % 32]),
+                              __uint_as_float(s[(c + 1) / 32][(c + 1) % 32]));
+    const float row_max =
+        fmaxf(max3f(mx[0], mx[1], mx[2]), max3f(max3f(mx[3], mx[4], mx[5]), mx[6], mx[7])) * scale_log2;
 
     if (j == 0) {
       m_use = row_max;  // O is overwritten by the first P V product
@@ -274,20 +280,28 @@ __device__ __forceinline__ void fwd_softmax(const FwdWork& w, int tile, uint32_t
     }
     __syncwarp();
     const float m_off = (m_use == -INFINITY) ? 0.f : m_use;
-    float sum[4] = {0.f, 0.f, 0.f, 0.f};
+    // x = s * scale * log2(e) - m and the row sums, two columns per packed instruction
+    const float2 sc2 = make_float2(scale_log2, scale_log2), mo2 = make_float2(-m_off, -m_off);
+    float2 sum[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sum[i] = make_float2(0.f, 0.f);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {  // keys [64h, 64h+64) -> P columns [32h, 32h+32)
       uint32_t pk[32];
 #pragma unroll
       for (int c = 64 * h; c < 64 * h + 64; c += 2) {
-        const float p0 = ex2_approx(fmaf(__uint_as_float(s[c / 32][c % 32]), scale_log2, -m_off));
-        const float p1 = ex2_approx(fmaf(__uint_as_float(s[(c + 1) / 32][(c + 1) % 32]), scale_log2, -m_off));
-        sum[(c / 2) % 4] += p0 + p1;
-        pk[(c / 2) % 32] = pack_bf16x2(p0, p1);
+        const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[c / 32][c % 32]),
+                                                __uint_as_float(s[(c + 1) / 32][(c + 1) % 32])),
+                                    sc2, mo2);
+        const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+        sum[(c / 2) % 4] = __fadd2_rn(sum[(c / 2) % 4], pp);
+        pk[(c / 2) % 32] = pack_bf16x2(pp.x, pp.y);
       }
       tmem_st32(tS + 32 * h, pk);
     }
-    l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
+    const float2 s01 = __fadd2_rn(sum[0], sum[1]), s23 = __fadd2_rn(sum[2], sum[3]);
+    const float2 s0123 = __fadd2_rn(s01, s23);
+    l += s0123.x + s0123.y;
     tmem_st_wait();
     tc_fence_before();
     mbar_arrive(&p_full[tile]);

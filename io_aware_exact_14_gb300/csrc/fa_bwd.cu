@@ -241,23 +241,24 @@ __device__ __forceinline__ void bwd_store_acc(uint32_t tacc, uint8_t* stage, int
   }
 }
 
-// Row vectors for a query tile: lse2 = lse * log2(e) (+inf past N, so P = 0
-// there) and D (0 past N).  The whole producer warp writes them.
-__device__ __forceinline__ void load_row_vectors(float* lse2, float* dvec, const float* __restrict__ lse,
+// Row vectors for a query tile, stored negated so the compute warps add them
+// with packed FMAs: -lse * log2(e) (-inf past N, so P = 0 there) and -D
+// (0 past N).  The whole producer warp writes them.
+__device__ __forceinline__ void load_row_vectors(float* nlse2, float* nd, const float* __restrict__ lse,
                                                  const float* __restrict__ Dg, size_t row_base, int q0, int N,
                                                  int lane) {
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const int c = lane + 32 * k;
     const int q = q0 + c;
-    float a = INFINITY, d = 0.f;
+    float a = -INFINITY, d = 0.f;
     if (q < N) {
       const float l = lse[row_base + q];
-      a = (l == -INFINITY) ? INFINITY : l * kLog2e;
-      d = Dg[row_base + q];
+      a = (l == -INFINITY) ? -INFINITY : -l * kLog2e;
+      d = -Dg[row_base + q];
     }
-    lse2[c] = a;
-    dvec[c] = d;
+    nlse2[c] = a;
+    nd[c] = d;
   }
 }
 
@@ -400,8 +401,8 @@ __global__ void __launch_bounds__(384, 1)
     const int st = it % C::kStages;
     const uint32_t par = it & 1;
     const int qt = i0 + it;
-    const float* lse2 = reinterpret_cast<const float*>(smem + C::vec_off(st)) + 64 * h;
-    const float* dv = lse2 + 128;
+    const float* nlse2 = reinterpret_cast<const float*>(smem + C::vec_off(st)) + 64 * h;
+    const float* dv = nlse2 + 128;   // -D
     // the row vectors were written by the producer before it arrived on full[st]
     if (!(ok = mbar_wait(&bb.full[st], (it / C::kStages) & 1, g, kSiteDkdv | 7u))) break;
     if (!(ok = mbar_wait(bb.s_full, par, g, kSiteDkdv | 8u))) break;
@@ -413,15 +414,19 @@ __global__ void __launch_bounds__(384, 1)
     tmem_ld_wait(sr[0]);
     tmem_ld_fence(sr[1]);
     float p[64];
-    const float4* lse4 = reinterpret_cast<const float4*>(lse2);
+    const float4* lse4 = reinterpret_cast<const float4*>(nlse2);   // holds -lse * log2(e)
+    const float2 sc2 = make_float2(scale_log2, scale_log2);
 #pragma unroll
     for (int c4 = 0; c4 < 16; ++c4) {  // one 16-byte broadcast load per four columns
       const float4 l4 = lse4[c4];
-      const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
+      for (int e = 0; e < 4; e += 2) {
         const int c = 4 * c4 + e;
-        p[c] = ex2_approx(fmaf(__uint_as_float(sr[c / 32][c % 32]), scale_log2, -lv[e]));
+        const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[c / 32][c % 32]),
+                                                __uint_as_float(sr[(c + 1) / 32][(c + 1) % 32])),
+                                    sc2, e ? make_float2(l4.z, l4.w) : make_float2(l4.x, l4.y));
+        p[c] = ex2_approx(x.x);
+        p[c + 1] = ex2_approx(x.y);
       }
     }
     if (CAUSAL && qt == kt) {
@@ -447,15 +452,19 @@ __global__ void __launch_bounds__(384, 1)
     tmem_ld32(tDP + 32, dr[1]);
     tmem_ld_wait(dr[0]);
     tmem_ld_fence(dr[1]);
-    const float4* dv4 = reinterpret_cast<const float4*>(dv);
+    const float4* dv4 = reinterpret_cast<const float4*>(dv);   // holds -D
 #pragma unroll
     for (int c4 = 0; c4 < 16; ++c4) {
       const float4 d4 = dv4[c4];
-      const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
+      for (int e = 0; e < 4; e += 2) {
         const int c = 4 * c4 + e;
-        p[c] = p[c] * (__uint_as_float(dr[c / 32][c % 32]) - dd[e]);
+        const float2 dp = __fadd2_rn(make_float2(__uint_as_float(dr[c / 32][c % 32]),
+                                                 __uint_as_float(dr[(c + 1) / 32][(c + 1) % 32])),
+                                     e ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y));
+        const float2 ds = __fmul2_rn(make_float2(p[c], p[c + 1]), dp);
+        p[c] = ds.x;
+        p[c + 1] = ds.y;
       }
     }
 #pragma unroll
@@ -597,12 +606,14 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
   const uint32_t tS = tmem + lane_base + C::kColS + 64 * h;
   const uint32_t tDP = tmem + lane_base + C::kColDP + 64 * h;
-  float lse2 = INFINITY, drow = 0.f;
+  float nlse2 = -INFINITY, ndrow = 0.f;   // -lse * log2(e) and -D of this row
   if (row < N) {
     const float l = lse[row_base + row];
-    lse2 = (l == -INFINITY) ? INFINITY : l * kLog2e;
-    drow = Dg[row_base + row];
+    nlse2 = (l == -INFINITY) ? -INFINITY : -l * kLog2e;
+    ndrow = -Dg[row_base + row];
   }
+  const float2 sc2 = make_float2(scale_log2, scale_log2), nl2 = make_float2(nlse2, nlse2);
+  const float2 nd2 = make_float2(ndrow, ndrow);
   bool ok = true;
   for (int it = 0; ok && it < cnt; ++it) {
     const uint32_t par = it & 1;
@@ -622,7 +633,13 @@ __global__ void __launch_bounds__(384, 1)
     if (CAUSAL) lim = min(lim, row - k0 + 1);
     float p[64];
 #pragma unroll
-    for (int c = 0; c < 64; ++c) p[c] = ex2_approx(fmaf(__uint_as_float(sr[c / 32][c % 32]), scale_log2, -lse2));
+    for (int c = 0; c < 64; c += 2) {
+      const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[c / 32][c % 32]),
+                                              __uint_as_float(sr[(c + 1) / 32][(c + 1) % 32])),
+                                  sc2, nl2);
+      p[c] = ex2_approx(x.x);
+      p[c + 1] = ex2_approx(x.y);
+    }
     if (lim < 64) {  // diagonal or ragged-tail tile only
 #pragma unroll
       for (int c = 0; c < 64; ++c)
@@ -637,7 +654,14 @@ __global__ void __launch_bounds__(384, 1)
     tmem_ld_wait(dr[0]);
     tmem_ld_fence(dr[1]);
 #pragma unroll
-    for (int c = 0; c < 64; ++c) p[c] = p[c] * (__uint_as_float(dr[c / 32][c % 32]) - drow);
+    for (int c = 0; c < 64; c += 2) {
+      const float2 dp = __fadd2_rn(make_float2(__uint_as_float(dr[c / 32][c % 32]),
+                                               __uint_as_float(dr[(c + 1) / 32][(c + 1) % 32])),
+                                   nd2);
+      const float2 ds = __fmul2_rn(make_float2(p[c], p[c + 1]), dp);
+      p[c] = ds.x;
+      p[c + 1] = ds.y;
+    }
 #pragma unroll
     for (int c = 0; c < 64; c += 32) st_bf16_16cols(tDP + c / 2, p + c);
     tmem_st_wait();

@@ -278,15 +278,15 @@ __global__ void __launch_bounds__(384, 1)
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                        const __grid_constant__ CUtensorMap tmDK, const __grid_constant__ CUtensorMap tmDV,
                        const float* __restrict__ lse, const float* __restrict__ Dg, int N, int n_tiles,
-                       float scale, float scale_log2) {
+                       int BH, int band, float scale, float scale_log2) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const BwdBars bb = bwd_bars<D>(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const int bh = blockIdx.x / n_tiles;
-  const int kt = static_cast<int>(blockIdx.x % n_tiles);       // key tile; causal: small kt is heavy
+  int bh, kt;   // key tile; causal: small kt is heavy, so rank 0 -> kt 0
+  banded_order(blockIdx.x, n_tiles, BH, band, bh, kt);
   const int i0 = CAUSAL ? kt : 0;                               // first query tile
   const int cnt = n_tiles - i0;                                 // query tiles visited (>= 1)
   const size_t row_base = static_cast<size_t>(bh) * N;
@@ -501,15 +501,17 @@ __global__ void __launch_bounds__(384, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                      const __grid_constant__ CUtensorMap tmDQ, const float* __restrict__ lse,
-                     const float* __restrict__ Dg, int N, int n_tiles, float scale, float scale_log2) {
+                     const float* __restrict__ Dg, int N, int n_tiles, int BH, int band, float scale,
+                     float scale_log2) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const BwdBars bb = bwd_bars<D>(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const int bh = blockIdx.x / n_tiles;
-  const int qt = n_tiles - 1 - static_cast<int>(blockIdx.x % n_tiles);  // causal: large qt is heavy
+  int bh, rank;
+  banded_order(blockIdx.x, n_tiles, BH, band, bh, rank);
+  const int qt = n_tiles - 1 - rank;  // causal: large qt is heavy
   const int cnt = CAUSAL ? qt + 1 : n_tiles;                             // key tiles visited
   const size_t row_base = static_cast<size_t>(bh) * N;
 
@@ -690,8 +692,8 @@ cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CU
   const int n_tiles = (s.N + 127) / 128;
   const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
   const dim3 grid(static_cast<unsigned>(s.B) * s.H * n_tiles);
-  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s.N, n_tiles, s.scale,
-                                                 scale_log2);
+  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s.N, n_tiles, s.B * s.H,
+                                                 head_band(s.N, s.d), s.scale, scale_log2);
   return cudaGetLastError();
 }
 
@@ -706,8 +708,8 @@ cudaError_t launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   const int n_tiles = (s.N + 127) / 128;
   const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
   const dim3 grid(static_cast<unsigned>(s.B) * s.H * n_tiles);
-  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, tdq, lse, Dvec, s.N, n_tiles, s.scale,
-                                                 scale_log2);
+  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, tdq, lse, Dvec, s.N, n_tiles, s.B * s.H,
+                                                 head_band(s.N, s.d), s.scale, scale_log2);
   return cudaGetLastError();
 }
 

@@ -71,10 +71,11 @@ struct FwdWork {
   int bh, qt0, n0, n1, n;
 };
 
-__device__ __forceinline__ FwdWork fwd_work(int N, int n_pairs, bool causal) {
+__device__ __forceinline__ FwdWork fwd_work(int N, int n_pairs, int BH, int band, bool causal) {
   FwdWork w;
-  w.bh = blockIdx.x / n_pairs;
-  const int pair = n_pairs - 1 - static_cast<int>(blockIdx.x % n_pairs);  // heavy tiles first
+  int rank;
+  banded_order(blockIdx.x, n_pairs, BH, band, w.bh, rank);
+  const int pair = n_pairs - 1 - rank;  // heavy (causal) pairs first
   const int n_qt = (N + 127) / 128;
   w.qt0 = 2 * pair;
   const int qt1 = w.qt0 + 1;
@@ -345,7 +346,7 @@ template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                  float* __restrict__ lse, int N, int n_pairs, float scale_log2) {
+                  float* __restrict__ lse, int N, int n_pairs, int BH, int band, float scale_log2) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -363,7 +364,7 @@ __global__ void __launch_bounds__(384, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const FwdWork w = fwd_work(N, n_pairs, CAUSAL);
+  const FwdWork w = fwd_work(N, n_pairs, BH, band, CAUSAL);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kSlots; ++i) {
@@ -443,7 +444,8 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   const int n_pairs = (n_qt + 1) / 2;
   const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
   const dim3 grid(static_cast<unsigned>(s.B) * s.H * n_pairs);
-  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, to, lse, s.N, n_pairs, scale_log2);
+  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, to, lse, s.N, n_pairs, s.B * s.H, head_band(s.N, s.d),
+                                                 scale_log2);
   return cudaGetLastError();
 }
 

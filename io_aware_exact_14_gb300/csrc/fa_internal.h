@@ -41,6 +41,14 @@ cudaError_t launch_bwd_dq(const CUtensorMap& tq, const CUtensorMap& tk, const CU
 constexpr size_t kNoAllocRows = size_t(1) << 21;  // 8 MiB of fp32
 cudaError_t noalloc_scratch(float** out);
 
+// Heads per scheduling band: the band's K and V (2 * N * d bf16 per head)
+// stay within ~48 MB of L2, at most 16 heads.
+inline int head_band(int N, int d) {
+  const long long per_head = 4ll * N * d;
+  long long b = (48ll << 20) / (per_head > 0 ? per_head : 1);
+  return static_cast<int>(b < 1 ? 1 : (b > 16 ? 16 : b));
+}
+
 // Device status words (0 = no kernel gave up on a wait).  `reset` clears them.
 // Synchronous: copies from the device.
 cudaError_t fwd_status(uint32_t* out, bool reset);

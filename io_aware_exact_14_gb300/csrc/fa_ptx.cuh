@@ -299,6 +299,25 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // ---------------------------------------------------------------------------
+// Work order
+// ---------------------------------------------------------------------------
+
+// CTA -> (head bh, work rank) for grids of BH heads x n_tiles tiles.  Heads
+// are taken in bands of `band`; inside a band all rank-0 tiles come first,
+// then rank 1, ...  Callers map rank 0 to their heaviest (causal) tile, so
+// the last CTAs to start are the light ones, while the heads in flight stay
+// few enough for their K/V (or Q/dO) to remain in L2.
+__device__ __forceinline__ void banded_order(int cta, int n_tiles, int BH, int band, int& bh, int& rank) {
+  const int per_band = band * n_tiles;
+  const int b = cta / per_band;
+  const int bh0 = b * band;
+  const int width = min(band, BH - bh0);
+  const int r = cta - b * per_band;
+  rank = r / width;
+  bh = bh0 + r % width;
+}
+
+// ---------------------------------------------------------------------------
 // Small numeric helpers
 // ---------------------------------------------------------------------------
 

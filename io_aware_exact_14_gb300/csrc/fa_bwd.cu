@@ -113,7 +113,7 @@ struct BwdCfg {
   static constexpr uint32_t kMiscOff = kBarOff + kBars * 8;
   static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;
   static constexpr int kThreads = 384;
-  static constexpr uint32_t kColS = 0, kColDP = 128, kColAcc0 = 256, kColAcc1 = 256 + D;
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColAcc0 = 256;
   __host__ __device__ static constexpr uint32_t x_off(int st) { return kStageOff + st * kStageBytes; }
   __host__ __device__ static constexpr uint32_t y_off(int st) { return x_off(st) + kTileBytes; }
   __host__ __device__ static constexpr uint32_t vec_off(int st) { return x_off(st) + 2 * kTileBytes; }
@@ -176,7 +176,7 @@ __device__ __forceinline__ void mma_nt(uint32_t tmem_d, uint64_t a_desc, uint64_
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint64_t off = ((kk / 4) * C::kBoxBytes + (kk % 4) * 32) >> 4;   // descriptor address units
-    tc_mma_ss(tmem_d, a_desc + off, b_desc + off, idesc, kk > 0 ? 1u : 0u);
+    tc_mma_ss_w(tmem_d, a_desc + off, b_desc + off, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
@@ -188,7 +188,7 @@ __device__ __forceinline__ void mma_tn_acc(uint32_t tmem_d, uint32_t a_tmem, uin
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
     const uint32_t a = a_tmem + (kk / 4) * 64 + (kk % 4) * 8;
-    tc_mma_ts(tmem_d, a, b_desc + ((kk * 2048) >> 4), idesc, (acc || kk > 0) ? 1u : 0u);
+    tc_mma_ts_w(tmem_d, a, b_desc + ((kk * 2048) >> 4), idesc, (acc || kk > 0) ? 1u : 0u);
   }
 }
 
@@ -243,23 +243,28 @@ __device__ __forceinline__ void bwd_store_acc(uint32_t tacc, uint8_t* stage, int
 
 // Row vectors for a query tile, stored negated so the compute warps add them
 // with packed FMAs: -lse * log2(e) (-inf past N, so P = 0 there) and -D
-// (0 past N).  The whole producer warp writes them.
-__device__ __forceinline__ void load_row_vectors(float* nlse2, float* nd, const float* __restrict__ lse,
-                                                 const float* __restrict__ Dg, size_t row_base, int q0, int N,
-                                                 int lane) {
+// (0 past N).  The whole producer warp handles them, four columns per lane:
+// fetched into registers one tile ahead (so the global-load latency hides
+// behind the wait for a free stage), then written to the stage.
+struct RowVecs {
+  float a[4], d[4];
+};
+
+__device__ __forceinline__ RowVecs fetch_row_vectors(const float* __restrict__ lse, const float* __restrict__ Dg,
+                                                     size_t row_base, int q0, int N, int lane) {
+  RowVecs r;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const int c = lane + 32 * k;
-    const int q = q0 + c;
-    float a = -INFINITY, d = 0.f;
+    const int q = q0 + lane + 32 * k;
+    r.a[k] = -INFINITY;
+    r.d[k] = 0.f;
     if (q < N) {
       const float l = lse[row_base + q];
-      a = (l == -INFINITY) ? -INFINITY : -l * kLog2e;
-      d = -Dg[row_base + q];
+      r.a[k] = (l == -INFINITY) ? -INFINITY : -l * kLog2e;
+      r.d[k] = -Dg[row_base + q];
     }
-    nlse2[c] = a;
-    nd[c] = d;
   }
+  return r;
 }
 
 // ---------------------------------------------------------------------------
@@ -267,10 +272,44 @@ __device__ __forceinline__ void load_row_vectors(float* nlse2, float* nd, const 
 //   S^T = K_j Q_i^T, P^T = exp2(S^T * scale * log2e - lse2_i)
 //   dP^T = V_j dO_i^T, dS^T = P^T o (dP^T - D_i)
 //   dV_j += P^T dO_i,  dK_j += dS^T Q_i,  finally dK_j *= scale
-// MMA order S(i) dP(i) dV(i) S(i+1) dK(i) dP(i+1) ...: the exponentials of tile i
-// run under dP(i), the dS products under dV(i) and S(i+1).
+// K_j and V_j stay resident; Q_i (with -lse) streams through a 3-deep ring and
+// dO_i (with -D) through a 2-deep ring, so the next query tile is loaded well
+// before S^T(i+1) needs it.
+// MMA order S(i) dP(i) dV(i) {S(i+1), dK(i)} dP(i+1) ...: the exponentials of
+// tile i run under dP(i), the dS products under dV(i); S^T(i+1) and dK(i)
+// touch different TMEM columns and go in whichever order their inputs land.
 // TMEM: T0 = S^T, T1 = dP^T, acc0 = dV, acc1 = dK.
 // ---------------------------------------------------------------------------
+
+template <int D>
+struct DkdvCfg {
+  static_assert(D == 64 || D == 128, "head dim");
+  static constexpr int kBoxes = D / 64;
+  static constexpr uint32_t kBoxBytes = 128u * 128u;
+  static constexpr uint32_t kTileBytes = kBoxes * kBoxBytes;
+  static constexpr int kQStages = 3, kDOStages = 2;
+  static constexpr uint32_t kKOff = 0, kVOff = kTileBytes;
+  static constexpr uint32_t kQOff = 2 * kTileBytes;
+  static constexpr uint32_t kDOOff = kQOff + kQStages * kTileBytes;
+  static constexpr uint32_t kLseOff = kDOOff + kDOStages * kTileBytes;   // 128 fp32 per Q stage
+  static constexpr uint32_t kDVecOff = kLseOff + kQStages * 512;          // 128 fp32 per dO stage
+  static constexpr uint32_t kBarOff = kDVecOff + kDOStages * 512;
+  // res_full, q_full[3], q_empty[3], do_full[2], do_empty[2], s_full, dp_full, p_full, ds_full,
+  // acc_done, drain, staged[2]
+  static constexpr int kBars = 1 + 2 * kQStages + 2 * kDOStages + 8;
+  static constexpr uint32_t kMiscOff = kBarOff + kBars * 8;
+  static constexpr uint32_t kLayoutBytes = kMiscOff + 16;
+  static constexpr uint32_t kMaxSmem = 232448;   // per-CTA opt-in limit
+  // room for the 1024-byte alignment of the base when it fits, else all there is
+  static constexpr uint32_t kSmemBytes = kLayoutBytes + 1024 <= kMaxSmem ? kLayoutBytes + 1024 : kMaxSmem;
+  static_assert(kLayoutBytes <= kMaxSmem, "dK/dV shared-memory layout too large");
+  static constexpr int kThreads = 384;
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+  __host__ __device__ static constexpr uint32_t q_off(int s) { return kQOff + s * kTileBytes; }
+  __host__ __device__ static constexpr uint32_t do_off(int s) { return kDOOff + s * kTileBytes; }
+  __host__ __device__ static constexpr uint32_t lse_off(int s) { return kLseOff + s * 512; }
+  __host__ __device__ static constexpr uint32_t dvec_off(int s) { return kDVecOff + s * 512; }
+};
 
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(384, 1)
@@ -279,10 +318,29 @@ __global__ void __launch_bounds__(384, 1)
                        const __grid_constant__ CUtensorMap tmDK, const __grid_constant__ CUtensorMap tmDV,
                        const float* __restrict__ lse, const float* __restrict__ Dg, int N, int n_tiles,
                        int BH, int band, float scale, float scale_log2) {
-  using C = BwdCfg<D>;
+  using C = DkdvCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const BwdBars bb = bwd_bars<D>(smem);
+  if (static_cast<uint32_t>(smem - smem_raw) + C::kLayoutBytes > C::kSmemBytes) {
+    // the aligned layout does not fit this launch's shared memory: report, touch nothing
+    if (threadIdx.x == 0) atomicCAS(&g_status_bwd, 0u, kSiteDkdv | 0xFFu);
+    return;
+  }
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+  uint64_t* res_full = bars;
+  uint64_t* q_full = bars + 1;
+  uint64_t* q_empty = q_full + C::kQStages;
+  uint64_t* do_full = q_empty + C::kQStages;
+  uint64_t* do_empty = do_full + C::kDOStages;
+  uint64_t* s_full = do_empty + C::kDOStages;
+  uint64_t* dp_full = s_full + 1;
+  uint64_t* p_full = dp_full + 1;
+  uint64_t* ds_full = p_full + 1;
+  uint64_t* acc_done = ds_full + 1;
+  uint64_t* drain = acc_done + 1;
+  uint64_t* staged = drain + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kMiscOff + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   int bh, kt;   // key tile; causal: small kt is heavy, so rank 0 -> kt 0
@@ -291,96 +349,139 @@ __global__ void __launch_bounds__(384, 1)
   const int cnt = n_tiles - i0;                                 // query tiles visited (>= 1)
   const size_t row_base = static_cast<size_t>(bh) * N;
 
-  if (threadIdx.x == 0) bwd_init<D>(bb, 128);
+  if (threadIdx.x == 0) {
+    mbar_init(res_full, 1);
+    for (int i = 0; i < C::kQStages; ++i) {
+      mbar_init(&q_full[i], 2);     // TMA bytes + the producer warp's -lse writes
+      mbar_init(&q_empty[i], 1);
+    }
+    for (int i = 0; i < C::kDOStages; ++i) {
+      mbar_init(&do_full[i], 2);    // TMA bytes + the producer warp's -D writes
+      mbar_init(&do_empty[i], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(dp_full, 1);
+    mbar_init(p_full, 256);
+    mbar_init(ds_full, 256);
+    mbar_init(acc_done, 1);
+    mbar_init(drain, 1);
+    mbar_init(&staged[0], 128);
+    mbar_init(&staged[1], 128);
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
   if (warp == 9) {
-    tmem_alloc(bb.tmem_holder, 512);
+    tmem_alloc(tmem_holder, 512);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *bb.tmem_holder;
-  const CtaGuard g{bb.abort_flag, &g_status_bwd};
+  const uint32_t tmem = *tmem_holder;
+  const CtaGuard g{abort_flag, &g_status_bwd};
   const uint32_t sbase = smem_u32(smem);
 
   if (warp >= 8) {
-    if (warp == 8) {  // producer
+    if (warp == 8) {  // producer: K_j, V_j once; Q_i and dO_i (+ row vectors) per query tile
       if (lane == 0) {
-        mbar_arrive_expect_tx(bb.res_full, 2 * C::kTileBytes);
+        mbar_arrive_expect_tx(res_full, 2 * C::kTileBytes);
         for (int b = 0; b < C::kBoxes; ++b) {
-          tma_load_3d(smem + C::kResOff + b * C::kBoxBytes, &tmK, bb.res_full, 64 * b, 128 * kt, bh);
-          tma_load_3d(smem + C::kResOff + C::kTileBytes + b * C::kBoxBytes, &tmV, bb.res_full, 64 * b, 128 * kt,
-                      bh);
+          tma_load_3d(smem + C::kKOff + b * C::kBoxBytes, &tmK, res_full, 64 * b, 128 * kt, bh);
+          tma_load_3d(smem + C::kVOff + b * C::kBoxBytes, &tmV, res_full, 64 * b, 128 * kt, bh);
         }
       }
+      RowVecs rv = fetch_row_vectors(lse, Dg, row_base, 128 * i0, N, lane);
       for (int it = 0; it < cnt; ++it) {
-        const int st = it % C::kStages;
-        const uint32_t ph = (it / C::kStages) & 1;
-        int ok = 1;
-        if (lane == 0) ok = mbar_wait(&bb.empty[st], ph ^ 1u, g, kSiteDkdv | 1u);
-        if (!__shfl_sync(0xffffffffu, ok, 0)) break;   // the whole warp follows lane 0
         const int qt = i0 + it;
+        const int qs = it % C::kQStages, ds = it % C::kDOStages;
+        int ok = 1;
+        if (lane == 0) ok = mbar_wait(&q_empty[qs], ((it / C::kQStages) & 1u) ^ 1u, g, kSiteDkdv | 1u);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;   // the whole warp follows lane 0
         if (lane == 0) {
-          mbar_arrive_expect_tx(&bb.full[st], 2 * C::kTileBytes);
-          for (int b = 0; b < C::kBoxes; ++b) {
-            tma_load_3d(smem + C::x_off(st) + b * C::kBoxBytes, &tmQ, &bb.full[st], 64 * b, 128 * qt, bh);
-            tma_load_3d(smem + C::y_off(st) + b * C::kBoxBytes, &tmDO, &bb.full[st], 64 * b, 128 * qt, bh);
-          }
+          mbar_arrive_expect_tx(&q_full[qs], C::kTileBytes);
+          for (int b = 0; b < C::kBoxes; ++b)
+            tma_load_3d(smem + C::q_off(qs) + b * C::kBoxBytes, &tmQ, &q_full[qs], 64 * b, 128 * qt, bh);
         }
-        float* vec = reinterpret_cast<float*>(smem + C::vec_off(st));
-        load_row_vectors(vec, vec + 128, lse, Dg, row_base, 128 * qt, N, lane);
+        float* nl = reinterpret_cast<float*>(smem + C::lse_off(qs));
+#pragma unroll
+        for (int k = 0; k < 4; ++k) nl[lane + 32 * k] = rv.a[k];
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bb.full[st]);
-      }
-    } else if (warp == 9) {  // MMA issuer
-      if (lane == 0) {
-        const uint32_t tS = tmem + C::kColS, tDP = tmem + C::kColDP;
-        const uint32_t tDV = tmem + C::kColAcc0, tDK = tmem + C::kColAcc1;
-        const uint64_t kK = kmaj<D>(sbase + C::kResOff), kV = kmaj<D>(sbase + C::kResOff + C::kTileBytes);
-        // stage st: Q and dO as K-major B operands (S^T, dP^T) and as MN-major
-        // B operands (dK, dV); stages are kStageBytes apart
-        const uint64_t kQ0 = kmaj<D>(sbase + C::x_off(0)), kDO0 = kmaj<D>(sbase + C::y_off(0));
-        const uint64_t mQ0 = mnmaj<D>(sbase + C::x_off(0)), mDO0 = mnmaj<D>(sbase + C::y_off(0));
-        auto stg = [](int st) { return static_cast<uint64_t>(st) * (C::kStageBytes >> 4); };
-        auto kQ = [&](int st) { return kQ0 + stg(st); };
-        auto kDO = [&](int st) { return kDO0 + stg(st); };
-        auto mQ = [&](int st) { return mQ0 + stg(st); };
-        auto mDO = [&](int st) { return mDO0 + stg(st); };
-        bool ok = mbar_wait(bb.res_full, 0, g, kSiteDkdv | 2u) && mbar_wait(&bb.full[0], 0, g, kSiteDkdv | 3u);
-        if (ok) {
-          mma_nt<D>(tS, kK, kQ(0));
-          tc_commit(bb.s_full);
-          mma_nt<D>(tDP, kV, kDO(0));
-          tc_commit(bb.dp_full);
+        if (lane == 0) mbar_arrive(&q_full[qs]);
+        if (lane == 0) ok = mbar_wait(&do_empty[ds], ((it / C::kDOStages) & 1u) ^ 1u, g, kSiteDkdv | 12u);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&do_full[ds], C::kTileBytes);
+          for (int b = 0; b < C::kBoxes; ++b)
+            tma_load_3d(smem + C::do_off(ds) + b * C::kBoxBytes, &tmDO, &do_full[ds], 64 * b, 128 * qt, bh);
         }
-        for (int it = 0; ok && it < cnt; ++it) {
-          const int st = it % C::kStages;
-          const uint32_t par = it & 1;
-          const bool next = it + 1 < cnt;
-          const int st1 = (it + 1) % C::kStages;
-          if (!(ok = mbar_wait(bb.p_full, par, g, kSiteDkdv | 4u))) break;
-          tc_fence_after();
-          mma_tn_acc<D>(tDV, tS, mDO(st), it > 0);          // dV += P^T dO_i
-          if (next) {
-            // with two stages the next query tile is still loading when dV(i) can
-            // start, so it is awaited only here
-            if (!(ok = mbar_wait(&bb.full[st1], ((it + 1) / C::kStages) & 1, g, kSiteDkdv | 5u))) break;
-            mma_nt<D>(tS, kK, kQ(st1));                     // S^T(i+1)
-            tc_commit(bb.s_full);
-          }
-          if (!(ok = mbar_wait(bb.ds_full, par, g, kSiteDkdv | 6u))) break;
-          tc_fence_after();
-          mma_tn_acc<D>(tDK, tDP, mQ(st), it > 0);          // dK += dS^T Q_i
-          tc_commit(&bb.empty[st]);
-          if (next) {
-            mma_nt<D>(tDP, kV, kDO(st1));                   // dP^T(i+1)
-            tc_commit(bb.dp_full);
+        float* nd = reinterpret_cast<float*>(smem + C::dvec_off(ds));
+#pragma unroll
+        for (int k = 0; k < 4; ++k) nd[lane + 32 * k] = rv.d[k];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&do_full[ds]);
+        if (it + 1 < cnt) rv = fetch_row_vectors(lse, Dg, row_base, 128 * (qt + 1), N, lane);
+      }
+    } else if (warp == 9) {  // MMA issuer: the whole warp runs the loop, one lane issues
+      const uint32_t tS = tmem + C::kColS, tDP = tmem + C::kColDP;
+      const uint32_t tDV = tmem + C::kColDV, tDK = tmem + C::kColDK;
+      const uint64_t kK = kmaj<D>(sbase + C::kKOff), kV = kmaj<D>(sbase + C::kVOff);
+      // Q and dO stages as K-major B operands (S^T, dP^T) and MN-major B operands (dK, dV)
+      auto kQ = [&](int s) { return kmaj<D>(sbase + C::q_off(s)); };
+      auto mQ = [&](int s) { return mnmaj<D>(sbase + C::q_off(s)); };
+      auto kDO = [&](int s) { return kmaj<D>(sbase + C::do_off(s)); };
+      auto mDO = [&](int s) { return mnmaj<D>(sbase + C::do_off(s)); };
+      bool ok = mbar_wait_w(res_full, 0, g, kSiteDkdv | 2u) && mbar_wait_w(&q_full[0], 0, g, kSiteDkdv | 3u);
+      if (ok) {
+        mma_nt<D>(tS, kK, kQ(0));
+        tc_commit_w(s_full);
+        ok = mbar_wait_w(&do_full[0], 0, g, kSiteDkdv | 3u);
+      }
+      if (ok) {
+        mma_nt<D>(tDP, kV, kDO(0));
+        tc_commit_w(dp_full);
+      }
+      for (int it = 0; ok && it < cnt; ++it) {
+        const int qs = it % C::kQStages, ds = it % C::kDOStages;
+        const int qs1 = (it + 1) % C::kQStages, ds1 = (it + 1) % C::kDOStages;
+        const uint32_t par = it & 1;
+        const bool next = it + 1 < cnt;
+        if (!(ok = mbar_wait_w(p_full, par, g, kSiteDkdv | 4u))) break;
+        tc_fence_after();
+        mma_tn_acc<D>(tDV, tS, mDO(ds), it > 0);          // dV += P^T dO_i
+        bool s_done = !next, k_done = false;
+        const uint32_t qph1 = ((it + 1) / C::kQStages) & 1u;
+        while (ok && !(s_done && k_done)) {
+          int which;
+          if (!s_done && !k_done)
+            which = mbar_wait_either_w(&q_full[qs1], qph1, ds_full, par, g, kSiteDkdv | 5u);
+          else if (!s_done)
+            which = mbar_wait_w(&q_full[qs1], qph1, g, kSiteDkdv | 5u) ? 0 : -1;
+          else
+            which = mbar_wait_w(ds_full, par, g, kSiteDkdv | 6u) ? 1 : -1;
+          if (which < 0) {
+            ok = false;
+          } else if (which == 0) {
+            mma_nt<D>(tS, kK, kQ(qs1));                     // S^T(i+1)
+            tc_commit_w(s_full);
+            s_done = true;
+          } else {
+            tc_fence_after();
+            mma_tn_acc<D>(tDK, tDP, mQ(qs), it > 0);        // dK += dS^T Q_i
+            tc_commit_w(&q_empty[qs]);                     // Q_i, -lse_i: last reader done
+            tc_commit_w(&do_empty[ds]);                    // dO_i (dP^T, dV), -D_i (read before dS)
+            k_done = true;
           }
         }
-        if (ok) tc_commit(bb.acc_done);
-        tc_commit(bb.drain);
-        mbar_drain(bb.drain, 0);
+        if (!ok) break;
+        if (next) {
+          if (!(ok = mbar_wait_w(&do_full[ds1], ((it + 1) / C::kDOStages) & 1u, g, kSiteDkdv | 13u))) break;
+          mma_nt<D>(tDP, kV, kDO(ds1));                     // dP^T(i+1), after dK(i) has read dS^T(i)
+          tc_commit_w(dp_full);
+        }
       }
+      if (ok) tc_commit_w(acc_done);
+      tc_commit_w(drain);
+      mbar_drain(drain, 0);
       __syncwarp();
       tc_fence_before();
       named_bar_sync(1, 288);
@@ -396,16 +497,15 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
   const uint32_t tS = tmem + lane_base + C::kColS + 64 * h;
   const uint32_t tDP = tmem + lane_base + C::kColDP + 64 * h;
+  const float2 sc2 = make_float2(scale_log2, scale_log2);
   bool ok = true;
   for (int it = 0; ok && it < cnt; ++it) {
-    const int st = it % C::kStages;
+    const int qs = it % C::kQStages, ds = it % C::kDOStages;
     const uint32_t par = it & 1;
     const int qt = i0 + it;
-    const float* nlse2 = reinterpret_cast<const float*>(smem + C::vec_off(st)) + 64 * h;
-    const float* dv = nlse2 + 128;   // -D
-    // the row vectors were written by the producer before it arrived on full[st]
-    if (!(ok = mbar_wait(&bb.full[st], (it / C::kStages) & 1, g, kSiteDkdv | 7u))) break;
-    if (!(ok = mbar_wait(bb.s_full, par, g, kSiteDkdv | 8u))) break;
+    // -lse arrived with Q_i (q_full), -D with dO_i (do_full)
+    if (!(ok = mbar_wait(&q_full[qs], (it / C::kQStages) & 1u, g, kSiteDkdv | 7u))) break;
+    if (!(ok = mbar_wait(s_full, par, g, kSiteDkdv | 8u))) break;
     __syncwarp();
     tc_fence_after();
     uint32_t sr[2][32];
@@ -414,19 +514,23 @@ __global__ void __launch_bounds__(384, 1)
     tmem_ld_wait(sr[0]);
     tmem_ld_fence(sr[1]);
     float p[64];
-    const float4* lse4 = reinterpret_cast<const float4*>(nlse2);   // holds -lse * log2(e)
-    const float2 sc2 = make_float2(scale_log2, scale_log2);
+    const uint32_t lse_addr = sbase + C::lse_off(qs) + 256 * h;   // -lse * log2(e) of this half's columns
 #pragma unroll
-    for (int c4 = 0; c4 < 16; ++c4) {  // one 16-byte broadcast load per four columns
-      const float4 l4 = lse4[c4];
+    for (int b8 = 0; b8 < 2; ++b8) {   // 32 columns at a time: their loads go out before the math
+      float4 l4[8];
 #pragma unroll
-      for (int e = 0; e < 4; e += 2) {
-        const int c = 4 * c4 + e;
-        const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[c / 32][c % 32]),
-                                                __uint_as_float(sr[(c + 1) / 32][(c + 1) % 32])),
-                                    sc2, e ? make_float2(l4.z, l4.w) : make_float2(l4.x, l4.y));
-        p[c] = ex2_approx(x.x);
-        p[c + 1] = ex2_approx(x.y);
+      for (int i = 0; i < 8; ++i) l4[i] = ld_shared_f4(lse_addr + (8 * b8 + i) * 16);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+#pragma unroll
+        for (int e = 0; e < 4; e += 2) {
+          const int c = 32 * b8 + 4 * i + e;
+          const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[c / 32][c % 32]),
+                                                  __uint_as_float(sr[(c + 1) / 32][(c + 1) % 32])),
+                                      sc2, e ? make_float2(l4[i].z, l4[i].w) : make_float2(l4[i].x, l4[i].y));
+          p[c] = ex2_approx(x.x);
+          p[c + 1] = ex2_approx(x.y);
+        }
       }
     }
     if (CAUSAL && qt == kt) {
@@ -437,14 +541,13 @@ __global__ void __launch_bounds__(384, 1)
         if (c < lim) p[c] = 0.f;
     }
 #pragma unroll
-    for (int c = 0; c < 64; c += 32) {
-      st_bf16_16cols(tS + c / 2, p + c);
-    }
+    for (int c = 0; c < 64; c += 32) st_bf16_16cols(tS + c / 2, p + c);
     tmem_st_wait();
     tc_fence_before();
-    mbar_arrive(bb.p_full);
+    mbar_arrive(p_full);
 
-    if (!(ok = mbar_wait(bb.dp_full, par, g, kSiteDkdv | 9u))) break;
+    if (!(ok = mbar_wait(&do_full[ds], (it / C::kDOStages) & 1u, g, kSiteDkdv | 14u))) break;
+    if (!(ok = mbar_wait(dp_full, par, g, kSiteDkdv | 9u))) break;
     __syncwarp();
     tc_fence_after();
     uint32_t dr[2][32];
@@ -452,34 +555,39 @@ __global__ void __launch_bounds__(384, 1)
     tmem_ld32(tDP + 32, dr[1]);
     tmem_ld_wait(dr[0]);
     tmem_ld_fence(dr[1]);
-    const float4* dv4 = reinterpret_cast<const float4*>(dv);   // holds -D
+    const uint32_t d_addr = sbase + C::dvec_off(ds) + 256 * h;   // -D of this half's columns
 #pragma unroll
-    for (int c4 = 0; c4 < 16; ++c4) {
-      const float4 d4 = dv4[c4];
+    for (int b8 = 0; b8 < 2; ++b8) {
+      float4 d4[8];
 #pragma unroll
-      for (int e = 0; e < 4; e += 2) {
-        const int c = 4 * c4 + e;
-        const float2 dp = __fadd2_rn(make_float2(__uint_as_float(dr[c / 32][c % 32]),
-                                                 __uint_as_float(dr[(c + 1) / 32][(c + 1) % 32])),
-                                     e ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y));
-        const float2 ds = __fmul2_rn(make_float2(p[c], p[c + 1]), dp);
-        p[c] = ds.x;
-        p[c + 1] = ds.y;
+      for (int i = 0; i < 8; ++i) d4[i] = ld_shared_f4(d_addr + (8 * b8 + i) * 16);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+#pragma unroll
+        for (int e = 0; e < 4; e += 2) {
+          const int c = 32 * b8 + 4 * i + e;
+          const float2 dp = __fadd2_rn(make_float2(__uint_as_float(dr[c / 32][c % 32]),
+                                                   __uint_as_float(dr[(c + 1) / 32][(c + 1) % 32])),
+                                       e ? make_float2(d4[i].z, d4[i].w) : make_float2(d4[i].x, d4[i].y));
+          const float2 dsv = __fmul2_rn(make_float2(p[c], p[c + 1]), dp);
+          p[c] = dsv.x;
+          p[c + 1] = dsv.y;
+        }
       }
     }
 #pragma unroll
     for (int c = 0; c < 64; c += 32) st_bf16_16cols(tDP + c / 2, p + c);
     tmem_st_wait();
     tc_fence_before();
-    mbar_arrive(bb.ds_full);
+    mbar_arrive(ds_full);
   }
-  if (ok && mbar_wait(bb.acc_done, 0, g, kSiteDkdv | 10u)) {
+  if (ok && mbar_wait(acc_done, 0, g, kSiteDkdv | 10u)) {
     __syncwarp();
     tc_fence_after();
-    // warpgroup 0 writes dV (staged in stage 0's X tile), warpgroup 1 writes dK (stage 0's Y tile)
-    const uint32_t tacc = tmem + lane_base + (h ? C::kColAcc1 : C::kColAcc0);
-    uint8_t* stage = smem + (h ? C::y_off(0) : C::x_off(0));
-    bwd_store_acc<D>(tacc, stage, 0, D, h ? scale : 1.f, t, &bb.staged[h], t == 0, h ? &tmDK : &tmDV, 128 * kt,
+    // warpgroup 0 writes dV (staged in Q stage 0), warpgroup 1 writes dK (staged in Q stage 1)
+    const uint32_t tacc = tmem + lane_base + (h ? C::kColDK : C::kColDV);
+    uint8_t* stage = smem + C::q_off(h);
+    bwd_store_acc<D>(tacc, stage, 0, D, h ? scale : 1.f, t, &staged[h], t == 0, h ? &tmDK : &tmDV, 128 * kt,
                      bh, g, kSiteDkdv | 11u);
   }
   __syncwarp();
@@ -548,8 +656,8 @@ __global__ void __launch_bounds__(384, 1)
           mbar_arrive(&bb.full[st]);  // no row vectors here: second arrival of the two expected
         }
       }
-    } else if (warp == 9) {  // MMA issuer
-      if (lane == 0) {
+    } else if (warp == 9) {  // MMA issuer: the whole warp runs the loop, one lane issues
+      {
         const uint32_t tS = tmem + C::kColS, tDP = tmem + C::kColDP, tDQ = tmem + C::kColAcc0;
         const uint64_t kQ = kmaj<D>(sbase + C::kResOff), kDO = kmaj<D>(sbase + C::kResOff + C::kTileBytes);
         // stage st: K, V as K-major B operands (S, dP) and K as the MN-major B
@@ -560,12 +668,12 @@ __global__ void __launch_bounds__(384, 1)
         auto kK = [&](int st) { return kK0 + stg(st); };
         auto kV = [&](int st) { return kV0 + stg(st); };
         auto mK = [&](int st) { return mK0 + stg(st); };
-        bool ok = mbar_wait(bb.res_full, 0, g, kSiteDq | 2u) && mbar_wait(&bb.full[0], 0, g, kSiteDq | 3u);
+        bool ok = mbar_wait_w(bb.res_full, 0, g, kSiteDq | 2u) && mbar_wait_w(&bb.full[0], 0, g, kSiteDq | 3u);
         if (ok) {
           mma_nt<D>(tS, kQ, kK(0));
-          tc_commit(bb.s_full);
+          tc_commit_w(bb.s_full);
           mma_nt<D>(tDP, kDO, kV(0));
-          tc_commit(bb.dp_full);
+          tc_commit_w(bb.dp_full);
         }
         for (int it = 0; ok && it < cnt; ++it) {
           const int st = it % C::kStages;
@@ -573,23 +681,23 @@ __global__ void __launch_bounds__(384, 1)
           const bool next = it + 1 < cnt;
           const int st1 = (it + 1) % C::kStages;
           if (next) {
-            if (!(ok = mbar_wait(&bb.full[st1], ((it + 1) / C::kStages) & 1, g, kSiteDq | 4u))) break;
-            if (!(ok = mbar_wait(bb.s_free, par, g, kSiteDq | 5u))) break;
+            if (!(ok = mbar_wait_w(&bb.full[st1], ((it + 1) / C::kStages) & 1, g, kSiteDq | 4u))) break;
+            if (!(ok = mbar_wait_w(bb.s_free, par, g, kSiteDq | 5u))) break;
             tc_fence_after();
             mma_nt<D>(tS, kQ, kK(st1));                 // S(j+1)
-            tc_commit(bb.s_full);
+            tc_commit_w(bb.s_full);
           }
-          if (!(ok = mbar_wait(bb.ds_full, par, g, kSiteDq | 6u))) break;
+          if (!(ok = mbar_wait_w(bb.ds_full, par, g, kSiteDq | 6u))) break;
           tc_fence_after();
           mma_tn_acc<D>(tDQ, tDP, mK(st), it > 0);     // dQ += dS K_j
-          tc_commit(&bb.empty[st]);
+          tc_commit_w(&bb.empty[st]);
           if (next) {
             mma_nt<D>(tDP, kDO, kV(st1));               // dP(j+1)
-            tc_commit(bb.dp_full);
+            tc_commit_w(bb.dp_full);
           }
         }
-        if (ok) tc_commit(bb.acc_done);
-        tc_commit(bb.drain);
+        if (ok) tc_commit_w(bb.acc_done);
+        tc_commit_w(bb.drain);
         mbar_drain(bb.drain, 0);
       }
       __syncwarp();
@@ -685,7 +793,7 @@ template <int D, bool CAUSAL>
 cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv, const float* lse,
                           const float* Dvec, const Shape& s, cudaStream_t st) {
-  using C = BwdCfg<D>;
+  using C = DkdvCfg<D>;
   auto kern = fa_bwd_dkdv_kernel<D, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;

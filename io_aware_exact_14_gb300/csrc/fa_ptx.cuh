@@ -222,6 +222,72 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
       : "memory");
 }
 
+// Warp-converged forms: all 32 lanes execute the instruction with the same
+// (warp-uniform) operands and one elected lane issues it.  Keeping the whole
+// MMA warp converged lets the compiler hold descriptors and TMEM addresses in
+// uniform registers, which is what the tensor-core instructions read.
+__device__ __forceinline__ void tc_mma_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_commit_w(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+// Bounded wait by a whole warp; every lane returns lane 0's verdict.
+__device__ __forceinline__ bool mbar_wait_w(uint64_t* bar, uint32_t parity, const CtaGuard& g, uint32_t site) {
+  const bool ok = mbar_wait(bar, parity, g, site);
+  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
+// Bounded wait, by a whole warp, for whichever of two barrier phases completes
+// first: 0 for `a`, 1 for `b`, -1 if the CTA is aborting or the limit passed.
+__device__ __forceinline__ int mbar_wait_either_w(uint64_t* a, uint32_t pa, uint64_t* b, uint32_t pb,
+                                                  const CtaGuard& g, uint32_t site) {
+  int which = -1;
+  if ((threadIdx.x & 31) == 0) {
+    const unsigned long long t0 = global_ns();
+    for (uint32_t it = 1;; ++it) {
+      if (mbar_try_wait(a, pa)) { which = 0; break; }
+      if (mbar_try_wait(b, pb)) { which = 1; break; }
+      if ((it & 63u) == 0u) {
+        if (*g.abort_flag || *reinterpret_cast<volatile unsigned int*>(g.status) != 0u) {
+          *g.abort_flag = 1u;
+          break;
+        }
+        if (global_ns() - t0 > kWaitLimitNs) {
+          guard_fail(g, site);
+          break;
+        }
+      }
+    }
+  }
+  return __shfl_sync(0xffffffffu, which, 0);
+}
+
 // Instruction descriptor for kind::f16 with bf16 A/B and fp32 D.
 //   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format,
 //   15 A major (1 = MN), 16 B major (1 = MN), 17-22 N>>3, 24-28 M>>4.
@@ -338,6 +404,13 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// 16-byte shared-memory load (not volatile: the compiler may hoist it).
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
+  float4 v;
+  asm("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+  return v;
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {

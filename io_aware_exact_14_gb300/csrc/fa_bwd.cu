@@ -96,77 +96,16 @@ __global__ void __launch_bounds__(kPreThreads) fa_bwd_preprocess_kernel(const ui
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Tile geometry shared by both kernels: a 128-row tile of d bf16 columns is
+// d/64 swizzled boxes of 128 rows x 128 bytes.
 template <int D>
 struct BwdCfg {
   static_assert(D == 64 || D == 128, "head dim");
   static constexpr int kBoxes = D / 64;
   static constexpr uint32_t kBoxBytes = 128u * 128u;
   static constexpr uint32_t kTileBytes = kBoxes * kBoxBytes;
-  static constexpr int kStages = 2;
-  // resident tiles R0, R1; each stage: tiles X, Y and two fp32[128] vectors
-  static constexpr uint32_t kResOff = 0;
-  static constexpr uint32_t kStageOff = 2 * kTileBytes;
-  static constexpr uint32_t kStageBytes = 2 * kTileBytes + 1024;
-  static constexpr uint32_t kBarOff = kStageOff + kStages * kStageBytes;
-  // res_full, full[S], empty[S], s_full, s_free, dp_full, p_full, ds_full, acc_done, drain, staged[2]
-  static constexpr int kBars = 1 + 2 * kStages + 10;
-  static constexpr uint32_t kMiscOff = kBarOff + kBars * 8;
-  static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;
-  static constexpr int kThreads = 384;
-  static constexpr uint32_t kColS = 0, kColDP = 128, kColAcc0 = 256;
-  __host__ __device__ static constexpr uint32_t x_off(int st) { return kStageOff + st * kStageBytes; }
-  __host__ __device__ static constexpr uint32_t y_off(int st) { return x_off(st) + kTileBytes; }
-  __host__ __device__ static constexpr uint32_t vec_off(int st) { return x_off(st) + 2 * kTileBytes; }
+  static constexpr uint32_t kMaxSmem = 232448;   // per-CTA opt-in limit
 };
-
-struct BwdBars {
-  uint64_t *res_full, *full, *empty, *s_full, *s_free, *dp_full, *p_full, *ds_full, *acc_done, *drain, *staged;
-  uint32_t* tmem_holder;
-  volatile uint32_t* abort_flag;
-};
-
-template <int D>
-__device__ __forceinline__ BwdBars bwd_bars(uint8_t* smem) {
-  using C = BwdCfg<D>;
-  uint64_t* b = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
-  BwdBars r;
-  r.res_full = b;
-  r.full = b + 1;
-  r.empty = b + 1 + C::kStages;
-  uint64_t* m = b + 1 + 2 * C::kStages;
-  r.s_full = m;
-  r.s_free = m + 1;
-  r.dp_full = m + 2;
-  r.p_full = m + 3;
-  r.ds_full = m + 4;
-  r.acc_done = m + 5;
-  r.drain = m + 6;
-  r.staged = m + 7;  // two
-  r.tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
-  r.abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kMiscOff + 4);
-  return r;
-}
-
-template <int D>
-__device__ __forceinline__ void bwd_init(const BwdBars& b, uint32_t staged_count) {
-  using C = BwdCfg<D>;
-  mbar_init(b.res_full, 1);
-  for (int i = 0; i < C::kStages; ++i) {
-    mbar_init(&b.full[i], 2);   // TMA bytes + the producer warp's vector writes
-    mbar_init(&b.empty[i], 1);
-  }
-  mbar_init(b.s_full, 1);
-  mbar_init(b.s_free, 256);
-  mbar_init(b.dp_full, 1);
-  mbar_init(b.p_full, 256);
-  mbar_init(b.ds_full, 256);
-  mbar_init(b.acc_done, 1);
-  mbar_init(b.drain, 1);
-  mbar_init(&b.staged[0], staged_count);
-  mbar_init(&b.staged[1], staged_count);
-  *b.abort_flag = 0u;
-  fence_mbar_init();
-}
 
 // S-like product: D(128 x 128) = A(128 x d) * B(128 x d)^T, both K-major tiles.
 template <int D>
@@ -299,7 +238,7 @@ struct DkdvCfg {
   static constexpr int kBars = 1 + 2 * kQStages + 2 * kDOStages + 8;
   static constexpr uint32_t kMiscOff = kBarOff + kBars * 8;
   static constexpr uint32_t kLayoutBytes = kMiscOff + 16;
-  static constexpr uint32_t kMaxSmem = 232448;   // per-CTA opt-in limit
+  static constexpr uint32_t kMaxSmem = BwdCfg<D>::kMaxSmem;
   // room for the 1024-byte alignment of the base when it fits, else all there is
   static constexpr uint32_t kSmemBytes = kLayoutBytes + 1024 <= kMaxSmem ? kLayoutBytes + 1024 : kMaxSmem;
   static_assert(kLayoutBytes <= kMaxSmem, "dK/dV shared-memory layout too large");
@@ -599,10 +538,35 @@ __global__ void __launch_bounds__(384, 1)
 // dQ: one CTA per (b, h, 128-query tile i); loop over key tiles j.
 //   S = Q_i K_j^T, P = exp2(S * scale * log2e - lse2_row)
 //   dP = dO_i V_j^T, dS = P o (dP - D_row),  dQ_i += dS K_j,  finally dQ_i *= scale
+// Q_i and dO_i stay resident; K_j streams through a 3-deep ring (read by S(j)
+// and dQ(j)) and V_j through a 2-deep ring (read by dP(j) only), so a key tile
+// is loaded well before S(j+1) needs it.
 // MMA order S(j) dP(j) S(j+1) dQ(j) dP(j+1) ...: the exponentials of tile j run
 // under dP(j), the dS products under S(j+1).
-// TMEM: T0 = S, T1 = dP, acc0 = dQ.
+// TMEM: T0 = S, T1 = dP, acc = dQ.
 // ---------------------------------------------------------------------------
+
+template <int D>
+struct DqCfg {
+  static constexpr int kKStages = 3, kVStages = 2;
+  static constexpr uint32_t kTileBytes = BwdCfg<D>::kTileBytes;
+  static constexpr uint32_t kQOff = 0, kDOOff = kTileBytes;
+  static constexpr uint32_t kKOff = 2 * kTileBytes;
+  static constexpr uint32_t kVOff = kKOff + kKStages * kTileBytes;
+  static constexpr uint32_t kBarOff = kVOff + kVStages * kTileBytes;
+  // res_full, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full, s_free, dp_full, ds_full,
+  // acc_done, drain, staged
+  static constexpr int kBars = 1 + 2 * kKStages + 2 * kVStages + 7;
+  static constexpr uint32_t kMiscOff = kBarOff + kBars * 8;
+  static constexpr uint32_t kLayoutBytes = kMiscOff + 16;
+  static constexpr uint32_t kMaxSmem = BwdCfg<D>::kMaxSmem;
+  static constexpr uint32_t kSmemBytes = kLayoutBytes + 1024 <= kMaxSmem ? kLayoutBytes + 1024 : kMaxSmem;
+  static_assert(kLayoutBytes <= kMaxSmem, "dQ shared-memory layout too large");
+  static constexpr int kThreads = 384;
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColAcc = 256;
+  __host__ __device__ static constexpr uint32_t k_off(int s) { return kKOff + s * kTileBytes; }
+  __host__ __device__ static constexpr uint32_t v_off(int s) { return kVOff + s * kTileBytes; }
+};
 
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(384, 1)
@@ -611,10 +575,29 @@ __global__ void __launch_bounds__(384, 1)
                      const __grid_constant__ CUtensorMap tmDQ, const float* __restrict__ lse,
                      const float* __restrict__ Dg, int N, int n_tiles, int BH, int band, float scale,
                      float scale_log2) {
-  using C = BwdCfg<D>;
+  using C = DqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const BwdBars bb = bwd_bars<D>(smem);
+  if (static_cast<uint32_t>(smem - smem_raw) + C::kLayoutBytes > C::kSmemBytes) {
+    // the aligned layout does not fit this launch's shared memory: report, touch nothing
+    if (threadIdx.x == 0) atomicCAS(&g_status_bwd, 0u, kSiteDq | 0xFFu);
+    return;
+  }
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+  uint64_t* res_full = bars;
+  uint64_t* k_full = bars + 1;
+  uint64_t* k_empty = k_full + C::kKStages;
+  uint64_t* v_full = k_empty + C::kKStages;
+  uint64_t* v_empty = v_full + C::kVStages;
+  uint64_t* s_full = v_empty + C::kVStages;
+  uint64_t* s_free = s_full + 1;
+  uint64_t* dp_full = s_free + 1;
+  uint64_t* ds_full = dp_full + 1;
+  uint64_t* acc_done = ds_full + 1;
+  uint64_t* drain = acc_done + 1;
+  uint64_t* staged = drain + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kMiscOff + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   int bh, rank;
@@ -623,83 +606,101 @@ __global__ void __launch_bounds__(384, 1)
   const int cnt = CAUSAL ? qt + 1 : n_tiles;                             // key tiles visited
   const size_t row_base = static_cast<size_t>(bh) * N;
 
-  if (threadIdx.x == 0) bwd_init<D>(bb, 256);
+  if (threadIdx.x == 0) {
+    mbar_init(res_full, 1);
+    for (int i = 0; i < C::kKStages; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+    }
+    for (int i = 0; i < C::kVStages; ++i) {
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(s_free, 256);
+    mbar_init(dp_full, 1);
+    mbar_init(ds_full, 256);
+    mbar_init(acc_done, 1);
+    mbar_init(drain, 1);
+    mbar_init(staged, 256);
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
   if (warp == 9) {
-    tmem_alloc(bb.tmem_holder, 512);
+    tmem_alloc(tmem_holder, 512);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *bb.tmem_holder;
-  const CtaGuard g{bb.abort_flag, &g_status_bwd};
+  const uint32_t tmem = *tmem_holder;
+  const CtaGuard g{abort_flag, &g_status_bwd};
   const uint32_t sbase = smem_u32(smem);
 
   if (warp >= 8) {
-    if (warp == 8) {  // producer: Q_i, dO_i once; K_j, V_j per stage
+    if (warp == 8) {  // producer: Q_i, dO_i once; K_j and V_j through their rings
       if (lane == 0) {
-        mbar_arrive_expect_tx(bb.res_full, 2 * C::kTileBytes);
-        for (int b = 0; b < C::kBoxes; ++b) {
-          tma_load_3d(smem + C::kResOff + b * C::kBoxBytes, &tmQ, bb.res_full, 64 * b, 128 * qt, bh);
-          tma_load_3d(smem + C::kResOff + C::kTileBytes + b * C::kBoxBytes, &tmDO, bb.res_full, 64 * b,
-                      128 * qt, bh);
+        mbar_arrive_expect_tx(res_full, 2 * C::kTileBytes);
+        for (int b = 0; b < BwdCfg<D>::kBoxes; ++b) {
+          tma_load_3d(smem + C::kQOff + b * BwdCfg<D>::kBoxBytes, &tmQ, res_full, 64 * b, 128 * qt, bh);
+          tma_load_3d(smem + C::kDOOff + b * BwdCfg<D>::kBoxBytes, &tmDO, res_full, 64 * b, 128 * qt, bh);
         }
         for (int it = 0; it < cnt; ++it) {
-          const int st = it % C::kStages;
-          const uint32_t ph = (it / C::kStages) & 1;
-          if (!mbar_wait(&bb.empty[st], ph ^ 1u, g, kSiteDq | 1u)) break;
-          mbar_arrive_expect_tx(&bb.full[st], 2 * C::kTileBytes);
-          for (int b = 0; b < C::kBoxes; ++b) {
-            tma_load_3d(smem + C::x_off(st) + b * C::kBoxBytes, &tmK, &bb.full[st], 64 * b, 128 * it, bh);
-            tma_load_3d(smem + C::y_off(st) + b * C::kBoxBytes, &tmV, &bb.full[st], 64 * b, 128 * it, bh);
-          }
-          mbar_arrive(&bb.full[st]);  // no row vectors here: second arrival of the two expected
+          const int ks = it % C::kKStages, vs = it % C::kVStages;
+          if (!mbar_wait(&k_empty[ks], ((it / C::kKStages) & 1u) ^ 1u, g, kSiteDq | 1u)) break;
+          mbar_arrive_expect_tx(&k_full[ks], C::kTileBytes);
+          for (int b = 0; b < BwdCfg<D>::kBoxes; ++b)
+            tma_load_3d(smem + C::k_off(ks) + b * BwdCfg<D>::kBoxBytes, &tmK, &k_full[ks], 64 * b, 128 * it, bh);
+          if (!mbar_wait(&v_empty[vs], ((it / C::kVStages) & 1u) ^ 1u, g, kSiteDq | 11u)) break;
+          mbar_arrive_expect_tx(&v_full[vs], C::kTileBytes);
+          for (int b = 0; b < BwdCfg<D>::kBoxes; ++b)
+            tma_load_3d(smem + C::v_off(vs) + b * BwdCfg<D>::kBoxBytes, &tmV, &v_full[vs], 64 * b, 128 * it, bh);
         }
       }
     } else if (warp == 9) {  // MMA issuer: the whole warp runs the loop, one lane issues
-      {
-        const uint32_t tS = tmem + C::kColS, tDP = tmem + C::kColDP, tDQ = tmem + C::kColAcc0;
-        const uint64_t kQ = kmaj<D>(sbase + C::kResOff), kDO = kmaj<D>(sbase + C::kResOff + C::kTileBytes);
-        // stage st: K, V as K-major B operands (S, dP) and K as the MN-major B
-        // operand of dQ; stages are kStageBytes apart
-        const uint64_t kK0 = kmaj<D>(sbase + C::x_off(0)), kV0 = kmaj<D>(sbase + C::y_off(0));
-        const uint64_t mK0 = mnmaj<D>(sbase + C::x_off(0));
-        auto stg = [](int st) { return static_cast<uint64_t>(st) * (C::kStageBytes >> 4); };
-        auto kK = [&](int st) { return kK0 + stg(st); };
-        auto kV = [&](int st) { return kV0 + stg(st); };
-        auto mK = [&](int st) { return mK0 + stg(st); };
-        bool ok = mbar_wait_w(bb.res_full, 0, g, kSiteDq | 2u) && mbar_wait_w(&bb.full[0], 0, g, kSiteDq | 3u);
-        if (ok) {
-          mma_nt<D>(tS, kQ, kK(0));
-          tc_commit_w(bb.s_full);
-          mma_nt<D>(tDP, kDO, kV(0));
-          tc_commit_w(bb.dp_full);
-        }
-        for (int it = 0; ok && it < cnt; ++it) {
-          const int st = it % C::kStages;
-          const uint32_t par = it & 1;
-          const bool next = it + 1 < cnt;
-          const int st1 = (it + 1) % C::kStages;
-          if (next) {
-            if (!(ok = mbar_wait_w(&bb.full[st1], ((it + 1) / C::kStages) & 1, g, kSiteDq | 4u))) break;
-            if (!(ok = mbar_wait_w(bb.s_free, par, g, kSiteDq | 5u))) break;
-            tc_fence_after();
-            mma_nt<D>(tS, kQ, kK(st1));                 // S(j+1)
-            tc_commit_w(bb.s_full);
-          }
-          if (!(ok = mbar_wait_w(bb.ds_full, par, g, kSiteDq | 6u))) break;
-          tc_fence_after();
-          mma_tn_acc<D>(tDQ, tDP, mK(st), it > 0);     // dQ += dS K_j
-          tc_commit_w(&bb.empty[st]);
-          if (next) {
-            mma_nt<D>(tDP, kDO, kV(st1));               // dP(j+1)
-            tc_commit_w(bb.dp_full);
-          }
-        }
-        if (ok) tc_commit_w(bb.acc_done);
-        tc_commit_w(bb.drain);
-        mbar_drain(bb.drain, 0);
+      const uint32_t tS = tmem + C::kColS, tDP = tmem + C::kColDP, tDQ = tmem + C::kColAcc;
+      const uint64_t kQ = kmaj<D>(sbase + C::kQOff), kDO = kmaj<D>(sbase + C::kDOOff);
+      // K stages as K-major B operands (S) and MN-major B operands (dQ); V stages K-major (dP)
+      auto kK = [&](int s) { return kmaj<D>(sbase + C::k_off(s)); };
+      auto mK = [&](int s) { return mnmaj<D>(sbase + C::k_off(s)); };
+      auto kV = [&](int s) { return kmaj<D>(sbase + C::v_off(s)); };
+      bool ok = mbar_wait_w(res_full, 0, g, kSiteDq | 2u) && mbar_wait_w(&k_full[0], 0, g, kSiteDq | 3u);
+      if (ok) {
+        mma_nt<D>(tS, kQ, kK(0));
+        tc_commit_w(s_full);
+        ok = mbar_wait_w(&v_full[0], 0, g, kSiteDq | 3u);
       }
+      if (ok) {
+        mma_nt<D>(tDP, kDO, kV(0));
+        tc_commit_w(dp_full);
+        tc_commit_w(&v_empty[0]);
+      }
+      for (int it = 0; ok && it < cnt; ++it) {
+        const int ks = it % C::kKStages;
+        const int ks1 = (it + 1) % C::kKStages, vs1 = (it + 1) % C::kVStages;
+        const uint32_t par = it & 1;
+        const bool next = it + 1 < cnt;
+        if (next) {
+          if (!(ok = mbar_wait_w(&k_full[ks1], ((it + 1) / C::kKStages) & 1u, g, kSiteDq | 4u))) break;
+          if (!(ok = mbar_wait_w(s_free, par, g, kSiteDq | 5u))) break;
+          tc_fence_after();
+          mma_nt<D>(tS, kQ, kK(ks1));                 // S(j+1)
+          tc_commit_w(s_full);
+        }
+        if (!(ok = mbar_wait_w(ds_full, par, g, kSiteDq | 6u))) break;
+        tc_fence_after();
+        mma_tn_acc<D>(tDQ, tDP, mK(ks), it > 0);     // dQ += dS K_j
+        tc_commit_w(&k_empty[ks]);                   // K_j: last reader done
+        if (next) {
+          if (!(ok = mbar_wait_w(&v_full[vs1], ((it + 1) / C::kVStages) & 1u, g, kSiteDq | 12u))) break;
+          mma_nt<D>(tDP, kDO, kV(vs1));               // dP(j+1), after dQ(j) has read dS(j)
+          tc_commit_w(dp_full);
+          tc_commit_w(&v_empty[vs1]);
+        }
+      }
+      if (ok) tc_commit_w(acc_done);
+      tc_commit_w(drain);
+      mbar_drain(drain, 0);
       __syncwarp();
       tc_fence_before();
       named_bar_sync(1, 288);
@@ -727,7 +728,7 @@ __global__ void __launch_bounds__(384, 1)
   bool ok = true;
   for (int it = 0; ok && it < cnt; ++it) {
     const uint32_t par = it & 1;
-    if (!(ok = mbar_wait(bb.s_full, par, g, kSiteDq | 7u))) break;
+    if (!(ok = mbar_wait(s_full, par, g, kSiteDq | 7u))) break;
     __syncwarp();
     tc_fence_after();
     uint32_t sr[2][32];
@@ -736,7 +737,7 @@ __global__ void __launch_bounds__(384, 1)
     tmem_ld_wait(sr[0]);
     tmem_ld_fence(sr[1]);
     tc_fence_before();
-    mbar_arrive(bb.s_free);   // S(j) is in registers: the tensor core may overwrite it
+    mbar_arrive(s_free);   // S(j) is in registers: the tensor core may overwrite it
     // keys k0 .. k0+lim-1 of this half are visible to the row
     const int k0 = 128 * it + 64 * h;
     int lim = N - k0;
@@ -755,7 +756,7 @@ __global__ void __launch_bounds__(384, 1)
       for (int c = 0; c < 64; ++c)
         if (c >= lim) p[c] = 0.f;
     }
-    if (!(ok = mbar_wait(bb.dp_full, par, g, kSiteDq | 8u))) break;
+    if (!(ok = mbar_wait(dp_full, par, g, kSiteDq | 8u))) break;
     __syncwarp();
     tc_fence_after();
     uint32_t dr[2][32];
@@ -776,19 +777,20 @@ __global__ void __launch_bounds__(384, 1)
     for (int c = 0; c < 64; c += 32) st_bf16_16cols(tDP + c / 2, p + c);
     tmem_st_wait();
     tc_fence_before();
-    mbar_arrive(bb.ds_full);
+    mbar_arrive(ds_full);
   }
-  if (ok && mbar_wait(bb.acc_done, 0, g, kSiteDq | 9u)) {
+  if (ok && mbar_wait(acc_done, 0, g, kSiteDq | 9u)) {
     __syncwarp();
     tc_fence_after();
     // both warpgroups stage dQ into the (now idle) Q tile; thread 0 stores it
-    bwd_store_acc<D>(tmem + lane_base + C::kColAcc0, smem + C::kResOff, h * (D / 2), (h + 1) * (D / 2), scale, r,
-                     &bb.staged[0], threadIdx.x == 0, &tmDQ, 128 * qt, bh, g, kSiteDq | 10u);
+    bwd_store_acc<D>(tmem + lane_base + C::kColAcc, smem + C::kQOff, h * (D / 2), (h + 1) * (D / 2), scale, r,
+                     staged, threadIdx.x == 0, &tmDQ, 128 * qt, bh, g, kSiteDq | 10u);
   }
   __syncwarp();
   tc_fence_before();
   named_bar_sync(1, 288);
 }
+
 template <int D, bool CAUSAL>
 cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv, const float* lse,
@@ -809,7 +811,7 @@ template <int D, bool CAUSAL>
 cudaError_t launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                         const CUtensorMap& tdo, const CUtensorMap& tdq, const float* lse, const float* Dvec,
                         const Shape& s, cudaStream_t st) {
-  using C = BwdCfg<D>;
+  using C = DqCfg<D>;
   auto kern = fa_bwd_dq_kernel<D, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;

@@ -139,7 +139,7 @@ __device__ __forceinline__ void fwd_issue_s(uint32_t tmem_d, uint64_t q_desc, ui
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint64_t off = ((kk / 4) * C::kBoxBytes + (kk % 4) * 32) >> 4;
-    tc_mma_ss(tmem_d, q_desc + off, k_desc + off, idesc, kk > 0 ? 1u : 0u);
+    tc_mma_ss_w(tmem_d, q_desc + off, k_desc + off, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
@@ -148,13 +148,15 @@ __device__ __forceinline__ void fwd_issue_pv(uint32_t tmem_o, uint32_t tmem_p, u
   constexpr uint32_t idesc = idesc_bf16(128, D, false, true);
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk)  // 128 keys, 16 per MMA; P packs 2 keys per TMEM column
-    tc_mma_ts(tmem_o, tmem_p + kk * 8, v_desc + ((kk * 2048) >> 4), idesc, (acc || kk > 0) ? 1u : 0u);
+    tc_mma_ts_w(tmem_o, tmem_p + kk * 8, v_desc + ((kk * 2048) >> 4), idesc, (acc || kk > 0) ? 1u : 0u);
 }
 
 // Issue order S0(0) S1(0) | PV0(0) S0(1) PV1(0) S1(1) | PV0(1) ...: while one
 // tile's softmax runs, the tensor core works on the other tile.  All slot
 // waits of an iteration happen before the first P wait, so once P is ready a
-// PV product and the next S product go out back to back.
+// PV product and the next S product go out back to back.  Run by the whole
+// warp: waits and descriptors are warp-uniform and `elect.sync` picks the
+// issuing lane inside each MMA and commit.
 template <int D>
 __device__ __forceinline__ void fwd_mma(const FwdWork& w, uint32_t tmem, uint32_t smem_base, uint64_t* full,
                                         uint64_t* empty, uint64_t* q_full, uint64_t* s_full, uint64_t* p_full,
@@ -168,19 +170,19 @@ __device__ __forceinline__ void fwd_mma(const FwdWork& w, uint32_t tmem, uint32_
   const uint64_t v_desc0 = sdesc_sw128(smem_base + C::kSlotOff, C::kBoxBytes, 1024);
   auto slot_off = [&](int idx) { return static_cast<uint64_t>((idx % C::kSlots) * (C::kTileBytes >> 4)); };
   auto slot_wait = [&](int idx) {
-    return mbar_wait(&full[idx % C::kSlots], (idx / C::kSlots) & 1, g, kSiteFwd | 2u);
+    return mbar_wait_w(&full[idx % C::kSlots], (idx / C::kSlots) & 1, g, kSiteFwd | 2u);
   };
-  if (!mbar_wait(q_full, 0, g, kSiteFwd | 3u)) return;
+  if (!mbar_wait_w(q_full, 0, g, kSiteFwd | 3u)) return;
   if (!slot_wait(0)) return;
   if (w.n0 > 0) {
     fwd_issue_s<D>(tmem + C::col_s(0), q_desc[0], k_desc0 + slot_off(0));
-    tc_commit(&s_full[0]);
+    tc_commit_w(&s_full[0]);
   }
   if (w.n1 > 0) {
     fwd_issue_s<D>(tmem + C::col_s(1), q_desc[1], k_desc0 + slot_off(0));
-    tc_commit(&s_full[1]);
+    tc_commit_w(&s_full[1]);
   }
-  tc_commit(&empty[0]);
+  tc_commit_w(&empty[0]);
   for (int j = 0; j < w.n; ++j) {
     const int iv = 2 * j + 1, ik = 2 * j + 2;
     const bool next = j + 1 < w.n;
@@ -188,23 +190,23 @@ __device__ __forceinline__ void fwd_mma(const FwdWork& w, uint32_t tmem, uint32_
     if (next && !slot_wait(ik)) return;
     const uint64_t vd = v_desc0 + slot_off(iv), kd = k_desc0 + slot_off(ik);
     if (j < w.n0) {
-      if (!mbar_wait(&p_full[0], j & 1, g, kSiteFwd | 4u)) return;
+      if (!mbar_wait_w(&p_full[0], j & 1, g, kSiteFwd | 4u)) return;
       tc_fence_after();
       fwd_issue_pv<D>(tmem + C::col_o(0), tmem + C::col_s(0), vd, j > 0);
       if (next && j + 1 < w.n0) fwd_issue_s<D>(tmem + C::col_s(0), q_desc[0], kd);
-      if (j == w.n0 - 1) tc_commit(&o_done[0]);
-      if (next && j + 1 < w.n0) tc_commit(&s_full[0]);
+      if (j == w.n0 - 1) tc_commit_w(&o_done[0]);
+      if (next && j + 1 < w.n0) tc_commit_w(&s_full[0]);
     }
     if (j < w.n1) {
-      if (!mbar_wait(&p_full[1], j & 1, g, kSiteFwd | 5u)) return;
+      if (!mbar_wait_w(&p_full[1], j & 1, g, kSiteFwd | 5u)) return;
       tc_fence_after();
       fwd_issue_pv<D>(tmem + C::col_o(1), tmem + C::col_s(1), vd, j > 0);
       if (next && j + 1 < w.n1) fwd_issue_s<D>(tmem + C::col_s(1), q_desc[1], kd);
-      if (j == w.n1 - 1) tc_commit(&o_done[1]);
-      if (next && j + 1 < w.n1) tc_commit(&s_full[1]);
+      if (j == w.n1 - 1) tc_commit_w(&o_done[1]);
+      if (next && j + 1 < w.n1) tc_commit_w(&s_full[1]);
     }
-    tc_commit(&empty[iv % C::kSlots]);
-    if (next) tc_commit(&empty[ik % C::kSlots]);
+    tc_commit_w(&empty[iv % C::kSlots]);
+    if (next) tc_commit_w(&empty[ik % C::kSlots]);
   }
 }
 
@@ -406,11 +408,10 @@ __global__ void __launch_bounds__(384, 1)
     if (warp == 8) {
       if (lane == 0) fwd_producer<D>(w, smem, full, empty, q_full, &tmQ, &tmK, &tmV, g);
     } else if (warp == 9) {
-      if (lane == 0) {
-        fwd_mma<D>(w, tmem, smem_u32(smem), full, empty, q_full, s_full, p_full, o_done, g);
-        tc_commit(drain);  // every MMA issued above has finished before TMEM is released
-        mbar_drain(drain, 0);
-      }
+      // the whole warp runs the issue loop (uniform operands), one elected lane issues
+      fwd_mma<D>(w, tmem, smem_u32(smem), full, empty, q_full, s_full, p_full, o_done, g);
+      tc_commit_w(drain);  // every MMA issued above has finished before TMEM is released
+      mbar_drain(drain, 0);
       __syncwarp();
       tc_fence_before();
       named_bar_sync(1, 288);

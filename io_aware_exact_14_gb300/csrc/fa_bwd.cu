@@ -95,6 +95,7 @@ __global__ void __launch_bounds__(kPreThreads) fa_bwd_preprocess_kernel(const ui
 // ---------------------------------------------------------------------------
 
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kL2Ahead = 4;   // tiles a producer prefetches into L2 ahead of its loads
 
 // Tile geometry shared by both kernels: a 128-row tile of d bf16 columns is
 // d/64 swizzled boxes of 128 rows x 128 bytes.
@@ -337,6 +338,12 @@ __global__ void __launch_bounds__(384, 1)
         if (lane == 0) ok = mbar_wait(&q_empty[qs], ((it / C::kQStages) & 1u) ^ 1u, g, kSiteDkdv | 1u);
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;   // the whole warp follows lane 0
         if (lane == 0) {
+          if (it + kL2Ahead < cnt) {   // query tile it + kL2Ahead into L2 while this one lands
+            for (int b = 0; b < C::kBoxes; ++b) {
+              tma_prefetch_l2_3d(&tmQ, 64 * b, 128 * (qt + kL2Ahead), bh);
+              tma_prefetch_l2_3d(&tmDO, 64 * b, 128 * (qt + kL2Ahead), bh);
+            }
+          }
           mbar_arrive_expect_tx(&q_full[qs], C::kTileBytes);
           for (int b = 0; b < C::kBoxes; ++b)
             tma_load_3d(smem + C::q_off(qs) + b * C::kBoxBytes, &tmQ, &q_full[qs], 64 * b, 128 * qt, bh);
@@ -535,14 +542,22 @@ __global__ void __launch_bounds__(384, 1)
 }
 
 // ---------------------------------------------------------------------------
-// dQ: one CTA per (b, h, 128-query tile i); loop over key tiles j.
+// dQ: one work unit per (b, h, 128-query tile i); loop over key tiles j.
 //   S = Q_i K_j^T, P = exp2(S * scale * log2e - lse2_row)
 //   dP = dO_i V_j^T, dS = P o (dP - D_row),  dQ_i += dS K_j,  finally dQ_i *= scale
-// Q_i and dO_i stay resident; K_j streams through a 3-deep ring (read by S(j)
-// and dQ(j)) and V_j through a 2-deep ring (read by dP(j) only), so a key tile
-// is loaded well before S(j+1) needs it.
-// MMA order S(j) dP(j) S(j+1) dQ(j) dP(j+1) ...: the exponentials of tile j run
-// under dP(j), the dS products under S(j+1).
+// Persistent CTAs: the grid has one CTA per unit, but a running CTA takes the
+// next not-yet-started CTA's unit over (cluster launch control) instead of
+// exiting, so TMEM, barriers and pipelines carry on and the next unit's loads
+// and first products overlap this unit's tail and epilogue.  The request goes
+// out a few tiles before the unit ends, so units still start in launch order
+// (heaviest first) on whichever CTA frees up first.
+// Q_i and dO_i are resident per unit; K_j streams through a 3-deep ring (read
+// by S(j) and dQ(j)) and V_j through a 2-deep ring (read by dP(j) only); the
+// rings and the per-tile barriers run on across units (global tile count).
+// The epilogue stages dQ in the dO buffer for a TMA store, so the next unit's
+// Q (and its S(0)) can arrive while it runs; the next dO follows the store.
+// MMA order S(j) dP(j) S(j+1) dQ(j) dP(j+1) ...: the exponentials of tile j
+// run under dP(j), the dS products under S(j+1).
 // TMEM: T0 = S, T1 = dP, acc = dQ.
 // ---------------------------------------------------------------------------
 
@@ -554,19 +569,37 @@ struct DqCfg {
   static constexpr uint32_t kKOff = 2 * kTileBytes;
   static constexpr uint32_t kVOff = kKOff + kKStages * kTileBytes;
   static constexpr uint32_t kBarOff = kVOff + kVStages * kTileBytes;
-  // res_full, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full, s_free, dp_full, ds_full,
-  // acc_done, drain, staged
-  static constexpr int kBars = 1 + 2 * kKStages + 2 * kVStages + 7;
-  static constexpr uint32_t kMiscOff = kBarOff + kBars * 8;
-  static constexpr uint32_t kLayoutBytes = kMiscOff + 16;
+  // q_full, q_empty, do_full, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full, s_free,
+  // dp_full, ds_full, acc_done, acc_free, staged, drain, sched, id_taken
+  static constexpr int kBars = 3 + 2 * kKStages + 2 * kVStages + 10;
+  // readers of a unit id: the MMA warp, the eight compute warps, the dO loader
+  static constexpr uint32_t kIdReaders = 10;
+  static constexpr uint32_t kMiscOff = kBarOff + kBars * 8;   // tmem holder, abort flag, unit ids [2]
+  static constexpr uint32_t kRespOff = (kMiscOff + 16 + 15) / 16 * 16;   // 16-byte work-steal response
+  static constexpr uint32_t kLayoutBytes = kRespOff + 16;
   static constexpr uint32_t kMaxSmem = BwdCfg<D>::kMaxSmem;
   static constexpr uint32_t kSmemBytes = kLayoutBytes + 1024 <= kMaxSmem ? kLayoutBytes + 1024 : kMaxSmem;
   static_assert(kLayoutBytes <= kMaxSmem, "dQ shared-memory layout too large");
   static constexpr int kThreads = 384;
+  static constexpr int kRequestAhead = 5;   // key tiles before a unit's end at which the next is requested
   static constexpr uint32_t kColS = 0, kColDP = 128, kColAcc = 256;
   __host__ __device__ static constexpr uint32_t k_off(int s) { return kKOff + s * kTileBytes; }
   __host__ __device__ static constexpr uint32_t v_off(int s) { return kVOff + s * kTileBytes; }
 };
+
+// Work unit u (a CTA index of the launch grid) -> head and query tile.
+struct DqUnit {
+  int bh, qt, cnt;
+};
+template <bool CAUSAL>
+__device__ __forceinline__ DqUnit dq_unit(int u, int n_tiles, int BH, int band) {
+  DqUnit w;
+  int rank;
+  banded_order(u, n_tiles, BH, band, w.bh, rank);
+  w.qt = n_tiles - 1 - rank;                 // causal: large qt is heavy, rank 0 first
+  w.cnt = CAUSAL ? w.qt + 1 : n_tiles;       // key tiles visited
+  return w;
+}
 
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(384, 1)
@@ -584,8 +617,10 @@ __global__ void __launch_bounds__(384, 1)
     return;
   }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
-  uint64_t* res_full = bars;
-  uint64_t* k_full = bars + 1;
+  uint64_t* q_full = bars;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* do_full = bars + 2;
+  uint64_t* k_full = bars + 3;
   uint64_t* k_empty = k_full + C::kKStages;
   uint64_t* v_full = k_empty + C::kKStages;
   uint64_t* v_empty = v_full + C::kVStages;
@@ -594,20 +629,24 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* dp_full = s_free + 1;
   uint64_t* ds_full = dp_full + 1;
   uint64_t* acc_done = ds_full + 1;
-  uint64_t* drain = acc_done + 1;
-  uint64_t* staged = drain + 1;
+  uint64_t* acc_free = acc_done + 1;
+  uint64_t* staged = acc_free + 1;
+  uint64_t* drain = staged + 1;
+  uint64_t* sched = drain + 1;
+  uint64_t* id_taken = sched + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kMiscOff + 4);
+  // Unit ids, by unit parity.  The producer publishes unit k+1 (id, then the
+  // q_full phase) only after every reader has taken unit k's id, so q_full is
+  // never two phases ahead of a reader's wait.
+  volatile int* unit_id = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 8);
+  uint8_t* resp = smem + C::kRespOff;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  int bh, rank;
-  banded_order(blockIdx.x, n_tiles, BH, band, bh, rank);
-  const int qt = n_tiles - 1 - rank;  // causal: large qt is heavy
-  const int cnt = CAUSAL ? qt + 1 : n_tiles;                             // key tiles visited
-  const size_t row_base = static_cast<size_t>(bh) * N;
-
   if (threadIdx.x == 0) {
-    mbar_init(res_full, 1);
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    mbar_init(do_full, 1);
     for (int i = 0; i < C::kKStages; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
@@ -621,8 +660,12 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(dp_full, 1);
     mbar_init(ds_full, 256);
     mbar_init(acc_done, 1);
-    mbar_init(drain, 1);
+    mbar_init(acc_free, 256);
     mbar_init(staged, 256);
+    mbar_init(drain, 1);
+    mbar_init(sched, 1);
+    mbar_init(id_taken, C::kIdReaders);
+    unit_id[0] = static_cast<int>(blockIdx.x);
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -636,26 +679,89 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tmem = *tmem_holder;
   const CtaGuard g{abort_flag, &g_status_bwd};
   const uint32_t sbase = smem_u32(smem);
+  auto kpar = [](int j) { return static_cast<uint32_t>((j / C::kKStages) & 1); };
+  auto vpar = [](int j) { return static_cast<uint32_t>((j / C::kVStages) & 1); };
 
   if (warp >= 8) {
-    if (warp == 8) {  // producer: Q_i, dO_i once; K_j and V_j through their rings
+    if (warp == 8) {  // producer: per unit Q_i; K_j and V_j through their rings; next unit
       if (lane == 0) {
-        mbar_arrive_expect_tx(res_full, 2 * C::kTileBytes);
-        for (int b = 0; b < BwdCfg<D>::kBoxes; ++b) {
-          tma_load_3d(smem + C::kQOff + b * BwdCfg<D>::kBoxBytes, &tmQ, res_full, 64 * b, 128 * qt, bh);
-          tma_load_3d(smem + C::kDOOff + b * BwdCfg<D>::kBoxBytes, &tmDO, res_full, 64 * b, 128 * qt, bh);
-        }
-        for (int it = 0; it < cnt; ++it) {
-          const int ks = it % C::kKStages, vs = it % C::kVStages;
-          if (!mbar_wait(&k_empty[ks], ((it / C::kKStages) & 1u) ^ 1u, g, kSiteDq | 1u)) break;
-          mbar_arrive_expect_tx(&k_full[ks], C::kTileBytes);
+        int u = static_cast<int>(blockIdx.x);
+        int gk = 0;   // global key-tile count (ring index)
+        for (int su = 0;; ++su) {
+          const DqUnit w = dq_unit<CAUSAL>(u, n_tiles, BH, band);
+          mbar_arrive_expect_tx(q_full, C::kTileBytes);
           for (int b = 0; b < BwdCfg<D>::kBoxes; ++b)
-            tma_load_3d(smem + C::k_off(ks) + b * BwdCfg<D>::kBoxBytes, &tmK, &k_full[ks], 64 * b, 128 * it, bh);
-          if (!mbar_wait(&v_empty[vs], ((it / C::kVStages) & 1u) ^ 1u, g, kSiteDq | 11u)) break;
-          mbar_arrive_expect_tx(&v_full[vs], C::kTileBytes);
-          for (int b = 0; b < BwdCfg<D>::kBoxes; ++b)
-            tma_load_3d(smem + C::v_off(vs) + b * BwdCfg<D>::kBoxBytes, &tmV, &v_full[vs], 64 * b, 128 * it, bh);
+            tma_load_3d(smem + C::kQOff + b * BwdCfg<D>::kBoxBytes, &tmQ, q_full, 64 * b, 128 * w.qt, w.bh);
+          bool ok = true;
+          for (int it = 0; it < w.cnt; ++it, ++gk) {
+            const int ks = gk % C::kKStages, vs = gk % C::kVStages;
+            if (it == max(0, w.cnt - C::kRequestAhead)) {   // ask for the next unit
+              mbar_arrive_expect_tx(sched, 16);
+              clc_try_cancel(resp, sched);
+            }
+            if (!(ok = mbar_wait(&k_empty[ks], kpar(gk) ^ 1u, g, kSiteDq | 1u))) break;
+            if (it + kL2Ahead < w.cnt) {   // key tile it + kL2Ahead into L2 while this one lands
+              for (int b = 0; b < BwdCfg<D>::kBoxes; ++b) {
+                tma_prefetch_l2_3d(&tmK, 64 * b, 128 * (it + kL2Ahead), w.bh);
+                tma_prefetch_l2_3d(&tmV, 64 * b, 128 * (it + kL2Ahead), w.bh);
+              }
+            }
+            mbar_arrive_expect_tx(&k_full[ks], C::kTileBytes);
+            for (int b = 0; b < BwdCfg<D>::kBoxes; ++b)
+              tma_load_3d(smem + C::k_off(ks) + b * BwdCfg<D>::kBoxBytes, &tmK, &k_full[ks], 64 * b, 128 * it,
+                          w.bh);
+            if (!(ok = mbar_wait(&v_empty[vs], vpar(gk) ^ 1u, g, kSiteDq | 11u))) break;
+            mbar_arrive_expect_tx(&v_full[vs], C::kTileBytes);
+            for (int b = 0; b < BwdCfg<D>::kBoxes; ++b)
+              tma_load_3d(smem + C::v_off(vs) + b * BwdCfg<D>::kBoxBytes, &tmV, &v_full[vs], 64 * b, 128 * it,
+                          w.bh);
+          }
+          if (!ok || !mbar_wait(sched, su & 1, g, kSiteDq | 13u)) break;
+          u = clc_decode(resp);
+          if (u >= 0) {   // the next unit's first tiles into L2 while this unit finishes
+            const DqUnit w1 = dq_unit<CAUSAL>(u, n_tiles, BH, band);
+            for (int b = 0; b < BwdCfg<D>::kBoxes; ++b) {
+              tma_prefetch_l2_3d(&tmQ, 64 * b, 128 * w1.qt, w1.bh);
+              tma_prefetch_l2_3d(&tmDO, 64 * b, 128 * w1.qt, w1.bh);
+              for (int t = 0; t < kL2Ahead && t < w1.cnt; ++t) {
+                tma_prefetch_l2_3d(&tmK, 64 * b, 128 * t, w1.bh);
+                tma_prefetch_l2_3d(&tmV, 64 * b, 128 * t, w1.bh);
+              }
+            }
+          }
+          // Q_i is free once this unit's last S product is done; every reader
+          // has taken this unit's id before the next one is published
+          if (!mbar_wait(q_empty, su & 1, g, kSiteDq | 14u)) break;
+          if (!mbar_wait(id_taken, su & 1, g, kSiteDq | 20u)) break;
+          unit_id[(su + 1) & 1] = u;
+          if (u < 0) {      // no work left: release the consumers with an empty phase
+            mbar_arrive(q_full);
+            break;
+          }
         }
+      }
+    } else if (warp == 10) {  // dO buffer owner: stores each unit's dQ from it, then loads the next dO
+      if (lane == 0) {
+        DqUnit prev{0, 0, 0};
+        for (int su = 0;; ++su) {
+          if (!mbar_wait_backoff(q_full, su & 1, g, kSiteDq | 17u)) break;
+          const int u = unit_id[su & 1];
+          if (u >= 0) mbar_arrive(id_taken);
+          if (su > 0) {   // the previous unit's dQ, staged by the compute warps
+            if (!mbar_wait_backoff(staged, (su - 1) & 1, g, kSiteDq | 18u)) break;
+            for (int b = 0; b < BwdCfg<D>::kBoxes; ++b)
+              tma_store_3d(&tmDQ, smem + C::kDOOff + b * BwdCfg<D>::kBoxBytes, 64 * b, 128 * prev.qt, prev.bh);
+            tma_store_commit();
+            tma_store_wait_read_all();
+          }
+          if (u < 0) break;
+          prev = dq_unit<CAUSAL>(u, n_tiles, BH, band);
+          mbar_arrive_expect_tx(do_full, C::kTileBytes);
+          for (int b = 0; b < BwdCfg<D>::kBoxes; ++b)
+            tma_load_3d(smem + C::kDOOff + b * BwdCfg<D>::kBoxBytes, &tmDO, do_full, 64 * b, 128 * prev.qt,
+                        prev.bh);
+        }
+        tma_store_wait_all();   // the last stores have landed before the CTA retires
       }
     } else if (warp == 9) {  // MMA issuer: the whole warp runs the loop, one lane issues
       const uint32_t tS = tmem + C::kColS, tDP = tmem + C::kColDP, tDQ = tmem + C::kColAcc;
@@ -664,41 +770,67 @@ __global__ void __launch_bounds__(384, 1)
       auto kK = [&](int s) { return kmaj<D>(sbase + C::k_off(s)); };
       auto mK = [&](int s) { return mnmaj<D>(sbase + C::k_off(s)); };
       auto kV = [&](int s) { return kmaj<D>(sbase + C::v_off(s)); };
-      bool ok = mbar_wait_w(res_full, 0, g, kSiteDq | 2u) && mbar_wait_w(&k_full[0], 0, g, kSiteDq | 3u);
-      if (ok) {
-        mma_nt<D>(tS, kQ, kK(0));
-        tc_commit_w(s_full);
-        ok = mbar_wait_w(&v_full[0], 0, g, kSiteDq | 3u);
-      }
-      if (ok) {
-        mma_nt<D>(tDP, kDO, kV(0));
-        tc_commit_w(dp_full);
-        tc_commit_w(&v_empty[0]);
-      }
-      for (int it = 0; ok && it < cnt; ++it) {
-        const int ks = it % C::kKStages;
-        const int ks1 = (it + 1) % C::kKStages, vs1 = (it + 1) % C::kVStages;
-        const uint32_t par = it & 1;
-        const bool next = it + 1 < cnt;
-        if (next) {
-          if (!(ok = mbar_wait_w(&k_full[ks1], ((it + 1) / C::kKStages) & 1u, g, kSiteDq | 4u))) break;
-          if (!(ok = mbar_wait_w(s_free, par, g, kSiteDq | 5u))) break;
-          tc_fence_after();
-          mma_nt<D>(tS, kQ, kK(ks1));                 // S(j+1)
-          tc_commit_w(s_full);
-        }
-        if (!(ok = mbar_wait_w(ds_full, par, g, kSiteDq | 6u))) break;
+      bool ok = true;
+      int gk = 0;
+      // One unit: S(0) dP(0) | S(1) dQ(0) dP(1) | ... | S(c-1) dQ(c-2) dP(c-1) | dQ(c-1).
+      // The first and last tile are peeled so the steady loop carries no
+      // per-unit conditions: this warp's issue time bounds the tensor core.
+      for (int su = 0; ok; ++su) {
+        if (!(ok = mbar_wait_w(q_full, su & 1, g, kSiteDq | 2u))) break;
+        const int u = unit_id[su & 1];
+        if (u < 0) break;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(id_taken);
+        const int cnt = dq_unit<CAUSAL>(u, n_tiles, BH, band).cnt;
+        const int g0 = gk;   // this unit's first global key tile
+        // S(0): its K tile and the previous S read out of TMEM
+        if (!(ok = mbar_wait_w(&k_full[g0 % C::kKStages], kpar(g0), g, kSiteDq | 3u))) break;
+        if (g0 > 0 && !(ok = mbar_wait_w(s_free, (g0 - 1) & 1, g, kSiteDq | 5u))) break;
         tc_fence_after();
-        mma_tn_acc<D>(tDQ, tDP, mK(ks), it > 0);     // dQ += dS K_j
-        tc_commit_w(&k_empty[ks]);                   // K_j: last reader done
-        if (next) {
-          if (!(ok = mbar_wait_w(&v_full[vs1], ((it + 1) / C::kVStages) & 1u, g, kSiteDq | 12u))) break;
-          mma_nt<D>(tDP, kDO, kV(vs1));               // dP(j+1), after dQ(j) has read dS(j)
+        mma_nt<D>(tS, kQ, kK(g0 % C::kKStages));
+        tc_commit_w(s_full);
+        if (!(ok = mbar_wait_w(&v_full[g0 % C::kVStages], vpar(g0), g, kSiteDq | 3u))) break;
+        if (!(ok = mbar_wait_w(do_full, su & 1, g, kSiteDq | 19u))) break;
+        mma_nt<D>(tDP, kDO, kV(g0 % C::kVStages));
+        tc_commit_w(dp_full);
+        tc_commit_w(&v_empty[g0 % C::kVStages]);
+        for (int it = 0; it < cnt; ++it) {
+          const int j = g0 + it;   // global index of key tile it
+          const uint32_t par = j & 1;
+          const bool next = it + 1 < cnt;
+          if (next) {   // S(j+1)
+            if (!(ok = mbar_wait_w(&k_full[(j + 1) % C::kKStages], kpar(j + 1), g, kSiteDq | 4u))) break;
+            if (!(ok = mbar_wait_w(s_free, par, g, kSiteDq | 5u))) break;
+            tc_fence_after();
+            mma_nt<D>(tS, kQ, kK((j + 1) % C::kKStages));
+            tc_commit_w(s_full);
+          } else {
+            tc_commit_w(q_empty);   // every reader of Q_i has been issued
+          }
+          if (!(ok = mbar_wait_w(ds_full, par, g, kSiteDq | 6u))) break;
+          if (it == 0) {
+            // the unit's first dQ overwrites the accumulator: the previous
+            // unit's epilogue must have read it out
+            if (su > 0 && !(ok = mbar_wait_w(acc_free, (su - 1) & 1, g, kSiteDq | 15u))) break;
+            tc_fence_after();
+            mma_tn_acc<D>(tDQ, tDP, mK(j % C::kKStages), false);
+          } else {
+            tc_fence_after();
+            mma_tn_acc<D>(tDQ, tDP, mK(j % C::kKStages), true);   // dQ += dS K_j
+          }
+          tc_commit_w(&k_empty[j % C::kKStages]);                 // K_j: last reader done
+          if (!next) {
+            tc_commit_w(acc_done);
+            break;
+          }
+          // dP(j+1), after dQ(j) has read dS(j) from the same columns
+          if (!(ok = mbar_wait_w(&v_full[(j + 1) % C::kVStages], vpar(j + 1), g, kSiteDq | 12u))) break;
+          mma_nt<D>(tDP, kDO, kV((j + 1) % C::kVStages));
           tc_commit_w(dp_full);
-          tc_commit_w(&v_empty[vs1]);
+          tc_commit_w(&v_empty[(j + 1) % C::kVStages]);
         }
+        gk = g0 + cnt;
       }
-      if (ok) tc_commit_w(acc_done);
       tc_commit_w(drain);
       mbar_drain(drain, 0);
       __syncwarp();
@@ -713,78 +845,110 @@ __global__ void __launch_bounds__(384, 1)
   // compute warpgroups: query row r = TMEM lane; half h owns key columns [64h, 64h+64)
   const int h = warp >> 2;
   const int r = threadIdx.x & 127;
-  const int row = 128 * qt + r;
   const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
   const uint32_t tS = tmem + lane_base + C::kColS + 64 * h;
   const uint32_t tDP = tmem + lane_base + C::kColDP + 64 * h;
-  float nlse2 = -INFINITY, ndrow = 0.f;   // -lse * log2(e) and -D of this row
-  if (row < N) {
-    const float l = lse[row_base + row];
-    nlse2 = (l == -INFINITY) ? -INFINITY : -l * kLog2e;
-    ndrow = -Dg[row_base + row];
-  }
-  const float2 sc2 = make_float2(scale_log2, scale_log2), nl2 = make_float2(nlse2, nlse2);
-  const float2 nd2 = make_float2(ndrow, ndrow);
+  const float2 sc2 = make_float2(scale_log2, scale_log2);
   bool ok = true;
-  for (int it = 0; ok && it < cnt; ++it) {
-    const uint32_t par = it & 1;
-    if (!(ok = mbar_wait(s_full, par, g, kSiteDq | 7u))) break;
+  int gk = 0;
+  for (int su = 0; ok; ++su) {
+    if (!(ok = mbar_wait(q_full, su & 1, g, kSiteDq | 16u))) break;
+    const int u = unit_id[su & 1];
+    if (u < 0) break;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(id_taken);
+    const DqUnit w = dq_unit<CAUSAL>(u, n_tiles, BH, band);
+    const size_t row_base = static_cast<size_t>(w.bh) * N;
+    const int row = 128 * w.qt + r;
+    float nlse2 = -INFINITY, ndrow = 0.f;   // -lse * log2(e) and -D of this row
+    if (row < N) {
+      const float l = lse[row_base + row];
+      nlse2 = (l == -INFINITY) ? -INFINITY : -l * kLog2e;
+      ndrow = -Dg[row_base + row];
+    }
+    const float2 nl2 = make_float2(nlse2, nlse2), nd2 = make_float2(ndrow, ndrow);
+    for (int it = 0; ok && it < w.cnt; ++it, ++gk) {
+      const uint32_t par = gk & 1;
+      if (!(ok = mbar_wait(s_full, par, g, kSiteDq | 7u))) break;
+      __syncwarp();
+      tc_fence_after();
+      uint32_t sr[2][32];
+      tmem_ld32(tS, sr[0]);
+      tmem_ld32(tS + 32, sr[1]);
+      tmem_ld_wait(sr[0]);
+      tmem_ld_fence(sr[1]);
+      tc_fence_before();
+      mbar_arrive(s_free);   // S(j) is in registers: the tensor core may overwrite it
+      // keys k0 .. k0+lim-1 of this half are visible to the row
+      const int k0 = 128 * it + 64 * h;
+      int lim = N - k0;
+      if (CAUSAL) lim = min(lim, row - k0 + 1);
+      float p[64];
+#pragma unroll
+      for (int c = 0; c < 64; c += 2) {
+        const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[c / 32][c % 32]),
+                                                __uint_as_float(sr[(c + 1) / 32][(c + 1) % 32])),
+                                    sc2, nl2);
+        p[c] = ex2_approx(x.x);
+        p[c + 1] = ex2_approx(x.y);
+      }
+      if (lim < 64) {  // diagonal or ragged-tail tile only
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (c >= lim) p[c] = 0.f;
+      }
+      if (!(ok = mbar_wait(dp_full, par, g, kSiteDq | 8u))) break;
+      __syncwarp();
+      tc_fence_after();
+      uint32_t dr[2][32];
+      tmem_ld32(tDP, dr[0]);
+      tmem_ld32(tDP + 32, dr[1]);
+      tmem_ld_wait(dr[0]);
+      tmem_ld_fence(dr[1]);
+#pragma unroll
+      for (int c = 0; c < 64; c += 2) {
+        const float2 dp = __fadd2_rn(make_float2(__uint_as_float(dr[c / 32][c % 32]),
+                                                 __uint_as_float(dr[(c + 1) / 32][(c + 1) % 32])),
+                                     nd2);
+        const float2 ds = __fmul2_rn(make_float2(p[c], p[c + 1]), dp);
+        p[c] = ds.x;
+        p[c + 1] = ds.y;
+      }
+#pragma unroll
+      for (int c = 0; c < 64; c += 32) st_bf16_16cols(tDP + c / 2, p + c);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(ds_full);
+    }
+    if (!ok || !(ok = mbar_wait(acc_done, su & 1, g, kSiteDq | 9u))) break;
     __syncwarp();
     tc_fence_after();
-    uint32_t sr[2][32];
-    tmem_ld32(tS, sr[0]);
-    tmem_ld32(tS + 32, sr[1]);
-    tmem_ld_wait(sr[0]);
-    tmem_ld_fence(sr[1]);
-    tc_fence_before();
-    mbar_arrive(s_free);   // S(j) is in registers: the tensor core may overwrite it
-    // keys k0 .. k0+lim-1 of this half are visible to the row
-    const int k0 = 128 * it + 64 * h;
-    int lim = N - k0;
-    if (CAUSAL) lim = min(lim, row - k0 + 1);
-    float p[64];
+    // epilogue: both warpgroups stage dQ (x scale, bf16) in the dO buffer (its
+    // last reader, dP, finished before acc_done); the dO buffer's owner warp
+    // stores it with TMA and then refills the buffer, so no compute warp waits
+    {
+      const uint32_t stage = sbase + C::kDOOff;
 #pragma unroll
-    for (int c = 0; c < 64; c += 2) {
-      const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[c / 32][c % 32]),
-                                              __uint_as_float(sr[(c + 1) / 32][(c + 1) % 32])),
-                                  sc2, nl2);
-      p[c] = ex2_approx(x.x);
-      p[c + 1] = ex2_approx(x.y);
+      for (int c = h * (D / 2); c < (h + 1) * (D / 2); c += 32) {
+        uint32_t o[32];
+        tmem_ld32(tmem + lane_base + C::kColAcc + c, o);
+        tmem_ld_wait(o);
+        const uint32_t box = stage + (c / 64) * BwdCfg<D>::kBoxBytes + r * 128;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int chunk = (c % 64) / 8 + q;
+          float f[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(o[8 * q + e]) * scale;
+          st_shared_v4(box + ((chunk ^ (r & 7)) << 4), pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                       pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(acc_free);   // the accumulator may be overwritten
+      fence_proxy_async_smem();
+      mbar_arrive(staged);
     }
-    if (lim < 64) {  // diagonal or ragged-tail tile only
-#pragma unroll
-      for (int c = 0; c < 64; ++c)
-        if (c >= lim) p[c] = 0.f;
-    }
-    if (!(ok = mbar_wait(dp_full, par, g, kSiteDq | 8u))) break;
-    __syncwarp();
-    tc_fence_after();
-    uint32_t dr[2][32];
-    tmem_ld32(tDP, dr[0]);
-    tmem_ld32(tDP + 32, dr[1]);
-    tmem_ld_wait(dr[0]);
-    tmem_ld_fence(dr[1]);
-#pragma unroll
-    for (int c = 0; c < 64; c += 2) {
-      const float2 dp = __fadd2_rn(make_float2(__uint_as_float(dr[c / 32][c % 32]),
-                                               __uint_as_float(dr[(c + 1) / 32][(c + 1) % 32])),
-                                   nd2);
-      const float2 ds = __fmul2_rn(make_float2(p[c], p[c + 1]), dp);
-      p[c] = ds.x;
-      p[c + 1] = ds.y;
-    }
-#pragma unroll
-    for (int c = 0; c < 64; c += 32) st_bf16_16cols(tDP + c / 2, p + c);
-    tmem_st_wait();
-    tc_fence_before();
-    mbar_arrive(ds_full);
-  }
-  if (ok && mbar_wait(acc_done, 0, g, kSiteDq | 9u)) {
-    __syncwarp();
-    tc_fence_after();
-    // both warpgroups stage dQ into the (now idle) Q tile; thread 0 stores it
-    bwd_store_acc<D>(tmem + lane_base + C::kColAcc, smem + C::kQOff, h * (D / 2), (h + 1) * (D / 2), scale, r,
-                     staged, threadIdx.x == 0, &tmDQ, 128 * qt, bh, g, kSiteDq | 10u);
   }
   __syncwarp();
   tc_fence_before();

@@ -41,6 +41,7 @@ namespace fa {
 namespace {
 
 __device__ unsigned int g_status_fwd = 0;
+constexpr int kL2Ahead = 4;   // key/value tiles the producer prefetches into L2 ahead of its loads
 
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLn2 = 0.6931471805599453f;
@@ -110,6 +111,10 @@ __device__ __forceinline__ void fwd_producer(const FwdWork& w, uint8_t* smem, ui
       if (!mbar_wait(&empty[slot], ph ^ 1u, g, kSiteFwd | 1u)) {
         ok = false;
         break;
+      }
+      if (j + kL2Ahead < w.n) {   // the same tile kL2Ahead steps on, into L2 while this one lands
+#pragma unroll
+        for (int b = 0; b < C::kBoxes; ++b) tma_prefetch_l2_3d(kind ? tmV : tmK, 64 * b, 128 * (j + kL2Ahead), w.bh);
       }
       mbar_arrive_expect_tx(&full[slot], C::kTileBytes);
       uint8_t* dst = smem + C::kSlotOff + slot * C::kTileBytes;

@@ -64,6 +64,7 @@ struct FwdCfg {
   static constexpr uint32_t kRegsSoftmax = 216;  // per thread, warpgroups 0-1
   static constexpr uint32_t kRegsOther = 56;     // per thread, warpgroup 2
   static constexpr uint32_t kRegsNeeded = 256 * kRegsSoftmax + 128 * kRegsOther;
+
   __host__ __device__ static constexpr uint32_t col_s(int tile) { return tile ? 128u : 0u; }
   __host__ __device__ static constexpr uint32_t col_o(int tile) { return tile ? 256u + D : 256u; }
 };
@@ -156,6 +157,59 @@ __device__ __forceinline__ void fwd_issue_pv(uint32_t tmem_o, uint32_t tmem_p, u
     tc_mma_ts_w(tmem_o, tmem_p + kk * 8, v_desc + ((kk * 2048) >> 4), idesc, (acc || kk > 0) ? 1u : 0u);
 }
 
+// One issuing warp per query tile (warp 9: tile 0, warp 10: tile 1), so the
+// waits, commits and issue of the two tiles' products proceed side by side;
+// each warp issues S_t(0) | PV_t(0) S_t(1) | PV_t(1) S_t(2) | ... and the
+// tensor core interleaves the two streams, so one tile's products run while
+// the other tile's softmax works.  Both warps walk every key step (a tile
+// with fewer steps just stops issuing) and both release each K/V slot.
+// Runs converged: waits and descriptors are warp-uniform and `elect.sync`
+// picks the issuing lane inside each MMA and commit.
+template <int D>
+__device__ __forceinline__ void fwd_mma(const FwdWork& w, int tile, uint32_t tmem, uint32_t smem_base,
+                                        uint64_t* full, uint64_t* empty, uint64_t* q_full, uint64_t* s_full,
+                                        uint64_t* p_full, uint64_t* o_done, const CtaGuard& g) {
+  using C = FwdCfg<D>;
+  const int n_t = tile ? w.n1 : w.n0;
+  const uint64_t q_desc = sdesc_sw128(smem_base + C::kQOff + tile * C::kTileBytes, 16, 1024);
+  // K-major (S = Q K^T) and MN-major (O += P V) descriptors of ring slot 0;
+  // slot s is `s * kTileBytes` further on
+  const uint64_t k_desc0 = sdesc_sw128(smem_base + C::kSlotOff, 16, 1024);
+  const uint64_t v_desc0 = sdesc_sw128(smem_base + C::kSlotOff, C::kBoxBytes, 1024);
+  const uint32_t t_s = tmem + C::col_s(tile), t_o = tmem + C::col_o(tile);
+  auto slot_off = [&](int idx) { return static_cast<uint64_t>((idx % C::kSlots) * (C::kTileBytes >> 4)); };
+  auto slot_wait = [&](int idx) {
+    return mbar_wait_w(&full[idx % C::kSlots], (idx / C::kSlots) & 1, g, kSiteFwd | 2u);
+  };
+  if (!mbar_wait_w(q_full, 0, g, kSiteFwd | 3u)) return;
+  if (!slot_wait(0)) return;
+  if (n_t > 0) {
+    fwd_issue_s<D>(t_s, q_desc, k_desc0 + slot_off(0));
+    tc_commit_w(&s_full[tile]);
+  }
+  tc_commit_w(&empty[0]);
+  for (int j = 0; j < w.n; ++j) {
+    const int iv = 2 * j + 1, ik = 2 * j + 2;
+    const bool next = j + 1 < w.n;
+    if (!slot_wait(iv)) return;
+    if (next && !slot_wait(ik)) return;
+    if (j < n_t) {
+      if (!mbar_wait_w(&p_full[tile], j & 1, g, tile ? (kSiteFwd | 5u) : (kSiteFwd | 4u))) return;
+      tc_fence_after();
+      fwd_issue_pv<D>(t_o, t_s, v_desc0 + slot_off(iv), j > 0);
+      if (j + 1 < n_t) {
+        fwd_issue_s<D>(t_s, q_desc, k_desc0 + slot_off(ik));
+        tc_commit_w(&s_full[tile]);
+      } else {
+        tc_commit_w(&o_done[tile]);
+      }
+    }
+    tc_commit_w(&empty[iv % C::kSlots]);
+    if (next) tc_commit_w(&empty[ik % C::kSlots]);
+  }
+}
+
+// One issuing warp for both tiles (d = 64).
 // Issue order S0(0) S1(0) | PV0(0) S0(1) PV1(0) S1(1) | PV0(1) ...: while one
 // tile's softmax runs, the tensor core works on the other tile.  All slot
 // waits of an iteration happen before the first P wait, so once P is ready a
@@ -163,7 +217,7 @@ __device__ __forceinline__ void fwd_issue_pv(uint32_t tmem_o, uint32_t tmem_p, u
 // warp: waits and descriptors are warp-uniform and `elect.sync` picks the
 // issuing lane inside each MMA and commit.
 template <int D>
-__device__ __forceinline__ void fwd_mma(const FwdWork& w, uint32_t tmem, uint32_t smem_base, uint64_t* full,
+__device__ __forceinline__ void fwd_mma_both(const FwdWork& w, uint32_t tmem, uint32_t smem_base, uint64_t* full,
                                         uint64_t* empty, uint64_t* q_full, uint64_t* s_full, uint64_t* p_full,
                                         uint64_t* o_done, const CtaGuard& g) {
   using C = FwdCfg<D>;
@@ -349,7 +403,8 @@ __device__ __forceinline__ void fwd_softmax(const FwdWork& w, int tile, uint32_t
   if (row < N) lse[static_cast<size_t>(w.bh) * N + row] = l > 0.f ? (m_use + __log2f(l)) * kLn2 : -INFINITY;
 }
 
-template <int D, bool CAUSAL>
+// ISSUERS: MMA-issuing warps, 1 (warp 9 issues both tiles) or 2 (one per tile).
+template <int D, bool CAUSAL, int ISSUERS>
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -376,7 +431,7 @@ __global__ void __launch_bounds__(384, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kSlots; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+      mbar_init(&empty[i], ISSUERS);   // released by every issuing warp
     }
     mbar_init(q_full, 1);
     for (int i = 0; i < 2; ++i) {
@@ -385,7 +440,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&o_done[i], 1);
       mbar_init(&staged[i], 128);
     }
-    mbar_init(drain, 1);
+    mbar_init(drain, ISSUERS);   // one commit per issuing warp
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -412,16 +467,19 @@ __global__ void __launch_bounds__(384, 1)
     regs_dec<C::kRegsOther>();
     if (warp == 8) {
       if (lane == 0) fwd_producer<D>(w, smem, full, empty, q_full, &tmQ, &tmK, &tmV, g);
-    } else if (warp == 9) {
-      // the whole warp runs the issue loop (uniform operands), one elected lane issues
-      fwd_mma<D>(w, tmem, smem_u32(smem), full, empty, q_full, s_full, p_full, o_done, g);
+    } else if (warp == 9 || (ISSUERS == 2 && warp == 10)) {
+      // issuing warps (warp 9 also owns TMEM): whole-warp loops, one elected lane issues
+      if (ISSUERS == 2)
+        fwd_mma<D>(w, warp - 9, tmem, smem_u32(smem), full, empty, q_full, s_full, p_full, o_done, g);
+      else
+        fwd_mma_both<D>(w, tmem, smem_u32(smem), full, empty, q_full, s_full, p_full, o_done, g);
       tc_commit_w(drain);  // every MMA issued above has finished before TMEM is released
       mbar_drain(drain, 0);
       __syncwarp();
       tc_fence_before();
-      named_bar_sync(1, 288);
+      named_bar_sync(1, 256 + 32 * ISSUERS);
       tc_fence_after();
-      tmem_dealloc(tmem, 512);
+      if (warp == 9) tmem_dealloc(tmem, 512);
     }
   } else {
     regs_inc<C::kRegsSoftmax>();
@@ -429,15 +487,15 @@ __global__ void __launch_bounds__(384, 1)
                            g);
     __syncwarp();
     tc_fence_before();
-    named_bar_sync(1, 288);
+    named_bar_sync(1, 256 + 32 * ISSUERS);
   }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, int ISSUERS>
 cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& to, float* lse, const Shape& s, cudaStream_t st) {
   using C = FwdCfg<D>;
-  auto kern = fa_fwd_kernel<D, CAUSAL>;
+  auto kern = fa_fwd_kernel<D, CAUSAL, ISSUERS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   // The warpgroups' register split must fit the launch allocation, or the
@@ -457,14 +515,26 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 
 }  // namespace
 
+// Issue strategy (measured on GB300): at d = 128 one warp's issue loop (two
+// tiles' waits, commits and 32 MMAs per key step) cannot keep the tensor core
+// fed once CTAs run long, so long rows get one issuing warp per tile; short
+// CTAs (few key steps, where prologue and epilogue weigh more) and d = 64
+// (half-length products, softmax-bound) keep one issuer.
+constexpr int kTwoIssuerMinSteps = 24;   // average key steps per CTA
+
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to, float* lse, const Shape& s, cudaStream_t st) {
   if (s.d == 128) {
-    return s.causal ? launch_fwd_t<128, true>(tq, tk, tv, to, lse, s, st)
-                    : launch_fwd_t<128, false>(tq, tk, tv, to, lse, s, st);
+    const int n_qt = (s.N + 127) / 128;
+    const int avg_steps = s.causal ? (n_qt + 1) / 2 : n_qt;
+    if (avg_steps >= kTwoIssuerMinSteps)
+      return s.causal ? launch_fwd_t<128, true, 2>(tq, tk, tv, to, lse, s, st)
+                      : launch_fwd_t<128, false, 2>(tq, tk, tv, to, lse, s, st);
+    return s.causal ? launch_fwd_t<128, true, 1>(tq, tk, tv, to, lse, s, st)
+                    : launch_fwd_t<128, false, 1>(tq, tk, tv, to, lse, s, st);
   }
-  return s.causal ? launch_fwd_t<64, true>(tq, tk, tv, to, lse, s, st)
-                  : launch_fwd_t<64, false>(tq, tk, tv, to, lse, s, st);
+  return s.causal ? launch_fwd_t<64, true, 1>(tq, tk, tv, to, lse, s, st)
+                  : launch_fwd_t<64, false, 1>(tq, tk, tv, to, lse, s, st);
 }
 
 cudaError_t fwd_status(uint32_t* out, bool reset) {

@@ -41,6 +41,21 @@ def test_fwd_small_full_parity(B, H, N, d, causal):
     assert oracle.lse_max_abs_err(f64(lse), lse_ref) <= TOL_LSE
 
 
+# Long rows switch the d = 128 forward to one MMA-issuing warp per query tile
+# (at >= 24 key steps per CTA on average): cover that launch path in full,
+# with ragged tails, non-causal (25 steps) and causal (25 steps on average).
+@pytest.mark.parametrize("B,H,N,d,causal", [(1, 1, 3100, 128, False), (1, 1, 6200, 128, True)])
+def test_fwd_two_issuer_full_parity(B, H, N, d, causal):
+    x, g = device_inputs(B, H, N, d, seed=500 + N + causal)
+    scale = 1.0 / np.sqrt(d)
+    o, lse = fa.fa_fwd(g["q"], g["k"], g["v"], scale, causal)
+    torch.cuda.synchronize()
+    assert_no_timeout()
+    o_ref, lse_ref = oracle.attn_fwd_ref(f64(x["q"]), f64(x["k"]), f64(x["v"]), scale, causal)
+    assert o_excess_err(f64(o), o_ref) <= TOL_O
+    assert oracle.lse_max_abs_err(f64(lse), lse_ref) <= TOL_LSE
+
+
 def test_fwd_scale_argument():
     x, g = device_inputs(1, 2, 300, 64, seed=7)
     for scale in (0.02, 0.5):

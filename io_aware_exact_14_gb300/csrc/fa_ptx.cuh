@@ -251,40 +251,12 @@ __device__ __forceinline__ void tc_fence_before() {
 
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// Arrive once on `bar` when every tcgen05 operation issued so far by this
-// thread has completed.
-__device__ __forceinline__ void tc_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   smem_u32(bar))
-               : "memory");
-}
-
-// D(tmem) (+)= A(smem) * B(smem), bf16 inputs, fp32 accumulate.
-__device__ __forceinline__ void tc_mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// D(tmem) (+)= A(tmem) * B(smem).
-__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Warp-converged forms: all 32 lanes execute the instruction with the same
+// tcgen05.mma kind::f16 (bf16 A/B, fp32 accumulate in TMEM), issued in
+// warp-converged form: all 32 lanes execute the instruction with the same
 // (warp-uniform) operands and one elected lane issues it.  Keeping the whole
 // MMA warp converged lets the compiler hold descriptors and TMEM addresses in
 // uniform registers, which is what the tensor-core instructions read.
+// SS form: D(tmem) (+)= A(smem) * B(smem); TS form: A from TMEM.
 __device__ __forceinline__ void tc_mma_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                             uint32_t accumulate) {
   asm volatile(
@@ -307,6 +279,8 @@ __device__ __forceinline__ void tc_mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// Arrive once on `bar` when every tcgen05 operation issued so far by the
+// issuing lane has completed.
 __device__ __forceinline__ void tc_commit_w(uint64_t* bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\t"
@@ -314,142 +288,6 @@ __device__ __forceinline__ void tc_commit_w(uint64_t* bar) {
       "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
           smem_u32(bar))
       : "memory");
-}
-
-// ---------------------------------------------------------------------------
-// GEMM groups.  One call issues the whole K loop of a 128 x N product (8 or 4
-// MMAs of K = 16), commits it to up to two mbarriers and probes up to two other
-// mbarriers, all from one asm block run by the whole (converged) MMA warp with
-// one elected issuing lane.
-//
-// Why: issuing is the scarce resource of the MMA warp.  The tensor core needs
-// ~64 cycles per 128x128x16 MMA and holds only a few queued MMAs, while the
-// warp pays ~40 cycles per MMA issue, ~55 per commit and ~120-180 for the
-// result of every mbarrier wait even when the phase has already completed.
-// A probe (`mbarrier.test_wait`, non-blocking) is issued before the MMAs and
-// read after them, so its latency hides behind the issue; the caller then
-// waits for real only when the probe found the phase incomplete.
-//
-// Operand walks (descriptor address units are 16 bytes):
-//   SS, both operands K-major SW128 tiles: k-step kk at +(kk/4)*1024 + (kk%4)*2
-//   TS, B MN-major SW128 tile: k-step kk at +kk*128 (2048 bytes)
-//     A in TMEM as two 64-key halves (backward): +(kk/4)*64 + (kk%4)*8 columns
-//     A in TMEM contiguous (forward P):          +kk*8 columns
-// Commit / probe arguments are shared-memory addresses; 0 means none.
-// Returns bit 0 / bit 1 set when probe 0 / probe 1 found its phase complete
-// (per lane; see mma_probe_ready for the warp-uniform verdict).
-// ---------------------------------------------------------------------------
-
-#define FA_GRP_OPEN                                                        \
-  "{\n\t.reg .pred e, p, t, q0, q1, c;\n\t.reg .b64 a1, b1;\n\t.reg .b32 ta, r0, r1;\n\t" \
-  "setp.ne.b32 q0, %8, 0;\n\t"                                             \
-  "setp.ne.b32 q1, %10, 0;\n\t"                                            \
-  "@q0 mbarrier.test_wait.parity.shared::cta.b64 q0, [%8], %9;\n\t"        \
-  "@q1 mbarrier.test_wait.parity.shared::cta.b64 q1, [%10], %11;\n\t"      \
-  "elect.sync _|e, 0xffffffff;\n\t"                                        \
-  "setp.ne.b32 p, %5, 0;\n\t"                                              \
-  "setp.eq.b32 t, %4, %4;\n\t"
-#define FA_GRP_CLOSE                                                                          \
-  "setp.ne.and.b32 c, %6, 0, e;\n\t"                                                          \
-  "@c tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t"       \
-  "setp.ne.and.b32 c, %7, 0, e;\n\t"                                                          \
-  "@c tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%7];\n\t"       \
-  "selp.u32 r0, 1, 0, q0;\n\t"                                                                \
-  "selp.u32 r1, 2, 0, q1;\n\t"                                                                \
-  "or.b32 %0, r0, r1;\n\t}"
-#define FA_SS_FIRST "@e tcgen05.mma.cta_group::1.kind::f16 [%1], %2, %3, %4, p;\n\t"
-#define FA_SS_STEP(OFF)                         \
-  "add.s64 a1, %2, " OFF ";\n\t"                \
-  "add.s64 b1, %3, " OFF ";\n\t"                \
-  "@e tcgen05.mma.cta_group::1.kind::f16 [%1], a1, b1, %4, t;\n\t"
-#define FA_TS_FIRST "@e tcgen05.mma.cta_group::1.kind::f16 [%1], [%2], %3, %4, p;\n\t"
-#define FA_TS_STEP(AOFF, BOFF)                  \
-  "add.u32 ta, %2, " AOFF ";\n\t"               \
-  "add.s64 b1, %3, " BOFF ";\n\t"               \
-  "@e tcgen05.mma.cta_group::1.kind::f16 [%1], [ta], b1, %4, t;\n\t"
-#define FA_GRP_OPERANDS(A_CONSTRAINT)                                                                    \
-  : "=r"(ready)                                                                                          \
-  : "r"(d_tmem), A_CONSTRAINT(a), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(commit0), "r"(commit1), \
-    "r"(probe0), "r"(parity0), "r"(probe1), "r"(parity1)                                               \
-  : "memory"
-
-struct GrpSync {
-  uint32_t commit0 = 0, commit1 = 0;   // barriers to arrive on when the group completes
-  uint32_t probe0 = 0, parity0 = 0;    // barrier phases to probe
-  uint32_t probe1 = 0, parity1 = 0;
-};
-
-__device__ __forceinline__ uint32_t bar_addr(uint64_t* bar) { return smem_u32(bar); }
-
-// SS product with K = 128 (8 steps over two 64-element boxes) or K = 64 (4 steps).
-template <int KSTEPS>
-__device__ __forceinline__ uint32_t grp_ss(uint32_t d_tmem, uint64_t a, uint64_t b_desc, uint32_t idesc,
-                                           uint32_t accumulate, const GrpSync& s) {
-  static_assert(KSTEPS == 8 || KSTEPS == 4, "K steps");
-  uint32_t ready;
-  const uint32_t commit0 = s.commit0, commit1 = s.commit1, probe0 = s.probe0, parity0 = s.parity0,
-                 probe1 = s.probe1, parity1 = s.parity1;
-  if (KSTEPS == 8) {
-    asm volatile(FA_GRP_OPEN FA_SS_FIRST FA_SS_STEP("2") FA_SS_STEP("4") FA_SS_STEP("6") FA_SS_STEP("1024")
-                     FA_SS_STEP("1026") FA_SS_STEP("1028") FA_SS_STEP("1030") FA_GRP_CLOSE FA_GRP_OPERANDS("l"));
-  } else {
-    asm volatile(FA_GRP_OPEN FA_SS_FIRST FA_SS_STEP("2") FA_SS_STEP("4") FA_SS_STEP("6") FA_GRP_CLOSE
-                     FA_GRP_OPERANDS("l"));
-  }
-  return ready;
-}
-
-// TS product over 128 keys, A = bf16 operand in TMEM.  SPLIT: A stored as two
-// 64-key halves 64 columns apart (backward); otherwise contiguous (forward P).
-template <bool SPLIT>
-__device__ __forceinline__ uint32_t grp_ts(uint32_t d_tmem, uint32_t a, uint64_t b_desc, uint32_t idesc,
-                                           uint32_t accumulate, const GrpSync& s) {
-  uint32_t ready;
-  const uint32_t commit0 = s.commit0, commit1 = s.commit1, probe0 = s.probe0, parity0 = s.parity0,
-                 probe1 = s.probe1, parity1 = s.parity1;
-  if (SPLIT) {
-    asm volatile(FA_GRP_OPEN FA_TS_FIRST FA_TS_STEP("8", "128") FA_TS_STEP("16", "256") FA_TS_STEP("24", "384")
-                     FA_TS_STEP("64", "512") FA_TS_STEP("72", "640") FA_TS_STEP("80", "768")
-                         FA_TS_STEP("88", "896") FA_GRP_CLOSE FA_GRP_OPERANDS("r"));
-  } else {
-    asm volatile(FA_GRP_OPEN FA_TS_FIRST FA_TS_STEP("8", "128") FA_TS_STEP("16", "256") FA_TS_STEP("24", "384")
-                     FA_TS_STEP("32", "512") FA_TS_STEP("40", "640") FA_TS_STEP("48", "768")
-                         FA_TS_STEP("56", "896") FA_GRP_CLOSE FA_GRP_OPERANDS("r"));
-  }
-  return ready;
-}
-
-#undef FA_GRP_OPEN
-#undef FA_GRP_CLOSE
-#undef FA_SS_FIRST
-#undef FA_SS_STEP
-#undef FA_TS_FIRST
-#undef FA_TS_STEP
-#undef FA_GRP_OPERANDS
-
-// Warp-uniform verdict of probe bits: true only if every lane saw every phase
-// in `bits` complete (otherwise the whole warp falls back to real waits).
-__device__ __forceinline__ bool mma_probe_ready(uint32_t ready, uint32_t bits) {
-  return __all_sync(0xffffffffu, (ready & bits) == bits);
-}
-
-// Wait by one lane for a whole warp: lane 0 polls the barrier, the others
-// take its verdict and are ordered after its acquire by the warp barrier.
-// (Fewer threads polling and arriving keeps the barrier unit free for the
-// MMA warp, whose waits sit on the tensor core's critical path.)
-__device__ __forceinline__ bool mbar_wait_lane0(uint64_t* bar, uint32_t parity, const CtaGuard& g,
-                                                uint32_t site) {
-  int ok = 1;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, g, site) ? 1 : 0;
-  ok = __shfl_sync(0xffffffffu, ok, 0);
-  __syncwarp();
-  return ok != 0;
-}
-
-// One arrival for a whole warp, after every lane's prior work (warp barrier).
-__device__ __forceinline__ void mbar_arrive_warp(uint64_t* bar) {
-  __syncwarp();
-  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
 // Bounded wait by a whole warp (every lane polls: measured faster than one
@@ -608,10 +446,6 @@ __device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
   float4 v;
   asm("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
   return v;
-}
-
-__device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {

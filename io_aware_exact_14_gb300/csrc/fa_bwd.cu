@@ -234,9 +234,10 @@ struct DkdvCfg {
   static constexpr uint32_t kLseOff = kDOOff + kDOStages * kTileBytes;   // 128 fp32 per Q stage
   static constexpr uint32_t kDVecOff = kLseOff + kQStages * 512;          // 128 fp32 per dO stage
   static constexpr uint32_t kBarOff = kDVecOff + kDOStages * 512;
-  // res_full, q_full[3], q_empty[3], do_full[2], do_empty[2], s_full, dp_full, p_full, ds_full,
-  // acc_done, drain, staged[2]
-  static constexpr int kBars = 1 + 2 * kQStages + 2 * kDOStages + 8;
+  // res_full, q_full[3], q_empty[3], do_full[2], s_full, dp_full, p_full, ds_full, acc_done, drain,
+  // staged[2].  A dO slot has no empty barrier of its own: dO_i's last reader
+  // (dV(i)) finishes before dK(i), whose commit already releases Q_i's slot.
+  static constexpr int kBars = 1 + 2 * kQStages + kDOStages + 8;
   static constexpr uint32_t kMiscOff = kBarOff + kBars * 8;
   static constexpr uint32_t kLayoutBytes = kMiscOff + 16;
   static constexpr uint32_t kMaxSmem = BwdCfg<D>::kMaxSmem;
@@ -271,8 +272,7 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* q_full = bars + 1;
   uint64_t* q_empty = q_full + C::kQStages;
   uint64_t* do_full = q_empty + C::kQStages;
-  uint64_t* do_empty = do_full + C::kDOStages;
-  uint64_t* s_full = do_empty + C::kDOStages;
+  uint64_t* s_full = do_full + C::kDOStages;
   uint64_t* dp_full = s_full + 1;
   uint64_t* p_full = dp_full + 1;
   uint64_t* ds_full = p_full + 1;
@@ -297,7 +297,6 @@ __global__ void __launch_bounds__(384, 1)
     }
     for (int i = 0; i < C::kDOStages; ++i) {
       mbar_init(&do_full[i], 2);    // TMA bytes + the producer warp's -D writes
-      mbar_init(&do_empty[i], 1);
     }
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
@@ -353,7 +352,12 @@ __global__ void __launch_bounds__(384, 1)
         for (int k = 0; k < 4; ++k) nl[lane + 32 * k] = rv.a[k];
         __syncwarp();
         if (lane == 0) mbar_arrive(&q_full[qs]);
-        if (lane == 0) ok = mbar_wait(&do_empty[ds], ((it / C::kDOStages) & 1u) ^ 1u, g, kSiteDkdv | 12u);
+        // dO slot reuse: tile it - 2's dK (after its dV) has completed, which
+        // the q_empty commit of that tile signals
+        if (lane == 0 && it >= C::kDOStages) {
+          const int pt = it - C::kDOStages;
+          ok = mbar_wait(&q_empty[pt % C::kQStages], (pt / C::kQStages) & 1u, g, kSiteDkdv | 12u);
+        }
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
         if (lane == 0) {
           mbar_arrive_expect_tx(&do_full[ds], C::kTileBytes);
@@ -413,8 +417,7 @@ __global__ void __launch_bounds__(384, 1)
           } else {
             tc_fence_after();
             mma_tn_acc<D>(tDK, tDP, mQ(qs), it > 0);        // dK += dS^T Q_i
-            tc_commit_w(&q_empty[qs]);                     // Q_i, -lse_i: last reader done
-            tc_commit_w(&do_empty[ds]);                    // dO_i (dP^T, dV), -D_i (read before dS)
+            tc_commit_w(&q_empty[qs]);                     // Q_i, -lse_i, and dO_i, -D_i: last readers done
             k_done = true;
           }
         }
@@ -569,9 +572,10 @@ struct DqCfg {
   static constexpr uint32_t kKOff = 2 * kTileBytes;
   static constexpr uint32_t kVOff = kKOff + kKStages * kTileBytes;
   static constexpr uint32_t kBarOff = kVOff + kVStages * kTileBytes;
-  // q_full, q_empty, do_full, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full, s_free,
-  // dp_full, ds_full, acc_done, acc_free, staged, drain, sched, id_taken
-  static constexpr int kBars = 3 + 2 * kKStages + 2 * kVStages + 10;
+  // q_full, q_empty, do_full, k_full[3], k_empty[3], v_full[2], s_full, s_free, dp_full, ds_full,
+  // acc_done, acc_free, staged, drain, sched, id_taken.  A V slot has no empty
+  // barrier of its own: dP(j) is issued before dQ(j), whose commit releases K_j.
+  static constexpr int kBars = 3 + 2 * kKStages + kVStages + 10;
   // readers of a unit id: the MMA warp, the eight compute warps, the dO loader
   static constexpr uint32_t kIdReaders = 10;
   static constexpr uint32_t kMiscOff = kBarOff + kBars * 8;   // tmem holder, abort flag, unit ids [2]
@@ -623,8 +627,7 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* k_full = bars + 3;
   uint64_t* k_empty = k_full + C::kKStages;
   uint64_t* v_full = k_empty + C::kKStages;
-  uint64_t* v_empty = v_full + C::kVStages;
-  uint64_t* s_full = v_empty + C::kVStages;
+  uint64_t* s_full = v_full + C::kVStages;
   uint64_t* s_free = s_full + 1;
   uint64_t* dp_full = s_free + 1;
   uint64_t* ds_full = dp_full + 1;
@@ -651,10 +654,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
     }
-    for (int i = 0; i < C::kVStages; ++i) {
-      mbar_init(&v_full[i], 1);
-      mbar_init(&v_empty[i], 1);
-    }
+    for (int i = 0; i < C::kVStages; ++i) mbar_init(&v_full[i], 1);
     mbar_init(s_full, 1);
     mbar_init(s_free, 256);
     mbar_init(dp_full, 1);
@@ -710,7 +710,12 @@ __global__ void __launch_bounds__(384, 1)
             for (int b = 0; b < BwdCfg<D>::kBoxes; ++b)
               tma_load_3d(smem + C::k_off(ks) + b * BwdCfg<D>::kBoxBytes, &tmK, &k_full[ks], 64 * b, 128 * it,
                           w.bh);
-            if (!(ok = mbar_wait(&v_empty[vs], vpar(gk) ^ 1u, g, kSiteDq | 11u))) break;
+            // V slot reuse: the dQ of key tile gk - 2 (issued after that tile's
+            // dP) has completed, which its k_empty commit signals
+            if (gk >= C::kVStages &&
+                !(ok = mbar_wait(&k_empty[(gk - C::kVStages) % C::kKStages], kpar(gk - C::kVStages), g,
+                                 kSiteDq | 11u)))
+              break;
             mbar_arrive_expect_tx(&v_full[vs], C::kTileBytes);
             for (int b = 0; b < BwdCfg<D>::kBoxes; ++b)
               tma_load_3d(smem + C::v_off(vs) + b * BwdCfg<D>::kBoxBytes, &tmV, &v_full[vs], 64 * b, 128 * it,
@@ -793,7 +798,6 @@ __global__ void __launch_bounds__(384, 1)
         if (!(ok = mbar_wait_w(do_full, su & 1, g, kSiteDq | 19u))) break;
         mma_nt<D>(tDP, kDO, kV(g0 % C::kVStages));
         tc_commit_w(dp_full);
-        tc_commit_w(&v_empty[g0 % C::kVStages]);
         for (int it = 0; it < cnt; ++it) {
           const int j = g0 + it;   // global index of key tile it
           const uint32_t par = j & 1;
@@ -827,7 +831,6 @@ __global__ void __launch_bounds__(384, 1)
           if (!(ok = mbar_wait_w(&v_full[(j + 1) % C::kVStages], vpar(j + 1), g, kSiteDq | 12u))) break;
           mma_nt<D>(tDP, kDO, kV((j + 1) % C::kVStages));
           tc_commit_w(dp_full);
-          tc_commit_w(&v_empty[(j + 1) % C::kVStages]);
         }
         gk = g0 + cnt;
       }

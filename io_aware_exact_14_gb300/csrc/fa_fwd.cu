@@ -56,8 +56,12 @@ struct FwdCfg {
   static constexpr uint32_t kQOff = 0;
   static constexpr uint32_t kSlotOff = 2 * kTileBytes;
   static constexpr uint32_t kBarOff = kSlotOff + kSlots * kTileBytes;
-  // full[S], empty[S], q_full, s_full[2], p_full[2], o_done[2], drain, staged[2]
-  static constexpr int kBars = 2 * kSlots + 10;
+  // Ring slots are released in groups by one commit each: group 0 is K_0
+  // (after S(0)), group j+1 is {V_j, K_{j+1}} (after key step j), so a step
+  // costs the issuing warp one commit; group q uses release[q % kReleases].
+  static constexpr int kReleases = kSlots / 2;
+  // full[S], release[S/2], q_full, s_full[2], p_full[2], o_done[2], drain, staged[2]
+  static constexpr int kBars = kSlots + kReleases + 10;
   static constexpr uint32_t kMiscOff = kBarOff + kBars * 8;
   static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;  // + alignment slack
   static constexpr int kThreads = 384;
@@ -108,10 +112,12 @@ __device__ __forceinline__ void fwd_producer(const FwdWork& w, uint8_t* smem, ui
     for (int kind = 0; kind < 2; ++kind) {
       const int idx = 2 * j + kind;
       const int slot = idx % C::kSlots;
-      const uint32_t ph = (idx / C::kSlots) & 1;
-      if (!mbar_wait(&empty[slot], ph ^ 1u, g, kSiteFwd | 1u)) {
-        ok = false;
-        break;
+      if (idx >= C::kSlots) {   // the slot's previous tile, idx - kSlots, released with its group
+        const int q = (idx - C::kSlots + 1) >> 1;
+        if (!mbar_wait(&empty[q % C::kReleases], (q / C::kReleases) & 1u, g, kSiteFwd | 1u)) {
+          ok = false;
+          break;
+        }
       }
       if (j + kL2Ahead < w.n) {   // the same tile kL2Ahead steps on, into L2 while this one lands
 #pragma unroll
@@ -187,7 +193,7 @@ __device__ __forceinline__ void fwd_mma(const FwdWork& w, int tile, uint32_t tme
     fwd_issue_s<D>(t_s, q_desc, k_desc0 + slot_off(0));
     tc_commit_w(&s_full[tile]);
   }
-  tc_commit_w(&empty[0]);
+  tc_commit_w(&empty[0]);   // group 0: K_0
   for (int j = 0; j < w.n; ++j) {
     const int iv = 2 * j + 1, ik = 2 * j + 2;
     const bool next = j + 1 < w.n;
@@ -204,8 +210,7 @@ __device__ __forceinline__ void fwd_mma(const FwdWork& w, int tile, uint32_t tme
         tc_commit_w(&o_done[tile]);
       }
     }
-    tc_commit_w(&empty[iv % C::kSlots]);
-    if (next) tc_commit_w(&empty[ik % C::kSlots]);
+    tc_commit_w(&empty[(j + 1) % C::kReleases]);   // group j+1: V_j and K_{j+1}
   }
 }
 
@@ -241,7 +246,7 @@ __device__ __forceinline__ void fwd_mma_both(const FwdWork& w, uint32_t tmem, ui
     fwd_issue_s<D>(tmem + C::col_s(1), q_desc[1], k_desc0 + slot_off(0));
     tc_commit_w(&s_full[1]);
   }
-  tc_commit_w(&empty[0]);
+  tc_commit_w(&empty[0]);   // group 0: K_0
   for (int j = 0; j < w.n; ++j) {
     const int iv = 2 * j + 1, ik = 2 * j + 2;
     const bool next = j + 1 < w.n;
@@ -264,8 +269,7 @@ __device__ __forceinline__ void fwd_mma_both(const FwdWork& w, uint32_t tmem, ui
       if (j == w.n1 - 1) tc_commit_w(&o_done[1]);
       if (next && j + 1 < w.n1) tc_commit_w(&s_full[1]);
     }
-    tc_commit_w(&empty[iv % C::kSlots]);
-    if (next) tc_commit_w(&empty[ik % C::kSlots]);
+    tc_commit_w(&empty[(j + 1) % C::kReleases]);   // group j+1: V_j and K_{j+1}
   }
 }
 
@@ -414,8 +418,8 @@ __global__ void __launch_bounds__(384, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
   uint64_t* full = bars;
-  uint64_t* empty = bars + C::kSlots;
-  uint64_t* q_full = bars + 2 * C::kSlots;
+  uint64_t* empty = bars + C::kSlots;   // release[kReleases]
+  uint64_t* q_full = empty + C::kReleases;
   uint64_t* s_full = q_full + 1;
   uint64_t* p_full = s_full + 2;
   uint64_t* o_done = p_full + 2;
@@ -429,10 +433,8 @@ __global__ void __launch_bounds__(384, 1)
   const FwdWork w = fwd_work(N, n_pairs, BH, band, CAUSAL);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::kSlots; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], ISSUERS);   // released by every issuing warp
-    }
+    for (int i = 0; i < C::kSlots; ++i) mbar_init(&full[i], 1);
+    for (int i = 0; i < C::kReleases; ++i) mbar_init(&empty[i], ISSUERS);   // by every issuing warp
     mbar_init(q_full, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);

@@ -56,12 +56,14 @@ struct FwdCfg {
   static constexpr uint32_t kQOff = 0;
   static constexpr uint32_t kSlotOff = 2 * kTileBytes;
   static constexpr uint32_t kBarOff = kSlotOff + kSlots * kTileBytes;
-  // Ring slots are released in groups by one commit each: group 0 is K_0
-  // (after S(0)), group j+1 is {V_j, K_{j+1}} (after key step j), so a step
-  // costs the issuing warp one commit; group q uses release[q % kReleases].
-  static constexpr int kReleases = kSlots / 2;
-  // full[S], release[S/2], q_full, s_full[2], p_full[2], o_done[2], drain, staged[2]
-  static constexpr int kBars = kSlots + kReleases + 10;
+  // Ring tiles travel in groups: group 0 is K_0, group j+1 is {V_j, K_{j+1}},
+  // the tiles key step j needs beyond those it already has.  A group lands on
+  // one full barrier and is released by one commit, so a key step costs the
+  // issuing warp one wait and one commit for its operands; group q uses
+  // gfull[q % kGroups] and release[q % kGroups].
+  static constexpr int kGroups = kSlots / 2;
+  // gfull[G], release[G], q_full, s_full[2], p_full[2], o_done[2], drain, staged[2]
+  static constexpr int kBars = 2 * kGroups + 10;
   static constexpr uint32_t kMiscOff = kBarOff + kBars * 8;
   static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;  // + alignment slack
   static constexpr int kThreads = 384;
@@ -106,35 +108,38 @@ __device__ __forceinline__ void fwd_producer(const FwdWork& w, uint8_t* smem, ui
       tma_load_3d(smem + C::kQOff + C::kTileBytes + b * C::kBoxBytes, tmQ, q_full, 64 * b, 128 * (w.qt0 + 1),
                   w.bh);
   }
-  int issued = 0;
+  int issued = 0;   // tiles whose load was issued
   bool ok = true;
   for (int j = 0; j < w.n && ok; ++j) {
-    for (int kind = 0; kind < 2; ++kind) {
+    for (int kind = 0; kind < 2; ++kind) {   // K_j (group j), then V_j (group j+1)
       const int idx = 2 * j + kind;
-      const int slot = idx % C::kSlots;
-      if (idx >= C::kSlots) {   // the slot's previous tile, idx - kSlots, released with its group
-        const int q = (idx - C::kSlots + 1) >> 1;
-        if (!mbar_wait(&empty[q % C::kReleases], (q / C::kReleases) & 1u, g, kSiteFwd | 1u)) {
+      const int grp = (idx + 1) >> 1;
+      if (kind == 1 || j == 0) {
+        // first tile of its group: wait until the group that last used these
+        // two slots (grp - kGroups) is released, then expect the whole group
+        if (grp >= C::kGroups &&
+            !mbar_wait(&empty[grp % C::kGroups], ((grp / C::kGroups) - 1) & 1u, g, kSiteFwd | 1u)) {
           ok = false;
           break;
         }
+        const bool pair = grp > 0 && grp < w.n;   // group n holds V_{n-1} alone
+        mbar_arrive_expect_tx(&full[grp % C::kGroups], (pair ? 2u : 1u) * C::kTileBytes);
       }
       if (j + kL2Ahead < w.n) {   // the same tile kL2Ahead steps on, into L2 while this one lands
 #pragma unroll
         for (int b = 0; b < C::kBoxes; ++b) tma_prefetch_l2_3d(kind ? tmV : tmK, 64 * b, 128 * (j + kL2Ahead), w.bh);
       }
-      mbar_arrive_expect_tx(&full[slot], C::kTileBytes);
-      uint8_t* dst = smem + C::kSlotOff + slot * C::kTileBytes;
+      uint8_t* dst = smem + C::kSlotOff + (idx % C::kSlots) * C::kTileBytes;
 #pragma unroll
       for (int b = 0; b < C::kBoxes; ++b)
-        tma_load_3d(dst + b * C::kBoxBytes, kind ? tmV : tmK, &full[slot], 64 * b, 128 * j, w.bh);
+        tma_load_3d(dst + b * C::kBoxBytes, kind ? tmV : tmK, &full[grp % C::kGroups], 64 * b, 128 * j, w.bh);
       issued = idx + 1;
     }
   }
-  if (!ok) {  // unwinding: let copies already issued land before smem is released
+  if (!ok) {  // unwinding: let copies already issued land before smem is released (bounded waits)
     mbar_drain(q_full, 0);
-    for (int idx = max(0, issued - C::kSlots); idx < issued; ++idx)
-      mbar_drain(&full[idx % C::kSlots], (idx / C::kSlots) & 1);
+    for (int q = max(0, ((issued + 1) >> 1) - C::kGroups); q <= (issued >> 1); ++q)
+      if (2 * q - 1 < issued || q == 0) mbar_drain(&full[q % C::kGroups], (q / C::kGroups) & 1);
   }
 }
 
@@ -184,21 +189,19 @@ __device__ __forceinline__ void fwd_mma(const FwdWork& w, int tile, uint32_t tme
   const uint64_t v_desc0 = sdesc_sw128(smem_base + C::kSlotOff, C::kBoxBytes, 1024);
   const uint32_t t_s = tmem + C::col_s(tile), t_o = tmem + C::col_o(tile);
   auto slot_off = [&](int idx) { return static_cast<uint64_t>((idx % C::kSlots) * (C::kTileBytes >> 4)); };
-  auto slot_wait = [&](int idx) {
-    return mbar_wait_w(&full[idx % C::kSlots], (idx / C::kSlots) & 1, g, kSiteFwd | 2u);
+  auto group_wait = [&](int grp) {   // group 0: K_0; group j+1: V_j and K_{j+1}
+    return mbar_wait_w(&full[grp % C::kGroups], (grp / C::kGroups) & 1, g, kSiteFwd | 2u);
   };
   if (!mbar_wait_w(q_full, 0, g, kSiteFwd | 3u)) return;
-  if (!slot_wait(0)) return;
+  if (!group_wait(0)) return;
   if (n_t > 0) {
     fwd_issue_s<D>(t_s, q_desc, k_desc0 + slot_off(0));
     tc_commit_w(&s_full[tile]);
   }
   tc_commit_w(&empty[0]);   // group 0: K_0
   for (int j = 0; j < w.n; ++j) {
-    const int iv = 2 * j + 1, ik = 2 * j + 2;
-    const bool next = j + 1 < w.n;
-    if (!slot_wait(iv)) return;
-    if (next && !slot_wait(ik)) return;
+    const int iv = 2 * j + 1, ik = 2 * j + 2;   // ring indices of V_j and K_{j+1}
+    if (!group_wait(j + 1)) return;
     if (j < n_t) {
       if (!mbar_wait_w(&p_full[tile], j & 1, g, tile ? (kSiteFwd | 5u) : (kSiteFwd | 4u))) return;
       tc_fence_after();
@@ -210,7 +213,7 @@ __device__ __forceinline__ void fwd_mma(const FwdWork& w, int tile, uint32_t tme
         tc_commit_w(&o_done[tile]);
       }
     }
-    tc_commit_w(&empty[(j + 1) % C::kReleases]);   // group j+1: V_j and K_{j+1}
+    tc_commit_w(&empty[(j + 1) % C::kGroups]);   // group j+1: V_j and K_{j+1}
   }
 }
 
@@ -233,11 +236,11 @@ __device__ __forceinline__ void fwd_mma_both(const FwdWork& w, uint32_t tmem, ui
   const uint64_t k_desc0 = sdesc_sw128(smem_base + C::kSlotOff, 16, 1024);
   const uint64_t v_desc0 = sdesc_sw128(smem_base + C::kSlotOff, C::kBoxBytes, 1024);
   auto slot_off = [&](int idx) { return static_cast<uint64_t>((idx % C::kSlots) * (C::kTileBytes >> 4)); };
-  auto slot_wait = [&](int idx) {
-    return mbar_wait_w(&full[idx % C::kSlots], (idx / C::kSlots) & 1, g, kSiteFwd | 2u);
+  auto group_wait = [&](int grp) {   // group 0: K_0; group j+1: V_j and K_{j+1}
+    return mbar_wait_w(&full[grp % C::kGroups], (grp / C::kGroups) & 1, g, kSiteFwd | 2u);
   };
   if (!mbar_wait_w(q_full, 0, g, kSiteFwd | 3u)) return;
-  if (!slot_wait(0)) return;
+  if (!group_wait(0)) return;
   if (w.n0 > 0) {
     fwd_issue_s<D>(tmem + C::col_s(0), q_desc[0], k_desc0 + slot_off(0));
     tc_commit_w(&s_full[0]);
@@ -250,8 +253,7 @@ __device__ __forceinline__ void fwd_mma_both(const FwdWork& w, uint32_t tmem, ui
   for (int j = 0; j < w.n; ++j) {
     const int iv = 2 * j + 1, ik = 2 * j + 2;
     const bool next = j + 1 < w.n;
-    if (!slot_wait(iv)) return;
-    if (next && !slot_wait(ik)) return;
+    if (!group_wait(j + 1)) return;
     const uint64_t vd = v_desc0 + slot_off(iv), kd = k_desc0 + slot_off(ik);
     if (j < w.n0) {
       if (!mbar_wait_w(&p_full[0], j & 1, g, kSiteFwd | 4u)) return;
@@ -269,7 +271,7 @@ __device__ __forceinline__ void fwd_mma_both(const FwdWork& w, uint32_t tmem, ui
       if (j == w.n1 - 1) tc_commit_w(&o_done[1]);
       if (next && j + 1 < w.n1) tc_commit_w(&s_full[1]);
     }
-    tc_commit_w(&empty[(j + 1) % C::kReleases]);   // group j+1: V_j and K_{j+1}
+    tc_commit_w(&empty[(j + 1) % C::kGroups]);   // group j+1: V_j and K_{j+1}
   }
 }
 
@@ -417,9 +419,9 @@ __global__ void __launch_bounds__(384, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
-  uint64_t* full = bars;
-  uint64_t* empty = bars + C::kSlots;   // release[kReleases]
-  uint64_t* q_full = empty + C::kReleases;
+  uint64_t* full = bars;                   // gfull[kGroups]
+  uint64_t* empty = bars + C::kGroups;     // release[kGroups]
+  uint64_t* q_full = empty + C::kGroups;
   uint64_t* s_full = q_full + 1;
   uint64_t* p_full = s_full + 2;
   uint64_t* o_done = p_full + 2;
@@ -433,8 +435,10 @@ __global__ void __launch_bounds__(384, 1)
   const FwdWork w = fwd_work(N, n_pairs, BH, band, CAUSAL);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::kSlots; ++i) mbar_init(&full[i], 1);
-    for (int i = 0; i < C::kReleases; ++i) mbar_init(&empty[i], ISSUERS);   // by every issuing warp
+    for (int i = 0; i < C::kGroups; ++i) {
+      mbar_init(&full[i], 1);          // one expect-tx arrival per group
+      mbar_init(&empty[i], ISSUERS);   // one commit per issuing warp
+    }
     mbar_init(q_full, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);

@@ -572,9 +572,11 @@ struct DqCfg {
   static constexpr uint32_t kKOff = 2 * kTileBytes;
   static constexpr uint32_t kVOff = kKOff + kKStages * kTileBytes;
   static constexpr uint32_t kBarOff = kVOff + kVStages * kTileBytes;
-  // q_full, q_empty, do_full, k_full[3], k_empty[3], v_full[2], s_full, s_free, dp_full, ds_full,
+  // q_full, q_empty, do_full, k_full[3], k_empty[3], v_full[2], s_full[2], dp_full, ds_full,
   // acc_done, acc_free, staged, drain, sched, id_taken.  A V slot has no empty
   // barrier of its own: dP(j) is issued before dQ(j), whose commit releases K_j.
+  // One s_full per S buffer: its next phase (tile j+2) needs this tile's dS(j)
+  // first, so no barrier runs two phases ahead of a compute warp's wait.
   static constexpr int kBars = 3 + 2 * kKStages + kVStages + 10;
   // readers of a unit id: the MMA warp, the eight compute warps, the dO loader
   static constexpr uint32_t kIdReaders = 10;
@@ -586,7 +588,13 @@ struct DqCfg {
   static_assert(kLayoutBytes <= kMaxSmem, "dQ shared-memory layout too large");
   static constexpr int kThreads = 384;
   static constexpr int kRequestAhead = 5;   // key tiles before a unit's end at which the next is requested
-  static constexpr uint32_t kColS = 0, kColDP = 128, kColAcc = 256;
+  // TMEM: S double-buffered (tile j in buffer j & 1), dP, dQ accumulator.  S(j+1)
+  // never overwrites the S the compute warps are reading, and S(j+2) is issued
+  // only after the MMA warp has seen dS(j) (so S(j) was read long before): no
+  // "S read" barrier is needed.
+  static constexpr uint32_t kColS0 = 0, kColDP = 128, kColAcc = 256, kColS1 = 384;
+  static_assert(kColAcc + D <= kColS1, "TMEM layout");
+  __host__ __device__ static constexpr uint32_t col_s(int j) { return (j & 1) ? kColS1 : kColS0; }
   __host__ __device__ static constexpr uint32_t k_off(int s) { return kKOff + s * kTileBytes; }
   __host__ __device__ static constexpr uint32_t v_off(int s) { return kVOff + s * kTileBytes; }
 };
@@ -628,8 +636,7 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* k_empty = k_full + C::kKStages;
   uint64_t* v_full = k_empty + C::kKStages;
   uint64_t* s_full = v_full + C::kVStages;
-  uint64_t* s_free = s_full + 1;
-  uint64_t* dp_full = s_free + 1;
+  uint64_t* dp_full = s_full + 2;   // s_full[2], by S buffer
   uint64_t* ds_full = dp_full + 1;
   uint64_t* acc_done = ds_full + 1;
   uint64_t* acc_free = acc_done + 1;
@@ -655,8 +662,8 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&k_empty[i], 1);
     }
     for (int i = 0; i < C::kVStages; ++i) mbar_init(&v_full[i], 1);
-    mbar_init(s_full, 1);
-    mbar_init(s_free, 256);
+    mbar_init(&s_full[0], 1);
+    mbar_init(&s_full[1], 1);
     mbar_init(dp_full, 1);
     mbar_init(ds_full, 256);
     mbar_init(acc_done, 1);
@@ -769,7 +776,7 @@ __global__ void __launch_bounds__(384, 1)
         tma_store_wait_all();   // the last stores have landed before the CTA retires
       }
     } else if (warp == 9) {  // MMA issuer: the whole warp runs the loop, one lane issues
-      const uint32_t tS = tmem + C::kColS, tDP = tmem + C::kColDP, tDQ = tmem + C::kColAcc;
+      const uint32_t tDP = tmem + C::kColDP, tDQ = tmem + C::kColAcc;
       const uint64_t kQ = kmaj<D>(sbase + C::kQOff), kDO = kmaj<D>(sbase + C::kDOOff);
       // K stages as K-major B operands (S) and MN-major B operands (dQ); V stages K-major (dP)
       auto kK = [&](int s) { return kmaj<D>(sbase + C::k_off(s)); };
@@ -788,12 +795,12 @@ __global__ void __launch_bounds__(384, 1)
         if (lane == 0) mbar_arrive(id_taken);
         const int cnt = dq_unit<CAUSAL>(u, n_tiles, BH, band).cnt;
         const int g0 = gk;   // this unit's first global key tile
-        // S(0): its K tile and the previous S read out of TMEM
+        // S(0): its K tile (its S buffer was read before the dS the previous
+        // unit's last dQ waited for)
         if (!(ok = mbar_wait_w(&k_full[g0 % C::kKStages], kpar(g0), g, kSiteDq | 3u))) break;
-        if (g0 > 0 && !(ok = mbar_wait_w(s_free, (g0 - 1) & 1, g, kSiteDq | 5u))) break;
         tc_fence_after();
-        mma_nt<D>(tS, kQ, kK(g0 % C::kKStages));
-        tc_commit_w(s_full);
+        mma_nt<D>(tmem + C::col_s(g0), kQ, kK(g0 % C::kKStages));
+        tc_commit_w(&s_full[g0 & 1]);
         if (!(ok = mbar_wait_w(&v_full[g0 % C::kVStages], vpar(g0), g, kSiteDq | 3u))) break;
         if (!(ok = mbar_wait_w(do_full, su & 1, g, kSiteDq | 19u))) break;
         mma_nt<D>(tDP, kDO, kV(g0 % C::kVStages));
@@ -802,12 +809,11 @@ __global__ void __launch_bounds__(384, 1)
           const int j = g0 + it;   // global index of key tile it
           const uint32_t par = j & 1;
           const bool next = it + 1 < cnt;
-          if (next) {   // S(j+1)
+          if (next) {   // S(j+1), into the other S buffer
             if (!(ok = mbar_wait_w(&k_full[(j + 1) % C::kKStages], kpar(j + 1), g, kSiteDq | 4u))) break;
-            if (!(ok = mbar_wait_w(s_free, par, g, kSiteDq | 5u))) break;
             tc_fence_after();
-            mma_nt<D>(tS, kQ, kK((j + 1) % C::kKStages));
-            tc_commit_w(s_full);
+            mma_nt<D>(tmem + C::col_s(j + 1), kQ, kK((j + 1) % C::kKStages));
+            tc_commit_w(&s_full[(j + 1) & 1]);
           } else {
             tc_commit_w(q_empty);   // every reader of Q_i has been issued
           }
@@ -849,7 +855,6 @@ __global__ void __launch_bounds__(384, 1)
   const int h = warp >> 2;
   const int r = threadIdx.x & 127;
   const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-  const uint32_t tS = tmem + lane_base + C::kColS + 64 * h;
   const uint32_t tDP = tmem + lane_base + C::kColDP + 64 * h;
   const float2 sc2 = make_float2(scale_log2, scale_log2);
   bool ok = true;
@@ -872,16 +877,15 @@ __global__ void __launch_bounds__(384, 1)
     const float2 nl2 = make_float2(nlse2, nlse2), nd2 = make_float2(ndrow, ndrow);
     for (int it = 0; ok && it < w.cnt; ++it, ++gk) {
       const uint32_t par = gk & 1;
-      if (!(ok = mbar_wait(s_full, par, g, kSiteDq | 7u))) break;
+      if (!(ok = mbar_wait(&s_full[gk & 1], (gk >> 1) & 1, g, kSiteDq | 7u))) break;
       __syncwarp();
       tc_fence_after();
+      const uint32_t tS = tmem + lane_base + C::col_s(gk) + 64 * h;
       uint32_t sr[2][32];
       tmem_ld32(tS, sr[0]);
       tmem_ld32(tS + 32, sr[1]);
       tmem_ld_wait(sr[0]);
       tmem_ld_fence(sr[1]);
-      tc_fence_before();
-      mbar_arrive(s_free);   // S(j) is in registers: the tensor core may overwrite it
       // keys k0 .. k0+lim-1 of this half are visible to the row
       const int k0 = 128 * it + 64 * h;
       int lim = N - k0;

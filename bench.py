@@ -313,47 +313,76 @@ def run_ours(args, dist: Dist):
 
 
 def run_e2e(args, w, causal, x, dev, dist, flops_step):
-    """Same step through the public API with host buffers: pinned H2D copies of
-    q, k, v, dO and D2H copies of O, LSE, dQ, dK, dV inside the timed region."""
+    """Same step through the public API with host buffers, as a training loop
+    would run it: every step copies q, k, v, dO from pinned host memory to the
+    device and O, LSE, dQ, dK, dV back, all inside the timed region.  The loop
+    is pipelined over two device buffer sets and three streams (copy in,
+    compute, copy out, ordered by events), so step s+1's inputs travel while
+    step s computes and step s-1's results travel back."""
     import torch
     from io_aware_exact_14_gb300 import fa
     B, H, N, d = w.shape
     h_in = [x[n].pin_memory() for n in ("q", "k", "v", "do")]
-    d_in = [torch.empty_like(t, device=dev) for t in h_in]
     h_out = [torch.empty((B, H, N, d), dtype=torch.bfloat16).pin_memory() for _ in range(4)]
     h_lse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
     ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
-    o = torch.empty_like(d_in[0])
-    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-    g = [torch.empty_like(d_in[0]) for _ in range(3)]
+    # two device buffer sets: inputs q, k, v, dO; outputs O, dQ, dK, dV and LSE
+    d_in = [[torch.empty_like(t, device=dev) for t in h_in] for _ in range(2)]
+    d_out = [[torch.empty_like(d_in[0][0]) for _ in range(4)] for _ in range(2)]
+    d_lse = [torch.empty((B, H, N), dtype=torch.float32, device=dev) for _ in range(2)]
+    s_in, s_comp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()
+    in_done = [ev(), ev()]
+    comp_done = [ev(), ev()]
+    out_done = [ev(), ev()]
+    started = [False, False]
 
-    def step():
-        for hd, dd in zip(h_in, d_in):
-            dd.copy_(hd, non_blocking=True)
-        fa.fa_fwd(d_in[0], d_in[1], d_in[2], w.scale, causal, out=o, lse=lse)
-        fa.fa_bwd(d_in[0], d_in[1], d_in[2], o, lse, d_in[3], w.scale, causal, dq=g[0], dk=g[1], dv=g[2],
-                  workspace=ws)
-        for hd, dd in zip(h_out, [o] + g):
-            hd.copy_(dd, non_blocking=True)
-        h_lse.copy_(lse, non_blocking=True)
+    def step(i):
+        b = i % 2
+        with torch.cuda.stream(s_in):
+            if started[b]:
+                s_in.wait_event(comp_done[b])      # step i-2 has finished reading these inputs
+            for hd, dd in zip(h_in, d_in[b]):
+                dd.copy_(hd, non_blocking=True)
+            in_done[b].record(s_in)
+        with torch.cuda.stream(s_comp):
+            s_comp.wait_event(in_done[b])
+            if started[b]:
+                s_comp.wait_event(out_done[b])     # step i-2's results have left these outputs
+            q, k, v, do = d_in[b]
+            o, dq, dk, dv = d_out[b]
+            fa.fa_fwd(q, k, v, w.scale, causal, out=o, lse=d_lse[b], stream=s_comp)
+            fa.fa_bwd(q, k, v, o, d_lse[b], do, w.scale, causal, dq=dq, dk=dk, dv=dv, workspace=ws,
+                      stream=s_comp)
+            comp_done[b].record(s_comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(comp_done[b])
+            for hd, dd in zip(h_out, d_out[b]):
+                hd.copy_(dd, non_blocking=True)
+            h_lse.copy_(d_lse[b], non_blocking=True)
+            out_done[b].record(s_out)
+        started[b] = True
 
-    steps = max(1, min(args.steps, 10))
-    for _ in range(max(1, min(args.warmup, 3))):
-        step()
+    steps = max(2, min(args.steps, 10))
+    for i in range(max(2, min(args.warmup, 4))):
+        step(i)
     torch.cuda.synchronize()
     dist.barrier()
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.record()
-    for _ in range(steps):
-        step()
-    e.record()
+    s.record(s_in)
+    for i in range(steps):
+        step(i)
+    # the timed region ends when the last results are on the host
+    s_out.wait_stream(s_in)
+    s_out.wait_stream(s_comp)
+    e.record(s_out)
     torch.cuda.synchronize()
     ms = dist.max(s.elapsed_time(e))
     h2d = sum(t.numel() * t.element_size() for t in h_in)
     d2h = sum(t.numel() * t.element_size() for t in h_out) + h_lse.numel() * 4
     return {"value": round(flops_step * dist.world * steps / (ms * 1e-3) / 1e12, 2), "unit": UNIT,
             "steps": steps, "ms_per_step": round(ms / steps, 4), "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h}
+            "d2h_bytes_per_step": d2h, "pipelined": "2 buffer sets, copy-in / compute / copy-out streams"}
 
 
 # ---------------------------------------------------------------------------

@@ -86,12 +86,15 @@ __global__ void __launch_bounds__(kPreThreads) fa_bwd_preprocess_kernel(const ui
 // Shared layout: one CTA per SM, 384 threads.
 //   warps 0-3  compute warpgroup 0: columns [0, 64) of each 128 x 128 tile
 //   warps 4-7  compute warpgroup 1: columns [64, 128)
-//   warp  8    producer (TMA tiles; the whole warp gathers the row vectors)
-//   warp  9    TMEM owner and single-thread tcgen05.mma issuer
-//   warps 10-11 idle
-// TMEM (512 columns): T0 [0,128) scores, T1 [128,256) dP, then accumulators.
-// bf16 operands made by the compute warps (P^T, dS^T, dS) overwrite the first
-// 32 columns of their own half of T0 / T1 and feed the next MMA from TMEM.
+//   warp  8    producer (TMA tiles; in dK/dV the whole warp gathers the row
+//              vectors; in dQ also the work-unit sequence)
+//   warp  9    TMEM owner and tcgen05.mma issuer (elect.sync in a converged warp)
+//   warp  10   dQ: owner of the dO buffer (dQ epilogue store, next dO load)
+//   others     idle
+// TMEM (512 columns): scores, dP, then accumulators (dQ double-buffers its
+// scores in the columns its single accumulator leaves free).  bf16 operands
+// made by the compute warps (P^T, dS^T, dS) overwrite the first 32 columns of
+// their own half of the score / dP tile and feed the next MMA from TMEM.
 // ---------------------------------------------------------------------------
 
 constexpr float kLog2e = 1.4426950408889634f;

@@ -20,8 +20,10 @@
 //   warps 0-3  softmax for query tile 0 (thread = query row = TMEM lane)
 //   warps 4-7  softmax for query tile 1
 //   warp  8    TMA producer: Q0/Q1 once, then K_j, V_j through a ring of slots
-//   warp  9    TMEM owner and single-thread tcgen05.mma issuer
-//   warps 10-11 idle
+//              (tiles grouped per key step, one barrier per group)
+//   warp  9    TMEM owner and tcgen05.mma issuer (elect.sync in a converged warp)
+//   warp  10   second issuer for long rows (d = 128): tile 1's products
+//   warp  11   idle
 // The third warpgroup gives registers to the softmax warpgroups (setmaxnreg):
 // each softmax thread holds a full 128-score row in registers.
 // TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+d) O1 [256+d,256+2d).

@@ -117,3 +117,27 @@ def test_bwd_workload_parity(index):
             ref = oracle.attn_bwd_ref(sl(x["q"]), sl(x["k"]), sl(x["v"]), sl(x["do"]), w.scale, causal)
             _assert_grads((dq[b:b + 1, h:h + 1], dk[b:b + 1, h:h + 1], dv[b:b + 1, h:h + 1]), ref,
                           f" (b={b}, h={h}, causal={causal})")
+
+
+def test_dq_concurrent_streams_bitwise():
+    """The dQ kernel takes work over from not-yet-started CTAs of its own grid:
+    two launches running at once on two streams must each give exactly what
+    they give alone."""
+    _, ga = device_inputs(2, 4, 1500, 128, seed=31, with_grad=True)
+    _, gb = device_inputs(2, 4, 1500, 128, seed=32, with_grad=True)
+    ref = []
+    for g in (ga, gb):
+        o, lse = fa.fa_fwd(g["q"], g["k"], g["v"], None, True)
+        Dvec = fa.fa_bwd_preprocess(o, g["do"])
+        torch.cuda.synchronize()
+        dq = fa.fa_bwd_dq(g["q"], g["k"], g["v"], lse, g["do"], Dvec, None, True)
+        torch.cuda.synchronize()
+        ref.append((lse, Dvec, dq))
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    out = [torch.empty_like(ref[0][2]), torch.empty_like(ref[1][2])]
+    for _ in range(3):
+        for g, (lse, Dvec, _), s, dq in zip((ga, gb), ref, (sa, sb), out):
+            fa.fa_bwd_dq(g["q"], g["k"], g["v"], lse, g["do"], Dvec, None, True, dq=dq, stream=s)
+        torch.cuda.synchronize()
+        assert_no_timeout()
+        assert torch.equal(out[0], ref[0][2]) and torch.equal(out[1], ref[1][2])

@@ -86,8 +86,9 @@ __global__ void __launch_bounds__(kPreThreads) fa_bwd_preprocess_kernel(const ui
 // Shared layout: one CTA per SM, 384 threads.
 //   warps 0-3  compute warpgroup 0: columns [0, 64) of each 128 x 128 tile
 //   warps 4-7  compute warpgroup 1: columns [64, 128)
-//   warp  8    producer (TMA tiles; in dK/dV the whole warp gathers the row
-//              vectors; in dQ also the work-unit sequence)
+//   warp  8    producer (TMA tiles and the work-unit sequence; in dK/dV the
+//              whole warp gathers the row vectors, and lane 0 also issues the
+//              epilogue stores)
 //   warp  9    TMEM owner and tcgen05.mma issuer (elect.sync in a converged warp)
 //   warp  10   dQ: owner of the dO buffer (dQ epilogue store, next dO load)
 //   others     idle
@@ -150,20 +151,18 @@ __device__ __forceinline__ void st_bf16_16cols(uint32_t taddr, const float* v) {
   tmem_st16(taddr, w);
 }
 
-// Epilogue for one 128 x d accumulator: TMEM -> * mult -> bf16 -> swizzled
-// staging -> TMA store (rows past N clipped).  `c0, c1` bound the columns this
-// warpgroup writes; the TMA store is issued by `leader` once `staged` fills.
+// Epilogue staging for one 128 x d accumulator: TMEM -> * mult -> bf16 ->
+// swizzled tile (the layout a TMA store reads) at shared address `stage`;
+// thread r writes row r.
 template <int D>
-__device__ __forceinline__ void bwd_store_acc(uint32_t tacc, uint8_t* stage, int c0, int c1, float mult, int r,
-                                              uint64_t* staged, bool leader, const CUtensorMap* map, int row0,
-                                              int bh, const CtaGuard& g, uint32_t site) {
+__device__ __forceinline__ void bwd_stage_acc(uint32_t tacc, uint32_t stage, float mult, int r) {
   using C = BwdCfg<D>;
-  const uint32_t st = smem_u32(stage);
-  for (int c = c0; c < c1; c += 32) {
+#pragma unroll
+  for (int c = 0; c < D; c += 32) {
     uint32_t o[32];
     tmem_ld32(tacc + c, o);
     tmem_ld_wait(o);
-    const uint32_t box = st + (c / 64) * C::kBoxBytes + r * 128;
+    const uint32_t box = stage + (c / 64) * C::kBoxBytes + r * 128;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int chunk = (c % 64) / 8 + q;
@@ -173,14 +172,6 @@ __device__ __forceinline__ void bwd_store_acc(uint32_t tacc, uint8_t* stage, int
       st_shared_v4(box + ((chunk ^ (r & 7)) << 4), pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
                    pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
     }
-  }
-  fence_proxy_async_smem();
-  mbar_arrive(staged);
-  if (leader && mbar_wait(staged, 0, g, site)) {
-#pragma unroll
-    for (int b = 0; b < C::kBoxes; ++b) tma_store_3d(map, stage + b * C::kBoxBytes, 64 * b, row0, bh);
-    tma_store_commit();
-    tma_store_wait_read_all();
   }
 }
 
@@ -211,17 +202,26 @@ __device__ __forceinline__ RowVecs fetch_row_vectors(const float* __restrict__ l
 }
 
 // ---------------------------------------------------------------------------
-// dK / dV: one CTA per (b, h, 128-key tile j); loop over query tiles i.
+// dK / dV: one work unit per (b, h, 128-key tile j); loop over query tiles i.
 //   S^T = K_j Q_i^T, P^T = exp2(S^T * scale * log2e - lse2_i)
 //   dP^T = V_j dO_i^T, dS^T = P^T o (dP^T - D_i)
 //   dV_j += P^T dO_i,  dK_j += dS^T Q_i,  finally dK_j *= scale
-// K_j and V_j stay resident; Q_i (with -lse) streams through a 3-deep ring and
-// dO_i (with -D) through a 2-deep ring, so the next query tile is loaded well
-// before S^T(i+1) needs it.
+// K_j and V_j are resident per unit; Q_i (with -lse) streams through a 3-deep
+// ring and dO_i (with -D) through a 2-deep ring, so the next query tile is
+// loaded well before S^T(i+1) needs it.
 // MMA order S(i) dP(i) dV(i) {S(i+1), dK(i)} dP(i+1) ...: the exponentials of
 // tile i run under dP(i), the dS products under dV(i); S^T(i+1) and dK(i)
 // touch different TMEM columns and go in whichever order their inputs land.
 // TMEM: T0 = S^T, T1 = dP^T, acc0 = dV, acc1 = dK.
+// Persistent CTAs (cluster launch control, as in dQ below): a running CTA
+// takes over the next not-yet-started CTA's unit, so barriers, TMEM and the
+// rings carry on across units (global query-tile count).  The next unit's
+// K_j, V_j load as soon as this unit's last S^T and dP^T have read the old
+// ones, and its first S^T and dP^T run while the compute warps drain this
+// unit's accumulators.  Epilogue: the compute warps stage dV in the dO slot
+// and dK in the Q slot of the unit's last query tile L (both free once dK(L)
+// is done); the producer stores them with TMA and reloads those slots (with
+// dO(L+2) and Q(L+3)) only after the stores have read them.
 // ---------------------------------------------------------------------------
 
 template <int D>
@@ -237,23 +237,40 @@ struct DkdvCfg {
   static constexpr uint32_t kLseOff = kDOOff + kDOStages * kTileBytes;   // 128 fp32 per Q stage
   static constexpr uint32_t kDVecOff = kLseOff + kQStages * 512;          // 128 fp32 per dO stage
   static constexpr uint32_t kBarOff = kDVecOff + kDOStages * 512;
-  // res_full, q_full[3], q_empty[3], do_full[2], s_full, dp_full, p_full, ds_full, acc_done, drain,
-  // staged[2].  A dO slot has no empty barrier of its own: dO_i's last reader
-  // (dV(i)) finishes before dK(i), whose commit already releases Q_i's slot.
-  static constexpr int kBars = 1 + 2 * kQStages + kDOStages + 8;
-  static constexpr uint32_t kMiscOff = kBarOff + kBars * 8;
-  static constexpr uint32_t kLayoutBytes = kMiscOff + 16;
+  // kv_full[2], kv_free, q_full[3], q_empty[3], do_full[2], s_full, dp_full,
+  // p_full, ds_full, acc_done, acc_free, drain, staged[2], sched.  A dO slot
+  // has no empty barrier of its own: dO_i's last reader (dV(i)) finishes
+  // before dK(i), whose commit already releases Q_i's slot.  kv_full and
+  // staged go by unit parity, so neither runs two phases ahead of a waiter.
+  static constexpr int kBars = 3 + 2 * kQStages + kDOStages + 10;
+  static constexpr uint32_t kMiscOff = kBarOff + kBars * 8;   // tmem holder, abort flag, unit ids [2]
+  static constexpr uint32_t kRespOff = (kMiscOff + 16 + 15) / 16 * 16;   // 16-byte work-steal response
+  static constexpr uint32_t kLayoutBytes = kRespOff + 16;
   static constexpr uint32_t kMaxSmem = BwdCfg<D>::kMaxSmem;
   // room for the 1024-byte alignment of the base when it fits, else all there is
   static constexpr uint32_t kSmemBytes = kLayoutBytes + 1024 <= kMaxSmem ? kLayoutBytes + 1024 : kMaxSmem;
   static_assert(kLayoutBytes <= kMaxSmem, "dK/dV shared-memory layout too large");
   static constexpr int kThreads = 384;
+  static constexpr int kRequestAhead = 3;   // query tiles before a unit's end at which the next is requested
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
   __host__ __device__ static constexpr uint32_t q_off(int s) { return kQOff + s * kTileBytes; }
   __host__ __device__ static constexpr uint32_t do_off(int s) { return kDOOff + s * kTileBytes; }
   __host__ __device__ static constexpr uint32_t lse_off(int s) { return kLseOff + s * 512; }
   __host__ __device__ static constexpr uint32_t dvec_off(int s) { return kDVecOff + s * 512; }
 };
+
+// Work unit u (a CTA index of the launch grid) -> head, key tile, query tiles.
+struct DkdvUnit {
+  int bh, kt, i0, cnt;
+};
+template <bool CAUSAL>
+__device__ __forceinline__ DkdvUnit dkdv_unit(int u, int n_tiles, int BH, int band) {
+  DkdvUnit w;
+  banded_order(u, n_tiles, BH, band, w.bh, w.kt);   // causal: small kt is heavy, rank 0 -> kt 0
+  w.i0 = CAUSAL ? w.kt : 0;                          // first query tile
+  w.cnt = n_tiles - w.i0;                            // query tiles visited (>= 1)
+  return w;
+}
 
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(384, 1)
@@ -271,8 +288,9 @@ __global__ void __launch_bounds__(384, 1)
     return;
   }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
-  uint64_t* res_full = bars;
-  uint64_t* q_full = bars + 1;
+  uint64_t* kv_full = bars;                 // [2], by unit parity; also publishes the unit id
+  uint64_t* kv_free = kv_full + 2;
+  uint64_t* q_full = kv_free + 1;
   uint64_t* q_empty = q_full + C::kQStages;
   uint64_t* do_full = q_empty + C::kQStages;
   uint64_t* s_full = do_full + C::kDOStages;
@@ -280,20 +298,24 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* p_full = dp_full + 1;
   uint64_t* ds_full = p_full + 1;
   uint64_t* acc_done = ds_full + 1;
-  uint64_t* drain = acc_done + 1;
-  uint64_t* staged = drain + 1;
+  uint64_t* acc_free = acc_done + 1;
+  uint64_t* drain = acc_free + 1;
+  uint64_t* staged = drain + 1;             // [2], by unit parity
+  uint64_t* sched = staged + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kMiscOff + 4);
+  // unit ids by unit parity: unit k + 2's id is written only after unit k + 1's
+  // S^T and dP^T have all been issued, by which time every reader has taken k's
+  volatile int* unit_id = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 8);
+  uint8_t* resp = smem + C::kRespOff;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  int bh, kt;   // key tile; causal: small kt is heavy, so rank 0 -> kt 0
-  banded_order(blockIdx.x, n_tiles, BH, band, bh, kt);
-  const int i0 = CAUSAL ? kt : 0;                               // first query tile
-  const int cnt = n_tiles - i0;                                 // query tiles visited (>= 1)
-  const size_t row_base = static_cast<size_t>(bh) * N;
-
   if (threadIdx.x == 0) {
-    mbar_init(res_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&kv_full[i], 1);    // the producer's expect-tx arrival (plain arrival when no unit is left)
+      mbar_init(&staged[i], 256);   // every compute thread, after staging its rows
+    }
+    mbar_init(kv_free, 1);
     for (int i = 0; i < C::kQStages; ++i) {
       mbar_init(&q_full[i], 2);     // TMA bytes + the producer warp's -lse writes
       mbar_init(&q_empty[i], 1);
@@ -306,9 +328,9 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(p_full, 256);
     mbar_init(ds_full, 256);
     mbar_init(acc_done, 1);
+    mbar_init(acc_free, 256);
     mbar_init(drain, 1);
-    mbar_init(&staged[0], 128);
-    mbar_init(&staged[1], 128);
+    mbar_init(sched, 1);
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -324,55 +346,150 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t sbase = smem_u32(smem);
 
   if (warp >= 8) {
-    if (warp == 8) {  // producer: K_j, V_j once; Q_i and dO_i (+ row vectors) per query tile
-      if (lane == 0) {
-        mbar_arrive_expect_tx(res_full, 2 * C::kTileBytes);
-        for (int b = 0; b < C::kBoxes; ++b) {
-          tma_load_3d(smem + C::kKOff + b * C::kBoxBytes, &tmK, res_full, 64 * b, 128 * kt, bh);
-          tma_load_3d(smem + C::kVOff + b * C::kBoxBytes, &tmV, res_full, 64 * b, 128 * kt, bh);
-        }
-      }
-      RowVecs rv = fetch_row_vectors(lse, Dg, row_base, 128 * i0, N, lane);
-      for (int it = 0; it < cnt; ++it) {
-        const int qt = i0 + it;
-        const int qs = it % C::kQStages, ds = it % C::kDOStages;
-        int ok = 1;
-        if (lane == 0) ok = mbar_wait(&q_empty[qs], ((it / C::kQStages) & 1u) ^ 1u, g, kSiteDkdv | 1u);
-        if (!__shfl_sync(0xffffffffu, ok, 0)) break;   // the whole warp follows lane 0
+    if (warp == 8) {
+      // Producer: per unit K_j, V_j; per query tile Q_i and dO_i (+ row
+      // vectors); the next unit; the epilogue stores.  The whole warp runs the
+      // loop (it writes the row vectors), lane 0 issues every copy.
+      //
+      // Pending epilogue stores, oldest first: unit `pend_su` and the next.  A
+      // unit ending at query tile L is stored just before dO(L+2) reuses its dV
+      // slot; its dK store may still be reading when that load goes out and is
+      // waited for before the next Q load (Q(L+3) is the first to reuse it).
+      int p0_bh = 0, p0_kt = 0, p0_last = 0, p1_bh = 0, p1_kt = 0, p1_last = 0;
+      int n_pend = 0, pend_su = 0;
+      bool dk_reading = false;
+      auto store_front = [&]() -> bool {   // lane 0
+        if (!mbar_wait(&staged[pend_su & 1], (pend_su >> 1) & 1, g, kSiteDkdv | 16u)) return false;
+        for (int b = 0; b < C::kBoxes; ++b)
+          tma_store_3d(&tmDV, smem + C::do_off(p0_last % C::kDOStages) + b * C::kBoxBytes, 64 * b, 128 * p0_kt,
+                       p0_bh);
+        tma_store_commit();
+        for (int b = 0; b < C::kBoxes; ++b)
+          tma_store_3d(&tmDK, smem + C::q_off(p0_last % C::kQStages) + b * C::kBoxBytes, 64 * b, 128 * p0_kt,
+                       p0_bh);
+        tma_store_commit();
+        tma_store_wait_read_but_one();   // dV has been read out of the dO slot
+        dk_reading = true;
+        p0_bh = p1_bh;
+        p0_kt = p1_kt;
+        p0_last = p1_last;
+        --n_pend;
+        ++pend_su;
+        return true;
+      };
+      int u = static_cast<int>(blockIdx.x);
+      int gi = 0;   // global query-tile count (ring index)
+      bool ok = true;
+      for (int su = 0; ok; ++su) {
+        // unit su's K_j, V_j replace unit su-1's once its S^T and dP^T are done
+        int okl = 1;
+        if (lane == 0 && su > 0) okl = mbar_wait(kv_free, (su - 1) & 1, g, kSiteDkdv | 15u);
+        if (!__shfl_sync(0xffffffffu, okl, 0)) break;
         if (lane == 0) {
-          if (it + kL2Ahead < cnt) {   // query tile it + kL2Ahead into L2 while this one lands
-            for (int b = 0; b < C::kBoxes; ++b) {
-              tma_prefetch_l2_3d(&tmQ, 64 * b, 128 * (qt + kL2Ahead), bh);
-              tma_prefetch_l2_3d(&tmDO, 64 * b, 128 * (qt + kL2Ahead), bh);
+          unit_id[su & 1] = u;
+          if (u < 0) mbar_arrive(&kv_full[su & 1]);   // no work left: release the consumers
+        }
+        if (u < 0) break;
+        const DkdvUnit w = dkdv_unit<CAUSAL>(u, n_tiles, BH, band);
+        const size_t row_base = static_cast<size_t>(w.bh) * N;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&kv_full[su & 1], 2 * C::kTileBytes);
+          for (int b = 0; b < C::kBoxes; ++b) {
+            tma_load_3d(smem + C::kKOff + b * C::kBoxBytes, &tmK, &kv_full[su & 1], 64 * b, 128 * w.kt, w.bh);
+            tma_load_3d(smem + C::kVOff + b * C::kBoxBytes, &tmV, &kv_full[su & 1], 64 * b, 128 * w.kt, w.bh);
+          }
+        }
+        RowVecs rv = fetch_row_vectors(lse, Dg, row_base, 128 * w.i0, N, lane);
+        for (int it = 0; it < w.cnt; ++it, ++gi) {
+          const int qt = w.i0 + it;
+          const int qs = gi % C::kQStages, ds = gi % C::kDOStages;
+          if (lane == 0) {
+            if (it == max(0, w.cnt - C::kRequestAhead)) {   // ask for the next unit
+              mbar_arrive_expect_tx(sched, 16);
+              clc_try_cancel(resp, sched);
+            }
+            okl = mbar_wait(&q_empty[qs], ((gi / C::kQStages) & 1u) ^ 1u, g, kSiteDkdv | 1u);
+            if (okl && dk_reading) {   // a staged dK may still be read from this slot
+              tma_store_wait_read_all();
+              dk_reading = false;
             }
           }
-          mbar_arrive_expect_tx(&q_full[qs], C::kTileBytes);
-          for (int b = 0; b < C::kBoxes; ++b)
-            tma_load_3d(smem + C::q_off(qs) + b * C::kBoxBytes, &tmQ, &q_full[qs], 64 * b, 128 * qt, bh);
-        }
-        float* nl = reinterpret_cast<float*>(smem + C::lse_off(qs));
+          if (!__shfl_sync(0xffffffffu, okl, 0)) { ok = false; break; }
+          if (lane == 0) {
+            if (it + kL2Ahead < w.cnt) {   // query tile it + kL2Ahead into L2 while this one lands
+              for (int b = 0; b < C::kBoxes; ++b) {
+                tma_prefetch_l2_3d(&tmQ, 64 * b, 128 * (qt + kL2Ahead), w.bh);
+                tma_prefetch_l2_3d(&tmDO, 64 * b, 128 * (qt + kL2Ahead), w.bh);
+              }
+            }
+            mbar_arrive_expect_tx(&q_full[qs], C::kTileBytes);
+            for (int b = 0; b < C::kBoxes; ++b)
+              tma_load_3d(smem + C::q_off(qs) + b * C::kBoxBytes, &tmQ, &q_full[qs], 64 * b, 128 * qt, w.bh);
+          }
+          float* nl = reinterpret_cast<float*>(smem + C::lse_off(qs));
 #pragma unroll
-        for (int k = 0; k < 4; ++k) nl[lane + 32 * k] = rv.a[k];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&q_full[qs]);
-        // dO slot reuse: tile it - 2's dK (after its dV) has completed, which
-        // the q_empty commit of that tile signals
-        if (lane == 0 && it >= C::kDOStages) {
-          const int pt = it - C::kDOStages;
-          ok = mbar_wait(&q_empty[pt % C::kQStages], (pt / C::kQStages) & 1u, g, kSiteDkdv | 12u);
+          for (int k = 0; k < 4; ++k) nl[lane + 32 * k] = rv.a[k];
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&q_full[qs]);
+          // dO slot reuse: tile gi - 2's dK (after its dV) has completed, which
+          // the q_empty commit of that tile signals; a unit that ended there
+          // is stored first (its dV is staged in this slot)
+          if (lane == 0) {
+            if (gi >= C::kDOStages) {
+              const int pt = gi - C::kDOStages;
+              okl = mbar_wait(&q_empty[pt % C::kQStages], (pt / C::kQStages) & 1u, g, kSiteDkdv | 12u);
+            }
+            if (okl && n_pend > 0 && p0_last + C::kDOStages == gi) okl = store_front();
+          }
+          if (!__shfl_sync(0xffffffffu, okl, 0)) { ok = false; break; }
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&do_full[ds], C::kTileBytes);
+            for (int b = 0; b < C::kBoxes; ++b)
+              tma_load_3d(smem + C::do_off(ds) + b * C::kBoxBytes, &tmDO, &do_full[ds], 64 * b, 128 * qt, w.bh);
+          }
+          float* nd = reinterpret_cast<float*>(smem + C::dvec_off(ds));
+#pragma unroll
+          for (int k = 0; k < 4; ++k) nd[lane + 32 * k] = rv.d[k];
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&do_full[ds]);
+          if (it + 1 < w.cnt) rv = fetch_row_vectors(lse, Dg, row_base, 128 * (qt + 1), N, lane);
         }
-        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        if (!ok) break;
+        int nu = -1;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&do_full[ds], C::kTileBytes);
-          for (int b = 0; b < C::kBoxes; ++b)
-            tma_load_3d(smem + C::do_off(ds) + b * C::kBoxBytes, &tmDO, &do_full[ds], 64 * b, 128 * qt, bh);
+          if (n_pend == 0) {   // at most one older store is still pending here
+            p0_bh = w.bh;
+            p0_kt = w.kt;
+            p0_last = gi - 1;
+          } else {
+            p1_bh = w.bh;
+            p1_kt = w.kt;
+            p1_last = gi - 1;
+          }
+          ++n_pend;
+          okl = mbar_wait(sched, su & 1, g, kSiteDkdv | 19u);
+          if (okl) {
+            nu = clc_decode(resp);
+            if (nu >= 0) {   // the next unit's K, V and first query tiles into L2
+              const DkdvUnit w1 = dkdv_unit<CAUSAL>(nu, n_tiles, BH, band);
+              for (int b = 0; b < C::kBoxes; ++b) {
+                tma_prefetch_l2_3d(&tmK, 64 * b, 128 * w1.kt, w1.bh);
+                tma_prefetch_l2_3d(&tmV, 64 * b, 128 * w1.kt, w1.bh);
+                for (int t = 0; t < kL2Ahead && t < w1.cnt; ++t) {
+                  tma_prefetch_l2_3d(&tmQ, 64 * b, 128 * (w1.i0 + t), w1.bh);
+                  tma_prefetch_l2_3d(&tmDO, 64 * b, 128 * (w1.i0 + t), w1.bh);
+                }
+              }
+            }
+          }
         }
-        float* nd = reinterpret_cast<float*>(smem + C::dvec_off(ds));
-#pragma unroll
-        for (int k = 0; k < 4; ++k) nd[lane + 32 * k] = rv.d[k];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&do_full[ds]);
-        if (it + 1 < cnt) rv = fetch_row_vectors(lse, Dg, row_base, 128 * (qt + 1), N, lane);
+        if (!__shfl_sync(0xffffffffu, okl, 0)) break;
+        u = __shfl_sync(0xffffffffu, nu, 0);
+      }
+      if (lane == 0) {   // the remaining epilogue stores; all of them land before the CTA retires
+        bool sok = true;
+        while (sok && n_pend > 0) sok = store_front();
+        tma_store_wait_all();
       }
     } else if (warp == 9) {  // MMA issuer: the whole warp runs the loop, one lane issues
       const uint32_t tS = tmem + C::kColS, tDP = tmem + C::kColDP;
@@ -383,55 +500,71 @@ __global__ void __launch_bounds__(384, 1)
       auto mQ = [&](int s) { return mnmaj<D>(sbase + C::q_off(s)); };
       auto kDO = [&](int s) { return kmaj<D>(sbase + C::do_off(s)); };
       auto mDO = [&](int s) { return mnmaj<D>(sbase + C::do_off(s)); };
-      bool ok = mbar_wait_w(res_full, 0, g, kSiteDkdv | 2u) && mbar_wait_w(&q_full[0], 0, g, kSiteDkdv | 3u);
-      if (ok) {
-        mma_nt<D>(tS, kK, kQ(0));
+      auto qpar = [](int i) { return static_cast<uint32_t>((i / C::kQStages) & 1); };
+      auto dpar = [](int i) { return static_cast<uint32_t>((i / C::kDOStages) & 1); };
+      bool ok = true;
+      int gi = 0;
+      for (int su = 0; ok; ++su) {
+        if (!(ok = mbar_wait_w(&kv_full[su & 1], (su >> 1) & 1, g, kSiteDkdv | 2u))) break;
+        const int u = unit_id[su & 1];
+        if (u < 0) break;
+        const int cnt = dkdv_unit<CAUSAL>(u, n_tiles, BH, band).cnt;
+        const int g0 = gi;
+        // S^T(0), dP^T(0): the previous unit's readers of these columns (its
+        // last dV and dK) were issued before
+        if (!(ok = mbar_wait_w(&q_full[g0 % C::kQStages], qpar(g0), g, kSiteDkdv | 3u))) break;
+        mma_nt<D>(tS, kK, kQ(g0 % C::kQStages));
         tc_commit_w(s_full);
-        ok = mbar_wait_w(&do_full[0], 0, g, kSiteDkdv | 3u);
-      }
-      if (ok) {
-        mma_nt<D>(tDP, kV, kDO(0));
+        if (!(ok = mbar_wait_w(&do_full[g0 % C::kDOStages], dpar(g0), g, kSiteDkdv | 3u))) break;
+        mma_nt<D>(tDP, kV, kDO(g0 % C::kDOStages));
         tc_commit_w(dp_full);
-      }
-      for (int it = 0; ok && it < cnt; ++it) {
-        const int qs = it % C::kQStages, ds = it % C::kDOStages;
-        const int qs1 = (it + 1) % C::kQStages, ds1 = (it + 1) % C::kDOStages;
-        const uint32_t par = it & 1;
-        const bool next = it + 1 < cnt;
-        if (!(ok = mbar_wait_w(p_full, par, g, kSiteDkdv | 4u))) break;
-        tc_fence_after();
-        mma_tn_acc<D>(tDV, tS, mDO(ds), it > 0);          // dV += P^T dO_i
-        bool s_done = !next, k_done = false;
-        const uint32_t qph1 = ((it + 1) / C::kQStages) & 1u;
-        while (ok && !(s_done && k_done)) {
-          int which;
-          if (!s_done && !k_done)
-            which = mbar_wait_either_w(&q_full[qs1], qph1, ds_full, par, g, kSiteDkdv | 5u);
-          else if (!s_done)
-            which = mbar_wait_w(&q_full[qs1], qph1, g, kSiteDkdv | 5u) ? 0 : -1;
-          else
-            which = mbar_wait_w(ds_full, par, g, kSiteDkdv | 6u) ? 1 : -1;
-          if (which < 0) {
-            ok = false;
-          } else if (which == 0) {
-            mma_nt<D>(tS, kK, kQ(qs1));                     // S^T(i+1)
-            tc_commit_w(s_full);
-            s_done = true;
-          } else {
-            tc_fence_after();
-            mma_tn_acc<D>(tDK, tDP, mQ(qs), it > 0);        // dK += dS^T Q_i
-            tc_commit_w(&q_empty[qs]);                     // Q_i, -lse_i, and dO_i, -D_i: last readers done
-            k_done = true;
+        if (cnt == 1) tc_commit_w(kv_free);   // K_j, V_j: last readers issued
+        for (int it = 0; ok && it < cnt; ++it) {
+          const int i = g0 + it;
+          const int qs = i % C::kQStages, ds = i % C::kDOStages;
+          const int qs1 = (i + 1) % C::kQStages, ds1 = (i + 1) % C::kDOStages;
+          const uint32_t par = i & 1;
+          const bool next = it + 1 < cnt;
+          if (!(ok = mbar_wait_w(p_full, par, g, kSiteDkdv | 4u))) break;
+          // the unit's first dV overwrites the accumulator: the previous
+          // unit's epilogue must have read both accumulators out
+          if (it == 0 && su > 0 && !(ok = mbar_wait_w(acc_free, (su - 1) & 1, g, kSiteDkdv | 18u))) break;
+          tc_fence_after();
+          mma_tn_acc<D>(tDV, tS, mDO(ds), it > 0);          // dV += P^T dO_i
+          bool s_done = !next, k_done = false;
+          while (ok && !(s_done && k_done)) {
+            int which;
+            if (!s_done && !k_done)
+              which = mbar_wait_either_w(&q_full[qs1], qpar(i + 1), ds_full, par, g, kSiteDkdv | 5u);
+            else if (!s_done)
+              which = mbar_wait_w(&q_full[qs1], qpar(i + 1), g, kSiteDkdv | 5u) ? 0 : -1;
+            else
+              which = mbar_wait_w(ds_full, par, g, kSiteDkdv | 6u) ? 1 : -1;
+            if (which < 0) {
+              ok = false;
+            } else if (which == 0) {
+              mma_nt<D>(tS, kK, kQ(qs1));                     // S^T(i+1)
+              tc_commit_w(s_full);
+              s_done = true;
+            } else {
+              tc_fence_after();
+              mma_tn_acc<D>(tDK, tDP, mQ(qs), it > 0);        // dK += dS^T Q_i
+              tc_commit_w(&q_empty[qs]);                     // Q_i, -lse_i, and dO_i, -D_i: last readers done
+              k_done = true;
+            }
+          }
+          if (!ok) break;
+          if (next) {
+            if (!(ok = mbar_wait_w(&do_full[ds1], dpar(i + 1), g, kSiteDkdv | 13u))) break;
+            mma_nt<D>(tDP, kV, kDO(ds1));                     // dP^T(i+1), after dK(i) has read dS^T(i)
+            tc_commit_w(dp_full);
+            if (it + 2 == cnt) tc_commit_w(kv_free);        // K_j, V_j: last readers issued
           }
         }
         if (!ok) break;
-        if (next) {
-          if (!(ok = mbar_wait_w(&do_full[ds1], ((it + 1) / C::kDOStages) & 1u, g, kSiteDkdv | 13u))) break;
-          mma_nt<D>(tDP, kV, kDO(ds1));                     // dP^T(i+1), after dK(i) has read dS^T(i)
-          tc_commit_w(dp_full);
-        }
+        tc_commit_w(acc_done);
+        gi = g0 + cnt;
       }
-      if (ok) tc_commit_w(acc_done);
       tc_commit_w(drain);
       mbar_drain(drain, 0);
       __syncwarp();
@@ -451,96 +584,107 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tDP = tmem + lane_base + C::kColDP + 64 * h;
   const float2 sc2 = make_float2(scale_log2, scale_log2);
   bool ok = true;
-  for (int it = 0; ok && it < cnt; ++it) {
-    const int qs = it % C::kQStages, ds = it % C::kDOStages;
-    const uint32_t par = it & 1;
-    const int qt = i0 + it;
-    // -lse arrived with Q_i (q_full), -D with dO_i (do_full)
-    if (!(ok = mbar_wait(&q_full[qs], (it / C::kQStages) & 1u, g, kSiteDkdv | 7u))) break;
-    if (!(ok = mbar_wait(s_full, par, g, kSiteDkdv | 8u))) break;
-    __syncwarp();
-    tc_fence_after();
-    uint32_t sr[2][32];
-    tmem_ld32(tS, sr[0]);
-    tmem_ld32(tS + 32, sr[1]);
-    tmem_ld_wait(sr[0]);
-    tmem_ld_fence(sr[1]);
-    float p[64];
-    const uint32_t lse_addr = sbase + C::lse_off(qs) + 256 * h;   // -lse * log2(e) of this half's columns
+  int gi = 0;
+  for (int su = 0; ok; ++su) {
+    if (!(ok = mbar_wait(&kv_full[su & 1], (su >> 1) & 1, g, kSiteDkdv | 17u))) break;
+    const int u = unit_id[su & 1];
+    if (u < 0) break;
+    const DkdvUnit w = dkdv_unit<CAUSAL>(u, n_tiles, BH, band);
+    for (int it = 0; ok && it < w.cnt; ++it, ++gi) {
+      const int qs = gi % C::kQStages, ds = gi % C::kDOStages;
+      const uint32_t par = gi & 1;
+      const int qt = w.i0 + it;
+      // -lse arrived with Q_i (q_full), -D with dO_i (do_full)
+      if (!(ok = mbar_wait(&q_full[qs], (gi / C::kQStages) & 1u, g, kSiteDkdv | 7u))) break;
+      if (!(ok = mbar_wait(s_full, par, g, kSiteDkdv | 8u))) break;
+      __syncwarp();
+      tc_fence_after();
+      uint32_t sr[2][32];
+      tmem_ld32(tS, sr[0]);
+      tmem_ld32(tS + 32, sr[1]);
+      tmem_ld_wait(sr[0]);
+      tmem_ld_fence(sr[1]);
+      float p[64];
+      const uint32_t lse_addr = sbase + C::lse_off(qs) + 256 * h;   // -lse * log2(e) of this half's columns
 #pragma unroll
-    for (int b8 = 0; b8 < 2; ++b8) {   // 32 columns at a time: their loads go out before the math
-      float4 l4[8];
+      for (int b8 = 0; b8 < 2; ++b8) {   // 32 columns at a time: their loads go out before the math
+        float4 l4[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) l4[i] = ld_shared_f4(lse_addr + (8 * b8 + i) * 16);
+        for (int i = 0; i < 8; ++i) l4[i] = ld_shared_f4(lse_addr + (8 * b8 + i) * 16);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < 8; ++i) {
 #pragma unroll
-        for (int e = 0; e < 4; e += 2) {
-          const int c = 32 * b8 + 4 * i + e;
-          const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[c / 32][c % 32]),
-                                                  __uint_as_float(sr[(c + 1) / 32][(c + 1) % 32])),
-                                      sc2, e ? make_float2(l4[i].z, l4[i].w) : make_float2(l4[i].x, l4[i].y));
-          p[c] = ex2_approx(x.x);
-          p[c + 1] = ex2_approx(x.y);
+          for (int e = 0; e < 4; e += 2) {
+            const int c = 32 * b8 + 4 * i + e;
+            const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[c / 32][c % 32]),
+                                                    __uint_as_float(sr[(c + 1) / 32][(c + 1) % 32])),
+                                        sc2, e ? make_float2(l4[i].z, l4[i].w) : make_float2(l4[i].x, l4[i].y));
+            p[c] = ex2_approx(x.x);
+            p[c + 1] = ex2_approx(x.y);
+          }
         }
       }
-    }
-    if (CAUSAL && qt == kt) {
-      // diagonal tile: query column 64h + c precedes key t (and is masked) when c < t - 64h
-      const int lim = t - 64 * h;
+      if (CAUSAL && qt == w.kt) {
+        // diagonal tile: query column 64h + c precedes key t (and is masked) when c < t - 64h
+        const int lim = t - 64 * h;
 #pragma unroll
-      for (int c = 0; c < 64; ++c)
-        if (c < lim) p[c] = 0.f;
-    }
+        for (int c = 0; c < 64; ++c)
+          if (c < lim) p[c] = 0.f;
+      }
 #pragma unroll
-    for (int c = 0; c < 64; c += 32) st_bf16_16cols(tS + c / 2, p + c);
-    tmem_st_wait();
-    tc_fence_before();
-    mbar_arrive(p_full);
+      for (int c = 0; c < 64; c += 32) st_bf16_16cols(tS + c / 2, p + c);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(p_full);
 
-    if (!(ok = mbar_wait(&do_full[ds], (it / C::kDOStages) & 1u, g, kSiteDkdv | 14u))) break;
-    if (!(ok = mbar_wait(dp_full, par, g, kSiteDkdv | 9u))) break;
-    __syncwarp();
-    tc_fence_after();
-    uint32_t dr[2][32];
-    tmem_ld32(tDP, dr[0]);
-    tmem_ld32(tDP + 32, dr[1]);
-    tmem_ld_wait(dr[0]);
-    tmem_ld_fence(dr[1]);
-    const uint32_t d_addr = sbase + C::dvec_off(ds) + 256 * h;   // -D of this half's columns
+      if (!(ok = mbar_wait(&do_full[ds], (gi / C::kDOStages) & 1u, g, kSiteDkdv | 14u))) break;
+      if (!(ok = mbar_wait(dp_full, par, g, kSiteDkdv | 9u))) break;
+      __syncwarp();
+      tc_fence_after();
+      uint32_t dr[2][32];
+      tmem_ld32(tDP, dr[0]);
+      tmem_ld32(tDP + 32, dr[1]);
+      tmem_ld_wait(dr[0]);
+      tmem_ld_fence(dr[1]);
+      const uint32_t d_addr = sbase + C::dvec_off(ds) + 256 * h;   // -D of this half's columns
 #pragma unroll
-    for (int b8 = 0; b8 < 2; ++b8) {
-      float4 d4[8];
+      for (int b8 = 0; b8 < 2; ++b8) {
+        float4 d4[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) d4[i] = ld_shared_f4(d_addr + (8 * b8 + i) * 16);
+        for (int i = 0; i < 8; ++i) d4[i] = ld_shared_f4(d_addr + (8 * b8 + i) * 16);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < 8; ++i) {
 #pragma unroll
-        for (int e = 0; e < 4; e += 2) {
-          const int c = 32 * b8 + 4 * i + e;
-          const float2 dp = __fadd2_rn(make_float2(__uint_as_float(dr[c / 32][c % 32]),
-                                                   __uint_as_float(dr[(c + 1) / 32][(c + 1) % 32])),
-                                       e ? make_float2(d4[i].z, d4[i].w) : make_float2(d4[i].x, d4[i].y));
-          const float2 dsv = __fmul2_rn(make_float2(p[c], p[c + 1]), dp);
-          p[c] = dsv.x;
-          p[c + 1] = dsv.y;
+          for (int e = 0; e < 4; e += 2) {
+            const int c = 32 * b8 + 4 * i + e;
+            const float2 dp = __fadd2_rn(make_float2(__uint_as_float(dr[c / 32][c % 32]),
+                                                     __uint_as_float(dr[(c + 1) / 32][(c + 1) % 32])),
+                                         e ? make_float2(d4[i].z, d4[i].w) : make_float2(d4[i].x, d4[i].y));
+            const float2 dsv = __fmul2_rn(make_float2(p[c], p[c + 1]), dp);
+            p[c] = dsv.x;
+            p[c + 1] = dsv.y;
+          }
         }
       }
-    }
 #pragma unroll
-    for (int c = 0; c < 64; c += 32) st_bf16_16cols(tDP + c / 2, p + c);
-    tmem_st_wait();
-    tc_fence_before();
-    mbar_arrive(ds_full);
-  }
-  if (ok && mbar_wait(acc_done, 0, g, kSiteDkdv | 10u)) {
+      for (int c = 0; c < 64; c += 32) st_bf16_16cols(tDP + c / 2, p + c);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(ds_full);
+    }
+    if (!ok || !(ok = mbar_wait(acc_done, su & 1, g, kSiteDkdv | 10u))) break;
     __syncwarp();
     tc_fence_after();
-    // warpgroup 0 writes dV (staged in Q stage 0), warpgroup 1 writes dK (staged in Q stage 1)
-    const uint32_t tacc = tmem + lane_base + (h ? C::kColDK : C::kColDV);
-    uint8_t* stage = smem + C::q_off(h);
-    bwd_store_acc<D>(tacc, stage, 0, D, h ? scale : 1.f, t, &staged[h], t == 0, h ? &tmDK : &tmDV, 128 * kt,
-                     bh, g, kSiteDkdv | 11u);
+    // warpgroup 0 stages dV in the dO slot, warpgroup 1 dK (x scale) in the Q
+    // slot of the unit's last query tile; the producer stores both
+    const int last = gi - 1;
+    bwd_stage_acc<D>(tmem + lane_base + (h ? C::kColDK : C::kColDV),
+                     sbase + (h ? C::q_off(last % C::kQStages) : C::do_off(last % C::kDOStages)),
+                     h ? scale : 1.f, t);
+    tc_fence_before();
+    mbar_arrive(acc_free);   // both accumulators may be overwritten
+    fence_proxy_async_smem();
+    mbar_arrive(&staged[su & 1]);
   }
   __syncwarp();
   tc_fence_before();

@@ -35,6 +35,8 @@
 // 2^8; P values stay <= 256, and O is rescaled in TMEM only when some row of
 // the warp moved its reference.  The final O = acc / l is unchanged.
 #include "fa_internal.h"
+// the softmax and MMA warps change their register budgets (setmaxnreg)
+#define FA_INLINE_WAITS 1
 #include "fa_ptx.cuh"
 
 #include <cmath>

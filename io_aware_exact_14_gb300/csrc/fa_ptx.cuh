@@ -75,10 +75,19 @@ __device__ __forceinline__ void guard_fail(const CtaGuard& g, uint32_t site) {
   atomicCAS(g.status, 0u, site);
 }
 
+// The polling loops run out of line by default: every wait site then shares
+// one copy, which keeps the hot loops around them compact in the instruction
+// cache.  A translation unit whose warps change their register budget with
+// setmaxnreg (which out-of-line calls cannot follow) defines FA_INLINE_WAITS.
+#ifdef FA_INLINE_WAITS
+#define FA_WAIT_LINKAGE __forceinline__
+#else
+#define FA_WAIT_LINKAGE __noinline__
+#endif
+
 // Wait for the phase of `bar` with the given parity.  Returns false (without
 // waiting further) once the CTA is aborting or the wait limit is exceeded.
-__device__ __forceinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, const CtaGuard& g,
-                                            uint32_t site) {
+__device__ __forceinline__ bool mbar_poll(uint64_t* bar, uint32_t parity, const CtaGuard& g, uint32_t site) {
   const unsigned long long t0 = global_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -100,8 +109,7 @@ __device__ __forceinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, c
 // off the critical path (a loader waiting for the next unit), so that their
 // polling does not take issue slots from the compute warps of the same SM
 // sub-partition.
-__device__ __forceinline__ bool mbar_wait_backoff(uint64_t* bar, uint32_t parity, const CtaGuard& g,
-                                                  uint32_t site) {
+__device__ FA_WAIT_LINKAGE bool mbar_wait_backoff(uint64_t* bar, uint32_t parity, CtaGuard g, uint32_t site) {
   const unsigned long long t0 = global_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -117,6 +125,10 @@ __device__ __forceinline__ bool mbar_wait_backoff(uint64_t* bar, uint32_t parity
       }
     }
   }
+}
+
+__device__ FA_WAIT_LINKAGE bool mbar_wait_slow(uint64_t* bar, uint32_t parity, CtaGuard g, uint32_t site) {
+  return mbar_poll(bar, parity, g, site);
 }
 
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const CtaGuard& g,
@@ -219,6 +231,11 @@ __device__ __forceinline__ void tma_store_wait_read_all() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// Wait until at most one bulk store group is still reading shared memory.
+__device__ __forceinline__ void tma_store_wait_read_but_one() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
 __device__ __forceinline__ void tma_store_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Make generic-proxy shared-memory writes visible to the async proxy (TMA store).
@@ -298,27 +315,35 @@ __device__ __forceinline__ bool mbar_wait_w(uint64_t* bar, uint32_t parity, cons
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
+// The polling loop of mbar_wait_either_w (out of line, like mbar_wait_slow).
+__device__ FA_WAIT_LINKAGE int mbar_wait_either_slow(uint64_t* a, uint32_t pa, uint64_t* b, uint32_t pb, CtaGuard g,
+                                                  uint32_t site) {
+  const unsigned long long t0 = global_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(a, pa)) return 0;
+    if (mbar_try_wait(b, pb)) return 1;
+    if ((it & 63u) == 0u) {
+      if (*g.abort_flag || *reinterpret_cast<volatile unsigned int*>(g.status) != 0u) {
+        *g.abort_flag = 1u;
+        return -1;
+      }
+      if (global_ns() - t0 > kWaitLimitNs) {
+        guard_fail(g, site);
+        return -1;
+      }
+    }
+  }
+}
+
 // Bounded wait, by a whole warp, for whichever of two barrier phases completes
 // first: 0 for `a`, 1 for `b`, -1 if the CTA is aborting or the limit passed.
 __device__ __forceinline__ int mbar_wait_either_w(uint64_t* a, uint32_t pa, uint64_t* b, uint32_t pb,
                                                   const CtaGuard& g, uint32_t site) {
   int which = -1;
   if ((threadIdx.x & 31) == 0) {
-    const unsigned long long t0 = global_ns();
-    for (uint32_t it = 1;; ++it) {
-      if (mbar_try_wait(a, pa)) { which = 0; break; }
-      if (mbar_try_wait(b, pb)) { which = 1; break; }
-      if ((it & 63u) == 0u) {
-        if (*g.abort_flag || *reinterpret_cast<volatile unsigned int*>(g.status) != 0u) {
-          *g.abort_flag = 1u;
-          break;
-        }
-        if (global_ns() - t0 > kWaitLimitNs) {
-          guard_fail(g, site);
-          break;
-        }
-      }
-    }
+    if (mbar_try_wait(a, pa)) which = 0;
+    else if (mbar_try_wait(b, pb)) which = 1;
+    else which = mbar_wait_either_slow(a, pa, b, pb, g, site);
   }
   return __shfl_sync(0xffffffffu, which, 0);
 }

@@ -99,7 +99,12 @@ __global__ void __launch_bounds__(kPreThreads) fa_bwd_preprocess_kernel(const ui
 // ---------------------------------------------------------------------------
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kL2Ahead = 4;   // tiles a producer prefetches into L2 ahead of its loads
+// L2 prefetch: the dQ producer warms the first kL2Ahead key tiles of its next
+// unit.  Per-tile prefetches in the steady loops, and the dK/dV producer's
+// prefetch of its next unit, measured slower: the prefetches queue on the
+// SM's copy engine ahead of the loads that need it, and the streamed tiles of
+// a head are L2 hits anyway (heads run in small bands).
+constexpr int kL2Ahead = 4;
 
 // Tile geometry shared by both kernels: a 128-row tile of d bf16 columns is
 // d/64 swizzled boxes of 128 rows x 128 bytes.
@@ -216,9 +221,10 @@ __device__ __forceinline__ RowVecs fetch_row_vectors(const float* __restrict__ l
 // Persistent CTAs (cluster launch control, as in dQ below): a running CTA
 // takes over the next not-yet-started CTA's unit, so barriers, TMEM and the
 // rings carry on across units (global query-tile count).  The next unit's
-// K_j, V_j load as soon as this unit's last S^T and dP^T have read the old
-// ones, and its first S^T and dP^T run while the compute warps drain this
-// unit's accumulators.  Epilogue: the compute warps stage dV in the dO slot
+// first Q tile loads as soon as the unit is known, its K_j once this unit's
+// last S^T has read the old one and its V_j once the last dP^T has, so its
+// first S^T and dP^T run while the compute warps drain this unit's
+// accumulators.  Epilogue: the compute warps stage dV in the dO slot
 // and dK in the Q slot of the unit's last query tile L (both free once dK(L)
 // is done); the producer stores them with TMA and reloads those slots (with
 // dO(L+2) and Q(L+3)) only after the stores have read them.
@@ -237,12 +243,13 @@ struct DkdvCfg {
   static constexpr uint32_t kLseOff = kDOOff + kDOStages * kTileBytes;   // 128 fp32 per Q stage
   static constexpr uint32_t kDVecOff = kLseOff + kQStages * 512;          // 128 fp32 per dO stage
   static constexpr uint32_t kBarOff = kDVecOff + kDOStages * 512;
-  // kv_full[2], kv_free, q_full[3], q_empty[3], do_full[2], s_full, dp_full,
-  // p_full, ds_full, acc_done, acc_free, drain, staged[2], sched.  A dO slot
-  // has no empty barrier of its own: dO_i's last reader (dV(i)) finishes
-  // before dK(i), whose commit already releases Q_i's slot.  kv_full and
-  // staged go by unit parity, so neither runs two phases ahead of a waiter.
-  static constexpr int kBars = 3 + 2 * kQStages + kDOStages + 10;
+  // k_full[2], v_full[2], k_free, v_free, q_full[3], q_empty[3], do_full[2],
+  // s_full, dp_full, p_full, ds_full, acc_done, acc_free, drain, staged[2],
+  // sched.  A dO slot has no empty barrier of its own: dO_i's last reader
+  // (dV(i)) finishes before dK(i), whose commit already releases Q_i's slot.
+  // k_full, v_full and staged go by unit parity, so none of them runs two
+  // phases ahead of a waiter.
+  static constexpr int kBars = 6 + 2 * kQStages + kDOStages + 10;
   static constexpr uint32_t kMiscOff = kBarOff + kBars * 8;   // tmem holder, abort flag, unit ids [2]
   static constexpr uint32_t kRespOff = (kMiscOff + 16 + 15) / 16 * 16;   // 16-byte work-steal response
   static constexpr uint32_t kLayoutBytes = kRespOff + 16;
@@ -288,9 +295,11 @@ __global__ void __launch_bounds__(384, 1)
     return;
   }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
-  uint64_t* kv_full = bars;                 // [2], by unit parity; also publishes the unit id
-  uint64_t* kv_free = kv_full + 2;
-  uint64_t* q_full = kv_free + 1;
+  uint64_t* k_full = bars;                  // [2], by unit parity; also publishes the unit id
+  uint64_t* v_full = k_full + 2;            // [2], by unit parity
+  uint64_t* k_free = v_full + 2;
+  uint64_t* v_free = k_free + 1;
+  uint64_t* q_full = v_free + 1;
   uint64_t* q_empty = q_full + C::kQStages;
   uint64_t* do_full = q_empty + C::kQStages;
   uint64_t* s_full = do_full + C::kDOStages;
@@ -305,17 +314,19 @@ __global__ void __launch_bounds__(384, 1)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kMiscOff + 4);
   // unit ids by unit parity: unit k + 2's id is written only after unit k + 1's
-  // S^T and dP^T have all been issued, by which time every reader has taken k's
+  // S^T have all been issued, by which time every reader has taken k's
   volatile int* unit_id = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 8);
   uint8_t* resp = smem + C::kRespOff;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&kv_full[i], 1);    // the producer's expect-tx arrival (plain arrival when no unit is left)
+      mbar_init(&k_full[i], 1);     // the producer's expect-tx arrival (plain arrival when no unit is left)
+      mbar_init(&v_full[i], 1);
       mbar_init(&staged[i], 256);   // every compute thread, after staging its rows
     }
-    mbar_init(kv_free, 1);
+    mbar_init(k_free, 1);
+    mbar_init(v_free, 1);
     for (int i = 0; i < C::kQStages; ++i) {
       mbar_init(&q_full[i], 2);     // TMA bytes + the producer warp's -lse writes
       mbar_init(&q_empty[i], 1);
@@ -381,24 +392,16 @@ __global__ void __launch_bounds__(384, 1)
       int gi = 0;   // global query-tile count (ring index)
       bool ok = true;
       for (int su = 0; ok; ++su) {
-        // unit su's K_j, V_j replace unit su-1's once its S^T and dP^T are done
         int okl = 1;
-        if (lane == 0 && su > 0) okl = mbar_wait(kv_free, (su - 1) & 1, g, kSiteDkdv | 15u);
-        if (!__shfl_sync(0xffffffffu, okl, 0)) break;
-        if (lane == 0) {
-          unit_id[su & 1] = u;
-          if (u < 0) mbar_arrive(&kv_full[su & 1]);   // no work left: release the consumers
+        if (u < 0) {   // no work left: release the consumers (published like a unit id)
+          if (lane == 0 && (su == 0 || mbar_wait(k_free, (su - 1) & 1, g, kSiteDkdv | 15u))) {
+            unit_id[su & 1] = -1;
+            mbar_arrive(&k_full[su & 1]);
+          }
+          break;
         }
-        if (u < 0) break;
         const DkdvUnit w = dkdv_unit<CAUSAL>(u, n_tiles, BH, band);
         const size_t row_base = static_cast<size_t>(w.bh) * N;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&kv_full[su & 1], 2 * C::kTileBytes);
-          for (int b = 0; b < C::kBoxes; ++b) {
-            tma_load_3d(smem + C::kKOff + b * C::kBoxBytes, &tmK, &kv_full[su & 1], 64 * b, 128 * w.kt, w.bh);
-            tma_load_3d(smem + C::kVOff + b * C::kBoxBytes, &tmV, &kv_full[su & 1], 64 * b, 128 * w.kt, w.bh);
-          }
-        }
         RowVecs rv = fetch_row_vectors(lse, Dg, row_base, 128 * w.i0, N, lane);
         for (int it = 0; it < w.cnt; ++it, ++gi) {
           const int qt = w.i0 + it;
@@ -416,15 +419,31 @@ __global__ void __launch_bounds__(384, 1)
           }
           if (!__shfl_sync(0xffffffffu, okl, 0)) { ok = false; break; }
           if (lane == 0) {
-            if (it + kL2Ahead < w.cnt) {   // query tile it + kL2Ahead into L2 while this one lands
-              for (int b = 0; b < C::kBoxes; ++b) {
-                tma_prefetch_l2_3d(&tmQ, 64 * b, 128 * (qt + kL2Ahead), w.bh);
-                tma_prefetch_l2_3d(&tmDO, 64 * b, 128 * (qt + kL2Ahead), w.bh);
-              }
-            }
             mbar_arrive_expect_tx(&q_full[qs], C::kTileBytes);
             for (int b = 0; b < C::kBoxes; ++b)
               tma_load_3d(smem + C::q_off(qs) + b * C::kBoxBytes, &tmQ, &q_full[qs], 64 * b, 128 * qt, w.bh);
+          }
+          if (it == 0) {
+            // the unit's K_j replaces the previous unit's once its last S^T is
+            // done (and goes out with the unit id), V_j once its last dP^T is;
+            // both before this tile's row vector, whose global loads may still
+            // be in flight
+            if (lane == 0) {
+              if (su > 0) okl = mbar_wait(k_free, (su - 1) & 1, g, kSiteDkdv | 15u);
+              if (okl) {
+                unit_id[su & 1] = u;
+                mbar_arrive_expect_tx(&k_full[su & 1], C::kTileBytes);
+                for (int b = 0; b < C::kBoxes; ++b)
+                  tma_load_3d(smem + C::kKOff + b * C::kBoxBytes, &tmK, &k_full[su & 1], 64 * b, 128 * w.kt, w.bh);
+                if (su > 0) okl = mbar_wait(v_free, (su - 1) & 1, g, kSiteDkdv | 20u);
+              }
+              if (okl) {
+                mbar_arrive_expect_tx(&v_full[su & 1], C::kTileBytes);
+                for (int b = 0; b < C::kBoxes; ++b)
+                  tma_load_3d(smem + C::kVOff + b * C::kBoxBytes, &tmV, &v_full[su & 1], 64 * b, 128 * w.kt, w.bh);
+              }
+            }
+            if (!__shfl_sync(0xffffffffu, okl, 0)) { ok = false; break; }
           }
           float* nl = reinterpret_cast<float*>(smem + C::lse_off(qs));
 #pragma unroll
@@ -468,20 +487,7 @@ __global__ void __launch_bounds__(384, 1)
           }
           ++n_pend;
           okl = mbar_wait(sched, su & 1, g, kSiteDkdv | 19u);
-          if (okl) {
-            nu = clc_decode(resp);
-            if (nu >= 0) {   // the next unit's K, V and first query tiles into L2
-              const DkdvUnit w1 = dkdv_unit<CAUSAL>(nu, n_tiles, BH, band);
-              for (int b = 0; b < C::kBoxes; ++b) {
-                tma_prefetch_l2_3d(&tmK, 64 * b, 128 * w1.kt, w1.bh);
-                tma_prefetch_l2_3d(&tmV, 64 * b, 128 * w1.kt, w1.bh);
-                for (int t = 0; t < kL2Ahead && t < w1.cnt; ++t) {
-                  tma_prefetch_l2_3d(&tmQ, 64 * b, 128 * (w1.i0 + t), w1.bh);
-                  tma_prefetch_l2_3d(&tmDO, 64 * b, 128 * (w1.i0 + t), w1.bh);
-                }
-              }
-            }
-          }
+          if (okl) nu = clc_decode(resp);
         }
         if (!__shfl_sync(0xffffffffu, okl, 0)) break;
         u = __shfl_sync(0xffffffffu, nu, 0);
@@ -505,7 +511,7 @@ __global__ void __launch_bounds__(384, 1)
       bool ok = true;
       int gi = 0;
       for (int su = 0; ok; ++su) {
-        if (!(ok = mbar_wait_w(&kv_full[su & 1], (su >> 1) & 1, g, kSiteDkdv | 2u))) break;
+        if (!(ok = mbar_wait_w(&k_full[su & 1], (su >> 1) & 1, g, kSiteDkdv | 2u))) break;
         const int u = unit_id[su & 1];
         if (u < 0) break;
         const int cnt = dkdv_unit<CAUSAL>(u, n_tiles, BH, band).cnt;
@@ -515,10 +521,12 @@ __global__ void __launch_bounds__(384, 1)
         if (!(ok = mbar_wait_w(&q_full[g0 % C::kQStages], qpar(g0), g, kSiteDkdv | 3u))) break;
         mma_nt<D>(tS, kK, kQ(g0 % C::kQStages));
         tc_commit_w(s_full);
+        if (cnt == 1) tc_commit_w(k_free);    // K_j: last reader issued
+        if (!(ok = mbar_wait_w(&v_full[su & 1], (su >> 1) & 1, g, kSiteDkdv | 3u))) break;
         if (!(ok = mbar_wait_w(&do_full[g0 % C::kDOStages], dpar(g0), g, kSiteDkdv | 3u))) break;
         mma_nt<D>(tDP, kV, kDO(g0 % C::kDOStages));
         tc_commit_w(dp_full);
-        if (cnt == 1) tc_commit_w(kv_free);   // K_j, V_j: last readers issued
+        if (cnt == 1) tc_commit_w(v_free);    // V_j: last reader issued
         for (int it = 0; ok && it < cnt; ++it) {
           const int i = g0 + it;
           const int qs = i % C::kQStages, ds = i % C::kDOStages;
@@ -545,6 +553,7 @@ __global__ void __launch_bounds__(384, 1)
             } else if (which == 0) {
               mma_nt<D>(tS, kK, kQ(qs1));                     // S^T(i+1)
               tc_commit_w(s_full);
+              if (it + 2 == cnt) tc_commit_w(k_free);       // K_j: last reader issued
               s_done = true;
             } else {
               tc_fence_after();
@@ -558,7 +567,7 @@ __global__ void __launch_bounds__(384, 1)
             if (!(ok = mbar_wait_w(&do_full[ds1], dpar(i + 1), g, kSiteDkdv | 13u))) break;
             mma_nt<D>(tDP, kV, kDO(ds1));                     // dP^T(i+1), after dK(i) has read dS^T(i)
             tc_commit_w(dp_full);
-            if (it + 2 == cnt) tc_commit_w(kv_free);        // K_j, V_j: last readers issued
+            if (it + 2 == cnt) tc_commit_w(v_free);         // V_j: last reader issued
           }
         }
         if (!ok) break;
@@ -586,7 +595,7 @@ __global__ void __launch_bounds__(384, 1)
   bool ok = true;
   int gi = 0;
   for (int su = 0; ok; ++su) {
-    if (!(ok = mbar_wait(&kv_full[su & 1], (su >> 1) & 1, g, kSiteDkdv | 17u))) break;
+    if (!(ok = mbar_wait(&k_full[su & 1], (su >> 1) & 1, g, kSiteDkdv | 17u))) break;
     const int u = unit_id[su & 1];
     if (u < 0) break;
     const DkdvUnit w = dkdv_unit<CAUSAL>(u, n_tiles, BH, band);
@@ -854,12 +863,6 @@ __global__ void __launch_bounds__(384, 1)
               clc_try_cancel(resp, sched);
             }
             if (!(ok = mbar_wait(&k_empty[ks], kpar(gk) ^ 1u, g, kSiteDq | 1u))) break;
-            if (it + kL2Ahead < w.cnt) {   // key tile it + kL2Ahead into L2 while this one lands
-              for (int b = 0; b < BwdCfg<D>::kBoxes; ++b) {
-                tma_prefetch_l2_3d(&tmK, 64 * b, 128 * (it + kL2Ahead), w.bh);
-                tma_prefetch_l2_3d(&tmV, 64 * b, 128 * (it + kL2Ahead), w.bh);
-              }
-            }
             mbar_arrive_expect_tx(&k_full[ks], C::kTileBytes);
             for (int b = 0; b < BwdCfg<D>::kBoxes; ++b)
               tma_load_3d(smem + C::k_off(ks) + b * BwdCfg<D>::kBoxBytes, &tmK, &k_full[ks], 64 * b, 128 * it,

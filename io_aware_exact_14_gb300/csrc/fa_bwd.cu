@@ -709,12 +709,16 @@ __global__ void __launch_bounds__(384, 1)
 // exiting, so TMEM, barriers and pipelines carry on and the next unit's loads
 // and first products overlap this unit's tail and epilogue.  The request goes
 // out a few tiles before the unit ends, so units still start in launch order
-// (heaviest first) on whichever CTA frees up first.
+// (heaviest first) on whichever CTA frees up first; the next unit's id is
+// published as soon as it is known, so the compute warps fetch its row terms
+// (-lse, -D) before this unit's epilogue.
 // Q_i and dO_i are resident per unit; K_j streams through a 3-deep ring (read
 // by S(j) and dQ(j)) and V_j through a 2-deep ring (read by dP(j) only); the
 // rings and the per-tile barriers run on across units (global tile count).
-// The epilogue stages dQ in the dO buffer for a TMA store, so the next unit's
-// Q (and its S(0)) can arrive while it runs; the next dO follows the store.
+// The epilogue stages dQ in the K slot of the unit's last key tile L (free
+// once dQ(L) is done); the producer stores it with TMA and reloads that slot
+// (with K(L+3)) only after the store has read it.  The next unit's Q loads
+// once this unit's last S is done, its dO once the last dP is.
 // MMA order S(j) dP(j) S(j+1) dQ(j) dP(j+1) ...: the exponentials of tile j
 // run under dP(j), the dS products under S(j+1).
 // TMEM: T0 = S, T1 = dP, acc = dQ.
@@ -728,12 +732,15 @@ struct DqCfg {
   static constexpr uint32_t kKOff = 2 * kTileBytes;
   static constexpr uint32_t kVOff = kKOff + kKStages * kTileBytes;
   static constexpr uint32_t kBarOff = kVOff + kVStages * kTileBytes;
-  // q_full, q_empty, do_full, k_full[3], k_empty[3], v_full[2], s_full[2], dp_full, ds_full,
-  // acc_done, acc_free, staged, drain, sched, id_taken.  A V slot has no empty
-  // barrier of its own: dP(j) is issued before dQ(j), whose commit releases K_j.
-  // One s_full per S buffer: its next phase (tile j+2) needs this tile's dS(j)
-  // first, so no barrier runs two phases ahead of a compute warp's wait.
-  static constexpr int kBars = 3 + 2 * kKStages + kVStages + 10;
+  // q_full, q_empty, do_full, do_empty, k_full[3], k_empty[3], v_full[2],
+  // s_full[2], dp_full, ds_full, acc_done, acc_free, drain, sched, id_taken,
+  // id_full[2], staged[4].  A V slot has no empty barrier of its own: dP(j) is
+  // issued before dQ(j), whose commit releases K_j.  One s_full per S buffer:
+  // its next phase (tile j+2) needs this tile's dS(j) first, so no barrier
+  // runs two phases ahead of a compute warp's wait.  id_full goes by unit
+  // parity, staged by unit index mod 4 (a unit's store waits for K(L+3), by
+  // which time at most three later units can have staged theirs).
+  static constexpr int kBars = 4 + 2 * kKStages + kVStages + 15;
   // readers of a unit id: the MMA warp, the eight compute warps, the dO loader
   static constexpr uint32_t kIdReaders = 10;
   static constexpr uint32_t kMiscOff = kBarOff + kBars * 8;   // tmem holder, abort flag, unit ids [2]
@@ -769,6 +776,22 @@ __device__ __forceinline__ DqUnit dq_unit(int u, int n_tiles, int BH, int band) 
   return w;
 }
 
+// A compute thread's row terms for unit u: -lse * log2(e) and -D of its query row.
+template <bool CAUSAL>
+__device__ __forceinline__ float2 dq_row_terms(int u, int n_tiles, int BH, int band, int N, int r,
+                                               const float* __restrict__ lse, const float* __restrict__ Dg) {
+  const DqUnit w = dq_unit<CAUSAL>(u, n_tiles, BH, band);
+  const int row = 128 * w.qt + r;
+  float2 t = make_float2(-INFINITY, 0.f);
+  if (row < N) {
+    const size_t idx = static_cast<size_t>(w.bh) * N + row;
+    const float l = lse[idx];
+    t.x = (l == -INFINITY) ? -INFINITY : -l * kLog2e;
+    t.y = -Dg[idx];
+  }
+  return t;
+}
+
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(384, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -788,7 +811,8 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* q_full = bars;
   uint64_t* q_empty = bars + 1;
   uint64_t* do_full = bars + 2;
-  uint64_t* k_full = bars + 3;
+  uint64_t* do_empty = bars + 3;
+  uint64_t* k_full = bars + 4;
   uint64_t* k_empty = k_full + C::kKStages;
   uint64_t* v_full = k_empty + C::kKStages;
   uint64_t* s_full = v_full + C::kVStages;
@@ -796,15 +820,16 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* ds_full = dp_full + 1;
   uint64_t* acc_done = ds_full + 1;
   uint64_t* acc_free = acc_done + 1;
-  uint64_t* staged = acc_free + 1;
-  uint64_t* drain = staged + 1;
+  uint64_t* drain = acc_free + 1;
   uint64_t* sched = drain + 1;
   uint64_t* id_taken = sched + 1;
+  uint64_t* id_full = id_taken + 1;   // [2], by unit parity
+  uint64_t* staged = id_full + 2;     // [4], by unit index mod 4
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kMiscOff + 4);
-  // Unit ids, by unit parity.  The producer publishes unit k+1 (id, then the
-  // q_full phase) only after every reader has taken unit k's id, so q_full is
-  // never two phases ahead of a reader's wait.
+  // Unit ids, by unit parity.  The producer publishes unit k+1's id (id_full)
+  // only after every reader has taken unit k's (id_taken), so no id is
+  // overwritten unread and no id_full phase runs two ahead of a reader.
   volatile int* unit_id = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 8);
   uint8_t* resp = smem + C::kRespOff;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -813,6 +838,7 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     mbar_init(do_full, 1);
+    mbar_init(do_empty, 1);
     for (int i = 0; i < C::kKStages; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
@@ -824,10 +850,11 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(ds_full, 256);
     mbar_init(acc_done, 1);
     mbar_init(acc_free, 256);
-    mbar_init(staged, 256);
     mbar_init(drain, 1);
     mbar_init(sched, 1);
     mbar_init(id_taken, C::kIdReaders);
+    for (int i = 0; i < 2; ++i) mbar_init(&id_full[i], 1);
+    for (int i = 0; i < 4; ++i) mbar_init(&staged[i], 256);
     unit_id[0] = static_cast<int>(blockIdx.x);
     *abort_flag = 0u;
     fence_mbar_init();
@@ -846,16 +873,35 @@ __global__ void __launch_bounds__(384, 1)
   auto vpar = [](int j) { return static_cast<uint32_t>((j / C::kVStages) & 1); };
 
   if (warp >= 8) {
-    if (warp == 8) {  // producer: per unit Q_i; K_j and V_j through their rings; next unit
+    if (warp == 8) {  // producer: unit ids; per unit Q_i; K_j and V_j through their rings; dQ stores
       if (lane == 0) {
+        // Pending dQ stores, oldest first (a ring of 4, by unit index): unit p
+        // ended at key tile last[p & 3] and staged dQ in that tile's K slot,
+        // which K(last + 3) reuses; the store goes out just before that load.
+        int pend_bh[4], pend_qt[4], pend_last[4];
+        int pend_head = 0, pend_tail = 0;   // unit indices: [head, tail) pending
+        auto store_front = [&]() -> bool {
+          const int p = pend_head & 3;
+          if (!mbar_wait(&staged[p], (pend_head >> 2) & 1, g, kSiteDq | 18u)) return false;
+          for (int b = 0; b < BwdCfg<D>::kBoxes; ++b)
+            tma_store_3d(&tmDQ, smem + C::k_off(pend_last[p] % C::kKStages) + b * BwdCfg<D>::kBoxBytes, 64 * b,
+                         128 * pend_qt[p], pend_bh[p]);
+          tma_store_commit();
+          tma_store_wait_read_all();
+          ++pend_head;
+          return true;
+        };
+        mbar_arrive(&id_full[0]);   // unit 0: this CTA's own (its id was written before the start)
         int u = static_cast<int>(blockIdx.x);
         int gk = 0;   // global key-tile count (ring index)
-        for (int su = 0;; ++su) {
+        bool ok = true;
+        for (int su = 0; ok; ++su) {
           const DqUnit w = dq_unit<CAUSAL>(u, n_tiles, BH, band);
+          // Q_i: the previous unit's last S product has read the buffer
+          if (su > 0 && !(ok = mbar_wait(q_empty, (su - 1) & 1, g, kSiteDq | 14u))) break;
           mbar_arrive_expect_tx(q_full, C::kTileBytes);
           for (int b = 0; b < BwdCfg<D>::kBoxes; ++b)
             tma_load_3d(smem + C::kQOff + b * BwdCfg<D>::kBoxBytes, &tmQ, q_full, 64 * b, 128 * w.qt, w.bh);
-          bool ok = true;
           for (int it = 0; it < w.cnt; ++it, ++gk) {
             const int ks = gk % C::kKStages, vs = gk % C::kVStages;
             if (it == max(0, w.cnt - C::kRequestAhead)) {   // ask for the next unit
@@ -863,6 +909,8 @@ __global__ void __launch_bounds__(384, 1)
               clc_try_cancel(resp, sched);
             }
             if (!(ok = mbar_wait(&k_empty[ks], kpar(gk) ^ 1u, g, kSiteDq | 1u))) break;
+            // a unit that ended at key tile gk - 3 staged its dQ in this slot
+            if (pend_head < pend_tail && pend_last[pend_head & 3] + C::kKStages == gk && !(ok = store_front())) break;
             mbar_arrive_expect_tx(&k_full[ks], C::kTileBytes);
             for (int b = 0; b < BwdCfg<D>::kBoxes; ++b)
               tma_load_3d(smem + C::k_off(ks) + b * BwdCfg<D>::kBoxBytes, &tmK, &k_full[ks], 64 * b, 128 * it,
@@ -878,7 +926,13 @@ __global__ void __launch_bounds__(384, 1)
               tma_load_3d(smem + C::v_off(vs) + b * BwdCfg<D>::kBoxBytes, &tmV, &v_full[vs], 64 * b, 128 * it,
                           w.bh);
           }
-          if (!ok || !mbar_wait(sched, su & 1, g, kSiteDq | 13u)) break;
+          if (!ok) break;
+          const int p = pend_tail & 3;   // at most three older stores are still pending here
+          pend_bh[p] = w.bh;
+          pend_qt[p] = w.qt;
+          pend_last[p] = gk - 1;
+          ++pend_tail;
+          if (!(ok = mbar_wait(sched, su & 1, g, kSiteDq | 13u))) break;
           u = clc_decode(resp);
           if (u >= 0) {   // the next unit's first tiles into L2 while this unit finishes
             const DqUnit w1 = dq_unit<CAUSAL>(u, n_tiles, BH, band);
@@ -891,39 +945,31 @@ __global__ void __launch_bounds__(384, 1)
               }
             }
           }
-          // Q_i is free once this unit's last S product is done; every reader
-          // has taken this unit's id before the next one is published
-          if (!mbar_wait(q_empty, su & 1, g, kSiteDq | 14u)) break;
-          if (!mbar_wait(id_taken, su & 1, g, kSiteDq | 20u)) break;
+          // publish the next unit's id once every reader has taken this one's
+          if (!(ok = mbar_wait(id_taken, su & 1, g, kSiteDq | 20u))) break;
           unit_id[(su + 1) & 1] = u;
-          if (u < 0) {      // no work left: release the consumers with an empty phase
-            mbar_arrive(q_full);
+          mbar_arrive(&id_full[(su + 1) & 1]);
+          if (u < 0) {   // no work left: release the MMA warp with an empty Q phase
+            if (mbar_wait(q_empty, su & 1, g, kSiteDq | 14u)) mbar_arrive(q_full);
             break;
           }
         }
+        while (ok && pend_head < pend_tail) ok = store_front();   // the remaining stores
+        tma_store_wait_all();   // every store has landed before the CTA retires
       }
-    } else if (warp == 10) {  // dO buffer owner: stores each unit's dQ from it, then loads the next dO
+    } else if (warp == 10) {  // dO loader: each unit's dO once the previous unit's last dP is done
       if (lane == 0) {
-        DqUnit prev{0, 0, 0};
         for (int su = 0;; ++su) {
-          if (!mbar_wait_backoff(q_full, su & 1, g, kSiteDq | 17u)) break;
+          if (!mbar_wait_backoff(&id_full[su & 1], (su >> 1) & 1, g, kSiteDq | 17u)) break;
           const int u = unit_id[su & 1];
-          if (u >= 0) mbar_arrive(id_taken);
-          if (su > 0) {   // the previous unit's dQ, staged by the compute warps
-            if (!mbar_wait_backoff(staged, (su - 1) & 1, g, kSiteDq | 18u)) break;
-            for (int b = 0; b < BwdCfg<D>::kBoxes; ++b)
-              tma_store_3d(&tmDQ, smem + C::kDOOff + b * BwdCfg<D>::kBoxBytes, 64 * b, 128 * prev.qt, prev.bh);
-            tma_store_commit();
-            tma_store_wait_read_all();
-          }
           if (u < 0) break;
-          prev = dq_unit<CAUSAL>(u, n_tiles, BH, band);
+          mbar_arrive(id_taken);
+          if (su > 0 && !mbar_wait_backoff(do_empty, (su - 1) & 1, g, kSiteDq | 19u)) break;
+          const DqUnit w = dq_unit<CAUSAL>(u, n_tiles, BH, band);
           mbar_arrive_expect_tx(do_full, C::kTileBytes);
           for (int b = 0; b < BwdCfg<D>::kBoxes; ++b)
-            tma_load_3d(smem + C::kDOOff + b * BwdCfg<D>::kBoxBytes, &tmDO, do_full, 64 * b, 128 * prev.qt,
-                        prev.bh);
+            tma_load_3d(smem + C::kDOOff + b * BwdCfg<D>::kBoxBytes, &tmDO, do_full, 64 * b, 128 * w.qt, w.bh);
         }
-        tma_store_wait_all();   // the last stores have landed before the CTA retires
       }
     } else if (warp == 9) {  // MMA issuer: the whole warp runs the loop, one lane issues
       const uint32_t tDP = tmem + C::kColDP, tDQ = tmem + C::kColAcc;
@@ -955,6 +1001,7 @@ __global__ void __launch_bounds__(384, 1)
         if (!(ok = mbar_wait_w(do_full, su & 1, g, kSiteDq | 19u))) break;
         mma_nt<D>(tDP, kDO, kV(g0 % C::kVStages));
         tc_commit_w(dp_full);
+        if (cnt == 1) tc_commit_w(do_empty);   // dO_i: last reader issued
         for (int it = 0; it < cnt; ++it) {
           const int j = g0 + it;   // global index of key tile it
           const uint32_t par = j & 1;
@@ -987,6 +1034,7 @@ __global__ void __launch_bounds__(384, 1)
           if (!(ok = mbar_wait_w(&v_full[(j + 1) % C::kVStages], vpar(j + 1), g, kSiteDq | 12u))) break;
           mma_nt<D>(tDP, kDO, kV((j + 1) % C::kVStages));
           tc_commit_w(dp_full);
+          if (it + 2 == cnt) tc_commit_w(do_empty);   // dO_i: last reader issued
         }
         gk = g0 + cnt;
       }
@@ -1007,24 +1055,16 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
   const uint32_t tDP = tmem + lane_base + C::kColDP + 64 * h;
   const float2 sc2 = make_float2(scale_log2, scale_log2);
-  bool ok = true;
+  bool ok = mbar_wait(&id_full[0], 0, g, kSiteDq | 16u);
+  int u = unit_id[0];
+  __syncwarp();
+  if (ok && lane == 0) mbar_arrive(id_taken);
+  float2 terms = dq_row_terms<CAUSAL>(u, n_tiles, BH, band, N, r, lse, Dg);
   int gk = 0;
-  for (int su = 0; ok; ++su) {
-    if (!(ok = mbar_wait(q_full, su & 1, g, kSiteDq | 16u))) break;
-    const int u = unit_id[su & 1];
-    if (u < 0) break;
-    __syncwarp();
-    if (lane == 0) mbar_arrive(id_taken);
+  for (int su = 0; ok && u >= 0; ++su) {
     const DqUnit w = dq_unit<CAUSAL>(u, n_tiles, BH, band);
-    const size_t row_base = static_cast<size_t>(w.bh) * N;
     const int row = 128 * w.qt + r;
-    float nlse2 = -INFINITY, ndrow = 0.f;   // -lse * log2(e) and -D of this row
-    if (row < N) {
-      const float l = lse[row_base + row];
-      nlse2 = (l == -INFINITY) ? -INFINITY : -l * kLog2e;
-      ndrow = -Dg[row_base + row];
-    }
-    const float2 nl2 = make_float2(nlse2, nlse2), nd2 = make_float2(ndrow, ndrow);
+    const float2 nl2 = make_float2(terms.x, terms.x), nd2 = make_float2(terms.y, terms.y);
     for (int it = 0; ok && it < w.cnt; ++it, ++gk) {
       const uint32_t par = gk & 1;
       if (!(ok = mbar_wait(&s_full[gk & 1], (gk >> 1) & 1, g, kSiteDq | 7u))) break;
@@ -1077,14 +1117,21 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_before();
       mbar_arrive(ds_full);
     }
-    if (!ok || !(ok = mbar_wait(acc_done, su & 1, g, kSiteDq | 9u))) break;
+    if (!ok) break;
+    // the next unit's id and row terms: their loads overlap this epilogue
+    if (!(ok = mbar_wait(&id_full[(su + 1) & 1], ((su + 1) >> 1) & 1, g, kSiteDq | 16u))) break;
+    const int u_next = unit_id[(su + 1) & 1];
+    __syncwarp();
+    if (u_next >= 0 && lane == 0) mbar_arrive(id_taken);
+    if (u_next >= 0) terms = dq_row_terms<CAUSAL>(u_next, n_tiles, BH, band, N, r, lse, Dg);
+    if (!(ok = mbar_wait(acc_done, su & 1, g, kSiteDq | 9u))) break;
     __syncwarp();
     tc_fence_after();
-    // epilogue: both warpgroups stage dQ (x scale, bf16) in the dO buffer (its
-    // last reader, dP, finished before acc_done); the dO buffer's owner warp
-    // stores it with TMA and then refills the buffer, so no compute warp waits
+    // epilogue: both warpgroups stage dQ (x scale, bf16) in the K slot of the
+    // unit's last key tile (its last reader, dQ, finished before acc_done);
+    // the producer stores it with TMA before that slot is reloaded
     {
-      const uint32_t stage = sbase + C::kDOOff;
+      const uint32_t stage = sbase + C::k_off((gk - 1) % C::kKStages);
 #pragma unroll
       for (int c = h * (D / 2); c < (h + 1) * (D / 2); c += 32) {
         uint32_t o[32];
@@ -1104,8 +1151,9 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_before();
       mbar_arrive(acc_free);   // the accumulator may be overwritten
       fence_proxy_async_smem();
-      mbar_arrive(staged);
+      mbar_arrive(&staged[su & 3]);
     }
+    u = u_next;
   }
   __syncwarp();
   tc_fence_before();

@@ -86,11 +86,10 @@ __global__ void __launch_bounds__(kPreThreads) fa_bwd_preprocess_kernel(const ui
 // Shared layout: one CTA per SM, 384 threads.
 //   warps 0-3  compute warpgroup 0: columns [0, 64) of each 128 x 128 tile
 //   warps 4-7  compute warpgroup 1: columns [64, 128)
-//   warp  8    producer (TMA tiles and the work-unit sequence; in dK/dV the
-//              whole warp gathers the row vectors, and lane 0 also issues the
-//              epilogue stores)
+//   warp  8    producer (TMA tiles, the work-unit sequence and the epilogue
+//              stores; in dK/dV the whole warp also writes the row vectors)
 //   warp  9    TMEM owner and tcgen05.mma issuer (elect.sync in a converged warp)
-//   warp  10   dQ: owner of the dO buffer (dQ epilogue store, next dO load)
+//   warp  10   dQ: loads each unit's dO
 //   others     idle
 // TMEM (512 columns): scores, dP, then accumulators (dQ double-buffers its
 // scores in the columns its single accumulator leaves free).  bf16 operands

@@ -141,3 +141,40 @@ def test_dq_concurrent_streams_bitwise():
         torch.cuda.synchronize()
         assert_no_timeout()
         assert torch.equal(out[0], ref[0][2]) and torch.equal(out[1], ref[1][2])
+
+
+def test_dkdv_concurrent_streams_bitwise():
+    """The dK/dV kernel, like dQ, takes work over from not-yet-started CTAs of
+    its own grid: two launches running at once on two streams must each give
+    exactly what they give alone."""
+    _, ga = device_inputs(2, 4, 1500, 128, seed=33, with_grad=True)
+    _, gb = device_inputs(2, 4, 1500, 128, seed=34, with_grad=True)
+    ref = []
+    for g in (ga, gb):
+        o, lse = fa.fa_fwd(g["q"], g["k"], g["v"], None, True)
+        Dvec = fa.fa_bwd_preprocess(o, g["do"])
+        torch.cuda.synchronize()
+        dk, dv = fa.fa_bwd_dkdv(g["q"], g["k"], g["v"], lse, g["do"], Dvec, None, True)
+        torch.cuda.synchronize()
+        ref.append((lse, Dvec, dk, dv))
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    out = [(torch.empty_like(r[2]), torch.empty_like(r[3])) for r in ref]
+    for _ in range(3):
+        for g, (lse, Dvec, _, _), s, (dk, dv) in zip((ga, gb), ref, (sa, sb), out):
+            fa.fa_bwd_dkdv(g["q"], g["k"], g["v"], lse, g["do"], Dvec, None, True, dk=dk, dv=dv, stream=s)
+        torch.cuda.synchronize()
+        assert_no_timeout()
+        for (dk, dv), r in zip(out, ref):
+            assert torch.equal(dk, r[2]) and torch.equal(dv, r[3])
+
+
+@pytest.mark.parametrize("B,H,N,d,causal", [(4, 64, 300, 64, True), (2, 96, 256, 128, False)])
+def test_bwd_many_short_units_parity(B, H, N, d, causal):
+    """Hundreds of one- to three-tile work units, several per persistent CTA:
+    the protocols that carry rings, barriers and epilogue stores from one unit
+    to the next (and the stores still pending when a CTA runs out of work)."""
+    x, g = device_inputs(B, H, N, d, seed=900 + N + d, with_grad=True)
+    scale = 1.0 / np.sqrt(d)
+    _, _, dq, dk, dv = _grads(g, scale, causal)
+    ref = oracle.attn_bwd_ref(f64(x["q"]), f64(x["k"]), f64(x["v"]), f64(x["do"]), scale, causal)
+    _assert_grads((dq, dk, dv), ref)

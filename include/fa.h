@@ -68,6 +68,38 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  struct CUstream_st* stream);
 
 /*
+ * Split-KV forward (non-causal) for short query blocks against long key
+ * sequences, e.g. decoding: the keys are cut into num_splits chunks of whole
+ * 128-key tiles, each chunk's (O_s, LSE_s) is computed as in fa_fwd and the
+ * chunks are merged with the two-block merge identity of [WHY-FAST]
+ * "在线Softmax技巧" (LSE = log sum_s e^{LSE_s}, O = sum_s e^{LSE_s - LSE} O_s),
+ * which reaches the same exact result.
+ *   q          in : bf16 [B, H, Nq, d]
+ *   k, v       in : bf16 [B, H, Nk, d]
+ *   o          out: bf16 [B, H, Nq, d]
+ *   lse        out: fp32 [B, H, Nq]  (Nk == 0: O = 0, LSE = -inf)
+ *   num_splits  chunks wanted (<= 0: chosen from the SM count); the count
+ *               used is at most ceil(Nk / 128), every chunk non-empty
+ *   workspace   scratch for the chunks' fp32 (O_s, LSE_s), owned by the
+ *               caller, 16-byte aligned, at least
+ *               fa_fwd_splitkv_workspace_bytes(...) bytes (may be NULL when
+ *               that is 0); FA_ERR_WORKSPACE otherwise
+ * Nq == 0 is a no-op; k and v may be NULL when Nk == 0.  Sizes, alignment
+ * and overlap rules as for fa_fwd, with Nq and Nk each in place of N.
+ */
+fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                         int B, int H, int Nq, int Nk, int d, float scale, int num_splits,
+                         void* workspace, size_t workspace_bytes, struct CUstream_st* stream);
+
+/*
+ * Workspace bytes fa_fwd_splitkv needs for these arguments (the same
+ * num_splits rule, on the current device): n_used * B*H*Nq*d fp32 partial
+ * outputs plus n_used * B*H*Nq fp32 partial LSE, each rounded up to 256
+ * bytes.  0 for invalid sizes, Nq == 0 or Nk == 0.
+ */
+size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int d, int num_splits);
+
+/*
  * Bytes of device workspace fa_bwd needs: the fp32 row term D [B, H, N],
  * rounded up to 256 bytes.  Returns 0 for N <= 0 or invalid sizes.
  */

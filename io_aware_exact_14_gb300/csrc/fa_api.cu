@@ -113,6 +113,41 @@ fa_status cuda_status(cudaError_t e, const char* what) {
   return e == cudaSuccess ? FA_OK : fail(what, static_cast<int>(e), cudaGetErrorString(e));
 }
 
+// 3-D view {d, Nq, Z} of fp32 rows (split-KV partial outputs, Z = splits *
+// B*H); boxes of 32 floats (128 bytes) x 128 rows, 128-byte swizzle.
+fa_status make_map_f32(CUtensorMap* m, const void* base, int d, int Nq, long long Z) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(Nq), static_cast<cuuint64_t>(Z)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(Nq) * d * 4};
+  const cuuint32_t box[3] = {32, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box,
+                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : fail("cuTensorMapEncodeTiled", static_cast<int>(r), "invalid tensor map");
+}
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Split-KV workspace: fp32 partial O [n, B*H, Nq, d], then fp32 partial LSE [n, B*H, Nq].
+struct SplitPlan {
+  int kt_per_split, n_splits;
+  size_t o_bytes, lse_bytes;
+};
+
+fa_status split_plan(int B, int H, int Nq, int Nk, int d, int want, SplitPlan& p) {
+  int sms = 0;
+  if (want <= 0) {
+    int dev = 0;
+    FA_TRY(cuda_status(cudaGetDevice(&dev), "cudaGetDevice"));
+    FA_TRY(cuda_status(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev), "cudaDeviceGetAttribute"));
+  }
+  fa::splitkv_chunks(B, H, Nq, Nk, want, sms, p.kt_per_split, p.n_splits);
+  const size_t rows = static_cast<size_t>(B) * H * Nq * p.n_splits;
+  p.o_bytes = round256(rows * d * 4);
+  p.lse_bytes = round256(rows * 4);
+  return FA_OK;
+}
+
 fa_status dkdv_checked(const void* q, const void* k, const void* v, const float* lse, const void* dO,
                        const float* Dvec, void* dk, void* dv, const Shape& s, cudaStream_t st) {
   if (!load_encoder()) return FA_ERR_CUDA;
@@ -158,6 +193,49 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   FA_TRY(make_map(&tv, v, s));
   FA_TRY(make_map(&to, o, s));
   return cuda_status(fa::launch_fwd(tq, tk, tv, to, lse, s, stream), "forward kernel launch");
+}
+
+fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+                         int Nk, int d, float scale, int num_splits, void* workspace, size_t workspace_bytes,
+                         struct CUstream_st* stream) {
+  FA_TRY(check_sizes(B, H, Nq, d));
+  FA_TRY(check_sizes(B, H, Nk, d));
+  if (Nq == 0) return FA_OK;
+  FA_TRY(check_ptrs({q, o}, {lse}));
+  if (Nk > 0) FA_TRY(check_ptrs({k, v}, {}));   // never read when there are no keys
+  FA_TRY(check_scale(scale));
+  SplitPlan p;
+  FA_TRY(split_plan(B, H, Nq, Nk, d, num_splits, p));
+  if (static_cast<long long>(B) * H * p.n_splits * ((Nq + 127) / 128) > INT32_MAX) return FA_ERR_UNSUPPORTED;
+  const size_t need = p.n_splits > 0 ? p.o_bytes + p.lse_bytes : 0;
+  if (need > 0 && (workspace == nullptr || !aligned(workspace, 16) || workspace_bytes < need)) return FA_ERR_WORKSPACE;
+  const Shape sq{B, H, Nq, d, scale, 0}, sk{B, H, Nk, d, scale, 0};
+  const size_t qb = tensor_bytes(sq), kb = tensor_bytes(sk);
+  FA_TRY(check_disjoint({{o, qb}, {lse, vec_bytes(sq)}, {workspace, need}}, {{q, qb}, {k, kb}, {v, kb}}));
+  if (!load_encoder()) return FA_ERR_CUDA;
+  CUtensorMap tq, tk, tv, top;
+  FA_TRY(make_map(&tq, q, sq));
+  if (p.n_splits > 0) {
+    FA_TRY(make_map(&tk, k, sk));
+    FA_TRY(make_map(&tv, v, sk));
+    FA_TRY(make_map_f32(&top, workspace, d, Nq, static_cast<long long>(p.n_splits) * B * H));
+  } else {
+    tk = tq;
+    tv = tq;
+    top = tq;
+  }
+  const float* o_part = static_cast<const float*>(workspace);
+  float* lse_part = p.n_splits > 0 ? reinterpret_cast<float*>(static_cast<char*>(workspace) + p.o_bytes) : nullptr;
+  return cuda_status(fa::launch_fwd_splitkv(tq, tk, tv, top, o_part, lse_part, o, lse, sq, Nk, p.n_splits,
+                                            p.kt_per_split, stream),
+                     "split-KV forward launch");
+}
+
+size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int d, int num_splits) {
+  if (check_sizes(B, H, Nq, d) != FA_OK || check_sizes(B, H, Nk, d) != FA_OK || Nq <= 0 || Nk <= 0) return 0;
+  SplitPlan p;
+  if (split_plan(B, H, Nq, Nk, d, num_splits, p) != FA_OK || p.n_splits == 0) return 0;
+  return p.o_bytes + p.lse_bytes;
 }
 
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {

@@ -79,12 +79,17 @@ struct FwdCfg {
   __host__ __device__ static constexpr uint32_t col_o(int tile) { return tile ? 256u + D : 256u; }
 };
 
+// A CTA's work: head bh, query tiles qt0 (and qt0 + 1 when n1 > 0), key
+// tiles kt0 .. kt0 + n - 1 (n0 / n1 of them for tile 0 / 1), and the key
+// split whose partial result it writes (split-KV launches only).
 struct FwdWork {
-  int bh, qt0, n0, n1, n;
+  int bh, qt0, n0, n1, n, kt0, split;
 };
 
 __device__ __forceinline__ FwdWork fwd_work(int N, int n_pairs, int BH, int band, bool causal) {
   FwdWork w;
+  w.kt0 = 0;
+  w.split = 0;
   int rank;
   banded_order(blockIdx.x, n_pairs, BH, band, w.bh, rank);
   const int pair = n_pairs - 1 - rank;  // heavy (causal) pairs first
@@ -94,6 +99,22 @@ __device__ __forceinline__ FwdWork fwd_work(int N, int n_pairs, int BH, int band
   w.n0 = causal ? min(w.qt0 + 1, n_qt) : n_qt;
   w.n1 = qt1 < n_qt ? (causal ? min(qt1 + 1, n_qt) : n_qt) : 0;
   w.n = max(w.n0, w.n1);
+  return w;
+}
+
+// Split-KV: CTA u takes one query tile of one head and one chunk of
+// kt_per_split key tiles (the last chunk may be shorter, never empty).  CTAs
+// of one (head, chunk) are adjacent, so they share the chunk's K/V in L2.
+__device__ __forceinline__ FwdWork fwd_split_work(int u, int n_qt, int n_splits, int kt_per_split, int n_kt) {
+  FwdWork w;
+  w.qt0 = u % n_qt;
+  const int rest = u / n_qt;
+  w.split = rest % n_splits;
+  w.bh = rest / n_splits;
+  w.kt0 = w.split * kt_per_split;
+  w.n0 = min(kt_per_split, n_kt - w.kt0);
+  w.n1 = 0;
+  w.n = w.n0;
   return w;
 }
 
@@ -131,12 +152,14 @@ __device__ __forceinline__ void fwd_producer(const FwdWork& w, uint8_t* smem, ui
       }
       if (j + kL2Ahead < w.n) {   // the same tile kL2Ahead steps on, into L2 while this one lands
 #pragma unroll
-        for (int b = 0; b < C::kBoxes; ++b) tma_prefetch_l2_3d(kind ? tmV : tmK, 64 * b, 128 * (j + kL2Ahead), w.bh);
+        for (int b = 0; b < C::kBoxes; ++b)
+          tma_prefetch_l2_3d(kind ? tmV : tmK, 64 * b, 128 * (w.kt0 + j + kL2Ahead), w.bh);
       }
       uint8_t* dst = smem + C::kSlotOff + (idx % C::kSlots) * C::kTileBytes;
 #pragma unroll
       for (int b = 0; b < C::kBoxes; ++b)
-        tma_load_3d(dst + b * C::kBoxBytes, kind ? tmV : tmK, &full[grp % C::kGroups], 64 * b, 128 * j, w.bh);
+        tma_load_3d(dst + b * C::kBoxBytes, kind ? tmV : tmK, &full[grp % C::kGroups], 64 * b, 128 * (w.kt0 + j),
+                    w.bh);
       issued = idx + 1;
     }
   }
@@ -279,11 +302,15 @@ __device__ __forceinline__ void fwd_mma_both(const FwdWork& w, uint32_t tmem, ui
   }
 }
 
-template <int D, bool CAUSAL>
+// SPLIT: a split-KV CTA (one query tile, one chunk of keys): O of the chunk
+// is stored in fp32 to the partial-output map (z = split * BH + bh) and the
+// chunk's LSE to lse[(split * BH + bh) * N + row]; otherwise O goes out in
+// bf16 and z = bh, split = 0.  N is the query length, Nk the key length.
+template <int D, bool CAUSAL, bool SPLIT>
 __device__ __forceinline__ void fwd_softmax(const FwdWork& w, int tile, uint32_t tmem, uint8_t* smem,
                                             uint64_t* s_full, uint64_t* p_full, uint64_t* o_done,
                                             uint64_t* staged, const CUtensorMap* tmO, float* __restrict__ lse, int N,
-                                            float scale_log2, const CtaGuard& g) {
+                                            int Nk, int BH, float scale_log2, const CtaGuard& g) {
   using C = FwdCfg<D>;
   const int n_i = tile ? w.n1 : w.n0;
   if (n_i == 0) return;
@@ -311,8 +338,8 @@ __device__ __forceinline__ void fwd_softmax(const FwdWork& w, int tile, uint32_t
     tmem_ld_fence(s[3]);
 
     // keys kv0 .. kv0+lim-1 are visible to this row
-    const int kv0 = j * 128;
-    int lim = N - kv0;
+    const int kv0 = (w.kt0 + j) * 128;
+    int lim = Nk - kv0;
     if (CAUSAL) lim = min(lim, row - kv0 + 1);
     if (lim < 128) {
 #pragma unroll
@@ -384,41 +411,78 @@ __device__ __forceinline__ void fwd_softmax(const FwdWork& w, int tile, uint32_t
   __syncwarp();
   tc_fence_after();
   const float inv_l = l > 0.f ? 1.f / l : 0.f;
-  const uint32_t stage = smem_u32(smem + C::kQOff + tile * C::kTileBytes);
+  if constexpr (SPLIT) {
+    // fp32 staging: D/32 boxes of 128 rows x 32 floats (128-byte rows, swizzled)
+    // across both Q buffers; a split-KV CTA has one query tile, and its last
+    // S product (the Q buffer's last reader) finished before o_done
+    static_assert(2 * C::kTileBytes >= 128u * D * 4u, "fp32 staging fits the two Q buffers");
+    const uint32_t stage = smem_u32(smem + C::kQOff);
 #pragma unroll
-  for (int c = 0; c < D; c += 32) {
-    uint32_t o[32];
-    tmem_ld32(tO + c, o);
-    tmem_ld_wait(o);
-    const uint32_t box = stage + (c / 64) * C::kBoxBytes + r * 128;
+    for (int c = 0; c < D; c += 32) {
+      uint32_t o[32];
+      tmem_ld32(tO + c, o);
+      tmem_ld_wait(o);
+      const uint32_t box = stage + (c / 32) * 16384u + r * 128;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int chunk = (c % 64) / 8 + q;
-      float f[8];
+      for (int q = 0; q < 8; ++q)
+        st_shared_v4(box + ((q ^ (r & 7)) << 4), __float_as_uint(__uint_as_float(o[4 * q]) * inv_l),
+                     __float_as_uint(__uint_as_float(o[4 * q + 1]) * inv_l),
+                     __float_as_uint(__uint_as_float(o[4 * q + 2]) * inv_l),
+                     __float_as_uint(__uint_as_float(o[4 * q + 3]) * inv_l));
+    }
+    fence_proxy_async_smem();
+    mbar_arrive(&staged[tile]);
+    if (r == 0 && mbar_wait(&staged[tile], 0, g, kSiteFwd | 8u)) {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(o[8 * q + e]) * inv_l;
-      st_shared_v4(box + ((chunk ^ (r & 7)) << 4), pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
-                   pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+      for (int b = 0; b < D / 32; ++b)
+        tma_store_3d(tmO, smem + C::kQOff + b * 16384u, 32 * b, qt * 128, w.split * BH + w.bh);
+      tma_store_commit();
+      tma_store_wait_read_all();
+    }
+  } else {
+    const uint32_t stage = smem_u32(smem + C::kQOff + tile * C::kTileBytes);
+#pragma unroll
+    for (int c = 0; c < D; c += 32) {
+      uint32_t o[32];
+      tmem_ld32(tO + c, o);
+      tmem_ld_wait(o);
+      const uint32_t box = stage + (c / 64) * C::kBoxBytes + r * 128;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int chunk = (c % 64) / 8 + q;
+        float f[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(o[8 * q + e]) * inv_l;
+        st_shared_v4(box + ((chunk ^ (r & 7)) << 4), pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                     pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+      }
+    }
+    fence_proxy_async_smem();
+    mbar_arrive(&staged[tile]);
+    if (r == 0 && mbar_wait(&staged[tile], 0, g, kSiteFwd | 8u)) {
+#pragma unroll
+      for (int b = 0; b < C::kBoxes; ++b)
+        tma_store_3d(tmO, smem + C::kQOff + tile * C::kTileBytes + b * C::kBoxBytes, 64 * b, qt * 128, w.bh);
+      tma_store_commit();
+      tma_store_wait_read_all();
     }
   }
-  fence_proxy_async_smem();
-  mbar_arrive(&staged[tile]);
-  if (r == 0 && mbar_wait(&staged[tile], 0, g, kSiteFwd | 8u)) {
-#pragma unroll
-    for (int b = 0; b < C::kBoxes; ++b)
-      tma_store_3d(tmO, smem + C::kQOff + tile * C::kTileBytes + b * C::kBoxBytes, 64 * b, qt * 128, w.bh);
-    tma_store_commit();
-    tma_store_wait_read_all();
-  }
-  if (row < N) lse[static_cast<size_t>(w.bh) * N + row] = l > 0.f ? (m_use + __log2f(l)) * kLn2 : -INFINITY;
+  if (row < N)
+    lse[static_cast<size_t>(w.split * BH + w.bh) * N + row] = l > 0.f ? (m_use + __log2f(l)) * kLn2 : -INFINITY;
 }
 
 // ISSUERS: MMA-issuing warps, 1 (warp 9 issues both tiles) or 2 (one per tile).
-template <int D, bool CAUSAL, int ISSUERS>
+// SPLIT: a split-KV launch (non-causal, one issuer): CTA u takes query tile
+// u % n_qt of one head and one chunk of kt_per_split of the n_kt key tiles;
+// tmO is then the fp32 partial-output map and lse the partial LSE.  N is the
+// query length and Nk the key length (equal outside split-KV launches).
+template <int D, bool CAUSAL, int ISSUERS, bool SPLIT>
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                  float* __restrict__ lse, int N, int n_pairs, int BH, int band, float scale_log2) {
+                  float* __restrict__ lse, int N, int n_pairs, int BH, int band, float scale_log2, int Nk,
+                  int n_qt, int n_kt, int n_splits, int kt_per_split) {
+  static_assert(!SPLIT || (!CAUSAL && ISSUERS == 1), "split-KV launches are non-causal with one issuer");
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -436,7 +500,8 @@ __global__ void __launch_bounds__(384, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const FwdWork w = fwd_work(N, n_pairs, BH, band, CAUSAL);
+  const FwdWork w = SPLIT ? fwd_split_work(static_cast<int>(blockIdx.x), n_qt, n_splits, kt_per_split, n_kt)
+                          : fwd_work(N, n_pairs, BH, band, CAUSAL);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kGroups; ++i) {
@@ -493,8 +558,8 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else {
     regs_inc<C::kRegsSoftmax>();
-    fwd_softmax<D, CAUSAL>(w, warp >> 2, tmem, smem, s_full, p_full, o_done, staged, &tmO, lse, N, scale_log2,
-                           g);
+    fwd_softmax<D, CAUSAL, SPLIT>(w, warp >> 2, tmem, smem, s_full, p_full, o_done, staged, &tmO, lse, N, Nk, BH,
+                                  scale_log2, g);
     __syncwarp();
     tc_fence_before();
     named_bar_sync(1, 256 + 32 * ISSUERS);
@@ -505,7 +570,7 @@ template <int D, bool CAUSAL, int ISSUERS>
 cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& to, float* lse, const Shape& s, cudaStream_t st) {
   using C = FwdCfg<D>;
-  auto kern = fa_fwd_kernel<D, CAUSAL, ISSUERS>;
+  auto kern = fa_fwd_kernel<D, CAUSAL, ISSUERS, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   // The warpgroups' register split must fit the launch allocation, or the
@@ -519,11 +584,100 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
   const dim3 grid(static_cast<unsigned>(s.B) * s.H * n_pairs);
   kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, to, lse, s.N, n_pairs, s.B * s.H, head_band(s.N, s.d),
-                                                 scale_log2);
+                                                 scale_log2, s.N, n_qt, n_qt, 1, n_qt);
+  return cudaGetLastError();
+}
+
+// Split-KV merge: for each query row, the chunks' (O_s, LSE_s) combine by the
+// two-block merge identity of [WHY-FAST] "在线Softmax技巧" applied to all
+// chunks at once: LSE = log sum_s e^{LSE_s}, O = sum_s e^{LSE_s - LSE} O_s
+// (each O_s is its chunk's normalised output).  HBM-bound: one warp per row,
+// each lane D/32 consecutive floats of every chunk; a row whose chunks are
+// all empty (or that has none) gets O = 0, LSE = -inf.
+template <int D>
+__global__ void __launch_bounds__(256) fa_fwd_merge_kernel(const float* __restrict__ o_part,
+                                                           const float* __restrict__ lse_part,
+                                                           __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
+                                                           long long rows, int n_splits) {
+  constexpr int kPer = D / 32;
+  const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;   // whole warps: one row each
+  float m = -INFINITY;
+  for (int s = lane; s < n_splits; s += 32) m = fmaxf(m, lse_part[static_cast<long long>(s) * rows + row]);
+#pragma unroll
+  for (int w = 16; w > 0; w /= 2) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, w));
+  float acc[kPer];
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
+  float wsum = 0.f;
+  if (m != -INFINITY) {
+    for (int s = 0; s < n_splits; ++s) {
+      const long long idx = static_cast<long long>(s) * rows + row;
+      const float ls = lse_part[idx];
+      const float wgt = ls == -INFINITY ? 0.f : __expf(ls - m);
+      wsum += wgt;
+      const float* src = o_part + idx * D + lane * kPer;
+      if constexpr (kPer == 4) {
+        const float4 x = *reinterpret_cast<const float4*>(src);
+        acc[0] = fmaf(wgt, x.x, acc[0]);
+        acc[1] = fmaf(wgt, x.y, acc[1]);
+        acc[2] = fmaf(wgt, x.z, acc[2]);
+        acc[3] = fmaf(wgt, x.w, acc[3]);
+      } else {
+        const float2 x = *reinterpret_cast<const float2*>(src);
+        acc[0] = fmaf(wgt, x.x, acc[0]);
+        acc[1] = fmaf(wgt, x.y, acc[1]);
+      }
+    }
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  __nv_bfloat16* dst = o + row * D + lane * kPer;
+#pragma unroll
+  for (int e = 0; e < kPer; e += 2)
+    *reinterpret_cast<__nv_bfloat162*>(dst + e) = __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
+  if (lane == 0) lse[row] = wsum > 0.f ? m + __logf(wsum) : -INFINITY;
+}
+
+template <int D>
+cudaError_t launch_fwd_splitkv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                 const CUtensorMap& top, const float* o_part, float* lse_part, void* o, float* lse,
+                                 const Shape& s, int Nk, int n_splits, int kt_per_split, cudaStream_t st) {
+  using C = FwdCfg<D>;
+  const int BH = s.B * s.H;
+  const int n_qt = (s.N + 127) / 128;
+  const int n_kt = (Nk + 127) / 128;
+  cudaError_t e;
+  if (n_splits > 0) {
+    auto kern = fa_fwd_kernel<D, false, 1, true>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    cudaFuncAttributes attr;
+    e = cudaFuncGetAttributes(&attr, kern);
+    if (e != cudaSuccess) return e;
+    if (static_cast<uint32_t>(attr.numRegs) * C::kThreads < C::kRegsNeeded) return cudaErrorInvalidConfiguration;
+    const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
+    const dim3 grid(static_cast<unsigned>(BH) * n_splits * n_qt);
+    kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, top, lse_part, s.N, n_qt, BH, 1, scale_log2, Nk,
+                                                   n_qt, n_kt, n_splits, kt_per_split);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  const long long rows = static_cast<long long>(BH) * s.N;
+  const long long blocks = (rows + 7) / 8;   // 8 warps (rows) per block
+  fa_fwd_merge_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+      o_part, lse_part, static_cast<__nv_bfloat16*>(o), lse, rows, n_splits);
   return cudaGetLastError();
 }
 
 }  // namespace
+
+cudaError_t launch_fwd_splitkv(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                               const CUtensorMap& top, const float* o_part, float* lse_part, void* o, float* lse,
+                               const Shape& s, int Nk, int n_splits, int kt_per_split, cudaStream_t st) {
+  return s.d == 128
+             ? launch_fwd_splitkv_t<128>(tq, tk, tv, top, o_part, lse_part, o, lse, s, Nk, n_splits, kt_per_split, st)
+             : launch_fwd_splitkv_t<64>(tq, tk, tv, top, o_part, lse_part, o, lse, s, Nk, n_splits, kt_per_split, st);
+}
 
 // Issue strategy (measured on GB300): at d = 128 one warp's issue loop (two
 // tiles' waits, commits and 32 MMAs per key step) cannot keep the tensor core

@@ -20,6 +20,39 @@ struct Shape {
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to, float* lse, const Shape& s, cudaStream_t st);
 
+// Split-KV forward for short query blocks against long key sequences
+// (non-causal): Q maps {d, Nq, B*H} (s.N = Nq), K/V maps {d, Nk, B*H}; each
+// chunk of key tiles writes its normalised O (fp32, map `top` {d, Nq,
+// n_splits*B*H}, box {32, 128, 1}) and its LSE (lse_part, fp32
+// [n_splits, B*H, Nq]); a merge kernel then writes o (bf16 [B, H, Nq, d]) and
+// lse (fp32 [B, H, Nq]).  n_splits and kt_per_split come from splitkv_chunks.
+cudaError_t launch_fwd_splitkv(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                               const CUtensorMap& top, const float* o_part, float* lse_part, void* o, float* lse,
+                               const Shape& s, int Nk, int n_splits, int kt_per_split, cudaStream_t st);
+
+// Split-KV chunking: `want` splits (<= 0: chosen from the SM count) of the
+// ceil(Nk/128) key tiles into chunks of kt_per_split whole tiles; n_splits is
+// the number of non-empty chunks (0 when Nk == 0).
+inline void splitkv_chunks(int B, int H, int Nq, int Nk, int want, int sm_count, int& kt_per_split,
+                           int& n_splits) {
+  const int n_kt = (Nk + 127) / 128;
+  if (n_kt <= 0) {
+    kt_per_split = 0;
+    n_splits = 0;
+    return;
+  }
+  if (want <= 0) {
+    // enough CTAs for two per SM, keeping chunks of at least two key tiles
+    const long long units = static_cast<long long>(B) * H * ((Nq + 127) / 128);
+    const long long need = (2ll * sm_count + units - 1) / units;
+    const int cap = n_kt >= 2 ? n_kt / 2 : 1;
+    want = static_cast<int>(need < 1 ? 1 : (need > cap ? cap : need));
+  }
+  const int w = want < n_kt ? want : n_kt;
+  kt_per_split = (n_kt + w - 1) / w;
+  n_splits = (n_kt + kt_per_split - 1) / kt_per_split;
+}
+
 // Backward, step 1: D_i = sum_c dO_ic O_ic (fp32).
 cudaError_t launch_bwd_preprocess(const void* o, const void* dO, float* Dvec, const Shape& s,
                                   cudaStream_t st);

@@ -18,6 +18,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libfa.so")
 
 FA_OK = 0
+FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_WORKSPACE, FA_ERR_TIMEOUT = 1, 2, 3, 4, 5
 STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_CUDA",
                 4: "FA_ERR_WORKSPACE", 5: "FA_ERR_TIMEOUT"}
 
@@ -30,6 +31,8 @@ _SZ = ctypes.c_size_t
 
 SIGNATURES = {
     "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
+    "fa_fwd_splitkv": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
+    "fa_fwd_splitkv_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "fa_bwd_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
     "fa_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
@@ -134,6 +137,38 @@ def fa_fwd(q, k, v, scale: Optional[float] = None, causal: bool = False, out=Non
     st = load().fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                        B, H, N, d, scale, int(bool(causal)), _stream_ptr(stream))
     _check("fa_fwd", st)
+    return out, lse
+
+
+def fa_fwd_splitkv_workspace_bytes(B: int, H: int, Nq: int, Nk: int, d: int, num_splits: int = 0) -> int:
+    return int(load().fa_fwd_splitkv_workspace_bytes(B, H, Nq, Nk, d, int(num_splits)))
+
+
+def fa_fwd_splitkv(q, k, v, scale: Optional[float] = None, num_splits: int = 0, out=None, lse=None,
+                   workspace=None, stream=None):
+    """Non-causal O, LSE for q [B, H, Nq, d] against k, v [B, H, Nk, d], the keys cut
+    into `num_splits` chunks (<= 0: the library's choice) merged by their LSE."""
+    qs = _bhnd(q, "q")
+    ks = _bhnd(k, "k")
+    _same(ks, v, "v")
+    B, H, Nq, d = qs
+    if ks[0] != B or ks[1] != H or ks[3] != d:
+        raise ValueError(f"k has shape {ks}, expected [{B}, {H}, Nk, {d}]")
+    Nk = ks[2]
+    scale = default_scale(d) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    _same(qs, out, "out")
+    _vec(lse, qs, "lse")
+    need = fa_fwd_splitkv_workspace_bytes(B, H, Nq, Nk, d, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    st = load().fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                               B, H, Nq, Nk, d, scale, int(num_splits), workspace.data_ptr(),
+                               workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    _check("fa_fwd_splitkv", st)
     return out, lse
 
 

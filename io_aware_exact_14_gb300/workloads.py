@@ -83,6 +83,17 @@ def make_inputs(B: int, H: int, N: int, d: int, seed: int, qk_mult: float = 1.0,
     return out
 
 
+def make_splitkv_inputs(B: int, H: int, Nq: int, Nk: int, d: int, seed: int) -> Dict[str, torch.Tensor]:
+    """Short query blocks against long key sequences: q [B, H, Nq, d], k and v
+    [B, H, Nk, d], contiguous bf16 CPU tensors drawn as fp32 N(0, 1) in that order."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    out = {}
+    for name, n in (("q", Nq), ("k", Nk), ("v", Nk)):
+        out[name] = torch.randn((B, H, n, d), generator=g, dtype=torch.float32).to(torch.bfloat16).contiguous()
+    return out
+
+
 def workload_inputs(w: Workload, with_grad: Optional[bool] = None) -> Dict[str, torch.Tensor]:
     if with_grad is None:
         with_grad = "bwd" in w.passes

@@ -285,6 +285,23 @@ def pin_preprocess(ref):
         assert np.abs(D[0, 0] - (P * dP).sum(axis=1)).max() <= 1e-12
 
 
+def pin_unequal_lengths(ref):
+    """Nq != Nk (short query blocks against long key sequences, non-causal):
+    scipy's softmax / logsumexp per head, and with Q = 0 every row is the mean
+    of all Nk values with LSE = ln Nk."""
+    q, k, v = _rand((2, 2, 5, 4), 151), _rand((2, 2, 23, 4), 152), _rand((2, 2, 23, 4), 153)
+    o, lse = ref.attn_fwd_ref(q, k, v, 0.45, False)
+    assert o.shape == (2, 2, 5, 4) and lse.shape == (2, 2, 5)
+    for b in range(2):
+        for h in range(2):
+            s = 0.45 * np.einsum("id,jd->ij", q[b, h], k[b, h])
+            assert np.abs(o[b, h] - special.softmax(s, axis=1) @ v[b, h]).max() <= 1e-13
+            assert np.abs(lse[b, h] - special.logsumexp(s, axis=1)).max() <= 1e-12
+    o, lse = ref.attn_fwd_ref(np.zeros((1, 1, 3, 4)), k[:1, :1], v[:1, :1], 0.45, False)
+    assert np.abs(o - v[:1, :1].mean(axis=2, keepdims=True)).max() <= 1e-13
+    assert np.abs(lse - math.log(23)).max() <= 1e-13
+
+
 ALL_PINS = [
     pin_worked_example,
     pin_online_scalar,
@@ -300,4 +317,5 @@ ALL_PINS = [
     pin_finite_differences,
     pin_gradient_identities,
     pin_preprocess,
+    pin_unequal_lengths,
 ]

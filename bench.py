@@ -53,6 +53,10 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU-baseline time budget")
     ap.add_argument("--batch", type=int, default=None, help="override B (smaller cases for profiler captures)")
+    ap.add_argument("--splitkv", action="store_true",
+                    help="time the split-KV forward on --splitkv-shape instead of the training step")
+    ap.add_argument("--splitkv-shape", default="8,32,1,16384,128", help="B,H,Nq,Nk,d (non-causal)")
+    ap.add_argument("--splitkv-splits", type=int, default=0, help="key chunks (0: the library's choice)")
     return ap.parse_args()
 
 
@@ -462,9 +466,89 @@ def run_reference(args, dist: Dist):
     print(json.dumps(out), flush=True)
 
 
+SPLITKV_METRIC = "split-KV forward GB/s (bf16 Q, K, V read, O and LSE written, 1xGB300) and % of measured HBM copy"
+
+
+def run_splitkv(args, dist: Dist):
+    """Split-KV forward on a decode-shaped workload: HBM-bound (each K/V byte read
+    once), so the metric is algorithmic bytes per second against the measured copy
+    bandwidth.  Algorithmic bytes per call: Q, K, V read and O, LSE written; the
+    chunks' fp32 partial results in the workspace are counted as overhead, not work."""
+    import torch
+    from io_aware_exact_14_gb300 import fa
+    from io_aware_exact_14_gb300.workloads import make_splitkv_inputs
+
+    B, H, Nq, Nk, d = (int(x) for x in args.splitkv_shape.split(","))
+    torch.cuda.set_device(dist.local)
+    dist.init("nccl")
+    dev = torch.device("cuda", dist.local)
+    x = make_splitkv_inputs(B, H, Nq, Nk, d, 14 + 100 * dist.rank)
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
+    ns = args.splitkv_splits
+    ws = torch.empty(max(fa.fa_fwd_splitkv_workspace_bytes(B, H, Nq, Nk, d, ns), 1), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    call = lambda: fa.fa_fwd_splitkv(q, k, v, None, ns, out=o, lse=lse, workspace=ws)
+    clocks = ClockSampler(dist.local)
+    clocks.start()
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    dist.barrier()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        call()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    clk = clocks.stop()
+    if fa.fa_debug_status(reset=True) != fa.FA_OK:
+        raise RuntimeError(f"kernel pipeline timeout at site {fa.fa_debug_site():#x}")
+    ms = dist.max(t0.elapsed_time(t1)) / args.steps
+    algo = 2 * B * H * (2 * Nq + 2 * Nk) * d + 4 * B * H * Nq
+    value = algo * dist.world / (ms * 1e-3) / 1e9
+    peaks, peak_src = load_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    out = {
+        "metric": SPLITKV_METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16 q, k, v)",
+        "config": {"workload": f"decode_splitkv_B{B}_H{H}_Nq{Nq}_Nk{Nk}_d{d}", "B": B, "H": H, "Nq": Nq, "Nk": Nk,
+                   "d": d, "causal": False, "num_splits": ns if ns > 0 else "library choice (0)",
+                   "l2": f"inputs larger than L2: K and V are {2 * B * H * Nk * d * 2 / 1e6:.0f} MB together",
+                   "step": "fa_fwd_splitkv (split forward kernel + merge kernel)"},
+        "roofline": {"kernel": "fa_fwd_kernel<split> + fa_fwd_merge_kernel", "bound": "hbm",
+                     "achieved": round(algo / (ms * 1e-3) / 1e9, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(algo / (ms * 1e-3) / 1e9 / hbm, 3), "peak_source": f"{peak_src} HBM copy",
+                     "work_per_launch": algo, "traffic": None},
+        "gpu_launches": 2 * args.steps, "clocks": clk,
+    }
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        import oracle
+        from io_aware_exact_14_gb300.workloads import to_f64
+        done, tb = 0, time.time()
+        while time.time() - tb < min(args.cpu_seconds, 10.0):
+            b, h = done % B, (done // B) % H
+            oracle.attn_fwd_ref(to_f64(x["q"][b:b + 1, h:h + 1]), to_f64(x["k"][b:b + 1, h:h + 1]),
+                                to_f64(x["v"][b:b + 1, h:h + 1]), 1.0 / math.sqrt(d), False)
+            done += 1
+        dt = time.time() - tb
+        out["cpu_baseline"] = {"value": round(done * algo / (B * H) / dt / 1e9, 3), "unit": "GB/s",
+                               "cores": blas_threads(), "kind": "oracle",
+                               "sample": f"{done} (batch, head) slices in fp64 NumPy, {dt:.1f} s"}
+    if dist.rank == 0:
+        print(json.dumps(out), flush=True)
+    dist.close()
+
+
 def main():
     args = parse()
     dist = Dist()
+    if args.splitkv and args.impl == "ours":
+        run_splitkv(args, dist)
+        return
     if args.impl == "reference":
         run_reference(args, dist)
     else:

@@ -42,11 +42,30 @@ inline void splitkv_chunks(int B, int H, int Nq, int Nk, int want, int sm_count,
     return;
   }
   if (want <= 0) {
-    // enough CTAs for two per SM, keeping chunks of at least two key tiles
+    // One CTA per SM at a time; the chunks stream K/V from HBM.  Cost model
+    // (hundredths of the time one tile takes when every SM streams at once,
+    // fitted to GB300 measurements of decode shapes): a full wave costs
+    // per-chunk tiles x 100 plus a fixed 120 (load latency, epilogue, launch
+    // gap); a partial wave of m CTAs streams at the shared rate 100 m / SMs
+    // per tile but no faster than one CTA's own limit, 83.
     const long long units = static_cast<long long>(B) * H * ((Nq + 127) / 128);
-    const long long need = (2ll * sm_count + units - 1) / units;
-    const int cap = n_kt >= 2 ? n_kt / 2 : 1;
-    want = static_cast<int>(need < 1 ? 1 : (need > cap ? cap : need));
+    const long long sms = sm_count > 0 ? sm_count : 1;
+    long long best = -1;
+    want = 1;
+    for (int s = 1; s <= n_kt && s <= 256; ++s) {
+      const long long per = (n_kt + s - 1) / s;
+      if (s > 1 && per == (n_kt + s - 2) / (s - 1)) continue;   // same chunks as s - 1
+      const long long ctas = units * s, full = ctas / sms, m = ctas % sms;
+      long long cost = full * (per * 100 + 120);
+      if (m > 0) {
+        const long long rate = 100 * m / sms > 83 ? 100 * m / sms : 83;
+        cost += per * rate + 120;
+      }
+      if (best < 0 || cost < best) {
+        best = cost;
+        want = s;
+      }
+    }
   }
   const int w = want < n_kt ? want : n_kt;
   kt_per_split = (n_kt + w - 1) / w;

@@ -100,6 +100,30 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, f
 size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int d, int num_splits);
 
 /*
+ * Element strides of a [B, H, N, d] bf16 view whose d elements are
+ * contiguous, so any layout that permutes B, H and N (for example
+ * [B, N, H, d], or q, k, v packed as [B, N, 3, H, d]) can be passed without a
+ * copy: element (b, h, n, c) sits at base + b*b + h*h + n*n + c (in
+ * elements).  Each stride is a positive multiple of 8 elements (the copy
+ * engine's 16-byte rule) below 2^37, and n >= d; FA_ERR_INVALID_ARG
+ * otherwise.  A NULL fa_strides pointer means the contiguous layout.  The row
+ * statistics (LSE, D) stay contiguous fp32 [B, H, N].
+ */
+typedef struct {
+  long long b, h, n;
+} fa_strides;
+
+/*
+ * fa_fwd on strided views (see fa_strides).  Outputs must not share an
+ * element with an input or with each other: views with identical strides are
+ * checked element-exactly (so interleaved outputs are accepted), others by
+ * their address spans.
+ */
+fa_status fa_fwd_strided(const void* q, const fa_strides* q_st, const void* k, const fa_strides* k_st,
+                         const void* v, const fa_strides* v_st, void* o, const fa_strides* o_st, float* lse,
+                         int B, int H, int N, int d, float scale, int causal, struct CUstream_st* stream);
+
+/*
  * Bytes of device workspace fa_bwd needs: the fp32 row term D [B, H, N],
  * rounded up to 256 bytes.  Returns 0 for N <= 0 or invalid sizes.
  */
@@ -124,6 +148,17 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  const void* dO, void* dq, void* dk, void* dv,
                  int B, int H, int N, int d, float scale, int causal,
                  void* workspace, size_t workspace_bytes, struct CUstream_st* stream);
+
+/*
+ * fa_bwd on strided views (see fa_strides and fa_fwd_strided); dq, dk, dv may
+ * be interleaved (for example one [B, N, 3, H, d] buffer).
+ */
+fa_status fa_bwd_strided(const void* q, const fa_strides* q_st, const void* k, const fa_strides* k_st,
+                         const void* v, const fa_strides* v_st, const void* o, const fa_strides* o_st,
+                         const float* lse, const void* dO, const fa_strides* dO_st, void* dq,
+                         const fa_strides* dq_st, void* dk, const fa_strides* dk_st, void* dv,
+                         const fa_strides* dv_st, int B, int H, int N, int d, float scale, int causal,
+                         void* workspace, size_t workspace_bytes, struct CUstream_st* stream);
 
 /*
  * Backward step 1: D_i = sum_c dO_ic O_ic (fp32 [B, H, N]), the row term of

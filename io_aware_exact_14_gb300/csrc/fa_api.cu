@@ -14,6 +14,7 @@
 namespace {
 
 using fa::Shape;
+using fa::Strides;
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -84,19 +85,106 @@ fa_status check_disjoint(std::initializer_list<Span> outs, std::initializer_list
   return FA_OK;
 }
 
-// 3-D view {d, N, B*H} of a [B, H, N, d] bf16 tensor; boxes of 64 x 128 rows
-// with the 128-byte swizzle the tensor-core descriptors expect.  Rows past N
-// read as zero and are clipped on store.
-fa_status make_map(CUtensorMap* m, const void* base, const Shape& s) {
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(s.d), static_cast<cuuint64_t>(s.N),
-                              static_cast<cuuint64_t>(s.B) * s.H};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(s.d) * 2, static_cast<cuuint64_t>(s.N) * s.d * 2};
-  const cuuint32_t box[3] = {64, 128, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+// 4-D view {d, N, H, B} of a [B, H, N, d] bf16 tensor with element strides
+// `st` (d contiguous); boxes of 64 x 128 rows with the 128-byte swizzle the
+// tensor-core descriptors expect.  Rows past N read as zero and are clipped
+// on store.
+fa_status make_map(CUtensorMap* m, const void* base, const Shape& s, const Strides& st) {
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(s.d), static_cast<cuuint64_t>(s.N),
+                              static_cast<cuuint64_t>(s.H), static_cast<cuuint64_t>(s.B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(st.n) * 2, static_cast<cuuint64_t>(st.h) * 2,
+                                 static_cast<cuuint64_t>(st.b) * 2};
+  const cuuint32_t box[4] = {64, 128, 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
                               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? FA_OK : fail("cuTensorMapEncodeTiled", static_cast<int>(r), "invalid tensor map");
+}
+
+fa_status make_map(CUtensorMap* m, const void* base, const Shape& s) {
+  return make_map(m, base, s, fa::contiguous_strides(s));
+}
+
+// A caller's strides (NULL: contiguous [B, H, N, d]).  Each stride must be a
+// positive multiple of 8 elements (16 bytes, the copy engine's rule) below
+// 2^37, with rows at least d apart.
+fa_status read_strides(const fa_strides* in, const Shape& s, Strides& out) {
+  if (in == nullptr) {
+    out = fa::contiguous_strides(s);
+    return FA_OK;
+  }
+  out = Strides{in->b, in->h, in->n};
+  for (long long x : {out.b, out.h, out.n})
+    if (x <= 0 || (x & 7) != 0 || x >= (1ll << 37)) return FA_ERR_INVALID_ARG;
+  if (out.n < s.d) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+// Element span [0, extent) covered by a strided [B, H, N, d] view.
+long long view_extent(const Shape& s, const Strides& st) {
+  return (s.B - 1) * st.b + (s.H - 1) * st.h + (s.N - 1) * st.n + s.d;
+}
+
+// Can some element of view a equal one of view b?  Both views have the same
+// sizes.  When they also share strides that nest (each stride at least the
+// span of the dimensions with smaller strides), a common element exists iff
+// the base offset (in elements) is sum_k delta_k stride_k + delta_c with
+// |delta_k| < size_k and |delta_c| < d, which a short search decides (packed
+// layouts such as [B, N, 3, H, d] pass); otherwise overlapping spans count as
+// overlap.
+bool views_overlap(const void* a, const Strides& sa, const void* b, const Strides& sb, const Shape& s) {
+  const long long ea = view_extent(s, sa) * 2, eb = view_extent(s, sb) * 2;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  if (!(a0 < b0 + eb && b0 < a0 + ea)) return false;
+  if (!(sa.b == sb.b && sa.h == sb.h && sa.n == sb.n)) return true;
+  long long diff = static_cast<long long>(b0 > a0 ? b0 - a0 : a0 - b0);
+  if (diff & 1) return true;
+  diff /= 2;
+  struct Dim { long long stride, size; };
+  Dim dims[3] = {{sa.b, s.B}, {sa.h, s.H}, {sa.n, s.N}};
+  for (int i = 0; i < 3; ++i)   // by decreasing stride
+    for (int j = i + 1; j < 3; ++j)
+      if (dims[j].stride > dims[i].stride) { const Dim t = dims[i]; dims[i] = dims[j]; dims[j] = t; }
+  long long inner = s.d;   // span of the dimensions below the current one
+  for (int i = 2; i >= 0; --i) {
+    if (dims[i].stride < inner) return true;   // not nested: stay conservative
+    inner += (dims[i].size - 1) * dims[i].stride;
+  }
+  // search delta_k in {floor(r / stride), floor(r / stride) + 1} level by level
+  struct Frame { int level; long long r; };
+  Frame stack[16];
+  int top = 0;
+  stack[top++] = {0, diff};
+  while (top > 0) {
+    const Frame f = stack[--top];
+    if (f.level == 3) {
+      if (f.r > -s.d && f.r < s.d) return true;
+      continue;
+    }
+    const long long st = dims[f.level].stride, sz = dims[f.level].size;
+    long long q = f.r >= 0 ? f.r / st : -((-f.r + st - 1) / st);
+    for (long long dq = q; dq <= q + 1; ++dq)
+      if (dq > -sz && dq < sz && top < 16) stack[top++] = {f.level + 1, f.r - dq * st};
+  }
+  return false;
+}
+
+struct TView {
+  const void* p;
+  Strides st;
+};
+
+// No output view may overlap an input view or another output view.
+fa_status check_views_disjoint(std::initializer_list<TView> outs, std::initializer_list<TView> ins,
+                               const Shape& s) {
+  for (auto o = outs.begin(); o != outs.end(); ++o) {
+    for (const TView& i : ins)
+      if (views_overlap(o->p, o->st, i.p, i.st, s)) return FA_ERR_INVALID_ARG;
+    for (auto o2 = o + 1; o2 != outs.end(); ++o2)
+      if (views_overlap(o->p, o->st, o2->p, o2->st, s)) return FA_ERR_INVALID_ARG;
+  }
+  return FA_OK;
 }
 
 size_t tensor_bytes(const Shape& s) { return static_cast<size_t>(s.B) * s.H * s.N * s.d * 2; }
@@ -148,29 +236,104 @@ fa_status split_plan(int B, int H, int Nq, int Nk, int d, int want, SplitPlan& p
   return FA_OK;
 }
 
+// Strides of every tensor of a backward call: q, k, v, o, dO, dq, dk, dv.
+struct BwdStrides {
+  Strides q, k, v, o, dO, dq, dk, dv;
+};
+
+BwdStrides contiguous_bwd(const Shape& s) {
+  const Strides c = fa::contiguous_strides(s);
+  return BwdStrides{c, c, c, c, c, c, c, c};
+}
+
 fa_status dkdv_checked(const void* q, const void* k, const void* v, const float* lse, const void* dO,
-                       const float* Dvec, void* dk, void* dv, const Shape& s, cudaStream_t st) {
+                       const float* Dvec, void* dk, void* dv, const Shape& s, const BwdStrides& t,
+                       cudaStream_t st) {
   if (!load_encoder()) return FA_ERR_CUDA;
   CUtensorMap tq, tk, tv, tdo, tdk, tdv;
-  FA_TRY(make_map(&tq, q, s));
-  FA_TRY(make_map(&tk, k, s));
-  FA_TRY(make_map(&tv, v, s));
-  FA_TRY(make_map(&tdo, dO, s));
-  FA_TRY(make_map(&tdk, dk, s));
-  FA_TRY(make_map(&tdv, dv, s));
+  FA_TRY(make_map(&tq, q, s, t.q));
+  FA_TRY(make_map(&tk, k, s, t.k));
+  FA_TRY(make_map(&tv, v, s, t.v));
+  FA_TRY(make_map(&tdo, dO, s, t.dO));
+  FA_TRY(make_map(&tdk, dk, s, t.dk));
+  FA_TRY(make_map(&tdv, dv, s, t.dv));
   return cuda_status(fa::launch_bwd_dkdv(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s, st), "dK/dV kernel launch");
 }
 
 fa_status dq_checked(const void* q, const void* k, const void* v, const float* lse, const void* dO,
-                     const float* Dvec, void* dq, const Shape& s, cudaStream_t st) {
+                     const float* Dvec, void* dq, const Shape& s, const BwdStrides& t, cudaStream_t st) {
   if (!load_encoder()) return FA_ERR_CUDA;
   CUtensorMap tq, tk, tv, tdo, tdq;
-  FA_TRY(make_map(&tq, q, s));
-  FA_TRY(make_map(&tk, k, s));
-  FA_TRY(make_map(&tv, v, s));
-  FA_TRY(make_map(&tdo, dO, s));
-  FA_TRY(make_map(&tdq, dq, s));
+  FA_TRY(make_map(&tq, q, s, t.q));
+  FA_TRY(make_map(&tk, k, s, t.k));
+  FA_TRY(make_map(&tv, v, s, t.v));
+  FA_TRY(make_map(&tdo, dO, s, t.dO));
+  FA_TRY(make_map(&tdq, dq, s, t.dq));
   return cuda_status(fa::launch_bwd_dq(tq, tk, tv, tdo, tdq, lse, Dvec, s, st), "dQ kernel launch");
+}
+
+Span view_span(const void* p, const Shape& s, const Strides& st) {
+  return Span{p, static_cast<size_t>(view_extent(s, st)) * 2};
+}
+
+fa_status fwd_impl(const void* q, const fa_strides* qs, const void* k, const fa_strides* ks, const void* v,
+                   const fa_strides* vs, void* o, const fa_strides* os, float* lse, int B, int H, int N, int d,
+                   float scale, int causal, cudaStream_t stream) {
+  FA_TRY(check_sizes(B, H, N, d));
+  if (N == 0) return FA_OK;
+  FA_TRY(check_ptrs({q, k, v, o}, {lse}));
+  FA_TRY(check_scale(scale));
+  const Shape s{B, H, N, d, scale, causal ? 1 : 0};
+  Strides Sq, Sk, Sv, So;
+  FA_TRY(read_strides(qs, s, Sq));
+  FA_TRY(read_strides(ks, s, Sk));
+  FA_TRY(read_strides(vs, s, Sv));
+  FA_TRY(read_strides(os, s, So));
+  FA_TRY(check_views_disjoint({{o, So}}, {{q, Sq}, {k, Sk}, {v, Sv}}, s));
+  FA_TRY(check_disjoint({{lse, vec_bytes(s)}}, {view_span(q, s, Sq), view_span(k, s, Sk), view_span(v, s, Sv),
+                                                 view_span(o, s, So)}));
+  if (!load_encoder()) return FA_ERR_CUDA;
+  CUtensorMap tq, tk, tv, to;
+  FA_TRY(make_map(&tq, q, s, Sq));
+  FA_TRY(make_map(&tk, k, s, Sk));
+  FA_TRY(make_map(&tv, v, s, Sv));
+  FA_TRY(make_map(&to, o, s, So));
+  return cuda_status(fa::launch_fwd(tq, tk, tv, to, lse, s, stream), "forward kernel launch");
+}
+
+fa_status bwd_impl(const void* q, const fa_strides* qs, const void* k, const fa_strides* ks, const void* v,
+                   const fa_strides* vs, const void* o, const fa_strides* os, const float* lse, const void* dO,
+                   const fa_strides* dos, void* dq, const fa_strides* dqs, void* dk, const fa_strides* dks,
+                   void* dv, const fa_strides* dvs, int B, int H, int N, int d, float scale, int causal,
+                   void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  FA_TRY(check_sizes(B, H, N, d));
+  if (N == 0) return FA_OK;
+  FA_TRY(check_ptrs({q, k, v, o, dO, dq, dk, dv}, {lse}));
+  FA_TRY(check_scale(scale));
+  const Shape s{B, H, N, d, scale, causal ? 1 : 0};
+  BwdStrides t;
+  FA_TRY(read_strides(qs, s, t.q));
+  FA_TRY(read_strides(ks, s, t.k));
+  FA_TRY(read_strides(vs, s, t.v));
+  FA_TRY(read_strides(os, s, t.o));
+  FA_TRY(read_strides(dos, s, t.dO));
+  FA_TRY(read_strides(dqs, s, t.dq));
+  FA_TRY(read_strides(dks, s, t.dk));
+  FA_TRY(read_strides(dvs, s, t.dv));
+  const size_t need = workspace_need(s);
+  if (workspace == nullptr || !aligned(workspace, 16) || workspace_bytes < need) return FA_ERR_WORKSPACE;
+  FA_TRY(check_views_disjoint({{dq, t.dq}, {dk, t.dk}, {dv, t.dv}},
+                              {{q, t.q}, {k, t.k}, {v, t.v}, {o, t.o}, {dO, t.dO}}, s));
+  const size_t vb = vec_bytes(s);
+  FA_TRY(check_disjoint({{workspace, need}},
+                        {view_span(q, s, t.q), view_span(k, s, t.k), view_span(v, s, t.v), view_span(o, s, t.o),
+                         view_span(dO, s, t.dO), view_span(dq, s, t.dq), view_span(dk, s, t.dk),
+                         view_span(dv, s, t.dv), {lse, vb}}));
+  FA_TRY(check_disjoint({{lse, vb}}, {view_span(dq, s, t.dq), view_span(dk, s, t.dk), view_span(dv, s, t.dv)}));
+  float* Dvec = static_cast<float*>(workspace);
+  FA_TRY(cuda_status(fa::launch_bwd_preprocess(o, t.o, dO, t.dO, Dvec, s, stream), "preprocess kernel launch"));
+  FA_TRY(dkdv_checked(q, k, v, lse, dO, Dvec, dk, dv, s, t, stream));
+  return dq_checked(q, k, v, lse, dO, Dvec, dq, s, t, stream);
 }
 
 }  // namespace
@@ -179,20 +342,13 @@ extern "C" {
 
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
                  float scale, int causal, struct CUstream_st* stream) {
-  FA_TRY(check_sizes(B, H, N, d));
-  if (N == 0) return FA_OK;
-  FA_TRY(check_ptrs({q, k, v, o}, {lse}));
-  FA_TRY(check_scale(scale));
-  const Shape s{B, H, N, d, scale, causal ? 1 : 0};
-  const size_t tb = tensor_bytes(s), vb = vec_bytes(s);
-  FA_TRY(check_disjoint({{o, tb}, {lse, vb}}, {{q, tb}, {k, tb}, {v, tb}}));
-  if (!load_encoder()) return FA_ERR_CUDA;
-  CUtensorMap tq, tk, tv, to;
-  FA_TRY(make_map(&tq, q, s));
-  FA_TRY(make_map(&tk, k, s));
-  FA_TRY(make_map(&tv, v, s));
-  FA_TRY(make_map(&to, o, s));
-  return cuda_status(fa::launch_fwd(tq, tk, tv, to, lse, s, stream), "forward kernel launch");
+  return fwd_impl(q, nullptr, k, nullptr, v, nullptr, o, nullptr, lse, B, H, N, d, scale, causal, stream);
+}
+
+fa_status fa_fwd_strided(const void* q, const fa_strides* q_st, const void* k, const fa_strides* k_st,
+                         const void* v, const fa_strides* v_st, void* o, const fa_strides* o_st, float* lse,
+                         int B, int H, int N, int d, float scale, int causal, struct CUstream_st* stream) {
+  return fwd_impl(q, q_st, k, k_st, v, v_st, o, o_st, lse, B, H, N, d, scale, causal, stream);
 }
 
 fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
@@ -251,7 +407,7 @@ fa_status fa_bwd_preprocess(const void* o, const void* dO, float* Dvec, int B, i
   const Shape s{B, H, N, d, 1.f, 0};
   const size_t tb = tensor_bytes(s);
   FA_TRY(check_disjoint({{Dvec, vec_bytes(s)}}, {{o, tb}, {dO, tb}}));
-  return cuda_status(fa::launch_bwd_preprocess(o, dO, Dvec, s, stream), "preprocess kernel launch");
+  return cuda_status(fa::launch_bwd_preprocess(o, fa::contiguous_strides(s), dO, fa::contiguous_strides(s), Dvec, s, stream), "preprocess kernel launch");
 }
 
 fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const float* lse, const void* dO,
@@ -264,7 +420,7 @@ fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const float* 
   const Shape s{B, H, N, d, scale, causal ? 1 : 0};
   const size_t tb = tensor_bytes(s), vb = vec_bytes(s);
   FA_TRY(check_disjoint({{dk, tb}, {dv, tb}}, {{q, tb}, {k, tb}, {v, tb}, {dO, tb}, {lse, vb}, {Dvec, vb}}));
-  return dkdv_checked(q, k, v, lse, dO, Dvec, dk, dv, s, stream);
+  return dkdv_checked(q, k, v, lse, dO, Dvec, dk, dv, s, contiguous_bwd(s), stream);
 }
 
 fa_status fa_bwd_dq(const void* q, const void* k, const void* v, const float* lse, const void* dO,
@@ -277,26 +433,24 @@ fa_status fa_bwd_dq(const void* q, const void* k, const void* v, const float* ls
   const Shape s{B, H, N, d, scale, causal ? 1 : 0};
   const size_t tb = tensor_bytes(s), vb = vec_bytes(s);
   FA_TRY(check_disjoint({{dq, tb}}, {{q, tb}, {k, tb}, {v, tb}, {dO, tb}, {lse, vb}, {Dvec, vb}}));
-  return dq_checked(q, k, v, lse, dO, Dvec, dq, s, stream);
+  return dq_checked(q, k, v, lse, dO, Dvec, dq, s, contiguous_bwd(s), stream);
 }
 
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
                  void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
                  void* workspace, size_t workspace_bytes, struct CUstream_st* stream) {
-  FA_TRY(check_sizes(B, H, N, d));
-  if (N == 0) return FA_OK;
-  FA_TRY(check_ptrs({q, k, v, o, dO, dq, dk, dv}, {lse}));
-  FA_TRY(check_scale(scale));
-  const Shape s{B, H, N, d, scale, causal ? 1 : 0};
-  const size_t need = workspace_need(s);
-  if (workspace == nullptr || !aligned(workspace, 16) || workspace_bytes < need) return FA_ERR_WORKSPACE;
-  const size_t tb = tensor_bytes(s), vb = vec_bytes(s);
-  FA_TRY(check_disjoint({{dq, tb}, {dk, tb}, {dv, tb}, {workspace, need}},
-                        {{q, tb}, {k, tb}, {v, tb}, {o, tb}, {dO, tb}, {lse, vb}}));
-  float* Dvec = static_cast<float*>(workspace);
-  FA_TRY(cuda_status(fa::launch_bwd_preprocess(o, dO, Dvec, s, stream), "preprocess kernel launch"));
-  FA_TRY(dkdv_checked(q, k, v, lse, dO, Dvec, dk, dv, s, stream));
-  return dq_checked(q, k, v, lse, dO, Dvec, dq, s, stream);
+  return bwd_impl(q, nullptr, k, nullptr, v, nullptr, o, nullptr, lse, dO, nullptr, dq, nullptr, dk, nullptr, dv,
+                  nullptr, B, H, N, d, scale, causal, workspace, workspace_bytes, stream);
+}
+
+fa_status fa_bwd_strided(const void* q, const fa_strides* q_st, const void* k, const fa_strides* k_st,
+                         const void* v, const fa_strides* v_st, const void* o, const fa_strides* o_st,
+                         const float* lse, const void* dO, const fa_strides* dO_st, void* dq,
+                         const fa_strides* dq_st, void* dk, const fa_strides* dk_st, void* dv,
+                         const fa_strides* dv_st, int B, int H, int N, int d, float scale, int causal,
+                         void* workspace, size_t workspace_bytes, struct CUstream_st* stream) {
+  return bwd_impl(q, q_st, k, k_st, v, v_st, o, o_st, lse, dO, dO_st, dq, dq_st, dk, dk_st, dv, dv_st, B, H, N, d,
+                  scale, causal, workspace, workspace_bytes, stream);
 }
 
 fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -317,9 +471,9 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
   FA_TRY(check_disjoint({{dq, tb}, {dk, tb}, {dv, tb}}, {{q, tb}, {k, tb}, {v, tb}, {o, tb}, {dO, tb}, {lse, vb}}));
   float* Dvec = nullptr;
   FA_TRY(cuda_status(fa::noalloc_scratch(&Dvec), "locating the built-in scratch (cudaGetSymbolAddress)"));
-  FA_TRY(cuda_status(fa::launch_bwd_preprocess(o, dO, Dvec, s, stream), "preprocess kernel launch"));
-  FA_TRY(dkdv_checked(q, k, v, lse, dO, Dvec, dk, dv, s, stream));
-  return dq_checked(q, k, v, lse, dO, Dvec, dq, s, stream);
+  FA_TRY(cuda_status(fa::launch_bwd_preprocess(o, fa::contiguous_strides(s), dO, fa::contiguous_strides(s), Dvec, s, stream), "preprocess kernel launch"));
+  FA_TRY(dkdv_checked(q, k, v, lse, dO, Dvec, dk, dv, s, contiguous_bwd(s), stream));
+  return dq_checked(q, k, v, lse, dO, Dvec, dq, s, contiguous_bwd(s), stream);
 }
 
 const char* fa_status_string(fa_status s) {

@@ -49,10 +49,21 @@ __device__ __forceinline__ uint4 ldg_stream(const void* p) {
   return v;
 }
 
+// Byte offset of row `row` (= (b H + h) N + n) of a strided [B, H, N, d] bf16
+// view; `contig` takes the contiguous layout's plain row * d.
+__device__ __forceinline__ size_t pre_row_offset(long long row, bool contig, int D, int H, int N,
+                                                 const Strides& st) {
+  if (contig) return static_cast<size_t>(row) * D * 2;
+  const long long t = row / N, n = row - t * N, b = t / H, h = t - b * H;
+  return static_cast<size_t>(b * st.b + h * st.h + n * st.n) * 2;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kPreThreads) fa_bwd_preprocess_kernel(const uint8_t* __restrict__ o,
                                                                        const uint8_t* __restrict__ dO,
-                                                                       float* __restrict__ Dvec, long long rows) {
+                                                                       float* __restrict__ Dvec, long long rows,
+                                                                       int H, int N, Strides so, Strides sdo,
+                                                                       bool contig) {
   constexpr int kTpr = D / 8;                 // threads per row, one 16-byte chunk each
   constexpr int kRows = kPreThreads / kTpr;   // rows per block per step
   const int sub = threadIdx.x % kTpr;
@@ -64,9 +75,8 @@ __global__ void __launch_bounds__(kPreThreads) fa_bwd_preprocess_kernel(const ui
     for (int u = 0; u < kPreUnroll; ++u) {
       const long long row = base + static_cast<long long>(u) * kRows;
       if (row < rows) {
-        const size_t off = (static_cast<size_t>(row) * D + sub * 8) * 2;
-        a[u] = ldg_stream(o + off);
-        b[u] = ldg_stream(dO + off);
+        a[u] = ldg_stream(o + pre_row_offset(row, contig, D, H, N, so) + sub * 16);
+        b[u] = ldg_stream(dO + pre_row_offset(row, contig, D, H, N, sdo) + sub * 16);
       }
     }
 #pragma unroll
@@ -284,7 +294,7 @@ __global__ void __launch_bounds__(384, 1)
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                        const __grid_constant__ CUtensorMap tmDK, const __grid_constant__ CUtensorMap tmDV,
                        const float* __restrict__ lse, const float* __restrict__ Dg, int N, int n_tiles,
-                       int BH, int band, float scale, float scale_log2) {
+                       int BH, int H, int band, float scale, float scale_log2) {
   using C = DkdvCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -370,13 +380,12 @@ __global__ void __launch_bounds__(384, 1)
       bool dk_reading = false;
       auto store_front = [&]() -> bool {   // lane 0
         if (!mbar_wait(&staged[pend_su & 1], (pend_su >> 1) & 1, g, kSiteDkdv | 16u)) return false;
+        const HeadCoord phc = head_coord(p0_bh, H);
         for (int b = 0; b < C::kBoxes; ++b)
-          tma_store_3d(&tmDV, smem + C::do_off(p0_last % C::kDOStages) + b * C::kBoxBytes, 64 * b, 128 * p0_kt,
-                       p0_bh);
+          tma_store_hd(&tmDV, smem + C::do_off(p0_last % C::kDOStages) + b * C::kBoxBytes, 64 * b, 128 * p0_kt, phc);
         tma_store_commit();
         for (int b = 0; b < C::kBoxes; ++b)
-          tma_store_3d(&tmDK, smem + C::q_off(p0_last % C::kQStages) + b * C::kBoxBytes, 64 * b, 128 * p0_kt,
-                       p0_bh);
+          tma_store_hd(&tmDK, smem + C::q_off(p0_last % C::kQStages) + b * C::kBoxBytes, 64 * b, 128 * p0_kt, phc);
         tma_store_commit();
         tma_store_wait_read_but_one();   // dV has been read out of the dO slot
         dk_reading = true;
@@ -400,6 +409,7 @@ __global__ void __launch_bounds__(384, 1)
           break;
         }
         const DkdvUnit w = dkdv_unit<CAUSAL>(u, n_tiles, BH, band);
+        const HeadCoord hc = head_coord(w.bh, H);
         const size_t row_base = static_cast<size_t>(w.bh) * N;
         RowVecs rv = fetch_row_vectors(lse, Dg, row_base, 128 * w.i0, N, lane);
         for (int it = 0; it < w.cnt; ++it, ++gi) {
@@ -420,7 +430,7 @@ __global__ void __launch_bounds__(384, 1)
           if (lane == 0) {
             mbar_arrive_expect_tx(&q_full[qs], C::kTileBytes);
             for (int b = 0; b < C::kBoxes; ++b)
-              tma_load_3d(smem + C::q_off(qs) + b * C::kBoxBytes, &tmQ, &q_full[qs], 64 * b, 128 * qt, w.bh);
+              tma_load_hd(smem + C::q_off(qs) + b * C::kBoxBytes, &tmQ, &q_full[qs], 64 * b, 128 * qt, hc);
           }
           if (it == 0) {
             // the unit's K_j replaces the previous unit's once its last S^T is
@@ -433,13 +443,13 @@ __global__ void __launch_bounds__(384, 1)
                 unit_id[su & 1] = u;
                 mbar_arrive_expect_tx(&k_full[su & 1], C::kTileBytes);
                 for (int b = 0; b < C::kBoxes; ++b)
-                  tma_load_3d(smem + C::kKOff + b * C::kBoxBytes, &tmK, &k_full[su & 1], 64 * b, 128 * w.kt, w.bh);
+                  tma_load_hd(smem + C::kKOff + b * C::kBoxBytes, &tmK, &k_full[su & 1], 64 * b, 128 * w.kt, hc);
                 if (su > 0) okl = mbar_wait(v_free, (su - 1) & 1, g, kSiteDkdv | 20u);
               }
               if (okl) {
                 mbar_arrive_expect_tx(&v_full[su & 1], C::kTileBytes);
                 for (int b = 0; b < C::kBoxes; ++b)
-                  tma_load_3d(smem + C::kVOff + b * C::kBoxBytes, &tmV, &v_full[su & 1], 64 * b, 128 * w.kt, w.bh);
+                  tma_load_hd(smem + C::kVOff + b * C::kBoxBytes, &tmV, &v_full[su & 1], 64 * b, 128 * w.kt, hc);
               }
             }
             if (!__shfl_sync(0xffffffffu, okl, 0)) { ok = false; break; }
@@ -463,7 +473,7 @@ __global__ void __launch_bounds__(384, 1)
           if (lane == 0) {
             mbar_arrive_expect_tx(&do_full[ds], C::kTileBytes);
             for (int b = 0; b < C::kBoxes; ++b)
-              tma_load_3d(smem + C::do_off(ds) + b * C::kBoxBytes, &tmDO, &do_full[ds], 64 * b, 128 * qt, w.bh);
+              tma_load_hd(smem + C::do_off(ds) + b * C::kBoxBytes, &tmDO, &do_full[ds], 64 * b, 128 * qt, hc);
           }
           float* nd = reinterpret_cast<float*>(smem + C::dvec_off(ds));
 #pragma unroll
@@ -796,7 +806,7 @@ __global__ void __launch_bounds__(384, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                      const __grid_constant__ CUtensorMap tmDQ, const float* __restrict__ lse,
-                     const float* __restrict__ Dg, int N, int n_tiles, int BH, int band, float scale,
+                     const float* __restrict__ Dg, int N, int n_tiles, int BH, int H, int band, float scale,
                      float scale_log2) {
   using C = DqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -882,9 +892,10 @@ __global__ void __launch_bounds__(384, 1)
         auto store_front = [&]() -> bool {
           const int p = pend_head & 3;
           if (!mbar_wait(&staged[p], (pend_head >> 2) & 1, g, kSiteDq | 18u)) return false;
+          const HeadCoord phc = head_coord(pend_bh[p], H);
           for (int b = 0; b < BwdCfg<D>::kBoxes; ++b)
-            tma_store_3d(&tmDQ, smem + C::k_off(pend_last[p] % C::kKStages) + b * BwdCfg<D>::kBoxBytes, 64 * b,
-                         128 * pend_qt[p], pend_bh[p]);
+            tma_store_hd(&tmDQ, smem + C::k_off(pend_last[p] % C::kKStages) + b * BwdCfg<D>::kBoxBytes, 64 * b,
+                         128 * pend_qt[p], phc);
           tma_store_commit();
           tma_store_wait_read_all();
           ++pend_head;
@@ -896,11 +907,12 @@ __global__ void __launch_bounds__(384, 1)
         bool ok = true;
         for (int su = 0; ok; ++su) {
           const DqUnit w = dq_unit<CAUSAL>(u, n_tiles, BH, band);
+          const HeadCoord hc = head_coord(w.bh, H);
           // Q_i: the previous unit's last S product has read the buffer
           if (su > 0 && !(ok = mbar_wait(q_empty, (su - 1) & 1, g, kSiteDq | 14u))) break;
           mbar_arrive_expect_tx(q_full, C::kTileBytes);
           for (int b = 0; b < BwdCfg<D>::kBoxes; ++b)
-            tma_load_3d(smem + C::kQOff + b * BwdCfg<D>::kBoxBytes, &tmQ, q_full, 64 * b, 128 * w.qt, w.bh);
+            tma_load_hd(smem + C::kQOff + b * BwdCfg<D>::kBoxBytes, &tmQ, q_full, 64 * b, 128 * w.qt, hc);
           for (int it = 0; it < w.cnt; ++it, ++gk) {
             const int ks = gk % C::kKStages, vs = gk % C::kVStages;
             if (it == max(0, w.cnt - C::kRequestAhead)) {   // ask for the next unit
@@ -912,8 +924,8 @@ __global__ void __launch_bounds__(384, 1)
             if (pend_head < pend_tail && pend_last[pend_head & 3] + C::kKStages == gk && !(ok = store_front())) break;
             mbar_arrive_expect_tx(&k_full[ks], C::kTileBytes);
             for (int b = 0; b < BwdCfg<D>::kBoxes; ++b)
-              tma_load_3d(smem + C::k_off(ks) + b * BwdCfg<D>::kBoxBytes, &tmK, &k_full[ks], 64 * b, 128 * it,
-                          w.bh);
+              tma_load_hd(smem + C::k_off(ks) + b * BwdCfg<D>::kBoxBytes, &tmK, &k_full[ks], 64 * b, 128 * it,
+                          hc);
             // V slot reuse: the dQ of key tile gk - 2 (issued after that tile's
             // dP) has completed, which its k_empty commit signals
             if (gk >= C::kVStages &&
@@ -922,8 +934,8 @@ __global__ void __launch_bounds__(384, 1)
               break;
             mbar_arrive_expect_tx(&v_full[vs], C::kTileBytes);
             for (int b = 0; b < BwdCfg<D>::kBoxes; ++b)
-              tma_load_3d(smem + C::v_off(vs) + b * BwdCfg<D>::kBoxBytes, &tmV, &v_full[vs], 64 * b, 128 * it,
-                          w.bh);
+              tma_load_hd(smem + C::v_off(vs) + b * BwdCfg<D>::kBoxBytes, &tmV, &v_full[vs], 64 * b, 128 * it,
+                          hc);
           }
           if (!ok) break;
           const int p = pend_tail & 3;   // at most three older stores are still pending here
@@ -935,12 +947,13 @@ __global__ void __launch_bounds__(384, 1)
           u = clc_decode(resp);
           if (u >= 0) {   // the next unit's first tiles into L2 while this unit finishes
             const DqUnit w1 = dq_unit<CAUSAL>(u, n_tiles, BH, band);
+            const HeadCoord hc1 = head_coord(w1.bh, H);
             for (int b = 0; b < BwdCfg<D>::kBoxes; ++b) {
-              tma_prefetch_l2_3d(&tmQ, 64 * b, 128 * w1.qt, w1.bh);
-              tma_prefetch_l2_3d(&tmDO, 64 * b, 128 * w1.qt, w1.bh);
+              tma_prefetch_l2_hd(&tmQ, 64 * b, 128 * w1.qt, hc1);
+              tma_prefetch_l2_hd(&tmDO, 64 * b, 128 * w1.qt, hc1);
               for (int t = 0; t < kL2Ahead && t < w1.cnt; ++t) {
-                tma_prefetch_l2_3d(&tmK, 64 * b, 128 * t, w1.bh);
-                tma_prefetch_l2_3d(&tmV, 64 * b, 128 * t, w1.bh);
+                tma_prefetch_l2_hd(&tmK, 64 * b, 128 * t, hc1);
+                tma_prefetch_l2_hd(&tmV, 64 * b, 128 * t, hc1);
               }
             }
           }
@@ -967,7 +980,8 @@ __global__ void __launch_bounds__(384, 1)
           const DqUnit w = dq_unit<CAUSAL>(u, n_tiles, BH, band);
           mbar_arrive_expect_tx(do_full, C::kTileBytes);
           for (int b = 0; b < BwdCfg<D>::kBoxes; ++b)
-            tma_load_3d(smem + C::kDOOff + b * BwdCfg<D>::kBoxBytes, &tmDO, do_full, 64 * b, 128 * w.qt, w.bh);
+            tma_load_hd(smem + C::kDOOff + b * BwdCfg<D>::kBoxBytes, &tmDO, do_full, 64 * b, 128 * w.qt,
+                        head_coord(w.bh, H));
         }
       }
     } else if (warp == 9) {  // MMA issuer: the whole warp runs the loop, one lane issues
@@ -1170,7 +1184,7 @@ cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CU
   const int n_tiles = (s.N + 127) / 128;
   const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
   const dim3 grid(static_cast<unsigned>(s.B) * s.H * n_tiles);
-  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s.N, n_tiles, s.B * s.H,
+  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s.N, n_tiles, s.B * s.H, s.H,
                                                  head_band(s.N, s.d), s.scale, scale_log2);
   return cudaGetLastError();
 }
@@ -1186,7 +1200,7 @@ cudaError_t launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   const int n_tiles = (s.N + 127) / 128;
   const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
   const dim3 grid(static_cast<unsigned>(s.B) * s.H * n_tiles);
-  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, tdq, lse, Dvec, s.N, n_tiles, s.B * s.H,
+  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, tdq, lse, Dvec, s.N, n_tiles, s.B * s.H, s.H,
                                                  head_band(s.N, s.d), s.scale, scale_log2);
   return cudaGetLastError();
 }
@@ -1213,7 +1227,8 @@ cudaError_t launch_bwd_dq(const CUtensorMap& tq, const CUtensorMap& tk, const CU
                   : launch_dq_t<64, false>(tq, tk, tv, tdo, tdq, lse, Dvec, s, st);
 }
 
-cudaError_t launch_bwd_preprocess(const void* o, const void* dO, float* Dvec, const Shape& s, cudaStream_t st) {
+cudaError_t launch_bwd_preprocess(const void* o, const Strides& so, const void* dO, const Strides& sdo, float* Dvec,
+                                  const Shape& s, cudaStream_t st) {
   const long long rows = static_cast<long long>(s.B) * s.H * s.N;
   int dev = 0, sms = 148;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1223,12 +1238,14 @@ cudaError_t launch_bwd_preprocess(const void* o, const void* dO, float* Dvec, co
   const int rows_per_block = (kPreThreads / (s.d / 8)) * kPreUnroll;
   const long long want = (rows + rows_per_block - 1) / rows_per_block;
   const int grid = static_cast<int>(want < 8LL * sms ? want : 8LL * sms);
+  const Strides c = contiguous_strides(s);
+  const bool contig = so.b == c.b && so.h == c.h && so.n == c.n && sdo.b == c.b && sdo.h == c.h && sdo.n == c.n;
   if (s.d == 128)
-    fa_bwd_preprocess_kernel<128><<<grid, kPreThreads, 0, st>>>(static_cast<const uint8_t*>(o),
-                                                                 static_cast<const uint8_t*>(dO), Dvec, rows);
+    fa_bwd_preprocess_kernel<128><<<grid, kPreThreads, 0, st>>>(
+        static_cast<const uint8_t*>(o), static_cast<const uint8_t*>(dO), Dvec, rows, s.H, s.N, so, sdo, contig);
   else
-    fa_bwd_preprocess_kernel<64><<<grid, kPreThreads, 0, st>>>(static_cast<const uint8_t*>(o),
-                                                                static_cast<const uint8_t*>(dO), Dvec, rows);
+    fa_bwd_preprocess_kernel<64><<<grid, kPreThreads, 0, st>>>(
+        static_cast<const uint8_t*>(o), static_cast<const uint8_t*>(dO), Dvec, rows, s.H, s.N, so, sdo, contig);
   return cudaGetLastError();
 }
 

@@ -84,14 +84,16 @@ struct FwdCfg {
 // split whose partial result it writes (split-KV launches only).
 struct FwdWork {
   int bh, qt0, n0, n1, n, kt0, split;
+  HeadCoord hc;   // bh as (h, b) for the 4-D tensor maps
 };
 
-__device__ __forceinline__ FwdWork fwd_work(int N, int n_pairs, int BH, int band, bool causal) {
+__device__ __forceinline__ FwdWork fwd_work(int N, int n_pairs, int BH, int H, int band, bool causal) {
   FwdWork w;
   w.kt0 = 0;
   w.split = 0;
   int rank;
   banded_order(blockIdx.x, n_pairs, BH, band, w.bh, rank);
+  w.hc = head_coord(w.bh, H);
   const int pair = n_pairs - 1 - rank;  // heavy (causal) pairs first
   const int n_qt = (N + 127) / 128;
   w.qt0 = 2 * pair;
@@ -105,12 +107,14 @@ __device__ __forceinline__ FwdWork fwd_work(int N, int n_pairs, int BH, int band
 // Split-KV: CTA u takes one query tile of one head and one chunk of
 // kt_per_split key tiles (the last chunk may be shorter, never empty).  CTAs
 // of one (head, chunk) are adjacent, so they share the chunk's K/V in L2.
-__device__ __forceinline__ FwdWork fwd_split_work(int u, int n_qt, int n_splits, int kt_per_split, int n_kt) {
+__device__ __forceinline__ FwdWork fwd_split_work(int u, int n_qt, int n_splits, int kt_per_split, int n_kt,
+                                                 int H) {
   FwdWork w;
   w.qt0 = u % n_qt;
   const int rest = u / n_qt;
   w.split = rest % n_splits;
   w.bh = rest / n_splits;
+  w.hc = head_coord(w.bh, H);
   w.kt0 = w.split * kt_per_split;
   w.n0 = min(kt_per_split, n_kt - w.kt0);
   w.n1 = 0;
@@ -126,12 +130,12 @@ __device__ __forceinline__ void fwd_producer(const FwdWork& w, uint8_t* smem, ui
   mbar_arrive_expect_tx(q_full, (w.n1 > 0 ? 2u : 1u) * C::kTileBytes);
 #pragma unroll
   for (int b = 0; b < C::kBoxes; ++b)
-    tma_load_3d(smem + C::kQOff + b * C::kBoxBytes, tmQ, q_full, 64 * b, 128 * w.qt0, w.bh);
+    tma_load_hd(smem + C::kQOff + b * C::kBoxBytes, tmQ, q_full, 64 * b, 128 * w.qt0, w.hc);
   if (w.n1 > 0) {
 #pragma unroll
     for (int b = 0; b < C::kBoxes; ++b)
-      tma_load_3d(smem + C::kQOff + C::kTileBytes + b * C::kBoxBytes, tmQ, q_full, 64 * b, 128 * (w.qt0 + 1),
-                  w.bh);
+      tma_load_hd(smem + C::kQOff + C::kTileBytes + b * C::kBoxBytes, tmQ, q_full, 64 * b, 128 * (w.qt0 + 1),
+                  w.hc);
   }
   int issued = 0;   // tiles whose load was issued
   bool ok = true;
@@ -153,13 +157,13 @@ __device__ __forceinline__ void fwd_producer(const FwdWork& w, uint8_t* smem, ui
       if (j + kL2Ahead < w.n) {   // the same tile kL2Ahead steps on, into L2 while this one lands
 #pragma unroll
         for (int b = 0; b < C::kBoxes; ++b)
-          tma_prefetch_l2_3d(kind ? tmV : tmK, 64 * b, 128 * (w.kt0 + j + kL2Ahead), w.bh);
+          tma_prefetch_l2_hd(kind ? tmV : tmK, 64 * b, 128 * (w.kt0 + j + kL2Ahead), w.hc);
       }
       uint8_t* dst = smem + C::kSlotOff + (idx % C::kSlots) * C::kTileBytes;
 #pragma unroll
       for (int b = 0; b < C::kBoxes; ++b)
-        tma_load_3d(dst + b * C::kBoxBytes, kind ? tmV : tmK, &full[grp % C::kGroups], 64 * b, 128 * (w.kt0 + j),
-                    w.bh);
+        tma_load_hd(dst + b * C::kBoxBytes, kind ? tmV : tmK, &full[grp % C::kGroups], 64 * b, 128 * (w.kt0 + j),
+                    w.hc);
       issued = idx + 1;
     }
   }
@@ -462,7 +466,7 @@ __device__ __forceinline__ void fwd_softmax(const FwdWork& w, int tile, uint32_t
     if (r == 0 && mbar_wait(&staged[tile], 0, g, kSiteFwd | 8u)) {
 #pragma unroll
       for (int b = 0; b < C::kBoxes; ++b)
-        tma_store_3d(tmO, smem + C::kQOff + tile * C::kTileBytes + b * C::kBoxBytes, 64 * b, qt * 128, w.bh);
+        tma_store_hd(tmO, smem + C::kQOff + tile * C::kTileBytes + b * C::kBoxBytes, 64 * b, qt * 128, w.hc);
       tma_store_commit();
       tma_store_wait_read_all();
     }
@@ -480,7 +484,7 @@ template <int D, bool CAUSAL, int ISSUERS, bool SPLIT>
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                  float* __restrict__ lse, int N, int n_pairs, int BH, int band, float scale_log2, int Nk,
+                  float* __restrict__ lse, int N, int n_pairs, int BH, int H, int band, float scale_log2, int Nk,
                   int n_qt, int n_kt, int n_splits, int kt_per_split) {
   static_assert(!SPLIT || (!CAUSAL && ISSUERS == 1), "split-KV launches are non-causal with one issuer");
   using C = FwdCfg<D>;
@@ -500,8 +504,8 @@ __global__ void __launch_bounds__(384, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const FwdWork w = SPLIT ? fwd_split_work(static_cast<int>(blockIdx.x), n_qt, n_splits, kt_per_split, n_kt)
-                          : fwd_work(N, n_pairs, BH, band, CAUSAL);
+  const FwdWork w = SPLIT ? fwd_split_work(static_cast<int>(blockIdx.x), n_qt, n_splits, kt_per_split, n_kt, H)
+                          : fwd_work(N, n_pairs, BH, H, band, CAUSAL);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kGroups; ++i) {
@@ -583,8 +587,8 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   const int n_pairs = (n_qt + 1) / 2;
   const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
   const dim3 grid(static_cast<unsigned>(s.B) * s.H * n_pairs);
-  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, to, lse, s.N, n_pairs, s.B * s.H, head_band(s.N, s.d),
-                                                 scale_log2, s.N, n_qt, n_qt, 1, n_qt);
+  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, to, lse, s.N, n_pairs, s.B * s.H, s.H,
+                                                 head_band(s.N, s.d), scale_log2, s.N, n_qt, n_qt, 1, n_qt);
   return cudaGetLastError();
 }
 
@@ -658,8 +662,8 @@ cudaError_t launch_fwd_splitkv_t(const CUtensorMap& tq, const CUtensorMap& tk, c
     if (static_cast<uint32_t>(attr.numRegs) * C::kThreads < C::kRegsNeeded) return cudaErrorInvalidConfiguration;
     const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
     const dim3 grid(static_cast<unsigned>(BH) * n_splits * n_qt);
-    kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, top, lse_part, s.N, n_qt, BH, 1, scale_log2, Nk,
-                                                   n_qt, n_kt, n_splits, kt_per_split);
+    kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, top, lse_part, s.N, n_qt, BH, s.H, 1, scale_log2,
+                                                   Nk, n_qt, n_kt, n_splits, kt_per_split);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   const long long rows = static_cast<long long>(BH) * s.N;

@@ -16,12 +16,21 @@ struct Shape {
   int causal;    // 0 or 1
 };
 
-// Forward: O and LSE from Q, K, V (TMA maps are 3-D {d, N, B*H}, box {64, 128, 1}).
+// Element strides of a [B, H, N, d] bf16 view (d contiguous).
+struct Strides {
+  long long b, h, n;
+};
+inline Strides contiguous_strides(const Shape& s) {
+  return Strides{static_cast<long long>(s.H) * s.N * s.d, static_cast<long long>(s.N) * s.d, s.d};
+}
+
+// Forward: O and LSE from Q, K, V (TMA maps are 4-D {d, N, H, B}, box
+// {64, 128, 1, 1}, with each tensor's own strides).
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to, float* lse, const Shape& s, cudaStream_t st);
 
 // Split-KV forward for short query blocks against long key sequences
-// (non-causal): Q maps {d, Nq, B*H} (s.N = Nq), K/V maps {d, Nk, B*H}; each
+// (non-causal): Q maps {d, Nq, H, B} (s.N = Nq), K/V maps {d, Nk, H, B}; each
 // chunk of key tiles writes its normalised O (fp32, map `top` {d, Nq,
 // n_splits*B*H}, box {32, 128, 1}) and its LSE (lse_part, fp32
 // [n_splits, B*H, Nq]); a merge kernel then writes o (bf16 [B, H, Nq, d]) and
@@ -73,8 +82,8 @@ inline void splitkv_chunks(int B, int H, int Nq, int Nk, int want, int sm_count,
 }
 
 // Backward, step 1: D_i = sum_c dO_ic O_ic (fp32).
-cudaError_t launch_bwd_preprocess(const void* o, const void* dO, float* Dvec, const Shape& s,
-                                  cudaStream_t st);
+cudaError_t launch_bwd_preprocess(const void* o, const Strides& so, const void* dO, const Strides& sdo, float* Dvec,
+                                  const Shape& s, cudaStream_t st);
 
 // Backward, step 2: dK, dV for each 128-key tile, looping over query tiles.
 cudaError_t launch_bwd_dkdv(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -188,6 +188,32 @@ __device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int x
                : "memory");
 }
 
+// Tensors are viewed by TMA as 4-D {d, N, H, B} (any element strides, d
+// contiguous): a tile of head bh is addressed by (x, row, h, b) with
+// h = bh % H, b = bh / H, computed once per work unit.
+struct HeadCoord {
+  int h, b;
+};
+__device__ __forceinline__ HeadCoord head_coord(int bh, int H) { return HeadCoord{bh % H, bh / H}; }
+
+// 4-D tile load of head `hc` into shared memory, completing bytes on `bar`.
+__device__ __forceinline__ void tma_load_hd(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
+                                            HeadCoord hc) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(hc.h), "r"(hc.b)
+      : "memory");
+}
+
+// Bring a 4-D tile of head `hc` into L2 ahead of its load.
+__device__ __forceinline__ void tma_prefetch_l2_hd(const CUtensorMap* map, int x, int y, HeadCoord hc) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(hc.h), "r"(hc.b)
+               : "memory");
+}
+
 // Work stealing (cluster launch control): ask the scheduler for a CTA of this
 // grid that has not started yet; if it grants one, that CTA never launches and
 // its work falls to the caller.  The 16-byte response lands at `resp` (16-byte
@@ -222,6 +248,15 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void*
   asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
                    reinterpret_cast<uint64_t>(map)),
                "r"(smem_u32(smem_src)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
+// 4-D tile store of head `hc` from shared memory (rows outside the tensor are clipped).
+__device__ __forceinline__ void tma_store_hd(const CUtensorMap* map, const void* smem_src, int x, int y,
+                                             HeadCoord hc) {
+  asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(smem_src)), "r"(x), "r"(y), "r"(hc.h), "r"(hc.b)
                : "memory");
 }
 

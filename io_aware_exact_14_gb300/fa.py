@@ -31,6 +31,9 @@ _SZ = ctypes.c_size_t
 
 SIGNATURES = {
     "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
+    "fa_fwd_strided": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
+    "fa_bwd_strided": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                            _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
     "fa_fwd_splitkv": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
     "fa_fwd_splitkv_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "fa_bwd_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
@@ -44,6 +47,11 @@ SIGNATURES = {
     "fa_debug_site": (ctypes.c_uint, []),
     "fa_last_error_detail": (ctypes.c_char_p, []),
 }
+
+
+class FaStrides(ctypes.Structure):
+    """fa_strides: element strides (b, h, n) of a [B, H, N, d] view, d contiguous."""
+    _fields_ = [("b", ctypes.c_longlong), ("h", ctypes.c_longlong), ("n", ctypes.c_longlong)]
 
 
 class FAError(RuntimeError):
@@ -138,6 +146,76 @@ def fa_fwd(q, k, v, scale: Optional[float] = None, causal: bool = False, out=Non
                        B, H, N, d, scale, int(bool(causal)), _stream_ptr(stream))
     _check("fa_fwd", st)
     return out, lse
+
+
+def _view(t: torch.Tensor, name: str):
+    """Shape and fa_strides of a [B, H, N, d] bf16 CUDA view whose last dim is contiguous."""
+    if not isinstance(t, torch.Tensor) or t.dim() != 4:
+        raise ValueError(f"{name} must be a 4-D [B, H, N, d] view")
+    if not t.is_cuda or t.dtype != torch.bfloat16:
+        raise ValueError(f"{name} must be a bfloat16 CUDA tensor")
+    if t.stride(3) != 1:
+        raise ValueError(f"{name} must have a contiguous last (d) dimension")
+    sb, sh, sn = t.stride()[:3]
+    return tuple(t.shape), FaStrides(sb, sh, sn)
+
+
+def fa_fwd_strided(q, k, v, scale: Optional[float] = None, causal: bool = False, out=None, lse=None, stream=None):
+    """fa_fwd on [B, H, N, d] views of any layout that keeps d contiguous (for example
+    x.transpose(1, 2) of a [B, N, H, d] tensor); `out` may be such a view too."""
+    shape, qs = _view(q, "q")
+    ks, vs = _view(k, "k"), _view(v, "v")
+    for (sh, _), n in ((ks, "k"), (vs, "v")):
+        if sh != shape:
+            raise ValueError(f"{n} has shape {sh}, expected {shape}")
+    B, H, N, d = shape
+    scale = default_scale(d) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty(shape, dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    oshape, os_ = _view(out, "out")
+    if oshape != shape:
+        raise ValueError(f"out has shape {oshape}, expected {shape}")
+    _vec(lse, shape, "lse")
+    st = load().fa_fwd_strided(q.data_ptr(), ctypes.addressof(qs), k.data_ptr(), ctypes.addressof(ks[1]),
+                               v.data_ptr(), ctypes.addressof(vs[1]), out.data_ptr(), ctypes.addressof(os_),
+                               lse.data_ptr(), B, H, N, d, scale, int(bool(causal)), _stream_ptr(stream))
+    _check("fa_fwd_strided", st)
+    return out, lse
+
+
+def fa_bwd_strided(q, k, v, o, lse, do, scale: Optional[float] = None, causal: bool = False,
+                   dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """fa_bwd on [B, H, N, d] views (d contiguous); dq, dk, dv may be views into one
+    buffer (for example a packed [B, N, 3, H, d] gradient)."""
+    shape, qs = _view(q, "q")
+    views = {"k": _view(k, "k"), "v": _view(v, "v"), "o": _view(o, "o"), "do": _view(do, "do")}
+    for n, (sh, _) in views.items():
+        if sh != shape:
+            raise ValueError(f"{n} has shape {sh}, expected {shape}")
+    _vec(lse, shape, "lse")
+    B, H, N, d = shape
+    scale = default_scale(d) if scale is None else float(scale)
+    grads = []
+    for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
+        t = torch.empty(shape, dtype=torch.bfloat16, device=q.device) if t is None else t
+        sh, st_ = _view(t, n)
+        if sh != shape:
+            raise ValueError(f"{n} has shape {sh}, expected {shape}")
+        grads.append((t, st_))
+    need = fa_bwd_workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    a = ctypes.addressof
+    st = load().fa_bwd_strided(q.data_ptr(), a(qs), k.data_ptr(), a(views["k"][1]), v.data_ptr(), a(views["v"][1]),
+                               o.data_ptr(), a(views["o"][1]), lse.data_ptr(), do.data_ptr(), a(views["do"][1]),
+                               grads[0][0].data_ptr(), a(grads[0][1]), grads[1][0].data_ptr(), a(grads[1][1]),
+                               grads[2][0].data_ptr(), a(grads[2][1]), B, H, N, d, scale, int(bool(causal)),
+                               workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                               _stream_ptr(stream))
+    _check("fa_bwd_strided", st)
+    return grads[0][0], grads[1][0], grads[2][0]
 
 
 def fa_fwd_splitkv_workspace_bytes(B: int, H: int, Nq: int, Nk: int, d: int, num_splits: int = 0) -> int:

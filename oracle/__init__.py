@@ -7,6 +7,12 @@ from .attention_ref import (  # noqa: F401
     attn_fwd_ref,
     attn_fwd_ref_rows,
     attn_bwd_ref,
+    attn_fwd_dropout_ref,
+    attn_bwd_dropout_ref,
+    philox4x32_10,
+    dropout_keep,
+    dropout_threshold,
+    dropout_scale,
     bwd_preprocess_ref,
     online_softmax_scalar,
     online_softmax_blocks,

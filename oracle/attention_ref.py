@@ -205,6 +205,129 @@ def bwd_preprocess_ref(o, do) -> np.ndarray:
 
 
 # ---------------------------------------------------------------------------
+# Dropout on the probabilities (the pages name it only as a fused step of the
+# GPU kernels, [WHY-FAST] §"标准注意力机制的内存困局"; the RNG contract below is
+# this project's reading, written out in full)
+# ---------------------------------------------------------------------------
+#
+# Random numbers: Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel
+# random numbers: as easy as 1, 2, 3", SC 2011), a counter-based generator:
+# ten rounds of two 32 x 32 -> 64-bit products with the multipliers
+# 0xD2511F53 and 0xCD9E8D57, the key bumped by the Weyl constants 0x9E3779B9
+# and 0xBB67AE85 between rounds.  Key = (seed mod 2^32, seed div 2^32).
+#
+# One call covers a 4 x 4 block of (query i, key j) for head bh:
+#   counter = (j div 4, i div 4, bh, offset);  output word (i mod 4), byte
+#   (j mod 4) (byte 0 = least significant) is the element's uniform byte u.
+# Dropout probability p is quantised to t = round(256 p) clamped to [0, 255];
+# the element is kept when u >= t, and kept probabilities are scaled by
+# 256 / (256 - t), so E[mask * scale] = 1.
+#   O = (P o Mt) V with Mt = keep * 256 / (256 - t), P the plain softmax;
+#   LSE is the plain one (dropout acts after normalisation).
+
+_PHILOX_M = (0xD2511F53, 0xCD9E8D57)
+_PHILOX_W = (0x9E3779B9, 0xBB67AE85)
+_U32 = np.uint64(0xFFFFFFFF)
+
+
+def philox4x32_10(c0, c1, c2, c3, k0, k1):
+    """Philox4x32-10 on uint32 counter words (arrays broadcast) and key words;
+    returns the four uint32 output words (computed in uint64)."""
+    c = [np.asarray(x, dtype=np.uint64) & _U32 for x in (c0, c1, c2, c3)]
+    k0 = np.uint64(int(k0) & 0xFFFFFFFF)
+    k1 = np.uint64(int(k1) & 0xFFFFFFFF)
+    m0, m1 = np.uint64(_PHILOX_M[0]), np.uint64(_PHILOX_M[1])
+    w0, w1 = np.uint64(_PHILOX_W[0]), np.uint64(_PHILOX_W[1])
+    for r in range(10):
+        if r:
+            k0 = (k0 + w0) & _U32
+            k1 = (k1 + w1) & _U32
+        p0 = m0 * c[0]
+        p1 = m1 * c[2]
+        hi0, lo0 = p0 >> np.uint64(32), p0 & _U32
+        hi1, lo1 = p1 >> np.uint64(32), p1 & _U32
+        c = [(hi1 ^ c[1] ^ k0) & _U32, lo1, (hi0 ^ c[3] ^ k1) & _U32, lo0]
+    return c
+
+
+def dropout_threshold(p: float) -> int:
+    """t = round(256 p), clamped to [0, 255]."""
+    return int(min(255, max(0, math.floor(256.0 * float(p) + 0.5))))
+
+
+def dropout_keep(bh: int, Nq: int, Nk: int, p: float, seed: int, offset: int) -> np.ndarray:
+    """Keep mask [Nq, Nk] (bool) of head bh under the contract above."""
+    i = np.arange(Nq, dtype=np.uint64)[:, None]
+    j = np.arange(Nk, dtype=np.uint64)[None, :]
+    words = philox4x32_10(j >> np.uint64(2), i >> np.uint64(2), np.uint64(bh), np.uint64(offset),
+                          seed & 0xFFFFFFFF, (seed >> 32) & 0xFFFFFFFF)
+    sub = (i & np.uint64(3)) + np.zeros_like(j)      # word index = i mod 4
+    word = np.select([sub == 0, sub == 1, sub == 2, sub == 3], words)
+    u = (word >> ((j & np.uint64(3)) * np.uint64(8))) & np.uint64(0xFF)
+    return u >= np.uint64(dropout_threshold(p))
+
+
+def dropout_scale(p: float) -> float:
+    t = dropout_threshold(p)
+    return 256.0 / (256.0 - t)
+
+
+def attn_fwd_dropout_ref(q, k, v, scale: float, causal: bool, p: float, seed: int,
+                         offset: int) -> Tuple[np.ndarray, np.ndarray]:
+    """O = (P o Mt) V and the plain LSE, float64, [B,H,N,d] inputs."""
+    q, k, v = _as64(q), _as64(k), _as64(v)
+    B, H, N, d = q.shape
+    O = np.zeros((B, H, N, v.shape[-1]))
+    LSE = np.zeros((B, H, N))
+    rows = np.arange(N)
+    mult = dropout_scale(p)
+    for b in range(B):
+        for h in range(H):
+            S = _scores(q[b, h], k[b, h], scale)
+            if causal:
+                S = _apply_causal(S, rows)
+            P, m, l = _softmax_stats(S)
+            Mt = dropout_keep(b * H + h, N, k.shape[2], p, seed, offset) * mult
+            O[b, h] = (P * Mt) @ v[b, h]
+            LSE[b, h] = _lse(m, l)
+    return O, LSE
+
+
+def _grad_s_dropout(P: np.ndarray, Mt: np.ndarray, dP: np.ndarray, D: np.ndarray) -> np.ndarray:
+    """dS = P o (Mt o dP - D 1^T): the softmax Jacobian applied to dL/dP = Mt o dP."""
+    return P * (Mt * dP - D[:, None])
+
+
+def attn_bwd_dropout_ref(q, k, v, do, scale: float, causal: bool, p: float, seed: int,
+                         offset: int) -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """dQ, dK, dV of L = <dO, O> for the dropout forward above (fixed mask):
+      dV = (P o Mt)^T dO,  dP = dO V^T,  D_i = sum_c dO_ic O_ic (O with dropout),
+      dS = P o (Mt o dP - D 1^T),  dQ = scale dS K,  dK = scale dS^T Q
+    (the softmax Jacobian applied to dL/dP = Mt o dP, whose row sums against P
+    are D because O = (P o Mt) V)."""
+    q, k, v, do = _as64(q), _as64(k), _as64(v), _as64(do)
+    B, H, N, d = q.shape
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    rows = np.arange(N)
+    mult = dropout_scale(p)
+    for b in range(B):
+        for h in range(H):
+            S = _scores(q[b, h], k[b, h], scale)
+            if causal:
+                S = _apply_causal(S, rows)
+            P, _, _ = _softmax_stats(S)
+            Mt = dropout_keep(b * H + h, N, k.shape[2], p, seed, offset) * mult
+            Pd = P * Mt
+            O = Pd @ v[b, h]
+            dv[b, h] = Pd.T @ do[b, h]
+            dP = _grad_p(do[b, h], v[b, h])
+            dS = _grad_s_dropout(P, Mt, dP, _row_term(do[b, h], O))
+            dq[b, h] = _grad_q(dS, k[b, h], scale)
+            dk[b, h] = _grad_k(dS, q[b, h], scale)
+    return dq, dk, dv
+
+
+# ---------------------------------------------------------------------------
 # The pages' streaming algorithms (pinned, not used for GPU parity)
 # ---------------------------------------------------------------------------
 

@@ -302,6 +302,86 @@ def pin_unequal_lengths(ref):
     assert np.abs(lse - math.log(23)).max() <= 1e-13
 
 
+# ---------------------------------------------------------------------------
+# Dropout: the counter-based generator and the dropout algebra
+# ---------------------------------------------------------------------------
+
+def pin_philox_known_answers(ref):
+    """Philox4x32-10 reproduces the generator's published known-answer vectors
+    (counter, key -> output), from all-zero, all-ones and pi-digit inputs."""
+    cases = [((0, 0, 0, 0), (0, 0), (0x6627E8D5, 0xE169C58D, 0xBC57AC4C, 0x9B00DBD8)),
+             ((0xFFFFFFFF,) * 4, (0xFFFFFFFF, 0xFFFFFFFF), (0x408F276D, 0x41C83B0E, 0xA20BC7C6, 0x6D5451FD)),
+             ((0x243F6A88, 0x85A308D3, 0x13198A2E, 0x03707344), (0xA4093822, 0x299F31D0),
+              (0xD16CFE09, 0x94FDCCEB, 0x5001E420, 0x24126EA1))]
+    for ctr, key, want in cases:
+        got = tuple(int(x) for x in ref.philox4x32_10(*ctr, *key))
+        assert got == want, [hex(x) for x in got]
+
+
+def pin_dropout_p0_is_plain(ref):
+    """Dropout probability 0 keeps everything with scale 1: the plain results."""
+    q, k, v, do = (_rand((1, 2, 13, 4), 160 + i) for i in range(4))
+    for causal in (False, True):
+        o, lse = ref.attn_fwd_ref(q, k, v, 0.5, causal)
+        od, lsed = ref.attn_fwd_dropout_ref(q, k, v, 0.5, causal, 0.0, 99, 3)
+        assert np.abs(od - o).max() <= 1e-15 and np.abs(lsed - lse).max() <= 1e-15
+        g = ref.attn_bwd_ref(q, k, v, do, 0.5, causal)
+        gd = ref.attn_bwd_dropout_ref(q, k, v, do, 0.5, causal, 0.0, 99, 3)
+        for a, b in zip(gd, g):
+            assert np.abs(a - b).max() <= 1e-14
+
+
+def pin_dropout_rates(ref):
+    """Keep fractions match 1 - t/256 and the uniform bytes are flat (6-sigma bounds)."""
+    for p in (0.1, 0.3, 0.5, 0.9):
+        m = ref.dropout_keep(2, 200, 300, p, 0x0123456789ABCDEF, 11)
+        keep = 1.0 - ref.dropout_threshold(p) / 256.0
+        sd = math.sqrt(keep * (1 - keep) / m.size)
+        assert abs(m.mean() - keep) <= 6 * sd, (p, m.mean(), keep)
+    w = ref.philox4x32_10(np.arange(4096), 5, 6, 7, 0xDEADBEEF, 0x12345678)
+    b = np.concatenate([(np.asarray(x, dtype=np.uint64) >> np.uint64(8 * s)) & np.uint64(0xFF)
+                        for x in w for s in range(4)]).astype(np.int64)
+    counts = np.bincount(b, minlength=256)
+    e = b.size / 256.0
+    chi2 = float(((counts - e) ** 2 / e).sum())
+    assert chi2 <= 255 + 6 * math.sqrt(2 * 255), chi2
+
+
+def pin_dropout_unbiased(ref):
+    """Averaged over many masks (offsets) the output approaches the plain one:
+    with V = 1 every plain row is exactly 1, and E[Mt] = 1 (variance <= 1 per mask)."""
+    q, k = _rand((1, 1, 12, 3), 171), _rand((1, 1, 12, 3), 172)
+    v = np.ones((1, 1, 12, 3))
+    acc = np.zeros((1, 1, 12, 3))
+    n = 400
+    for off in range(n):
+        acc += ref.attn_fwd_dropout_ref(q, k, v, 0.8, False, 0.5, 2024, off)[0]
+    assert np.abs(acc / n - 1.0).max() <= 6 / math.sqrt(n)
+
+
+def pin_dropout_finite_differences(ref):
+    """Central differences of L = <dO, O> with the mask fixed agree with the dropout backward."""
+    h = 1e-6
+    for causal, (N, d), seed in ((False, (6, 3), 181), (True, (7, 4), 182)):
+        q, k, v = (_rand((1, 1, N, d), seed + i) for i in range(3))
+        do = _rand((1, 1, N, d), seed + 3)
+        s, p, sd, off = 0.7, 0.3, 77, 5
+        dq, dk, dv = ref.attn_bwd_dropout_ref(q, k, v, do, s, causal, p, sd, off)
+        loss = lambda a, b, c: float((ref.attn_fwd_dropout_ref(a, b, c, s, causal, p, sd, off)[0] * do).sum())
+        for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+            fd = np.zeros_like(x)
+            for idx in np.ndindex(x.shape):
+                xp, xm = x.copy(), x.copy()
+                xp[idx] += h
+                xm[idx] -= h
+                ap = {"q": q, "k": k, "v": v}
+                am = {"q": q, "k": k, "v": v}
+                ap[name], am[name] = xp, xm
+                fd[idx] = (loss(ap["q"], ap["k"], ap["v"]) - loss(am["q"], am["k"], am["v"])) / (2 * h)
+            err = np.abs(fd - g).max() / max(1.0, np.abs(g).max())
+            assert err <= 1e-7, (name, causal, err)
+
+
 ALL_PINS = [
     pin_worked_example,
     pin_online_scalar,
@@ -318,4 +398,9 @@ ALL_PINS = [
     pin_gradient_identities,
     pin_preprocess,
     pin_unequal_lengths,
+    pin_philox_known_answers,
+    pin_dropout_p0_is_plain,
+    pin_dropout_rates,
+    pin_dropout_unbiased,
+    pin_dropout_finite_differences,
 ]

@@ -39,6 +39,22 @@ def _stats_unnormalised(S):
     return E, m, E.sum(axis=1)
 
 
+def _philox_rounds(n):
+    """Philox4x32 with n rounds instead of 10 (a dropped round)."""
+    def f(c0, c1, c2, c3, k0, k1):
+        u32 = np.uint64(0xFFFFFFFF)
+        c = [np.asarray(x, dtype=np.uint64) & u32 for x in (c0, c1, c2, c3)]
+        k0, k1 = np.uint64(int(k0) & 0xFFFFFFFF), np.uint64(int(k1) & 0xFFFFFFFF)
+        for r in range(n):
+            if r:
+                k0, k1 = (k0 + np.uint64(0x9E3779B9)) & u32, (k1 + np.uint64(0xBB67AE85)) & u32
+            p0, p1 = np.uint64(0xD2511F53) * c[0], np.uint64(0xCD9E8D57) * c[2]
+            c = [((p1 >> np.uint64(32)) ^ c[1] ^ k0) & u32, p1 & u32, ((p0 >> np.uint64(32)) ^ c[3] ^ k1) & u32,
+                 p0 & u32]
+        return c
+    return f
+
+
 MUTANTS = {
     "scores_without_scale": {"_scores": lambda q, k, s: q @ k.T},
     "scores_transposed": {"_scores": lambda q, k, s: s * (k @ q.T)},
@@ -55,6 +71,10 @@ MUTANTS = {
     "dq_transposed_ds": {"_grad_q": lambda dS, k, s: s * (dS.T @ k)},
     "dk_not_transposed": {"_grad_k": lambda dS, q, s: s * (dS @ q)},
     "row_term_wrong_operand": {"_row_term": lambda do, O: (do * do).sum(axis=1)},
+    "dropout_scale_omitted": {"dropout_scale": lambda p: 1.0},
+    "dropout_keep_inverted": {"dropout_keep": lambda *a: ~_fresh_oracle().dropout_keep(*a)},
+    "dropout_ds_without_mask": {"_grad_s_dropout": lambda P, Mt, dP, D: P * (dP - D[:, None])},
+    "philox_nine_rounds": {"philox4x32_10": _philox_rounds(9)},
 }
 
 

@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU-baseline time budget")
     ap.add_argument("--batch", type=int, default=None, help="override B (smaller cases for profiler captures)")
+    ap.add_argument("--dropout", type=float, default=0.0,
+                    help="drop probability p: time fa_fwd_dropout + fa_bwd_dropout instead (fwd and bwd split only)")
     ap.add_argument("--splitkv", action="store_true",
                     help="time the split-KV forward on --splitkv-shape instead of the training step")
     ap.add_argument("--splitkv-shape", default="8,32,1,16384,128", help="B,H,Nq,Nk,d (non-causal)")
@@ -211,7 +213,27 @@ def run_ours(args, dist: Dist):
     dq, dk, dv = (torch.empty_like(q) for _ in range(3))
     stream = torch.cuda.current_stream(dev)
 
+    p_drop = float(args.dropout)
+    ws = torch.empty(max(fa.fa_bwd_workspace_bytes(B, H, N, d), 1), dtype=torch.uint8, device=dev)
+
+    def step_dropout(evs=None):
+        # the fused backward entry point runs preprocess, dK/dV and dQ: events
+        # separate the forward from the whole backward only
+        if evs:
+            evs[0].record(stream)
+        fa.fa_fwd_dropout(q, k, v, p_drop, 0x5EED, offset=0, scale=scale, causal=causal, out=o, lse=lse)
+        if evs:
+            evs[1].record(stream)
+            evs[2].record(stream)
+            evs[3].record(stream)
+        fa.fa_bwd_dropout(q, k, v, o, lse, do, p_drop, 0x5EED, offset=0, scale=scale, causal=causal,
+                          dq=dq, dk=dk, dv=dv, workspace=ws)
+        if evs:
+            evs[4].record(stream)
+
     def step(evs=None):
+        if p_drop > 0:
+            return step_dropout(evs)
         if evs:
             evs[0].record(stream)
         fa.fa_fwd(q, k, v, scale, causal, out=o, lse=lse)
@@ -267,7 +289,13 @@ def run_ours(args, dist: Dist):
             kernels[nm] = {"ms": round(ms, 4), "TFLOP/s": round(wk / ms / 1e9, 1),
                            "frac_bf16": round(wk / ms / 1e9 / burst, 3)}
     dom = max(range(4), key=lambda j: kern_ms[j])
-    src = {"fa_fwd_kernel": ["io_aware_exact_14_gb300/csrc/fa_fwd.cu", "io_aware_exact_14_gb300/csrc/fa_ptx.cuh"],
+    if p_drop > 0:
+        # only the forward is a single timed kernel in this mode
+        names[0] = "fa_fwd_kernel<dropout>"
+        kernels = {"fa_fwd_kernel<dropout>": kernels["fa_fwd_kernel"]}
+        dom = 0
+    src = {"fa_fwd_kernel<dropout>": [],
+           "fa_fwd_kernel": ["io_aware_exact_14_gb300/csrc/fa_fwd.cu", "io_aware_exact_14_gb300/csrc/fa_ptx.cuh"],
            "fa_bwd_preprocess_kernel": ["io_aware_exact_14_gb300/csrc/fa_bwd.cu"],
            "fa_bwd_dkdv_kernel": ["io_aware_exact_14_gb300/csrc/fa_bwd.cu", "io_aware_exact_14_gb300/csrc/fa_ptx.cuh"],
            "fa_bwd_dq_kernel": ["io_aware_exact_14_gb300/csrc/fa_bwd.cu", "io_aware_exact_14_gb300/csrc/fa_ptx.cuh"]}
@@ -292,7 +320,7 @@ def run_ours(args, dist: Dist):
                       "frac_bf16": round(bwd_fl / bwd_ms / 1e9 / burst, 3)}}
 
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and p_drop == 0:
         e2e = run_e2e(args, w, causal, x, dev, dist, flops_step)
 
     out = {
@@ -300,16 +328,19 @@ def run_ours(args, dist: Dist):
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16 q, k, v, dO)",
         "config": {"workload": w.name, "B": B, "H": H, "N": N, "d": d, "causal": causal, "scale": scale,
-                   "step": "fa_fwd + fa_bwd_preprocess + fa_bwd_dkdv + fa_bwd_dq",
+                   "step": ("fa_fwd_dropout + fa_bwd_dropout" if p_drop > 0 else
+                            "fa_fwd + fa_bwd_preprocess + fa_bwd_dkdv + fa_bwd_dq"),
+                   **({"dropout_p": p_drop} if p_drop > 0 else {}),
                    "l2": "inputs larger than L2: q, k, v, o, dO are 134 MB each (L2 129 MB)",
                    "parallelism": "replicas" if dist.world > 1 else "single GPU"},
         "frac_of_peak": round(value / dist.world / burst, 3),
         "passes": passes, "kernels": kernels, "roofline": roof,
         "gpu_launches": 4 * args.steps, "clocks": clk,
+        **({"note": "dropout timing line, not the headline"} if p_drop > 0 else {}),
     }
     if e2e is not None:
         out["e2e"] = e2e
-    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline and p_drop == 0:
         out["cpu_baseline"] = cpu_baseline(w, causal, args.cpu_seconds)
     dist.close()
     if dist.rank == 0:

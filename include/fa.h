@@ -161,6 +161,47 @@ fa_status fa_bwd_strided(const void* q, const fa_strides* q_st, const void* k, c
                          void* workspace, size_t workspace_bytes, struct CUstream_st* stream);
 
 /*
+ * Dropout on the attention probabilities, fused into the kernels ([WHY-FAST]
+ * "标准注意力机制的内存困局" names dropout among the steps a fused kernel
+ * does on chip; the random-number contract is this library's):
+ *   p       drop probability, 0 <= p < 1 (FA_ERR_INVALID_ARG otherwise); it is
+ *           quantised to t = round(256 p) clamped to 255, and t = 0 runs the
+ *           plain kernels
+ *   seed    Philox4x32-10 key: (seed mod 2^32, seed div 2^32)
+ *   offset  fourth counter word, so one seed gives independent masks per call
+ * Element (b, h, i, j) uses byte j mod 4 (least significant first) of word
+ * i mod 4 of Philox(counter = (j div 4, i div 4, b*H + h, offset)); it is kept
+ * when that byte is >= t, and kept probabilities are scaled by 256 / (256 - t).
+ * The same (seed, offset) in forward and backward gives the same mask.
+ */
+typedef struct {
+  float p;
+  unsigned long long seed;
+  unsigned int offset;
+} fa_dropout;
+
+/*
+ * fa_fwd with dropout: O = (P o M~) V, M~ = keep * 256 / (256 - t), P the
+ * softmax of the scores; lse is the plain log-sum-exp (dropout acts after
+ * normalisation).  dropout must not be NULL (FA_ERR_INVALID_ARG).  Other
+ * arguments, layout and errors as fa_fwd.
+ */
+fa_status fa_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* lse,
+                         int B, int H, int N, int d, float scale, int causal,
+                         const fa_dropout* dropout, struct CUstream_st* stream);
+
+/*
+ * fa_bwd for fa_fwd_dropout (same dropout parameters, so the same mask):
+ *   dV = (P o M~)^T dO, dP = dO V^T, D_i = sum_c dO_ic O_ic (O with dropout),
+ *   dS = P o (M~ o dP - D), dQ = scale dS K, dK = scale dS^T Q.
+ * Other arguments, layout, workspace and errors as fa_bwd.
+ */
+fa_status fa_bwd_dropout(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                         const void* dO, void* dq, void* dk, void* dv,
+                         int B, int H, int N, int d, float scale, int causal, const fa_dropout* dropout,
+                         void* workspace, size_t workspace_bytes, struct CUstream_st* stream);
+
+/*
  * Backward step 1: D_i = sum_c dO_ic O_ic (fp32 [B, H, N]), the row term of
  * the softmax Jacobian (derived; not on the pages).  Memory-bound.
  */

@@ -246,9 +246,24 @@ BwdStrides contiguous_bwd(const Shape& s) {
   return BwdStrides{c, c, c, c, c, c, c, c};
 }
 
+// No dropout: threshold 0 selects the plain kernels.
+const fa::DropArgs kNoDrop = fa::no_drop_args();
+
+// The dropout contract of fa.h: t = round(256 p) (p in [0, 1)), clamped to
+// 255; kept entries scaled by 256 / (256 - t).
+fa_status read_dropout(const fa_dropout* in, fa::DropArgs& out) {
+  if (in == nullptr) return FA_ERR_INVALID_ARG;
+  const float p = in->p;
+  if (!(p >= 0.f && p < 1.f)) return FA_ERR_INVALID_ARG;   // also rejects NaN
+  int t = static_cast<int>(std::floor(256.0 * static_cast<double>(p) + 0.5));
+  t = t < 0 ? 0 : (t > 255 ? 255 : t);
+  out = fa::make_drop_args(in->seed, in->offset, t);
+  return FA_OK;
+}
+
 fa_status dkdv_checked(const void* q, const void* k, const void* v, const float* lse, const void* dO,
                        const float* Dvec, void* dk, void* dv, const Shape& s, const BwdStrides& t,
-                       cudaStream_t st) {
+                       cudaStream_t st, const fa::DropArgs& drop = kNoDrop) {
   if (!load_encoder()) return FA_ERR_CUDA;
   CUtensorMap tq, tk, tv, tdo, tdk, tdv;
   FA_TRY(make_map(&tq, q, s, t.q));
@@ -257,11 +272,12 @@ fa_status dkdv_checked(const void* q, const void* k, const void* v, const float*
   FA_TRY(make_map(&tdo, dO, s, t.dO));
   FA_TRY(make_map(&tdk, dk, s, t.dk));
   FA_TRY(make_map(&tdv, dv, s, t.dv));
-  return cuda_status(fa::launch_bwd_dkdv(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s, st), "dK/dV kernel launch");
+  return cuda_status(fa::launch_bwd_dkdv(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s, drop, st), "dK/dV kernel launch");
 }
 
 fa_status dq_checked(const void* q, const void* k, const void* v, const float* lse, const void* dO,
-                     const float* Dvec, void* dq, const Shape& s, const BwdStrides& t, cudaStream_t st) {
+                     const float* Dvec, void* dq, const Shape& s, const BwdStrides& t, cudaStream_t st,
+                     const fa::DropArgs& drop = kNoDrop) {
   if (!load_encoder()) return FA_ERR_CUDA;
   CUtensorMap tq, tk, tv, tdo, tdq;
   FA_TRY(make_map(&tq, q, s, t.q));
@@ -269,7 +285,7 @@ fa_status dq_checked(const void* q, const void* k, const void* v, const float* l
   FA_TRY(make_map(&tv, v, s, t.v));
   FA_TRY(make_map(&tdo, dO, s, t.dO));
   FA_TRY(make_map(&tdq, dq, s, t.dq));
-  return cuda_status(fa::launch_bwd_dq(tq, tk, tv, tdo, tdq, lse, Dvec, s, st), "dQ kernel launch");
+  return cuda_status(fa::launch_bwd_dq(tq, tk, tv, tdo, tdq, lse, Dvec, s, drop, st), "dQ kernel launch");
 }
 
 Span view_span(const void* p, const Shape& s, const Strides& st) {
@@ -278,7 +294,7 @@ Span view_span(const void* p, const Shape& s, const Strides& st) {
 
 fa_status fwd_impl(const void* q, const fa_strides* qs, const void* k, const fa_strides* ks, const void* v,
                    const fa_strides* vs, void* o, const fa_strides* os, float* lse, int B, int H, int N, int d,
-                   float scale, int causal, cudaStream_t stream) {
+                   float scale, int causal, cudaStream_t stream, const fa::DropArgs& drop = kNoDrop) {
   FA_TRY(check_sizes(B, H, N, d));
   if (N == 0) return FA_OK;
   FA_TRY(check_ptrs({q, k, v, o}, {lse}));
@@ -298,14 +314,15 @@ fa_status fwd_impl(const void* q, const fa_strides* qs, const void* k, const fa_
   FA_TRY(make_map(&tk, k, s, Sk));
   FA_TRY(make_map(&tv, v, s, Sv));
   FA_TRY(make_map(&to, o, s, So));
-  return cuda_status(fa::launch_fwd(tq, tk, tv, to, lse, s, stream), "forward kernel launch");
+  return cuda_status(fa::launch_fwd(tq, tk, tv, to, lse, s, drop, stream), "forward kernel launch");
 }
 
 fa_status bwd_impl(const void* q, const fa_strides* qs, const void* k, const fa_strides* ks, const void* v,
                    const fa_strides* vs, const void* o, const fa_strides* os, const float* lse, const void* dO,
                    const fa_strides* dos, void* dq, const fa_strides* dqs, void* dk, const fa_strides* dks,
                    void* dv, const fa_strides* dvs, int B, int H, int N, int d, float scale, int causal,
-                   void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+                   void* workspace, size_t workspace_bytes, cudaStream_t stream,
+                   const fa::DropArgs& drop = kNoDrop) {
   FA_TRY(check_sizes(B, H, N, d));
   if (N == 0) return FA_OK;
   FA_TRY(check_ptrs({q, k, v, o, dO, dq, dk, dv}, {lse}));
@@ -332,8 +349,8 @@ fa_status bwd_impl(const void* q, const fa_strides* qs, const void* k, const fa_
   FA_TRY(check_disjoint({{lse, vb}}, {view_span(dq, s, t.dq), view_span(dk, s, t.dk), view_span(dv, s, t.dv)}));
   float* Dvec = static_cast<float*>(workspace);
   FA_TRY(cuda_status(fa::launch_bwd_preprocess(o, t.o, dO, t.dO, Dvec, s, stream), "preprocess kernel launch"));
-  FA_TRY(dkdv_checked(q, k, v, lse, dO, Dvec, dk, dv, s, t, stream));
-  return dq_checked(q, k, v, lse, dO, Dvec, dq, s, t, stream);
+  FA_TRY(dkdv_checked(q, k, v, lse, dO, Dvec, dk, dv, s, t, stream, drop));
+  return dq_checked(q, k, v, lse, dO, Dvec, dq, s, t, stream, drop);
 }
 
 }  // namespace
@@ -451,6 +468,23 @@ fa_status fa_bwd_strided(const void* q, const fa_strides* q_st, const void* k, c
                          void* workspace, size_t workspace_bytes, struct CUstream_st* stream) {
   return bwd_impl(q, q_st, k, k_st, v, v_st, o, o_st, lse, dO, dO_st, dq, dq_st, dk, dk_st, dv, dv_st, B, H, N, d,
                   scale, causal, workspace, workspace_bytes, stream);
+}
+
+fa_status fa_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                         int d, float scale, int causal, const fa_dropout* dropout, struct CUstream_st* stream) {
+  fa::DropArgs drop;
+  FA_TRY(read_dropout(dropout, drop));
+  return fwd_impl(q, nullptr, k, nullptr, v, nullptr, o, nullptr, lse, B, H, N, d, scale, causal, stream, drop);
+}
+
+fa_status fa_bwd_dropout(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                         const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
+                         int causal, const fa_dropout* dropout, void* workspace, size_t workspace_bytes,
+                         struct CUstream_st* stream) {
+  fa::DropArgs drop;
+  FA_TRY(read_dropout(dropout, drop));
+  return bwd_impl(q, nullptr, k, nullptr, v, nullptr, o, nullptr, lse, dO, nullptr, dq, nullptr, dk, nullptr, dv,
+                  nullptr, B, H, N, d, scale, causal, workspace, workspace_bytes, stream, drop);
 }
 
 fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,

@@ -7,6 +7,9 @@
 //   dV = P^T dO, dP = dO V^T, D_i = sum_c dO_ic O_ic, dS = P o (dP - D),
 //   dQ = scale dS K, dK = scale dS^T Q,
 // with P recomputed as exp(scale q.k - LSE) from the forward's log-sum-exp.
+// With dropout on the probabilities (mask M~ = keep / (1 - p), regenerated
+// from the same counter-based Philox stream as the forward), dV = (P o M~)^T dO
+// and dS = P o (M~ o dP - D), D taken from the dropped O.
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
 
@@ -165,6 +168,21 @@ __device__ __forceinline__ void st_bf16_16cols(uint32_t taddr, const float* v) {
   tmem_st16(taddr, w);
 }
 
+// The same for v o M (0/1): column c is zeroed unless kept, its keep bit in
+// byte c % 4 of ge[c / 4] (byte-MSB form).
+__device__ __forceinline__ void st_bf16_16cols_dropped(uint32_t taddr, const float* v, const uint32_t* ge) {
+  uint32_t w[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]) & keep_mask_pair(ge[i / 2], 2 * (i % 2));
+  tmem_st16(taddr, w);
+}
+
+// (M o dP) for columns c, c + 1: dP where kept, else 0.
+__device__ __forceinline__ float2 keep_pair_f(float2 v, const uint32_t* ge, int c) {
+  return make_float2(__uint_as_float(__float_as_uint(v.x) & keep_mask_one(ge[c / 4], c % 4)),
+                     __uint_as_float(__float_as_uint(v.y) & keep_mask_one(ge[c / 4], (c + 1) % 4)));
+}
+
 // Epilogue staging for one 128 x d accumulator: TMEM -> * mult -> bf16 ->
 // swizzled tile (the layout a TMA store reads) at shared address `stage`;
 // thread r writes row r.
@@ -288,13 +306,14 @@ __device__ __forceinline__ DkdvUnit dkdv_unit(int u, int n_tiles, int BH, int ba
   return w;
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool DROPOUT>
 __global__ void __launch_bounds__(384, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                        const __grid_constant__ CUtensorMap tmDK, const __grid_constant__ CUtensorMap tmDV,
                        const float* __restrict__ lse, const float* __restrict__ Dg, int N, int n_tiles,
-                       int BH, int H, int band, float scale, float scale_log2) {
+                       int BH, int H, int band, float scale, float scale_log2,
+                       const __grid_constant__ DropArgs drop) {
   using C = DkdvCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -612,6 +631,10 @@ __global__ void __launch_bounds__(384, 1)
       const int qs = gi % C::kQStages, ds = gi % C::kDOStages;
       const uint32_t par = gi & 1;
       const int qt = w.i0 + it;
+      // dropout keep words of key 128 kt + t against this half's 64 queries,
+      // drawn before S^T lands: query column c in byte c % 4 of ge[c / 4]
+      uint32_t ge[DROPOUT ? 16 : 1];
+      if constexpr (DROPOUT) dropout_cols<4>(drop, w.bh, 128 * w.kt + t, 128 * qt + 64 * h, ge);
       // -lse arrived with Q_i (q_full), -D with dO_i (do_full)
       if (!(ok = mbar_wait(&q_full[qs], (gi / C::kQStages) & 1u, g, kSiteDkdv | 7u))) break;
       if (!(ok = mbar_wait(s_full, par, g, kSiteDkdv | 8u))) break;
@@ -649,8 +672,13 @@ __global__ void __launch_bounds__(384, 1)
         for (int c = 0; c < 64; ++c)
           if (c < lim) p[c] = 0.f;
       }
+      if constexpr (DROPOUT) {   // dV takes (P o M)^T (x 1/(1-p) at the end); dS below still needs P
 #pragma unroll
-      for (int c = 0; c < 64; c += 32) st_bf16_16cols(tS + c / 2, p + c);
+        for (int c = 0; c < 64; c += 32) st_bf16_16cols_dropped(tS + c / 2, p + c, ge + c / 4);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 64; c += 32) st_bf16_16cols(tS + c / 2, p + c);
+      }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(p_full);
@@ -675,9 +703,14 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int e = 0; e < 4; e += 2) {
             const int c = 32 * b8 + 4 * i + e;
-            const float2 dp = __fadd2_rn(make_float2(__uint_as_float(dr[c / 32][c % 32]),
-                                                     __uint_as_float(dr[(c + 1) / 32][(c + 1) % 32])),
-                                         e ? make_float2(d4[i].z, d4[i].w) : make_float2(d4[i].x, d4[i].y));
+            const float2 dr2 = make_float2(__uint_as_float(dr[c / 32][c % 32]),
+                                           __uint_as_float(dr[(c + 1) / 32][(c + 1) % 32]));
+            const float2 nd = e ? make_float2(d4[i].z, d4[i].w) : make_float2(d4[i].x, d4[i].y);
+            float2 dp;
+            if constexpr (DROPOUT)
+              dp = __ffma2_rn(keep_pair_f(dr2, ge, c), make_float2(drop.scale, drop.scale), nd);   // M~ o dP - D
+            else
+              dp = __fadd2_rn(dr2, nd);
             const float2 dsv = __fmul2_rn(make_float2(p[c], p[c + 1]), dp);
             p[c] = dsv.x;
             p[c + 1] = dsv.y;
@@ -698,7 +731,7 @@ __global__ void __launch_bounds__(384, 1)
     const int last = gi - 1;
     bwd_stage_acc<D>(tmem + lane_base + (h ? C::kColDK : C::kColDV),
                      sbase + (h ? C::q_off(last % C::kQStages) : C::do_off(last % C::kDOStages)),
-                     h ? scale : 1.f, t);
+                     h ? scale : (DROPOUT ? drop.scale : 1.f), t);
     tc_fence_before();
     mbar_arrive(acc_free);   // both accumulators may be overwritten
     fence_proxy_async_smem();
@@ -801,13 +834,13 @@ __device__ __forceinline__ float2 dq_row_terms(int u, int n_tiles, int BH, int b
   return t;
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool DROPOUT>
 __global__ void __launch_bounds__(384, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                      const __grid_constant__ CUtensorMap tmDQ, const float* __restrict__ lse,
                      const float* __restrict__ Dg, int N, int n_tiles, int BH, int H, int band, float scale,
-                     float scale_log2) {
+                     float scale_log2, const __grid_constant__ DropArgs drop) {
   using C = DqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1080,6 +1113,10 @@ __global__ void __launch_bounds__(384, 1)
     const float2 nl2 = make_float2(terms.x, terms.x), nd2 = make_float2(terms.y, terms.y);
     for (int it = 0; ok && it < w.cnt; ++it, ++gk) {
       const uint32_t par = gk & 1;
+      // dropout keep words of this row against this half's 64 keys, drawn
+      // before S lands: key column c in byte c % 4 of ge[c / 4]
+      uint32_t ge[DROPOUT ? 16 : 1];
+      if constexpr (DROPOUT) dropout_rows<4>(drop, w.bh, row, 128 * it + 64 * h, ge);
       if (!(ok = mbar_wait(&s_full[gk & 1], (gk >> 1) & 1, g, kSiteDq | 7u))) break;
       __syncwarp();
       tc_fence_after();
@@ -1117,9 +1154,13 @@ __global__ void __launch_bounds__(384, 1)
       tmem_ld_fence(dr[1]);
 #pragma unroll
       for (int c = 0; c < 64; c += 2) {
-        const float2 dp = __fadd2_rn(make_float2(__uint_as_float(dr[c / 32][c % 32]),
-                                                 __uint_as_float(dr[(c + 1) / 32][(c + 1) % 32])),
-                                     nd2);
+        const float2 dr2 = make_float2(__uint_as_float(dr[c / 32][c % 32]),
+                                       __uint_as_float(dr[(c + 1) / 32][(c + 1) % 32]));
+        float2 dp;
+        if constexpr (DROPOUT)
+          dp = __ffma2_rn(keep_pair_f(dr2, ge, c), make_float2(drop.scale, drop.scale), nd2);   // M~ o dP - D
+        else
+          dp = __fadd2_rn(dr2, nd2);
         const float2 ds = __fmul2_rn(make_float2(p[c], p[c + 1]), dp);
         p[c] = ds.x;
         p[c + 1] = ds.y;
@@ -1173,58 +1214,76 @@ __global__ void __launch_bounds__(384, 1)
   named_bar_sync(1, 288);
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool DROPOUT>
 cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv, const float* lse,
-                          const float* Dvec, const Shape& s, cudaStream_t st) {
+                          const float* Dvec, const Shape& s, const DropArgs& drop, cudaStream_t st) {
   using C = DkdvCfg<D>;
-  auto kern = fa_bwd_dkdv_kernel<D, CAUSAL>;
+  auto kern = fa_bwd_dkdv_kernel<D, CAUSAL, DROPOUT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int n_tiles = (s.N + 127) / 128;
   const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
   const dim3 grid(static_cast<unsigned>(s.B) * s.H * n_tiles);
   kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s.N, n_tiles, s.B * s.H, s.H,
-                                                 head_band(s.N, s.d), s.scale, scale_log2);
+                                                 head_band(s.N, s.d), s.scale, scale_log2, drop);
   return cudaGetLastError();
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool DROPOUT>
 cudaError_t launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                         const CUtensorMap& tdo, const CUtensorMap& tdq, const float* lse, const float* Dvec,
-                        const Shape& s, cudaStream_t st) {
+                        const Shape& s, const DropArgs& drop, cudaStream_t st) {
   using C = DqCfg<D>;
-  auto kern = fa_bwd_dq_kernel<D, CAUSAL>;
+  auto kern = fa_bwd_dq_kernel<D, CAUSAL, DROPOUT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int n_tiles = (s.N + 127) / 128;
   const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
   const dim3 grid(static_cast<unsigned>(s.B) * s.H * n_tiles);
   kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, tdq, lse, Dvec, s.N, n_tiles, s.B * s.H, s.H,
-                                                 head_band(s.N, s.d), s.scale, scale_log2);
+                                                 head_band(s.N, s.d), s.scale, scale_log2, drop);
   return cudaGetLastError();
+}
+
+
+template <int D>
+cudaError_t launch_dkdv_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv, const float* lse,
+                          const float* Dvec, const Shape& s, const DropArgs& drop, cudaStream_t st) {
+  if (drop.t4 != 0)
+    return s.causal ? launch_dkdv_t<D, true, true>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s, drop, st)
+                    : launch_dkdv_t<D, false, true>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s, drop, st);
+  return s.causal ? launch_dkdv_t<D, true, false>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s, drop, st)
+                  : launch_dkdv_t<D, false, false>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s, drop, st);
+}
+
+template <int D>
+cudaError_t launch_dq_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                        const CUtensorMap& tdo, const CUtensorMap& tdq, const float* lse, const float* Dvec,
+                        const Shape& s, const DropArgs& drop, cudaStream_t st) {
+  if (drop.t4 != 0)
+    return s.causal ? launch_dq_t<D, true, true>(tq, tk, tv, tdo, tdq, lse, Dvec, s, drop, st)
+                    : launch_dq_t<D, false, true>(tq, tk, tv, tdo, tdq, lse, Dvec, s, drop, st);
+  return s.causal ? launch_dq_t<D, true, false>(tq, tk, tv, tdo, tdq, lse, Dvec, s, drop, st)
+                  : launch_dq_t<D, false, false>(tq, tk, tv, tdo, tdq, lse, Dvec, s, drop, st);
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_dkdv(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
-                            const float* lse, const float* Dvec, const Shape& s, cudaStream_t st) {
-  if (s.d == 128)
-    return s.causal ? launch_dkdv_t<128, true>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s, st)
-                    : launch_dkdv_t<128, false>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s, st);
-  return s.causal ? launch_dkdv_t<64, true>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s, st)
-                  : launch_dkdv_t<64, false>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s, st);
+                            const float* lse, const float* Dvec, const Shape& s, const DropArgs& drop,
+                            cudaStream_t st) {
+  return s.d == 128 ? launch_dkdv_d<128>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s, drop, st)
+                    : launch_dkdv_d<64>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s, drop, st);
 }
 
 cudaError_t launch_bwd_dq(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const CUtensorMap& tdq, const float* lse, const float* Dvec,
-                          const Shape& s, cudaStream_t st) {
-  if (s.d == 128)
-    return s.causal ? launch_dq_t<128, true>(tq, tk, tv, tdo, tdq, lse, Dvec, s, st)
-                    : launch_dq_t<128, false>(tq, tk, tv, tdo, tdq, lse, Dvec, s, st);
-  return s.causal ? launch_dq_t<64, true>(tq, tk, tv, tdo, tdq, lse, Dvec, s, st)
-                  : launch_dq_t<64, false>(tq, tk, tv, tdo, tdq, lse, Dvec, s, st);
+                          const Shape& s, const DropArgs& drop, cudaStream_t st) {
+  return s.d == 128 ? launch_dq_d<128>(tq, tk, tv, tdo, tdq, lse, Dvec, s, drop, st)
+                    : launch_dq_d<64>(tq, tk, tv, tdo, tdq, lse, Dvec, s, drop, st);
 }
 
 cudaError_t launch_bwd_preprocess(const void* o, const Strides& so, const void* dO, const Strides& sdo, float* Dvec,

@@ -310,11 +310,14 @@ __device__ __forceinline__ void fwd_mma_both(const FwdWork& w, uint32_t tmem, ui
 // is stored in fp32 to the partial-output map (z = split * BH + bh) and the
 // chunk's LSE to lse[(split * BH + bh) * N + row]; otherwise O goes out in
 // bf16 and z = bh, split = 0.  N is the query length, Nk the key length.
-template <int D, bool CAUSAL, bool SPLIT>
+// DROPOUT: the probabilities that feed O += P V are multiplied by the keep
+// mask and the scale (the row sum l, hence LSE, uses the plain ones).
+template <int D, bool CAUSAL, bool SPLIT, bool DROPOUT>
 __device__ __forceinline__ void fwd_softmax(const FwdWork& w, int tile, uint32_t tmem, uint8_t* smem,
                                             uint64_t* s_full, uint64_t* p_full, uint64_t* o_done,
                                             uint64_t* staged, const CUtensorMap* tmO, float* __restrict__ lse, int N,
-                                            int Nk, int BH, float scale_log2, const CtaGuard& g) {
+                                            int Nk, int BH, float scale_log2, const DropArgs& drop,
+                                            const CtaGuard& g) {
   using C = FwdCfg<D>;
   const int n_i = tile ? w.n1 : w.n0;
   if (n_i == 0) return;
@@ -328,6 +331,16 @@ __device__ __forceinline__ void fwd_softmax(const FwdWork& w, int tile, uint32_t
   float m_use = -INFINITY;  // reference max, base-2 units
   float l = 0.f;
   for (int j = 0; j < n_i; ++j) {
+    // dropout keep words of this row's 128 keys, drawn before S lands (they
+    // depend only on the row and the key tile): key c in byte c % 4 of ge[c / 4]
+    // (four words per register: key c in byte c % 4 of word (c / 4) % 4 of kp[c / 16])
+    uint32_t kp[DROPOUT ? 8 : 1];
+    if constexpr (DROPOUT) {
+      uint32_t ge[32];
+      dropout_rows<8>(drop, w.bh, row, (w.kt0 + j) * 128, ge);
+#pragma unroll
+      for (int g = 0; g < 8; ++g) kp[g] = pack_keep4(ge[4 * g], ge[4 * g + 1], ge[4 * g + 2], ge[4 * g + 3]);
+    }
     if (!mbar_wait(&s_full[tile], j & 1, g, kSiteFwd | 6u)) return;
     __syncwarp();
     tc_fence_after();
@@ -398,7 +411,11 @@ __device__ __forceinline__ void fwd_softmax(const FwdWork& w, int tile, uint32_t
                                     sc2, mo2);
         const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
         sum[(c / 2) % 4] = __fadd2_rn(sum[(c / 2) % 4], pp);
-        pk[(c / 2) % 32] = pack_bf16x2(pp.x, pp.y);
+        if constexpr (DROPOUT) {   // P o M (0/1); the 1/(1-p) scale goes into the epilogue
+          pk[(c / 2) % 32] = pack_bf16x2(pp.x, pp.y) & keep_mask_pair(unpack_keep4(kp[c / 16], (c / 4) % 4), c % 4);
+        } else {
+          pk[(c / 2) % 32] = pack_bf16x2(pp.x, pp.y);
+        }
       }
       tmem_st32(tS + 32 * h, pk);
     }
@@ -414,7 +431,7 @@ __device__ __forceinline__ void fwd_softmax(const FwdWork& w, int tile, uint32_t
   if (!mbar_wait(&o_done[tile], 0, g, kSiteFwd | 7u)) return;
   __syncwarp();
   tc_fence_after();
-  const float inv_l = l > 0.f ? 1.f / l : 0.f;
+  const float inv_l = l > 0.f ? (DROPOUT ? drop.scale : 1.f) / l : 0.f;
   if constexpr (SPLIT) {
     // fp32 staging: D/32 boxes of 128 rows x 32 floats (128-byte rows, swizzled)
     // across both Q buffers; a split-KV CTA has one query tile, and its last
@@ -480,13 +497,15 @@ __device__ __forceinline__ void fwd_softmax(const FwdWork& w, int tile, uint32_t
 // u % n_qt of one head and one chunk of kt_per_split of the n_kt key tiles;
 // tmO is then the fp32 partial-output map and lse the partial LSE.  N is the
 // query length and Nk the key length (equal outside split-KV launches).
-template <int D, bool CAUSAL, int ISSUERS, bool SPLIT>
+// DROPOUT: dropout on the probabilities (mask from `drop`, see fwd_softmax).
+template <int D, bool CAUSAL, int ISSUERS, bool SPLIT, bool DROPOUT>
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                   float* __restrict__ lse, int N, int n_pairs, int BH, int H, int band, float scale_log2, int Nk,
-                  int n_qt, int n_kt, int n_splits, int kt_per_split) {
+                  int n_qt, int n_kt, int n_splits, int kt_per_split, const __grid_constant__ DropArgs drop) {
   static_assert(!SPLIT || (!CAUSAL && ISSUERS == 1), "split-KV launches are non-causal with one issuer");
+  static_assert(!(SPLIT && DROPOUT), "split-KV launches have no dropout");
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -562,19 +581,19 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else {
     regs_inc<C::kRegsSoftmax>();
-    fwd_softmax<D, CAUSAL, SPLIT>(w, warp >> 2, tmem, smem, s_full, p_full, o_done, staged, &tmO, lse, N, Nk, BH,
-                                  scale_log2, g);
+    fwd_softmax<D, CAUSAL, SPLIT, DROPOUT>(w, warp >> 2, tmem, smem, s_full, p_full, o_done, staged, &tmO, lse, N,
+                                           Nk, BH, scale_log2, drop, g);
     __syncwarp();
     tc_fence_before();
     named_bar_sync(1, 256 + 32 * ISSUERS);
   }
 }
 
-template <int D, bool CAUSAL, int ISSUERS>
+template <int D, bool CAUSAL, int ISSUERS, bool DROPOUT>
 cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                         const CUtensorMap& to, float* lse, const Shape& s, cudaStream_t st) {
+                         const CUtensorMap& to, float* lse, const Shape& s, const DropArgs& drop, cudaStream_t st) {
   using C = FwdCfg<D>;
-  auto kern = fa_fwd_kernel<D, CAUSAL, ISSUERS, false>;
+  auto kern = fa_fwd_kernel<D, CAUSAL, ISSUERS, false, DROPOUT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   // The warpgroups' register split must fit the launch allocation, or the
@@ -588,7 +607,7 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
   const dim3 grid(static_cast<unsigned>(s.B) * s.H * n_pairs);
   kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, to, lse, s.N, n_pairs, s.B * s.H, s.H,
-                                                 head_band(s.N, s.d), scale_log2, s.N, n_qt, n_qt, 1, n_qt);
+                                                 head_band(s.N, s.d), scale_log2, s.N, n_qt, n_qt, 1, n_qt, drop);
   return cudaGetLastError();
 }
 
@@ -653,7 +672,7 @@ cudaError_t launch_fwd_splitkv_t(const CUtensorMap& tq, const CUtensorMap& tk, c
   const int n_kt = (Nk + 127) / 128;
   cudaError_t e;
   if (n_splits > 0) {
-    auto kern = fa_fwd_kernel<D, false, 1, true>;
+    auto kern = fa_fwd_kernel<D, false, 1, true, false>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     cudaFuncAttributes attr;
@@ -663,7 +682,7 @@ cudaError_t launch_fwd_splitkv_t(const CUtensorMap& tq, const CUtensorMap& tk, c
     const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
     const dim3 grid(static_cast<unsigned>(BH) * n_splits * n_qt);
     kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, top, lse_part, s.N, n_qt, BH, s.H, 1, scale_log2,
-                                                   Nk, n_qt, n_kt, n_splits, kt_per_split);
+                                                   Nk, n_qt, n_kt, n_splits, kt_per_split, no_drop_args());
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   const long long rows = static_cast<long long>(BH) * s.N;
@@ -691,18 +710,25 @@ cudaError_t launch_fwd_splitkv(const CUtensorMap& tq, const CUtensorMap& tk, con
 constexpr int kTwoIssuerMinSteps = 24;   // average key steps per CTA
 
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& to, float* lse, const Shape& s, cudaStream_t st) {
+                       const CUtensorMap& to, float* lse, const Shape& s, const DropArgs& drop, cudaStream_t st) {
+  if (drop.t4 != 0) {   // dropout launches keep one issuing warp
+    if (s.d == 128)
+      return s.causal ? launch_fwd_t<128, true, 1, true>(tq, tk, tv, to, lse, s, drop, st)
+                      : launch_fwd_t<128, false, 1, true>(tq, tk, tv, to, lse, s, drop, st);
+    return s.causal ? launch_fwd_t<64, true, 1, true>(tq, tk, tv, to, lse, s, drop, st)
+                    : launch_fwd_t<64, false, 1, true>(tq, tk, tv, to, lse, s, drop, st);
+  }
   if (s.d == 128) {
     const int n_qt = (s.N + 127) / 128;
     const int avg_steps = s.causal ? (n_qt + 1) / 2 : n_qt;
     if (avg_steps >= kTwoIssuerMinSteps)
-      return s.causal ? launch_fwd_t<128, true, 2>(tq, tk, tv, to, lse, s, st)
-                      : launch_fwd_t<128, false, 2>(tq, tk, tv, to, lse, s, st);
-    return s.causal ? launch_fwd_t<128, true, 1>(tq, tk, tv, to, lse, s, st)
-                    : launch_fwd_t<128, false, 1>(tq, tk, tv, to, lse, s, st);
+      return s.causal ? launch_fwd_t<128, true, 2, false>(tq, tk, tv, to, lse, s, drop, st)
+                      : launch_fwd_t<128, false, 2, false>(tq, tk, tv, to, lse, s, drop, st);
+    return s.causal ? launch_fwd_t<128, true, 1, false>(tq, tk, tv, to, lse, s, drop, st)
+                    : launch_fwd_t<128, false, 1, false>(tq, tk, tv, to, lse, s, drop, st);
   }
-  return s.causal ? launch_fwd_t<64, true, 1>(tq, tk, tv, to, lse, s, st)
-                  : launch_fwd_t<64, false, 1>(tq, tk, tv, to, lse, s, st);
+  return s.causal ? launch_fwd_t<64, true, 1, false>(tq, tk, tv, to, lse, s, drop, st)
+                  : launch_fwd_t<64, false, 1, false>(tq, tk, tv, to, lse, s, drop, st);
 }
 
 cudaError_t fwd_status(uint32_t* out, bool reset) {

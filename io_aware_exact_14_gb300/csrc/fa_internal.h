@@ -16,6 +16,35 @@ struct Shape {
   int causal;    // 0 or 1
 };
 
+// Dropout on the probabilities: Philox4x32-10 with key (k0, k1) = the seed's
+// low and high words (rk0[r] = k0 + r * 0x9E3779B9, rk1[r] = k1 + r *
+// 0xBB67AE85: the key of round r), counter word 3 = offset.  t (0..255) is
+// the keep threshold: t4 holds it in every byte, tlo4 its low 7 bits in every
+// byte and maj is ~0 when t < 128, else 0 (the two cases of the byte compare).
+// Kept probabilities are multiplied by scale = 256 / (256 - t).  t == 0 (t4 ==
+// 0) means no dropout.
+struct DropArgs {
+  uint32_t rk0[10], rk1[10];
+  uint32_t offset, t4, tlo4, maj;
+  float scale;
+};
+
+inline DropArgs make_drop_args(uint64_t seed, uint32_t offset, int t) {
+  DropArgs a{};
+  const uint32_t k0 = static_cast<uint32_t>(seed & 0xffffffffull), k1 = static_cast<uint32_t>(seed >> 32);
+  for (uint32_t r = 0; r < 10; ++r) {
+    a.rk0[r] = k0 + r * 0x9E3779B9u;
+    a.rk1[r] = k1 + r * 0xBB67AE85u;
+  }
+  a.offset = offset;
+  a.t4 = 0x01010101u * static_cast<uint32_t>(t);
+  a.tlo4 = 0x01010101u * static_cast<uint32_t>(t & 0x7f);
+  a.maj = t < 128 ? 0xffffffffu : 0u;
+  a.scale = static_cast<float>(256.0 / (256.0 - t));
+  return a;
+}
+inline DropArgs no_drop_args() { return make_drop_args(0, 0, 0); }
+
 // Element strides of a [B, H, N, d] bf16 view (d contiguous).
 struct Strides {
   long long b, h, n;
@@ -27,7 +56,7 @@ inline Strides contiguous_strides(const Shape& s) {
 // Forward: O and LSE from Q, K, V (TMA maps are 4-D {d, N, H, B}, box
 // {64, 128, 1, 1}, with each tensor's own strides).
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& to, float* lse, const Shape& s, cudaStream_t st);
+                       const CUtensorMap& to, float* lse, const Shape& s, const DropArgs& drop, cudaStream_t st);
 
 // Split-KV forward for short query blocks against long key sequences
 // (non-causal): Q maps {d, Nq, H, B} (s.N = Nq), K/V maps {d, Nk, H, B}; each
@@ -88,12 +117,13 @@ cudaError_t launch_bwd_preprocess(const void* o, const Strides& so, const void* 
 // Backward, step 2: dK, dV for each 128-key tile, looping over query tiles.
 cudaError_t launch_bwd_dkdv(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
-                            const float* lse, const float* Dvec, const Shape& s, cudaStream_t st);
+                            const float* lse, const float* Dvec, const Shape& s, const DropArgs& drop,
+                            cudaStream_t st);
 
 // Backward, step 3: dQ for each 128-query tile, looping over key tiles.
 cudaError_t launch_bwd_dq(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const CUtensorMap& tdq, const float* lse,
-                          const float* Dvec, const Shape& s, cudaStream_t st);
+                          const float* Dvec, const Shape& s, const DropArgs& drop, cudaStream_t st);
 
 // Fixed device scratch for callers that cannot allocate: room for the fp32
 // row term of up to kNoAllocRows rows (B*H*N), in a file-scope device array of

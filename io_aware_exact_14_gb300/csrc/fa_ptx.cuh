@@ -10,6 +10,8 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include "fa_internal.h"
+
 namespace fa {
 
 // ---------------------------------------------------------------------------
@@ -476,6 +478,153 @@ __device__ __forceinline__ void banded_order(int cta, int n_tiles, int BH, int b
   const int r = cta - b * per_band;
   rank = r / width;
   bh = bh0 + r % width;
+}
+
+// ---------------------------------------------------------------------------
+// Dropout masks: Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel
+// random numbers: as easy as 1, 2, 3", SC 2011) on a 4 x 4 (query, key) block
+// per call: counter (key / 4, query / 4, head, offset), output word
+// (query mod 4), byte (key mod 4) is the element's uniform byte; kept when the
+// byte is at least the threshold t.
+// ---------------------------------------------------------------------------
+
+// Philox4x32-10 on counter (c0, c1, c2, c3); the round keys come from the
+// kernel parameters (DropArgs::rk0/rk1), so each round is two widening
+// multiplies and two three-way xors.
+__device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
+                                               const DropArgs& d) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint64_t p0 = static_cast<uint64_t>(0xD2511F53u) * c0;
+    const uint64_t p1 = static_cast<uint64_t>(0xCD9E8D57u) * c2;
+    const uint32_t n0 = static_cast<uint32_t>(p1 >> 32) ^ c1 ^ d.rk0[r];
+    const uint32_t n2 = static_cast<uint32_t>(p0 >> 32) ^ c3 ^ d.rk1[r];
+    c1 = static_cast<uint32_t>(p1);
+    c3 = static_cast<uint32_t>(p0);
+    c0 = n0;
+    c2 = n2;
+  }
+  return make_uint4(c0, c1, c2, c3);
+}
+
+// Keep test of four uniform bytes at once, in byte-MSB form: bit 8b+7 of the
+// result is set where byte b >= t; the other bits are don't-care.  SWAR
+// compare (Hacker's Delight, multibyte arithmetic): z = (x | 0x80..) -
+// (t & 0x7f..) cannot borrow across bytes and has a byte's MSB set where its
+// low 7 bits are >= those of t; the MSBs of x and t then decide: x >= t is
+// x_msb | z_msb when t < 128 and x_msb & z_msb otherwise, i.e. the majority
+// of (x, z, maj) with maj = t < 128 ? ~0 : 0.
+__device__ __forceinline__ uint32_t keep_msb4(uint32_t x, const DropArgs& d) {
+  const uint32_t z = (x | 0x80808080u) - d.tlo4;
+  return (x & z) | ((x | z) & d.maj);
+}
+
+// 0xFFFF in the half of a bf16x2 whose element is kept: elements b, b+1
+// (b = 0 or 2) of a byte-MSB keep word (prmt replicating the bytes' sign bits).
+__device__ __forceinline__ uint32_t keep_mask_pair(uint32_t ge, int b) {
+  uint32_t m;
+  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(m) : "r"(ge), "r"(b == 0 ? 0x9988u : 0xBBAAu));
+  return m;
+}
+
+// All ones where element b (0..3) of a byte-MSB keep word is kept, else 0.
+__device__ __forceinline__ uint32_t keep_mask_one(uint32_t ge, int b) {
+  uint32_t m;
+  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(m) : "r"(ge), "r"(0x1111u * (8u | static_cast<uint32_t>(b))));
+  return m;
+}
+
+// Quad exchange: lane s of each quad holds y[k] = its word for lane (s + k)
+// mod 4; returns z[m] = lane m's word for lane s.  Rotations are selects on
+// the lane's position (branch-free); three shuffles.
+__device__ __forceinline__ void quad_exchange(const uint32_t (&x)[4], uint32_t (&z)[4]) {
+  const int lane = threadIdx.x & 31, s = lane & 3, qb = lane & ~3;
+  // y[k] = x[(s + k) mod 4]: rotate left by s
+  uint32_t y[4];
+  {
+    const bool r1 = s & 1, r2 = s & 2;
+    uint32_t a0 = r1 ? x[1] : x[0], a1 = r1 ? x[2] : x[1], a2 = r1 ? x[3] : x[2], a3 = r1 ? x[0] : x[3];
+    y[0] = r2 ? a2 : a0;
+    y[1] = r2 ? a3 : a1;
+    y[2] = r2 ? a0 : a2;
+    y[3] = r2 ? a1 : a3;
+  }
+  // step k: receive from lane (s - k) mod 4 its y[k], which is meant for lane s
+  uint32_t r[4];
+  r[0] = y[0];
+#pragma unroll
+  for (int k = 1; k < 4; ++k) r[k] = __shfl_sync(0xffffffffu, y[k], qb + ((s - k) & 3));
+  // z[m] = r[(s - m) mod 4]: with r'[j] = r[-j mod 4], z[m] = r'[(m - s) mod 4]
+  const uint32_t q0 = r[0], q1 = r[3], q2 = r[2], q3 = r[1];
+  const bool r1 = s & 1, r2 = s & 2;
+  const uint32_t b0 = r1 ? q3 : q0, b1 = r1 ? q0 : q1, b2 = r1 ? q1 : q2, b3 = r1 ? q2 : q3;
+  z[0] = r2 ? b2 : b0;
+  z[1] = r2 ? b3 : b1;
+  z[2] = r2 ? b0 : b2;
+  z[3] = r2 ? b1 : b3;
+}
+
+// Keep words of query row i against keys j0 .. j0 + 16G - 1 (j0 a multiple of
+// 16), for warps whose lanes hold consecutive rows: ge[c / 4] has element c's
+// keep bit at bit 8 (c mod 4) + 7 (byte-MSB form).  Lane s of a quad draws the
+// 4 x 4 blocks of keys j0 + 16g + 4s .. +3 for the quad's rows (all G calls
+// first, independent chains), then the quad swaps words.
+template <int G>
+__device__ __forceinline__ void dropout_rows(const DropArgs& d, int bh, int i, int j0, uint32_t (&ge)[4 * G]) {
+  const int s = threadIdx.x & 3;
+  uint4 x[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+    x[g] = philox4x32_10(static_cast<uint32_t>(j0 >> 2) + 4 * g + s, static_cast<uint32_t>(i >> 2),
+                         static_cast<uint32_t>(bh), d.offset, d);
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const uint32_t w[4] = {keep_msb4(x[g].x, d), keep_msb4(x[g].y, d), keep_msb4(x[g].z, d),
+                           keep_msb4(x[g].w, d)};
+    uint32_t z[4];
+    quad_exchange(w, z);   // word w of lane m = row 4q + w, keys 16g + 4m ..
+#pragma unroll
+    for (int m = 0; m < 4; ++m) ge[4 * g + m] = z[m];
+  }
+}
+
+// Four byte-MSB keep words in one register: word k's MSBs moved to bit 7 - k
+// of each byte (unpack_keep4 shifts them back; other bits are don't-care).
+__device__ __forceinline__ uint32_t pack_keep4(uint32_t a, uint32_t b, uint32_t c, uint32_t e) {
+  uint32_t r = a & 0x80808080u;
+  r |= (b >> 1) & 0x40404040u;
+  r |= (c >> 2) & 0x20202020u;
+  r |= (e >> 3) & 0x10101010u;
+  return r;
+}
+__device__ __forceinline__ uint32_t unpack_keep4(uint32_t r, int k) { return r << k; }
+
+// Keep words of key j against queries i0 .. i0 + 16G - 1 (i0 a multiple of
+// 16), for warps whose lanes hold consecutive keys: ge[c / 4] has the keep bit
+// of query i0 + c at bit 8 (c mod 4) + 7.  Lane s of a quad draws the blocks
+// of queries i0 + 16g + 4s .. +3 for the quad's keys, transposes its 4 x 4
+// bytes (word w byte b -> word b byte w) and the quad swaps words.
+template <int G>
+__device__ __forceinline__ void dropout_cols(const DropArgs& d, int bh, int j, int i0, uint32_t (&ge)[4 * G]) {
+  const int s = threadIdx.x & 3;
+  uint4 x[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+    x[g] = philox4x32_10(static_cast<uint32_t>(j >> 2), static_cast<uint32_t>(i0 >> 2) + 4 * g + s,
+                         static_cast<uint32_t>(bh), d.offset, d);
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const uint32_t a = keep_msb4(x[g].x, d), b = keep_msb4(x[g].y, d), c = keep_msb4(x[g].z, d),
+                   e = keep_msb4(x[g].w, d);
+    const uint32_t lo01 = __byte_perm(a, b, 0x5140), hi01 = __byte_perm(a, b, 0x7362);
+    const uint32_t lo23 = __byte_perm(c, e, 0x5140), hi23 = __byte_perm(c, e, 0x7362);
+    const uint32_t w[4] = {__byte_perm(lo01, lo23, 0x5410), __byte_perm(lo01, lo23, 0x7632),
+                           __byte_perm(hi01, hi23, 0x5410), __byte_perm(hi01, hi23, 0x7632)};
+    uint32_t z[4];
+    quad_exchange(w, z);   // word b of lane m = key 4(j/4) + b, queries 16g + 4m ..
+#pragma unroll
+    for (int m = 0; m < 4; ++m) ge[4 * g + m] = z[m];
+  }
 }
 
 // ---------------------------------------------------------------------------

@@ -38,6 +38,8 @@ SIGNATURES = {
     "fa_fwd_splitkv_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "fa_bwd_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
+    "fa_fwd_dropout": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P]),
+    "fa_bwd_dropout": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P, _SZ, _P]),
     "fa_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
     "fa_bwd_preprocess": (_I, [_P, _P, _P, _I, _I, _I, _I, _P]),
     "fa_bwd_dkdv": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
@@ -52,6 +54,11 @@ SIGNATURES = {
 class FaStrides(ctypes.Structure):
     """fa_strides: element strides (b, h, n) of a [B, H, N, d] view, d contiguous."""
     _fields_ = [("b", ctypes.c_longlong), ("h", ctypes.c_longlong), ("n", ctypes.c_longlong)]
+
+
+class FaDropout(ctypes.Structure):
+    """fa_dropout: drop probability p, Philox key `seed` and counter word `offset`."""
+    _fields_ = [("p", ctypes.c_float), ("seed", ctypes.c_ulonglong), ("offset", ctypes.c_uint)]
 
 
 class FAError(RuntimeError):
@@ -275,6 +282,52 @@ def fa_bwd(q, k, v, o, lse, do, scale: Optional[float] = None, causal: bool = Fa
                        dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, scale, int(bool(causal)),
                        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_ptr(stream))
     _check("fa_bwd", st)
+    return dq, dk, dv
+
+
+def fa_fwd_dropout(q, k, v, p: float, seed: int, offset: int = 0, scale: Optional[float] = None,
+                   causal: bool = False, out=None, lse=None, stream=None):
+    """fa_fwd with dropout on the probabilities: O = (P o M~) V and the plain LSE."""
+    shape = _bhnd(q, "q")
+    _same(shape, k, "k")
+    _same(shape, v, "v")
+    B, H, N, d = shape
+    scale = default_scale(d) if scale is None else float(scale)
+    out = torch.empty_like(q) if out is None else out
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _same(shape, out, "out")
+    _vec(lse, shape, "lse")
+    drop = FaDropout(float(p), int(seed), int(offset))
+    st = load().fa_fwd_dropout(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                               B, H, N, d, scale, int(bool(causal)), ctypes.addressof(drop), _stream_ptr(stream))
+    _check("fa_fwd_dropout", st)
+    return out, lse
+
+
+def fa_bwd_dropout(q, k, v, o, lse, do, p: float, seed: int, offset: int = 0, scale: Optional[float] = None,
+                   causal: bool = False, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """fa_bwd for fa_fwd_dropout with the same (p, seed, offset): the same mask."""
+    shape = _bhnd(q, "q")
+    for t, n in ((k, "k"), (v, "v"), (o, "o"), (do, "do")):
+        _same(shape, t, n)
+    _vec(lse, shape, "lse")
+    B, H, N, d = shape
+    scale = default_scale(d) if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _same(shape, t, n)
+    need = fa_bwd_workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    drop = FaDropout(float(p), int(seed), int(offset))
+    st = load().fa_bwd_dropout(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                               do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, scale,
+                               int(bool(causal)), ctypes.addressof(drop), workspace.data_ptr(),
+                               workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    _check("fa_bwd_dropout", st)
     return dq, dk, dv
 
 

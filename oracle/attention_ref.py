@@ -273,8 +273,10 @@ def dropout_scale(p: float) -> float:
 
 
 def attn_fwd_dropout_ref(q, k, v, scale: float, causal: bool, p: float, seed: int,
-                         offset: int) -> Tuple[np.ndarray, np.ndarray]:
-    """O = (P o Mt) V and the plain LSE, float64, [B,H,N,d] inputs."""
+                         offset: int, head0: int = 0) -> Tuple[np.ndarray, np.ndarray]:
+    """O = (P o Mt) V and the plain LSE, float64, [B,H,N,d] inputs.  The mask of
+    slice [b, h] is that of head index head0 + b*H + h (head0 > 0 for one head
+    cut out of a larger batch)."""
     q, k, v = _as64(q), _as64(k), _as64(v)
     B, H, N, d = q.shape
     O = np.zeros((B, H, N, v.shape[-1]))
@@ -287,7 +289,7 @@ def attn_fwd_dropout_ref(q, k, v, scale: float, causal: bool, p: float, seed: in
             if causal:
                 S = _apply_causal(S, rows)
             P, m, l = _softmax_stats(S)
-            Mt = dropout_keep(b * H + h, N, k.shape[2], p, seed, offset) * mult
+            Mt = dropout_keep(head0 + b * H + h, N, k.shape[2], p, seed, offset) * mult
             O[b, h] = (P * Mt) @ v[b, h]
             LSE[b, h] = _lse(m, l)
     return O, LSE
@@ -299,7 +301,7 @@ def _grad_s_dropout(P: np.ndarray, Mt: np.ndarray, dP: np.ndarray, D: np.ndarray
 
 
 def attn_bwd_dropout_ref(q, k, v, do, scale: float, causal: bool, p: float, seed: int,
-                         offset: int) -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
+                         offset: int, head0: int = 0) -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
     """dQ, dK, dV of L = <dO, O> for the dropout forward above (fixed mask):
       dV = (P o Mt)^T dO,  dP = dO V^T,  D_i = sum_c dO_ic O_ic (O with dropout),
       dS = P o (Mt o dP - D 1^T),  dQ = scale dS K,  dK = scale dS^T Q
@@ -316,7 +318,7 @@ def attn_bwd_dropout_ref(q, k, v, do, scale: float, causal: bool, p: float, seed
             if causal:
                 S = _apply_causal(S, rows)
             P, _, _ = _softmax_stats(S)
-            Mt = dropout_keep(b * H + h, N, k.shape[2], p, seed, offset) * mult
+            Mt = dropout_keep(head0 + b * H + h, N, k.shape[2], p, seed, offset) * mult
             Pd = P * Mt
             O = Pd @ v[b, h]
             dv[b, h] = Pd.T @ do[b, h]

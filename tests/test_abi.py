@@ -109,3 +109,33 @@ def test_status_strings(lib):
         text = lib.fa_status_string(s).decode()
         assert text.startswith("FA_")
     assert lib.fa_status_string(99).decode() == "unknown fa_status"
+
+
+class _Dropout(ctypes.Structure):
+    _fields_ = [("p", ctypes.c_float), ("seed", ctypes.c_ulonglong), ("offset", ctypes.c_uint)]
+
+
+def test_dropout_argument_checks(lib):
+    """A NULL fa_dropout or p outside [0, 1) is rejected before any device access;
+    so are the usual pointer and size errors."""
+    def fwd_d(drop, **kw):
+        a = dict(q=FAKE, k=FAKE + 0x100000, v=FAKE + 0x200000, o=FAKE + 0x300000, lse=FAKE + 0x400000, d=64)
+        a.update(kw)
+        ptr = ctypes.addressof(drop) if drop is not None else None
+        return lib.fa_fwd_dropout(a["q"], a["k"], a["v"], a["o"], a["lse"], 1, 1, 128, a["d"], 0.125, 0, ptr, None)
+
+    assert fwd_d(None) == 1
+    for p in (1.0, 1.5, -0.1, float("nan"), float("inf")):
+        assert fwd_d(_Dropout(p, 1, 0)) == 1, p
+    assert fwd_d(_Dropout(0.1, 1, 0), q=0) == 1
+    assert fwd_d(_Dropout(0.1, 1, 0), d=96) == 2
+    assert fwd_d(_Dropout(0.1, 1, 0), o=FAKE) == 1
+    p = [FAKE + i * 0x100000 for i in range(12)]
+    ws = lib.fa_bwd_workspace_bytes(1, 1, 128, 64)
+    drop = _Dropout(0.2, 5, 0)
+    assert lib.fa_bwd_dropout(*p[:9], 1, 1, 128, 64, 0.125, 1, None, p[9], ws, None) == 1
+    assert lib.fa_bwd_dropout(*p[:9], 1, 1, 128, 64, 0.125, 1, ctypes.addressof(_Dropout(1.0, 5, 0)), p[9], ws,
+                              None) == 1
+    assert lib.fa_bwd_dropout(*p[:9], 1, 1, 128, 64, 0.125, 1, ctypes.addressof(drop), 0, ws, None) == 4
+    assert lib.fa_bwd_dropout(*p[:6], p[0], *p[7:9], 1, 1, 128, 64, 0.125, 1, ctypes.addressof(drop), p[9], ws,
+                              None) == 1

@@ -11,7 +11,10 @@
  * Conventions shared by every entry point
  *   - Tensors are row-major, contiguous, [B, H, N, d] bf16 (d innermost);
  *     row statistics (LSE, D) are [B, H, N] fp32.  Q, K, V share one N.
- *   - d must be 64 or 128, else FA_ERR_UNSUPPORTED.  N >= 0; N == 0 is a
+ *   - d must be a multiple of 8 from 8 to 128, else FA_ERR_UNSUPPORTED
+ *     (d <= 64 runs the d = 64 kernels and 64 < d <= 128 the d = 128 ones,
+ *     at their cost: the missing columns are zero-filled on chip, never
+ *     read from or written to memory).  N >= 0; N == 0 is a
  *     no-op that returns FA_OK.  B, H >= 1.  B*H*ceil(N/128) must fit in
  *     2^31 - 1.
  *   - Every device pointer must be 16-byte aligned (fp32 vectors: 4-byte),
@@ -45,7 +48,7 @@ struct CUstream_st; /* cudaStream_t and CUstream are both `struct CUstream_st *`
 typedef enum {
   FA_OK = 0,
   FA_ERR_INVALID_ARG = 1,  /* null/misaligned/overlapping pointer, bad size or scale */
-  FA_ERR_UNSUPPORTED = 2,  /* head dim other than 64/128, or sizes beyond the limits */
+  FA_ERR_UNSUPPORTED = 2,  /* head dim not a multiple of 8 in [8, 128], or sizes beyond the limits */
   FA_ERR_CUDA = 3,         /* a CUDA runtime/driver call or a launch failed */
   FA_ERR_WORKSPACE = 4,    /* workspace missing, misaligned or too small */
   FA_ERR_TIMEOUT = 5       /* a kernel gave up on a wait (see fa_debug_status) */
@@ -93,9 +96,10 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, f
 
 /*
  * Workspace bytes fa_fwd_splitkv needs for these arguments (the same
- * num_splits rule, on the current device): n_used * B*H*Nq*d fp32 partial
- * outputs plus n_used * B*H*Nq fp32 partial LSE, each rounded up to 256
- * bytes.  0 for invalid sizes, Nq == 0 or Nk == 0.
+ * num_splits rule, on the current device): n_used * B*H*Nq*D fp32 partial
+ * outputs (D = 64 for d <= 64, else 128) plus n_used * B*H*Nq fp32 partial
+ * LSE, each rounded up to 256 bytes.  0 for invalid sizes, Nq == 0 or
+ * Nk == 0.
  */
 size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int d, int num_splits);
 

@@ -51,10 +51,10 @@ bool overlaps(const Span& a, const Span& b) {
   return a.bytes && b.bytes && a0 < b0 + b.bytes && b0 < a0 + a.bytes;
 }
 
-// Sizes: B, H >= 1, N >= 0, d in {64, 128}, grid-size limits.
+// Sizes: B, H >= 1, N >= 0, d a multiple of 8 in [8, 128], grid-size limits.
 fa_status check_sizes(int B, int H, int N, int d) {
   if (B < 1 || H < 1 || N < 0) return FA_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (d < 8 || d > 128 || d % 8 != 0) return FA_ERR_UNSUPPORTED;
   const long long bh = static_cast<long long>(B) * H;
   const long long tiles = bh * ((static_cast<long long>(N) + 127) / 128);
   if (bh > INT32_MAX || tiles > INT32_MAX || bh * N > (1ll << 40)) return FA_ERR_UNSUPPORTED;
@@ -87,8 +87,8 @@ fa_status check_disjoint(std::initializer_list<Span> outs, std::initializer_list
 
 // 4-D view {d, N, H, B} of a [B, H, N, d] bf16 tensor with element strides
 // `st` (d contiguous); boxes of 64 x 128 rows with the 128-byte swizzle the
-// tensor-core descriptors expect.  Rows past N read as zero and are clipped
-// on store.
+// tensor-core descriptors expect.  Rows past N and columns past d read as
+// zero and are clipped on store.
 fa_status make_map(CUtensorMap* m, const void* base, const Shape& s, const Strides& st) {
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(s.d), static_cast<cuuint64_t>(s.N),
                               static_cast<cuuint64_t>(s.H), static_cast<cuuint64_t>(s.B)};
@@ -201,8 +201,9 @@ fa_status cuda_status(cudaError_t e, const char* what) {
   return e == cudaSuccess ? FA_OK : fail(what, static_cast<int>(e), cudaGetErrorString(e));
 }
 
-// 3-D view {d, Nq, Z} of fp32 rows (split-KV partial outputs, Z = splits *
-// B*H); boxes of 32 floats (128 bytes) x 128 rows, 128-byte swizzle.
+// 3-D view {D, Nq, Z} of fp32 rows (split-KV partial outputs, Z = splits *
+// B*H, D the kernel's padded head dim); boxes of 32 floats (128 bytes) x 128
+// rows, 128-byte swizzle.
 fa_status make_map_f32(CUtensorMap* m, const void* base, int d, int Nq, long long Z) {
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(Nq), static_cast<cuuint64_t>(Z)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(Nq) * d * 4};
@@ -216,7 +217,8 @@ fa_status make_map_f32(CUtensorMap* m, const void* base, int d, int Nq, long lon
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Split-KV workspace: fp32 partial O [n, B*H, Nq, d], then fp32 partial LSE [n, B*H, Nq].
+// Split-KV workspace: fp32 partial O [n, B*H, Nq, D] (D = kernel_dim(d): the
+// kernel writes its padded columns, zeros), then fp32 partial LSE [n, B*H, Nq].
 struct SplitPlan {
   int kt_per_split, n_splits;
   size_t o_bytes, lse_bytes;
@@ -231,7 +233,7 @@ fa_status split_plan(int B, int H, int Nq, int Nk, int d, int want, SplitPlan& p
   }
   fa::splitkv_chunks(B, H, Nq, Nk, want, sms, p.kt_per_split, p.n_splits);
   const size_t rows = static_cast<size_t>(B) * H * Nq * p.n_splits;
-  p.o_bytes = round256(rows * d * 4);
+  p.o_bytes = round256(rows * fa::kernel_dim(d) * 4);
   p.lse_bytes = round256(rows * 4);
   return FA_OK;
 }
@@ -391,7 +393,7 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, f
   if (p.n_splits > 0) {
     FA_TRY(make_map(&tk, k, sk));
     FA_TRY(make_map(&tv, v, sk));
-    FA_TRY(make_map_f32(&top, workspace, d, Nq, static_cast<long long>(p.n_splits) * B * H));
+    FA_TRY(make_map_f32(&top, workspace, fa::kernel_dim(d), Nq, static_cast<long long>(p.n_splits) * B * H));
   } else {
     tk = tq;
     tv = tq;
@@ -514,7 +516,7 @@ const char* fa_status_string(fa_status s) {
   switch (s) {
     case FA_OK: return "FA_OK: success";
     case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: null, misaligned or overlapping pointer, or bad size/scale";
-    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: head dim must be 64 or 128, or sizes exceed the limits";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: head dim must be a multiple of 8 in [8, 128], or sizes exceed the limits";
     case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA call or kernel launch failed";
     case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE: workspace missing, misaligned or too small";
     case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a kernel gave up on a pipeline wait";

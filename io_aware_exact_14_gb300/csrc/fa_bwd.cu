@@ -54,9 +54,9 @@ __device__ __forceinline__ uint4 ldg_stream(const void* p) {
 
 // Byte offset of row `row` (= (b H + h) N + n) of a strided [B, H, N, d] bf16
 // view; `contig` takes the contiguous layout's plain row * d.
-__device__ __forceinline__ size_t pre_row_offset(long long row, bool contig, int D, int H, int N,
+__device__ __forceinline__ size_t pre_row_offset(long long row, bool contig, int d, int H, int N,
                                                  const Strides& st) {
-  if (contig) return static_cast<size_t>(row) * D * 2;
+  if (contig) return static_cast<size_t>(row) * d * 2;
   const long long t = row / N, n = row - t * N, b = t / H, h = t - b * H;
   return static_cast<size_t>(b * st.b + h * st.h + n * st.n) * 2;
 }
@@ -65,8 +65,9 @@ template <int D>
 __global__ void __launch_bounds__(kPreThreads) fa_bwd_preprocess_kernel(const uint8_t* __restrict__ o,
                                                                        const uint8_t* __restrict__ dO,
                                                                        float* __restrict__ Dvec, long long rows,
-                                                                       int H, int N, Strides so, Strides sdo,
-                                                                       bool contig) {
+                                                                       int H, int N, int d, Strides so,
+                                                                       Strides sdo, bool contig) {
+  // D = 64 or 128 covers d <= D: chunks at or past d count as zero
   constexpr int kTpr = D / 8;                 // threads per row, one 16-byte chunk each
   constexpr int kRows = kPreThreads / kTpr;   // rows per block per step
   const int sub = threadIdx.x % kTpr;
@@ -77,9 +78,11 @@ __global__ void __launch_bounds__(kPreThreads) fa_bwd_preprocess_kernel(const ui
 #pragma unroll
     for (int u = 0; u < kPreUnroll; ++u) {
       const long long row = base + static_cast<long long>(u) * kRows;
-      if (row < rows) {
-        a[u] = ldg_stream(o + pre_row_offset(row, contig, D, H, N, so) + sub * 16);
-        b[u] = ldg_stream(dO + pre_row_offset(row, contig, D, H, N, sdo) + sub * 16);
+      a[u] = make_uint4(0u, 0u, 0u, 0u);
+      b[u] = a[u];
+      if (row < rows && sub * 8 < d) {
+        a[u] = ldg_stream(o + pre_row_offset(row, contig, d, H, N, so) + sub * 16);
+        b[u] = ldg_stream(dO + pre_row_offset(row, contig, d, H, N, sdo) + sub * 16);
       }
     }
 #pragma unroll
@@ -1275,14 +1278,14 @@ cudaError_t launch_bwd_dkdv(const CUtensorMap& tq, const CUtensorMap& tk, const 
                             const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
                             const float* lse, const float* Dvec, const Shape& s, const DropArgs& drop,
                             cudaStream_t st) {
-  return s.d == 128 ? launch_dkdv_d<128>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s, drop, st)
+  return kernel_dim(s.d) == 128 ? launch_dkdv_d<128>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s, drop, st)
                     : launch_dkdv_d<64>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s, drop, st);
 }
 
 cudaError_t launch_bwd_dq(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const CUtensorMap& tdq, const float* lse, const float* Dvec,
                           const Shape& s, const DropArgs& drop, cudaStream_t st) {
-  return s.d == 128 ? launch_dq_d<128>(tq, tk, tv, tdo, tdq, lse, Dvec, s, drop, st)
+  return kernel_dim(s.d) == 128 ? launch_dq_d<128>(tq, tk, tv, tdo, tdq, lse, Dvec, s, drop, st)
                     : launch_dq_d<64>(tq, tk, tv, tdo, tdq, lse, Dvec, s, drop, st);
 }
 
@@ -1294,17 +1297,17 @@ cudaError_t launch_bwd_preprocess(const void* o, const Strides& so, const void* 
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  const int rows_per_block = (kPreThreads / (s.d / 8)) * kPreUnroll;
+  const int rows_per_block = (kPreThreads / (kernel_dim(s.d) / 8)) * kPreUnroll;
   const long long want = (rows + rows_per_block - 1) / rows_per_block;
   const int grid = static_cast<int>(want < 8LL * sms ? want : 8LL * sms);
   const Strides c = contiguous_strides(s);
   const bool contig = so.b == c.b && so.h == c.h && so.n == c.n && sdo.b == c.b && sdo.h == c.h && sdo.n == c.n;
-  if (s.d == 128)
+  if (kernel_dim(s.d) == 128)
     fa_bwd_preprocess_kernel<128><<<grid, kPreThreads, 0, st>>>(
-        static_cast<const uint8_t*>(o), static_cast<const uint8_t*>(dO), Dvec, rows, s.H, s.N, so, sdo, contig);
+        static_cast<const uint8_t*>(o), static_cast<const uint8_t*>(dO), Dvec, rows, s.H, s.N, s.d, so, sdo, contig);
   else
     fa_bwd_preprocess_kernel<64><<<grid, kPreThreads, 0, st>>>(
-        static_cast<const uint8_t*>(o), static_cast<const uint8_t*>(dO), Dvec, rows, s.H, s.N, so, sdo, contig);
+        static_cast<const uint8_t*>(o), static_cast<const uint8_t*>(dO), Dvec, rows, s.H, s.N, s.d, so, sdo, contig);
   return cudaGetLastError();
 }
 

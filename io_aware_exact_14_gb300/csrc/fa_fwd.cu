@@ -621,7 +621,7 @@ template <int D>
 __global__ void __launch_bounds__(256) fa_fwd_merge_kernel(const float* __restrict__ o_part,
                                                            const float* __restrict__ lse_part,
                                                            __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
-                                                           long long rows, int n_splits) {
+                                                           long long rows, int n_splits, int d) {
   constexpr int kPer = D / 32;
   const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -655,10 +655,13 @@ __global__ void __launch_bounds__(256) fa_fwd_merge_kernel(const float* __restri
     }
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-  __nv_bfloat16* dst = o + row * D + lane * kPer;
+  // partial rows are D wide (padded with zeros); O rows are d wide
+  __nv_bfloat16* dst = o + row * d + lane * kPer;
+  if (lane * kPer < d) {
 #pragma unroll
-  for (int e = 0; e < kPer; e += 2)
-    *reinterpret_cast<__nv_bfloat162*>(dst + e) = __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
+    for (int e = 0; e < kPer; e += 2)
+      *reinterpret_cast<__nv_bfloat162*>(dst + e) = __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
+  }
   if (lane == 0) lse[row] = wsum > 0.f ? m + __logf(wsum) : -INFINITY;
 }
 
@@ -688,7 +691,7 @@ cudaError_t launch_fwd_splitkv_t(const CUtensorMap& tq, const CUtensorMap& tk, c
   const long long rows = static_cast<long long>(BH) * s.N;
   const long long blocks = (rows + 7) / 8;   // 8 warps (rows) per block
   fa_fwd_merge_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
-      o_part, lse_part, static_cast<__nv_bfloat16*>(o), lse, rows, n_splits);
+      o_part, lse_part, static_cast<__nv_bfloat16*>(o), lse, rows, n_splits, s.d);
   return cudaGetLastError();
 }
 
@@ -697,7 +700,7 @@ cudaError_t launch_fwd_splitkv_t(const CUtensorMap& tq, const CUtensorMap& tk, c
 cudaError_t launch_fwd_splitkv(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                const CUtensorMap& top, const float* o_part, float* lse_part, void* o, float* lse,
                                const Shape& s, int Nk, int n_splits, int kt_per_split, cudaStream_t st) {
-  return s.d == 128
+  return kernel_dim(s.d) == 128
              ? launch_fwd_splitkv_t<128>(tq, tk, tv, top, o_part, lse_part, o, lse, s, Nk, n_splits, kt_per_split, st)
              : launch_fwd_splitkv_t<64>(tq, tk, tv, top, o_part, lse_part, o, lse, s, Nk, n_splits, kt_per_split, st);
 }
@@ -712,13 +715,13 @@ constexpr int kTwoIssuerMinSteps = 24;   // average key steps per CTA
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to, float* lse, const Shape& s, const DropArgs& drop, cudaStream_t st) {
   if (drop.t4 != 0) {   // dropout launches keep one issuing warp
-    if (s.d == 128)
+    if (kernel_dim(s.d) == 128)
       return s.causal ? launch_fwd_t<128, true, 1, true>(tq, tk, tv, to, lse, s, drop, st)
                       : launch_fwd_t<128, false, 1, true>(tq, tk, tv, to, lse, s, drop, st);
     return s.causal ? launch_fwd_t<64, true, 1, true>(tq, tk, tv, to, lse, s, drop, st)
                     : launch_fwd_t<64, false, 1, true>(tq, tk, tv, to, lse, s, drop, st);
   }
-  if (s.d == 128) {
+  if (kernel_dim(s.d) == 128) {
     const int n_qt = (s.N + 127) / 128;
     const int avg_steps = s.causal ? (n_qt + 1) / 2 : n_qt;
     if (avg_steps >= kTwoIssuerMinSteps)

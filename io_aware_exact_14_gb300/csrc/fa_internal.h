@@ -45,6 +45,12 @@ inline DropArgs make_drop_args(uint64_t seed, uint32_t offset, int t) {
 }
 inline DropArgs no_drop_args() { return make_drop_args(0, 0, 0); }
 
+// Head dims: any multiple of 8 from 8 to 128 runs in the kernel built for
+// D = 64 (d <= 64) or D = 128.  The tensor maps carry the true extent d, so
+// TMA loads fill columns d .. D-1 of every tile with zeros (they add nothing
+// to Q K^T, and P V gives zeros there) and TMA stores clip them.
+inline int kernel_dim(int d) { return d > 64 ? 128 : 64; }
+
 // Element strides of a [B, H, N, d] bf16 view (d contiguous).
 struct Strides {
   long long b, h, n;

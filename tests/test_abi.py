@@ -49,8 +49,11 @@ def fwd(lib, q=FAKE, k=FAKE + 0x100000, v=FAKE + 0x200000, o=FAKE + 0x300000, ls
 
 
 def test_fwd_argument_checks(lib):
-    assert fwd(lib, d=96) == 2            # FA_ERR_UNSUPPORTED
+    assert fwd(lib, d=100) == 2           # FA_ERR_UNSUPPORTED: not a multiple of 8
+    assert fwd(lib, d=136) == 2           # above 128
     assert fwd(lib, d=256) == 2
+    assert fwd(lib, d=4) == 2
+    assert fwd(lib, d=0) == 2
     assert fwd(lib, N=0, q=0, k=0, v=0, o=0, lse=0) == 0  # empty problem is a no-op
     assert fwd(lib, q=0) == 1             # FA_ERR_INVALID_ARG: null
     assert fwd(lib, lse=0) == 1
@@ -72,7 +75,8 @@ def test_bwd_argument_checks(lib):
     assert ws == 512  # 128 fp32 row terms, 256-byte rounded
     assert lib.fa_bwd_workspace_bytes(2, 3, 100, 128) == ((2 * 3 * 100 * 4 + 255) // 256) * 256
     assert lib.fa_bwd_workspace_bytes(1, 1, 0, 64) == 0
-    assert lib.fa_bwd_workspace_bytes(1, 1, 128, 96) == 0
+    assert lib.fa_bwd_workspace_bytes(1, 1, 128, 100) == 0
+    assert lib.fa_bwd_workspace_bytes(1, 1, 128, 96) == 512
 
     def bwd(**kw):
         a = dict(q=p[0], k=p[1], v=p[2], o=p[3], lse=p[4], do=p[5], dq=p[6], dk=p[7], dv=p[8],
@@ -81,7 +85,7 @@ def test_bwd_argument_checks(lib):
         return lib.fa_bwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["do"], a["dq"], a["dk"], a["dv"],
                           a["B"], a["H"], a["N"], a["d"], a["scale"], a["causal"], a["ws"], a["wsb"], None)
 
-    assert bwd(d=80) == 2
+    assert bwd(d=84) == 2
     assert bwd(N=0, q=0) == 0
     assert bwd(dq=0) == 1
     assert bwd(do=BAD_ALIGN) == 1
@@ -100,7 +104,7 @@ def test_noalloc_rejects_oversized_problem_without_a_device(lib):
     p = [FAKE + i * 0x100000 for i in range(9)]
     assert lib.fa_bwd_noalloc(*p, 1, 64, 32769, 64, 0.125, 0, None) == 4   # 2^21 + 64 rows
     assert b"exceeds the built-in scratch" in lib.fa_last_error_detail()
-    assert lib.fa_bwd_noalloc(*p, 1, 1, 128, 96, 0.125, 0, None) == 2
+    assert lib.fa_bwd_noalloc(*p, 1, 1, 128, 100, 0.125, 0, None) == 2
     assert lib.fa_bwd_noalloc(0, *p[1:], 1, 1, 128, 64, 0.125, 0, None) == 1
 
 
@@ -128,7 +132,7 @@ def test_dropout_argument_checks(lib):
     for p in (1.0, 1.5, -0.1, float("nan"), float("inf")):
         assert fwd_d(_Dropout(p, 1, 0)) == 1, p
     assert fwd_d(_Dropout(0.1, 1, 0), q=0) == 1
-    assert fwd_d(_Dropout(0.1, 1, 0), d=96) == 2
+    assert fwd_d(_Dropout(0.1, 1, 0), d=200) == 2
     assert fwd_d(_Dropout(0.1, 1, 0), o=FAKE) == 1
     p = [FAKE + i * 0x100000 for i in range(12)]
     ws = lib.fa_bwd_workspace_bytes(1, 1, 128, 64)

@@ -61,13 +61,16 @@ __device__ __forceinline__ size_t pre_row_offset(long long row, bool contig, int
   return static_cast<size_t>(b * st.b + h * st.h + n * st.n) * 2;
 }
 
-template <int D>
+template <int D, bool FULL>
 __global__ void __launch_bounds__(kPreThreads) fa_bwd_preprocess_kernel(const uint8_t* __restrict__ o,
                                                                        const uint8_t* __restrict__ dO,
                                                                        float* __restrict__ Dvec, long long rows,
                                                                        int H, int N, int d, Strides so,
                                                                        Strides sdo, bool contig) {
-  // D = 64 or 128 covers d <= D: chunks at or past d count as zero
+  // D = 64 or 128 covers d <= D: chunks at or past d count as zero.  FULL
+  // (d == D) keeps the row length a compile-time constant, and the loads
+  // unconditional, on the common path.
+  if (FULL) d = D;
   constexpr int kTpr = D / 8;                 // threads per row, one 16-byte chunk each
   constexpr int kRows = kPreThreads / kTpr;   // rows per block per step
   const int sub = threadIdx.x % kTpr;
@@ -78,11 +81,18 @@ __global__ void __launch_bounds__(kPreThreads) fa_bwd_preprocess_kernel(const ui
 #pragma unroll
     for (int u = 0; u < kPreUnroll; ++u) {
       const long long row = base + static_cast<long long>(u) * kRows;
-      a[u] = make_uint4(0u, 0u, 0u, 0u);
-      b[u] = a[u];
-      if (row < rows && sub * 8 < d) {
-        a[u] = ldg_stream(o + pre_row_offset(row, contig, d, H, N, so) + sub * 16);
-        b[u] = ldg_stream(dO + pre_row_offset(row, contig, d, H, N, sdo) + sub * 16);
+      if constexpr (FULL) {
+        if (row < rows) {
+          a[u] = ldg_stream(o + pre_row_offset(row, contig, D, H, N, so) + sub * 16);
+          b[u] = ldg_stream(dO + pre_row_offset(row, contig, D, H, N, sdo) + sub * 16);
+        }
+      } else {
+        a[u] = make_uint4(0u, 0u, 0u, 0u);
+        b[u] = a[u];
+        if (row < rows && sub * 8 < d) {
+          a[u] = ldg_stream(o + pre_row_offset(row, contig, d, H, N, so) + sub * 16);
+          b[u] = ldg_stream(dO + pre_row_offset(row, contig, d, H, N, sdo) + sub * 16);
+        }
       }
     }
 #pragma unroll
@@ -1302,12 +1312,18 @@ cudaError_t launch_bwd_preprocess(const void* o, const Strides& so, const void* 
   const int grid = static_cast<int>(want < 8LL * sms ? want : 8LL * sms);
   const Strides c = contiguous_strides(s);
   const bool contig = so.b == c.b && so.h == c.h && so.n == c.n && sdo.b == c.b && sdo.h == c.h && sdo.n == c.n;
-  if (kernel_dim(s.d) == 128)
-    fa_bwd_preprocess_kernel<128><<<grid, kPreThreads, 0, st>>>(
-        static_cast<const uint8_t*>(o), static_cast<const uint8_t*>(dO), Dvec, rows, s.H, s.N, s.d, so, sdo, contig);
+  const auto* po = static_cast<const uint8_t*>(o);
+  const auto* pdo = static_cast<const uint8_t*>(dO);
+  if (s.d == 128)
+    fa_bwd_preprocess_kernel<128, true><<<grid, kPreThreads, 0, st>>>(po, pdo, Dvec, rows, s.H, s.N, s.d, so, sdo, contig);
+  else if (s.d == 64)
+    fa_bwd_preprocess_kernel<64, true><<<grid, kPreThreads, 0, st>>>(po, pdo, Dvec, rows, s.H, s.N, s.d, so, sdo, contig);
+  else if (kernel_dim(s.d) == 128)
+    fa_bwd_preprocess_kernel<128, false><<<grid, kPreThreads, 0, st>>>(po, pdo, Dvec, rows, s.H, s.N, s.d, so, sdo,
+                                                                       contig);
   else
-    fa_bwd_preprocess_kernel<64><<<grid, kPreThreads, 0, st>>>(
-        static_cast<const uint8_t*>(o), static_cast<const uint8_t*>(dO), Dvec, rows, s.H, s.N, s.d, so, sdo, contig);
+    fa_bwd_preprocess_kernel<64, false><<<grid, kPreThreads, 0, st>>>(po, pdo, Dvec, rows, s.H, s.N, s.d, so, sdo,
+                                                                      contig);
   return cudaGetLastError();
 }
 

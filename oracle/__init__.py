@@ -22,3 +22,4 @@ from .attention_ref import (  # noqa: F401
     rel_fro_err,
     lse_max_abs_err,
 )
+from . import fp8_ref  # noqa: F401,E402  (e4m3 quantisation and the FP8 forward)

@@ -55,6 +55,9 @@ def parse():
     ap.add_argument("--batch", type=int, default=None, help="override B (smaller cases for profiler captures)")
     ap.add_argument("--dropout", type=float, default=0.0,
                     help="drop probability p: time fa_fwd_dropout + fa_bwd_dropout instead (fwd and bwd split only)")
+    ap.add_argument("--fp8", action="store_true",
+                    help="time the FP8 (e4m3) forward and its quantiser on the workload instead")
+    ap.add_argument("--fp8-rotate", type=int, default=1, help="incoherent rotation of Q and K (1) or not (0)")
     ap.add_argument("--splitkv", action="store_true",
                     help="time the split-KV forward on --splitkv-shape instead of the training step")
     ap.add_argument("--splitkv-shape", default="8,32,1,16384,128", help="B,H,Nq,Nk,d (non-causal)")
@@ -574,9 +577,89 @@ def run_splitkv(args, dist: Dist):
     dist.close()
 
 
+def run_fp8(args, dist: Dist):
+    """FP8 forward on the training workload's shape: Q, K (rotated) and V^T are
+    quantised once outside the timed region (the quantiser is timed on its own),
+    then K steps of fa_fwd_fp8.  Tensor-bound: forward FLOPs per second against
+    the measured bf16 peak x 2 (the nominal FP8 / BF16 dense ratio, 4.5 / 2.25)."""
+    import torch
+    from io_aware_exact_14_gb300 import fa
+
+    torch.cuda.set_device(dist.local)
+    dist.init("nccl")
+    dev = torch.device("cuda", dist.local)
+    w = WORKLOADS[args.workload]
+    if args.batch is not None:
+        import dataclasses
+        w = dataclasses.replace(w, B=args.batch, name=f"{w.name}@B={args.batch}")
+    causal = w.causal[-1]
+    B, H, N, d = w.shape
+    x = make_inputs(B, H, N, d, w.seed + 100 * dist.rank, w.qk_mult, with_grad=False)
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    rot = 0x5EED if args.fp8_rotate else None
+    stream = torch.cuda.current_stream(dev)
+
+    def quantise():
+        return (fa.fa_fp8_quantize(q, rotate_seed=rot), fa.fa_fp8_quantize(k, rotate_seed=rot),
+                fa.fa_fp8_quantize(v, transpose=True))
+    (q8, dq), (k8, dk), (vt8, dv) = quantise()
+    o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    call = lambda: fa.fa_fwd_fp8(q8, k8, vt8, dq, dk, dv, w.scale, causal, out=o, lse=lse)
+    clocks = ClockSampler(dist.local)
+    clocks.start()
+    for _ in range(args.warmup):
+        call()
+        quantise()
+    torch.cuda.synchronize()
+    dist.barrier()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    ev[0].record(stream)
+    for _ in range(args.steps):
+        call()
+    ev[1].record(stream)
+    for _ in range(args.steps):
+        quantise()
+    ev[2].record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    clk = clocks.stop()
+    if fa.fa_debug_status(reset=True) != fa.FA_OK:
+        raise RuntimeError(f"kernel pipeline timeout at site {fa.fa_debug_site():#x}")
+    ms = dist.max(ev[0].elapsed_time(ev[1])) / args.steps
+    q_ms = dist.max(ev[1].elapsed_time(ev[2])) / args.steps
+    flops = counts.attn_flops(B, H, N, d, causal, "fwd")
+    value = flops * dist.world / (ms * 1e-3) / 1e12
+    peaks, peak_src = load_peaks()
+    fp8_peak = 2.0 * float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    q_bytes = 3 * B * H * N * d * 2 + 3 * B * H * N * d + 2 * B * H * N * d * 2   # read x (twice: amax, codes), write codes
+    out = {
+        "metric": "attention fwd TFLOP/s, FP8 e4m3 operands (1xGB300)", "value": round(value, 2), "unit": "TFLOP/s",
+        "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate)",
+        "data": "synthetic (seeded N(0,1) bf16 q, k, v, quantised per head)",
+        "config": {"workload": w.name, "B": B, "H": H, "N": N, "d": d, "causal": causal, "scale": w.scale,
+                   "step": "fa_fwd_fp8", "rotation": bool(rot),
+                   "l2": "inputs larger than L2: q8, k8, vt8 are 67 MB each, O 134 MB"},
+        "roofline": {"kernel": "fa_fwd_fp8_kernel", "bound": "tensor", "achieved": round(value / dist.world, 1),
+                     "peak": fp8_peak, "unit": "TFLOP/s", "frac": round(value / dist.world / fp8_peak, 3),
+                     "peak_source": f"{peak_src} bf16 burst x 2 (nominal fp8/bf16 dense ratio)",
+                     "work_per_launch": flops, "traffic": None},
+        "quantize": {"ms_per_call_set": round(q_ms, 4), "calls": "q (rotated), k (rotated), v (transposed): 9 kernels",
+                     "GB/s": round(q_bytes / (q_ms * 1e-3) / 1e9, 1)},
+        "gpu_launches": args.steps * 10, "clocks": clk,
+    }
+    if dist.rank == 0:
+        print(json.dumps(out), flush=True)
+    dist.close()
+
+
 def main():
     args = parse()
     dist = Dist()
+    if args.fp8 and args.impl == "ours":
+        run_fp8(args, dist)
+        return
     if args.splitkv and args.impl == "ours":
         run_splitkv(args, dist)
         return

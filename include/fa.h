@@ -206,6 +206,50 @@ fa_status fa_bwd_dropout(const void* q, const void* k, const void* v, const void
                          void* workspace, size_t workspace_bytes, struct CUstream_st* stream);
 
 /*
+ * FP8 (e4m3) forward.  [WHY-FAST] "Flash Attention 3：拥抱Hopper架构" names FP8
+ * tensor cores and "incoherent processing" (a random orthogonal rotation of
+ * Q and K before quantisation); the format and rounding contract is this
+ * library's: OCP FP8 E4M3FN codes (1 byte, largest 448), conversions round
+ * to nearest even and saturate, one dequantisation factor (descale) per
+ * (batch, head).
+ *
+ * fa_fp8_quantize: codes of a contiguous bf16 [B, H, N, d] tensor x.  Per
+ * (b, h): amax = max |x| (after the optional rotation), each element becomes
+ * e4m3(x * (448 / amax)) (fp32 arithmetic), descale[b*H + h] = amax / 448
+ * (1 for an all-zero head).
+ *   transpose 0: out is e4m3 [B, H, N, d]; 1: out is e4m3 [B, H, d, ldv],
+ *                ldv = fa_fp8_vt_ld(N) (the layout fa_fwd_fp8 takes for V;
+ *                entries past N are written as 0)
+ *   rotate != 0: x is first multiplied along d by diag(sigma) H_d / sqrt(d)
+ *                (Sylvester-Hadamard; sigma_c = +-1 from bit c of
+ *                Philox4x32-10(counter 0, key = seed)); apply it to Q and to
+ *                K with the same seed (Q K^T is unchanged).  d must be 64 or
+ *                128 (FA_ERR_UNSUPPORTED otherwise).
+ * d must be a multiple of 16 in [16, 128] (FA_ERR_UNSUPPORTED).  descale is
+ * fp32 [B, H] device memory; x, out 16-byte aligned.  Three kernels on `stream`.
+ */
+fa_status fa_fp8_quantize(const void* x, void* out, float* descale, int B, int H, int N, int d,
+                          int transpose, int rotate, unsigned long long seed, struct CUstream_st* stream);
+
+/* Row pitch (elements = bytes) of the transposed V codes: N rounded up to 16. */
+size_t fa_fp8_vt_ld(int N);
+
+/*
+ * Forward on e4m3 codes: q8, k8 [B, H, N, d], vt8 [B, H, d, fa_fp8_vt_ld(N)]
+ * (V transposed, from fa_fp8_quantize with transpose = 1), descales fp32
+ * [B, H].  S = scale (descale_q Q)(descale_k K)^T in fp32; the unnormalised
+ * probabilities P~ = exp(S - m) are rounded to e4m3 before P~ V;
+ * O = (P~ V) descale_v / l (l the fp32 sum of the unrounded P~), bf16
+ * [B, H, N, d]; lse fp32 [B, H, N] of S.  Error contract (derived, not on
+ * the pages): against the exact attention of the dequantised inputs,
+ * |O - O_exact| <= sum_j max(2^-4 P~_ij, 2^-10) |V_jc| / l_i plus fp32
+ * and bf16 output rounding.  d a multiple of 16 in [16, 128].
+ */
+fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* descale_q,
+                     const float* descale_k, const float* descale_v, void* o, float* lse,
+                     int B, int H, int N, int d, float scale, int causal, struct CUstream_st* stream);
+
+/*
  * Backward step 1: D_i = sum_c dO_ic O_ic (fp32 [B, H, N]), the row term of
  * the softmax Jacobian (derived; not on the pages).  Memory-bound.
  */

@@ -217,6 +217,25 @@ fa_status make_map_f32(CUtensorMap* m, const void* base, int d, int Nq, long lon
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// FP8: sizes (d a multiple of 16 in [16, 128], the copy engine's 16-byte row
+// rule for 1-byte elements), the transposed-V row pitch, and 4-D maps of
+// e4m3 codes with 128 x 128 boxes.
+fa_status check_sizes_fp8(int B, int H, int N, int d) {
+  FA_TRY(check_sizes(B, H, N, d));
+  return d % 16 == 0 ? FA_OK : FA_ERR_UNSUPPORTED;
+}
+
+long long fp8_vt_ld(int N) { return (static_cast<long long>(N) + 15) / 16 * 16; }
+
+fa_status make_map_u8(CUtensorMap* m, const void* base, const cuuint64_t (&dims)[4], const cuuint64_t (&strides)[3]) {
+  const cuuint32_t box[4] = {128, 128, 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : fail("cuTensorMapEncodeTiled", static_cast<int>(r), "invalid tensor map");
+}
+
 // Split-KV workspace: fp32 partial O [n, B*H, Nq, D] (D = kernel_dim(d): the
 // kernel writes its padded columns, zeros), then fp32 partial LSE [n, B*H, Nq].
 struct SplitPlan {
@@ -489,6 +508,50 @@ fa_status fa_bwd_dropout(const void* q, const void* k, const void* v, const void
                   nullptr, B, H, N, d, scale, causal, workspace, workspace_bytes, stream, drop);
 }
 
+size_t fa_fp8_vt_ld(int N) { return N > 0 ? static_cast<size_t>(fp8_vt_ld(N)) : 0; }
+
+fa_status fa_fp8_quantize(const void* x, void* out, float* descale, int B, int H, int N, int d, int transpose,
+                          int rotate, unsigned long long seed, struct CUstream_st* stream) {
+  FA_TRY(check_sizes_fp8(B, H, N, d));
+  if (rotate && d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (N == 0) return FA_OK;
+  FA_TRY(check_ptrs({x, out}, {descale}));
+  const Shape s{B, H, N, d, 1.f, 0};
+  const size_t out_bytes = transpose ? static_cast<size_t>(B) * H * d * fp8_vt_ld(N) : tensor_bytes(s) / 2;
+  FA_TRY(check_disjoint({{out, out_bytes}, {descale, static_cast<size_t>(B) * H * 4}}, {{x, tensor_bytes(s)}}));
+  FA_TRY(check_disjoint({{out, out_bytes}}, {{descale, static_cast<size_t>(B) * H * 4}}));
+  return cuda_status(fa::launch_fp8_quantize(x, out, descale, s, transpose != 0, fp8_vt_ld(N), rotate != 0, seed,
+                                             stream),
+                     "FP8 quantise launch");
+}
+
+fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* descale_q,
+                     const float* descale_k, const float* descale_v, void* o, float* lse, int B, int H, int N, int d,
+                     float scale, int causal, struct CUstream_st* stream) {
+  FA_TRY(check_sizes_fp8(B, H, N, d));
+  if (N == 0) return FA_OK;
+  FA_TRY(check_ptrs({q8, k8, vt8, o}, {descale_q, descale_k, descale_v, lse}));
+  FA_TRY(check_scale(scale));
+  const Shape s{B, H, N, d, scale, causal ? 1 : 0};
+  const size_t qk_bytes = tensor_bytes(s) / 2, vt_bytes = static_cast<size_t>(B) * H * d * fp8_vt_ld(N);
+  const size_t ds_bytes = static_cast<size_t>(B) * H * 4;
+  FA_TRY(check_disjoint({{o, tensor_bytes(s)}, {lse, vec_bytes(s)}},
+                        {{q8, qk_bytes}, {k8, qk_bytes}, {vt8, vt_bytes}, {descale_q, ds_bytes},
+                         {descale_k, ds_bytes}, {descale_v, ds_bytes}}));
+  FA_TRY(check_disjoint({{o, tensor_bytes(s)}}, {{lse, vec_bytes(s)}}));
+  if (!load_encoder()) return FA_ERR_CUDA;
+  const cuuint64_t dB = B, dH = H, dN = N, dd = d, ld = static_cast<cuuint64_t>(fp8_vt_ld(N));
+  CUtensorMap tq, tk, tvt, to;
+  const cuuint64_t qk_dims[4] = {dd, dN, dH, dB}, qk_str[3] = {dd, dN * dd, dH * dN * dd};
+  const cuuint64_t vt_dims[4] = {dN, dd, dH, dB}, vt_str[3] = {ld, dd * ld, dH * dd * ld};
+  FA_TRY(make_map_u8(&tq, q8, qk_dims, qk_str));
+  FA_TRY(make_map_u8(&tk, k8, qk_dims, qk_str));
+  FA_TRY(make_map_u8(&tvt, vt8, vt_dims, vt_str));
+  FA_TRY(make_map(&to, o, s));
+  return cuda_status(fa::launch_fwd_fp8(tq, tk, tvt, to, descale_q, descale_k, descale_v, lse, s, stream),
+                     "FP8 forward launch");
+}
+
 fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
                          const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
                          int causal, struct CUstream_st* stream) {
@@ -530,8 +593,11 @@ fa_status fa_debug_status(int reset) {
   if (e != cudaSuccess) return fail("reading the forward status word", e, cudaGetErrorString(e));
   e = fa::bwd_status(&b, reset != 0);
   if (e != cudaSuccess) return fail("reading the backward status word", e, cudaGetErrorString(e));
-  g_last_site = a ? a : b;
-  return (a | b) ? FA_ERR_TIMEOUT : FA_OK;
+  uint32_t c = 0;
+  e = fa::fp8_status(&c, reset != 0);
+  if (e != cudaSuccess) return fail("reading the FP8 status word", e, cudaGetErrorString(e));
+  g_last_site = a ? a : (b ? b : c);
+  return (a | b | c) ? FA_ERR_TIMEOUT : FA_OK;
 }
 
 unsigned int fa_debug_site(void) { return g_last_site; }

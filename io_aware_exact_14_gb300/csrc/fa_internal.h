@@ -131,6 +131,18 @@ cudaError_t launch_bwd_dq(const CUtensorMap& tq, const CUtensorMap& tk, const CU
                           const CUtensorMap& tdo, const CUtensorMap& tdq, const float* lse,
                           const float* Dvec, const Shape& s, const DropArgs& drop, cudaStream_t st);
 
+// FP8 (e4m3): per-(b, h) quantisation of a contiguous bf16 [B, H, N, d] tensor
+// into codes [B, H, N, d] (or, transposed, [B, H, d, ldv]) with descale[b*H + h]
+// = amax / 448, optionally rotated along d by the random-sign Hadamard
+// transform of `seed` (d = 64 or 128); and the forward on such codes (Q, K
+// [B, H, N, d], V transposed [B, H, d, ldv]; maps of 1-byte elements with
+// 128 x 128 boxes), writing bf16 O and fp32 LSE.
+cudaError_t launch_fp8_quantize(const void* x, void* out, float* descale, const Shape& s, bool transpose,
+                                long long ldv, bool rotate, uint64_t seed, cudaStream_t st);
+cudaError_t launch_fwd_fp8(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,
+                           const CUtensorMap& to, const float* dq, const float* dk, const float* dv, float* lse,
+                           const Shape& s, cudaStream_t st);
+
 // Fixed device scratch for callers that cannot allocate: room for the fp32
 // row term of up to kNoAllocRows rows (B*H*N), in a file-scope device array of
 // fa_bwd.cu.  Returns its device address for the current device, looking it up
@@ -150,5 +162,6 @@ inline int head_band(int N, int d) {
 // Synchronous: copies from the device.
 cudaError_t fwd_status(uint32_t* out, bool reset);
 cudaError_t bwd_status(uint32_t* out, bool reset);
+cudaError_t fp8_status(uint32_t* out, bool reset);
 
 }  // namespace fa

@@ -40,6 +40,9 @@ SIGNATURES = {
     "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
     "fa_fwd_dropout": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P]),
     "fa_bwd_dropout": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P, _SZ, _P]),
+    "fa_fp8_quantize": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_ulonglong, _P]),
+    "fa_fp8_vt_ld": (_SZ, [_I]),
+    "fa_fwd_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
     "fa_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
     "fa_bwd_preprocess": (_I, [_P, _P, _P, _I, _I, _I, _I, _P]),
     "fa_bwd_dkdv": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
@@ -329,6 +332,56 @@ def fa_bwd_dropout(q, k, v, o, lse, do, p: float, seed: int, offset: int = 0, sc
                                workspace.numel() * workspace.element_size(), _stream_ptr(stream))
     _check("fa_bwd_dropout", st)
     return dq, dk, dv
+
+
+def fa_fp8_vt_ld(N: int) -> int:
+    return int(load().fa_fp8_vt_ld(N))
+
+
+def fa_fp8_quantize(x, transpose: bool = False, rotate_seed: Optional[int] = None, out=None, descale=None,
+                    stream=None):
+    """e4m3 codes (uint8) of a contiguous bf16 [B, H, N, d] tensor, per-(b, h) descale
+    (fp32 [B, H]); transpose=True gives [B, H, d, fa_fp8_vt_ld(N)] (the V layout of
+    fa_fwd_fp8); rotate_seed applies the random-sign Hadamard rotation first."""
+    B, H, N, d = _bhnd(x, "x")
+    shape = (B, H, d, fa_fp8_vt_ld(N)) if transpose else (B, H, N, d)
+    out = torch.empty(shape, dtype=torch.uint8, device=x.device) if out is None else out
+    if tuple(out.shape) != shape or out.dtype != torch.uint8 or not out.is_contiguous() or not out.is_cuda:
+        raise ValueError(f"out must be a contiguous uint8 CUDA tensor of shape {shape}")
+    descale = torch.empty((B, H), dtype=torch.float32, device=x.device) if descale is None else descale
+    if tuple(descale.shape) != (B, H) or descale.dtype != torch.float32 or not descale.is_contiguous():
+        raise ValueError("descale must be a contiguous fp32 [B, H] tensor")
+    rotate = rotate_seed is not None
+    st = load().fa_fp8_quantize(x.data_ptr(), out.data_ptr(), descale.data_ptr(), B, H, N, d, int(transpose),
+                                int(rotate), int(rotate_seed or 0), _stream_ptr(stream))
+    _check("fa_fp8_quantize", st)
+    return out, descale
+
+
+def fa_fwd_fp8(q8, k8, vt8, descale_q, descale_k, descale_v, scale: Optional[float] = None, causal: bool = False,
+               out=None, lse=None, stream=None):
+    """Forward on e4m3 codes (uint8): q8, k8 [B, H, N, d], vt8 [B, H, d, fa_fp8_vt_ld(N)],
+    descales fp32 [B, H]; returns bf16 O [B, H, N, d] and fp32 LSE [B, H, N]."""
+    for t, n in ((q8, "q8"), (k8, "k8"), (vt8, "vt8")):
+        if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.uint8 and t.is_contiguous()
+                and t.dim() == 4):
+            raise ValueError(f"{n} must be a contiguous 4-D uint8 CUDA tensor")
+    B, H, N, d = q8.shape
+    if tuple(k8.shape) != (B, H, N, d) or tuple(vt8.shape) != (B, H, d, fa_fp8_vt_ld(N)):
+        raise ValueError("k8 must match q8 and vt8 must be [B, H, d, fa_fp8_vt_ld(N)]")
+    for t, n in ((descale_q, "descale_q"), (descale_k, "descale_k"), (descale_v, "descale_v")):
+        if not (t.is_cuda and t.dtype == torch.float32 and t.is_contiguous() and tuple(t.shape) == (B, H)):
+            raise ValueError(f"{n} must be a contiguous fp32 CUDA tensor [B, H]")
+    scale = default_scale(d) if scale is None else float(scale)
+    out = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device) if out is None else out
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device) if lse is None else lse
+    _same((B, H, N, d), out, "out")
+    _vec(lse, (B, H, N, d), "lse")
+    st = load().fa_fwd_fp8(q8.data_ptr(), k8.data_ptr(), vt8.data_ptr(), descale_q.data_ptr(), descale_k.data_ptr(),
+                           descale_v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, N, d, scale,
+                           int(bool(causal)), _stream_ptr(stream))
+    _check("fa_fwd_fp8", st)
+    return out, lse
 
 
 def fa_bwd_noalloc(q, k, v, o, lse, do, scale: Optional[float] = None, causal: bool = False,

@@ -143,3 +143,18 @@ def test_dropout_argument_checks(lib):
     assert lib.fa_bwd_dropout(*p[:9], 1, 1, 128, 64, 0.125, 1, ctypes.addressof(drop), 0, ws, None) == 4
     assert lib.fa_bwd_dropout(*p[:6], p[0], *p[7:9], 1, 1, 128, 64, 0.125, 1, ctypes.addressof(drop), p[9], ws,
                               None) == 1
+
+
+def test_fp8_argument_checks(lib):
+    x, out, ds = FAKE, FAKE + 0x100000, FAKE + 0x200000
+    assert lib.fa_fp8_quantize(x, out, ds, 1, 1, 128, 40, 0, 0, 0, None) == 2    # d not a multiple of 16
+    assert lib.fa_fp8_quantize(x, out, ds, 1, 1, 128, 96, 0, 1, 5, None) == 2    # rotation needs d = 64 or 128
+    assert lib.fa_fp8_quantize(0, out, ds, 1, 1, 128, 64, 0, 0, 0, None) == 1
+    assert lib.fa_fp8_quantize(x, x, ds, 1, 1, 128, 64, 0, 0, 0, None) == 1     # out aliases x
+    assert lib.fa_fp8_quantize(x, out, ds, 1, 1, 0, 64, 0, 0, 0, None) == 0      # empty
+    assert lib.fa_fp8_vt_ld(1) == 16 and lib.fa_fp8_vt_ld(32) == 32 and lib.fa_fp8_vt_ld(33) == 48
+    p = [FAKE + i * 0x100000 for i in range(8)]
+    assert lib.fa_fwd_fp8(*p, 1, 1, 128, 40, 0.1, 0, None) == 2
+    assert lib.fa_fwd_fp8(*p, 1, 1, 128, 64, 0.0, 0, None) == 1
+    assert lib.fa_fwd_fp8(*p[:6], p[0], p[7], 1, 1, 128, 64, 0.1, 0, None) == 1   # o aliases q8
+    assert lib.fa_fwd_fp8(0, *p[1:], 1, 1, 128, 64, 0.1, 0, None) == 1

@@ -350,16 +350,44 @@ def run_ours(args, dist: Dist):
         print(json.dumps(out), flush=True)
 
 
+def gpu_local_cpus(index: int):
+    """CPUs of the NUMA node that sysfs reports nearest to CUDA device `index`
+    (None when it cannot tell): pinned host buffers allocated by a thread
+    running there land in that node's memory, next to the GPU's host link."""
+    import torch
+    try:
+        pr = torch.cuda.get_device_properties(index)
+        bdf = f"{pr.pci_domain_id:04x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0"
+        with open(f"/sys/bus/pci/devices/{bdf}/numa_node") as f:
+            node = int(f.read())
+        if node < 0:
+            return None
+        with open(f"/sys/devices/system/node/node{node}/cpulist") as f:
+            spec = f.read().strip()
+        cpus = set()
+        for part in spec.split(","):
+            a, _, b = part.partition("-")
+            cpus.update(range(int(a), int(b or a) + 1))
+        return cpus or None
+    except Exception:
+        return None
+
+
 def run_e2e(args, w, causal, x, dev, dist, flops_step):
     """Same step through the public API with host buffers, as a training loop
     would run it: every step copies q, k, v, dO from pinned host memory to the
     device and O, LSE, dQ, dK, dV back, all inside the timed region.  The loop
-    is pipelined over two device buffer sets and three streams (copy in,
-    compute, copy out, ordered by events), so step s+1's inputs travel while
-    step s computes and step s-1's results travel back."""
+    is pipelined over two device buffer sets (step s+1's inputs travel while
+    step s computes and step s-1's results travel back); each tensor copies on
+    its own stream, so both directions use several copy engines, and the
+    pinned buffers are allocated from the GPU's own NUMA node."""
     import torch
     from io_aware_exact_14_gb300 import fa
     B, H, N, d = w.shape
+    saved_affinity = os.sched_getaffinity(0) if hasattr(os, "sched_getaffinity") else None
+    local = gpu_local_cpus(dev.index if dev.index is not None else 0)
+    if local and saved_affinity is not None:
+        os.sched_setaffinity(0, local & saved_affinity or local)
     h_in = [x[n].pin_memory() for n in ("q", "k", "v", "do")]
     h_out = [torch.empty((B, H, N, d), dtype=torch.bfloat16).pin_memory() for _ in range(4)]
     h_lse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
@@ -368,37 +396,42 @@ def run_e2e(args, w, causal, x, dev, dist, flops_step):
     d_in = [[torch.empty_like(t, device=dev) for t in h_in] for _ in range(2)]
     d_out = [[torch.empty_like(d_in[0][0]) for _ in range(4)] for _ in range(2)]
     d_lse = [torch.empty((B, H, N), dtype=torch.float32, device=dev) for _ in range(2)]
-    s_in, s_comp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    s_in = [torch.cuda.Stream(dev) for _ in range(4)]
+    s_out = [torch.cuda.Stream(dev) for _ in range(4)]
+    s_comp = torch.cuda.Stream(dev)
     ev = lambda: torch.cuda.Event()
-    in_done = [ev(), ev()]
+    in_done = [[ev() for _ in range(4)] for _ in range(2)]
     comp_done = [ev(), ev()]
-    out_done = [ev(), ev()]
+    out_done = [[ev() for _ in range(4)] for _ in range(2)]
     started = [False, False]
 
     def step(i):
         b = i % 2
-        with torch.cuda.stream(s_in):
-            if started[b]:
-                s_in.wait_event(comp_done[b])      # step i-2 has finished reading these inputs
-            for hd, dd in zip(h_in, d_in[b]):
+        for t, (hd, dd) in enumerate(zip(h_in, d_in[b])):
+            with torch.cuda.stream(s_in[t]):
+                if started[b]:
+                    s_in[t].wait_event(comp_done[b])      # step i-2 has finished reading these inputs
                 dd.copy_(hd, non_blocking=True)
-            in_done[b].record(s_in)
+                in_done[b][t].record(s_in[t])
         with torch.cuda.stream(s_comp):
-            s_comp.wait_event(in_done[b])
+            for e in in_done[b]:
+                s_comp.wait_event(e)
             if started[b]:
-                s_comp.wait_event(out_done[b])     # step i-2's results have left these outputs
+                for e in out_done[b]:
+                    s_comp.wait_event(e)               # step i-2's results have left these outputs
             q, k, v, do = d_in[b]
             o, dq, dk, dv = d_out[b]
             fa.fa_fwd(q, k, v, w.scale, causal, out=o, lse=d_lse[b], stream=s_comp)
             fa.fa_bwd(q, k, v, o, d_lse[b], do, w.scale, causal, dq=dq, dk=dk, dv=dv, workspace=ws,
                       stream=s_comp)
             comp_done[b].record(s_comp)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(comp_done[b])
-            for hd, dd in zip(h_out, d_out[b]):
+        for t, (hd, dd) in enumerate(zip(h_out, d_out[b])):
+            with torch.cuda.stream(s_out[t]):
+                s_out[t].wait_event(comp_done[b])
                 hd.copy_(dd, non_blocking=True)
-            h_lse.copy_(d_lse[b], non_blocking=True)
-            out_done[b].record(s_out)
+                if t == 3:
+                    h_lse.copy_(d_lse[b], non_blocking=True)
+                out_done[b][t].record(s_out[t])
         started[b] = True
 
     steps = max(2, min(args.steps, 10))
@@ -407,20 +440,26 @@ def run_e2e(args, w, causal, x, dev, dist, flops_step):
     torch.cuda.synchronize()
     dist.barrier()
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.record(s_in)
+    s.record(s_in[0])
+    for t in range(1, 4):
+        s_in[t].wait_event(s)
     for i in range(steps):
         step(i)
     # the timed region ends when the last results are on the host
-    s_out.wait_stream(s_in)
-    s_out.wait_stream(s_comp)
-    e.record(s_out)
+    for st in s_in[1:] + s_out + [s_comp]:
+        s_in[0].wait_stream(st)
+    e.record(s_in[0])
     torch.cuda.synchronize()
     ms = dist.max(s.elapsed_time(e))
+    if local and saved_affinity is not None:
+        os.sched_setaffinity(0, saved_affinity)
     h2d = sum(t.numel() * t.element_size() for t in h_in)
     d2h = sum(t.numel() * t.element_size() for t in h_out) + h_lse.numel() * 4
     return {"value": round(flops_step * dist.world * steps / (ms * 1e-3) / 1e12, 2), "unit": UNIT,
             "steps": steps, "ms_per_step": round(ms / steps, 4), "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "pipelined": "2 buffer sets, copy-in / compute / copy-out streams"}
+            "d2h_bytes_per_step": d2h,
+            "pipelined": "2 buffer sets; one copy stream per tensor each way, a compute stream",
+            "host_numa_local": bool(local)}
 
 
 # ---------------------------------------------------------------------------

@@ -70,7 +70,6 @@ __global__ void __launch_bounds__(kPreThreads) fa_bwd_preprocess_kernel(const ui
   // D = 64 or 128 covers d <= D: chunks at or past d count as zero.  FULL
   // (d == D) keeps the row length a compile-time constant, and the loads
   // unconditional, on the common path.
-  if (FULL) d = D;
   constexpr int kTpr = D / 8;                 // threads per row, one 16-byte chunk each
   constexpr int kRows = kPreThreads / kTpr;   // rows per block per step
   const int sub = threadIdx.x % kTpr;

@@ -33,7 +33,7 @@ def _onehot_v(B, H, N, d, kb):
     return v
 
 
-@pytest.mark.parametrize("p", [0.1, 0.5, 0.9])
+@pytest.mark.parametrize("p", [0.1, 0.5, 0.9, 0.999])
 def test_forward_mask_bit_exact(p):
     """Q = K = 0 makes P uniform (1/N), so with one-hot V each output element is
     keep * scale / N: nonzero exactly where the mask keeps."""

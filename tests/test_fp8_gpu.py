@@ -138,3 +138,37 @@ def test_incoherent_rotation_helps_with_outlier_channels():
         errs[rot] = oracle.rel_fro_err(f64(o), ref_o)
     assert errs[4321] < errs[None], errs
     assert errs[4321] <= 0.1, errs
+
+
+@pytest.mark.parametrize("N,causal", [(1, False), (1, True), (130, True)])
+def test_fp8_short_and_ragged_rows(N, causal):
+    B, H, d = 2, 2, 64
+    _, _, args = _quantized(B, H, N, d, seed=850 + N)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = fa.fa_fwd_fp8(*args, scale, causal)
+    torch.cuda.synchronize()
+    assert_no_timeout()
+    O, LSE, _, bound = _oracle(args, N, scale, causal)
+    assert np.max(np.abs(f64(o) - O) - (1.1 * bound + 2.0 ** -8 * np.abs(O) + 1e-3)) <= 0
+    assert np.max(np.abs(f64(lse) - LSE)) <= TOL_LSE
+
+
+def test_fp8_all_zero_head():
+    """An all-zero Q head quantises to zero codes with descale 1; its scores
+    are all 0, so its output is the mean of the (dequantised) values."""
+    B, H, N, d = 1, 2, 200, 128
+    x, g = device_inputs(B, H, N, d, seed=860)
+    q = g["q"].clone()
+    q[:, 1] = 0
+    q8, dq = fa.fa_fp8_quantize(q)
+    k8, dk = fa.fa_fp8_quantize(g["k"])
+    vt8, dv = fa.fa_fp8_quantize(g["v"], transpose=True)
+    torch.cuda.synchronize()
+    assert dq[0, 1].item() == 1.0 and int(q8[:, 1].to(torch.int32).sum()) == 0
+    o, lse = fa.fa_fwd_fp8(q8, k8, vt8, dq, dk, dv, None, False)
+    torch.cuda.synchronize()
+    vt = _codes_np(vt8)[..., :N]
+    V = np.swapaxes(fp8_ref.fp8_dequantize(vt, dv.cpu().numpy()), -1, -2)
+    mean = V[0, 1].mean(axis=0)
+    assert np.max(np.abs(f64(o[0, 1]) - mean[None, :]) - 2.0 ** -8 * np.abs(mean[None, :])) <= 1e-4
+    assert np.allclose(f64(lse[0, 1]), math.log(N), atol=1e-4)

@@ -49,7 +49,6 @@ struct Fp8Cfg {
   // Q_t at 2t tiles, a second 16 KB right after it: the epilogue stages the
   // 128 x 128 bf16 O of tile t (two 64-column boxes, 32 KB) across both
   __host__ __device__ static constexpr uint32_t q_off(int t) { return 2u * t * kTileBytes; }
-  __host__ __device__ static constexpr uint32_t p_off(int t) { return (2u * t + 1u) * kTileBytes; }
   static constexpr uint32_t kSlotOff = 4 * kTileBytes;
   static constexpr uint32_t kBarOff = kSlotOff + kSlots * kTileBytes;
   // gfull[G], release[G], q_full, s_full[2], p_full[2], o_done[2], drain, staged[2]

@@ -99,6 +99,20 @@ def test_fp8_forward_within_rounding_bound(B, H, N, d, causal, qk):
     assert np.max(np.abs(f64(lse) - LSE)) <= TOL_LSE
 
 
+@pytest.mark.parametrize("B,H,N,causal", [(1, 2, 4096, False), (1, 1, 6400, True)])
+def test_fp8_long_rows(B, H, N, causal):
+    """Rows of 25-50 key steps per CTA: the ring and barrier phases wrap many times."""
+    d = 128
+    _, _, args = _quantized(B, H, N, d, seed=870 + N)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = fa.fa_fwd_fp8(*args, scale, causal)
+    torch.cuda.synchronize()
+    assert_no_timeout()
+    O, LSE, _, bound = _oracle(args, N, scale, causal)
+    assert np.max(np.abs(f64(o) - O) - (1.1 * bound + 2.0 ** -8 * np.abs(O) + 1e-3)) <= 0
+    assert np.max(np.abs(f64(lse) - LSE)) <= TOL_LSE
+
+
 def test_fp8_full_size_sampled():
     """B=8 H=16 N=4096 d=128 causal: sampled heads within the bound."""
     B, H, N, d = 8, 16, 4096, 128

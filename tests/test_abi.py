@@ -158,3 +158,47 @@ def test_fp8_argument_checks(lib):
     assert lib.fa_fwd_fp8(*p, 1, 1, 128, 64, 0.0, 0, None) == 1
     assert lib.fa_fwd_fp8(*p[:6], p[0], p[7], 1, 1, 128, 64, 0.1, 0, None) == 1   # o aliases q8
     assert lib.fa_fwd_fp8(0, *p[1:], 1, 1, 128, 64, 0.1, 0, None) == 1
+
+
+def _prototypes():
+    """name -> parameter count of every function prototype in include/fa.h."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER, encoding="utf-8").read(), flags=re.S)
+    protos = {}
+    for m in re.finditer(r"\b(fa_[a-z_0-9]+)\s*\(([^;{]*?)\)\s*;", text, flags=re.S):
+        params = m.group(2).strip()
+        protos[m.group(1)] = 0 if params in ("", "void") else len(params.split(","))
+    return protos
+
+
+def test_binding_signatures_match_header_prototypes():
+    """Every ctypes signature passes exactly as many arguments as the C
+    prototype takes (a mismatch would hand the library garbage)."""
+    from io_aware_exact_14_gb300 import fa
+    protos = _prototypes()
+    assert set(protos) == set(declared_functions())
+    for name, n in protos.items():
+        assert name in fa.SIGNATURES, name
+        assert len(fa.SIGNATURES[name][1]) == n, (name, len(fa.SIGNATURES[name][1]), n)
+
+
+def _splitkv_ws(B, H, Nq, Nk, d, splits):
+    n_kt = (Nk + 127) // 128
+    w = min(splits, n_kt)
+    per = -(-n_kt // w)
+    n_used = -(-n_kt // per)
+    rows = B * H * Nq * n_used
+    kd = 64 if d <= 64 else 128
+    r256 = lambda x: (x + 255) // 256 * 256
+    return r256(rows * kd * 4) + r256(rows * 4)
+
+
+def test_splitkv_workspace_sizes(lib):
+    """With an explicit chunk count no device is consulted: the size is the
+    fp32 partial outputs (padded to the kernel's head width) plus the partial
+    LSE of the chunks actually used, each rounded to 256 bytes."""
+    for args in [(1, 1, 1, 1000, 128, 3), (2, 3, 5, 4097, 64, 7), (1, 2, 16, 129, 96, 4),
+                 (1, 1, 1, 128, 40, 8), (2, 1, 33, 70000, 128, 300)]:
+        assert lib.fa_fwd_splitkv_workspace_bytes(*args) == _splitkv_ws(*args), args
+    assert lib.fa_fwd_splitkv_workspace_bytes(1, 1, 1, 0, 128, 4) == 0     # no keys
+    assert lib.fa_fwd_splitkv_workspace_bytes(1, 1, 0, 100, 128, 4) == 0   # no queries
+    assert lib.fa_fwd_splitkv_workspace_bytes(1, 1, 1, 100, 100, 4) == 0   # d not a multiple of 8

@@ -671,7 +671,7 @@ def run_fp8(args, dist: Dist):
     value = flops * dist.world / (ms * 1e-3) / 1e12
     peaks, peak_src = load_peaks()
     fp8_peak = 2.0 * float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    q_bytes = 3 * B * H * N * d * 2 + 3 * B * H * N * d + 2 * B * H * N * d * 2   # read x (twice: amax, codes), write codes
+    q_bytes = 2 * 3 * B * H * N * d * 2 + 3 * B * H * N * d   # q, k, v read twice (amax, codes), codes written
     out = {
         "metric": "attention fwd TFLOP/s, FP8 e4m3 operands (1xGB300)", "value": round(value, 2), "unit": "TFLOP/s",
         "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),

@@ -343,8 +343,9 @@ def run_ours(args, dist: Dist):
     }
     if e2e is not None:
         out["e2e"] = e2e
-    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline and p_drop == 0:
-        out["cpu_baseline"] = cpu_baseline(w, causal, args.cpu_seconds)
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = (cpu_baseline_dropout(w, causal, p_drop, args.cpu_seconds) if p_drop > 0
+                               else cpu_baseline(w, causal, args.cpu_seconds))
     dist.close()
     if dist.rank == 0:
         print(json.dumps(out), flush=True)
@@ -506,6 +507,51 @@ def cpu_baseline(w, causal, budget_s):
             "kind": "oracle",
             "sample": f"{done} (batch, head) slices of the workload (N={w.N}, d={w.d}, causal={causal}), "
                       f"forward + backward in fp64 NumPy, {dt:.1f} s"}
+
+
+def cpu_baseline_dropout(w, causal, p, budget_s):
+    """The oracle's dropout forward + backward on (b, h) slices, timed on the
+    host cores (same FLOP convention as the GPU line)."""
+    import oracle
+    from io_aware_exact_14_gb300.workloads import to_f64
+    x = make_inputs(1, min(w.H, 4), w.N, w.d, w.seed, w.qk_mult, with_grad=True)
+    done, t0 = 0, time.time()
+    while True:
+        h = done % x["q"].shape[1]
+        sl = [to_f64(x[n][0:1, h:h + 1]) for n in ("q", "k", "v", "do")]
+        oracle.attn_fwd_dropout_ref(sl[0], sl[1], sl[2], w.scale, causal, p, 0x5EED, 0, head0=h)
+        oracle.attn_bwd_dropout_ref(sl[0], sl[1], sl[2], sl[3], w.scale, causal, p, 0x5EED, 0, head0=h)
+        done += 1
+        if time.time() - t0 >= budget_s:
+            break
+    dt = time.time() - t0
+    return {"value": round(slice_flops(w, causal) * done / dt / 1e12, 6), "unit": UNIT, "cores": blas_threads(),
+            "kind": "oracle",
+            "sample": f"{done} (batch, head) slices (N={w.N}, d={w.d}, causal={causal}, p={p}), dropout "
+                      f"forward + backward in fp64 NumPy, {dt:.1f} s"}
+
+
+def cpu_baseline_fp8(w, causal, rotate, budget_s):
+    """The oracle's e4m3 quantisation and FP8 forward on (b, h) slices, timed on
+    the host cores (forward FLOPs per second, as the GPU line)."""
+    from oracle import fp8_ref
+    x = make_inputs(1, min(w.H, 4), w.N, w.d, w.seed, w.qk_mult, with_grad=False)
+    done, t0 = 0, time.time()
+    while True:
+        h = done % x["q"].shape[1]
+        sl = [x[n][0:1, h:h + 1].float().numpy() for n in ("q", "k", "v")]
+        q8, dq = fp8_ref.fp8_quantize_ref(sl[0], rotate)
+        k8, dk = fp8_ref.fp8_quantize_ref(sl[1], rotate)
+        vt8, dv = fp8_ref.fp8_quantize_ref(sl[2], None, True)
+        fp8_ref.attn_fwd_fp8_ref(q8, k8, vt8, dq, dk, dv, w.scale, causal)
+        done += 1
+        if time.time() - t0 >= budget_s:
+            break
+    dt = time.time() - t0
+    return {"value": round(counts.attn_flops(1, 1, w.N, w.d, causal, "fwd") * done / dt / 1e12, 6),
+            "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"{done} (batch, head) slices (N={w.N}, d={w.d}, causal={causal}), quantisation + FP8 "
+                      f"forward in NumPy (fp32 quantiser steps, fp64 attention), {dt:.1f} s"}
 
 
 def run_reference(args, dist: Dist):
@@ -688,6 +734,8 @@ def run_fp8(args, dist: Dist):
                      "GB/s": round(q_bytes / (q_ms * 1e-3) / 1e9, 1)},
         "gpu_launches": args.steps * 10, "clocks": clk,
     }
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline_fp8(w, causal, rot, args.cpu_seconds)
     if dist.rank == 0:
         print(json.dumps(out), flush=True)
     dist.close()

@@ -226,7 +226,8 @@ fa_status fa_bwd_dropout(const void* q, const void* k, const void* v, const void
  *                K with the same seed (Q K^T is unchanged).  d must be 64 or
  *                128 (FA_ERR_UNSUPPORTED otherwise).
  * d must be a multiple of 16 in [16, 128] (FA_ERR_UNSUPPORTED).  descale is
- * fp32 [B, H] device memory; x, out 16-byte aligned.  Three kernels on `stream`.
+ * fp32 [B, H] device memory; x, out 16-byte aligned.  A memset and three
+ * kernels on `stream`.
  */
 fa_status fa_fp8_quantize(const void* x, void* out, float* descale, int B, int H, int N, int d,
                           int transpose, int rotate, unsigned long long seed, struct CUstream_st* stream);
@@ -243,7 +244,8 @@ size_t fa_fp8_vt_ld(int N);
  * [B, H, N, d]; lse fp32 [B, H, N] of S.  Error contract (derived, not on
  * the pages): against the exact attention of the dequantised inputs,
  * |O - O_exact| <= sum_j max(2^-4 P~_ij, 2^-10) |V_jc| / l_i plus fp32
- * and bf16 output rounding.  d a multiple of 16 in [16, 128].
+ * and bf16 output rounding.  d a multiple of 16 in [16, 128]; causal as in
+ * fa_fwd; other errors as fa_fwd.
  */
 fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* descale_q,
                      const float* descale_k, const float* descale_v, void* o, float* lse,

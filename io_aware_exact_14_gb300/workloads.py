@@ -55,10 +55,9 @@ class Workload:
 
 WORKLOADS: Dict[int, Workload] = {
     1: Workload(1, "single_head_fwd_B1_H1_N128_d64", 1, 1, 128, 64, (False,), ("fwd",)),
-    2: Workload(2, "fwd_bwd_B4_H16_N2048_d128", 4, 16, 2048, 128, (False, True), ("fwd", "bwd"),
-                oracle_slices=4),
+    2: Workload(2, "fwd_bwd_B4_H16_N2048_d128", 4, 16, 2048, 128, (False, True), ("fwd", "bwd")),
     3: Workload(3, "peaky_fwd_B2_H8_N4096_d64_qk_x3", 2, 8, 4096, 64, (False,), ("fwd",),
-                qk_mult=3.0, oracle_slices=4),
+                qk_mult=3.0),
     4: Workload(4, "long_causal_fwd_B1_H32_N16384_d128", 1, 32, 16384, 128, (True,), ("fwd",),
                 oracle_rows=256),
     5: Workload(5, "train_causal_fwd_bwd_B8_H16_N4096_d128", 8, 16, 4096, 128, (True,),
@@ -118,6 +117,16 @@ def sample_rows(w: Workload, count: int) -> np.ndarray:
                 r.append(r[-1])
             rows[b, h] = np.asarray(r[:count])
     return rows
+
+
+def all_slices(w: Workload) -> list:
+    """Every (b, h) slice of the workload, in order."""
+    return [(b, h) for b in range(w.B) for h in range(w.H)]
+
+
+def oracle_slices(w: Workload) -> list:
+    """(b, h) slices the oracle checks: the sampled ones, or all of them."""
+    return sample_slices(w, w.oracle_slices) if w.oracle_slices else all_slices(w)
 
 
 def sample_slices(w: Workload, count: int) -> list:

@@ -6,7 +6,7 @@ import torch
 
 import oracle
 from io_aware_exact_14_gb300 import fa
-from io_aware_exact_14_gb300.workloads import WORKLOADS, sample_rows, sample_slices, workload_inputs
+from io_aware_exact_14_gb300.workloads import WORKLOADS, oracle_slices, sample_rows, workload_inputs
 from gpu_util import TOL_LSE, TOL_O, assert_no_timeout, device_inputs, f64, o_excess_err
 
 pytestmark = pytest.mark.gpu
@@ -113,7 +113,11 @@ def _check_slices(w, x, o, lse, causal, slices):
 
 @pytest.mark.parametrize("index", [1, 2, 3, 4, 5])
 def test_fwd_workload_parity(index):
-    """Each workload at its full size, in the launch configuration the benchmark times."""
+    """Each workload at its full size, in the launch configuration the benchmark times.
+
+    The oracle checks every row of every head, slice by slice (bounded host
+    memory), except where the workload states a sample: 256 query rows per
+    head at N = 16384, two (b, h) slices of the B = 8 training step."""
     w = WORKLOADS[index]
     x = workload_inputs(w, with_grad=False)
     g = {k: t.cuda() for k, t in x.items()}
@@ -124,9 +128,5 @@ def test_fwd_workload_parity(index):
         assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
         if w.oracle_rows:
             _check_rows(w, x, o, lse, causal, sample_rows(w, w.oracle_rows))
-        elif w.oracle_slices:
-            _check_slices(w, x, o, lse, causal, sample_slices(w, w.oracle_slices))
         else:
-            o_ref, lse_ref = oracle.attn_fwd_ref(f64(x["q"]), f64(x["k"]), f64(x["v"]), w.scale, causal)
-            assert o_excess_err(f64(o), o_ref) <= TOL_O
-            assert oracle.lse_max_abs_err(f64(lse), lse_ref) <= TOL_LSE
+            _check_slices(w, x, o, lse, causal, oracle_slices(w))

@@ -292,7 +292,9 @@ fa_status fa_bwd_dq(const void* q, const void* k, const void* v, const float* ls
  * FA_ERR_WORKSPACE (see fa_last_error_detail) and must use fa_bwd.  This entry
  * point allocates nothing and calls no allocating routine.
  *   - The first call with a given device current looks up the scratch's
- *     device address; make that first call before any stream capture.
+ *     device address (and again when that device's CUDA context changes, for
+ *     example after cudaDeviceReset); make that first call before any stream
+ *     capture.
  *   - All calls share the one scratch array: two calls whose kernels overlap
  *     on the GPU (for example on different streams) race on it.  Calls
  *     ordered on one stream are safe; each call overwrites the rows it uses.
@@ -302,14 +304,37 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
                          int B, int H, int N, int d, float scale, int causal,
                          struct CUstream_st* stream);
 
+/*
+ * Test hook of the deadlock guard; not for production use.  fa_fwd with
+ * every pipeline wait bounded by wait_limit_us (>= 1) instead of the built-in
+ * 4 s, and with the copy producer of every CTA withholding K/V group
+ * withhold_group (>= 0) and all later ones: group 0 is K_0, group j+1 holds
+ * V_j and K_{j+1}.  The tensor-core warp's wait for that group then runs into
+ * the limit; the CTA records FA_ERR_TIMEOUT (fa_debug_status; fa_debug_site()
+ * == 0x102, the forward's K/V-group wait, unless another wait of the same
+ * launch gave up first), ends the waits of the launch's other CTAs, lets the
+ * copies and products already issued complete, frees its tensor memory and
+ * returns.  O and LSE are then incomplete.  Launches made before or after are
+ * unaffected: a launch that gives up ends only its own waits.  A group index
+ * past the last group withholds nothing (the call behaves as fa_fwd).
+ * FA_ERR_INVALID_ARG for withhold_group < 0 or wait_limit_us == 0; other
+ * arguments and errors as fa_fwd.
+ */
+fa_status fa_debug_fwd_withhold(const void* q, const void* k, const void* v, void* o, float* lse,
+                                int B, int H, int N, int d, float scale, int causal, int withhold_group,
+                                unsigned int wait_limit_us, struct CUstream_st* stream);
+
 /* Static description of a status code (never NULL). */
 const char* fa_status_string(fa_status s);
 
 /*
  * Device-side status of the kernels: FA_OK, or FA_ERR_TIMEOUT if some kernel
- * gave up on a pipeline wait (a deadlock guard; each wait is bounded and the
- * kernel unwinds instead of hanging).  Synchronous: reads device memory.
- * reset != 0 clears the recorded state.  FA_ERR_CUDA if the read fails.
+ * gave up on a pipeline wait (a deadlock guard; each wait is bounded, 4 s,
+ * and the kernel unwinds instead of hanging, leaving that launch's outputs
+ * incomplete).  The first failure's site is kept until a call with
+ * reset != 0 clears it; a failure ends only the waits of its own launch, so
+ * later calls run normally whether or not the state was cleared.
+ * Synchronous: reads device memory.  FA_ERR_CUDA if the read fails.
  */
 fa_status fa_debug_status(int reset);
 

@@ -6,10 +6,24 @@
 
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
 #include <mutex>
+
+namespace fa {
+
+// Launch ids start at 1 and skip 0 when the counter wraps (after 2^32 - 1
+// launches): 0 is the abort word's "no launch gave up".
+WaitCfg next_wait_cfg() {
+  static std::atomic<uint32_t> counter{0};
+  uint32_t e = counter.fetch_add(1, std::memory_order_relaxed) + 1;
+  if (e == 0) e = counter.fetch_add(1, std::memory_order_relaxed) + 1;
+  return WaitCfg{e, kDefaultWaitLimitUs, -1};
+}
+
+}  // namespace fa
 
 namespace {
 
@@ -293,7 +307,8 @@ fa_status dkdv_checked(const void* q, const void* k, const void* v, const float*
   FA_TRY(make_map(&tdo, dO, s, t.dO));
   FA_TRY(make_map(&tdk, dk, s, t.dk));
   FA_TRY(make_map(&tdv, dv, s, t.dv));
-  return cuda_status(fa::launch_bwd_dkdv(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s, drop, st), "dK/dV kernel launch");
+  return cuda_status(fa::launch_bwd_dkdv(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s, drop, fa::next_wait_cfg(), st),
+                     "dK/dV kernel launch");
 }
 
 fa_status dq_checked(const void* q, const void* k, const void* v, const float* lse, const void* dO,
@@ -306,7 +321,8 @@ fa_status dq_checked(const void* q, const void* k, const void* v, const float* l
   FA_TRY(make_map(&tv, v, s, t.v));
   FA_TRY(make_map(&tdo, dO, s, t.dO));
   FA_TRY(make_map(&tdq, dq, s, t.dq));
-  return cuda_status(fa::launch_bwd_dq(tq, tk, tv, tdo, tdq, lse, Dvec, s, drop, st), "dQ kernel launch");
+  return cuda_status(fa::launch_bwd_dq(tq, tk, tv, tdo, tdq, lse, Dvec, s, drop, fa::next_wait_cfg(), st),
+                     "dQ kernel launch");
 }
 
 Span view_span(const void* p, const Shape& s, const Strides& st) {
@@ -315,7 +331,8 @@ Span view_span(const void* p, const Shape& s, const Strides& st) {
 
 fa_status fwd_impl(const void* q, const fa_strides* qs, const void* k, const fa_strides* ks, const void* v,
                    const fa_strides* vs, void* o, const fa_strides* os, float* lse, int B, int H, int N, int d,
-                   float scale, int causal, cudaStream_t stream, const fa::DropArgs& drop = kNoDrop) {
+                   float scale, int causal, cudaStream_t stream, const fa::DropArgs& drop = kNoDrop,
+                   const fa::WaitCfg* wait = nullptr) {
   FA_TRY(check_sizes(B, H, N, d));
   if (N == 0) return FA_OK;
   FA_TRY(check_ptrs({q, k, v, o}, {lse}));
@@ -335,7 +352,8 @@ fa_status fwd_impl(const void* q, const fa_strides* qs, const void* k, const fa_
   FA_TRY(make_map(&tk, k, s, Sk));
   FA_TRY(make_map(&tv, v, s, Sv));
   FA_TRY(make_map(&to, o, s, So));
-  return cuda_status(fa::launch_fwd(tq, tk, tv, to, lse, s, drop, stream), "forward kernel launch");
+  return cuda_status(fa::launch_fwd(tq, tk, tv, to, lse, s, drop, wait ? *wait : fa::next_wait_cfg(), stream),
+                     "forward kernel launch");
 }
 
 fa_status bwd_impl(const void* q, const fa_strides* qs, const void* k, const fa_strides* ks, const void* v,
@@ -421,7 +439,7 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, f
   const float* o_part = static_cast<const float*>(workspace);
   float* lse_part = p.n_splits > 0 ? reinterpret_cast<float*>(static_cast<char*>(workspace) + p.o_bytes) : nullptr;
   return cuda_status(fa::launch_fwd_splitkv(tq, tk, tv, top, o_part, lse_part, o, lse, sq, Nk, p.n_splits,
-                                            p.kt_per_split, stream),
+                                            p.kt_per_split, fa::next_wait_cfg(), stream),
                      "split-KV forward launch");
 }
 
@@ -548,7 +566,8 @@ fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const floa
   FA_TRY(make_map_u8(&tk, k8, qk_dims, qk_str));
   FA_TRY(make_map_u8(&tvt, vt8, vt_dims, vt_str));
   FA_TRY(make_map(&to, o, s));
-  return cuda_status(fa::launch_fwd_fp8(tq, tk, tvt, to, descale_q, descale_k, descale_v, lse, s, stream),
+  return cuda_status(fa::launch_fwd_fp8(tq, tk, tvt, to, descale_q, descale_k, descale_v, lse, s,
+                                        fa::next_wait_cfg(), stream),
                      "FP8 forward launch");
 }
 
@@ -573,6 +592,17 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
   FA_TRY(cuda_status(fa::launch_bwd_preprocess(o, fa::contiguous_strides(s), dO, fa::contiguous_strides(s), Dvec, s, stream), "preprocess kernel launch"));
   FA_TRY(dkdv_checked(q, k, v, lse, dO, Dvec, dk, dv, s, contiguous_bwd(s), stream));
   return dq_checked(q, k, v, lse, dO, Dvec, dq, s, contiguous_bwd(s), stream);
+}
+
+fa_status fa_debug_fwd_withhold(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                                int N, int d, float scale, int causal, int withhold_group,
+                                unsigned int wait_limit_us, struct CUstream_st* stream) {
+  if (withhold_group < 0 || wait_limit_us == 0) return FA_ERR_INVALID_ARG;
+  fa::WaitCfg wc = fa::next_wait_cfg();
+  wc.limit_us = wait_limit_us;
+  wc.withhold = withhold_group;
+  return fwd_impl(q, nullptr, k, nullptr, v, nullptr, o, nullptr, lse, B, H, N, d, scale, causal, stream, kNoDrop,
+                  &wc);
 }
 
 const char* fa_status_string(fa_status s) {

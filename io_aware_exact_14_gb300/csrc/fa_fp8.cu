@@ -36,7 +36,7 @@
 namespace fa {
 namespace {
 
-__device__ unsigned int g_status_fp8 = 0;
+__device__ unsigned int g_status_fp8[2] = {0, 0};   // status, abort epoch (see CtaGuard)
 constexpr uint32_t kSiteFp8 = 0x400u;
 constexpr float kRescaleThreshold8 = 8.0f;   // log2 units; P~ stays <= 256 < 448
 constexpr float kLn2f = 0.6931471805599453f;
@@ -366,7 +366,8 @@ __global__ void __launch_bounds__(384, 1)
     fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmVt, const __grid_constant__ CUtensorMap tmO,
                       const float* __restrict__ dq, const float* __restrict__ dk, const float* __restrict__ dv,
-                      float* __restrict__ lse, int N, int n_pairs, int BH, int H, int band, float scale_log2) {
+                      float* __restrict__ lse, int N, int n_pairs, int BH, int H, int band, float scale_log2,
+                      const WaitCfg wc) {
   using C = Fp8Cfg;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -416,7 +417,7 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  const CtaGuard g{abort_flag, &g_status_fp8};
+  const CtaGuard g{abort_flag, g_status_fp8, wc.epoch, wc.limit_us};
 
   if (warp >= 8) {
     regs_dec<C::kRegsOther>();
@@ -638,7 +639,7 @@ cudaError_t launch_quant_d(const void* x, void* out, float* descale, int B, int 
 template <bool CAUSAL>
 cudaError_t launch_fwd_fp8_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,
                              const CUtensorMap& to, const float* dq, const float* dk, const float* dv, float* lse,
-                             const Shape& s, cudaStream_t st) {
+                             const Shape& s, const WaitCfg& wc, cudaStream_t st) {
   using C = Fp8Cfg;
   auto kern = fa_fwd_fp8_kernel<CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
@@ -653,7 +654,7 @@ cudaError_t launch_fwd_fp8_t(const CUtensorMap& tq, const CUtensorMap& tk, const
   const dim3 grid(static_cast<unsigned>(s.B) * s.H * n_pairs);
   // L2 band: e4m3 K and V of a head take 2 N d bytes
   kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tvt, to, dq, dk, dv, lse, s.N, n_pairs, s.B * s.H, s.H,
-                                                 head_band(s.N, (s.d + 1) / 2), scale_log2);
+                                                 head_band(s.N, (s.d + 1) / 2), scale_log2, wc);
   return cudaGetLastError();
 }
 
@@ -671,19 +672,19 @@ cudaError_t launch_fp8_quantize(const void* x, void* out, float* descale, const 
 
 cudaError_t launch_fwd_fp8(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,
                            const CUtensorMap& to, const float* dq, const float* dk, const float* dv, float* lse,
-                           const Shape& s, cudaStream_t st) {
-  return s.causal ? launch_fwd_fp8_t<true>(tq, tk, tvt, to, dq, dk, dv, lse, s, st)
-                  : launch_fwd_fp8_t<false>(tq, tk, tvt, to, dq, dk, dv, lse, s, st);
+                           const Shape& s, const WaitCfg& wc, cudaStream_t st) {
+  return s.causal ? launch_fwd_fp8_t<true>(tq, tk, tvt, to, dq, dk, dv, lse, s, wc, st)
+                  : launch_fwd_fp8_t<false>(tq, tk, tvt, to, dq, dk, dv, lse, s, wc, st);
 }
 
 cudaError_t fp8_status(uint32_t* out, bool reset) {
-  unsigned int v = 0;
-  cudaError_t e = cudaMemcpyFromSymbol(&v, g_status_fp8, sizeof(v));
+  unsigned int v[2] = {0, 0};
+  cudaError_t e = cudaMemcpyFromSymbol(v, g_status_fp8, sizeof(v));
   if (e != cudaSuccess) return e;
-  *out = v;
-  if (reset && v != 0) {
-    const unsigned int z = 0;
-    e = cudaMemcpyToSymbol(g_status_fp8, &z, sizeof(z));
+  *out = v[0];
+  if (reset && (v[0] | v[1]) != 0) {
+    const unsigned int z[2] = {0, 0};
+    e = cudaMemcpyToSymbol(g_status_fp8, z, sizeof(z));
   }
   return e;
 }

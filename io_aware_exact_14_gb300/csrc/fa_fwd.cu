@@ -44,7 +44,7 @@
 namespace fa {
 namespace {
 
-__device__ unsigned int g_status_fwd = 0;
+__device__ unsigned int g_status_fwd[2] = {0, 0};   // status, abort epoch (see CtaGuard)
 constexpr int kL2Ahead = 4;   // key/value tiles the producer prefetches into L2 ahead of its loads
 
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -125,7 +125,7 @@ __device__ __forceinline__ FwdWork fwd_split_work(int u, int n_qt, int n_splits,
 template <int D>
 __device__ __forceinline__ void fwd_producer(const FwdWork& w, uint8_t* smem, uint64_t* full, uint64_t* empty,
                                              uint64_t* q_full, const CUtensorMap* tmQ, const CUtensorMap* tmK,
-                                             const CUtensorMap* tmV, const CtaGuard& g) {
+                                             const CUtensorMap* tmV, int withhold, const CtaGuard& g) {
   using C = FwdCfg<D>;
   mbar_arrive_expect_tx(q_full, (w.n1 > 0 ? 2u : 1u) * C::kTileBytes);
 #pragma unroll
@@ -144,6 +144,10 @@ __device__ __forceinline__ void fwd_producer(const FwdWork& w, uint8_t* smem, ui
       const int idx = 2 * j + kind;
       const int grp = (idx + 1) >> 1;
       if (kind == 1 || j == 0) {
+        if (grp == withhold) {   // test hook: this group (and every later one) never arrives
+          ok = false;
+          break;
+        }
         // first tile of its group: wait until the group that last used these
         // two slots (grp - kGroups) is released, then expect the whole group
         if (grp >= C::kGroups &&
@@ -503,7 +507,8 @@ __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                   float* __restrict__ lse, int N, int n_pairs, int BH, int H, int band, float scale_log2, int Nk,
-                  int n_qt, int n_kt, int n_splits, int kt_per_split, const __grid_constant__ DropArgs drop) {
+                  int n_qt, int n_kt, int n_splits, int kt_per_split, const __grid_constant__ DropArgs drop,
+                  const WaitCfg wc) {
   static_assert(!SPLIT || (!CAUSAL && ISSUERS == 1), "split-KV launches are non-causal with one issuer");
   static_assert(!(SPLIT && DROPOUT), "split-KV launches have no dropout");
   using C = FwdCfg<D>;
@@ -556,7 +561,7 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  const CtaGuard g{abort_flag, &g_status_fwd};
+  const CtaGuard g{abort_flag, g_status_fwd, wc.epoch, wc.limit_us};
 
   // Roles.  Each branch ends the kernel on its own (no shared tail), so the
   // register budget set by setmaxnreg holds for the whole branch.  The MMA
@@ -564,7 +569,7 @@ __global__ void __launch_bounds__(384, 1)
   if (warp >= 8) {
     regs_dec<C::kRegsOther>();
     if (warp == 8) {
-      if (lane == 0) fwd_producer<D>(w, smem, full, empty, q_full, &tmQ, &tmK, &tmV, g);
+      if (lane == 0) fwd_producer<D>(w, smem, full, empty, q_full, &tmQ, &tmK, &tmV, wc.withhold, g);
     } else if (warp == 9 || (ISSUERS == 2 && warp == 10)) {
       // issuing warps (warp 9 also owns TMEM): whole-warp loops, one elected lane issues
       if (ISSUERS == 2)
@@ -591,7 +596,8 @@ __global__ void __launch_bounds__(384, 1)
 
 template <int D, bool CAUSAL, int ISSUERS, bool DROPOUT>
 cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                         const CUtensorMap& to, float* lse, const Shape& s, const DropArgs& drop, cudaStream_t st) {
+                         const CUtensorMap& to, float* lse, const Shape& s, const DropArgs& drop,
+                         const WaitCfg& wc, cudaStream_t st) {
   using C = FwdCfg<D>;
   auto kern = fa_fwd_kernel<D, CAUSAL, ISSUERS, false, DROPOUT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
@@ -607,7 +613,8 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
   const dim3 grid(static_cast<unsigned>(s.B) * s.H * n_pairs);
   kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, to, lse, s.N, n_pairs, s.B * s.H, s.H,
-                                                 head_band(s.N, s.d), scale_log2, s.N, n_qt, n_qt, 1, n_qt, drop);
+                                                 head_band(s.N, s.d), scale_log2, s.N, n_qt, n_qt, 1, n_qt, drop,
+                                                 wc);
   return cudaGetLastError();
 }
 
@@ -668,7 +675,8 @@ __global__ void __launch_bounds__(256) fa_fwd_merge_kernel(const float* __restri
 template <int D>
 cudaError_t launch_fwd_splitkv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                  const CUtensorMap& top, const float* o_part, float* lse_part, void* o, float* lse,
-                                 const Shape& s, int Nk, int n_splits, int kt_per_split, cudaStream_t st) {
+                                 const Shape& s, int Nk, int n_splits, int kt_per_split, const WaitCfg& wc,
+                                 cudaStream_t st) {
   using C = FwdCfg<D>;
   const int BH = s.B * s.H;
   const int n_qt = (s.N + 127) / 128;
@@ -685,7 +693,7 @@ cudaError_t launch_fwd_splitkv_t(const CUtensorMap& tq, const CUtensorMap& tk, c
     const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
     const dim3 grid(static_cast<unsigned>(BH) * n_splits * n_qt);
     kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, top, lse_part, s.N, n_qt, BH, s.H, 1, scale_log2,
-                                                   Nk, n_qt, n_kt, n_splits, kt_per_split, no_drop_args());
+                                                   Nk, n_qt, n_kt, n_splits, kt_per_split, no_drop_args(), wc);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   const long long rows = static_cast<long long>(BH) * s.N;
@@ -699,10 +707,13 @@ cudaError_t launch_fwd_splitkv_t(const CUtensorMap& tq, const CUtensorMap& tk, c
 
 cudaError_t launch_fwd_splitkv(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                const CUtensorMap& top, const float* o_part, float* lse_part, void* o, float* lse,
-                               const Shape& s, int Nk, int n_splits, int kt_per_split, cudaStream_t st) {
+                               const Shape& s, int Nk, int n_splits, int kt_per_split, const WaitCfg& wc,
+                               cudaStream_t st) {
   return kernel_dim(s.d) == 128
-             ? launch_fwd_splitkv_t<128>(tq, tk, tv, top, o_part, lse_part, o, lse, s, Nk, n_splits, kt_per_split, st)
-             : launch_fwd_splitkv_t<64>(tq, tk, tv, top, o_part, lse_part, o, lse, s, Nk, n_splits, kt_per_split, st);
+             ? launch_fwd_splitkv_t<128>(tq, tk, tv, top, o_part, lse_part, o, lse, s, Nk, n_splits, kt_per_split, wc,
+                                         st)
+             : launch_fwd_splitkv_t<64>(tq, tk, tv, top, o_part, lse_part, o, lse, s, Nk, n_splits, kt_per_split, wc,
+                                        st);
 }
 
 // Issue strategy (measured on GB300): at d = 128 one warp's issue loop (two
@@ -713,35 +724,36 @@ cudaError_t launch_fwd_splitkv(const CUtensorMap& tq, const CUtensorMap& tk, con
 constexpr int kTwoIssuerMinSteps = 24;   // average key steps per CTA
 
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& to, float* lse, const Shape& s, const DropArgs& drop, cudaStream_t st) {
+                       const CUtensorMap& to, float* lse, const Shape& s, const DropArgs& drop, const WaitCfg& wc,
+                       cudaStream_t st) {
   if (drop.t4 != 0) {   // dropout launches keep one issuing warp
     if (kernel_dim(s.d) == 128)
-      return s.causal ? launch_fwd_t<128, true, 1, true>(tq, tk, tv, to, lse, s, drop, st)
-                      : launch_fwd_t<128, false, 1, true>(tq, tk, tv, to, lse, s, drop, st);
-    return s.causal ? launch_fwd_t<64, true, 1, true>(tq, tk, tv, to, lse, s, drop, st)
-                    : launch_fwd_t<64, false, 1, true>(tq, tk, tv, to, lse, s, drop, st);
+      return s.causal ? launch_fwd_t<128, true, 1, true>(tq, tk, tv, to, lse, s, drop, wc, st)
+                      : launch_fwd_t<128, false, 1, true>(tq, tk, tv, to, lse, s, drop, wc, st);
+    return s.causal ? launch_fwd_t<64, true, 1, true>(tq, tk, tv, to, lse, s, drop, wc, st)
+                    : launch_fwd_t<64, false, 1, true>(tq, tk, tv, to, lse, s, drop, wc, st);
   }
   if (kernel_dim(s.d) == 128) {
     const int n_qt = (s.N + 127) / 128;
     const int avg_steps = s.causal ? (n_qt + 1) / 2 : n_qt;
     if (avg_steps >= kTwoIssuerMinSteps)
-      return s.causal ? launch_fwd_t<128, true, 2, false>(tq, tk, tv, to, lse, s, drop, st)
-                      : launch_fwd_t<128, false, 2, false>(tq, tk, tv, to, lse, s, drop, st);
-    return s.causal ? launch_fwd_t<128, true, 1, false>(tq, tk, tv, to, lse, s, drop, st)
-                    : launch_fwd_t<128, false, 1, false>(tq, tk, tv, to, lse, s, drop, st);
+      return s.causal ? launch_fwd_t<128, true, 2, false>(tq, tk, tv, to, lse, s, drop, wc, st)
+                      : launch_fwd_t<128, false, 2, false>(tq, tk, tv, to, lse, s, drop, wc, st);
+    return s.causal ? launch_fwd_t<128, true, 1, false>(tq, tk, tv, to, lse, s, drop, wc, st)
+                    : launch_fwd_t<128, false, 1, false>(tq, tk, tv, to, lse, s, drop, wc, st);
   }
-  return s.causal ? launch_fwd_t<64, true, 1, false>(tq, tk, tv, to, lse, s, drop, st)
-                  : launch_fwd_t<64, false, 1, false>(tq, tk, tv, to, lse, s, drop, st);
+  return s.causal ? launch_fwd_t<64, true, 1, false>(tq, tk, tv, to, lse, s, drop, wc, st)
+                  : launch_fwd_t<64, false, 1, false>(tq, tk, tv, to, lse, s, drop, wc, st);
 }
 
 cudaError_t fwd_status(uint32_t* out, bool reset) {
-  unsigned int v = 0;
-  cudaError_t e = cudaMemcpyFromSymbol(&v, g_status_fwd, sizeof(v));
+  unsigned int v[2] = {0, 0};
+  cudaError_t e = cudaMemcpyFromSymbol(v, g_status_fwd, sizeof(v));
   if (e != cudaSuccess) return e;
-  *out = v;
-  if (reset && v != 0) {
-    const unsigned int z = 0;
-    e = cudaMemcpyToSymbol(g_status_fwd, &z, sizeof(z));
+  *out = v[0];
+  if (reset && (v[0] | v[1]) != 0) {
+    const unsigned int z[2] = {0, 0};
+    e = cudaMemcpyToSymbol(g_status_fwd, z, sizeof(z));
   }
   return e;
 }

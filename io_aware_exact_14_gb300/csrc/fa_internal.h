@@ -45,6 +45,23 @@ inline DropArgs make_drop_args(uint64_t seed, uint32_t offset, int t) {
 }
 inline DropArgs no_drop_args() { return make_drop_args(0, 0, 0); }
 
+// Bounded waits of one launch.  Every pipeline wait of a kernel gives up after
+// limit_us microseconds: the CTA records a site in the kernel family's status
+// word (first failure wins, kept until read with reset) and writes `epoch` to
+// the family's abort word, which ends the waits of every other CTA of the same
+// launch.  epoch is unique per launch (never 0), so a launch that gave up never
+// cuts short a later one.  withhold >= 0 is a test hook of the forward: its
+// producer issues no copy for K/V group `withhold` (nor any later one), so a
+// consumer's wait on that group runs into the limit; < 0 in every normal call.
+struct WaitCfg {
+  uint32_t epoch;
+  uint32_t limit_us;
+  int32_t withhold;
+};
+constexpr uint32_t kDefaultWaitLimitUs = 4000000;   // 4 s
+// The next launch's configuration: a fresh epoch, the default limit, no hook.
+WaitCfg next_wait_cfg();
+
 // Head dims: any multiple of 8 from 8 to 128 runs in the kernel built for
 // D = 64 (d <= 64) or D = 128.  The tensor maps carry the true extent d, so
 // TMA loads fill columns d .. D-1 of every tile with zeros (they add nothing
@@ -62,7 +79,8 @@ inline Strides contiguous_strides(const Shape& s) {
 // Forward: O and LSE from Q, K, V (TMA maps are 4-D {d, N, H, B}, box
 // {64, 128, 1, 1}, with each tensor's own strides).
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& to, float* lse, const Shape& s, const DropArgs& drop, cudaStream_t st);
+                       const CUtensorMap& to, float* lse, const Shape& s, const DropArgs& drop, const WaitCfg& wc,
+                       cudaStream_t st);
 
 // Split-KV forward for short query blocks against long key sequences
 // (non-causal): Q maps {d, Nq, H, B} (s.N = Nq), K/V maps {d, Nk, H, B}; each
@@ -72,7 +90,8 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
 // lse (fp32 [B, H, Nq]).  n_splits and kt_per_split come from splitkv_chunks.
 cudaError_t launch_fwd_splitkv(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                const CUtensorMap& top, const float* o_part, float* lse_part, void* o, float* lse,
-                               const Shape& s, int Nk, int n_splits, int kt_per_split, cudaStream_t st);
+                               const Shape& s, int Nk, int n_splits, int kt_per_split, const WaitCfg& wc,
+                               cudaStream_t st);
 
 // Split-KV chunking: `want` splits (<= 0: chosen from the SM count) of the
 // ceil(Nk/128) key tiles into chunks of kt_per_split whole tiles; n_splits is
@@ -124,12 +143,13 @@ cudaError_t launch_bwd_preprocess(const void* o, const Strides& so, const void* 
 cudaError_t launch_bwd_dkdv(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
                             const float* lse, const float* Dvec, const Shape& s, const DropArgs& drop,
-                            cudaStream_t st);
+                            const WaitCfg& wc, cudaStream_t st);
 
 // Backward, step 3: dQ for each 128-query tile, looping over key tiles.
 cudaError_t launch_bwd_dq(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const CUtensorMap& tdq, const float* lse,
-                          const float* Dvec, const Shape& s, const DropArgs& drop, cudaStream_t st);
+                          const float* Dvec, const Shape& s, const DropArgs& drop, const WaitCfg& wc,
+                          cudaStream_t st);
 
 // FP8 (e4m3): per-(b, h) quantisation of a contiguous bf16 [B, H, N, d] tensor
 // into codes [B, H, N, d] (or, transposed, [B, H, d, ldv]) with descale[b*H + h]
@@ -141,7 +161,7 @@ cudaError_t launch_fp8_quantize(const void* x, void* out, float* descale, const 
                                 long long ldv, bool rotate, uint64_t seed, cudaStream_t st);
 cudaError_t launch_fwd_fp8(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,
                            const CUtensorMap& to, const float* dq, const float* dk, const float* dv, float* lse,
-                           const Shape& s, cudaStream_t st);
+                           const Shape& s, const WaitCfg& wc, cudaStream_t st);
 
 // Fixed device scratch for callers that cannot allocate: room for the fp32
 // row term of up to kNoAllocRows rows (B*H*N), in a file-scope device array of
@@ -158,7 +178,8 @@ inline int head_band(int N, int d) {
   return static_cast<int>(b < 1 ? 1 : (b > 16 ? 16 : b));
 }
 
-// Device status words (0 = no kernel gave up on a wait).  `reset` clears them.
+// Device status words (0 = no kernel gave up on a wait).  `reset` clears them
+// (and the abort words).
 // Synchronous: copies from the device.
 cudaError_t fwd_status(uint32_t* out, bool reset);
 cudaError_t bwd_status(uint32_t* out, bool reset);

@@ -23,10 +23,6 @@ enum : uint32_t {
   kSiteFwd = 0x100, kSiteDkdv = 0x200, kSiteDq = 0x300,
 };
 
-// A wait that has not completed after this long is treated as a deadlock: the
-// kernel records the site, raises the CTA's abort flag and unwinds cleanly.
-constexpr unsigned long long kWaitLimitNs = 4000000000ull;  // 4 s
-
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -66,15 +62,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Shared state every role of a CTA sees: the abort flag that ends all waits.
+// Shared state every role of a CTA sees.  A wait that has not completed
+// after limit_us is treated as a deadlock: the CTA records the site, raises its
+// abort flag (ending every other wait of the CTA) and writes the launch's
+// epoch to the abort word (ending the waits of the launch's other CTAs); all
+// roles then unwind cleanly.  Only CTAs of the same launch (same epoch) react
+// to the abort word, so a launch that gave up never cuts short another.
 struct CtaGuard {
   volatile uint32_t* abort_flag;   // in shared memory
-  unsigned int* status;            // device status word (first error wins)
+  unsigned int* status;            // device words: [0] status (first site wins), [1] abort epoch
+  uint32_t epoch;                  // this launch's id (never 0)
+  uint32_t limit_us;               // wait limit
 };
 
 __device__ __forceinline__ void guard_fail(const CtaGuard& g, uint32_t site) {
   *g.abort_flag = 1u;
   atomicCAS(g.status, 0u, site);
+  atomicExch(g.status + 1, g.epoch);
+}
+
+// Has this CTA, or another CTA of the same launch, given up?
+__device__ __forceinline__ bool guard_aborted(const CtaGuard& g) {
+  return *g.abort_flag || *reinterpret_cast<volatile unsigned int*>(g.status + 1) == g.epoch;
+}
+
+__device__ __forceinline__ bool guard_expired(const CtaGuard& g, unsigned long long t0) {
+  return global_ns() - t0 > static_cast<unsigned long long>(g.limit_us) * 1000ull;
 }
 
 // The polling loops run out of line by default: every wait site then shares
@@ -94,12 +107,12 @@ __device__ __forceinline__ bool mbar_poll(uint64_t* bar, uint32_t parity, const 
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0u) {
-      // another CTA already gave up: this launch is lost, unwind at once
-      if (*g.abort_flag || *reinterpret_cast<volatile unsigned int*>(g.status) != 0u) {
+      // this CTA or another of the launch gave up: unwind at once
+      if (guard_aborted(g)) {
         *g.abort_flag = 1u;
         return false;
       }
-      if (global_ns() - t0 > kWaitLimitNs) {
+      if (guard_expired(g, t0)) {
         guard_fail(g, site);
         return false;
       }
@@ -117,11 +130,11 @@ __device__ FA_WAIT_LINKAGE bool mbar_wait_backoff(uint64_t* bar, uint32_t parity
     if (mbar_try_wait(bar, parity)) return true;
     __nanosleep(200);
     if ((it & 15u) == 0u) {
-      if (*g.abort_flag || *reinterpret_cast<volatile unsigned int*>(g.status) != 0u) {
+      if (guard_aborted(g)) {
         *g.abort_flag = 1u;
         return false;
       }
-      if (global_ns() - t0 > kWaitLimitNs) {
+      if (guard_expired(g, t0)) {
         guard_fail(g, site);
         return false;
       }
@@ -360,11 +373,11 @@ __device__ FA_WAIT_LINKAGE int mbar_wait_either_slow(uint64_t* a, uint32_t pa, u
     if (mbar_try_wait(a, pa)) return 0;
     if (mbar_try_wait(b, pb)) return 1;
     if ((it & 63u) == 0u) {
-      if (*g.abort_flag || *reinterpret_cast<volatile unsigned int*>(g.status) != 0u) {
+      if (guard_aborted(g)) {
         *g.abort_flag = 1u;
         return -1;
       }
-      if (global_ns() - t0 > kWaitLimitNs) {
+      if (guard_expired(g, t0)) {
         guard_fail(g, site);
         return -1;
       }

@@ -47,6 +47,7 @@ SIGNATURES = {
     "fa_bwd_preprocess": (_I, [_P, _P, _P, _I, _I, _I, _I, _P]),
     "fa_bwd_dkdv": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
     "fa_bwd_dq": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
+    "fa_debug_fwd_withhold": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _I, ctypes.c_uint, _P]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_debug_status": (_I, [_I]),
     "fa_debug_site": (ctypes.c_uint, []),
@@ -449,6 +450,25 @@ def fa_bwd_dq(q, k, v, lse, do, Dvec, scale: Optional[float] = None, causal: boo
                                           do.data_ptr(), Dvec.data_ptr(), dq.data_ptr(),
                                           B, H, N, d, scale, int(bool(causal)), _stream_ptr(stream)))
     return dq
+
+
+def fa_debug_fwd_withhold(q, k, v, withhold_group: int, wait_limit_us: int, scale: Optional[float] = None,
+                          causal: bool = False, out=None, lse=None, stream=None):
+    """Test hook of the deadlock guard: fa_fwd whose producer withholds K/V group
+    `withhold_group` and whose waits give up after `wait_limit_us`.  Returns the
+    status code (the launch itself succeeds; the timeout shows in fa_debug_status)."""
+    shape = _bhnd(q, "q")
+    _same(shape, k, "k")
+    _same(shape, v, "v")
+    B, H, N, d = shape
+    scale = default_scale(d) if scale is None else float(scale)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    _same(shape, out, "out")
+    _vec(lse, shape, "lse")
+    return int(load().fa_debug_fwd_withhold(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                            lse.data_ptr(), B, H, N, d, scale, int(bool(causal)),
+                                            int(withhold_group), int(wait_limit_us), _stream_ptr(stream)))
 
 
 def fa_debug_status(reset: bool = False) -> int:

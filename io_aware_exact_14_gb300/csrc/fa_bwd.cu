@@ -19,7 +19,7 @@
 namespace fa {
 namespace {
 
-__device__ unsigned int g_status_bwd = 0;
+__device__ unsigned int g_status_bwd[2] = {0, 0};   // status, abort epoch (see CtaGuard)
 constexpr int kMaxDevices = 64;
 
 // ---------------------------------------------------------------------------
@@ -325,13 +325,13 @@ __global__ void __launch_bounds__(384, 1)
                        const __grid_constant__ CUtensorMap tmDK, const __grid_constant__ CUtensorMap tmDV,
                        const float* __restrict__ lse, const float* __restrict__ Dg, int N, int n_tiles,
                        int BH, int H, int band, float scale, float scale_log2,
-                       const __grid_constant__ DropArgs drop) {
+                       const __grid_constant__ DropArgs drop, const WaitCfg wc) {
   using C = DkdvCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   if (static_cast<uint32_t>(smem - smem_raw) + C::kLayoutBytes > C::kSmemBytes) {
     // the aligned layout does not fit this launch's shared memory: report, touch nothing
-    if (threadIdx.x == 0) atomicCAS(&g_status_bwd, 0u, kSiteDkdv | 0xFFu);
+    if (threadIdx.x == 0) atomicCAS(&g_status_bwd[0], 0u, kSiteDkdv | 0xFFu);
     return;
   }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
@@ -393,7 +393,7 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  const CtaGuard g{abort_flag, &g_status_bwd};
+  const CtaGuard g{abort_flag, g_status_bwd, wc.epoch, wc.limit_us};
   const uint32_t sbase = smem_u32(smem);
 
   if (warp >= 8) {
@@ -852,13 +852,13 @@ __global__ void __launch_bounds__(384, 1)
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                      const __grid_constant__ CUtensorMap tmDQ, const float* __restrict__ lse,
                      const float* __restrict__ Dg, int N, int n_tiles, int BH, int H, int band, float scale,
-                     float scale_log2, const __grid_constant__ DropArgs drop) {
+                     float scale_log2, const __grid_constant__ DropArgs drop, const WaitCfg wc) {
   using C = DqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   if (static_cast<uint32_t>(smem - smem_raw) + C::kLayoutBytes > C::kSmemBytes) {
     // the aligned layout does not fit this launch's shared memory: report, touch nothing
-    if (threadIdx.x == 0) atomicCAS(&g_status_bwd, 0u, kSiteDq | 0xFFu);
+    if (threadIdx.x == 0) atomicCAS(&g_status_bwd[0], 0u, kSiteDq | 0xFFu);
     return;
   }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
@@ -921,7 +921,7 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  const CtaGuard g{abort_flag, &g_status_bwd};
+  const CtaGuard g{abort_flag, g_status_bwd, wc.epoch, wc.limit_us};
   const uint32_t sbase = smem_u32(smem);
   auto kpar = [](int j) { return static_cast<uint32_t>((j / C::kKStages) & 1); };
   auto vpar = [](int j) { return static_cast<uint32_t>((j / C::kVStages) & 1); };
@@ -1229,7 +1229,8 @@ __global__ void __launch_bounds__(384, 1)
 template <int D, bool CAUSAL, bool DROPOUT>
 cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv, const float* lse,
-                          const float* Dvec, const Shape& s, const DropArgs& drop, cudaStream_t st) {
+                          const float* Dvec, const Shape& s, const DropArgs& drop, const WaitCfg& wc,
+                          cudaStream_t st) {
   using C = DkdvCfg<D>;
   auto kern = fa_bwd_dkdv_kernel<D, CAUSAL, DROPOUT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
@@ -1238,14 +1239,14 @@ cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CU
   const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
   const dim3 grid(static_cast<unsigned>(s.B) * s.H * n_tiles);
   kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s.N, n_tiles, s.B * s.H, s.H,
-                                                 head_band(s.N, s.d), s.scale, scale_log2, drop);
+                                                 head_band(s.N, s.d), s.scale, scale_log2, drop, wc);
   return cudaGetLastError();
 }
 
 template <int D, bool CAUSAL, bool DROPOUT>
 cudaError_t launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                         const CUtensorMap& tdo, const CUtensorMap& tdq, const float* lse, const float* Dvec,
-                        const Shape& s, const DropArgs& drop, cudaStream_t st) {
+                        const Shape& s, const DropArgs& drop, const WaitCfg& wc, cudaStream_t st) {
   using C = DqCfg<D>;
   auto kern = fa_bwd_dq_kernel<D, CAUSAL, DROPOUT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
@@ -1254,7 +1255,7 @@ cudaError_t launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
   const dim3 grid(static_cast<unsigned>(s.B) * s.H * n_tiles);
   kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, tdq, lse, Dvec, s.N, n_tiles, s.B * s.H, s.H,
-                                                 head_band(s.N, s.d), s.scale, scale_log2, drop);
+                                                 head_band(s.N, s.d), s.scale, scale_log2, drop, wc);
   return cudaGetLastError();
 }
 
@@ -1262,23 +1263,24 @@ cudaError_t launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
 template <int D>
 cudaError_t launch_dkdv_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv, const float* lse,
-                          const float* Dvec, const Shape& s, const DropArgs& drop, cudaStream_t st) {
+                          const float* Dvec, const Shape& s, const DropArgs& drop, const WaitCfg& wc,
+                          cudaStream_t st) {
   if (drop.t4 != 0)
-    return s.causal ? launch_dkdv_t<D, true, true>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s, drop, st)
-                    : launch_dkdv_t<D, false, true>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s, drop, st);
-  return s.causal ? launch_dkdv_t<D, true, false>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s, drop, st)
-                  : launch_dkdv_t<D, false, false>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s, drop, st);
+    return s.causal ? launch_dkdv_t<D, true, true>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s, drop, wc, st)
+                    : launch_dkdv_t<D, false, true>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s, drop, wc, st);
+  return s.causal ? launch_dkdv_t<D, true, false>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s, drop, wc, st)
+                  : launch_dkdv_t<D, false, false>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s, drop, wc, st);
 }
 
 template <int D>
 cudaError_t launch_dq_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                         const CUtensorMap& tdo, const CUtensorMap& tdq, const float* lse, const float* Dvec,
-                        const Shape& s, const DropArgs& drop, cudaStream_t st) {
+                        const Shape& s, const DropArgs& drop, const WaitCfg& wc, cudaStream_t st) {
   if (drop.t4 != 0)
-    return s.causal ? launch_dq_t<D, true, true>(tq, tk, tv, tdo, tdq, lse, Dvec, s, drop, st)
-                    : launch_dq_t<D, false, true>(tq, tk, tv, tdo, tdq, lse, Dvec, s, drop, st);
-  return s.causal ? launch_dq_t<D, true, false>(tq, tk, tv, tdo, tdq, lse, Dvec, s, drop, st)
-                  : launch_dq_t<D, false, false>(tq, tk, tv, tdo, tdq, lse, Dvec, s, drop, st);
+    return s.causal ? launch_dq_t<D, true, true>(tq, tk, tv, tdo, tdq, lse, Dvec, s, drop, wc, st)
+                    : launch_dq_t<D, false, true>(tq, tk, tv, tdo, tdq, lse, Dvec, s, drop, wc, st);
+  return s.causal ? launch_dq_t<D, true, false>(tq, tk, tv, tdo, tdq, lse, Dvec, s, drop, wc, st)
+                  : launch_dq_t<D, false, false>(tq, tk, tv, tdo, tdq, lse, Dvec, s, drop, wc, st);
 }
 
 }  // namespace
@@ -1286,16 +1288,16 @@ cudaError_t launch_dq_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
 cudaError_t launch_bwd_dkdv(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
                             const float* lse, const float* Dvec, const Shape& s, const DropArgs& drop,
-                            cudaStream_t st) {
-  return kernel_dim(s.d) == 128 ? launch_dkdv_d<128>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s, drop, st)
-                    : launch_dkdv_d<64>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s, drop, st);
+                            const WaitCfg& wc, cudaStream_t st) {
+  return kernel_dim(s.d) == 128 ? launch_dkdv_d<128>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s, drop, wc, st)
+                    : launch_dkdv_d<64>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s, drop, wc, st);
 }
 
 cudaError_t launch_bwd_dq(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const CUtensorMap& tdq, const float* lse, const float* Dvec,
-                          const Shape& s, const DropArgs& drop, cudaStream_t st) {
-  return kernel_dim(s.d) == 128 ? launch_dq_d<128>(tq, tk, tv, tdo, tdq, lse, Dvec, s, drop, st)
-                    : launch_dq_d<64>(tq, tk, tv, tdo, tdq, lse, Dvec, s, drop, st);
+                          const Shape& s, const DropArgs& drop, const WaitCfg& wc, cudaStream_t st) {
+  return kernel_dim(s.d) == 128 ? launch_dq_d<128>(tq, tk, tv, tdo, tdq, lse, Dvec, s, drop, wc, st)
+                    : launch_dq_d<64>(tq, tk, tv, tdo, tdq, lse, Dvec, s, drop, wc, st);
 }
 
 cudaError_t launch_bwd_preprocess(const void* o, const Strides& so, const void* dO, const Strides& sdo, float* Dvec,
@@ -1331,33 +1333,66 @@ cudaError_t launch_bwd_preprocess(const void* o, const Strides& so, const void* 
 // 8 MiB until the process exits; all calls share them.
 static __device__ __align__(256) float g_noalloc_rows[kNoAllocRows];
 
+// The current context's unique id (cuCtxGetCurrent + cuCtxGetId, fetched
+// through the runtime so nothing links libcuda); false when unavailable.
+bool current_context_id(unsigned long long* id) {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(fn);
+  });
+  CUcontext ctx = nullptr;
+  if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr)
+    return false;
+  return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// A symbol's host-side name is not a device address, and the address belongs
+// to one context: it is looked up (cudaGetSymbolAddress, which allocates
+// nothing) on the first call with a device current and again whenever the
+// current context is not the one it was looked up in (after cudaDeviceReset,
+// say, or on a thread with no context bound yet).
 cudaError_t noalloc_scratch(float** out) {
   static std::mutex mu;
   static float* addr[kMaxDevices] = {};
+  static unsigned long long ctx_of[kMaxDevices] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  unsigned long long ctx = 0;
+  const bool known_ctx = current_context_id(&ctx);
   std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
-    // a symbol's host-side name is not a device address: ask the runtime for it
+  if (addr[dev] == nullptr || !known_ctx || ctx_of[dev] != ctx) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_rows);
+    e = cudaGetSymbolAddress(&p, g_noalloc_rows);   // binds the device's context if none was current
     if (e != cudaSuccess) return e;
     addr[dev] = static_cast<float*>(p);
+    ctx_of[dev] = current_context_id(&ctx) ? ctx : 0;
   }
   *out = addr[dev];
   return cudaSuccess;
 }
 
 cudaError_t bwd_status(uint32_t* out, bool reset) {
-  unsigned int v = 0;
-  cudaError_t e = cudaMemcpyFromSymbol(&v, g_status_bwd, sizeof(v));
+  unsigned int v[2] = {0, 0};
+  cudaError_t e = cudaMemcpyFromSymbol(v, g_status_bwd, sizeof(v));
   if (e != cudaSuccess) return e;
-  *out = v;
-  if (reset && v != 0) {
-    const unsigned int z = 0;
-    e = cudaMemcpyToSymbol(g_status_bwd, &z, sizeof(z));
+  *out = v[0];
+  if (reset && (v[0] | v[1]) != 0) {
+    const unsigned int z[2] = {0, 0};
+    e = cudaMemcpyToSymbol(g_status_bwd, z, sizeof(z));
   }
   return e;
 }

@@ -7,7 +7,9 @@ them fa_bwd_noalloc keeps the backward's row term in scratch built into the
 library instead of a caller workspace.  This test calls it through the C ABI
 twice in a row (different shapes, so the second call reuses scratch that the
 first left behind) and checks each result against fa_bwd, the entry point
-with a caller workspace, within the gradient tolerance of the other tests.
+with a caller workspace: within the gradient tolerance of the other tests,
+and bit for bit, since both run the same deterministic kernels on the same
+row term (a stale row left in the scratch would show as a difference).
 
 The file name makes pytest collect it last; it also passes when run alone.
 """
@@ -41,6 +43,7 @@ def test_bwd_noalloc_matches_workspace_entry_point():
         for name, a, b in zip(("dq", "dk", "dv"), got, want):
             err = oracle.rel_fro_err(f64(a), f64(b))
             assert err <= TOL_GRAD, f"call {call}: {name} differs from fa_bwd by {err:.3g}"
+            assert torch.equal(a, b), f"call {call}: {name} is not bitwise equal to fa_bwd's"
 
 
 def test_bwd_noalloc_rejects_problems_beyond_its_scratch():

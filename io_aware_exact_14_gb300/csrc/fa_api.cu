@@ -65,10 +65,11 @@ bool overlaps(const Span& a, const Span& b) {
   return a.bytes && b.bytes && a0 < b0 + b.bytes && b0 < a0 + a.bytes;
 }
 
-// Sizes: B, H >= 1, N >= 0, d a multiple of 8 in [8, 128], grid-size limits.
-fa_status check_sizes(int B, int H, int N, int d) {
+// Sizes: B, H >= 1, N >= 0, d a multiple of 8 in [8, max_d], grid-size limits.
+// The forward takes d up to 256; the other entry points up to 128.
+fa_status check_sizes(int B, int H, int N, int d, int max_d = 128) {
   if (B < 1 || H < 1 || N < 0) return FA_ERR_INVALID_ARG;
-  if (d < 8 || d > 128 || d % 8 != 0) return FA_ERR_UNSUPPORTED;
+  if (d < 8 || d > max_d || d % 8 != 0) return FA_ERR_UNSUPPORTED;
   const long long bh = static_cast<long long>(B) * H;
   const long long tiles = bh * ((static_cast<long long>(N) + 127) / 128);
   if (bh > INT32_MAX || tiles > INT32_MAX || bh * N > (1ll << 40)) return FA_ERR_UNSUPPORTED;
@@ -333,7 +334,7 @@ fa_status fwd_impl(const void* q, const fa_strides* qs, const void* k, const fa_
                    const fa_strides* vs, void* o, const fa_strides* os, float* lse, int B, int H, int N, int d,
                    float scale, int causal, cudaStream_t stream, const fa::DropArgs& drop = kNoDrop,
                    const fa::WaitCfg* wait = nullptr) {
-  FA_TRY(check_sizes(B, H, N, d));
+  FA_TRY(check_sizes(B, H, N, d, drop.t4 == 0 && wait == nullptr ? fa::kMaxHeadDim : 128));
   if (N == 0) return FA_OK;
   FA_TRY(check_ptrs({q, k, v, o}, {lse}));
   FA_TRY(check_scale(scale));
@@ -352,6 +353,9 @@ fa_status fwd_impl(const void* q, const fa_strides* qs, const void* k, const fa_
   FA_TRY(make_map(&tk, k, s, Sk));
   FA_TRY(make_map(&tv, v, s, Sv));
   FA_TRY(make_map(&to, o, s, So));
+  if (d > 128)
+    return cuda_status(fa::launch_fwd_d256(tq, tk, tv, to, lse, s, fa::next_wait_cfg(), stream),
+                       "forward kernel launch");
   return cuda_status(fa::launch_fwd(tq, tk, tv, to, lse, s, drop, wait ? *wait : fa::next_wait_cfg(), stream),
                      "forward kernel launch");
 }
@@ -609,7 +613,7 @@ const char* fa_status_string(fa_status s) {
   switch (s) {
     case FA_OK: return "FA_OK: success";
     case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: null, misaligned or overlapping pointer, or bad size/scale";
-    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: head dim must be a multiple of 8 in [8, 128], or sizes exceed the limits";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: head dim not a multiple of 8 in the entry point's range, or sizes exceed the limits";
     case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA call or kernel launch failed";
     case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE: workspace missing, misaligned or too small";
     case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a kernel gave up on a pipeline wait";
@@ -626,8 +630,11 @@ fa_status fa_debug_status(int reset) {
   uint32_t c = 0;
   e = fa::fp8_status(&c, reset != 0);
   if (e != cudaSuccess) return fail("reading the FP8 status word", e, cudaGetErrorString(e));
-  g_last_site = a ? a : (b ? b : c);
-  return (a | b | c) ? FA_ERR_TIMEOUT : FA_OK;
+  uint32_t w = 0;
+  e = fa::fwd_d256_status(&w, reset != 0);
+  if (e != cudaSuccess) return fail("reading the wide-head forward status word", e, cudaGetErrorString(e));
+  g_last_site = a ? a : (b ? b : (c ? c : w));
+  return (a | b | c | w) ? FA_ERR_TIMEOUT : FA_OK;
 }
 
 unsigned int fa_debug_site(void) { return g_last_site; }

@@ -141,15 +141,16 @@ struct BwdCfg {
   static constexpr uint32_t kMaxSmem = 232448;   // per-CTA opt-in limit
 };
 
-// S-like product: D(128 x 128) = A(128 x d) * B(128 x d)^T, both K-major tiles.
+// S-like product: D(128 x 128) = A(128 x d) * B(128 x d)^T, both K-major
+// tiles; only the ks = ceil(d / 16) steps of 16 columns that hold data.
 template <int D>
-__device__ __forceinline__ void mma_nt(uint32_t tmem_d, uint64_t a_desc, uint64_t b_desc) {
+__device__ __forceinline__ void mma_nt(uint32_t tmem_d, uint64_t a_desc, uint64_t b_desc, int ks) {
   using C = BwdCfg<D>;
   constexpr uint32_t idesc = idesc_bf16(128, 128, false, false);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint64_t off = ((kk / 4) * C::kBoxBytes + (kk % 4) * 32) >> 4;   // descriptor address units
-    tc_mma_ss_w(tmem_d, a_desc + off, b_desc + off, idesc, kk > 0 ? 1u : 0u);
+    if (kk < ks) tc_mma_ss_w(tmem_d, a_desc + off, b_desc + off, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
@@ -324,7 +325,7 @@ __global__ void __launch_bounds__(384, 1)
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                        const __grid_constant__ CUtensorMap tmDK, const __grid_constant__ CUtensorMap tmDV,
                        const float* __restrict__ lse, const float* __restrict__ Dg, int N, int n_tiles,
-                       int BH, int H, int band, float scale, float scale_log2,
+                       int BH, int H, int band, float scale, float scale_log2, int ks,
                        const __grid_constant__ DropArgs drop, const WaitCfg wc) {
   using C = DkdvCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -559,12 +560,12 @@ __global__ void __launch_bounds__(384, 1)
         // S^T(0), dP^T(0): the previous unit's readers of these columns (its
         // last dV and dK) were issued before
         if (!(ok = mbar_wait_w(&q_full[g0 % C::kQStages], qpar(g0), g, kSiteDkdv | 3u))) break;
-        mma_nt<D>(tS, kK, kQ(g0 % C::kQStages));
+        mma_nt<D>(tS, kK, kQ(g0 % C::kQStages), ks);
         tc_commit_w(s_full);
         if (cnt == 1) tc_commit_w(k_free);    // K_j: last reader issued
         if (!(ok = mbar_wait_w(&v_full[su & 1], (su >> 1) & 1, g, kSiteDkdv | 3u))) break;
         if (!(ok = mbar_wait_w(&do_full[g0 % C::kDOStages], dpar(g0), g, kSiteDkdv | 3u))) break;
-        mma_nt<D>(tDP, kV, kDO(g0 % C::kDOStages));
+        mma_nt<D>(tDP, kV, kDO(g0 % C::kDOStages), ks);
         tc_commit_w(dp_full);
         if (cnt == 1) tc_commit_w(v_free);    // V_j: last reader issued
         for (int it = 0; ok && it < cnt; ++it) {
@@ -591,7 +592,7 @@ __global__ void __launch_bounds__(384, 1)
             if (which < 0) {
               ok = false;
             } else if (which == 0) {
-              mma_nt<D>(tS, kK, kQ(qs1));                     // S^T(i+1)
+              mma_nt<D>(tS, kK, kQ(qs1), ks);                     // S^T(i+1)
               tc_commit_w(s_full);
               if (it + 2 == cnt) tc_commit_w(k_free);       // K_j: last reader issued
               s_done = true;
@@ -605,7 +606,7 @@ __global__ void __launch_bounds__(384, 1)
           if (!ok) break;
           if (next) {
             if (!(ok = mbar_wait_w(&do_full[ds1], dpar(i + 1), g, kSiteDkdv | 13u))) break;
-            mma_nt<D>(tDP, kV, kDO(ds1));                     // dP^T(i+1), after dK(i) has read dS^T(i)
+            mma_nt<D>(tDP, kV, kDO(ds1), ks);                     // dP^T(i+1), after dK(i) has read dS^T(i)
             tc_commit_w(dp_full);
             if (it + 2 == cnt) tc_commit_w(v_free);         // V_j: last reader issued
           }
@@ -852,7 +853,7 @@ __global__ void __launch_bounds__(384, 1)
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                      const __grid_constant__ CUtensorMap tmDQ, const float* __restrict__ lse,
                      const float* __restrict__ Dg, int N, int n_tiles, int BH, int H, int band, float scale,
-                     float scale_log2, const __grid_constant__ DropArgs drop, const WaitCfg wc) {
+                     float scale_log2, int ks, const __grid_constant__ DropArgs drop, const WaitCfg wc) {
   using C = DqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1053,11 +1054,11 @@ __global__ void __launch_bounds__(384, 1)
         // unit's last dQ waited for)
         if (!(ok = mbar_wait_w(&k_full[g0 % C::kKStages], kpar(g0), g, kSiteDq | 3u))) break;
         tc_fence_after();
-        mma_nt<D>(tmem + C::col_s(g0), kQ, kK(g0 % C::kKStages));
+        mma_nt<D>(tmem + C::col_s(g0), kQ, kK(g0 % C::kKStages), ks);
         tc_commit_w(&s_full[g0 & 1]);
         if (!(ok = mbar_wait_w(&v_full[g0 % C::kVStages], vpar(g0), g, kSiteDq | 3u))) break;
         if (!(ok = mbar_wait_w(do_full, su & 1, g, kSiteDq | 19u))) break;
-        mma_nt<D>(tDP, kDO, kV(g0 % C::kVStages));
+        mma_nt<D>(tDP, kDO, kV(g0 % C::kVStages), ks);
         tc_commit_w(dp_full);
         if (cnt == 1) tc_commit_w(do_empty);   // dO_i: last reader issued
         for (int it = 0; it < cnt; ++it) {
@@ -1067,7 +1068,7 @@ __global__ void __launch_bounds__(384, 1)
           if (next) {   // S(j+1), into the other S buffer
             if (!(ok = mbar_wait_w(&k_full[(j + 1) % C::kKStages], kpar(j + 1), g, kSiteDq | 4u))) break;
             tc_fence_after();
-            mma_nt<D>(tmem + C::col_s(j + 1), kQ, kK((j + 1) % C::kKStages));
+            mma_nt<D>(tmem + C::col_s(j + 1), kQ, kK((j + 1) % C::kKStages), ks);
             tc_commit_w(&s_full[(j + 1) & 1]);
           } else {
             tc_commit_w(q_empty);   // every reader of Q_i has been issued
@@ -1090,7 +1091,7 @@ __global__ void __launch_bounds__(384, 1)
           }
           // dP(j+1), after dQ(j) has read dS(j) from the same columns
           if (!(ok = mbar_wait_w(&v_full[(j + 1) % C::kVStages], vpar(j + 1), g, kSiteDq | 12u))) break;
-          mma_nt<D>(tDP, kDO, kV((j + 1) % C::kVStages));
+          mma_nt<D>(tDP, kDO, kV((j + 1) % C::kVStages), ks);
           tc_commit_w(dp_full);
           if (it + 2 == cnt) tc_commit_w(do_empty);   // dO_i: last reader issued
         }
@@ -1239,7 +1240,8 @@ cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CU
   const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
   const dim3 grid(static_cast<unsigned>(s.B) * s.H * n_tiles);
   kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s.N, n_tiles, s.B * s.H, s.H,
-                                                 head_band(s.N, s.d), s.scale, scale_log2, drop, wc);
+                                                 head_band(s.N, s.d), s.scale, scale_log2, score_ksteps(s.d), drop,
+                                                 wc);
   return cudaGetLastError();
 }
 
@@ -1255,7 +1257,8 @@ cudaError_t launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
   const dim3 grid(static_cast<unsigned>(s.B) * s.H * n_tiles);
   kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, tdq, lse, Dvec, s.N, n_tiles, s.B * s.H, s.H,
-                                                 head_band(s.N, s.d), s.scale, scale_log2, drop, wc);
+                                                 head_band(s.N, s.d), s.scale, scale_log2, score_ksteps(s.d), drop,
+                                                 wc);
   return cudaGetLastError();
 }
 

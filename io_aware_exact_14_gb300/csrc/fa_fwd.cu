@@ -184,14 +184,16 @@ __device__ __forceinline__ void fwd_producer(const FwdWork& w, uint8_t* smem, ui
 // constants to a base descriptor, keeping the issuing thread's work per MMA
 // to a few instructions (the tensor core's queue is shallow, so a slow issuer
 // starves it).
+// The score product contracts over the true head dim: ks = ceil(d / 16) steps
+// of 16 columns (the zero-filled columns past d would add nothing).
 template <int D>
-__device__ __forceinline__ void fwd_issue_s(uint32_t tmem_d, uint64_t q_desc, uint64_t k_desc) {
+__device__ __forceinline__ void fwd_issue_s(uint32_t tmem_d, uint64_t q_desc, uint64_t k_desc, int ks) {
   using C = FwdCfg<D>;
   constexpr uint32_t idesc = idesc_bf16(128, 128, false, false);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint64_t off = ((kk / 4) * C::kBoxBytes + (kk % 4) * 32) >> 4;
-    tc_mma_ss_w(tmem_d, q_desc + off, k_desc + off, idesc, kk > 0 ? 1u : 0u);
+    if (kk < ks) tc_mma_ss_w(tmem_d, q_desc + off, k_desc + off, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
@@ -214,7 +216,7 @@ __device__ __forceinline__ void fwd_issue_pv(uint32_t tmem_o, uint32_t tmem_p, u
 template <int D>
 __device__ __forceinline__ void fwd_mma(const FwdWork& w, int tile, uint32_t tmem, uint32_t smem_base,
                                         uint64_t* full, uint64_t* empty, uint64_t* q_full, uint64_t* s_full,
-                                        uint64_t* p_full, uint64_t* o_done, const CtaGuard& g) {
+                                        uint64_t* p_full, uint64_t* o_done, int ks, const CtaGuard& g) {
   using C = FwdCfg<D>;
   const int n_t = tile ? w.n1 : w.n0;
   const uint64_t q_desc = sdesc_sw128(smem_base + C::kQOff + tile * C::kTileBytes, 16, 1024);
@@ -230,7 +232,7 @@ __device__ __forceinline__ void fwd_mma(const FwdWork& w, int tile, uint32_t tme
   if (!mbar_wait_w(q_full, 0, g, kSiteFwd | 3u)) return;
   if (!group_wait(0)) return;
   if (n_t > 0) {
-    fwd_issue_s<D>(t_s, q_desc, k_desc0 + slot_off(0));
+    fwd_issue_s<D>(t_s, q_desc, k_desc0 + slot_off(0), ks);
     tc_commit_w(&s_full[tile]);
   }
   tc_commit_w(&empty[0]);   // group 0: K_0
@@ -242,7 +244,7 @@ __device__ __forceinline__ void fwd_mma(const FwdWork& w, int tile, uint32_t tme
       tc_fence_after();
       fwd_issue_pv<D>(t_o, t_s, v_desc0 + slot_off(iv), j > 0);
       if (j + 1 < n_t) {
-        fwd_issue_s<D>(t_s, q_desc, k_desc0 + slot_off(ik));
+        fwd_issue_s<D>(t_s, q_desc, k_desc0 + slot_off(ik), ks);
         tc_commit_w(&s_full[tile]);
       } else {
         tc_commit_w(&o_done[tile]);
@@ -262,7 +264,7 @@ __device__ __forceinline__ void fwd_mma(const FwdWork& w, int tile, uint32_t tme
 template <int D>
 __device__ __forceinline__ void fwd_mma_both(const FwdWork& w, uint32_t tmem, uint32_t smem_base, uint64_t* full,
                                         uint64_t* empty, uint64_t* q_full, uint64_t* s_full, uint64_t* p_full,
-                                        uint64_t* o_done, const CtaGuard& g) {
+                                        uint64_t* o_done, int ks, const CtaGuard& g) {
   using C = FwdCfg<D>;
   const uint64_t q_desc[2] = {sdesc_sw128(smem_base + C::kQOff, 16, 1024),
                               sdesc_sw128(smem_base + C::kQOff + C::kTileBytes, 16, 1024)};
@@ -277,11 +279,11 @@ __device__ __forceinline__ void fwd_mma_both(const FwdWork& w, uint32_t tmem, ui
   if (!mbar_wait_w(q_full, 0, g, kSiteFwd | 3u)) return;
   if (!group_wait(0)) return;
   if (w.n0 > 0) {
-    fwd_issue_s<D>(tmem + C::col_s(0), q_desc[0], k_desc0 + slot_off(0));
+    fwd_issue_s<D>(tmem + C::col_s(0), q_desc[0], k_desc0 + slot_off(0), ks);
     tc_commit_w(&s_full[0]);
   }
   if (w.n1 > 0) {
-    fwd_issue_s<D>(tmem + C::col_s(1), q_desc[1], k_desc0 + slot_off(0));
+    fwd_issue_s<D>(tmem + C::col_s(1), q_desc[1], k_desc0 + slot_off(0), ks);
     tc_commit_w(&s_full[1]);
   }
   tc_commit_w(&empty[0]);   // group 0: K_0
@@ -294,7 +296,7 @@ __device__ __forceinline__ void fwd_mma_both(const FwdWork& w, uint32_t tmem, ui
       if (!mbar_wait_w(&p_full[0], j & 1, g, kSiteFwd | 4u)) return;
       tc_fence_after();
       fwd_issue_pv<D>(tmem + C::col_o(0), tmem + C::col_s(0), vd, j > 0);
-      if (next && j + 1 < w.n0) fwd_issue_s<D>(tmem + C::col_s(0), q_desc[0], kd);
+      if (next && j + 1 < w.n0) fwd_issue_s<D>(tmem + C::col_s(0), q_desc[0], kd, ks);
       if (j == w.n0 - 1) tc_commit_w(&o_done[0]);
       if (next && j + 1 < w.n0) tc_commit_w(&s_full[0]);
     }
@@ -302,7 +304,7 @@ __device__ __forceinline__ void fwd_mma_both(const FwdWork& w, uint32_t tmem, ui
       if (!mbar_wait_w(&p_full[1], j & 1, g, kSiteFwd | 5u)) return;
       tc_fence_after();
       fwd_issue_pv<D>(tmem + C::col_o(1), tmem + C::col_s(1), vd, j > 0);
-      if (next && j + 1 < w.n1) fwd_issue_s<D>(tmem + C::col_s(1), q_desc[1], kd);
+      if (next && j + 1 < w.n1) fwd_issue_s<D>(tmem + C::col_s(1), q_desc[1], kd, ks);
       if (j == w.n1 - 1) tc_commit_w(&o_done[1]);
       if (next && j + 1 < w.n1) tc_commit_w(&s_full[1]);
     }
@@ -507,8 +509,8 @@ __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                   float* __restrict__ lse, int N, int n_pairs, int BH, int H, int band, float scale_log2, int Nk,
-                  int n_qt, int n_kt, int n_splits, int kt_per_split, const __grid_constant__ DropArgs drop,
-                  const WaitCfg wc) {
+                  int n_qt, int n_kt, int n_splits, int kt_per_split, int ks,
+                  const __grid_constant__ DropArgs drop, const WaitCfg wc) {
   static_assert(!SPLIT || (!CAUSAL && ISSUERS == 1), "split-KV launches are non-causal with one issuer");
   static_assert(!(SPLIT && DROPOUT), "split-KV launches have no dropout");
   using C = FwdCfg<D>;
@@ -573,9 +575,9 @@ __global__ void __launch_bounds__(384, 1)
     } else if (warp == 9 || (ISSUERS == 2 && warp == 10)) {
       // issuing warps (warp 9 also owns TMEM): whole-warp loops, one elected lane issues
       if (ISSUERS == 2)
-        fwd_mma<D>(w, warp - 9, tmem, smem_u32(smem), full, empty, q_full, s_full, p_full, o_done, g);
+        fwd_mma<D>(w, warp - 9, tmem, smem_u32(smem), full, empty, q_full, s_full, p_full, o_done, ks, g);
       else
-        fwd_mma_both<D>(w, tmem, smem_u32(smem), full, empty, q_full, s_full, p_full, o_done, g);
+        fwd_mma_both<D>(w, tmem, smem_u32(smem), full, empty, q_full, s_full, p_full, o_done, ks, g);
       tc_commit_w(drain);  // every MMA issued above has finished before TMEM is released
       mbar_drain(drain, 0);
       __syncwarp();
@@ -613,8 +615,8 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
   const dim3 grid(static_cast<unsigned>(s.B) * s.H * n_pairs);
   kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, to, lse, s.N, n_pairs, s.B * s.H, s.H,
-                                                 head_band(s.N, s.d), scale_log2, s.N, n_qt, n_qt, 1, n_qt, drop,
-                                                 wc);
+                                                 head_band(s.N, s.d), scale_log2, s.N, n_qt, n_qt, 1, n_qt,
+                                                 score_ksteps(s.d), drop, wc);
   return cudaGetLastError();
 }
 
@@ -693,7 +695,8 @@ cudaError_t launch_fwd_splitkv_t(const CUtensorMap& tq, const CUtensorMap& tk, c
     const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
     const dim3 grid(static_cast<unsigned>(BH) * n_splits * n_qt);
     kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, top, lse_part, s.N, n_qt, BH, s.H, 1, scale_log2,
-                                                   Nk, n_qt, n_kt, n_splits, kt_per_split, no_drop_args(), wc);
+                                                   Nk, n_qt, n_kt, n_splits, kt_per_split, score_ksteps(s.d),
+                                                   no_drop_args(), wc);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   const long long rows = static_cast<long long>(BH) * s.N;

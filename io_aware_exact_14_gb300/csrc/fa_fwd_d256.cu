@@ -1,0 +1,428 @@
+// Forward pass for wide heads (128 < d <= 256, kernel built for D = 256) on
+// sm_103a: the same method as fa_fwd.cu -- query tile on chip, K/V tiles
+// streamed, running (m, l, acc) with one division by l at the end
+// ("为什么Flash Attention能将注意力计算提速数倍而不损失精度", sections
+// "分块计算（Tiling）" and "在线Softmax技巧"; "FlashAttention的Triton实现：
+// IO-aware注意力机制底层原理", section "分块策略：SRAM容量限制下的精打细算", which
+// sizes the blocks from the on-chip budget and the head dim).
+//
+// Why a kernel of its own: at D = 256 one query tile's O accumulator takes
+// 256 of the 512 TMEM columns, so a CTA holds one query tile (not two), and a
+// 128 x 256 bf16 K or V tile is 64 KB, so the ring moves d-halves.
+//
+// GB300 design (one CTA per SM, 192 threads):
+//   warps 0-3  softmax (thread = query row = TMEM lane)
+//   warp  4    TMA producer: Q once (4 boxes), then K/V d-halves ("units",
+//              128 rows x 128 columns = 32 KB) through a 5-slot ring
+//   warp  5    TMEM owner and tcgen05.mma issuer (elect.sync in a converged warp)
+// TMEM: S buffers [0,128) and [128,256) (key step j uses buffer j & 1, so
+// S(j+1) is computed while the softmax works on S(j)); O [256, 512).
+// P (bf16) overwrites the first 64 columns of its S buffer and feeds
+// O += P V from TMEM, one 128-column half of O per V unit.
+// Tiles stream in the order the products need them: K_0 K_1 V_0 K_2 V_1 ...
+// K_{n-1} V_{n-2} V_{n-1}; each tile is two units (d-halves), each unit lands
+// on its slot's barrier, and one commit per tile releases both units.
+// Lazy rescaling as in fa_fwd.cu: a row keeps its reference max until a block
+// exceeds it by more than 2^8; O is rescaled in TMEM only when some row of
+// the warp moves, after the previous P V product has completed.
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+
+#include <cmath>
+
+namespace fa {
+namespace {
+
+__device__ unsigned int g_status_fwd256[2] = {0, 0};   // status, abort epoch (see CtaGuard)
+
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr uint32_t kSiteFwd256 = 0x400;
+
+struct F256 {
+  static constexpr uint32_t kBoxBytes = 128u * 128u;       // 128 rows x 64 bf16 (128 B, swizzled)
+  static constexpr uint32_t kUnitBytes = 2 * kBoxBytes;    // 128 rows x 128 bf16: one d-half
+  static constexpr int kSlots = 5;
+  static constexpr int kTileBars = 4;
+  static constexpr uint32_t kQOff = 0;                     // 4 boxes; O staging at the end
+  static constexpr uint32_t kSlotOff = 4 * kBoxBytes;
+  static constexpr uint32_t kBarOff = kSlotOff + kSlots * kUnitBytes;
+  // full[kSlots], empty[kTileBars], q_full, s_full[2], p_full, o_ready, staged, drain
+  static constexpr int kBars = kSlots + kTileBars + 7;
+  static constexpr uint32_t kMiscOff = kBarOff + kBars * 8;   // tmem holder, abort flag
+  static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;   // + alignment slack
+  static_assert(kSmemBytes <= 232448, "shared-memory budget");
+  static constexpr int kThreads = 192;
+  static constexpr uint32_t kColO = 256;
+};
+
+// Stream position t (0 .. 2n-1) -> (K or V, key tile j): K_0 K_1 V_0 K_2 V_1 ...
+// K_{n-1} V_{n-2} V_{n-1}; and the positions of K_j and V_j.
+__device__ __forceinline__ void stream_tile(int t, int n, bool& is_v, int& j) {
+  if (t == 0) {
+    is_v = false;
+    j = 0;
+  } else if (t == 2 * n - 1) {
+    is_v = true;
+    j = n - 1;
+  } else if (t & 1) {
+    is_v = false;
+    j = (t + 1) >> 1;
+  } else {
+    is_v = true;
+    j = (t - 2) >> 1;
+  }
+}
+__device__ __forceinline__ int pos_k(int j) { return j == 0 ? 0 : 2 * j - 1; }
+__device__ __forceinline__ int pos_v(int j, int n) { return j == n - 1 ? 2 * n - 1 : 2 * j + 2; }
+
+// A CTA's work: head bh (hc for the 4-D maps), query tile qt, key tiles 0..n-1.
+struct W256 {
+  int bh, qt, n;
+  HeadCoord hc;
+};
+
+__device__ __forceinline__ W256 w256_work(int N, int n_qt, int BH, int H, int band, bool causal) {
+  W256 w;
+  int rank;
+  banded_order(blockIdx.x, n_qt, BH, band, w.bh, rank);
+  w.hc = head_coord(w.bh, H);
+  w.qt = causal ? n_qt - 1 - rank : rank;   // causal: heavy (long-row) tiles first
+  w.n = causal ? w.qt + 1 : n_qt;
+  (void)N;
+  return w;
+}
+
+__device__ void f256_producer(const W256& w, uint8_t* smem, uint64_t* full, uint64_t* empty, uint64_t* q_full,
+                              const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
+                              const CtaGuard& g) {
+  using C = F256;
+  mbar_arrive_expect_tx(q_full, 4 * C::kBoxBytes);
+#pragma unroll
+  for (int b = 0; b < 4; ++b) tma_load_hd(smem + C::kQOff + b * C::kBoxBytes, tmQ, q_full, 64 * b, 128 * w.qt, w.hc);
+  const int units = 4 * w.n;
+  int issued = 0;
+  for (int u = 0; u < units; ++u) {
+    const int t = u >> 1, h = u & 1, slot = u % C::kSlots;
+    if (u >= C::kSlots) {   // the slot's previous unit belongs to tile (u - kSlots) / 2: wait for its release
+      const int pt = (u - C::kSlots) >> 1;
+      if (!mbar_wait(&empty[pt % C::kTileBars], (pt / C::kTileBars) & 1, g, kSiteFwd256 | 1u)) break;
+    }
+    bool is_v;
+    int j;
+    stream_tile(t, w.n, is_v, j);
+    uint8_t* dst = smem + C::kSlotOff + slot * C::kUnitBytes;
+    mbar_arrive_expect_tx(&full[slot], C::kUnitBytes);
+#pragma unroll
+    for (int b = 0; b < 2; ++b)
+      tma_load_hd(dst + b * C::kBoxBytes, is_v ? tmV : tmK, &full[slot], 128 * h + 64 * b, 128 * j, w.hc);
+    issued = u + 1;
+  }
+  if (issued < units) {   // unwinding: let the copies in flight land before shared memory is released
+    mbar_drain(q_full, 0);
+    for (int u = (issued > C::kSlots ? issued - C::kSlots : 0); u < issued; ++u)
+      mbar_drain(&full[u % C::kSlots], (u / C::kSlots) & 1);
+  }
+}
+
+// Descriptor offset of K step kk (16 columns) inside a 2-box unit (K-major).
+__device__ __forceinline__ uint64_t kstep_off(int kk) {
+  return static_cast<uint64_t>(((kk / 4) * F256::kBoxBytes + (kk % 4) * 32) >> 4);
+}
+
+// The MMA warp: S(0) S(1) | PV(0) S(2) | PV(1) S(3) | ... | PV(n-1).
+// ks = ceil(d / 16) steps of 16 columns hold data (9..16 here).
+__device__ void f256_mma(const W256& w, uint32_t tmem, uint32_t sbase, uint64_t* full, uint64_t* empty,
+                         uint64_t* q_full, uint64_t* s_full, uint64_t* p_full, uint64_t* o_ready, int ks,
+                         const CtaGuard& g) {
+  using C = F256;
+  constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
+  constexpr uint32_t idesc_pv = idesc_bf16(128, 128, false, true);
+  const uint64_t qd0 = sdesc_sw128(sbase + C::kQOff, 16, 1024);
+  const uint64_t qd1 = sdesc_sw128(sbase + C::kQOff + C::kUnitBytes, 16, 1024);
+  const uint64_t kd0 = sdesc_sw128(sbase + C::kSlotOff, 16, 1024);            // slot 0, K-major
+  const uint64_t vd0 = sdesc_sw128(sbase + C::kSlotOff, C::kBoxBytes, 1024);  // slot 0, MN-major
+  auto slot_off = [](int u) { return static_cast<uint64_t>((u % C::kSlots) * (C::kUnitBytes >> 4)); };
+  auto unit_wait = [&](int u) {
+    return mbar_wait_w(&full[u % C::kSlots], (u / C::kSlots) & 1, g, kSiteFwd256 | 2u);
+  };
+  auto issue_s = [&](int buf, int t) -> bool {   // S into buffer `buf` from the K tile at stream position t
+    const uint32_t ts = tmem + 128u * buf;
+    for (int h = 0; h < 2; ++h) {
+      if (!unit_wait(2 * t + h)) return false;
+      const uint64_t q = h ? qd1 : qd0, k = kd0 + slot_off(2 * t + h);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        if (8 * h + kk < ks) tc_mma_ss_w(ts, q + kstep_off(kk), k + kstep_off(kk), idesc_s, (h | kk) ? 1u : 0u);
+    }
+    tc_commit_w(&s_full[buf]);
+    tc_commit_w(&empty[t % C::kTileBars]);
+    return true;
+  };
+  if (!mbar_wait_w(q_full, 0, g, kSiteFwd256 | 3u)) return;
+  if (!issue_s(0, pos_k(0))) return;
+  if (w.n > 1 && !issue_s(1, pos_k(1))) return;
+  for (int j = 0; j < w.n; ++j) {
+    const int t = pos_v(j, w.n), buf = j & 1;
+    if (!unit_wait(2 * t) || !unit_wait(2 * t + 1)) return;
+    if (!mbar_wait_w(p_full, j & 1, g, kSiteFwd256 | 4u)) return;
+    tc_fence_after();
+    const uint32_t tp = tmem + 128u * buf;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint64_t v = vd0 + slot_off(2 * t + h);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)   // 128 keys, 16 per MMA; P packs 2 keys per TMEM column
+        tc_mma_ts_w(tmem + C::kColO + 128u * h, tp + kk * 8, v + ((kk * 2048) >> 4), idesc_pv,
+                    (j > 0 || kk > 0) ? 1u : 0u);
+    }
+    tc_commit_w(o_ready);
+    tc_commit_w(&empty[t % C::kTileBars]);
+    if (j + 2 < w.n && !issue_s(buf, pos_k(j + 2))) return;
+  }
+}
+
+template <bool CAUSAL>
+__device__ void f256_softmax(const W256& w, uint32_t tmem, uint8_t* smem, uint64_t* s_full, uint64_t* p_full,
+                             uint64_t* o_ready, uint64_t* staged, const CUtensorMap* tmO, float* __restrict__ lse,
+                             int N, int d, float scale_log2, const CtaGuard& g) {
+  using C = F256;
+  const int r = threadIdx.x & 127;
+  const int row = w.qt * 128 + r;
+  const uint32_t lane_base = static_cast<uint32_t>((threadIdx.x >> 5) & 3) * 32u << 16;
+  const uint32_t tO = tmem + lane_base + C::kColO;
+
+  float m_use = -INFINITY;  // reference max, base-2 units
+  float l = 0.f;
+  for (int j = 0; j < w.n; ++j) {
+    const int buf = j & 1;
+    const uint32_t tS = tmem + lane_base + 128u * buf;
+    if (!mbar_wait(&s_full[buf], (j >> 1) & 1, g, kSiteFwd256 | 6u)) return;
+    __syncwarp();
+    tc_fence_after();
+    uint32_t s[4][32];
+    tmem_ld32(tS + 0, s[0]);
+    tmem_ld32(tS + 32, s[1]);
+    tmem_ld32(tS + 64, s[2]);
+    tmem_ld32(tS + 96, s[3]);
+    tmem_ld_wait(s[0]);
+    tmem_ld_fence(s[1]);
+    tmem_ld_fence(s[2]);
+    tmem_ld_fence(s[3]);
+
+    const int kv0 = j * 128;
+    int lim = N - kv0;
+    if (CAUSAL) lim = min(lim, row - kv0 + 1);
+    if (lim < 128) {
+#pragma unroll
+      for (int c = 0; c < 128; ++c)
+        if (c >= lim) s[c / 32][c % 32] = __float_as_uint(-INFINITY);
+    }
+    float mx[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < 128; c += 2)
+      mx[(c / 2) % 8] = max3f(mx[(c / 2) % 8], __uint_as_float(s[c / 32][c % 32]),
+                              __uint_as_float(s[(c + 1) / 32][(c + 1) % 32]));
+    const float row_max =
+        fmaxf(max3f(mx[0], mx[1], mx[2]), max3f(max3f(mx[3], mx[4], mx[5]), mx[6], mx[7])) * scale_log2;
+
+    bool rescale = false;
+    float corr = 1.f;
+    if (j == 0) {
+      m_use = row_max;   // O is overwritten by the first P V product
+    } else {
+      const bool need = row_max > m_use + kRescaleThreshold;
+      rescale = __any_sync(0xffffffffu, need);
+      if (rescale) {
+        const float m_new = need ? row_max : m_use;
+        corr = (m_use == -INFINITY) ? 0.f : ex2_approx(m_use - m_new);
+        l *= corr;
+        m_use = m_new;
+      }
+    }
+    const float m_off = (m_use == -INFINITY) ? 0.f : m_use;
+    const float2 sc2 = make_float2(scale_log2, scale_log2), mo2 = make_float2(-m_off, -m_off);
+    float2 sum[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sum[i] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {  // keys [64h, 64h+64) -> P columns [32h, 32h+32)
+      uint32_t pk[32];
+#pragma unroll
+      for (int c = 64 * h; c < 64 * h + 64; c += 2) {
+        const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[c / 32][c % 32]),
+                                                __uint_as_float(s[(c + 1) / 32][(c + 1) % 32])),
+                                    sc2, mo2);
+        const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+        sum[(c / 2) % 4] = __fadd2_rn(sum[(c / 2) % 4], pp);
+        pk[(c / 2) % 32] = pack_bf16x2(pp.x, pp.y);
+      }
+      tmem_st32(tS + 32 * h, pk);
+    }
+    const float2 s01 = __fadd2_rn(sum[0], sum[1]), s23 = __fadd2_rn(sum[2], sum[3]);
+    const float2 s0123 = __fadd2_rn(s01, s23);
+    l += s0123.x + s0123.y;
+    if (j > 0) {
+      // O may be touched only once the previous P V product has completed
+      if (!mbar_wait(o_ready, (j - 1) & 1, g, kSiteFwd256 | 5u)) return;
+      __syncwarp();
+      tc_fence_after();
+      if (rescale) {
+#pragma unroll 1
+        for (int c = 0; c < 256; c += 32) {
+          uint32_t o[32];
+          tmem_ld32(tO + c, o);
+          tmem_ld_wait(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
+          tmem_st32(tO + c, o);
+        }
+      }
+    }
+    tmem_st_wait();
+    tc_fence_before();
+    mbar_arrive(p_full);
+  }
+
+  // epilogue: O = acc / l -> bf16 -> swizzled staging in the Q buffer (its last
+  // reader, S(n-1), has completed) -> TMA store of the boxes holding columns < d
+  if (!mbar_wait(o_ready, (w.n - 1) & 1, g, kSiteFwd256 | 7u)) return;
+  __syncwarp();
+  tc_fence_after();
+  const float inv_l = l > 0.f ? 1.f / l : 0.f;
+  const uint32_t stage = smem_u32(smem + C::kQOff);
+#pragma unroll 1
+  for (int c = 0; c < 256; c += 32) {
+    uint32_t o[32];
+    tmem_ld32(tO + c, o);
+    tmem_ld_wait(o);
+    const uint32_t box = stage + (c / 64) * C::kBoxBytes + r * 128;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int chunk = (c % 64) / 8 + q;
+      float f[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(o[8 * q + e]) * inv_l;
+      st_shared_v4(box + ((chunk ^ (r & 7)) << 4), pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                   pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+    }
+  }
+  fence_proxy_async_smem();
+  mbar_arrive(staged);
+  if (r == 0 && mbar_wait(staged, 0, g, kSiteFwd256 | 8u)) {
+    for (int b = 0; b < 4; ++b)
+      if (64 * b < d) tma_store_hd(tmO, smem + C::kQOff + b * C::kBoxBytes, 64 * b, w.qt * 128, w.hc);
+    tma_store_commit();
+    tma_store_wait_read_all();
+  }
+  if (row < N) lse[static_cast<size_t>(w.bh) * N + row] = l > 0.f ? (m_use + __log2f(l)) * kLn2 : -INFINITY;
+}
+
+template <bool CAUSAL>
+__global__ void __launch_bounds__(192, 1)
+    fa_fwd_d256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                       float* __restrict__ lse, int N, int d, int n_qt, int BH, int H, int band, float scale_log2,
+                       int ks, const WaitCfg wc) {
+  using C = F256;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+  uint64_t* full = bars;                     // [kSlots]
+  uint64_t* empty = full + C::kSlots;        // [kTileBars]
+  uint64_t* q_full = empty + C::kTileBars;
+  uint64_t* s_full = q_full + 1;             // [2]
+  uint64_t* p_full = s_full + 2;
+  uint64_t* o_ready = p_full + 1;
+  uint64_t* staged = o_ready + 1;
+  uint64_t* drain = staged + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kMiscOff + 4);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const W256 w = w256_work(N, n_qt, BH, H, band, CAUSAL);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kSlots; ++i) mbar_init(&full[i], 1);
+    for (int i = 0; i < C::kTileBars; ++i) mbar_init(&empty[i], 1);
+    mbar_init(q_full, 1);
+    mbar_init(&s_full[0], 1);
+    mbar_init(&s_full[1], 1);
+    mbar_init(p_full, 128);
+    mbar_init(o_ready, 1);
+    mbar_init(staged, 128);
+    mbar_init(drain, 1);
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(tmem_holder, 512);
+    tmem_relinquish();
+  }
+  if (warp == 4 && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmO);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const CtaGuard g{abort_flag, g_status_fwd256, wc.epoch, wc.limit_us};
+
+  if (warp == 4) {
+    if (lane == 0) f256_producer(w, smem, full, empty, q_full, &tmQ, &tmK, &tmV, g);
+  } else if (warp == 5) {
+    f256_mma(w, tmem, smem_u32(smem), full, empty, q_full, s_full, p_full, o_ready, ks, g);
+    tc_commit_w(drain);   // every MMA issued above has finished before TMEM is released
+    mbar_drain(drain, 0);
+    __syncwarp();
+    tc_fence_before();
+    named_bar_sync(1, 160);
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  } else {
+    f256_softmax<CAUSAL>(w, tmem, smem, s_full, p_full, o_ready, staged, &tmO, lse, N, d, scale_log2, g);
+    __syncwarp();
+    tc_fence_before();
+    named_bar_sync(1, 160);
+  }
+}
+
+template <bool CAUSAL>
+cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
+                     float* lse, const Shape& s, const WaitCfg& wc, cudaStream_t st) {
+  using C = F256;
+  auto kern = fa_fwd_d256_kernel<CAUSAL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int n_qt = (s.N + 127) / 128;
+  const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
+  const dim3 grid(static_cast<unsigned>(s.B) * s.H * n_qt);
+  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, to, lse, s.N, s.d, n_qt, s.B * s.H, s.H,
+                                                 head_band(s.N, s.d), scale_log2, score_ksteps(s.d), wc);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_d256(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& to, float* lse, const Shape& s, const WaitCfg& wc, cudaStream_t st) {
+  return s.causal ? launch_t<true>(tq, tk, tv, to, lse, s, wc, st) : launch_t<false>(tq, tk, tv, to, lse, s, wc, st);
+}
+
+cudaError_t fwd_d256_status(uint32_t* out, bool reset) {
+  unsigned int v[2] = {0, 0};
+  cudaError_t e = cudaMemcpyFromSymbol(v, g_status_fwd256, sizeof(v));
+  if (e != cudaSuccess) return e;
+  *out = v[0];
+  if (reset && (v[0] | v[1]) != 0) {
+    const unsigned int z[2] = {0, 0};
+    e = cudaMemcpyToSymbol(g_status_fwd256, z, sizeof(z));
+  }
+  return e;
+}
+
+}  // namespace fa

@@ -62,11 +62,16 @@ constexpr uint32_t kDefaultWaitLimitUs = 4000000;   // 4 s
 // The next launch's configuration: a fresh epoch, the default limit, no hook.
 WaitCfg next_wait_cfg();
 
-// Head dims: any multiple of 8 from 8 to 128 runs in the kernel built for
-// D = 64 (d <= 64) or D = 128.  The tensor maps carry the true extent d, so
-// TMA loads fill columns d .. D-1 of every tile with zeros (they add nothing
-// to Q K^T, and P V gives zeros there) and TMA stores clip them.
-inline int kernel_dim(int d) { return d > 64 ? 128 : 64; }
+// Head dims: any multiple of 8 from 8 to 256 runs in the kernel built for
+// D = 64 (d <= 64), D = 128 (d <= 128) or D = 256.  The tensor maps carry the
+// true extent d, so TMA loads fill columns d .. D-1 of every tile with zeros
+// (they add nothing to Q K^T, and P V gives zeros there) and TMA stores clip
+// them.
+inline int kernel_dim(int d) { return d > 128 ? 256 : (d > 64 ? 128 : 64); }
+constexpr int kMaxHeadDim = 256;
+// Products that contract over the head dim (Q K^T, dO V^T and their
+// transposes) issue only the ceil(d / 16) steps of 16 columns that hold data.
+inline int score_ksteps(int d) { return (d + 15) / 16; }
 
 // Element strides of a [B, H, N, d] bf16 view (d contiguous).
 struct Strides {
@@ -81,6 +86,11 @@ inline Strides contiguous_strides(const Shape& s) {
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to, float* lse, const Shape& s, const DropArgs& drop, const WaitCfg& wc,
                        cudaStream_t st);
+
+// Forward for wide heads (128 < d <= 256): one query tile per CTA, K/V
+// d-halves through a ring (fa_fwd_d256.cu).  Same maps as launch_fwd.
+cudaError_t launch_fwd_d256(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& to, float* lse, const Shape& s, const WaitCfg& wc, cudaStream_t st);
 
 // Split-KV forward for short query blocks against long key sequences
 // (non-causal): Q maps {d, Nq, H, B} (s.N = Nq), K/V maps {d, Nk, H, B}; each
@@ -184,5 +194,6 @@ inline int head_band(int N, int d) {
 cudaError_t fwd_status(uint32_t* out, bool reset);
 cudaError_t bwd_status(uint32_t* out, bool reset);
 cudaError_t fp8_status(uint32_t* out, bool reset);
+cudaError_t fwd_d256_status(uint32_t* out, bool reset);
 
 }  // namespace fa

@@ -94,10 +94,11 @@ __device__ __forceinline__ bool guard_expired(const CtaGuard& g, unsigned long l
 // one copy, which keeps the hot loops around them compact in the instruction
 // cache.  A translation unit whose warps change their register budget with
 // setmaxnreg (which out-of-line calls cannot follow) defines FA_INLINE_WAITS.
+// Internal linkage either way: several translation units include this header.
 #ifdef FA_INLINE_WAITS
-#define FA_WAIT_LINKAGE __forceinline__
+#define FA_WAIT_LINKAGE static __forceinline__
 #else
-#define FA_WAIT_LINKAGE __noinline__
+#define FA_WAIT_LINKAGE static __noinline__
 #endif
 
 // Wait for the phase of `bar` with the given parity.  Returns false (without

@@ -50,8 +50,8 @@ def fwd(lib, q=FAKE, k=FAKE + 0x100000, v=FAKE + 0x200000, o=FAKE + 0x300000, ls
 
 def test_fwd_argument_checks(lib):
     assert fwd(lib, d=100) == 2           # FA_ERR_UNSUPPORTED: not a multiple of 8
-    assert fwd(lib, d=136) == 2           # above 128
-    assert fwd(lib, d=256) == 2
+    assert fwd(lib, d=264) == 2           # above 256
+    assert fwd(lib, d=260) == 2
     assert fwd(lib, d=4) == 2
     assert fwd(lib, d=0) == 2
     assert fwd(lib, N=0, q=0, k=0, v=0, o=0, lse=0) == 0  # empty problem is a no-op
@@ -86,6 +86,7 @@ def test_bwd_argument_checks(lib):
                           a["B"], a["H"], a["N"], a["d"], a["scale"], a["causal"], a["ws"], a["wsb"], None)
 
     assert bwd(d=84) == 2
+    assert bwd(d=264) == 2
     assert bwd(N=0, q=0) == 0
     assert bwd(dq=0) == 1
     assert bwd(do=BAD_ALIGN) == 1

@@ -1,8 +1,8 @@
-"""Head dims other than 64 and 128 (any multiple of 8 up to 128) on the GPU
-against the fp64 oracle: they run in the d = 64 or d = 128 kernels with the
-tensor maps' true extent, so the columns past d are zero-filled on load and
-clipped on store; the sentinel tests check that no byte past column d of
-any output row is written."""
+"""Head dims other than 64 and 128 on the GPU against the fp64 oracle: any
+multiple of 8 up to 128 runs in the d = 64 or d = 128 kernels and 136 to 256
+in the wide-head (d = 256) kernels, with the tensor maps' true extent, so the
+columns past d are zero-filled on load and clipped on store; the sentinel
+tests check that no byte past column d of any output row is written."""
 import numpy as np
 import pytest
 import torch
@@ -16,7 +16,10 @@ pytestmark = pytest.mark.gpu
 
 FWD = [(1, 2, 300, 8, True), (2, 1, 257, 16, False), (1, 3, 200, 32, True), (1, 1, 129, 40, False),
        (2, 2, 384, 48, True), (1, 2, 333, 72, False), (1, 1, 500, 80, True), (2, 2, 256, 96, True),
-       (1, 2, 1000, 96, False), (1, 1, 17, 112, True), (1, 2, 640, 120, False)]
+       (1, 2, 1000, 96, False), (1, 1, 17, 112, True), (1, 2, 640, 120, False),
+       # wide heads: one query tile per CTA, K/V moved as d-halves
+       (1, 1, 128, 256, False), (1, 2, 300, 256, True), (2, 1, 1000, 256, False), (1, 2, 777, 192, True),
+       (1, 1, 1, 256, True), (1, 3, 129, 136, False), (1, 1, 2100, 256, True), (1, 2, 512, 224, False)]
 BWD = [(1, 2, 300, 8, True), (1, 3, 200, 32, False), (2, 1, 384, 48, True), (1, 2, 333, 80, False),
        (2, 2, 256, 96, True), (1, 1, 1000, 96, True), (1, 2, 129, 120, False)]
 
@@ -107,3 +110,37 @@ def test_dropout_head_dim():
     ref = oracle.attn_bwd_dropout_ref(f64(x["q"]), f64(x["k"]), f64(x["v"]), f64(x["do"]), scale, True, p, seed, 2)
     for name, a, b in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
         assert oracle.rel_fro_err(f64(a), b) <= TOL_GRAD, name
+
+
+def test_wide_head_forward_leaves_columns_past_d_untouched():
+    """d = 192 in the d = 256 kernel: the fourth 64-column box of each O row is
+    never stored, and the strided call equals the contiguous one bit for bit."""
+    B, H, N, d, causal = 1, 2, 300, 192, True
+    _, g = device_inputs(B, H, N, d, seed=780)
+    o_c, lse_c = fa.fa_fwd(g["q"], g["k"], g["v"], None, causal)
+    buf = torch.full((B, H, N, 256), 7.0, dtype=torch.bfloat16, device="cuda")
+    o = buf[..., :d]
+    lse = torch.empty_like(lse_c)
+    fa.fa_fwd_strided(g["q"], g["k"], g["v"], None, causal, out=o, lse=lse)
+    torch.cuda.synchronize()
+    assert_no_timeout()
+    assert torch.all(buf[..., d:] == 7.0)
+    assert torch.equal(o, o_c) and torch.equal(lse, lse_c)
+
+
+def test_wide_head_long_rows_sampled():
+    """B=2 H=4 N=4096 d=256 causal and not: 64 sampled query rows per head."""
+    from io_aware_exact_14_gb300.workloads import Workload, sample_rows
+    for causal in (False, True):
+        w = Workload(0, "wide", 2, 4, 4096, 256, (causal,), ("fwd",), oracle_rows=64)
+        x, g = device_inputs(w.B, w.H, w.N, w.d, seed=790 + causal)
+        o, lse = fa.fa_fwd(g["q"], g["k"], g["v"], w.scale, causal)
+        torch.cuda.synchronize()
+        assert_no_timeout()
+        rows = sample_rows(w, 64)
+        o_ref, lse_ref = oracle.attn_fwd_ref_rows(f64(x["q"]), f64(x["k"]), f64(x["v"]), w.scale, causal, rows)
+        o_np, l_np = f64(o), f64(lse)
+        got_o = np.stack([np.stack([o_np[b, h, rows[b, h]] for h in range(w.H)]) for b in range(w.B)])
+        got_l = np.stack([np.stack([l_np[b, h, rows[b, h]] for h in range(w.H)]) for b in range(w.B)])
+        assert o_excess_err(got_o, o_ref) <= TOL_O
+        assert oracle.lse_max_abs_err(got_l, lse_ref) <= TOL_LSE

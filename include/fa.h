@@ -11,12 +11,15 @@
  * Conventions shared by every entry point
  *   - Tensors are row-major, contiguous, [B, H, N, d] bf16 (d innermost);
  *     row statistics (LSE, D) are [B, H, N] fp32.  Q, K, V share one N.
- *   - d must be a multiple of 8 from 8 to 128, else FA_ERR_UNSUPPORTED
- *     (d <= 64 runs the d = 64 kernels and 64 < d <= 128 the d = 128 ones,
- *     at their cost: the missing columns are zero-filled on chip, never
- *     read from or written to memory).  N >= 0; N == 0 is a
- *     no-op that returns FA_OK.  B, H >= 1.  B*H*ceil(N/128) must fit in
- *     2^31 - 1.
+ *   - d must be a multiple of 8 from 8 to 256 for fa_fwd, fa_fwd_strided,
+ *     fa_bwd, fa_bwd_strided, the three backward steps and fa_bwd_noalloc,
+ *     and from 8 to 128 for the dropout, split-KV and FP8 entry points;
+ *     else FA_ERR_UNSUPPORTED.  d <= 64 runs the d = 64 kernels, 64 < d <=
+ *     128 the d = 128 ones and 128 < d <= 256 the wide-head (d = 256) ones:
+ *     the missing columns are zero-filled on chip, never read from or
+ *     written to memory, and the products that contract over d skip the
+ *     all-zero 16-column steps.  N >= 0; N == 0 is a no-op that returns
+ *     FA_OK.  B, H >= 1.  B*H*ceil(N/128) must fit in 2^31 - 1.
  *   - Every device pointer must be 16-byte aligned (fp32 vectors: 4-byte),
  *     outputs must not overlap inputs or each other; otherwise
  *     FA_ERR_INVALID_ARG.  The library never writes its inputs.
@@ -48,7 +51,7 @@ struct CUstream_st; /* cudaStream_t and CUstream are both `struct CUstream_st *`
 typedef enum {
   FA_OK = 0,
   FA_ERR_INVALID_ARG = 1,  /* null/misaligned/overlapping pointer, bad size or scale */
-  FA_ERR_UNSUPPORTED = 2,  /* head dim not a multiple of 8 in [8, 128], or sizes beyond the limits */
+  FA_ERR_UNSUPPORTED = 2,  /* head dim not a multiple of 8 in the entry point's range, or sizes beyond the limits */
   FA_ERR_CUDA = 3,         /* a CUDA runtime/driver call or a launch failed */
   FA_ERR_WORKSPACE = 4,    /* workspace missing, misaligned or too small */
   FA_ERR_TIMEOUT = 5       /* a kernel gave up on a wait (see fa_debug_status) */
@@ -140,7 +143,10 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
  * the forward definition (the pages give none):
  *   dV = P^T dO, dP = dO V^T, D_i = sum_c dO_ic O_ic,
  *   dS = P o (dP - D), dQ = scale dS K, dK = scale dS^T Q.
- * Runs fa_bwd_preprocess, fa_bwd_dkdv and fa_bwd_dq in that order on `stream`.
+ * Runs fa_bwd_preprocess, fa_bwd_dkdv and fa_bwd_dq in that order on `stream`
+ * (for d > 128, fa_bwd_dkdv is two launches, dV then dK: one CTA's tensor
+ * memory holds one 128 x 256 fp32 accumulator next to its score tiles, so
+ * the dK launch recomputes the scores the dV launch used).
  *   q, k, v, o, dO in : bf16 [B, H, N, d]; o and lse from fa_fwd
  *   lse            in : fp32 [B, H, N]
  *   dq, dk, dv     out: bf16 [B, H, N, d]

@@ -104,12 +104,12 @@ fa_status check_disjoint(std::initializer_list<Span> outs, std::initializer_list
 // `st` (d contiguous); boxes of 64 x 128 rows with the 128-byte swizzle the
 // tensor-core descriptors expect.  Rows past N and columns past d read as
 // zero and are clipped on store.
-fa_status make_map(CUtensorMap* m, const void* base, const Shape& s, const Strides& st) {
+fa_status make_map(CUtensorMap* m, const void* base, const Shape& s, const Strides& st, unsigned box_rows = 128) {
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(s.d), static_cast<cuuint64_t>(s.N),
                               static_cast<cuuint64_t>(s.H), static_cast<cuuint64_t>(s.B)};
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(st.n) * 2, static_cast<cuuint64_t>(st.h) * 2,
                                  static_cast<cuuint64_t>(st.b) * 2};
-  const cuuint32_t box[4] = {64, 128, 1, 1};
+  const cuuint32_t box[4] = {64, box_rows, 1, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
                               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -297,10 +297,37 @@ fa_status read_dropout(const fa_dropout* in, fa::DropArgs& out) {
   return FA_OK;
 }
 
+// Wide heads (d > 128): every map the three launches use; `which` = 0 for
+// the dK/dV maps, 1 for the dQ maps (outputs not in use stay unencoded).
+fa_status wide_maps(fa::WideBwdMaps& m, const void* q, const void* k, const void* v, const void* dO, void* dq,
+                    void* dk, void* dv, const Shape& s, const BwdStrides& t, int which) {
+  if (which == 0) {
+    FA_TRY(make_map(&m.k128, k, s, t.k));
+    FA_TRY(make_map(&m.v128, v, s, t.v));
+    FA_TRY(make_map(&m.q64, q, s, t.q, 64));
+    FA_TRY(make_map(&m.do64, dO, s, t.dO, 64));
+    FA_TRY(make_map(&m.dk128, dk, s, t.dk));
+    FA_TRY(make_map(&m.dv128, dv, s, t.dv));
+  } else {
+    FA_TRY(make_map(&m.q128, q, s, t.q));
+    FA_TRY(make_map(&m.do128, dO, s, t.dO));
+    FA_TRY(make_map(&m.k64, k, s, t.k, 64));
+    FA_TRY(make_map(&m.v64, v, s, t.v, 64));
+    FA_TRY(make_map(&m.dq128, dq, s, t.dq));
+  }
+  return FA_OK;
+}
+
 fa_status dkdv_checked(const void* q, const void* k, const void* v, const float* lse, const void* dO,
                        const float* Dvec, void* dk, void* dv, const Shape& s, const BwdStrides& t,
                        cudaStream_t st, const fa::DropArgs& drop = kNoDrop) {
   if (!load_encoder()) return FA_ERR_CUDA;
+  if (s.d > 128) {
+    if (drop.t4 != 0) return FA_ERR_UNSUPPORTED;
+    fa::WideBwdMaps m;
+    FA_TRY(wide_maps(m, q, k, v, dO, nullptr, dk, dv, s, t, 0));
+    return cuda_status(fa::launch_bwd_d256_dkdv(m, lse, Dvec, s, st), "wide-head dK/dV kernel launch");
+  }
   CUtensorMap tq, tk, tv, tdo, tdk, tdv;
   FA_TRY(make_map(&tq, q, s, t.q));
   FA_TRY(make_map(&tk, k, s, t.k));
@@ -316,6 +343,12 @@ fa_status dq_checked(const void* q, const void* k, const void* v, const float* l
                      const float* Dvec, void* dq, const Shape& s, const BwdStrides& t, cudaStream_t st,
                      const fa::DropArgs& drop = kNoDrop) {
   if (!load_encoder()) return FA_ERR_CUDA;
+  if (s.d > 128) {
+    if (drop.t4 != 0) return FA_ERR_UNSUPPORTED;
+    fa::WideBwdMaps m;
+    FA_TRY(wide_maps(m, q, k, v, dO, dq, nullptr, nullptr, s, t, 1));
+    return cuda_status(fa::launch_bwd_d256_dq(m, lse, Dvec, s, st), "wide-head dQ kernel launch");
+  }
   CUtensorMap tq, tk, tv, tdo, tdq;
   FA_TRY(make_map(&tq, q, s, t.q));
   FA_TRY(make_map(&tk, k, s, t.k));
@@ -366,7 +399,7 @@ fa_status bwd_impl(const void* q, const fa_strides* qs, const void* k, const fa_
                    void* dv, const fa_strides* dvs, int B, int H, int N, int d, float scale, int causal,
                    void* workspace, size_t workspace_bytes, cudaStream_t stream,
                    const fa::DropArgs& drop = kNoDrop) {
-  FA_TRY(check_sizes(B, H, N, d));
+  FA_TRY(check_sizes(B, H, N, d, drop.t4 == 0 ? fa::kMaxHeadDim : 128));
   if (N == 0) return FA_OK;
   FA_TRY(check_ptrs({q, k, v, o, dO, dq, dk, dv}, {lse}));
   FA_TRY(check_scale(scale));
@@ -455,13 +488,13 @@ size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int d, int n
 }
 
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
-  if (check_sizes(B, H, N, d) != FA_OK || N <= 0) return 0;
+  if (check_sizes(B, H, N, d, fa::kMaxHeadDim) != FA_OK || N <= 0) return 0;
   return workspace_need(Shape{B, H, N, d, 1.f, 0});
 }
 
 fa_status fa_bwd_preprocess(const void* o, const void* dO, float* Dvec, int B, int H, int N, int d,
                             struct CUstream_st* stream) {
-  FA_TRY(check_sizes(B, H, N, d));
+  FA_TRY(check_sizes(B, H, N, d, fa::kMaxHeadDim));
   if (N == 0) return FA_OK;
   FA_TRY(check_ptrs({o, dO}, {Dvec}));
   const Shape s{B, H, N, d, 1.f, 0};
@@ -473,7 +506,7 @@ fa_status fa_bwd_preprocess(const void* o, const void* dO, float* Dvec, int B, i
 fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const float* lse, const void* dO,
                       const float* Dvec, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
                       struct CUstream_st* stream) {
-  FA_TRY(check_sizes(B, H, N, d));
+  FA_TRY(check_sizes(B, H, N, d, fa::kMaxHeadDim));
   if (N == 0) return FA_OK;
   FA_TRY(check_ptrs({q, k, v, dO, dk, dv}, {lse, Dvec}));
   FA_TRY(check_scale(scale));
@@ -486,7 +519,7 @@ fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const float* 
 fa_status fa_bwd_dq(const void* q, const void* k, const void* v, const float* lse, const void* dO,
                     const float* Dvec, void* dq, int B, int H, int N, int d, float scale, int causal,
                     struct CUstream_st* stream) {
-  FA_TRY(check_sizes(B, H, N, d));
+  FA_TRY(check_sizes(B, H, N, d, fa::kMaxHeadDim));
   if (N == 0) return FA_OK;
   FA_TRY(check_ptrs({q, k, v, dO, dq}, {lse, Dvec}));
   FA_TRY(check_scale(scale));
@@ -578,7 +611,7 @@ fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const floa
 fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
                          const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
                          int causal, struct CUstream_st* stream) {
-  FA_TRY(check_sizes(B, H, N, d));
+  FA_TRY(check_sizes(B, H, N, d, fa::kMaxHeadDim));
   if (N == 0) return FA_OK;
   FA_TRY(check_ptrs({q, k, v, o, dO, dq, dk, dv}, {lse}));
   FA_TRY(check_scale(scale));
@@ -633,8 +666,11 @@ fa_status fa_debug_status(int reset) {
   uint32_t w = 0;
   e = fa::fwd_d256_status(&w, reset != 0);
   if (e != cudaSuccess) return fail("reading the wide-head forward status word", e, cudaGetErrorString(e));
-  g_last_site = a ? a : (b ? b : (c ? c : w));
-  return (a | b | c | w) ? FA_ERR_TIMEOUT : FA_OK;
+  uint32_t x = 0;
+  e = fa::bwd_d256_status(&x, reset != 0);
+  if (e != cudaSuccess) return fail("reading the wide-head backward status word", e, cudaGetErrorString(e));
+  g_last_site = a ? a : (b ? b : (c ? c : (w ? w : x)));
+  return (a | b | c | w | x) ? FA_ERR_TIMEOUT : FA_OK;
 }
 
 unsigned int fa_debug_site(void) { return g_last_site; }

@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(kPreThreads) fa_bwd_preprocess_kernel(const ui
                                                                        float* __restrict__ Dvec, long long rows,
                                                                        int H, int N, int d, Strides so,
                                                                        Strides sdo, bool contig) {
-  // D = 64 or 128 covers d <= D: chunks at or past d count as zero.  FULL
+  // D = 64, 128 or 256 covers d <= D: chunks at or past d count as zero.  FULL
   // (d == D) keeps the row length a compile-time constant, and the loads
   // unconditional, on the common path.
   constexpr int kTpr = D / 8;                 // threads per row, one 16-byte chunk each
@@ -1318,7 +1318,12 @@ cudaError_t launch_bwd_preprocess(const void* o, const Strides& so, const void* 
   const bool contig = so.b == c.b && so.h == c.h && so.n == c.n && sdo.b == c.b && sdo.h == c.h && sdo.n == c.n;
   const auto* po = static_cast<const uint8_t*>(o);
   const auto* pdo = static_cast<const uint8_t*>(dO);
-  if (s.d == 128)
+  if (s.d == 256)
+    fa_bwd_preprocess_kernel<256, true><<<grid, kPreThreads, 0, st>>>(po, pdo, Dvec, rows, s.H, s.N, s.d, so, sdo, contig);
+  else if (kernel_dim(s.d) == 256)
+    fa_bwd_preprocess_kernel<256, false><<<grid, kPreThreads, 0, st>>>(po, pdo, Dvec, rows, s.H, s.N, s.d, so, sdo,
+                                                                       contig);
+  else if (s.d == 128)
     fa_bwd_preprocess_kernel<128, true><<<grid, kPreThreads, 0, st>>>(po, pdo, Dvec, rows, s.H, s.N, s.d, so, sdo, contig);
   else if (s.d == 64)
     fa_bwd_preprocess_kernel<64, true><<<grid, kPreThreads, 0, st>>>(po, pdo, Dvec, rows, s.H, s.N, s.d, so, sdo, contig);

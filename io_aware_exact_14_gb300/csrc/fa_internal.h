@@ -161,6 +161,18 @@ cudaError_t launch_bwd_dq(const CUtensorMap& tq, const CUtensorMap& tk, const CU
                           const float* Dvec, const Shape& s, const DropArgs& drop, const WaitCfg& wc,
                           cudaStream_t st);
 
+// Backward for wide heads (128 < d <= 256, fa_bwd_d256.cu): three launches
+// (dV, dK, dQ), each with resident 128-row tiles and streamed 64-row tiles,
+// so every tensor is mapped with 128-row boxes and, where it streams, 64-row
+// boxes.  wide_dkdv runs the dV and dK launches, wide_dq the dQ launch.
+struct WideBwdMaps {
+  CUtensorMap q128, q64, k128, k64, v128, v64, do128, do64, dq128, dk128, dv128;
+};
+cudaError_t launch_bwd_d256_dkdv(const WideBwdMaps& m, const float* lse, const float* Dvec, const Shape& s,
+                                 cudaStream_t st);
+cudaError_t launch_bwd_d256_dq(const WideBwdMaps& m, const float* lse, const float* Dvec, const Shape& s,
+                               cudaStream_t st);
+
 // FP8 (e4m3): per-(b, h) quantisation of a contiguous bf16 [B, H, N, d] tensor
 // into codes [B, H, N, d] (or, transposed, [B, H, d, ldv]) with descale[b*H + h]
 // = amax / 448, optionally rotated along d by the random-sign Hadamard
@@ -195,5 +207,6 @@ cudaError_t fwd_status(uint32_t* out, bool reset);
 cudaError_t bwd_status(uint32_t* out, bool reset);
 cudaError_t fp8_status(uint32_t* out, bool reset);
 cudaError_t fwd_d256_status(uint32_t* out, bool reset);
+cudaError_t bwd_d256_status(uint32_t* out, bool reset);
 
 }  // namespace fa

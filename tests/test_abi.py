@@ -87,6 +87,8 @@ def test_bwd_argument_checks(lib):
 
     assert bwd(d=84) == 2
     assert bwd(d=264) == 2
+    assert lib.fa_bwd_workspace_bytes(1, 1, 128, 256) == 512
+    assert lib.fa_bwd_workspace_bytes(1, 1, 128, 264) == 0
     assert bwd(N=0, q=0) == 0
     assert bwd(dq=0) == 1
     assert bwd(do=BAD_ALIGN) == 1

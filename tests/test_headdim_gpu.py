@@ -21,7 +21,10 @@ FWD = [(1, 2, 300, 8, True), (2, 1, 257, 16, False), (1, 3, 200, 32, True), (1, 
        (1, 1, 128, 256, False), (1, 2, 300, 256, True), (2, 1, 1000, 256, False), (1, 2, 777, 192, True),
        (1, 1, 1, 256, True), (1, 3, 129, 136, False), (1, 1, 2100, 256, True), (1, 2, 512, 224, False)]
 BWD = [(1, 2, 300, 8, True), (1, 3, 200, 32, False), (2, 1, 384, 48, True), (1, 2, 333, 80, False),
-       (2, 2, 256, 96, True), (1, 1, 1000, 96, True), (1, 2, 129, 120, False)]
+       (2, 2, 256, 96, True), (1, 1, 1000, 96, True), (1, 2, 129, 120, False),
+       # wide heads: separate dV, dK and dQ launches with 64-row streamed tiles
+       (1, 1, 128, 256, False), (1, 2, 300, 256, True), (2, 1, 1000, 192, True), (1, 2, 777, 256, False),
+       (1, 1, 1, 256, True), (1, 3, 129, 136, True), (1, 1, 2100, 256, True), (1, 2, 500, 224, False)]
 
 
 @pytest.mark.parametrize("B,H,N,d,causal", FWD)
@@ -50,15 +53,16 @@ def test_bwd_head_dim_parity(B, H, N, d, causal):
         assert err <= TOL_GRAD, f"{name}: relative Frobenius error {err:.3g}"
 
 
-@pytest.mark.parametrize("d", [40, 96])
+@pytest.mark.parametrize("d", [40, 96, 192])
 def test_outputs_leave_columns_past_d_untouched(d):
-    """Outputs as [..., :d] views of rows 128 wide filled with a sentinel: the
-    kernels' (64 or 128 wide) tile stores must clip at column d."""
+    """Outputs as [..., :d] views of rows 128 (256) wide filled with a sentinel:
+    the kernels' (64, 128 or 256 wide) tile stores must clip at column d."""
     B, H, N, causal = 1, 2, 300, True
     x, g = device_inputs(B, H, N, d, seed=740 + d, with_grad=True)
     o_c, lse_c = fa.fa_fwd(g["q"], g["k"], g["v"], None, causal)
     dq_c, dk_c, dv_c = fa.fa_bwd(g["q"], g["k"], g["v"], o_c, lse_c, g["do"], None, causal)
-    bufs = [torch.full((B, H, N, 128), 7.0, dtype=torch.bfloat16, device="cuda") for _ in range(4)]
+    width = 128 if d <= 128 else 256
+    bufs = [torch.full((B, H, N, width), 7.0, dtype=torch.bfloat16, device="cuda") for _ in range(4)]
     o, dq, dk, dv = (b[..., :d] for b in bufs)
     fa.fa_fwd_strided(g["q"], g["k"], g["v"], None, causal, out=o)
     fa.fa_bwd_strided(g["q"], g["k"], g["v"], o, lse_c, g["do"], None, causal, dq=dq, dk=dk, dv=dv)
@@ -72,7 +76,7 @@ def test_outputs_leave_columns_past_d_untouched(d):
 
 
 def test_preprocess_head_dims():
-    for d in (8, 40, 96):
+    for d in (8, 40, 96, 200, 256):
         _, g = device_inputs(2, 3, 201, d, seed=750 + d, with_grad=True)
         o = torch.randn_like(g["q"])
         Dvec = fa.fa_bwd_preprocess(o, g["do"])
@@ -144,3 +148,38 @@ def test_wide_head_long_rows_sampled():
         got_l = np.stack([np.stack([l_np[b, h, rows[b, h]] for h in range(w.H)]) for b in range(w.B)])
         assert o_excess_err(got_o, o_ref) <= TOL_O
         assert oracle.lse_max_abs_err(got_l, lse_ref) <= TOL_LSE
+
+
+def test_wide_head_backward_steps_equal_fused_call():
+    """fa_bwd at d = 256 equals fa_bwd_preprocess + fa_bwd_dkdv + fa_bwd_dq, bit for bit,
+    and reruns are bitwise identical (no atomics)."""
+    _, g = device_inputs(1, 2, 520, 256, seed=795, with_grad=True)
+    o, lse = fa.fa_fwd(g["q"], g["k"], g["v"], None, True)
+    dq, dk, dv = fa.fa_bwd(g["q"], g["k"], g["v"], o, lse, g["do"], None, True)
+    Dvec = fa.fa_bwd_preprocess(o, g["do"])
+    dk2, dv2 = fa.fa_bwd_dkdv(g["q"], g["k"], g["v"], lse, g["do"], Dvec, None, True)
+    dq2 = fa.fa_bwd_dq(g["q"], g["k"], g["v"], lse, g["do"], Dvec, None, True)
+    dq3, dk3, dv3 = fa.fa_bwd(g["q"], g["k"], g["v"], o, lse, g["do"], None, True)
+    torch.cuda.synchronize()
+    assert_no_timeout()
+    assert torch.equal(dq, dq2) and torch.equal(dk, dk2) and torch.equal(dv, dv2)
+    assert torch.equal(dq, dq3) and torch.equal(dk, dk3) and torch.equal(dv, dv3)
+
+
+def test_wide_head_training_shape_sampled_slices():
+    """B=2 H=8 N=4096 d=256 causal forward + backward; gradients of two sampled
+    (b, h) slices against the oracle."""
+    from io_aware_exact_14_gb300.workloads import Workload, sample_slices
+    w = Workload(0, "wide_train", 2, 8, 4096, 256, (True,), ("fwd", "bwd"), oracle_slices=2)
+    x, g = device_inputs(w.B, w.H, w.N, w.d, seed=797, with_grad=True)
+    o, lse = fa.fa_fwd(g["q"], g["k"], g["v"], w.scale, True)
+    dq, dk, dv = fa.fa_bwd(g["q"], g["k"], g["v"], o, lse, g["do"], w.scale, True)
+    torch.cuda.synchronize()
+    assert_no_timeout()
+    for b, h in sample_slices(w, 2):
+        sl = lambda t: f64(t[b:b + 1, h:h + 1])
+        ref = oracle.attn_bwd_ref(sl(x["q"]), sl(x["k"]), sl(x["v"]), sl(x["do"]), w.scale, True)
+        for name, a, r in zip(("dq", "dk", "dv"), (dq[b:b + 1, h:h + 1], dk[b:b + 1, h:h + 1],
+                                                     dv[b:b + 1, h:h + 1]), ref):
+            err = oracle.rel_fro_err(f64(a), r)
+            assert err <= TOL_GRAD, f"{name} (b={b}, h={h}): relative Frobenius error {err:.3g}"

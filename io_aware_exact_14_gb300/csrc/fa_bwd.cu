@@ -156,9 +156,10 @@ __device__ __forceinline__ void mma_nt(uint32_t tmem_d, uint64_t a_desc, uint64_
 
 // Accumulating product: D(128 x d) += A(128 x 128, TMEM bf16) * B(128 x d, MN-major tile).
 // A's 128 K columns live as two 64-wide halves at a_tmem and a_tmem + 64.
+// idesc: M = 128, N = ceil(d / 16) * 16, B MN-major.
 template <int D>
-__device__ __forceinline__ void mma_tn_acc(uint32_t tmem_d, uint32_t a_tmem, uint64_t b_desc, bool acc) {
-  constexpr uint32_t idesc = idesc_bf16(128, D, false, true);
+__device__ __forceinline__ void mma_tn_acc(uint32_t tmem_d, uint32_t a_tmem, uint64_t b_desc, bool acc,
+                                           uint32_t idesc) {
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
     const uint32_t a = a_tmem + (kk / 4) * 64 + (kk % 4) * 8;
@@ -325,7 +326,7 @@ __global__ void __launch_bounds__(384, 1)
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                        const __grid_constant__ CUtensorMap tmDK, const __grid_constant__ CUtensorMap tmDV,
                        const float* __restrict__ lse, const float* __restrict__ Dg, int N, int n_tiles,
-                       int BH, int H, int band, float scale, float scale_log2, int ks,
+                       int BH, int H, int band, float scale, float scale_log2, int ks, uint32_t idesc_acc,
                        const __grid_constant__ DropArgs drop, const WaitCfg wc) {
   using C = DkdvCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -579,7 +580,7 @@ __global__ void __launch_bounds__(384, 1)
           // unit's epilogue must have read both accumulators out
           if (it == 0 && su > 0 && !(ok = mbar_wait_w(acc_free, (su - 1) & 1, g, kSiteDkdv | 18u))) break;
           tc_fence_after();
-          mma_tn_acc<D>(tDV, tS, mDO(ds), it > 0);          // dV += P^T dO_i
+          mma_tn_acc<D>(tDV, tS, mDO(ds), it > 0, idesc_acc);          // dV += P^T dO_i
           bool s_done = !next, k_done = false;
           while (ok && !(s_done && k_done)) {
             int which;
@@ -598,7 +599,7 @@ __global__ void __launch_bounds__(384, 1)
               s_done = true;
             } else {
               tc_fence_after();
-              mma_tn_acc<D>(tDK, tDP, mQ(qs), it > 0);        // dK += dS^T Q_i
+              mma_tn_acc<D>(tDK, tDP, mQ(qs), it > 0, idesc_acc);        // dK += dS^T Q_i
               tc_commit_w(&q_empty[qs]);                     // Q_i, -lse_i, and dO_i, -D_i: last readers done
               k_done = true;
             }
@@ -853,7 +854,8 @@ __global__ void __launch_bounds__(384, 1)
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                      const __grid_constant__ CUtensorMap tmDQ, const float* __restrict__ lse,
                      const float* __restrict__ Dg, int N, int n_tiles, int BH, int H, int band, float scale,
-                     float scale_log2, int ks, const __grid_constant__ DropArgs drop, const WaitCfg wc) {
+                     float scale_log2, int ks, uint32_t idesc_acc, const __grid_constant__ DropArgs drop,
+                     const WaitCfg wc) {
   using C = DqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1079,10 +1081,10 @@ __global__ void __launch_bounds__(384, 1)
             // unit's epilogue must have read it out
             if (su > 0 && !(ok = mbar_wait_w(acc_free, (su - 1) & 1, g, kSiteDq | 15u))) break;
             tc_fence_after();
-            mma_tn_acc<D>(tDQ, tDP, mK(j % C::kKStages), false);
+            mma_tn_acc<D>(tDQ, tDP, mK(j % C::kKStages), false, idesc_acc);
           } else {
             tc_fence_after();
-            mma_tn_acc<D>(tDQ, tDP, mK(j % C::kKStages), true);   // dQ += dS K_j
+            mma_tn_acc<D>(tDQ, tDP, mK(j % C::kKStages), true, idesc_acc);   // dQ += dS K_j
           }
           tc_commit_w(&k_empty[j % C::kKStages]);                 // K_j: last reader done
           if (!next) {
@@ -1240,8 +1242,8 @@ cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CU
   const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
   const dim3 grid(static_cast<unsigned>(s.B) * s.H * n_tiles);
   kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, tdk, tdv, lse, Dvec, s.N, n_tiles, s.B * s.H, s.H,
-                                                 head_band(s.N, s.d), s.scale, scale_log2, score_ksteps(s.d), drop,
-                                                 wc);
+                                                 head_band(s.N, s.d), s.scale, scale_log2, score_ksteps(s.d),
+                                                 idesc_bf16(128, out_cols(s.d), false, true), drop, wc);
   return cudaGetLastError();
 }
 
@@ -1257,8 +1259,8 @@ cudaError_t launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
   const dim3 grid(static_cast<unsigned>(s.B) * s.H * n_tiles);
   kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, tdq, lse, Dvec, s.N, n_tiles, s.B * s.H, s.H,
-                                                 head_band(s.N, s.d), s.scale, scale_log2, score_ksteps(s.d), drop,
-                                                 wc);
+                                                 head_band(s.N, s.d), s.scale, scale_log2, score_ksteps(s.d),
+                                                 idesc_bf16(128, out_cols(s.d), false, true), drop, wc);
   return cudaGetLastError();
 }
 

@@ -181,11 +181,12 @@ __device__ __forceinline__ void b256_score(uint32_t tmem_d, uint64_t a_desc, uin
   }
 }
 
-// Accumulating product acc(128 x 256) += A(128 x 64, bf16 in TMEM) * B(64 x 256),
-// B a streamed tile read MN-major (four 64-column blocks 8 KB apart).
+// Accumulating product acc(128 x d) += A(128 x 64, bf16 in TMEM) * B(64 x d),
+// B a streamed tile read MN-major (64-column blocks 8 KB apart); idesc has
+// N = ceil(d / 16) * 16.
 template <int MODE>
-__device__ __forceinline__ void b256_acc(uint32_t tmem_acc, uint32_t a_tmem, uint64_t b_desc, bool acc) {
-  constexpr uint32_t idesc = idesc_bf16(128, 256, false, true);
+__device__ __forceinline__ void b256_acc(uint32_t tmem_acc, uint32_t a_tmem, uint64_t b_desc, bool acc,
+                                         uint32_t idesc) {
 #pragma unroll
   for (int kk = 0; kk < 4; ++kk)   // 64 rows, 16 per MMA; A packs 2 per TMEM column
     tc_mma_ts_w(tmem_acc, a_tmem + kk * 8, b_desc + ((kk * 2048) >> 4), idesc, (acc || kk > 0) ? 1u : 0u);
@@ -194,7 +195,8 @@ __device__ __forceinline__ void b256_acc(uint32_t tmem_acc, uint32_t a_tmem, uin
 template <int MODE>
 __device__ void b256_mma(const U256& w, uint32_t tmem, uint32_t sbase, uint64_t* r_full, uint64_t* t1_full,
                          uint64_t* t1_empty, uint64_t* t2_full, uint64_t* t2_empty, uint64_t* s_full,
-                         uint64_t* dp_full, uint64_t* ds_full, uint64_t* acc_done, int ks, const CtaGuard& g) {
+                         uint64_t* dp_full, uint64_t* ds_full, uint64_t* acc_done, int ks, uint32_t idesc_acc,
+                         const CtaGuard& g) {
   using C = B256<MODE>;
   const uint64_t r1 = sdesc_sw128(sbase + C::kR1Off, 16, 1024);
   const uint64_t r2 = sdesc_sw128(sbase + C::kR2Off, 16, 1024);
@@ -226,11 +228,11 @@ __device__ void b256_mma(const U256& w, uint32_t tmem, uint32_t sbase, uint64_t*
     if (!mbar_wait_w(ds_full, j & 1, g, kSiteBwd256 | 5u)) return;
     tc_fence_after();
     if (C::kHasDP) {
-      b256_acc<MODE>(tmem + C::kColAcc, tmem + C::kColDP, t1m(j % C::kT1Slots), j > 0);   // += dS K_j / dS^T Q_i
+      b256_acc<MODE>(tmem + C::kColAcc, tmem + C::kColDP, t1m(j % C::kT1Slots), j > 0, idesc_acc);   // += dS K_j / dS^T Q_i
       tc_commit_w(&t1_empty[j & 1]);   // last reader of the tile; its -lse was read before ds_full
       if (j + 1 < w.n && !issue_dp(j + 1)) return;   // after acc(j) has read dS(j) from the dP columns
     } else {
-      b256_acc<MODE>(tmem + C::kColAcc, tmem + 64u * (j & 1), t2m(j % C::kT2Slots), j > 0);   // += P^T dO_i
+      b256_acc<MODE>(tmem + C::kColAcc, tmem + 64u * (j & 1), t2m(j % C::kT2Slots), j > 0, idesc_acc);   // += P^T dO_i
       tc_commit_w(&t2_empty[j & 1]);
       tc_commit_w(&t1_empty[j & 1]);   // Q_i was read by S(j), its -lse before ds_full
     }
@@ -407,7 +409,7 @@ __global__ void __launch_bounds__(192, 1)
                        const __grid_constant__ CUtensorMap tmT1, const __grid_constant__ CUtensorMap tmT2,
                        const __grid_constant__ CUtensorMap tmOut, const float* __restrict__ lse,
                        const float* __restrict__ Dg, int N, int d, int n_res, int BH, int H, int band, float scale,
-                       float scale_log2, int ks, const WaitCfg wc) {
+                       float scale_log2, int ks, uint32_t idesc_acc, const WaitCfg wc) {
   using C = B256<MODE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -468,7 +470,7 @@ __global__ void __launch_bounds__(192, 1)
                         N, g);
   } else if (warp == 5) {
     b256_mma<MODE>(w, tmem, smem_u32(smem), r_full, t1_full, t1_empty, t2_full, t2_empty, s_full, dp_full, ds_full,
-                   acc_done, ks, g);
+                   acc_done, ks, idesc_acc, g);
     tc_commit_w(drain);   // every MMA issued above has finished before TMEM is released
     mbar_drain(drain, 0);
     __syncwarp();
@@ -497,7 +499,8 @@ cudaError_t launch_t(const CUtensorMap& r1, const CUtensorMap& r2, const CUtenso
   const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
   const dim3 grid(static_cast<unsigned>(s.B) * s.H * n_res);
   kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(r1, r2, t1, t2, out, lse, Dvec, s.N, s.d, n_res, s.B * s.H, s.H,
-                                                 head_band(s.N, s.d), s.scale, scale_log2, score_ksteps(s.d), wc);
+                                                 head_band(s.N, s.d), s.scale, scale_log2, score_ksteps(s.d),
+                                                 idesc_bf16(128, out_cols(s.d), false, true), wc);
   return cudaGetLastError();
 }
 

@@ -197,9 +197,10 @@ __device__ __forceinline__ void fwd_issue_s(uint32_t tmem_d, uint64_t q_desc, ui
   }
 }
 
+// idesc: M = 128, N = ceil(d / 16) * 16, B (V) MN-major.
 template <int D>
-__device__ __forceinline__ void fwd_issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint64_t v_desc, bool acc) {
-  constexpr uint32_t idesc = idesc_bf16(128, D, false, true);
+__device__ __forceinline__ void fwd_issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint64_t v_desc, bool acc,
+                                             uint32_t idesc) {
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk)  // 128 keys, 16 per MMA; P packs 2 keys per TMEM column
     tc_mma_ts_w(tmem_o, tmem_p + kk * 8, v_desc + ((kk * 2048) >> 4), idesc, (acc || kk > 0) ? 1u : 0u);
@@ -216,7 +217,8 @@ __device__ __forceinline__ void fwd_issue_pv(uint32_t tmem_o, uint32_t tmem_p, u
 template <int D>
 __device__ __forceinline__ void fwd_mma(const FwdWork& w, int tile, uint32_t tmem, uint32_t smem_base,
                                         uint64_t* full, uint64_t* empty, uint64_t* q_full, uint64_t* s_full,
-                                        uint64_t* p_full, uint64_t* o_done, int ks, const CtaGuard& g) {
+                                        uint64_t* p_full, uint64_t* o_done, int ks, uint32_t idesc_pv,
+                                        const CtaGuard& g) {
   using C = FwdCfg<D>;
   const int n_t = tile ? w.n1 : w.n0;
   const uint64_t q_desc = sdesc_sw128(smem_base + C::kQOff + tile * C::kTileBytes, 16, 1024);
@@ -242,7 +244,7 @@ __device__ __forceinline__ void fwd_mma(const FwdWork& w, int tile, uint32_t tme
     if (j < n_t) {
       if (!mbar_wait_w(&p_full[tile], j & 1, g, tile ? (kSiteFwd | 5u) : (kSiteFwd | 4u))) return;
       tc_fence_after();
-      fwd_issue_pv<D>(t_o, t_s, v_desc0 + slot_off(iv), j > 0);
+      fwd_issue_pv<D>(t_o, t_s, v_desc0 + slot_off(iv), j > 0, idesc_pv);
       if (j + 1 < n_t) {
         fwd_issue_s<D>(t_s, q_desc, k_desc0 + slot_off(ik), ks);
         tc_commit_w(&s_full[tile]);
@@ -264,7 +266,7 @@ __device__ __forceinline__ void fwd_mma(const FwdWork& w, int tile, uint32_t tme
 template <int D>
 __device__ __forceinline__ void fwd_mma_both(const FwdWork& w, uint32_t tmem, uint32_t smem_base, uint64_t* full,
                                         uint64_t* empty, uint64_t* q_full, uint64_t* s_full, uint64_t* p_full,
-                                        uint64_t* o_done, int ks, const CtaGuard& g) {
+                                        uint64_t* o_done, int ks, uint32_t idesc_pv, const CtaGuard& g) {
   using C = FwdCfg<D>;
   const uint64_t q_desc[2] = {sdesc_sw128(smem_base + C::kQOff, 16, 1024),
                               sdesc_sw128(smem_base + C::kQOff + C::kTileBytes, 16, 1024)};
@@ -295,7 +297,7 @@ __device__ __forceinline__ void fwd_mma_both(const FwdWork& w, uint32_t tmem, ui
     if (j < w.n0) {
       if (!mbar_wait_w(&p_full[0], j & 1, g, kSiteFwd | 4u)) return;
       tc_fence_after();
-      fwd_issue_pv<D>(tmem + C::col_o(0), tmem + C::col_s(0), vd, j > 0);
+      fwd_issue_pv<D>(tmem + C::col_o(0), tmem + C::col_s(0), vd, j > 0, idesc_pv);
       if (next && j + 1 < w.n0) fwd_issue_s<D>(tmem + C::col_s(0), q_desc[0], kd, ks);
       if (j == w.n0 - 1) tc_commit_w(&o_done[0]);
       if (next && j + 1 < w.n0) tc_commit_w(&s_full[0]);
@@ -303,7 +305,7 @@ __device__ __forceinline__ void fwd_mma_both(const FwdWork& w, uint32_t tmem, ui
     if (j < w.n1) {
       if (!mbar_wait_w(&p_full[1], j & 1, g, kSiteFwd | 5u)) return;
       tc_fence_after();
-      fwd_issue_pv<D>(tmem + C::col_o(1), tmem + C::col_s(1), vd, j > 0);
+      fwd_issue_pv<D>(tmem + C::col_o(1), tmem + C::col_s(1), vd, j > 0, idesc_pv);
       if (next && j + 1 < w.n1) fwd_issue_s<D>(tmem + C::col_s(1), q_desc[1], kd, ks);
       if (j == w.n1 - 1) tc_commit_w(&o_done[1]);
       if (next && j + 1 < w.n1) tc_commit_w(&s_full[1]);
@@ -509,7 +511,7 @@ __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                   float* __restrict__ lse, int N, int n_pairs, int BH, int H, int band, float scale_log2, int Nk,
-                  int n_qt, int n_kt, int n_splits, int kt_per_split, int ks,
+                  int n_qt, int n_kt, int n_splits, int kt_per_split, int ks, uint32_t idesc_pv,
                   const __grid_constant__ DropArgs drop, const WaitCfg wc) {
   static_assert(!SPLIT || (!CAUSAL && ISSUERS == 1), "split-KV launches are non-causal with one issuer");
   static_assert(!(SPLIT && DROPOUT), "split-KV launches have no dropout");
@@ -575,9 +577,9 @@ __global__ void __launch_bounds__(384, 1)
     } else if (warp == 9 || (ISSUERS == 2 && warp == 10)) {
       // issuing warps (warp 9 also owns TMEM): whole-warp loops, one elected lane issues
       if (ISSUERS == 2)
-        fwd_mma<D>(w, warp - 9, tmem, smem_u32(smem), full, empty, q_full, s_full, p_full, o_done, ks, g);
+        fwd_mma<D>(w, warp - 9, tmem, smem_u32(smem), full, empty, q_full, s_full, p_full, o_done, ks, idesc_pv, g);
       else
-        fwd_mma_both<D>(w, tmem, smem_u32(smem), full, empty, q_full, s_full, p_full, o_done, ks, g);
+        fwd_mma_both<D>(w, tmem, smem_u32(smem), full, empty, q_full, s_full, p_full, o_done, ks, idesc_pv, g);
       tc_commit_w(drain);  // every MMA issued above has finished before TMEM is released
       mbar_drain(drain, 0);
       __syncwarp();
@@ -616,7 +618,8 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   const dim3 grid(static_cast<unsigned>(s.B) * s.H * n_pairs);
   kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, to, lse, s.N, n_pairs, s.B * s.H, s.H,
                                                  head_band(s.N, s.d), scale_log2, s.N, n_qt, n_qt, 1, n_qt,
-                                                 score_ksteps(s.d), drop, wc);
+                                                 score_ksteps(s.d), idesc_bf16(128, out_cols(s.d), false, true),
+                                                 drop, wc);
   return cudaGetLastError();
 }
 
@@ -696,7 +699,7 @@ cudaError_t launch_fwd_splitkv_t(const CUtensorMap& tq, const CUtensorMap& tk, c
     const dim3 grid(static_cast<unsigned>(BH) * n_splits * n_qt);
     kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, top, lse_part, s.N, n_qt, BH, s.H, 1, scale_log2,
                                                    Nk, n_qt, n_kt, n_splits, kt_per_split, score_ksteps(s.d),
-                                                   no_drop_args(), wc);
+                                                   idesc_bf16(128, out_cols(s.d), false, true), no_drop_args(), wc);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   const long long rows = static_cast<long long>(BH) * s.N;

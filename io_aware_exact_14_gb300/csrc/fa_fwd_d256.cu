@@ -131,10 +131,11 @@ __device__ __forceinline__ uint64_t kstep_off(int kk) {
 }
 
 // The MMA warp: S(0) S(1) | PV(0) S(2) | PV(1) S(3) | ... | PV(n-1).
-// ks = ceil(d / 16) steps of 16 columns hold data (9..16 here).
+// ks = ceil(d / 16) steps of 16 columns hold data (9..16 here); the second
+// half of O is idesc_pv1 wide (N = ceil(d / 16) * 16 - 128).
 __device__ void f256_mma(const W256& w, uint32_t tmem, uint32_t sbase, uint64_t* full, uint64_t* empty,
                          uint64_t* q_full, uint64_t* s_full, uint64_t* p_full, uint64_t* o_ready, int ks,
-                         const CtaGuard& g) {
+                         uint32_t idesc_pv1, const CtaGuard& g) {
   using C = F256;
   constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
   constexpr uint32_t idesc_pv = idesc_bf16(128, 128, false, true);
@@ -173,7 +174,7 @@ __device__ void f256_mma(const W256& w, uint32_t tmem, uint32_t sbase, uint64_t*
       const uint64_t v = vd0 + slot_off(2 * t + h);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)   // 128 keys, 16 per MMA; P packs 2 keys per TMEM column
-        tc_mma_ts_w(tmem + C::kColO + 128u * h, tp + kk * 8, v + ((kk * 2048) >> 4), idesc_pv,
+        tc_mma_ts_w(tmem + C::kColO + 128u * h, tp + kk * 8, v + ((kk * 2048) >> 4), h ? idesc_pv1 : idesc_pv,
                     (j > 0 || kk > 0) ? 1u : 0u);
     }
     tc_commit_w(o_ready);
@@ -325,7 +326,7 @@ __global__ void __launch_bounds__(192, 1)
     fa_fwd_d256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                        float* __restrict__ lse, int N, int d, int n_qt, int BH, int H, int band, float scale_log2,
-                       int ks, const WaitCfg wc) {
+                       int ks, uint32_t idesc_pv1, const WaitCfg wc) {
   using C = F256;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -375,7 +376,7 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 4) {
     if (lane == 0) f256_producer(w, smem, full, empty, q_full, &tmQ, &tmK, &tmV, g);
   } else if (warp == 5) {
-    f256_mma(w, tmem, smem_u32(smem), full, empty, q_full, s_full, p_full, o_ready, ks, g);
+    f256_mma(w, tmem, smem_u32(smem), full, empty, q_full, s_full, p_full, o_ready, ks, idesc_pv1, g);
     tc_commit_w(drain);   // every MMA issued above has finished before TMEM is released
     mbar_drain(drain, 0);
     __syncwarp();
@@ -402,7 +403,8 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
   const dim3 grid(static_cast<unsigned>(s.B) * s.H * n_qt);
   kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, to, lse, s.N, s.d, n_qt, s.B * s.H, s.H,
-                                                 head_band(s.N, s.d), scale_log2, score_ksteps(s.d), wc);
+                                                 head_band(s.N, s.d), scale_log2, score_ksteps(s.d),
+                                                 idesc_bf16(128, out_cols(s.d) - 128, false, true), wc);
   return cudaGetLastError();
 }
 

@@ -72,6 +72,11 @@ constexpr int kMaxHeadDim = 256;
 // Products that contract over the head dim (Q K^T, dO V^T and their
 // transposes) issue only the ceil(d / 16) steps of 16 columns that hold data.
 inline int score_ksteps(int d) { return (d + 15) / 16; }
+// Products whose output columns are the head dim (P V, dV, dK, dQ) run with
+// N = ceil(d / 16) * 16 (the tensor core's step for M = 128), not the
+// kernel's D: the accumulator columns from N to D are never written and the
+// stores clip them.
+inline int out_cols(int d) { return (d + 15) / 16 * 16; }
 
 // Element strides of a [B, H, N, d] bf16 view (d contiguous).
 struct Strides {

@@ -142,24 +142,31 @@ struct BwdCfg {
 };
 
 // S-like product: D(128 x 128) = A(128 x d) * B(128 x d)^T, both K-major
-// tiles; only the ks = ceil(d / 16) steps of 16 columns that hold data.
-template <int D>
+// tiles; only the ks = ceil(d / 16) steps of 16 columns that hold data.  FD
+// (d == D): all D / 16 steps as a straight run of MMAs; otherwise each
+// step's issue is predicated (a branch per MMA measured 11% slower).
+template <int D, bool FD>
 __device__ __forceinline__ void mma_nt(uint32_t tmem_d, uint64_t a_desc, uint64_t b_desc, int ks) {
   using C = BwdCfg<D>;
   constexpr uint32_t idesc = idesc_bf16(128, 128, false, false);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint64_t off = ((kk / 4) * C::kBoxBytes + (kk % 4) * 32) >> 4;   // descriptor address units
-    if (kk < ks) tc_mma_ss_w(tmem_d, a_desc + off, b_desc + off, idesc, kk > 0 ? 1u : 0u);
+    if constexpr (FD)
+      tc_mma_ss_w(tmem_d, a_desc + off, b_desc + off, idesc, kk > 0 ? 1u : 0u);
+    else
+      tc_mma_ss_w_if(tmem_d, a_desc + off, b_desc + off, idesc, kk > 0 ? 1u : 0u, kk < ks ? 1u : 0u);
   }
 }
 
 // Accumulating product: D(128 x d) += A(128 x 128, TMEM bf16) * B(128 x d, MN-major tile).
 // A's 128 K columns live as two 64-wide halves at a_tmem and a_tmem + 64.
-// idesc: M = 128, N = ceil(d / 16) * 16, B MN-major.
-template <int D>
+// idesc: M = 128, N = ceil(d / 16) * 16, B MN-major (a compile-time constant
+// when d == D).
+template <int D, bool FD>
 __device__ __forceinline__ void mma_tn_acc(uint32_t tmem_d, uint32_t a_tmem, uint64_t b_desc, bool acc,
-                                           uint32_t idesc) {
+                                           uint32_t idesc_rt) {
+  const uint32_t idesc = FD ? idesc_bf16(128, D, false, true) : idesc_rt;
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
     const uint32_t a = a_tmem + (kk / 4) * 64 + (kk % 4) * 8;
@@ -320,7 +327,8 @@ __device__ __forceinline__ DkdvUnit dkdv_unit(int u, int n_tiles, int BH, int ba
   return w;
 }
 
-template <int D, bool CAUSAL, bool DROPOUT>
+// FD: d == D (compile-time K steps and output width of the products).
+template <int D, bool CAUSAL, bool DROPOUT, bool FD>
 __global__ void __launch_bounds__(384, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -561,12 +569,12 @@ __global__ void __launch_bounds__(384, 1)
         // S^T(0), dP^T(0): the previous unit's readers of these columns (its
         // last dV and dK) were issued before
         if (!(ok = mbar_wait_w(&q_full[g0 % C::kQStages], qpar(g0), g, kSiteDkdv | 3u))) break;
-        mma_nt<D>(tS, kK, kQ(g0 % C::kQStages), ks);
+        mma_nt<D, FD>(tS, kK, kQ(g0 % C::kQStages), ks);
         tc_commit_w(s_full);
         if (cnt == 1) tc_commit_w(k_free);    // K_j: last reader issued
         if (!(ok = mbar_wait_w(&v_full[su & 1], (su >> 1) & 1, g, kSiteDkdv | 3u))) break;
         if (!(ok = mbar_wait_w(&do_full[g0 % C::kDOStages], dpar(g0), g, kSiteDkdv | 3u))) break;
-        mma_nt<D>(tDP, kV, kDO(g0 % C::kDOStages), ks);
+        mma_nt<D, FD>(tDP, kV, kDO(g0 % C::kDOStages), ks);
         tc_commit_w(dp_full);
         if (cnt == 1) tc_commit_w(v_free);    // V_j: last reader issued
         for (int it = 0; ok && it < cnt; ++it) {
@@ -580,7 +588,7 @@ __global__ void __launch_bounds__(384, 1)
           // unit's epilogue must have read both accumulators out
           if (it == 0 && su > 0 && !(ok = mbar_wait_w(acc_free, (su - 1) & 1, g, kSiteDkdv | 18u))) break;
           tc_fence_after();
-          mma_tn_acc<D>(tDV, tS, mDO(ds), it > 0, idesc_acc);          // dV += P^T dO_i
+          mma_tn_acc<D, FD>(tDV, tS, mDO(ds), it > 0, idesc_acc);          // dV += P^T dO_i
           bool s_done = !next, k_done = false;
           while (ok && !(s_done && k_done)) {
             int which;
@@ -593,13 +601,13 @@ __global__ void __launch_bounds__(384, 1)
             if (which < 0) {
               ok = false;
             } else if (which == 0) {
-              mma_nt<D>(tS, kK, kQ(qs1), ks);                     // S^T(i+1)
+              mma_nt<D, FD>(tS, kK, kQ(qs1), ks);                     // S^T(i+1)
               tc_commit_w(s_full);
               if (it + 2 == cnt) tc_commit_w(k_free);       // K_j: last reader issued
               s_done = true;
             } else {
               tc_fence_after();
-              mma_tn_acc<D>(tDK, tDP, mQ(qs), it > 0, idesc_acc);        // dK += dS^T Q_i
+              mma_tn_acc<D, FD>(tDK, tDP, mQ(qs), it > 0, idesc_acc);        // dK += dS^T Q_i
               tc_commit_w(&q_empty[qs]);                     // Q_i, -lse_i, and dO_i, -D_i: last readers done
               k_done = true;
             }
@@ -607,7 +615,7 @@ __global__ void __launch_bounds__(384, 1)
           if (!ok) break;
           if (next) {
             if (!(ok = mbar_wait_w(&do_full[ds1], dpar(i + 1), g, kSiteDkdv | 13u))) break;
-            mma_nt<D>(tDP, kV, kDO(ds1), ks);                     // dP^T(i+1), after dK(i) has read dS^T(i)
+            mma_nt<D, FD>(tDP, kV, kDO(ds1), ks);                     // dP^T(i+1), after dK(i) has read dS^T(i)
             tc_commit_w(dp_full);
             if (it + 2 == cnt) tc_commit_w(v_free);         // V_j: last reader issued
           }
@@ -848,7 +856,7 @@ __device__ __forceinline__ float2 dq_row_terms(int u, int n_tiles, int BH, int b
   return t;
 }
 
-template <int D, bool CAUSAL, bool DROPOUT>
+template <int D, bool CAUSAL, bool DROPOUT, bool FD>
 __global__ void __launch_bounds__(384, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -1056,11 +1064,11 @@ __global__ void __launch_bounds__(384, 1)
         // unit's last dQ waited for)
         if (!(ok = mbar_wait_w(&k_full[g0 % C::kKStages], kpar(g0), g, kSiteDq | 3u))) break;
         tc_fence_after();
-        mma_nt<D>(tmem + C::col_s(g0), kQ, kK(g0 % C::kKStages), ks);
+        mma_nt<D, FD>(tmem + C::col_s(g0), kQ, kK(g0 % C::kKStages), ks);
         tc_commit_w(&s_full[g0 & 1]);
         if (!(ok = mbar_wait_w(&v_full[g0 % C::kVStages], vpar(g0), g, kSiteDq | 3u))) break;
         if (!(ok = mbar_wait_w(do_full, su & 1, g, kSiteDq | 19u))) break;
-        mma_nt<D>(tDP, kDO, kV(g0 % C::kVStages), ks);
+        mma_nt<D, FD>(tDP, kDO, kV(g0 % C::kVStages), ks);
         tc_commit_w(dp_full);
         if (cnt == 1) tc_commit_w(do_empty);   // dO_i: last reader issued
         for (int it = 0; it < cnt; ++it) {
@@ -1070,7 +1078,7 @@ __global__ void __launch_bounds__(384, 1)
           if (next) {   // S(j+1), into the other S buffer
             if (!(ok = mbar_wait_w(&k_full[(j + 1) % C::kKStages], kpar(j + 1), g, kSiteDq | 4u))) break;
             tc_fence_after();
-            mma_nt<D>(tmem + C::col_s(j + 1), kQ, kK((j + 1) % C::kKStages), ks);
+            mma_nt<D, FD>(tmem + C::col_s(j + 1), kQ, kK((j + 1) % C::kKStages), ks);
             tc_commit_w(&s_full[(j + 1) & 1]);
           } else {
             tc_commit_w(q_empty);   // every reader of Q_i has been issued
@@ -1081,10 +1089,10 @@ __global__ void __launch_bounds__(384, 1)
             // unit's epilogue must have read it out
             if (su > 0 && !(ok = mbar_wait_w(acc_free, (su - 1) & 1, g, kSiteDq | 15u))) break;
             tc_fence_after();
-            mma_tn_acc<D>(tDQ, tDP, mK(j % C::kKStages), false, idesc_acc);
+            mma_tn_acc<D, FD>(tDQ, tDP, mK(j % C::kKStages), false, idesc_acc);
           } else {
             tc_fence_after();
-            mma_tn_acc<D>(tDQ, tDP, mK(j % C::kKStages), true, idesc_acc);   // dQ += dS K_j
+            mma_tn_acc<D, FD>(tDQ, tDP, mK(j % C::kKStages), true, idesc_acc);   // dQ += dS K_j
           }
           tc_commit_w(&k_empty[j % C::kKStages]);                 // K_j: last reader done
           if (!next) {
@@ -1093,7 +1101,7 @@ __global__ void __launch_bounds__(384, 1)
           }
           // dP(j+1), after dQ(j) has read dS(j) from the same columns
           if (!(ok = mbar_wait_w(&v_full[(j + 1) % C::kVStages], vpar(j + 1), g, kSiteDq | 12u))) break;
-          mma_nt<D>(tDP, kDO, kV((j + 1) % C::kVStages), ks);
+          mma_nt<D, FD>(tDP, kDO, kV((j + 1) % C::kVStages), ks);
           tc_commit_w(dp_full);
           if (it + 2 == cnt) tc_commit_w(do_empty);   // dO_i: last reader issued
         }
@@ -1235,7 +1243,7 @@ cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CU
                           const float* Dvec, const Shape& s, const DropArgs& drop, const WaitCfg& wc,
                           cudaStream_t st) {
   using C = DkdvCfg<D>;
-  auto kern = fa_bwd_dkdv_kernel<D, CAUSAL, DROPOUT>;
+  auto kern = s.d == D ? fa_bwd_dkdv_kernel<D, CAUSAL, DROPOUT, true> : fa_bwd_dkdv_kernel<D, CAUSAL, DROPOUT, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int n_tiles = (s.N + 127) / 128;
@@ -1252,7 +1260,7 @@ cudaError_t launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
                         const CUtensorMap& tdo, const CUtensorMap& tdq, const float* lse, const float* Dvec,
                         const Shape& s, const DropArgs& drop, const WaitCfg& wc, cudaStream_t st) {
   using C = DqCfg<D>;
-  auto kern = fa_bwd_dq_kernel<D, CAUSAL, DROPOUT>;
+  auto kern = s.d == D ? fa_bwd_dq_kernel<D, CAUSAL, DROPOUT, true> : fa_bwd_dq_kernel<D, CAUSAL, DROPOUT, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int n_tiles = (s.N + 127) / 128;

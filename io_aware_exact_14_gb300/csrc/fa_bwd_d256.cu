@@ -169,7 +169,7 @@ __device__ void b256_producer(const U256& w, uint8_t* smem, uint64_t* r_full, ui
 // Score product D(128 x 64) = A(128 x d) B(64 x d)^T: A a resident tile
 // (boxes 16 KB apart), B a streamed one (boxes 8 KB apart), both K-major;
 // ks = ceil(d / 16) steps of 16 columns.
-template <int MODE>
+template <int MODE, bool FD>
 __device__ __forceinline__ void b256_score(uint32_t tmem_d, uint64_t a_desc, uint64_t b_desc, int ks) {
   using C = B256<MODE>;
   constexpr uint32_t idesc = idesc_bf16(128, 64, false, false);
@@ -177,22 +177,26 @@ __device__ __forceinline__ void b256_score(uint32_t tmem_d, uint64_t a_desc, uin
   for (int kk = 0; kk < 16; ++kk) {
     const uint64_t oa = ((kk / 4) * C::kResBox + (kk % 4) * 32) >> 4;
     const uint64_t ob = ((kk / 4) * C::kStrBox + (kk % 4) * 32) >> 4;
-    if (kk < ks) tc_mma_ss_w(tmem_d, a_desc + oa, b_desc + ob, idesc, kk > 0 ? 1u : 0u);
+    if constexpr (FD)
+      tc_mma_ss_w(tmem_d, a_desc + oa, b_desc + ob, idesc, kk > 0 ? 1u : 0u);
+    else
+      tc_mma_ss_w_if(tmem_d, a_desc + oa, b_desc + ob, idesc, kk > 0 ? 1u : 0u, kk < ks ? 1u : 0u);
   }
 }
 
 // Accumulating product acc(128 x d) += A(128 x 64, bf16 in TMEM) * B(64 x d),
 // B a streamed tile read MN-major (64-column blocks 8 KB apart); idesc has
 // N = ceil(d / 16) * 16.
-template <int MODE>
+template <int MODE, bool FD>
 __device__ __forceinline__ void b256_acc(uint32_t tmem_acc, uint32_t a_tmem, uint64_t b_desc, bool acc,
-                                         uint32_t idesc) {
+                                         uint32_t idesc_rt) {
+  const uint32_t idesc = FD ? idesc_bf16(128, 256, false, true) : idesc_rt;
 #pragma unroll
   for (int kk = 0; kk < 4; ++kk)   // 64 rows, 16 per MMA; A packs 2 per TMEM column
     tc_mma_ts_w(tmem_acc, a_tmem + kk * 8, b_desc + ((kk * 2048) >> 4), idesc, (acc || kk > 0) ? 1u : 0u);
 }
 
-template <int MODE>
+template <int MODE, bool FD>
 __device__ void b256_mma(const U256& w, uint32_t tmem, uint32_t sbase, uint64_t* r_full, uint64_t* t1_full,
                          uint64_t* t1_empty, uint64_t* t2_full, uint64_t* t2_empty, uint64_t* s_full,
                          uint64_t* dp_full, uint64_t* ds_full, uint64_t* acc_done, int ks, uint32_t idesc_acc,
@@ -208,13 +212,13 @@ __device__ void b256_mma(const U256& w, uint32_t tmem, uint32_t sbase, uint64_t*
   auto w2 = [&](int j) { return mbar_wait_w(&t2_full[j & 1], (j >> 1) & 1, g, kSiteBwd256 | 3u); };
   auto issue_s = [&](int j) -> bool {   // S(j) into buffer j & 1
     if (!w1(j)) return false;
-    b256_score<MODE>(tmem + 64u * (j & 1), r1, t1k(j % C::kT1Slots), ks);
+    b256_score<MODE, FD>(tmem + 64u * (j & 1), r1, t1k(j % C::kT1Slots), ks);
     tc_commit_w(&s_full[j & 1]);
     return true;
   };
   auto issue_dp = [&](int j) -> bool {   // dP(j)
     if (!w2(j)) return false;
-    b256_score<MODE>(tmem + C::kColDP, r2, t2k(j % C::kT2Slots), ks);
+    b256_score<MODE, FD>(tmem + C::kColDP, r2, t2k(j % C::kT2Slots), ks);
     tc_commit_w(dp_full);
     tc_commit_w(&t2_empty[j & 1]);   // V_j / dO_i: its only reader (its -D is read before dP(j + 1))
     return true;
@@ -228,11 +232,11 @@ __device__ void b256_mma(const U256& w, uint32_t tmem, uint32_t sbase, uint64_t*
     if (!mbar_wait_w(ds_full, j & 1, g, kSiteBwd256 | 5u)) return;
     tc_fence_after();
     if (C::kHasDP) {
-      b256_acc<MODE>(tmem + C::kColAcc, tmem + C::kColDP, t1m(j % C::kT1Slots), j > 0, idesc_acc);   // += dS K_j / dS^T Q_i
+      b256_acc<MODE, FD>(tmem + C::kColAcc, tmem + C::kColDP, t1m(j % C::kT1Slots), j > 0, idesc_acc);   // += dS K_j / dS^T Q_i
       tc_commit_w(&t1_empty[j & 1]);   // last reader of the tile; its -lse was read before ds_full
       if (j + 1 < w.n && !issue_dp(j + 1)) return;   // after acc(j) has read dS(j) from the dP columns
     } else {
-      b256_acc<MODE>(tmem + C::kColAcc, tmem + 64u * (j & 1), t2m(j % C::kT2Slots), j > 0, idesc_acc);   // += P^T dO_i
+      b256_acc<MODE, FD>(tmem + C::kColAcc, tmem + 64u * (j & 1), t2m(j % C::kT2Slots), j > 0, idesc_acc);   // += P^T dO_i
       tc_commit_w(&t2_empty[j & 1]);
       tc_commit_w(&t1_empty[j & 1]);   // Q_i was read by S(j), its -lse before ds_full
     }
@@ -403,7 +407,8 @@ __device__ void b256_compute(const U256& w, uint32_t tmem, uint8_t* smem, uint64
   }
 }
 
-template <int MODE, bool CAUSAL>
+// FD: d = 256 (compile-time K steps and output width of the products).
+template <int MODE, bool CAUSAL, bool FD>
 __global__ void __launch_bounds__(192, 1)
     fa_bwd_d256_kernel(const __grid_constant__ CUtensorMap tmR1, const __grid_constant__ CUtensorMap tmR2,
                        const __grid_constant__ CUtensorMap tmT1, const __grid_constant__ CUtensorMap tmT2,
@@ -469,7 +474,7 @@ __global__ void __launch_bounds__(192, 1)
     b256_producer<MODE>(w, smem, r_full, t1_full, t1_empty, t2_full, t2_empty, &tmR1, &tmR2, &tmT1, &tmT2, lse, Dg,
                         N, g);
   } else if (warp == 5) {
-    b256_mma<MODE>(w, tmem, smem_u32(smem), r_full, t1_full, t1_empty, t2_full, t2_empty, s_full, dp_full, ds_full,
+    b256_mma<MODE, FD>(w, tmem, smem_u32(smem), r_full, t1_full, t1_empty, t2_full, t2_empty, s_full, dp_full, ds_full,
                    acc_done, ks, idesc_acc, g);
     tc_commit_w(drain);   // every MMA issued above has finished before TMEM is released
     mbar_drain(drain, 0);
@@ -492,7 +497,7 @@ cudaError_t launch_t(const CUtensorMap& r1, const CUtensorMap& r2, const CUtenso
                      const CUtensorMap& out, const float* lse, const float* Dvec, const Shape& s, const WaitCfg& wc,
                      cudaStream_t st) {
   using C = B256<MODE>;
-  auto kern = fa_bwd_d256_kernel<MODE, CAUSAL>;
+  auto kern = s.d == 256 ? fa_bwd_d256_kernel<MODE, CAUSAL, true> : fa_bwd_d256_kernel<MODE, CAUSAL, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int n_res = (s.N + 127) / 128;

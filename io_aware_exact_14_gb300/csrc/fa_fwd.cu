@@ -185,22 +185,30 @@ __device__ __forceinline__ void fwd_producer(const FwdWork& w, uint8_t* smem, ui
 // to a few instructions (the tensor core's queue is shallow, so a slow issuer
 // starves it).
 // The score product contracts over the true head dim: ks = ceil(d / 16) steps
-// of 16 columns (the zero-filled columns past d would add nothing).
-template <int D>
+// of 16 columns (the zero-filled columns past d would add nothing).  FD (d ==
+// D): all D / 16 steps, a straight run of MMAs; otherwise each step's issue is
+// predicated on kk < ks (a branch per MMA measured 11% slower on the
+// backward kernels, the predicate alone a few percent).
+template <int D, bool FD>
 __device__ __forceinline__ void fwd_issue_s(uint32_t tmem_d, uint64_t q_desc, uint64_t k_desc, int ks) {
   using C = FwdCfg<D>;
   constexpr uint32_t idesc = idesc_bf16(128, 128, false, false);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint64_t off = ((kk / 4) * C::kBoxBytes + (kk % 4) * 32) >> 4;
-    if (kk < ks) tc_mma_ss_w(tmem_d, q_desc + off, k_desc + off, idesc, kk > 0 ? 1u : 0u);
+    if constexpr (FD)
+      tc_mma_ss_w(tmem_d, q_desc + off, k_desc + off, idesc, kk > 0 ? 1u : 0u);
+    else
+      tc_mma_ss_w_if(tmem_d, q_desc + off, k_desc + off, idesc, kk > 0 ? 1u : 0u, kk < ks ? 1u : 0u);
   }
 }
 
-// idesc: M = 128, N = ceil(d / 16) * 16, B (V) MN-major.
-template <int D>
+// idesc: M = 128, N = ceil(d / 16) * 16, B (V) MN-major (a compile-time
+// constant when d == D).
+template <int D, bool FD>
 __device__ __forceinline__ void fwd_issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint64_t v_desc, bool acc,
-                                             uint32_t idesc) {
+                                             uint32_t idesc_rt) {
+  const uint32_t idesc = FD ? idesc_bf16(128, D, false, true) : idesc_rt;
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk)  // 128 keys, 16 per MMA; P packs 2 keys per TMEM column
     tc_mma_ts_w(tmem_o, tmem_p + kk * 8, v_desc + ((kk * 2048) >> 4), idesc, (acc || kk > 0) ? 1u : 0u);
@@ -214,7 +222,7 @@ __device__ __forceinline__ void fwd_issue_pv(uint32_t tmem_o, uint32_t tmem_p, u
 // with fewer steps just stops issuing) and both release each K/V slot.
 // Runs converged: waits and descriptors are warp-uniform and `elect.sync`
 // picks the issuing lane inside each MMA and commit.
-template <int D>
+template <int D, bool FD>
 __device__ __forceinline__ void fwd_mma(const FwdWork& w, int tile, uint32_t tmem, uint32_t smem_base,
                                         uint64_t* full, uint64_t* empty, uint64_t* q_full, uint64_t* s_full,
                                         uint64_t* p_full, uint64_t* o_done, int ks, uint32_t idesc_pv,
@@ -234,7 +242,7 @@ __device__ __forceinline__ void fwd_mma(const FwdWork& w, int tile, uint32_t tme
   if (!mbar_wait_w(q_full, 0, g, kSiteFwd | 3u)) return;
   if (!group_wait(0)) return;
   if (n_t > 0) {
-    fwd_issue_s<D>(t_s, q_desc, k_desc0 + slot_off(0), ks);
+    fwd_issue_s<D, FD>(t_s, q_desc, k_desc0 + slot_off(0), ks);
     tc_commit_w(&s_full[tile]);
   }
   tc_commit_w(&empty[0]);   // group 0: K_0
@@ -244,9 +252,9 @@ __device__ __forceinline__ void fwd_mma(const FwdWork& w, int tile, uint32_t tme
     if (j < n_t) {
       if (!mbar_wait_w(&p_full[tile], j & 1, g, tile ? (kSiteFwd | 5u) : (kSiteFwd | 4u))) return;
       tc_fence_after();
-      fwd_issue_pv<D>(t_o, t_s, v_desc0 + slot_off(iv), j > 0, idesc_pv);
+      fwd_issue_pv<D, FD>(t_o, t_s, v_desc0 + slot_off(iv), j > 0, idesc_pv);
       if (j + 1 < n_t) {
-        fwd_issue_s<D>(t_s, q_desc, k_desc0 + slot_off(ik), ks);
+        fwd_issue_s<D, FD>(t_s, q_desc, k_desc0 + slot_off(ik), ks);
         tc_commit_w(&s_full[tile]);
       } else {
         tc_commit_w(&o_done[tile]);
@@ -263,7 +271,7 @@ __device__ __forceinline__ void fwd_mma(const FwdWork& w, int tile, uint32_t tme
 // PV product and the next S product go out back to back.  Run by the whole
 // warp: waits and descriptors are warp-uniform and `elect.sync` picks the
 // issuing lane inside each MMA and commit.
-template <int D>
+template <int D, bool FD>
 __device__ __forceinline__ void fwd_mma_both(const FwdWork& w, uint32_t tmem, uint32_t smem_base, uint64_t* full,
                                         uint64_t* empty, uint64_t* q_full, uint64_t* s_full, uint64_t* p_full,
                                         uint64_t* o_done, int ks, uint32_t idesc_pv, const CtaGuard& g) {
@@ -281,11 +289,11 @@ __device__ __forceinline__ void fwd_mma_both(const FwdWork& w, uint32_t tmem, ui
   if (!mbar_wait_w(q_full, 0, g, kSiteFwd | 3u)) return;
   if (!group_wait(0)) return;
   if (w.n0 > 0) {
-    fwd_issue_s<D>(tmem + C::col_s(0), q_desc[0], k_desc0 + slot_off(0), ks);
+    fwd_issue_s<D, FD>(tmem + C::col_s(0), q_desc[0], k_desc0 + slot_off(0), ks);
     tc_commit_w(&s_full[0]);
   }
   if (w.n1 > 0) {
-    fwd_issue_s<D>(tmem + C::col_s(1), q_desc[1], k_desc0 + slot_off(0), ks);
+    fwd_issue_s<D, FD>(tmem + C::col_s(1), q_desc[1], k_desc0 + slot_off(0), ks);
     tc_commit_w(&s_full[1]);
   }
   tc_commit_w(&empty[0]);   // group 0: K_0
@@ -297,16 +305,16 @@ __device__ __forceinline__ void fwd_mma_both(const FwdWork& w, uint32_t tmem, ui
     if (j < w.n0) {
       if (!mbar_wait_w(&p_full[0], j & 1, g, kSiteFwd | 4u)) return;
       tc_fence_after();
-      fwd_issue_pv<D>(tmem + C::col_o(0), tmem + C::col_s(0), vd, j > 0, idesc_pv);
-      if (next && j + 1 < w.n0) fwd_issue_s<D>(tmem + C::col_s(0), q_desc[0], kd, ks);
+      fwd_issue_pv<D, FD>(tmem + C::col_o(0), tmem + C::col_s(0), vd, j > 0, idesc_pv);
+      if (next && j + 1 < w.n0) fwd_issue_s<D, FD>(tmem + C::col_s(0), q_desc[0], kd, ks);
       if (j == w.n0 - 1) tc_commit_w(&o_done[0]);
       if (next && j + 1 < w.n0) tc_commit_w(&s_full[0]);
     }
     if (j < w.n1) {
       if (!mbar_wait_w(&p_full[1], j & 1, g, kSiteFwd | 5u)) return;
       tc_fence_after();
-      fwd_issue_pv<D>(tmem + C::col_o(1), tmem + C::col_s(1), vd, j > 0, idesc_pv);
-      if (next && j + 1 < w.n1) fwd_issue_s<D>(tmem + C::col_s(1), q_desc[1], kd, ks);
+      fwd_issue_pv<D, FD>(tmem + C::col_o(1), tmem + C::col_s(1), vd, j > 0, idesc_pv);
+      if (next && j + 1 < w.n1) fwd_issue_s<D, FD>(tmem + C::col_s(1), q_desc[1], kd, ks);
       if (j == w.n1 - 1) tc_commit_w(&o_done[1]);
       if (next && j + 1 < w.n1) tc_commit_w(&s_full[1]);
     }
@@ -506,7 +514,8 @@ __device__ __forceinline__ void fwd_softmax(const FwdWork& w, int tile, uint32_t
 // tmO is then the fp32 partial-output map and lse the partial LSE.  N is the
 // query length and Nk the key length (equal outside split-KV launches).
 // DROPOUT: dropout on the probabilities (mask from `drop`, see fwd_softmax).
-template <int D, bool CAUSAL, int ISSUERS, bool SPLIT, bool DROPOUT>
+// FD: d == D (compile-time K steps and output width of the products).
+template <int D, bool CAUSAL, int ISSUERS, bool SPLIT, bool DROPOUT, bool FD>
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -577,9 +586,9 @@ __global__ void __launch_bounds__(384, 1)
     } else if (warp == 9 || (ISSUERS == 2 && warp == 10)) {
       // issuing warps (warp 9 also owns TMEM): whole-warp loops, one elected lane issues
       if (ISSUERS == 2)
-        fwd_mma<D>(w, warp - 9, tmem, smem_u32(smem), full, empty, q_full, s_full, p_full, o_done, ks, idesc_pv, g);
+        fwd_mma<D, FD>(w, warp - 9, tmem, smem_u32(smem), full, empty, q_full, s_full, p_full, o_done, ks, idesc_pv, g);
       else
-        fwd_mma_both<D>(w, tmem, smem_u32(smem), full, empty, q_full, s_full, p_full, o_done, ks, idesc_pv, g);
+        fwd_mma_both<D, FD>(w, tmem, smem_u32(smem), full, empty, q_full, s_full, p_full, o_done, ks, idesc_pv, g);
       tc_commit_w(drain);  // every MMA issued above has finished before TMEM is released
       mbar_drain(drain, 0);
       __syncwarp();
@@ -603,7 +612,9 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
                          const CUtensorMap& to, float* lse, const Shape& s, const DropArgs& drop,
                          const WaitCfg& wc, cudaStream_t st) {
   using C = FwdCfg<D>;
-  auto kern = fa_fwd_kernel<D, CAUSAL, ISSUERS, false, DROPOUT>;
+  // d == D: the compile-time instantiation; two issuing warps only there
+  auto kern = s.d == D ? fa_fwd_kernel<D, CAUSAL, ISSUERS, false, DROPOUT, true>
+                       : fa_fwd_kernel<D, CAUSAL, 1, false, DROPOUT, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   // The warpgroups' register split must fit the launch allocation, or the
@@ -688,7 +699,8 @@ cudaError_t launch_fwd_splitkv_t(const CUtensorMap& tq, const CUtensorMap& tk, c
   const int n_kt = (Nk + 127) / 128;
   cudaError_t e;
   if (n_splits > 0) {
-    auto kern = fa_fwd_kernel<D, false, 1, true, false>;
+    auto kern = s.d == D ? fa_fwd_kernel<D, false, 1, true, false, true>
+                         : fa_fwd_kernel<D, false, 1, true, false, false>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     cudaFuncAttributes attr;

@@ -132,7 +132,9 @@ __device__ __forceinline__ uint64_t kstep_off(int kk) {
 
 // The MMA warp: S(0) S(1) | PV(0) S(2) | PV(1) S(3) | ... | PV(n-1).
 // ks = ceil(d / 16) steps of 16 columns hold data (9..16 here); the second
-// half of O is idesc_pv1 wide (N = ceil(d / 16) * 16 - 128).
+// half of O is idesc_pv1 wide (N = ceil(d / 16) * 16 - 128).  FD (d = 256):
+// compile-time steps and widths; otherwise the steps are predicated.
+template <bool FD>
 __device__ void f256_mma(const W256& w, uint32_t tmem, uint32_t sbase, uint64_t* full, uint64_t* empty,
                          uint64_t* q_full, uint64_t* s_full, uint64_t* p_full, uint64_t* o_ready, int ks,
                          uint32_t idesc_pv1, const CtaGuard& g) {
@@ -154,7 +156,11 @@ __device__ void f256_mma(const W256& w, uint32_t tmem, uint32_t sbase, uint64_t*
       const uint64_t q = h ? qd1 : qd0, k = kd0 + slot_off(2 * t + h);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        if (8 * h + kk < ks) tc_mma_ss_w(ts, q + kstep_off(kk), k + kstep_off(kk), idesc_s, (h | kk) ? 1u : 0u);
+        if constexpr (FD)
+          tc_mma_ss_w(ts, q + kstep_off(kk), k + kstep_off(kk), idesc_s, (h | kk) ? 1u : 0u);
+        else
+          tc_mma_ss_w_if(ts, q + kstep_off(kk), k + kstep_off(kk), idesc_s, (h | kk) ? 1u : 0u,
+                         8 * h + kk < ks ? 1u : 0u);
     }
     tc_commit_w(&s_full[buf]);
     tc_commit_w(&empty[t % C::kTileBars]);
@@ -174,7 +180,7 @@ __device__ void f256_mma(const W256& w, uint32_t tmem, uint32_t sbase, uint64_t*
       const uint64_t v = vd0 + slot_off(2 * t + h);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)   // 128 keys, 16 per MMA; P packs 2 keys per TMEM column
-        tc_mma_ts_w(tmem + C::kColO + 128u * h, tp + kk * 8, v + ((kk * 2048) >> 4), h ? idesc_pv1 : idesc_pv,
+        tc_mma_ts_w(tmem + C::kColO + 128u * h, tp + kk * 8, v + ((kk * 2048) >> 4), (h && !FD) ? idesc_pv1 : idesc_pv,
                     (j > 0 || kk > 0) ? 1u : 0u);
     }
     tc_commit_w(o_ready);
@@ -321,7 +327,7 @@ __device__ void f256_softmax(const W256& w, uint32_t tmem, uint8_t* smem, uint64
   if (row < N) lse[static_cast<size_t>(w.bh) * N + row] = l > 0.f ? (m_use + __log2f(l)) * kLn2 : -INFINITY;
 }
 
-template <bool CAUSAL>
+template <bool CAUSAL, bool FD>
 __global__ void __launch_bounds__(192, 1)
     fa_fwd_d256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -376,7 +382,7 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 4) {
     if (lane == 0) f256_producer(w, smem, full, empty, q_full, &tmQ, &tmK, &tmV, g);
   } else if (warp == 5) {
-    f256_mma(w, tmem, smem_u32(smem), full, empty, q_full, s_full, p_full, o_ready, ks, idesc_pv1, g);
+    f256_mma<FD>(w, tmem, smem_u32(smem), full, empty, q_full, s_full, p_full, o_ready, ks, idesc_pv1, g);
     tc_commit_w(drain);   // every MMA issued above has finished before TMEM is released
     mbar_drain(drain, 0);
     __syncwarp();
@@ -396,7 +402,7 @@ template <bool CAUSAL>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
                      float* lse, const Shape& s, const WaitCfg& wc, cudaStream_t st) {
   using C = F256;
-  auto kern = fa_fwd_d256_kernel<CAUSAL>;
+  auto kern = s.d == 256 ? fa_fwd_d256_kernel<CAUSAL, true> : fa_fwd_d256_kernel<CAUSAL, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int n_qt = (s.N + 127) / 128;

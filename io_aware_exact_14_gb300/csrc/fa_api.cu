@@ -23,6 +23,87 @@ WaitCfg next_wait_cfg() {
   return WaitCfg{e, kDefaultWaitLimitUs, -1};
 }
 
+unsigned long long current_context_id() {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(fn);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  return get_id(ctx, &id) == CUDA_SUCCESS ? id : 0;
+}
+
+cudaError_t prepare_kernel(const void* kern, uint32_t smem_bytes, int threads, uint32_t regs_needed) {
+  struct Entry {
+    unsigned long long ctx;
+    const void* kern;
+  };
+  static std::mutex mu;
+  static Entry done[256];
+  static int n_done = 0;
+  const unsigned long long ctx = current_context_id();
+  if (ctx != 0) {
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n_done; ++i)
+      if (done[i].ctx == ctx && done[i].kern == kern) return cudaSuccess;
+  }
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes));
+  if (e != cudaSuccess) return e;
+  if (regs_needed > 0) {
+    // the warpgroups' register split must fit the launch allocation, or the
+    // warpgroups asking for more would wait forever in setmaxnreg.inc
+    cudaFuncAttributes attr;
+    e = cudaFuncGetAttributes(&attr, kern);
+    if (e != cudaSuccess) return e;
+    if (static_cast<uint32_t>(attr.numRegs) * static_cast<uint32_t>(threads) < regs_needed)
+      return cudaErrorInvalidConfiguration;
+  }
+  const unsigned long long ctx_now = ctx != 0 ? ctx : current_context_id();   // the calls above bind one
+  if (ctx_now != 0) {
+    std::lock_guard<std::mutex> lock(mu);
+    bool seen = false;
+    for (int i = 0; i < n_done && !seen; ++i) seen = done[i].ctx == ctx_now && done[i].kern == kern;
+    if (!seen) {
+      if (n_done == 256) n_done = 0;   // more kernels x contexts than ever expected: start over
+      done[n_done++] = Entry{ctx_now, kern};
+    }
+  }
+  return cudaSuccess;
+}
+
+cudaError_t sm_count(int* out) {
+  static std::atomic<int> cached[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64) {
+    const int c = cached[dev].load(std::memory_order_relaxed);
+    if (c > 0) {
+      *out = c;
+      return cudaSuccess;
+    }
+  }
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64) cached[dev].store(sms, std::memory_order_relaxed);
+  *out = sms;
+  return cudaSuccess;
+}
+
 }  // namespace fa
 
 namespace {
@@ -100,11 +181,44 @@ fa_status check_disjoint(std::initializer_list<Span> outs, std::initializer_list
   return FA_OK;
 }
 
+// Encoded tensor maps, per thread: a map is a pure function of the base
+// address, sizes, strides and box, so a call that repeats an earlier one's
+// buffers reuses its maps instead of encoding them again.  Direct-mapped.
+struct MapKey {
+  const void* base;
+  long long d, N, H, B, sn, sh, sb;
+  unsigned box_rows;
+  bool operator==(const MapKey& o) const {
+    return base == o.base && d == o.d && N == o.N && H == o.H && B == o.B && sn == o.sn && sh == o.sh &&
+           sb == o.sb && box_rows == o.box_rows;
+  }
+};
+struct MapSlot {
+  bool valid;
+  MapKey key;
+  CUtensorMap map;
+};
+constexpr int kMapSlots = 64;
+thread_local MapSlot t_maps[kMapSlots];
+
+size_t map_slot(const MapKey& k) {
+  uint64_t h = reinterpret_cast<uintptr_t>(k.base) * 0x9E3779B97F4A7C15ull;
+  for (long long v : {k.d, k.N, k.H, k.B, k.sn, k.sh, k.sb, static_cast<long long>(k.box_rows)})
+    h = (h ^ static_cast<uint64_t>(v)) * 0x100000001B3ull;
+  return static_cast<size_t>(h >> 40) % kMapSlots;
+}
+
 // 4-D view {d, N, H, B} of a [B, H, N, d] bf16 tensor with element strides
 // `st` (d contiguous); boxes of 64 x 128 rows with the 128-byte swizzle the
 // tensor-core descriptors expect.  Rows past N and columns past d read as
 // zero and are clipped on store.
 fa_status make_map(CUtensorMap* m, const void* base, const Shape& s, const Strides& st, unsigned box_rows = 128) {
+  const MapKey key{base, s.d, s.N, s.H, s.B, st.n, st.h, st.b, box_rows};
+  MapSlot& slot = t_maps[map_slot(key)];
+  if (slot.valid && slot.key == key) {
+    *m = slot.map;
+    return FA_OK;
+  }
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(s.d), static_cast<cuuint64_t>(s.N),
                               static_cast<cuuint64_t>(s.H), static_cast<cuuint64_t>(s.B)};
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(st.n) * 2, static_cast<cuuint64_t>(st.h) * 2,
@@ -114,7 +228,11 @@ fa_status make_map(CUtensorMap* m, const void* base, const Shape& s, const Strid
   const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
                               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? FA_OK : fail("cuTensorMapEncodeTiled", static_cast<int>(r), "invalid tensor map");
+  if (r != CUDA_SUCCESS) return fail("cuTensorMapEncodeTiled", static_cast<int>(r), "invalid tensor map");
+  slot.valid = true;
+  slot.key = key;
+  slot.map = *m;
+  return FA_OK;
 }
 
 fa_status make_map(CUtensorMap* m, const void* base, const Shape& s) {
@@ -260,11 +378,7 @@ struct SplitPlan {
 
 fa_status split_plan(int B, int H, int Nq, int Nk, int d, int want, SplitPlan& p) {
   int sms = 0;
-  if (want <= 0) {
-    int dev = 0;
-    FA_TRY(cuda_status(cudaGetDevice(&dev), "cudaGetDevice"));
-    FA_TRY(cuda_status(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev), "cudaDeviceGetAttribute"));
-  }
+  if (want <= 0) FA_TRY(cuda_status(fa::sm_count(&sms), "reading the SM count"));
   fa::splitkv_chunks(B, H, Nq, Nk, want, sms, p.kt_per_split, p.n_splits);
   const size_t rows = static_cast<size_t>(B) * H * Nq * p.n_splits;
   p.o_bytes = round256(rows * fa::kernel_dim(d) * 4);

@@ -1244,7 +1244,7 @@ cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CU
                           cudaStream_t st) {
   using C = DkdvCfg<D>;
   auto kern = s.d == D ? fa_bwd_dkdv_kernel<D, CAUSAL, DROPOUT, true> : fa_bwd_dkdv_kernel<D, CAUSAL, DROPOUT, false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  const cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), C::kSmemBytes, C::kThreads, 0);
   if (e != cudaSuccess) return e;
   const int n_tiles = (s.N + 127) / 128;
   const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
@@ -1261,7 +1261,7 @@ cudaError_t launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
                         const Shape& s, const DropArgs& drop, const WaitCfg& wc, cudaStream_t st) {
   using C = DqCfg<D>;
   auto kern = s.d == D ? fa_bwd_dq_kernel<D, CAUSAL, DROPOUT, true> : fa_bwd_dq_kernel<D, CAUSAL, DROPOUT, false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  const cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), C::kSmemBytes, C::kThreads, 0);
   if (e != cudaSuccess) return e;
   const int n_tiles = (s.N + 127) / 128;
   const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
@@ -1316,10 +1316,8 @@ cudaError_t launch_bwd_dq(const CUtensorMap& tq, const CUtensorMap& tk, const CU
 cudaError_t launch_bwd_preprocess(const void* o, const Strides& so, const void* dO, const Strides& sdo, float* Dvec,
                                   const Shape& s, cudaStream_t st) {
   const long long rows = static_cast<long long>(s.B) * s.H * s.N;
-  int dev = 0, sms = 148;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int sms = 148;
+  const cudaError_t e = sm_count(&sms);
   if (e != cudaSuccess) return e;
   const int rows_per_block = (kPreThreads / (kernel_dim(s.d) / 8)) * kPreUnroll;
   const long long want = (rows + rows_per_block - 1) / rows_per_block;
@@ -1351,31 +1349,6 @@ cudaError_t launch_bwd_preprocess(const void* o, const Strides& so, const void* 
 // 8 MiB until the process exits; all calls share them.
 static __device__ __align__(256) float g_noalloc_rows[kNoAllocRows];
 
-// The current context's unique id (cuCtxGetCurrent + cuCtxGetId, fetched
-// through the runtime so nothing links libcuda); false when unavailable.
-bool current_context_id(unsigned long long* id) {
-  using GetCurrent = CUresult (*)(CUcontext*);
-  using GetId = CUresult (*)(CUcontext, unsigned long long*);
-  static GetCurrent get_current = nullptr;
-  static GetId get_id = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
-    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      get_current = reinterpret_cast<GetCurrent>(fn);
-    fn = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      get_id = reinterpret_cast<GetId>(fn);
-  });
-  CUcontext ctx = nullptr;
-  if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr)
-    return false;
-  return get_id(ctx, id) == CUDA_SUCCESS;
-}
-
 // A symbol's host-side name is not a device address, and the address belongs
 // to one context: it is looked up (cudaGetSymbolAddress, which allocates
 // nothing) on the first call with a device current and again whenever the
@@ -1389,15 +1362,14 @@ cudaError_t noalloc_scratch(float** out) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  unsigned long long ctx = 0;
-  const bool known_ctx = current_context_id(&ctx);
+  const unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr || !known_ctx || ctx_of[dev] != ctx) {
+  if (addr[dev] == nullptr || ctx == 0 || ctx_of[dev] != ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_rows);   // binds the device's context if none was current
     if (e != cudaSuccess) return e;
     addr[dev] = static_cast<float*>(p);
-    ctx_of[dev] = current_context_id(&ctx) ? ctx : 0;
+    ctx_of[dev] = current_context_id();
   }
   *out = addr[dev];
   return cudaSuccess;

@@ -498,7 +498,7 @@ cudaError_t launch_t(const CUtensorMap& r1, const CUtensorMap& r2, const CUtenso
                      cudaStream_t st) {
   using C = B256<MODE>;
   auto kern = s.d == 256 ? fa_bwd_d256_kernel<MODE, CAUSAL, true> : fa_bwd_d256_kernel<MODE, CAUSAL, false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  const cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), C::kSmemBytes, C::kThreads, 0);
   if (e != cudaSuccess) return e;
   const int n_res = (s.N + 127) / 128;
   const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);

@@ -612,10 +612,8 @@ template <int D>
 cudaError_t launch_quant_d(const void* x, void* out, float* descale, int B, int H, int N, int d, bool transpose,
                            long long ldv, const QuantArgs& qa, cudaStream_t st) {
   const int BH = B * H;
-  int dev = 0, sms = 148;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int sms = 148;
+  cudaError_t e = sm_count(&sms);
   if (e != cudaSuccess) return e;
   e = cudaMemsetAsync(descale, 0, static_cast<size_t>(BH) * sizeof(float), st);
   if (e != cudaSuccess) return e;
@@ -642,12 +640,9 @@ cudaError_t launch_fwd_fp8_t(const CUtensorMap& tq, const CUtensorMap& tk, const
                              const Shape& s, const WaitCfg& wc, cudaStream_t st) {
   using C = Fp8Cfg;
   auto kern = fa_fwd_fp8_kernel<CAUSAL>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  // opt-in shared memory; the softmax warpgroups' setmaxnreg split must fit the launch allocation
+  const cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), C::kSmemBytes, C::kThreads, C::kRegsNeeded);
   if (e != cudaSuccess) return e;
-  cudaFuncAttributes attr;
-  e = cudaFuncGetAttributes(&attr, kern);
-  if (e != cudaSuccess) return e;
-  if (static_cast<uint32_t>(attr.numRegs) * C::kThreads < C::kRegsNeeded) return cudaErrorInvalidConfiguration;
   const int n_qt = (s.N + 127) / 128;
   const int n_pairs = (n_qt + 1) / 2;
   const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);

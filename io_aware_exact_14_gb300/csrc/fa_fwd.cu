@@ -615,14 +615,9 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   // d == D: the compile-time instantiation; two issuing warps only there
   auto kern = s.d == D ? fa_fwd_kernel<D, CAUSAL, ISSUERS, false, DROPOUT, true>
                        : fa_fwd_kernel<D, CAUSAL, 1, false, DROPOUT, false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  // opt-in shared memory; the softmax warpgroups' setmaxnreg split must fit the launch allocation
+  const cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), C::kSmemBytes, C::kThreads, C::kRegsNeeded);
   if (e != cudaSuccess) return e;
-  // The warpgroups' register split must fit the launch allocation, or the
-  // softmax warpgroups would wait forever in setmaxnreg.inc.
-  cudaFuncAttributes attr;
-  e = cudaFuncGetAttributes(&attr, kern);
-  if (e != cudaSuccess) return e;
-  if (static_cast<uint32_t>(attr.numRegs) * C::kThreads < C::kRegsNeeded) return cudaErrorInvalidConfiguration;
   const int n_qt = (s.N + 127) / 128;
   const int n_pairs = (n_qt + 1) / 2;
   const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
@@ -701,12 +696,8 @@ cudaError_t launch_fwd_splitkv_t(const CUtensorMap& tq, const CUtensorMap& tk, c
   if (n_splits > 0) {
     auto kern = s.d == D ? fa_fwd_kernel<D, false, 1, true, false, true>
                          : fa_fwd_kernel<D, false, 1, true, false, false>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    e = prepare_kernel(reinterpret_cast<const void*>(kern), C::kSmemBytes, C::kThreads, C::kRegsNeeded);
     if (e != cudaSuccess) return e;
-    cudaFuncAttributes attr;
-    e = cudaFuncGetAttributes(&attr, kern);
-    if (e != cudaSuccess) return e;
-    if (static_cast<uint32_t>(attr.numRegs) * C::kThreads < C::kRegsNeeded) return cudaErrorInvalidConfiguration;
     const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
     const dim3 grid(static_cast<unsigned>(BH) * n_splits * n_qt);
     kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, top, lse_part, s.N, n_qt, BH, s.H, 1, scale_log2,

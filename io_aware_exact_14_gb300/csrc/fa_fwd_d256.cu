@@ -403,7 +403,7 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
                      float* lse, const Shape& s, const WaitCfg& wc, cudaStream_t st) {
   using C = F256;
   auto kern = s.d == 256 ? fa_fwd_d256_kernel<CAUSAL, true> : fa_fwd_d256_kernel<CAUSAL, false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  const cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), C::kSmemBytes, C::kThreads, 0);
   if (e != cudaSuccess) return e;
   const int n_qt = (s.N + 127) / 128;
   const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);

@@ -62,6 +62,20 @@ constexpr uint32_t kDefaultWaitLimitUs = 4000000;   // 4 s
 // The next launch's configuration: a fresh epoch, the default limit, no hook.
 WaitCfg next_wait_cfg();
 
+// Host-side launch preparation, done once instead of on every call (a call
+// right after a synchronisation otherwise paid tens of microseconds of it):
+//   prepare_kernel: the opt-in dynamic shared-memory size, and the check that
+//     the launch's register allocation covers the warpgroups' setmaxnreg
+//     split (regs_needed = 0: no split), once per kernel and CUDA context;
+//     failures are not remembered;
+//   sm_count: the current device's SM count, looked up once per device;
+//   current_context_id: the current CUDA context's unique id (cuCtxGetCurrent
+//     and cuCtxGetId, fetched through the runtime so nothing links libcuda),
+//     0 when no context is current or the driver cannot say.
+cudaError_t prepare_kernel(const void* kern, uint32_t smem_bytes, int threads, uint32_t regs_needed);
+cudaError_t sm_count(int* out);
+unsigned long long current_context_id();
+
 // Head dims: any multiple of 8 from 8 to 256 runs in the kernel built for
 // D = 64 (d <= 64), D = 128 (d <= 128) or D = 256.  The tensor maps carry the
 // true extent d, so TMA loads fill columns d .. D-1 of every tile with zeros

@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU-baseline time budget")
     ap.add_argument("--batch", type=int, default=None, help="override B (smaller cases for profiler captures)")
+    ap.add_argument("--head-dim", type=int, default=None,
+                    help="override d (any multiple of 8 up to 256; d > 128 runs the wide-head kernels)")
     ap.add_argument("--dropout", type=float, default=0.0,
                     help="drop probability p: time fa_fwd_dropout + fa_bwd_dropout instead (fwd and bwd split only)")
     ap.add_argument("--fp8", action="store_true",
@@ -205,8 +207,12 @@ def run_ours(args, dist: Dist):
     if args.batch is not None:
         import dataclasses
         w = dataclasses.replace(w, B=args.batch, name=f"{w.name}@B={args.batch}")
+    if args.head_dim is not None:
+        import dataclasses
+        w = dataclasses.replace(w, d=args.head_dim, name=f"{w.name}@d={args.head_dim}")
     causal = w.causal[-1]
     B, H, N, d = w.shape
+    wide = d > 128
     scale = w.scale
     x = make_inputs(B, H, N, d, w.seed + 100 * dist.rank, w.qk_mult, with_grad=True)
     q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
@@ -281,7 +287,8 @@ def run_ours(args, dist: Dist):
     peaks, peak_src = load_peaks()
     burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    names = ["fa_fwd_kernel", "fa_bwd_preprocess_kernel", "fa_bwd_dkdv_kernel", "fa_bwd_dq_kernel"]
+    names = (["fa_fwd_d256_kernel", "fa_bwd_preprocess_kernel", "fa_bwd_d256_kernel<dV>+<dK>", "fa_bwd_d256_kernel<dQ>"]
+             if wide else ["fa_fwd_kernel", "fa_bwd_preprocess_kernel", "fa_bwd_dkdv_kernel", "fa_bwd_dq_kernel"])
     work = [counts.attn_flops(B, H, N, d, causal, "fwd"), counts.preprocess_bytes(B, H, N, d),
             counts.dkdv_flops(B, H, N, d, causal), counts.dq_flops(B, H, N, d, causal)]
     kernels = {}
@@ -312,7 +319,7 @@ def run_ours(args, dist: Dist):
                 "frac": round(ach / burst, 3)}
     roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json bf16 burst / hbm copy)"
     roof["work_per_launch"] = work[dom]
-    roof["traffic"] = traffic_for(names[dom], src[names[dom]])
+    roof["traffic"] = traffic_for(names[dom], src[names[dom]]) if names[dom] in src else None
 
     fwd_fl = counts.attn_flops(B, H, N, d, causal, "fwd")
     bwd_fl = counts.attn_flops(B, H, N, d, causal, "bwd")
@@ -334,11 +341,13 @@ def run_ours(args, dist: Dist):
                    "step": ("fa_fwd_dropout + fa_bwd_dropout" if p_drop > 0 else
                             "fa_fwd + fa_bwd_preprocess + fa_bwd_dkdv + fa_bwd_dq"),
                    **({"dropout_p": p_drop} if p_drop > 0 else {}),
-                   "l2": "inputs larger than L2: q, k, v, o, dO are 134 MB each (L2 129 MB)",
+                   "l2": (f"inputs larger than L2: q, k, v, o, dO are {B * H * N * d * 2 / 1e6:.0f} MB each (L2 129 MB)"
+                          if B * H * N * d * 2 > 129e6 else
+                          f"q, k, v, o, dO are {B * H * N * d * 2 / 1e6:.0f} MB each: below the 129 MB L2"),
                    "parallelism": "replicas" if dist.world > 1 else "single GPU"},
         "frac_of_peak": round(value / dist.world / burst, 3),
         "passes": passes, "kernels": kernels, "roofline": roof,
-        "gpu_launches": 4 * args.steps, "clocks": clk,
+        "gpu_launches": (5 if wide else 4) * args.steps, "clocks": clk,
         **({"note": "dropout timing line, not the headline"} if p_drop > 0 else {}),
     }
     if e2e is not None:

@@ -6,7 +6,9 @@ counted once: S recomputed, dP, dV, dK, dQ), both halved for a causal mask.
 
 Per-kernel executed work of the backward: the dK/dV kernel runs four
 contractions per (query tile, key tile) pair (S^T, dP^T, dV, dK) and the dQ
-kernel three (S, dP, dQ), so 14*B*H*N^2*d executed against 10 counted.
+kernel three (S, dP, dQ), so 14*B*H*N^2*d executed against 10 counted.  For
+wide heads (d > 128) dK and dV are two launches that each recompute S^T
+(S^T, dV; S^T, dP^T, dK), so the dK/dV step executes five contractions.
 """
 from __future__ import annotations
 
@@ -21,7 +23,7 @@ def attn_flops(B: int, H: int, N: int, d: int, causal: bool, pass_: str = "fwd")
 
 
 def dkdv_flops(B: int, H: int, N: int, d: int, causal: bool) -> float:
-    f = 8.0 * B * H * N * N * d
+    f = (10.0 if d > 128 else 8.0) * B * H * N * N * d
     return f / 2 if causal else f
 
 

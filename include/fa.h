@@ -232,8 +232,8 @@ fa_status fa_bwd_dropout(const void* q, const void* k, const void* v, const void
  *                K with the same seed (Q K^T is unchanged).  d must be 64 or
  *                128 (FA_ERR_UNSUPPORTED otherwise).
  * d must be a multiple of 16 in [16, 128] (FA_ERR_UNSUPPORTED).  descale is
- * fp32 [B, H] device memory; x, out 16-byte aligned.  A memset and three
- * kernels on `stream`.
+ * fp32 [B, H] device memory; x, out 16-byte aligned.  One kernel on
+ * `stream` (a cluster launch: one 8-CTA cluster per (b, h)).
  */
 fa_status fa_fp8_quantize(const void* x, void* out, float* descale, int B, int H, int N, int d,
                           int transpose, int rotate, unsigned long long seed, struct CUstream_st* stream);

@@ -461,10 +461,16 @@ struct QuantArgs {
   int rotate;
 };
 
-template <int D>
-__device__ __forceinline__ void load_row8(const uint8_t* __restrict__ x, long long row, int d, int sub, float (&v)[8]) {
+// A row's 8 bf16 values of lane `sub` as raw bits (0 past d), and their fp32
+// values.  Callers load all rows of a tile first, so the loads are in flight
+// together before the rotations' shuffles.
+__device__ __forceinline__ uint4 load_raw8(const uint8_t* __restrict__ x, long long row, int d, int sub) {
   uint4 u = make_uint4(0u, 0u, 0u, 0u);
   if (sub * 8 < d) u = *reinterpret_cast<const uint4*>(x + (static_cast<size_t>(row) * d + sub * 8) * 2);
+  return u;
+}
+
+__device__ __forceinline__ void unpack8(const uint4& u, float (&v)[8]) {
   const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -512,27 +518,118 @@ __device__ __forceinline__ uint32_t row_signs8(const QuantArgs& a, int sub) {
   return (word >> (8 * (sub % 4))) & 0xFFu;
 }
 
-// One block per 128-row tile of one head (block t: head t / n_tiles): the
-// tile's max |x| is reduced on chip and lands in amax[head] with one atomic.
-template <int D>
-__global__ void __launch_bounds__(kQThreads) fa_fp8_amax_kernel(const uint8_t* __restrict__ x, unsigned int* amax,
-                                                               int N, int d, QuantArgs qa) {
+// Thread-block cluster helpers: a barrier over the cluster's CTAs (release /
+// acquire, so shared-memory writes before it are visible after it) and a
+// load from another CTA's shared memory.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float ld_cluster_f32(const void* local, uint32_t rank) {
+  uint32_t remote;
+  float v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+
+// The codes of one 128-row tile (rows n0 ..) of head bh with scale s: out[row,
+// c], or out[(bh * d + c) * ldv + n] transposed, staged through shared memory
+// so that each 16-byte store holds 16 keys of one row of V^T.  In the staging
+// tile, row r's 8-byte column blocks are XOR-swizzled by (r / 16) mod 8: the
+// gather reads one column of rows 16 apart, which would otherwise all fall
+// in one shared-memory bank.
+template <int D, bool TRANSPOSE>
+__device__ __forceinline__ void quant_tile(const uint8_t* __restrict__ x, uint8_t* __restrict__ out, int bh, int n0,
+                                           int N, int d, long long ldv, float s, uint32_t signs,
+                                           const QuantArgs& qa, uint8_t (*tile)[D + 16]) {
   constexpr int kTpr = D / 8, kRows = kQThreads / kTpr;
+  const int sub = threadIdx.x % kTpr;
+  uint4 raw[128 / kRows];
+#pragma unroll
+  for (int it = 0; it < 128 / kRows; ++it) {   // all the tile's loads go out first
+    const int n = n0 + threadIdx.x / kTpr + it * kRows;
+    raw[it] = load_raw8(x, static_cast<long long>(bh) * N + (n < N ? n : N - 1), d, sub);
+  }
+#pragma unroll
+  for (int it = 0; it < 128 / kRows; ++it) {
+    const int rr = threadIdx.x / kTpr + it * kRows;
+    const int n = n0 + rr;
+    float v[8];
+    unpack8(raw[it], v);
+    if (qa.rotate) rotate_row8<D>(v, sub, signs, qa.inv_sqrt_d);
+    uint2 c;
+    c.x = e4m3x4(__fmul_rn(v[0], s), __fmul_rn(v[1], s), __fmul_rn(v[2], s), __fmul_rn(v[3], s));
+    c.y = e4m3x4(__fmul_rn(v[4], s), __fmul_rn(v[5], s), __fmul_rn(v[6], s), __fmul_rn(v[7], s));
+    if (n >= N) c = make_uint2(0u, 0u);
+    if constexpr (TRANSPOSE) {
+      if (sub * 8 < D) *reinterpret_cast<uint2*>(&tile[rr][(sub * 8) ^ (((rr >> 4) & 7) * 8)]) = c;
+    } else {
+      if (n < N && sub * 8 < d) *reinterpret_cast<uint2*>(out + (static_cast<size_t>(bh) * N + n) * d + sub * 8) = c;
+    }
+  }
+  if constexpr (TRANSPOSE) {
+    __syncthreads();
+    // row c of V^T gets keys n0 .. n0 + 127 (those below ldv), 16 per store
+    for (int i = threadIdx.x; i < d * 8; i += kQThreads) {
+      const int c = i / 8, k16 = (i % 8) * 16;
+      if (n0 + k16 >= ldv) continue;
+      const int cs = c ^ ((k16 >> 4) * 8);   // rows k16 .. k16 + 15 share one swizzle
+      uint32_t wv[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        wv[q] = tile[k16 + 4 * q][cs] | (tile[k16 + 4 * q + 1][cs] << 8) | (tile[k16 + 4 * q + 2][cs] << 16) |
+                (static_cast<uint32_t>(tile[k16 + 4 * q + 3][cs]) << 24);
+      *reinterpret_cast<uint4*>(out + (static_cast<size_t>(bh) * d + c) * ldv + n0 + k16) =
+          make_uint4(wv[0], wv[1], wv[2], wv[3]);
+    }
+    __syncthreads();
+  }
+}
+
+// One cluster of kQCluster CTAs per head (b, h): CTA r takes the head's
+// 128-row tiles r * per, .. (per = ceil(tiles / kQCluster)).  Pass 1: each CTA
+// reduces max |x| (after the optional rotation) over its rows; the cluster
+// combines the partial maxima through distributed shared memory.  Pass 2:
+// each CTA reads its rows again -- L2 hits, since only the heads of the
+// clusters in flight (about SMs / kQCluster of them) are being read -- and
+// writes their codes with s = 448 / amax; rank 0 writes descale = amax / 448
+// (1 for an all-zero head).  One launch, each input byte read once from HBM.
+constexpr int kQCluster = 8;
+
+template <int D, bool TRANSPOSE>
+__global__ void __launch_bounds__(kQThreads) fa_fp8_quant_cluster_kernel(const uint8_t* __restrict__ x,
+                                                                        uint8_t* __restrict__ out,
+                                                                        float* __restrict__ descale, int N, int d,
+                                                                        long long ldv, QuantArgs qa) {
+  constexpr int kTpr = D / 8, kRows = kQThreads / kTpr;
+  __shared__ __align__(16) uint8_t tile[128][D + 16];   // transposed path: 128 rows (keys) x d codes
   __shared__ float wmax[kQThreads / 32];
+  __shared__ float cta_max;
+  const int bh = static_cast<int>(blockIdx.x / kQCluster);
+  const int rank = static_cast<int>(blockIdx.x % kQCluster);   // the CTA's rank in its cluster (clusters along x)
   const int sub = threadIdx.x % kTpr;
   const uint32_t signs = row_signs8<D>(qa, sub);
   const int n_tiles = (N + 127) / 128;
-  const int bh = static_cast<int>(blockIdx.x / n_tiles), n0 = static_cast<int>(blockIdx.x % n_tiles) * 128;
+  const int per = (n_tiles + kQCluster - 1) / kQCluster;
+  const int t0 = rank * per, t1 = min(n_tiles, t0 + per);
   float m = 0.f;
+  for (int t = t0; t < t1; ++t) {
+    uint4 raw[128 / kRows];
 #pragma unroll
-  for (int it = 0; it < 128 / kRows; ++it) {
-    const int n = n0 + threadIdx.x / kTpr + it * kRows;
-    float v[8];
-    load_row8<D>(x, static_cast<long long>(bh) * N + (n < N ? n : N - 1), d, sub, v);
-    if (qa.rotate) rotate_row8<D>(v, sub, signs, qa.inv_sqrt_d);
-    if (n < N) {
+    for (int it = 0; it < 128 / kRows; ++it) {   // all the tile's loads go out first
+      const int n = t * 128 + threadIdx.x / kTpr + it * kRows;
+      raw[it] = load_raw8(x, static_cast<long long>(bh) * N + (n < N ? n : N - 1), d, sub);
+    }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
+    for (int it = 0; it < 128 / kRows; ++it) {
+      const int n = t * 128 + threadIdx.x / kTpr + it * kRows;
+      float v[8];
+      unpack8(raw[it], v);
+      if (qa.rotate) rotate_row8<D>(v, sub, signs, qa.inv_sqrt_d);
+      if (n < N) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
+      }
     }
   }
 #pragma unroll
@@ -540,98 +637,42 @@ __global__ void __launch_bounds__(kQThreads) fa_fp8_amax_kernel(const uint8_t* _
   if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
   __syncthreads();
   if (threadIdx.x == 0) {
-    float t = 0.f;
+    float c = 0.f;
 #pragma unroll
-    for (int i = 0; i < kQThreads / 32; ++i) t = fmaxf(t, wmax[i]);
-    atomicMax(&amax[bh], __float_as_uint(t));   // t >= 0: the bits order as the values
+    for (int i = 0; i < kQThreads / 32; ++i) c = fmaxf(c, wmax[i]);
+    cta_max = c;
   }
-}
-
-// Codes: out[row, c] (or out[(bh * d + c) * ldv + n] transposed, staged
-// through shared memory so that each 16-byte store holds 16 keys of one row).
-template <int D, bool TRANSPOSE>
-__global__ void __launch_bounds__(kQThreads) fa_fp8_quant_kernel(const uint8_t* __restrict__ x,
-                                                                uint8_t* __restrict__ out,
-                                                                const unsigned int* __restrict__ amax, int BH,
-                                                                int N, int d, long long ldv, QuantArgs qa) {
-  constexpr int kTpr = D / 8, kRows = kQThreads / kTpr;
-  __shared__ __align__(16) uint8_t tile[128][D + 16];   // transposed path: 128 rows (keys) x d codes
-  const int sub = threadIdx.x % kTpr;
-  const uint32_t signs = row_signs8<D>(qa, sub);
-  const int n_tiles = (N + 127) / 128;
-  for (long long t = blockIdx.x; t < static_cast<long long>(BH) * n_tiles; t += gridDim.x) {
-    const int bh = static_cast<int>(t / n_tiles), n0 = static_cast<int>(t % n_tiles) * 128;
-    const float am = __uint_as_float(amax[bh]);
-    const float s = am > 0.f ? __fdiv_rn(kE4m3Max, am) : 1.f;
+  cluster_sync();   // every CTA's partial maximum is written
+  float am = 0.f;
 #pragma unroll
-    for (int it = 0; it < 128 / kRows; ++it) {   // fixed trip count: the loads can all go out first
-      const int rr = threadIdx.x / kTpr + it * kRows;
-      const int n = n0 + rr;
-      float v[8];
-      load_row8<D>(x, static_cast<long long>(bh) * N + (n < N ? n : N - 1), d, sub, v);
-      if (qa.rotate) rotate_row8<D>(v, sub, signs, qa.inv_sqrt_d);
-      uint2 c;
-      c.x = e4m3x4(__fmul_rn(v[0], s), __fmul_rn(v[1], s), __fmul_rn(v[2], s), __fmul_rn(v[3], s));
-      c.y = e4m3x4(__fmul_rn(v[4], s), __fmul_rn(v[5], s), __fmul_rn(v[6], s), __fmul_rn(v[7], s));
-      if (n >= N) c = make_uint2(0u, 0u);
-      if constexpr (TRANSPOSE) {
-        if (sub * 8 < D) *reinterpret_cast<uint2*>(&tile[rr][sub * 8]) = c;
-      } else {
-        if (n < N && sub * 8 < d)
-          *reinterpret_cast<uint2*>(out + (static_cast<size_t>(bh) * N + n) * d + sub * 8) = c;
-      }
-    }
-    if constexpr (TRANSPOSE) {
-      __syncthreads();
-      // row c of V^T gets keys n0 .. n0 + 127 (those below ldv), 16 per store
-      for (int i = threadIdx.x; i < d * 8; i += kQThreads) {
-        const int c = i / 8, k16 = (i % 8) * 16;
-        if (n0 + k16 >= ldv) continue;
-        uint32_t wv[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          wv[q] = tile[k16 + 4 * q][c] | (tile[k16 + 4 * q + 1][c] << 8) | (tile[k16 + 4 * q + 2][c] << 16) |
-                  (static_cast<uint32_t>(tile[k16 + 4 * q + 3][c]) << 24);
-        *reinterpret_cast<uint4*>(out + (static_cast<size_t>(bh) * d + c) * ldv + n0 + k16) =
-            make_uint4(wv[0], wv[1], wv[2], wv[3]);
-      }
-      __syncthreads();
-    }
-  }
-}
-
-__global__ void fa_fp8_descale_kernel(unsigned int* amax_then_descale, int BH) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < BH) {
-    const float am = __uint_as_float(amax_then_descale[i]);
-    reinterpret_cast<float*>(amax_then_descale)[i] = am > 0.f ? __fdiv_rn(am, kE4m3Max) : 1.f;
-  }
+  for (int r = 0; r < kQCluster; ++r) am = fmaxf(am, ld_cluster_f32(&cta_max, static_cast<uint32_t>(r)));
+  cluster_sync();   // no CTA leaves while another may still read its partial
+  if (rank == 0 && threadIdx.x == 0) descale[bh] = am > 0.f ? __fdiv_rn(am, kE4m3Max) : 1.f;
+  const float s = am > 0.f ? __fdiv_rn(kE4m3Max, am) : 1.f;
+  for (int t = t0; t < t1; ++t) quant_tile<D, TRANSPOSE>(x, out, bh, t * 128, N, d, ldv, s, signs, qa, tile);
 }
 
 template <int D>
 cudaError_t launch_quant_d(const void* x, void* out, float* descale, int B, int H, int N, int d, bool transpose,
                            long long ldv, const QuantArgs& qa, cudaStream_t st) {
-  const int BH = B * H;
-  int sms = 148;
-  cudaError_t e = sm_count(&sms);
-  if (e != cudaSuccess) return e;
-  e = cudaMemsetAsync(descale, 0, static_cast<size_t>(BH) * sizeof(float), st);
-  if (e != cudaSuccess) return e;
-  auto* am = reinterpret_cast<unsigned int*>(descale);
+  const long long ctas = static_cast<long long>(B) * H * kQCluster;
+  if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+  cfg.blockDim = dim3(kQThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kQCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   const auto* xb = static_cast<const uint8_t*>(x);
-  const long long tiles = static_cast<long long>(BH) * ((N + 127) / 128);
-  if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  fa_fp8_amax_kernel<D><<<static_cast<unsigned>(tiles), kQThreads, 0, st>>>(xb, am, N, d, qa);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const int qgrid = static_cast<int>(tiles < 8LL * sms ? tiles : 8LL * sms);
-  if (transpose)
-    fa_fp8_quant_kernel<D, true><<<qgrid, kQThreads, 0, st>>>(xb, static_cast<uint8_t*>(out), am, BH, N, d, ldv, qa);
-  else
-    fa_fp8_quant_kernel<D, false><<<qgrid, kQThreads, 0, st>>>(xb, static_cast<uint8_t*>(out), am, BH, N, d, ldv,
-                                                               qa);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  fa_fp8_descale_kernel<<<(BH + 255) / 256, 256, 0, st>>>(am, BH);
-  return cudaGetLastError();
+  auto* ob = static_cast<uint8_t*>(out);
+  return transpose ? cudaLaunchKernelEx(&cfg, fa_fp8_quant_cluster_kernel<D, true>, xb, ob, descale, N, d, ldv, qa)
+                   : cudaLaunchKernelEx(&cfg, fa_fp8_quant_cluster_kernel<D, false>, xb, ob, descale, N, d, ldv, qa);
 }
 
 template <bool CAUSAL>

@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG, "libfa.so")
 
-SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_fwd_d256.cu", "fa_bwd.cu", "fa_bwd_d256.cu", "fa_fp8.cu"]
+SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_fwd_q4.cu", "fa_fwd_d256.cu", "fa_bwd.cu", "fa_bwd_d256.cu", "fa_fp8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "--expt-relaxed-constexpr"]

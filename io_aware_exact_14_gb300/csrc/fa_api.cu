@@ -503,6 +503,13 @@ fa_status fwd_impl(const void* q, const fa_strides* qs, const void* k, const fa_
   if (d > 128)
     return cuda_status(fa::launch_fwd_d256(tq, tk, tv, to, lse, s, fa::next_wait_cfg(), stream),
                        "forward kernel launch");
+  if (d <= 64 && drop.t4 == 0 && wait == nullptr) {   // narrow heads: four query tiles per CTA
+    CUtensorMap tk64, tv64;
+    FA_TRY(make_map(&tk64, k, s, Sk, 64));
+    FA_TRY(make_map(&tv64, v, s, Sv, 64));
+    return cuda_status(fa::launch_fwd_q4(tq, tk64, tv64, to, lse, s, fa::next_wait_cfg(), stream),
+                       "forward kernel launch");
+  }
   return cuda_status(fa::launch_fwd(tq, tk, tv, to, lse, s, drop, wait ? *wait : fa::next_wait_cfg(), stream),
                      "forward kernel launch");
 }
@@ -783,8 +790,11 @@ fa_status fa_debug_status(int reset) {
   uint32_t x = 0;
   e = fa::bwd_d256_status(&x, reset != 0);
   if (e != cudaSuccess) return fail("reading the wide-head backward status word", e, cudaGetErrorString(e));
-  g_last_site = a ? a : (b ? b : (c ? c : (w ? w : x)));
-  return (a | b | c | w | x) ? FA_ERR_TIMEOUT : FA_OK;
+  uint32_t y = 0;
+  e = fa::fwd_q4_status(&y, reset != 0);
+  if (e != cudaSuccess) return fail("reading the narrow-head forward status word", e, cudaGetErrorString(e));
+  g_last_site = a ? a : (b ? b : (c ? c : (w ? w : (x ? x : y))));
+  return (a | b | c | w | x | y) ? FA_ERR_TIMEOUT : FA_OK;
 }
 
 unsigned int fa_debug_site(void) { return g_last_site; }

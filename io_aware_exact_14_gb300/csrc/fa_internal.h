@@ -111,6 +111,12 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
 cudaError_t launch_fwd_d256(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& to, float* lse, const Shape& s, const WaitCfg& wc, cudaStream_t st);
 
+// Forward for narrow heads (d <= 64, no dropout): four query tiles per CTA,
+// 64-key steps (fa_fwd_q4.cu).  Q and O maps with 128-row boxes, K and V maps
+// with 64-row boxes.
+cudaError_t launch_fwd_q4(const CUtensorMap& tq, const CUtensorMap& tk64, const CUtensorMap& tv64,
+                          const CUtensorMap& to, float* lse, const Shape& s, const WaitCfg& wc, cudaStream_t st);
+
 // Split-KV forward for short query blocks against long key sequences
 // (non-causal): Q maps {d, Nq, H, B} (s.N = Nq), K/V maps {d, Nk, H, B}; each
 // chunk of key tiles writes its normalised O (fp32, map `top` {d, Nq,
@@ -227,5 +233,6 @@ cudaError_t bwd_status(uint32_t* out, bool reset);
 cudaError_t fp8_status(uint32_t* out, bool reset);
 cudaError_t fwd_d256_status(uint32_t* out, bool reset);
 cudaError_t bwd_d256_status(uint32_t* out, bool reset);
+cudaError_t fwd_q4_status(uint32_t* out, bool reset);
 
 }  // namespace fa

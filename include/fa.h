@@ -311,9 +311,10 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
                          struct CUstream_st* stream);
 
 /*
- * Test hook of the deadlock guard; not for production use.  fa_fwd with
- * every pipeline wait bounded by wait_limit_us (>= 1) instead of the built-in
- * 4 s, and with the copy producer of every CTA withholding K/V group
+ * Test hook of the deadlock guard; not for production use.  fa_fwd's
+ * two-query-tile kernel (d <= 128, whatever kernel fa_fwd would pick for d)
+ * with every pipeline wait bounded by wait_limit_us (>= 1) instead of the
+ * built-in 4 s, and with the copy producer of every CTA withholding K/V group
  * withhold_group (>= 0) and all later ones: group 0 is K_0, group j+1 holds
  * V_j and K_{j+1}.  The tensor-core warp's wait for that group then runs into
  * the limit; the CTA records FA_ERR_TIMEOUT (fa_debug_status; fa_debug_site()
@@ -322,9 +323,9 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
  * copies and products already issued complete, frees its tensor memory and
  * returns.  O and LSE are then incomplete.  Launches made before or after are
  * unaffected: a launch that gives up ends only its own waits.  A group index
- * past the last group withholds nothing (the call behaves as fa_fwd).
- * FA_ERR_INVALID_ARG for withhold_group < 0 or wait_limit_us == 0; other
- * arguments and errors as fa_fwd.
+ * past the last group withholds nothing (the call computes what fa_fwd
+ * does).  FA_ERR_INVALID_ARG for withhold_group < 0 or wait_limit_us == 0;
+ * FA_ERR_UNSUPPORTED for d > 128; other arguments and errors as fa_fwd.
  */
 fa_status fa_debug_fwd_withhold(const void* q, const void* k, const void* v, void* o, float* lse,
                                 int B, int H, int N, int d, float scale, int causal, int withhold_group,

@@ -18,7 +18,8 @@ def _bnhd(t):
     return t.transpose(1, 2).contiguous().transpose(1, 2)
 
 
-@pytest.mark.parametrize("B,H,N,d,causal", [(2, 3, 300, 64, True), (1, 4, 257, 128, False), (2, 2, 512, 128, True)])
+@pytest.mark.parametrize("B,H,N,d,causal", [(2, 3, 300, 64, True), (1, 4, 257, 128, False), (2, 2, 512, 128, True),
+                                             (1, 2, 300, 256, True), (2, 2, 200, 192, False), (1, 3, 700, 40, True)])
 def test_fwd_bnhd_bitwise_and_parity(B, H, N, d, causal):
     x, g = device_inputs(B, H, N, d, seed=610 + N + d)
     o_ref_dev, lse_ref_dev = fa.fa_fwd(g["q"], g["k"], g["v"], None, causal)
@@ -34,7 +35,8 @@ def test_fwd_bnhd_bitwise_and_parity(B, H, N, d, causal):
     assert oracle.lse_max_abs_err(f64(lse), lse64) <= TOL_LSE
 
 
-@pytest.mark.parametrize("B,H,N,d,causal", [(2, 3, 300, 64, True), (1, 2, 384, 128, False)])
+@pytest.mark.parametrize("B,H,N,d,causal", [(2, 3, 300, 64, True), (1, 2, 384, 128, False), (1, 2, 300, 256, True),
+                                             (1, 1, 200, 160, False)])
 def test_bwd_packed_qkv_bitwise_and_parity(B, H, N, d, causal):
     """q, k, v read from one [B, N, 3, H, d] buffer and dq, dk, dv written into
     another; o and dO stored as [N, B, H, d]."""

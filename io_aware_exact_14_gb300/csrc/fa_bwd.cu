@@ -943,7 +943,7 @@ __global__ void __launch_bounds__(384, 1)
         // Pending dQ stores, oldest first (a ring of 4, by unit index): unit p
         // ended at key tile last[p & 3] and staged dQ in that tile's K slot,
         // which K(last + 3) reuses; the store goes out just before that load.
-        int pend_bh[4], pend_qt[4], pend_last[4];
+        int pend_bh[4] = {}, pend_qt[4] = {}, pend_last[4] = {};
         int pend_head = 0, pend_tail = 0;   // unit indices: [head, tail) pending
         auto store_front = [&]() -> bool {
           const int p = pend_head & 3;

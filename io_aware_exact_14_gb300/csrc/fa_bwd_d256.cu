@@ -65,8 +65,8 @@ struct B256 {
   static constexpr uint32_t kVecOff = kT2Off + kT2Slots * kStrTile;     // 64 fp32 per streamed slot
   static constexpr uint32_t kBarOff = kVecOff + 4 * 256;
   // r_full, t1_full[2], t1_empty[2], t2_full[2], t2_empty[2], s_full[2],
-  // dp_full, ds_full, acc_done, staged, drain
-  static constexpr int kBars = 1 + 8 + 7;
+  // dp_full, ds_full[2], acc_done, staged, drain
+  static constexpr int kBars = 1 + 8 + 8;
   static constexpr uint32_t kMiscOff = kBarOff + kBars * 8;   // tmem holder, abort flag
   static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;
   static_assert(kSmemBytes <= 232448, "shared-memory budget");
@@ -229,7 +229,10 @@ __device__ void b256_mma(const U256& w, uint32_t tmem, uint32_t sbase, uint64_t*
   if (w.n > 1 && !issue_s(1)) return;
   for (int j = 0; j < w.n; ++j) {
     if (!C::kHasDP && !w2(j)) return;   // DV: dO_i
-    if (!mbar_wait_w(ds_full, j & 1, g, kSiteBwd256 | 5u)) return;
+    // ds_full by step parity: without a dP product (DV) the compute warps can
+    // finish step j + 1 before this wait, but not step j + 2 (S(j + 2) goes
+    // out below)
+    if (!mbar_wait_w(&ds_full[j & 1], (j >> 1) & 1, g, kSiteBwd256 | 5u)) return;
     tc_fence_after();
     if (C::kHasDP) {
       b256_acc<MODE, FD>(tmem + C::kColAcc, tmem + C::kColDP, t1m(j % C::kT1Slots), j > 0, idesc_acc);   // += dS K_j / dS^T Q_i
@@ -326,7 +329,7 @@ __device__ void b256_compute(const U256& w, uint32_t tmem, uint8_t* smem, uint64
       tmem_st32(tS, pk);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(ds_full);
+      mbar_arrive(&ds_full[j & 1]);
       continue;
     }
     if (MODE == kModeDK && !mbar_wait(&t2_full[j & 1], (j >> 1) & 1, g, kSiteBwd256 | 8u)) return;
@@ -371,7 +374,7 @@ __device__ void b256_compute(const U256& w, uint32_t tmem, uint8_t* smem, uint64
     tmem_st32(tDP, pk);   // dS (or dS^T) over the first 32 dP columns
     tmem_st_wait();
     tc_fence_before();
-    mbar_arrive(ds_full);
+    mbar_arrive(&ds_full[j & 1]);
   }
 
   // epilogue: acc * mult -> bf16 -> swizzled staging in the first resident
@@ -426,8 +429,8 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* t2_empty = t2_full + 2;   // [2]
   uint64_t* s_full = t2_empty + 2;    // [2]
   uint64_t* dp_full = s_full + 2;
-  uint64_t* ds_full = dp_full + 1;
-  uint64_t* acc_done = ds_full + 1;
+  uint64_t* ds_full = dp_full + 1;    // [2], by step parity
+  uint64_t* acc_done = ds_full + 2;
   uint64_t* staged = acc_done + 1;
   uint64_t* drain = staged + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
@@ -446,7 +449,8 @@ __global__ void __launch_bounds__(192, 1)
     mbar_init(&s_full[0], 1);
     mbar_init(&s_full[1], 1);
     mbar_init(dp_full, 1);
-    mbar_init(ds_full, 128);
+    mbar_init(&ds_full[0], 128);
+    mbar_init(&ds_full[1], 128);
     mbar_init(acc_done, 1);
     mbar_init(staged, 128);
     mbar_init(drain, 1);

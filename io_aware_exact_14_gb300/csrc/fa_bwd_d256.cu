@@ -65,13 +65,19 @@ struct B256 {
   static constexpr uint32_t kVecOff = kT2Off + kT2Slots * kStrTile;     // 64 fp32 per streamed slot
   static constexpr uint32_t kBarOff = kVecOff + 4 * 256;
   // r_full, t1_full[2], t1_empty[2], t2_full[2], t2_empty[2], s_full[2],
-  // dp_full, ds_full[2], acc_done, staged, drain
-  static constexpr int kBars = 1 + 8 + 8;
+  // dp_full, ds_full[2], acc_done, staged, drain, a_ready
+  static constexpr int kBars = 1 + 8 + 9;
   static constexpr uint32_t kMiscOff = kBarOff + kBars * 8;   // tmem holder, abort flag
   static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;
   static_assert(kSmemBytes <= 232448, "shared-memory budget");
   static constexpr int kThreads = 192;
   static constexpr uint32_t kColDP = 128, kColAcc = 256;
+  // DV (no dP product): the resident tile (K_j) is copied into the dP
+  // columns and its score products take A from TMEM (TS form): a 64-row
+  // streamed B operand from shared memory alone keeps the tensor core at
+  // full rate, where an N = 64 product with both operands in shared memory
+  // runs at 2/3 of it (the operand reads hit the 128 bytes per clock limit).
+  static constexpr bool kTmemA = MODE == kModeDV;
   __host__ __device__ static constexpr uint32_t t1_off(int s) { return kT1Off + s * kStrTile; }
   __host__ __device__ static constexpr uint32_t t2_off(int s) { return kT2Off + s * kStrTile; }
   __host__ __device__ static constexpr uint32_t t1_vec(int j) { return kVecOff + (j & 1) * 256; }
@@ -184,6 +190,21 @@ __device__ __forceinline__ void b256_score(uint32_t tmem_d, uint64_t a_desc, uin
   }
 }
 
+// The same with A (128 x d, bf16) in TMEM: K step kk at column a_tmem + 8 kk.
+template <int MODE, bool FD>
+__device__ __forceinline__ void b256_score_ts(uint32_t tmem_d, uint32_t a_tmem, uint64_t b_desc, int ks) {
+  using C = B256<MODE>;
+  constexpr uint32_t idesc = idesc_bf16(128, 64, false, false);
+#pragma unroll
+  for (int kk = 0; kk < 16; ++kk) {
+    const uint64_t ob = ((kk / 4) * C::kStrBox + (kk % 4) * 32) >> 4;
+    if constexpr (FD)
+      tc_mma_ts_w(tmem_d, a_tmem + kk * 8, b_desc + ob, idesc, kk > 0 ? 1u : 0u);
+    else
+      tc_mma_ts_w_if(tmem_d, a_tmem + kk * 8, b_desc + ob, idesc, kk > 0 ? 1u : 0u, kk < ks ? 1u : 0u);
+  }
+}
+
 // Accumulating product acc(128 x d) += A(128 x 64, bf16 in TMEM) * B(64 x d),
 // B a streamed tile read MN-major (64-column blocks 8 KB apart); idesc has
 // N = ceil(d / 16) * 16.
@@ -199,8 +220,8 @@ __device__ __forceinline__ void b256_acc(uint32_t tmem_acc, uint32_t a_tmem, uin
 template <int MODE, bool FD>
 __device__ void b256_mma(const U256& w, uint32_t tmem, uint32_t sbase, uint64_t* r_full, uint64_t* t1_full,
                          uint64_t* t1_empty, uint64_t* t2_full, uint64_t* t2_empty, uint64_t* s_full,
-                         uint64_t* dp_full, uint64_t* ds_full, uint64_t* acc_done, int ks, uint32_t idesc_acc,
-                         const CtaGuard& g) {
+                         uint64_t* dp_full, uint64_t* ds_full, uint64_t* acc_done, uint64_t* a_ready, int ks,
+                         uint32_t idesc_acc, const CtaGuard& g) {
   using C = B256<MODE>;
   const uint64_t r1 = sdesc_sw128(sbase + C::kR1Off, 16, 1024);
   const uint64_t r2 = sdesc_sw128(sbase + C::kR2Off, 16, 1024);
@@ -212,7 +233,10 @@ __device__ void b256_mma(const U256& w, uint32_t tmem, uint32_t sbase, uint64_t*
   auto w2 = [&](int j) { return mbar_wait_w(&t2_full[j & 1], (j >> 1) & 1, g, kSiteBwd256 | 3u); };
   auto issue_s = [&](int j) -> bool {   // S(j) into buffer j & 1
     if (!w1(j)) return false;
-    b256_score<MODE, FD>(tmem + 64u * (j & 1), r1, t1k(j % C::kT1Slots), ks);
+    if constexpr (C::kTmemA)
+      b256_score_ts<MODE, FD>(tmem + 64u * (j & 1), tmem + C::kColDP, t1k(j % C::kT1Slots), ks);
+    else
+      b256_score<MODE, FD>(tmem + 64u * (j & 1), r1, t1k(j % C::kT1Slots), ks);
     tc_commit_w(&s_full[j & 1]);
     return true;
   };
@@ -224,6 +248,10 @@ __device__ void b256_mma(const U256& w, uint32_t tmem, uint32_t sbase, uint64_t*
     return true;
   };
   if (!mbar_wait_w(r_full, 0, g, kSiteBwd256 | 4u)) return;
+  if (C::kTmemA) {   // the resident tile is in TMEM (copied by the compute warps)
+    if (!mbar_wait_w(a_ready, 0, g, kSiteBwd256 | 12u)) return;
+    tc_fence_after();
+  }
   if (!issue_s(0)) return;
   if (C::kHasDP && !issue_dp(0)) return;
   if (w.n > 1 && !issue_s(1)) return;
@@ -249,15 +277,37 @@ __device__ void b256_mma(const U256& w, uint32_t tmem, uint32_t sbase, uint64_t*
 }
 
 template <int MODE, bool CAUSAL>
-__device__ void b256_compute(const U256& w, uint32_t tmem, uint8_t* smem, uint64_t* t1_full, uint64_t* t2_full,
-                             uint64_t* s_full, uint64_t* dp_full, uint64_t* ds_full, uint64_t* acc_done,
-                             uint64_t* staged, const CUtensorMap* tmOut, const float* __restrict__ lse,
-                             const float* __restrict__ Dg, int N, int d, float scale, float scale_log2,
-                             const CtaGuard& g) {
+__device__ void b256_compute(const U256& w, uint32_t tmem, uint8_t* smem, uint64_t* r_full, uint64_t* t1_full,
+                             uint64_t* t2_full, uint64_t* s_full, uint64_t* dp_full, uint64_t* ds_full,
+                             uint64_t* acc_done, uint64_t* a_ready, uint64_t* staged, const CUtensorMap* tmOut,
+                             const float* __restrict__ lse, const float* __restrict__ Dg, int N, int d, float scale,
+                             float scale_log2, const CtaGuard& g) {
   using C = B256<MODE>;
   const int r = threadIdx.x & 127;
   const uint32_t lane_base = static_cast<uint32_t>((threadIdx.x >> 5) & 3) * 32u << 16;
   const uint32_t sbase = smem_u32(smem);
+  if constexpr (C::kTmemA) {
+    // row r of the resident tile (swizzled boxes of 64 columns) into TMEM lane
+    // r: box b's 128 bytes fill columns kColDP + 32b .. + 32 (two bf16 each)
+    if (!mbar_wait(r_full, 0, g, kSiteBwd256 | 13u)) return;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      uint32_t v[32];
+      const uint32_t row = sbase + C::kR1Off + b * C::kResBox + r * 128;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const float4 x = ld_shared_f4(row + ((c ^ (r & 7)) << 4));
+        v[4 * c] = __float_as_uint(x.x);
+        v[4 * c + 1] = __float_as_uint(x.y);
+        v[4 * c + 2] = __float_as_uint(x.z);
+        v[4 * c + 3] = __float_as_uint(x.w);
+      }
+      tmem_st32(tmem + lane_base + C::kColDP + 32 * b, v);
+    }
+    tmem_st_wait();
+    tc_fence_before();
+    mbar_arrive(a_ready);
+  }
   const int res_row = 128 * w.u + r;   // DQ: query row; DK, DV: key row
   // DQ: this row's terms (-inf / 0 past N, so P = dS = 0 there)
   float nl = -INFINITY, nd = 0.f;
@@ -433,6 +483,7 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* acc_done = ds_full + 2;
   uint64_t* staged = acc_done + 1;
   uint64_t* drain = staged + 1;
+  uint64_t* a_ready = drain + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kMiscOff + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -454,6 +505,7 @@ __global__ void __launch_bounds__(192, 1)
     mbar_init(acc_done, 1);
     mbar_init(staged, 128);
     mbar_init(drain, 1);
+    mbar_init(a_ready, 128);
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -479,7 +531,7 @@ __global__ void __launch_bounds__(192, 1)
                         N, g);
   } else if (warp == 5) {
     b256_mma<MODE, FD>(w, tmem, smem_u32(smem), r_full, t1_full, t1_empty, t2_full, t2_empty, s_full, dp_full, ds_full,
-                   acc_done, ks, idesc_acc, g);
+                       acc_done, a_ready, ks, idesc_acc, g);
     tc_commit_w(drain);   // every MMA issued above has finished before TMEM is released
     mbar_drain(drain, 0);
     __syncwarp();
@@ -488,8 +540,8 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   } else {
-    b256_compute<MODE, CAUSAL>(w, tmem, smem, t1_full, t2_full, s_full, dp_full, ds_full, acc_done, staged, &tmOut,
-                               lse, Dg, N, d, scale, scale_log2, g);
+    b256_compute<MODE, CAUSAL>(w, tmem, smem, r_full, t1_full, t2_full, s_full, dp_full, ds_full, acc_done, a_ready,
+                               staged, &tmOut, lse, Dg, N, d, scale, scale_log2, g);
     __syncwarp();
     tc_fence_before();
     named_bar_sync(1, 160);

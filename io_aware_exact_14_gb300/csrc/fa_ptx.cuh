@@ -362,6 +362,19 @@ __device__ __forceinline__ void tc_mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// TS form issued only where `issue` is non-zero (see tc_mma_ss_w_if).
+__device__ __forceinline__ void tc_mma_ts_w_if(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t accumulate, uint32_t issue) {
+  asm volatile(
+      "{\n\t.reg .pred e, p, q;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.ne.and.b32 q, %5, 0, e;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(issue)
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation issued so far by the
 // issuing lane has completed.
 __device__ __forceinline__ void tc_commit_w(uint64_t* bar) {

@@ -345,7 +345,14 @@ const char* fa_status_string(fa_status s);
  */
 fa_status fa_debug_status(int reset);
 
-/* Site code of the first recorded timeout (0 if none); valid after fa_debug_status. */
+/*
+ * Site code of the first recorded timeout (0 if none); valid after
+ * fa_debug_status.  The high byte names the kernel: 0x1 forward (d <= 128,
+ * two query tiles per CTA), 0x2 dK/dV, 0x3 dQ (d <= 128), 0x4 wide-head
+ * forward, 0x5 wide-head backward (its dV, dK and dQ launches), 0x6
+ * narrow-head forward (d <= 64, four query tiles per CTA), 0x7 FP8 forward;
+ * the low byte names the wait inside that kernel.
+ */
 unsigned int fa_debug_site(void);
 
 /*

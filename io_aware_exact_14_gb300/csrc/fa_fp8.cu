@@ -37,7 +37,7 @@ namespace fa {
 namespace {
 
 __device__ unsigned int g_status_fp8[2] = {0, 0};   // status, abort epoch (see CtaGuard)
-constexpr uint32_t kSiteFp8 = 0x400u;
+constexpr uint32_t kSiteFp8 = 0x700u;
 constexpr float kRescaleThreshold8 = 8.0f;   // log2 units; P~ stays <= 256 < 448
 constexpr float kLn2f = 0.6931471805599453f;
 constexpr float kE4m3Max = 448.0f;

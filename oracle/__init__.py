@@ -7,6 +7,7 @@ from .attention_ref import (  # noqa: F401
     attn_fwd_ref,
     attn_fwd_ref_rows,
     attn_bwd_ref,
+    attn_bwd_ref_sampled,
     attn_fwd_dropout_ref,
     attn_bwd_dropout_ref,
     philox4x32_10,

@@ -199,6 +199,54 @@ def attn_bwd_ref(q, k, v, do, scale: float, causal: bool
     return dq, dk, dv
 
 
+def attn_bwd_ref_sampled(q, k, v, do, scale: float, causal: bool, rows: np.ndarray, cols: np.ndarray,
+                         group: int = 1024) -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """The gradients of ``attn_bwd_ref`` at selected entries, for long rows.
+
+    ``rows`` [B, H, R] selects the query rows of dQ, ``cols`` [B, H, C] the key
+    rows of dK and dV.  Returns dQ [B,H,R,d], dK [B,H,C,d], dV [B,H,C,d].
+
+    The formulas are those of ``attn_bwd_ref``.  dQ_i needs only row i of P
+    and dP.  dK_j and dV_j sum over every query row i (dV_j = sum_i P_ij dO_i,
+    dK_j = scale sum_i dS_ij Q_i), and each term needs D_i and so the whole
+    forward row i: all query rows are evaluated, ``group`` of them at a time
+    so that no N x N matrix is held; the groups' contributions are added in
+    float64.  Nothing else is reordered.
+    """
+    q, k, v, do = _as64(q), _as64(k), _as64(v), _as64(do)
+    rows = np.asarray(rows, dtype=np.int64)
+    cols = np.asarray(cols, dtype=np.int64)
+    B, H, N, d = q.shape
+    dq = np.zeros((B, H, rows.shape[2], d))
+    dk = np.zeros((B, H, cols.shape[2], d))
+    dv = np.zeros((B, H, cols.shape[2], v.shape[-1]))
+    for b in range(B):
+        for h in range(H):
+            qh, kh, vh, doh = q[b, h], k[b, h], v[b, h], do[b, h]
+            # dQ at the selected rows: rows of P, dP and dS
+            r = rows[b, h]
+            S = _scores(qh[r], kh, scale)
+            if causal:
+                S = _apply_causal(S, r)
+            P, _, _ = _softmax_stats(S)
+            dS = _grad_s(P, _grad_p(doh[r], vh), _row_term(doh[r], P @ vh))
+            dq[b, h] = _grad_q(dS, kh, scale)
+            # dK, dV at the selected keys: every query row contributes
+            c = cols[b, h]
+            for g0 in range(0, N, group):
+                g = np.arange(g0, min(N, g0 + group))
+                S = _scores(qh[g], kh, scale)
+                if causal:
+                    S = _apply_causal(S, g)
+                P, _, _ = _softmax_stats(S)
+                D = _row_term(doh[g], P @ vh)
+                Pc = P[:, c]
+                dv[b, h] += _grad_v(Pc, doh[g])
+                dSc = _grad_s(Pc, _grad_p(doh[g], vh[c]), D)
+                dk[b, h] += _grad_k(dSc, qh[g], scale)
+    return dq, dk, dv
+
+
 def bwd_preprocess_ref(o, do) -> np.ndarray:
     """D_i = sum_c dO_ic * O_ic per row, float64 [B,H,N] (the backward's row term)."""
     return (_as64(o) * _as64(do)).sum(axis=-1)

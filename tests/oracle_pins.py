@@ -246,6 +246,39 @@ def pin_finite_differences(ref):
             assert err <= 1e-7, (name, causal, err)
 
 
+def pin_sampled_gradients(ref):
+    """The sampled-entry backward (query rows taken in groups) agrees with
+    central differences of L = <dO, O> at its entries, and with the
+    materialised backward at every row and column."""
+    h = 1e-6
+    for causal, N, d, seed in ((False, 7, 3, 141), (True, 8, 2, 142)):
+        q, k, v, do = (_rand((1, 1, N, d), seed + i) for i in range(4))
+        s = 0.8
+        rows = np.array([[[0, N - 1, 3]]])
+        cols = np.array([[[N - 1, 0, 2]]])
+        dq, dk, dv = ref.attn_bwd_ref_sampled(q, k, v, do, s, causal, rows, cols, group=3)
+        for name, x, g, sel in (("q", q, dq, rows), ("k", k, dk, cols), ("v", v, dv, cols)):
+            for a, r in enumerate(sel[0, 0]):
+                for c in range(d):
+                    xp, xm = x.copy(), x.copy()
+                    xp[0, 0, r, c] += h
+                    xm[0, 0, r, c] -= h
+                    args_p = {"q": q, "k": k, "v": v}
+                    args_m = {"q": q, "k": k, "v": v}
+                    args_p[name], args_m[name] = xp, xm
+                    fd = (_loss(ref, args_p["q"], args_p["k"], args_p["v"], do, s, causal)
+                          - _loss(ref, args_m["q"], args_m["k"], args_m["v"], do, s, causal)) / (2 * h)
+                    assert abs(fd - g[0, 0, a, c]) <= 1e-7 * max(1.0, abs(fd)), (name, causal, r, c)
+    B, H, N, d = 2, 2, 50, 8
+    q, k, v, do = (_rand((B, H, N, d), 150 + i) for i in range(4))
+    every = np.broadcast_to(np.arange(N), (B, H, N))
+    for causal in (False, True):
+        full = ref.attn_bwd_ref(q, k, v, do, 0.45, causal)
+        part = ref.attn_bwd_ref_sampled(q, k, v, do, 0.45, causal, every, every, group=16)
+        for a, b in zip(full, part):
+            assert np.abs(a - b).max() <= 1e-12 * max(1.0, np.abs(a).max())
+
+
 def pin_gradient_identities(ref):
     """sum_j dK_j = 0 and sum_j dV_j = sum_i dO_i; one-hot dO gives dV_j = P_ij g."""
     B, H, N, d, s = 1, 2, 21, 5, 0.5
@@ -395,6 +428,7 @@ ALL_PINS = [
     pin_invariances,
     pin_rows_equals_full,
     pin_finite_differences,
+    pin_sampled_gradients,
     pin_gradient_identities,
     pin_preprocess,
     pin_unequal_lengths,

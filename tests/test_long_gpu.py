@@ -1,0 +1,74 @@
+"""Long sequences: one head with a million keys through the forward, a 32K-row
+causal head through the backward (16K rows for the other head dims and the
+non-causal mask), a million-key decode through split-KV.
+
+At these lengths the oracle cannot materialise S, so it is evaluated at
+sampled entries (first rows, tile edges, the ragged tail and seeded random
+picks): the forward at sampled query rows, the backward at sampled query rows
+(dQ) and key rows (dK, dV), with every query row still contributing to the
+dK and dV sums.  What this exercises beyond the other tests: offsets and
+tensor-map coordinates near 2^20, fp32 row sums and accumulators over 8192
+key steps, persistent backward units with 256 query tiles, and split-KV
+partitions of very long key ranges.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from io_aware_exact_14_gb300 import fa
+from io_aware_exact_14_gb300.workloads import make_splitkv_inputs
+from gpu_util import TOL_GRAD, TOL_LSE, TOL_O, assert_no_timeout, device_inputs, f64, o_excess_err
+
+pytestmark = pytest.mark.gpu
+
+
+def _picks(N, n_random, seed):
+    fixed = [0, 1, 127, 128, 255, 256, N // 2, N - 129, N - 128, N - 2, N - 1]
+    rng = np.random.default_rng(seed)
+    r = rng.integers(0, N, n_random)
+    return np.unique(np.clip(np.concatenate([fixed, r]), 0, N - 1))
+
+
+@pytest.mark.parametrize("N,d,causal", [(1 << 20, 128, True), (1 << 20, 128, False), ((1 << 18) - 37, 64, True),
+                                        ((1 << 18) + 77, 256, True)])
+def test_fwd_long_rows(N, d, causal):
+    x, g = device_inputs(1, 1, N, d, seed=5000 + d + causal, with_grad=False)
+    scale = 1.0 / np.sqrt(d)
+    o, lse = fa.fa_fwd(g["q"], g["k"], g["v"], scale, causal)
+    rows = _picks(N, 16, 5100 + d)[None, None, :]
+    o = f64(o[:, :, rows[0, 0]])
+    lse = f64(lse[:, :, rows[0, 0]])
+    assert_no_timeout()
+    o_ref, lse_ref = oracle.attn_fwd_ref_rows(f64(x["q"]), f64(x["k"]), f64(x["v"]), scale, causal, rows)
+    assert o_excess_err(o, o_ref) <= TOL_O
+    assert oracle.lse_max_abs_err(lse, lse_ref) <= TOL_LSE
+
+
+@pytest.mark.parametrize("N,d,causal", [(32768 + 77, 128, True), (16384 + 77, 128, False), (16384 - 5, 64, True),
+                                        (16384 + 77, 256, True)])
+def test_bwd_long_rows(N, d, causal):
+    x, g = device_inputs(1, 1, N, d, seed=5200 + d + causal, with_grad=True)
+    scale = 1.0 / np.sqrt(d)
+    o, lse = fa.fa_fwd(g["q"], g["k"], g["v"], scale, causal)
+    dq, dk, dv = fa.fa_bwd(g["q"], g["k"], g["v"], o, lse, g["do"], scale, causal)
+    rows = _picks(N, 24, 5300 + d)[None, None, :]
+    cols = _picks(N, 24, 5400 + d)[None, None, :]
+    dq, dk, dv = f64(dq[:, :, rows[0, 0]]), f64(dk[:, :, cols[0, 0]]), f64(dv[:, :, cols[0, 0]])
+    assert_no_timeout()
+    ref = oracle.attn_bwd_ref_sampled(f64(x["q"]), f64(x["k"]), f64(x["v"]), f64(x["do"]), scale, causal,
+                                      rows, cols, group=2048)
+    for name, a, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        err = oracle.rel_fro_err(a, r)
+        assert err <= TOL_GRAD, f"{name}: relative Frobenius error {err:.3g}"
+
+
+def test_splitkv_million_keys():
+    B, H, Nq, Nk, d = 1, 1, 5, 1 << 20, 128
+    x = make_splitkv_inputs(B, H, Nq, Nk, d, seed=5500)
+    g = {k: t.cuda() for k, t in x.items()}
+    o, lse = fa.fa_fwd_splitkv(g["q"], g["k"], g["v"])
+    o, lse = f64(o), f64(lse)
+    assert_no_timeout()
+    o_ref, lse_ref = oracle.attn_fwd_ref(f64(x["q"]), f64(x["k"]), f64(x["v"]), 1.0 / np.sqrt(d), False)
+    assert o_excess_err(o, o_ref) <= TOL_O
+    assert oracle.lse_max_abs_err(lse, lse_ref) <= TOL_LSE

@@ -55,6 +55,24 @@ def _philox_rounds(n):
     return f
 
 
+def _sampled_shifted_cols(q, k, v, do, s, causal, rows, cols, group=1024):
+    """dK, dV taken one key further on (an index slip in the selection)."""
+    n = np.asarray(q).shape[2]
+    return _fresh_oracle().attn_bwd_ref_sampled(q, k, v, do, s, causal, rows,
+                                                np.minimum(np.asarray(cols) + 1, n - 1), group)
+
+
+def _sampled_drop_last_group(q, k, v, do, s, causal, rows, cols, group=1024):
+    """The last (partial) group of query rows left out of dK, dV."""
+    n = np.asarray(q).shape[2]
+    keep = (n // group) * group if n % group else n - group
+    dq, _, _ = _fresh_oracle().attn_bwd_ref_sampled(q, k, v, do, s, causal, rows, cols, group)
+    sl = lambda x: np.asarray(x)[:, :, :keep]
+    _, dk, dv = _fresh_oracle().attn_bwd_ref_sampled(sl(q), k, v, sl(do), s, causal,
+                                                     np.minimum(rows, keep - 1), cols, group)
+    return dq, dk, dv
+
+
 MUTANTS = {
     "scores_without_scale": {"_scores": lambda q, k, s: q @ k.T},
     "scores_transposed": {"_scores": lambda q, k, s: s * (k @ q.T)},
@@ -75,6 +93,8 @@ MUTANTS = {
     "dropout_keep_inverted": {"dropout_keep": lambda *a: ~_fresh_oracle().dropout_keep(*a)},
     "dropout_ds_without_mask": {"_grad_s_dropout": lambda P, Mt, dP, D: P * (dP - D[:, None])},
     "philox_nine_rounds": {"philox4x32_10": _philox_rounds(9)},
+    "sampled_cols_off_by_one": {"attn_bwd_ref_sampled": _sampled_shifted_cols},
+    "sampled_last_group_dropped": {"attn_bwd_ref_sampled": _sampled_drop_last_group},
 }
 
 

@@ -61,14 +61,21 @@ def test_preprocess_row_term():
         assert np.all(np.abs(f64(Dvec) - ref) <= bound)
 
 
-def test_bwd_steps_equal_fused_call():
-    """fa_bwd equals fa_bwd_preprocess + fa_bwd_dkdv + fa_bwd_dq, bit for bit."""
-    _, g = device_inputs(1, 2, 520, 128, seed=22, with_grad=True)
-    o, lse, dq, dk, dv = _grads(g, None, True)
-    Dvec = fa.fa_bwd_preprocess(o, g["do"])
-    dk2, dv2 = fa.fa_bwd_dkdv(g["q"], g["k"], g["v"], lse, g["do"], Dvec, None, True)
-    dq2 = fa.fa_bwd_dq(g["q"], g["k"], g["v"], lse, g["do"], Dvec, None, True)
+@pytest.mark.parametrize("d,causal", [(128, True), (128, False), (64, True), (96, False), (40, True), (256, True)])
+def test_bwd_steps_equal_fused_call(d, causal):
+    """fa_bwd equals fa_bwd_preprocess + fa_bwd_dkdv + fa_bwd_dq, bit for bit,
+    and leaves the row term D in its workspace."""
+    _, g = device_inputs(2, 2, 520, d, seed=22 + d, with_grad=True)
+    q, k, v, do = g["q"], g["k"], g["v"], g["do"]
+    o, lse = fa.fa_fwd(q, k, v, None, causal)
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(2, 2, 520, d), dtype=torch.uint8, device="cuda")
+    dq, dk, dv = fa.fa_bwd(q, k, v, o, lse, do, None, causal, workspace=ws)
+    Dvec = fa.fa_bwd_preprocess(o, do)
+    dk2, dv2 = fa.fa_bwd_dkdv(q, k, v, lse, do, Dvec, None, causal)
+    dq2 = fa.fa_bwd_dq(q, k, v, lse, do, Dvec, None, causal)
     torch.cuda.synchronize()
+    assert_no_timeout()
+    assert torch.equal(ws[:Dvec.numel() * 4].view(torch.float32).view_as(Dvec), Dvec)
     assert torch.equal(dq, dq2) and torch.equal(dk, dk2) and torch.equal(dv, dv2)
 
 

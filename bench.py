@@ -444,7 +444,9 @@ def run_e2e(args, w, causal, x, dev, dist, flops_step):
                 out_done[b][t].record(s_out[t])
         started[b] = True
 
-    steps = max(2, min(args.steps, 10))
+    # the device leg's K steps (at most 50): two buffer sets fill and drain once
+    # per timed region, with one copy direction idle at each end
+    steps = max(2, min(args.steps, 50))
     for i in range(max(2, min(args.warmup, 4))):
         step(i)
     torch.cuda.synchronize()

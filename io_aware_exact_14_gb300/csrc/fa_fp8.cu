@@ -480,12 +480,25 @@ __device__ __forceinline__ void unpack8(const uint4& u, float (&v)[8]) {
   }
 }
 
-// The rotation of one row, in place (all D/8 lanes of the row take part).
-template <int D>
-__device__ __forceinline__ void rotate_row8(float (&v)[8], int sub, uint32_t signs8, float inv_sqrt_d) {
+// The lane's 8 sign flips as a mask on its raw bf16 words (bit 15 of each
+// half): flipping a bf16's sign bit before the exact widening to fp32 flips
+// the fp32 value's sign, as multiplying by -1 would.
+__device__ __forceinline__ uint4 sign_mask8(uint32_t signs8) {
+  uint32_t w[4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
-    if ((signs8 >> i) & 1u) v[i] = __uint_as_float(__float_as_uint(v[i]) ^ 0x80000000u);
+  for (int i = 0; i < 4; ++i)
+    w[i] = (((signs8 >> (2 * i)) & 1u) << 15) | (((signs8 >> (2 * i + 1)) & 1u) << 31);
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__device__ __forceinline__ uint4 xor4(const uint4& a, const uint4& b) {
+  return make_uint4(a.x ^ b.x, a.y ^ b.y, a.z ^ b.z, a.w ^ b.w);
+}
+
+// The butterfly of one sign-flipped row, in place (all D/8 lanes of the row
+// take part); the caller multiplies by 1/sqrt(d).
+template <int D>
+__device__ __forceinline__ void butterfly_row8(float (&v)[8], int sub) {
 #pragma unroll
   for (int h = 1; h < 8; h *= 2) {
 #pragma unroll
@@ -499,15 +512,16 @@ __device__ __forceinline__ void rotate_row8(float (&v)[8], int sub, uint32_t sig
   }
 #pragma unroll
   for (int m = 1; m < D / 8; m *= 2) {   // lane partner sub ^ m holds columns 8m further on (or back)
-    const bool upper = (sub & m) != 0;
+    // the lower lane keeps v + o, the upper one o - v: o + sg v with sg = +-1
+    // is exact in the product, so one fused multiply-add rounds once, as the
+    // add or the subtract would
+    const float sg = (sub & m) != 0 ? -1.f : 1.f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const float o = __shfl_xor_sync(0xffffffffu, v[i], m);
-      v[i] = upper ? __fsub_rn(o, v[i]) : __fadd_rn(v[i], o);
+      v[i] = __fmaf_rn(v[i], sg, o);
     }
   }
-#pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(v[i], inv_sqrt_d);
 }
 
 template <int D>
@@ -540,7 +554,7 @@ __device__ __forceinline__ float ld_cluster_f32(const void* local, uint32_t rank
 // in one shared-memory bank.
 template <int D, bool TRANSPOSE>
 __device__ __forceinline__ void quant_tile(const uint8_t* __restrict__ x, uint8_t* __restrict__ out, int bh, int n0,
-                                           int N, int d, long long ldv, float s, uint32_t signs,
+                                           int N, int d, long long ldv, float s, uint4 smask,
                                            const QuantArgs& qa, uint8_t (*tile)[D + 16]) {
   constexpr int kTpr = D / 8, kRows = kQThreads / kTpr;
   const int sub = threadIdx.x % kTpr;
@@ -555,8 +569,14 @@ __device__ __forceinline__ void quant_tile(const uint8_t* __restrict__ x, uint8_
     const int rr = threadIdx.x / kTpr + it * kRows;
     const int n = n0 + rr;
     float v[8];
-    unpack8(raw[it], v);
-    if (qa.rotate) rotate_row8<D>(v, sub, signs, qa.inv_sqrt_d);
+    if (qa.rotate) {
+      unpack8(xor4(raw[it], smask), v);
+      butterfly_row8<D>(v, sub);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(v[i], qa.inv_sqrt_d);
+    } else {
+      unpack8(raw[it], v);
+    }
     uint2 c;
     c.x = e4m3x4(__fmul_rn(v[0], s), __fmul_rn(v[1], s), __fmul_rn(v[2], s), __fmul_rn(v[3], s));
     c.y = e4m3x4(__fmul_rn(v[4], s), __fmul_rn(v[5], s), __fmul_rn(v[6], s), __fmul_rn(v[7], s));
@@ -608,7 +628,7 @@ __global__ void __launch_bounds__(kQThreads) fa_fp8_quant_cluster_kernel(const u
   const int bh = static_cast<int>(blockIdx.x / kQCluster);
   const int rank = static_cast<int>(blockIdx.x % kQCluster);   // the CTA's rank in its cluster (clusters along x)
   const int sub = threadIdx.x % kTpr;
-  const uint32_t signs = row_signs8<D>(qa, sub);
+  const uint4 smask = sign_mask8(row_signs8<D>(qa, sub));
   const int n_tiles = (N + 127) / 128;
   const int per = (n_tiles + kQCluster - 1) / kQCluster;
   const int t0 = rank * per, t1 = min(n_tiles, t0 + per);
@@ -624,14 +644,21 @@ __global__ void __launch_bounds__(kQThreads) fa_fp8_quant_cluster_kernel(const u
     for (int it = 0; it < 128 / kRows; ++it) {
       const int n = t * 128 + threadIdx.x / kTpr + it * kRows;
       float v[8];
-      unpack8(raw[it], v);
-      if (qa.rotate) rotate_row8<D>(v, sub, signs, qa.inv_sqrt_d);
+      if (qa.rotate) {   // (the 1/sqrt(d) factor is applied to the maximum below)
+        unpack8(xor4(raw[it], smask), v);
+        butterfly_row8<D>(v, sub);
+      } else {
+        unpack8(raw[it], v);
+      }
       if (n < N) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
       }
     }
   }
+  // rounding a product with a positive constant is monotone and odd, so the
+  // largest |fl(v c)| is fl(c max |v|): one multiply instead of one per value
+  if (qa.rotate) m = __fmul_rn(m, qa.inv_sqrt_d);
 #pragma unroll
   for (int o = 16; o > 0; o /= 2) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
@@ -649,7 +676,7 @@ __global__ void __launch_bounds__(kQThreads) fa_fp8_quant_cluster_kernel(const u
   cluster_sync();   // no CTA leaves while another may still read its partial
   if (rank == 0 && threadIdx.x == 0) descale[bh] = am > 0.f ? __fdiv_rn(am, kE4m3Max) : 1.f;
   const float s = am > 0.f ? __fdiv_rn(kE4m3Max, am) : 1.f;
-  for (int t = t0; t < t1; ++t) quant_tile<D, TRANSPOSE>(x, out, bh, t * 128, N, d, ldv, s, signs, qa, tile);
+  for (int t = t0; t < t1; ++t) quant_tile<D, TRANSPOSE>(x, out, bh, t * 128, N, d, ldv, s, smask, qa, tile);
 }
 
 template <int D>

@@ -36,6 +36,14 @@
  *     error is left in the runtime's last-error slot).  Faults inside a
  *     kernel surface at the caller's next synchronisation.
  *   - No exception ever crosses this interface.
+ *   - Stream capture: the kernels take their tensor maps and wait settings as
+ *     launch parameters, so calls may be captured into a CUDA graph and
+ *     replayed on the same buffers.  Make one call of each kind (same
+ *     entry point, head-dim class and mask) before capturing: the first
+ *     sets kernel attributes, which capture does not record.  A replayed
+ *     launch reuses the wait epoch it was captured with, so after a kernel
+ *     of that graph has given up on a wait (FA_ERR_TIMEOUT), reset the
+ *     status (fa_debug_status(1)) before replaying it again.
  */
 #ifndef FA_H_
 #define FA_H_

@@ -46,6 +46,22 @@ def test_bwd_noalloc_matches_workspace_entry_point():
             assert torch.equal(a, b), f"call {call}: {name} is not bitwise equal to fa_bwd's"
 
 
+def test_bwd_noalloc_at_its_row_limit():
+    """B*H*N = 2^21 rows, exactly the built-in scratch: equal to fa_bwd bit
+    for bit (every row of the scratch is written and read)."""
+    B, H, N, d, causal = 2, 16, 65536, 64, True
+    g = torch.Generator(device="cpu")
+    g.manual_seed(931)
+    q, k, v, do = (torch.randn((B, H, N, d), generator=g).to(torch.bfloat16).cuda() for _ in range(4))
+    o, lse = fa.fa_fwd(q, k, v, None, causal)
+    want = fa.fa_bwd(q, k, v, o, lse, do, None, causal)
+    got = fa.fa_bwd_noalloc(q, k, v, o, lse, do, None, causal)
+    torch.cuda.synchronize()
+    assert fa.fa_debug_status(reset=True) == fa.FA_OK
+    for name, a, b in zip(("dq", "dk", "dv"), got, want):
+        assert torch.equal(a, b), f"{name} is not bitwise equal to fa_bwd's at 2^21 rows"
+
+
 def test_bwd_noalloc_rejects_problems_beyond_its_scratch():
     B, H, N, d = 1, 64, 32769, 64     # 2^21 + 64 rows > the built-in 2^21
     p = [0x100000 * (i + 1) for i in range(9)]

@@ -9,10 +9,14 @@ picks): the forward at sampled query rows, the backward at sampled query rows
 dK and dV sums.  What this exercises beyond the other tests: offsets and
 tensor-map coordinates near 2^20, fp32 row sums and accumulators over 8192
 key steps, persistent backward units with 256 query tiles, and split-KV
-partitions of very long key ranges.
+partitions of very long key ranges.  A last case runs tensors of 2^31
+elements (4 GiB each) through the forward and the backward: one seeded block
+of 8 batches repeated 64 times, so every copy must give the same bits as the
+first (which the oracle checks), whatever its offset.
 """
 import numpy as np
 import pytest
+import torch
 
 import oracle
 from io_aware_exact_14_gb300 import fa
@@ -72,3 +76,28 @@ def test_splitkv_million_keys():
     o_ref, lse_ref = oracle.attn_fwd_ref(f64(x["q"]), f64(x["k"]), f64(x["v"]), 1.0 / np.sqrt(d), False)
     assert o_excess_err(o, o_ref) <= TOL_O
     assert oracle.lse_max_abs_err(lse, lse_ref) <= TOL_LSE
+
+
+def test_tensors_of_2_31_elements():
+    reps, (b0, H, N, d), causal = 64, (8, 64, 512, 128), True   # [512, 64, 512, 128]: 2^31 elements
+    x, g = device_inputs(b0, H, N, d, seed=5600, with_grad=True)
+    big = {n: t.repeat(reps, 1, 1, 1) for n, t in g.items()}
+    assert big["q"].numel() == 1 << 31
+    scale = 1.0 / np.sqrt(d)
+    o, lse = fa.fa_fwd(big["q"], big["k"], big["v"], scale, causal)
+    grads = fa.fa_bwd(big["q"], big["k"], big["v"], o, lse, big["do"], scale, causal)
+    torch.cuda.synchronize()
+    assert_no_timeout()
+    for name, t in (("o", o), ("lse", lse)) + tuple(zip(("dq", "dk", "dv"), grads)):
+        blocks = t.view(reps, -1)
+        assert bool((blocks == blocks[:1]).all()), f"{name}: a repeated block differs from the first"
+    # the first block against the oracle on two (b, h) slices
+    for b, h in ((0, 0), (b0 - 1, H - 1)):
+        sl = lambda t: f64(t[b:b + 1, h:h + 1])
+        o_ref, lse_ref = oracle.attn_fwd_ref(sl(x["q"]), sl(x["k"]), sl(x["v"]), scale, causal)
+        assert o_excess_err(sl(o), o_ref) <= TOL_O
+        assert oracle.lse_max_abs_err(sl(lse), lse_ref) <= TOL_LSE
+        ref = oracle.attn_bwd_ref(sl(x["q"]), sl(x["k"]), sl(x["v"]), sl(x["do"]), scale, causal)
+        for name, a, r in zip(("dq", "dk", "dv"), grads, ref):
+            err = oracle.rel_fro_err(sl(a), r)
+            assert err <= TOL_GRAD, f"{name}: relative Frobenius error {err:.3g}"

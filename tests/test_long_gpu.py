@@ -10,9 +10,10 @@ dK and dV sums.  What this exercises beyond the other tests: offsets and
 tensor-map coordinates near 2^20, fp32 row sums and accumulators over 8192
 key steps, persistent backward units with 256 query tiles, and split-KV
 partitions of very long key ranges.  A last case runs tensors of 2^31
-elements (4 GiB each) through the forward and the backward: one seeded block
-of 8 batches repeated 64 times, so every copy must give the same bits as the
-first (which the oracle checks), whatever its offset.
+elements (4 GiB each) through the forward and the backward for each kernel
+family (d = 64, 128, 256): one seeded block of 8 batches repeated, so every
+copy must give the same bits as the first (which the oracle checks),
+whatever its offset.
 """
 import numpy as np
 import pytest
@@ -78,9 +79,11 @@ def test_splitkv_million_keys():
     assert oracle.lse_max_abs_err(lse, lse_ref) <= TOL_LSE
 
 
-def test_tensors_of_2_31_elements():
-    reps, (b0, H, N, d), causal = 64, (8, 64, 512, 128), True   # [512, 64, 512, 128]: 2^31 elements
-    x, g = device_inputs(b0, H, N, d, seed=5600, with_grad=True)
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_tensors_of_2_31_elements(d):
+    b0, H, N, causal = 8, 64, 512, True
+    reps = (1 << 31) // (b0 * H * N * d)          # [8 reps, 64, 512, d]: 2^31 elements
+    x, g = device_inputs(b0, H, N, d, seed=5600 + d, with_grad=True)
     big = {n: t.repeat(reps, 1, 1, 1) for n, t in g.items()}
     assert big["q"].numel() == 1 << 31
     scale = 1.0 / np.sqrt(d)

@@ -11,9 +11,9 @@ tensor-map coordinates near 2^20, fp32 row sums and accumulators over 8192
 key steps, persistent backward units with 256 query tiles, and split-KV
 partitions of very long key ranges.  A last case runs tensors of 2^31
 elements (4 GiB each) through the forward and the backward for each kernel
-family (d = 64, 128, 256): one seeded block of 8 batches repeated, so every
-copy must give the same bits as the first (which the oracle checks),
-whatever its offset.
+family (d = 64, 128, 256), through split-KV and through the FP8 path: one
+seeded block repeated along the batch, so every copy must give the same bits
+as the first (which the oracle checks), whatever its offset.
 """
 import numpy as np
 import pytest
@@ -104,3 +104,43 @@ def test_tensors_of_2_31_elements(d):
         for name, a, r in zip(("dq", "dk", "dv"), grads, ref):
             err = oracle.rel_fro_err(sl(a), r)
             assert err <= TOL_GRAD, f"{name}: relative Frobenius error {err:.3g}"
+
+
+def test_splitkv_keys_of_2_31_elements():
+    """Split-KV decode with K and V of 2^31 elements: repeated blocks agree bit
+    for bit, and the first matches the oracle."""
+    b0, H, Nq, Nk, d = 2, 64, 3, 4096, 128
+    reps = (1 << 31) // (b0 * H * Nk * d)
+    x = make_splitkv_inputs(b0, H, Nq, Nk, d, seed=5700)
+    g = {k: t.cuda().repeat(reps, 1, 1, 1) for k, t in x.items()}
+    assert g["k"].numel() == 1 << 31
+    o, lse = fa.fa_fwd_splitkv(g["q"], g["k"], g["v"])
+    torch.cuda.synchronize()
+    assert_no_timeout()
+    for name, t in (("o", o), ("lse", lse)):
+        blocks = t.view(reps, -1)
+        assert bool((blocks == blocks[:1]).all()), f"{name}: a repeated block differs from the first"
+    o_ref, lse_ref = oracle.attn_fwd_ref(f64(x["q"][:, :2]), f64(x["k"][:, :2]), f64(x["v"][:, :2]),
+                                         1.0 / np.sqrt(d), False)
+    assert o_excess_err(f64(o[:b0, :2]), o_ref) <= TOL_O
+    assert oracle.lse_max_abs_err(f64(lse[:b0, :2]), lse_ref) <= TOL_LSE
+
+
+def test_fp8_path_on_tensors_of_2_31_elements():
+    """The e4m3 quantiser (rotated and transposed) and the FP8 forward on
+    tensors of 2^31 elements: repeated blocks give identical codes, descales
+    and outputs (the FP8 oracle checks the codes elsewhere)."""
+    b0, H, N, d, causal = 8, 64, 512, 128, True
+    reps = (1 << 31) // (b0 * H * N * d)
+    _, g = device_inputs(b0, H, N, d, seed=5800)
+    big = {n: t.repeat(reps, 1, 1, 1) for n, t in g.items()}
+    q8, dq = fa.fa_fp8_quantize(big["q"], rotate_seed=11)
+    k8, dk = fa.fa_fp8_quantize(big["k"], rotate_seed=11)
+    vt8, dv = fa.fa_fp8_quantize(big["v"], transpose=True)
+    o, lse = fa.fa_fwd_fp8(q8, k8, vt8, dq, dk, dv, None, causal)
+    torch.cuda.synchronize()
+    assert_no_timeout()
+    for name, t in (("q8", q8), ("k8", k8), ("vt8", vt8), ("descale_q", dq), ("descale_v", dv), ("o", o),
+                    ("lse", lse)):
+        blocks = t.reshape(reps, -1)
+        assert bool((blocks == blocks[:1]).all()), f"{name}: a repeated block differs from the first"

@@ -144,3 +144,35 @@ def test_fp8_path_on_tensors_of_2_31_elements():
                     ("lse", lse)):
         blocks = t.reshape(reps, -1)
         assert bool((blocks == blocks[:1]).all()), f"{name}: a repeated block differs from the first"
+
+
+def test_strided_views_of_2_31_elements():
+    """q, k, v as views of one packed [B, N, 3, H, d] buffer and dq, dk, dv
+    written into another, each view of 2^31 elements: repeated blocks agree
+    bit for bit and the first matches the oracle."""
+    b0, H, N, d, causal = 8, 64, 512, 128, True
+    reps = (1 << 31) // (b0 * H * N * d)
+    x, g = device_inputs(b0, H, N, d, seed=5900, with_grad=True)
+    packed = torch.stack([g[n].transpose(1, 2) for n in ("q", "k", "v")], dim=2).repeat(reps, 1, 1, 1, 1)
+    q, k, v = (packed[:, :, i].transpose(1, 2) for i in range(3))   # [B, H, N, d] views
+    do = g["do"].repeat(reps, 1, 1, 1)
+    assert q.numel() == 1 << 31 and packed.numel() == 3 << 31
+    o, lse = fa.fa_fwd_strided(q, k, v, None, causal)
+    dpacked = torch.empty_like(packed)
+    dq, dk, dv = (dpacked[:, :, i].transpose(1, 2) for i in range(3))
+    fa.fa_bwd_strided(q, k, v, o, lse, do, None, causal, dq=dq, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    assert_no_timeout()
+    for name, t in (("o", o), ("lse", lse), ("dqkv", dpacked)):
+        blocks = t.reshape(reps, -1)
+        assert bool((blocks == blocks[:1]).all()), f"{name}: a repeated block differs from the first"
+    scale = 1.0 / np.sqrt(d)
+    b, h = b0 - 1, H - 1
+    sl = lambda t: f64(t[b:b + 1, h:h + 1])
+    o_ref, lse_ref = oracle.attn_fwd_ref(sl(x["q"]), sl(x["k"]), sl(x["v"]), scale, causal)
+    assert o_excess_err(sl(o), o_ref) <= TOL_O
+    assert oracle.lse_max_abs_err(sl(lse), lse_ref) <= TOL_LSE
+    ref = oracle.attn_bwd_ref(sl(x["q"]), sl(x["k"]), sl(x["v"]), sl(x["do"]), scale, causal)
+    for name, a, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        err = oracle.rel_fro_err(sl(a), r)
+        assert err <= TOL_GRAD, f"{name}: relative Frobenius error {err:.3g}"

@@ -301,8 +301,8 @@ def run_ours(args, dist: Dist):
     dom = max(range(4), key=lambda j: kern_ms[j])
     if p_drop > 0:
         # only the forward is a single timed kernel in this mode
-        names[0] = "fa_fwd_kernel<dropout>"
-        kernels = {"fa_fwd_kernel<dropout>": kernels["fa_fwd_kernel"]}
+        names[0] = names[0] + "<dropout>"
+        kernels = {names[0]: next(iter(kernels.values()))}
         dom = 0
     src = {"fa_fwd_kernel<dropout>": [],
            "fa_fwd_kernel": ["io_aware_exact_14_gb300/csrc/fa_fwd.cu", "io_aware_exact_14_gb300/csrc/fa_ptx.cuh"],

@@ -12,9 +12,9 @@
  *   - Tensors are row-major, contiguous, [B, H, N, d] bf16 (d innermost);
  *     row statistics (LSE, D) are [B, H, N] fp32.  Q, K, V share one N.
  *   - d must be a multiple of 8 from 8 to 256 for fa_fwd, fa_fwd_strided,
- *     fa_bwd, fa_bwd_strided, the three backward steps and fa_bwd_noalloc,
- *     and from 8 to 128 for the dropout, split-KV and FP8 entry points;
- *     else FA_ERR_UNSUPPORTED.  d <= 64 runs the d = 64 kernels, 64 < d <=
+ *     fa_bwd, fa_bwd_strided, the three backward steps, fa_bwd_noalloc and
+ *     the two dropout entry points, and from 8 to 128 for the split-KV and
+ *     FP8 entry points; else FA_ERR_UNSUPPORTED.  d <= 64 runs the d = 64 kernels, 64 < d <=
  *     128 the d = 128 ones and 128 < d <= 256 the wide-head (d = 256) ones:
  *     the missing columns are zero-filled on chip, never read from or
  *     written to memory, and the products that contract over d skip the

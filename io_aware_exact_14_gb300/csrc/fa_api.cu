@@ -437,10 +437,9 @@ fa_status dkdv_checked(const void* q, const void* k, const void* v, const float*
                        cudaStream_t st, const fa::DropArgs& drop = kNoDrop) {
   if (!load_encoder()) return FA_ERR_CUDA;
   if (s.d > 128) {
-    if (drop.t4 != 0) return FA_ERR_UNSUPPORTED;
     fa::WideBwdMaps m;
     FA_TRY(wide_maps(m, q, k, v, dO, nullptr, dk, dv, s, t, 0));
-    return cuda_status(fa::launch_bwd_d256_dkdv(m, lse, Dvec, s, st), "wide-head dK/dV kernel launch");
+    return cuda_status(fa::launch_bwd_d256_dkdv(m, lse, Dvec, s, drop, st), "wide-head dK/dV kernel launch");
   }
   CUtensorMap tq, tk, tv, tdo, tdk, tdv;
   FA_TRY(make_map(&tq, q, s, t.q));
@@ -458,10 +457,9 @@ fa_status dq_checked(const void* q, const void* k, const void* v, const float* l
                      const fa::DropArgs& drop = kNoDrop) {
   if (!load_encoder()) return FA_ERR_CUDA;
   if (s.d > 128) {
-    if (drop.t4 != 0) return FA_ERR_UNSUPPORTED;
     fa::WideBwdMaps m;
     FA_TRY(wide_maps(m, q, k, v, dO, dq, nullptr, nullptr, s, t, 1));
-    return cuda_status(fa::launch_bwd_d256_dq(m, lse, Dvec, s, st), "wide-head dQ kernel launch");
+    return cuda_status(fa::launch_bwd_d256_dq(m, lse, Dvec, s, drop, st), "wide-head dQ kernel launch");
   }
   CUtensorMap tq, tk, tv, tdo, tdq;
   FA_TRY(make_map(&tq, q, s, t.q));
@@ -481,7 +479,7 @@ fa_status fwd_impl(const void* q, const fa_strides* qs, const void* k, const fa_
                    const fa_strides* vs, void* o, const fa_strides* os, float* lse, int B, int H, int N, int d,
                    float scale, int causal, cudaStream_t stream, const fa::DropArgs& drop = kNoDrop,
                    const fa::WaitCfg* wait = nullptr) {
-  FA_TRY(check_sizes(B, H, N, d, drop.t4 == 0 && wait == nullptr ? fa::kMaxHeadDim : 128));
+  FA_TRY(check_sizes(B, H, N, d, wait == nullptr ? fa::kMaxHeadDim : 128));
   if (N == 0) return FA_OK;
   FA_TRY(check_ptrs({q, k, v, o}, {lse}));
   FA_TRY(check_scale(scale));
@@ -501,7 +499,7 @@ fa_status fwd_impl(const void* q, const fa_strides* qs, const void* k, const fa_
   FA_TRY(make_map(&tv, v, s, Sv));
   FA_TRY(make_map(&to, o, s, So));
   if (d > 128)
-    return cuda_status(fa::launch_fwd_d256(tq, tk, tv, to, lse, s, fa::next_wait_cfg(), stream),
+    return cuda_status(fa::launch_fwd_d256(tq, tk, tv, to, lse, s, drop, fa::next_wait_cfg(), stream),
                        "forward kernel launch");
   if (d <= 64 && drop.t4 == 0 && wait == nullptr) {   // narrow heads: four query tiles per CTA
     CUtensorMap tk64, tv64;
@@ -520,7 +518,7 @@ fa_status bwd_impl(const void* q, const fa_strides* qs, const void* k, const fa_
                    void* dv, const fa_strides* dvs, int B, int H, int N, int d, float scale, int causal,
                    void* workspace, size_t workspace_bytes, cudaStream_t stream,
                    const fa::DropArgs& drop = kNoDrop) {
-  FA_TRY(check_sizes(B, H, N, d, drop.t4 == 0 ? fa::kMaxHeadDim : 128));
+  FA_TRY(check_sizes(B, H, N, d, fa::kMaxHeadDim));
   if (N == 0) return FA_OK;
   FA_TRY(check_ptrs({q, k, v, o, dO, dq, dk, dv}, {lse}));
   FA_TRY(check_scale(scale));

@@ -198,12 +198,6 @@ __device__ __forceinline__ void st_bf16_16cols_dropped(uint32_t taddr, const flo
   tmem_st16(taddr, w);
 }
 
-// (M o dP) for columns c, c + 1: dP where kept, else 0.
-__device__ __forceinline__ float2 keep_pair_f(float2 v, const uint32_t* ge, int c) {
-  return make_float2(__uint_as_float(__float_as_uint(v.x) & keep_mask_one(ge[c / 4], c % 4)),
-                     __uint_as_float(__float_as_uint(v.y) & keep_mask_one(ge[c / 4], (c + 1) % 4)));
-}
-
 // Epilogue staging for one 128 x d accumulator: TMEM -> * mult -> bf16 ->
 // swizzled tile (the layout a TMA store reads) at shared address `stage`;
 // thread r writes row r.

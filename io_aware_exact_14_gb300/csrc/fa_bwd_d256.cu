@@ -276,12 +276,14 @@ __device__ void b256_mma(const U256& w, uint32_t tmem, uint32_t sbase, uint64_t*
   tc_commit_w(acc_done);
 }
 
-template <int MODE, bool CAUSAL>
+// DROPOUT: the keep mask of the forward, redrawn on chip: dV takes (P o M)^T
+// (x 1/(1-p) in the epilogue), dS = P o (M~ o dP - D) with M~ = M / (1-p).
+template <int MODE, bool CAUSAL, bool DROPOUT>
 __device__ void b256_compute(const U256& w, uint32_t tmem, uint8_t* smem, uint64_t* r_full, uint64_t* t1_full,
                              uint64_t* t2_full, uint64_t* s_full, uint64_t* dp_full, uint64_t* ds_full,
                              uint64_t* acc_done, uint64_t* a_ready, uint64_t* staged, const CUtensorMap* tmOut,
                              const float* __restrict__ lse, const float* __restrict__ Dg, int N, int d, float scale,
-                             float scale_log2, const CtaGuard& g) {
+                             float scale_log2, const DropArgs& drop, const CtaGuard& g) {
   using C = B256<MODE>;
   const int r = threadIdx.x & 127;
   const uint32_t lane_base = static_cast<uint32_t>((threadIdx.x >> 5) & 3) * 32u << 16;
@@ -320,6 +322,15 @@ __device__ void b256_compute(const U256& w, uint32_t tmem, uint8_t* smem, uint64
   for (int j = 0; j < w.n; ++j) {
     const int col0 = 64 * (w.first + j);   // first streamed row of this step
     const uint32_t tS = tmem + lane_base + 64u * (j & 1);
+    // keep words of this row against the step's 64 streamed rows, drawn before
+    // the scores land: column c in byte c % 4 of ge[c / 4]
+    uint32_t ge[DROPOUT ? 16 : 1];
+    if constexpr (DROPOUT) {
+      if constexpr (MODE == kModeDQ)
+        dropout_rows<4>(drop, w.bh, res_row, col0, ge);   // query row against keys
+      else
+        dropout_cols<4>(drop, w.bh, res_row, col0, ge);   // key row against queries
+    }
     if (C::kColVecs && !mbar_wait(&t1_full[j & 1], (j >> 1) & 1, g, kSiteBwd256 | 6u)) return;
     if (!mbar_wait(&s_full[j & 1], (j >> 1) & 1, g, kSiteBwd256 | 7u)) return;
     __syncwarp();
@@ -375,7 +386,10 @@ __device__ void b256_compute(const U256& w, uint32_t tmem, uint8_t* smem, uint64
     if (!C::kHasDP) {   // DV: P^T (bf16) into the first 32 columns of its score buffer
       uint32_t pk[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(p[2 * i], p[2 * i + 1]);
+      for (int i = 0; i < 32; ++i) {
+        pk[i] = pack_bf16x2(p[2 * i], p[2 * i + 1]);
+        if constexpr (DROPOUT) pk[i] &= keep_mask_pair(ge[i / 2], 2 * (i % 2));   // (P o M)^T
+      }
       tmem_st32(tS, pk);
       tmem_st_wait();
       tc_fence_before();
@@ -399,12 +413,18 @@ __device__ void b256_compute(const U256& w, uint32_t tmem, uint8_t* smem, uint64
       for (int i = 0; i < 16; ++i) {
         const float4 d4 = ld_shared_f4(vd + 16 * i);
         const int c = 4 * i;
-        const float2 a = __fadd2_rn(make_float2(__uint_as_float(dr[c / 32][c % 32]),
-                                                __uint_as_float(dr[c / 32][c % 32 + 1])),
-                                    make_float2(d4.x, d4.y));
-        const float2 b = __fadd2_rn(make_float2(__uint_as_float(dr[c / 32][c % 32 + 2]),
-                                                __uint_as_float(dr[c / 32][c % 32 + 3])),
-                                    make_float2(d4.z, d4.w));
+        const float2 dr01 = make_float2(__uint_as_float(dr[c / 32][c % 32]), __uint_as_float(dr[c / 32][c % 32 + 1]));
+        const float2 dr23 = make_float2(__uint_as_float(dr[c / 32][c % 32 + 2]),
+                                        __uint_as_float(dr[c / 32][c % 32 + 3]));
+        float2 a, b;
+        if constexpr (DROPOUT) {   // M~ o dP - D
+          const float2 ds2 = make_float2(drop.scale, drop.scale);
+          a = __ffma2_rn(keep_pair_f(dr01, ge, c), ds2, make_float2(d4.x, d4.y));
+          b = __ffma2_rn(keep_pair_f(dr23, ge, c + 2), ds2, make_float2(d4.z, d4.w));
+        } else {
+          a = __fadd2_rn(dr01, make_float2(d4.x, d4.y));
+          b = __fadd2_rn(dr23, make_float2(d4.z, d4.w));
+        }
         const float2 s0 = __fmul2_rn(make_float2(p[c], p[c + 1]), a);
         const float2 s1 = __fmul2_rn(make_float2(p[c + 2], p[c + 3]), b);
         pk[2 * i] = pack_bf16x2(s0.x, s0.y);
@@ -414,9 +434,12 @@ __device__ void b256_compute(const U256& w, uint32_t tmem, uint8_t* smem, uint64
       const float2 nd2 = make_float2(nd, nd);
 #pragma unroll
       for (int c = 0; c < 64; c += 2) {
-        const float2 a = __fadd2_rn(make_float2(__uint_as_float(dr[c / 32][c % 32]),
-                                                __uint_as_float(dr[c / 32][c % 32 + 1])),
-                                    nd2);
+        const float2 dr01 = make_float2(__uint_as_float(dr[c / 32][c % 32]), __uint_as_float(dr[c / 32][c % 32 + 1]));
+        float2 a;
+        if constexpr (DROPOUT)   // M~ o dP - D
+          a = __ffma2_rn(keep_pair_f(dr01, ge, c), make_float2(drop.scale, drop.scale), nd2);
+        else
+          a = __fadd2_rn(dr01, nd2);
         const float2 s0 = __fmul2_rn(make_float2(p[c], p[c + 1]), a);
         pk[c / 2] = pack_bf16x2(s0.x, s0.y);
       }
@@ -432,7 +455,7 @@ __device__ void b256_compute(const U256& w, uint32_t tmem, uint8_t* smem, uint64
   if (!mbar_wait(acc_done, 0, g, kSiteBwd256 | 10u)) return;
   __syncwarp();
   tc_fence_after();
-  const float mult = MODE == kModeDV ? 1.f : scale;
+  const float mult = MODE == kModeDV ? (DROPOUT ? drop.scale : 1.f) : scale;
   const uint32_t tAcc = tmem + lane_base + C::kColAcc;
 #pragma unroll 1
   for (int c = 0; c < 256; c += 32) {
@@ -461,13 +484,14 @@ __device__ void b256_compute(const U256& w, uint32_t tmem, uint8_t* smem, uint64
 }
 
 // FD: d = 256 (compile-time K steps and output width of the products).
-template <int MODE, bool CAUSAL, bool FD>
+template <int MODE, bool CAUSAL, bool FD, bool DROPOUT>
 __global__ void __launch_bounds__(192, 1)
     fa_bwd_d256_kernel(const __grid_constant__ CUtensorMap tmR1, const __grid_constant__ CUtensorMap tmR2,
                        const __grid_constant__ CUtensorMap tmT1, const __grid_constant__ CUtensorMap tmT2,
                        const __grid_constant__ CUtensorMap tmOut, const float* __restrict__ lse,
                        const float* __restrict__ Dg, int N, int d, int n_res, int BH, int H, int band, float scale,
-                       float scale_log2, int ks, uint32_t idesc_acc, const WaitCfg wc) {
+                       float scale_log2, int ks, uint32_t idesc_acc, const __grid_constant__ DropArgs drop,
+                       const WaitCfg wc) {
   using C = B256<MODE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -540,20 +564,21 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   } else {
-    b256_compute<MODE, CAUSAL>(w, tmem, smem, r_full, t1_full, t2_full, s_full, dp_full, ds_full, acc_done, a_ready,
-                               staged, &tmOut, lse, Dg, N, d, scale, scale_log2, g);
+    b256_compute<MODE, CAUSAL, DROPOUT>(w, tmem, smem, r_full, t1_full, t2_full, s_full, dp_full, ds_full, acc_done,
+                                        a_ready, staged, &tmOut, lse, Dg, N, d, scale, scale_log2, drop, g);
     __syncwarp();
     tc_fence_before();
     named_bar_sync(1, 160);
   }
 }
 
-template <int MODE, bool CAUSAL>
+template <int MODE, bool CAUSAL, bool DROPOUT>
 cudaError_t launch_t(const CUtensorMap& r1, const CUtensorMap& r2, const CUtensorMap& t1, const CUtensorMap& t2,
-                     const CUtensorMap& out, const float* lse, const float* Dvec, const Shape& s, const WaitCfg& wc,
-                     cudaStream_t st) {
+                     const CUtensorMap& out, const float* lse, const float* Dvec, const Shape& s,
+                     const DropArgs& drop, const WaitCfg& wc, cudaStream_t st) {
   using C = B256<MODE>;
-  auto kern = s.d == 256 ? fa_bwd_d256_kernel<MODE, CAUSAL, true> : fa_bwd_d256_kernel<MODE, CAUSAL, false>;
+  auto kern = s.d == 256 ? fa_bwd_d256_kernel<MODE, CAUSAL, true, DROPOUT>
+                         : fa_bwd_d256_kernel<MODE, CAUSAL, false, DROPOUT>;
   const cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), C::kSmemBytes, C::kThreads, 0);
   if (e != cudaSuccess) return e;
   const int n_res = (s.N + 127) / 128;
@@ -561,30 +586,34 @@ cudaError_t launch_t(const CUtensorMap& r1, const CUtensorMap& r2, const CUtenso
   const dim3 grid(static_cast<unsigned>(s.B) * s.H * n_res);
   kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(r1, r2, t1, t2, out, lse, Dvec, s.N, s.d, n_res, s.B * s.H, s.H,
                                                  head_band(s.N, s.d), s.scale, scale_log2, score_ksteps(s.d),
-                                                 idesc_bf16(128, out_cols(s.d), false, true), wc);
+                                                 idesc_bf16(128, out_cols(s.d), false, true), drop, wc);
   return cudaGetLastError();
 }
 
 template <int MODE>
 cudaError_t launch_m(const CUtensorMap& r1, const CUtensorMap& r2, const CUtensorMap& t1, const CUtensorMap& t2,
-                     const CUtensorMap& out, const float* lse, const float* Dvec, const Shape& s, const WaitCfg& wc,
-                     cudaStream_t st) {
-  return s.causal ? launch_t<MODE, true>(r1, r2, t1, t2, out, lse, Dvec, s, wc, st)
-                  : launch_t<MODE, false>(r1, r2, t1, t2, out, lse, Dvec, s, wc, st);
+                     const CUtensorMap& out, const float* lse, const float* Dvec, const Shape& s,
+                     const DropArgs& drop, const WaitCfg& wc, cudaStream_t st) {
+  if (drop.t4 != 0)
+    return s.causal ? launch_t<MODE, true, true>(r1, r2, t1, t2, out, lse, Dvec, s, drop, wc, st)
+                    : launch_t<MODE, false, true>(r1, r2, t1, t2, out, lse, Dvec, s, drop, wc, st);
+  return s.causal ? launch_t<MODE, true, false>(r1, r2, t1, t2, out, lse, Dvec, s, drop, wc, st)
+                  : launch_t<MODE, false, false>(r1, r2, t1, t2, out, lse, Dvec, s, drop, wc, st);
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_d256_dkdv(const WideBwdMaps& m, const float* lse, const float* Dvec, const Shape& s,
-                                 cudaStream_t st) {
-  const cudaError_t e = launch_m<kModeDV>(m.k128, m.k128, m.q64, m.do64, m.dv128, lse, Dvec, s, next_wait_cfg(), st);
+                                 const DropArgs& drop, cudaStream_t st) {
+  const cudaError_t e =
+      launch_m<kModeDV>(m.k128, m.k128, m.q64, m.do64, m.dv128, lse, Dvec, s, drop, next_wait_cfg(), st);
   if (e != cudaSuccess) return e;
-  return launch_m<kModeDK>(m.k128, m.v128, m.q64, m.do64, m.dk128, lse, Dvec, s, next_wait_cfg(), st);
+  return launch_m<kModeDK>(m.k128, m.v128, m.q64, m.do64, m.dk128, lse, Dvec, s, drop, next_wait_cfg(), st);
 }
 
 cudaError_t launch_bwd_d256_dq(const WideBwdMaps& m, const float* lse, const float* Dvec, const Shape& s,
-                               cudaStream_t st) {
-  return launch_m<kModeDQ>(m.q128, m.do128, m.k64, m.v64, m.dq128, lse, Dvec, s, next_wait_cfg(), st);
+                               const DropArgs& drop, cudaStream_t st) {
+  return launch_m<kModeDQ>(m.q128, m.do128, m.k64, m.v64, m.dq128, lse, Dvec, s, drop, next_wait_cfg(), st);
 }
 
 cudaError_t bwd_d256_status(uint32_t* out, bool reset) {

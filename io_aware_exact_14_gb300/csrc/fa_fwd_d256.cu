@@ -189,10 +189,13 @@ __device__ void f256_mma(const W256& w, uint32_t tmem, uint32_t sbase, uint64_t*
   }
 }
 
-template <bool CAUSAL>
+// DROPOUT: dropout on the probabilities that feed O += P V (the keep mask of
+// the shared counter-based contract, drawn on chip; the row sum l, hence
+// LSE, uses the plain ones, and 1/(1-p) goes into the epilogue).
+template <bool CAUSAL, bool DROPOUT>
 __device__ void f256_softmax(const W256& w, uint32_t tmem, uint8_t* smem, uint64_t* s_full, uint64_t* p_full,
                              uint64_t* o_ready, uint64_t* staged, const CUtensorMap* tmO, float* __restrict__ lse,
-                             int N, int d, float scale_log2, const CtaGuard& g) {
+                             int N, int d, float scale_log2, const DropArgs& drop, const CtaGuard& g) {
   using C = F256;
   const int r = threadIdx.x & 127;
   const int row = w.qt * 128 + r;
@@ -204,6 +207,15 @@ __device__ void f256_softmax(const W256& w, uint32_t tmem, uint8_t* smem, uint64
   for (int j = 0; j < w.n; ++j) {
     const int buf = j & 1;
     const uint32_t tS = tmem + lane_base + 128u * buf;
+    // keep words of this row's 128 keys, drawn before S lands (key c in byte
+    // c % 4 of word (c / 4) % 4 of kp[c / 16])
+    uint32_t kp[DROPOUT ? 8 : 1];
+    if constexpr (DROPOUT) {
+      uint32_t ge[32];
+      dropout_rows<8>(drop, w.bh, row, j * 128, ge);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) kp[q] = pack_keep4(ge[4 * q], ge[4 * q + 1], ge[4 * q + 2], ge[4 * q + 3]);
+    }
     if (!mbar_wait(&s_full[buf], (j >> 1) & 1, g, kSiteFwd256 | 6u)) return;
     __syncwarp();
     tc_fence_after();
@@ -264,7 +276,10 @@ __device__ void f256_softmax(const W256& w, uint32_t tmem, uint8_t* smem, uint64
                                     sc2, mo2);
         const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
         sum[(c / 2) % 4] = __fadd2_rn(sum[(c / 2) % 4], pp);
-        pk[(c / 2) % 32] = pack_bf16x2(pp.x, pp.y);
+        if constexpr (DROPOUT)   // P o M (0/1); the 1/(1-p) scale goes into the epilogue
+          pk[(c / 2) % 32] = pack_bf16x2(pp.x, pp.y) & keep_mask_pair(unpack_keep4(kp[c / 16], (c / 4) % 4), c % 4);
+        else
+          pk[(c / 2) % 32] = pack_bf16x2(pp.x, pp.y);
       }
       tmem_st32(tS + 32 * h, pk);
     }
@@ -298,7 +313,7 @@ __device__ void f256_softmax(const W256& w, uint32_t tmem, uint8_t* smem, uint64
   if (!mbar_wait(o_ready, (w.n - 1) & 1, g, kSiteFwd256 | 7u)) return;
   __syncwarp();
   tc_fence_after();
-  const float inv_l = l > 0.f ? 1.f / l : 0.f;
+  const float inv_l = l > 0.f ? (DROPOUT ? drop.scale : 1.f) / l : 0.f;
   const uint32_t stage = smem_u32(smem + C::kQOff);
 #pragma unroll 1
   for (int c = 0; c < 256; c += 32) {
@@ -327,12 +342,12 @@ __device__ void f256_softmax(const W256& w, uint32_t tmem, uint8_t* smem, uint64
   if (row < N) lse[static_cast<size_t>(w.bh) * N + row] = l > 0.f ? (m_use + __log2f(l)) * kLn2 : -INFINITY;
 }
 
-template <bool CAUSAL, bool FD>
+template <bool CAUSAL, bool FD, bool DROPOUT>
 __global__ void __launch_bounds__(192, 1)
     fa_fwd_d256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                        float* __restrict__ lse, int N, int d, int n_qt, int BH, int H, int band, float scale_log2,
-                       int ks, uint32_t idesc_pv1, const WaitCfg wc) {
+                       int ks, uint32_t idesc_pv1, const __grid_constant__ DropArgs drop, const WaitCfg wc) {
   using C = F256;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -391,18 +406,19 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   } else {
-    f256_softmax<CAUSAL>(w, tmem, smem, s_full, p_full, o_ready, staged, &tmO, lse, N, d, scale_log2, g);
+    f256_softmax<CAUSAL, DROPOUT>(w, tmem, smem, s_full, p_full, o_ready, staged, &tmO, lse, N, d, scale_log2, drop,
+                                  g);
     __syncwarp();
     tc_fence_before();
     named_bar_sync(1, 160);
   }
 }
 
-template <bool CAUSAL>
+template <bool CAUSAL, bool DROPOUT>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
-                     float* lse, const Shape& s, const WaitCfg& wc, cudaStream_t st) {
+                     float* lse, const Shape& s, const DropArgs& drop, const WaitCfg& wc, cudaStream_t st) {
   using C = F256;
-  auto kern = s.d == 256 ? fa_fwd_d256_kernel<CAUSAL, true> : fa_fwd_d256_kernel<CAUSAL, false>;
+  auto kern = s.d == 256 ? fa_fwd_d256_kernel<CAUSAL, true, DROPOUT> : fa_fwd_d256_kernel<CAUSAL, false, DROPOUT>;
   const cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), C::kSmemBytes, C::kThreads, 0);
   if (e != cudaSuccess) return e;
   const int n_qt = (s.N + 127) / 128;
@@ -410,15 +426,20 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   const dim3 grid(static_cast<unsigned>(s.B) * s.H * n_qt);
   kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, to, lse, s.N, s.d, n_qt, s.B * s.H, s.H,
                                                  head_band(s.N, s.d), scale_log2, score_ksteps(s.d),
-                                                 idesc_bf16(128, out_cols(s.d) - 128, false, true), wc);
+                                                 idesc_bf16(128, out_cols(s.d) - 128, false, true), drop, wc);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_fwd_d256(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& to, float* lse, const Shape& s, const WaitCfg& wc, cudaStream_t st) {
-  return s.causal ? launch_t<true>(tq, tk, tv, to, lse, s, wc, st) : launch_t<false>(tq, tk, tv, to, lse, s, wc, st);
+                            const CUtensorMap& to, float* lse, const Shape& s, const DropArgs& drop,
+                            const WaitCfg& wc, cudaStream_t st) {
+  if (drop.t4 != 0)
+    return s.causal ? launch_t<true, true>(tq, tk, tv, to, lse, s, drop, wc, st)
+                    : launch_t<false, true>(tq, tk, tv, to, lse, s, drop, wc, st);
+  return s.causal ? launch_t<true, false>(tq, tk, tv, to, lse, s, drop, wc, st)
+                  : launch_t<false, false>(tq, tk, tv, to, lse, s, drop, wc, st);
 }
 
 cudaError_t fwd_d256_status(uint32_t* out, bool reset) {

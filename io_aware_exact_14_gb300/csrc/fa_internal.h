@@ -109,7 +109,8 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
 // Forward for wide heads (128 < d <= 256): one query tile per CTA, K/V
 // d-halves through a ring (fa_fwd_d256.cu).  Same maps as launch_fwd.
 cudaError_t launch_fwd_d256(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& to, float* lse, const Shape& s, const WaitCfg& wc, cudaStream_t st);
+                            const CUtensorMap& to, float* lse, const Shape& s, const DropArgs& drop,
+                            const WaitCfg& wc, cudaStream_t st);
 
 // Forward for narrow heads (d <= 64, no dropout): four query tiles per CTA,
 // 64-key steps (fa_fwd_q4.cu).  Q and O maps with 128-row boxes, K and V maps
@@ -194,9 +195,9 @@ struct WideBwdMaps {
   CUtensorMap q128, q64, k128, k64, v128, v64, do128, do64, dq128, dk128, dv128;
 };
 cudaError_t launch_bwd_d256_dkdv(const WideBwdMaps& m, const float* lse, const float* Dvec, const Shape& s,
-                                 cudaStream_t st);
+                                 const DropArgs& drop, cudaStream_t st);
 cudaError_t launch_bwd_d256_dq(const WideBwdMaps& m, const float* lse, const float* Dvec, const Shape& s,
-                               cudaStream_t st);
+                               const DropArgs& drop, cudaStream_t st);
 
 // FP8 (e4m3): per-(b, h) quantisation of a contiguous bf16 [B, H, N, d] tensor
 // into codes [B, H, N, d] (or, transposed, [B, H, d, ldv]) with descale[b*H + h]

@@ -558,6 +558,12 @@ __device__ __forceinline__ uint32_t keep_mask_one(uint32_t ge, int b) {
   return m;
 }
 
+// (M o dP) for columns c, c + 1 of keep words ge: dP where kept, else 0.
+__device__ __forceinline__ float2 keep_pair_f(float2 v, const uint32_t* ge, int c) {
+  return make_float2(__uint_as_float(__float_as_uint(v.x) & keep_mask_one(ge[c / 4], c % 4)),
+                     __uint_as_float(__float_as_uint(v.y) & keep_mask_one(ge[c / 4], (c + 1) % 4)));
+}
+
 // Quad exchange: lane s of each quad holds y[k] = its word for lane (s + k)
 // mod 4; returns z[m] = lane m's word for lane s.  Rotations are selects on
 // the lane's position (branch-free); three shuffles.

@@ -135,7 +135,8 @@ def test_dropout_argument_checks(lib):
     for p in (1.0, 1.5, -0.1, float("nan"), float("inf")):
         assert fwd_d(_Dropout(p, 1, 0)) == 1, p
     assert fwd_d(_Dropout(0.1, 1, 0), q=0) == 1
-    assert fwd_d(_Dropout(0.1, 1, 0), d=200) == 2
+    assert fwd_d(_Dropout(0.1, 1, 0), d=264) == 2   # above the widest head
+    assert fwd_d(_Dropout(0.1, 1, 0), d=100) == 2   # not a multiple of 8
     assert fwd_d(_Dropout(0.1, 1, 0), o=FAKE) == 1
     p = [FAKE + i * 0x100000 for i in range(12)]
     ws = lib.fa_bwd_workspace_bytes(1, 1, 128, 64)

@@ -22,6 +22,11 @@ SMALL = [
     (1, 1, 17, 128, True, 0.2),
     (2, 2, 1000, 64, True, 0.1),
     (1, 2, 1111, 128, False, 0.15),
+    (1, 2, 200, 256, True, 0.25),
+    (1, 1, 300, 160, False, 0.1),
+    (2, 1, 129, 192, True, 0.5),
+    (1, 1, 17, 256, False, 0.2),
+    (1, 1, 700, 256, False, 0.15),
 ]
 
 
@@ -33,11 +38,11 @@ def _onehot_v(B, H, N, d, kb):
     return v
 
 
-@pytest.mark.parametrize("p", [0.1, 0.5, 0.9, 0.999])
-def test_forward_mask_bit_exact(p):
+@pytest.mark.parametrize("p,d", [(0.1, 128), (0.5, 128), (0.9, 128), (0.999, 128), (0.1, 256), (0.5, 256)])
+def test_forward_mask_bit_exact(p, d):
     """Q = K = 0 makes P uniform (1/N), so with one-hot V each output element is
     keep * scale / N: nonzero exactly where the mask keeps."""
-    B, H, N, d = 2, 3, 384, 128
+    B, H, N = 2, 3, 384
     q = torch.zeros(B, H, N, d, dtype=torch.bfloat16, device="cuda")
     for kb in range((N + 127) // 128):
         v = _onehot_v(B, H, N, d, kb)
@@ -51,10 +56,11 @@ def test_forward_mask_bit_exact(p):
                 assert np.array_equal(got[b, h, :, :128], keep[:, 128 * kb:128 * kb + 128]), (b, h, kb)
 
 
-def test_dkdv_mask_bit_exact():
+@pytest.mark.parametrize("d", [128, 256])
+def test_dkdv_mask_bit_exact(d):
     """dV = (P o M~)^T dO with uniform P and one-hot dO reads the mask through
     the dK/dV kernel's own draw (its threads hold keys, not queries)."""
-    B, H, N, d, p = 1, 2, 256, 128, 0.3
+    B, H, N, p = 1, 2, 256, 0.3
     q = torch.zeros(B, H, N, d, dtype=torch.bfloat16, device="cuda")
     v = torch.randn(B, H, N, d, dtype=torch.bfloat16, device="cuda")
     o, lse = fa.fa_fwd_dropout(q, q, v, p, SEED, offset=3, scale=0.125)
@@ -66,7 +72,7 @@ def test_dkdv_mask_bit_exact():
         got = (dv.float() != 0).cpu().numpy()   # dV[j, c] = keep[128 ib + c, j] * scale / N
         for h in range(H):
             keep = oracle.dropout_keep(h, N, N, p, SEED, 3)
-            assert np.array_equal(got[0, h], keep[128 * ib:128 * ib + 128, :].T), (h, ib)
+            assert np.array_equal(got[0, h, :, :128], keep[128 * ib:128 * ib + 128, :].T), (h, ib)
 
 
 @pytest.mark.parametrize("B,H,N,d,causal,p", SMALL)

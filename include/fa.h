@@ -11,14 +11,13 @@
  * Conventions shared by every entry point
  *   - Tensors are row-major, contiguous, [B, H, N, d] bf16 (d innermost);
  *     row statistics (LSE, D) are [B, H, N] fp32.  Q, K, V share one N.
- *   - d must be a multiple of 8 from 8 to 256 for fa_fwd, fa_fwd_strided,
- *     fa_bwd, fa_bwd_strided, the three backward steps, fa_bwd_noalloc and
- *     the two dropout entry points, and from 8 to 128 for the split-KV and
- *     FP8 entry points; else FA_ERR_UNSUPPORTED.  d <= 64 runs the d = 64 kernels, 64 < d <=
- *     128 the d = 128 ones and 128 < d <= 256 the wide-head (d = 256) ones:
- *     the missing columns are zero-filled on chip, never read from or
- *     written to memory, and the products that contract over d skip the
- *     all-zero 16-column steps.  N >= 0; N == 0 is a no-op that returns
+ *   - d must be a multiple of 8 from 8 to 256 for every entry point but
+ *     the FP8 ones and the deadlock-guard test hook (d up to 128, see
+ *     there); else FA_ERR_UNSUPPORTED.  d <= 64 runs the d = 64 kernels,
+ *     64 < d <= 128 the d = 128 ones and 128 < d <= 256 the wide-head
+ *     (d = 256) ones: the missing columns are zero-filled on chip, never
+ *     read from or written to memory, and the products that contract over d
+ *     skip the all-zero 16-column steps.  N >= 0; N == 0 is a no-op that returns
  *     FA_OK.  B, H >= 1.  B*H*ceil(N/128) must fit in 2^31 - 1.
  *   - Every device pointer must be 16-byte aligned (fp32 vectors: 4-byte),
  *     outputs must not overlap inputs or each other; otherwise
@@ -108,9 +107,9 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, f
 /*
  * Workspace bytes fa_fwd_splitkv needs for these arguments (the same
  * num_splits rule, on the current device): n_used * B*H*Nq*D fp32 partial
- * outputs (D = 64 for d <= 64, else 128) plus n_used * B*H*Nq fp32 partial
- * LSE, each rounded up to 256 bytes.  0 for invalid sizes, Nq == 0 or
- * Nk == 0.
+ * outputs (D = 64 for d <= 64, 128 for d <= 128, else 256) plus
+ * n_used * B*H*Nq fp32 partial LSE, each rounded up to 256 bytes.  0 for
+ * invalid sizes, Nq == 0 or Nk == 0.
  */
 size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int d, int num_splits);
 

@@ -566,8 +566,8 @@ fa_status fa_fwd_strided(const void* q, const fa_strides* q_st, const void* k, c
 fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
                          int Nk, int d, float scale, int num_splits, void* workspace, size_t workspace_bytes,
                          struct CUstream_st* stream) {
-  FA_TRY(check_sizes(B, H, Nq, d));
-  FA_TRY(check_sizes(B, H, Nk, d));
+  FA_TRY(check_sizes(B, H, Nq, d, fa::kMaxHeadDim));
+  FA_TRY(check_sizes(B, H, Nk, d, fa::kMaxHeadDim));
   if (Nq == 0) return FA_OK;
   FA_TRY(check_ptrs({q, o}, {lse}));
   if (Nk > 0) FA_TRY(check_ptrs({k, v}, {}));   // never read when there are no keys
@@ -600,7 +600,9 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, f
 }
 
 size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int d, int num_splits) {
-  if (check_sizes(B, H, Nq, d) != FA_OK || check_sizes(B, H, Nk, d) != FA_OK || Nq <= 0 || Nk <= 0) return 0;
+  if (check_sizes(B, H, Nq, d, fa::kMaxHeadDim) != FA_OK || check_sizes(B, H, Nk, d, fa::kMaxHeadDim) != FA_OK ||
+      Nq <= 0 || Nk <= 0)
+    return 0;
   SplitPlan p;
   if (split_plan(B, H, Nq, Nk, d, num_splits, p) != FA_OK || p.n_splits == 0) return 0;
   return p.o_bytes + p.lse_bytes;

@@ -659,12 +659,15 @@ __global__ void __launch_bounds__(256) fa_fwd_merge_kernel(const float* __restri
       const float wgt = ls == -INFINITY ? 0.f : __expf(ls - m);
       wsum += wgt;
       const float* src = o_part + idx * D + lane * kPer;
-      if constexpr (kPer == 4) {
-        const float4 x = *reinterpret_cast<const float4*>(src);
-        acc[0] = fmaf(wgt, x.x, acc[0]);
-        acc[1] = fmaf(wgt, x.y, acc[1]);
-        acc[2] = fmaf(wgt, x.z, acc[2]);
-        acc[3] = fmaf(wgt, x.w, acc[3]);
+      if constexpr (kPer >= 4) {
+#pragma unroll
+        for (int e = 0; e < kPer; e += 4) {
+          const float4 x = *reinterpret_cast<const float4*>(src + e);
+          acc[e] = fmaf(wgt, x.x, acc[e]);
+          acc[e + 1] = fmaf(wgt, x.y, acc[e + 1]);
+          acc[e + 2] = fmaf(wgt, x.z, acc[e + 2]);
+          acc[e + 3] = fmaf(wgt, x.w, acc[e + 3]);
+        }
       } else {
         const float2 x = *reinterpret_cast<const float2*>(src);
         acc[0] = fmaf(wgt, x.x, acc[0]);
@@ -688,22 +691,28 @@ cudaError_t launch_fwd_splitkv_t(const CUtensorMap& tq, const CUtensorMap& tk, c
                                  const CUtensorMap& top, const float* o_part, float* lse_part, void* o, float* lse,
                                  const Shape& s, int Nk, int n_splits, int kt_per_split, const WaitCfg& wc,
                                  cudaStream_t st) {
-  using C = FwdCfg<D>;
   const int BH = s.B * s.H;
-  const int n_qt = (s.N + 127) / 128;
-  const int n_kt = (Nk + 127) / 128;
   cudaError_t e;
   if (n_splits > 0) {
-    auto kern = s.d == D ? fa_fwd_kernel<D, false, 1, true, false, true>
-                         : fa_fwd_kernel<D, false, 1, true, false, false>;
-    e = prepare_kernel(reinterpret_cast<const void*>(kern), C::kSmemBytes, C::kThreads, C::kRegsNeeded);
-    if (e != cudaSuccess) return e;
-    const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
-    const dim3 grid(static_cast<unsigned>(BH) * n_splits * n_qt);
-    kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, top, lse_part, s.N, n_qt, BH, s.H, 1, scale_log2,
-                                                   Nk, n_qt, n_kt, n_splits, kt_per_split, score_ksteps(s.d),
-                                                   idesc_bf16(128, out_cols(s.d), false, true), no_drop_args(), wc);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if constexpr (D == 256) {   // wide heads: their own kernel's split mode
+      e = launch_fwd_d256_split(tq, tk, tv, top, lse_part, s, Nk, n_splits, kt_per_split, wc, st);
+      if (e != cudaSuccess) return e;
+    } else {
+      using C = FwdCfg<D>;
+      const int n_qt = (s.N + 127) / 128;
+      const int n_kt = (Nk + 127) / 128;
+      auto kern = s.d == D ? fa_fwd_kernel<D, false, 1, true, false, true>
+                           : fa_fwd_kernel<D, false, 1, true, false, false>;
+      e = prepare_kernel(reinterpret_cast<const void*>(kern), C::kSmemBytes, C::kThreads, C::kRegsNeeded);
+      if (e != cudaSuccess) return e;
+      const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
+      const dim3 grid(static_cast<unsigned>(BH) * n_splits * n_qt);
+      kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, top, lse_part, s.N, n_qt, BH, s.H, 1, scale_log2,
+                                                     Nk, n_qt, n_kt, n_splits, kt_per_split, score_ksteps(s.d),
+                                                     idesc_bf16(128, out_cols(s.d), false, true), no_drop_args(),
+                                                     wc);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
   }
   const long long rows = static_cast<long long>(BH) * s.N;
   const long long blocks = (rows + 7) / 8;   // 8 warps (rows) per block
@@ -718,11 +727,17 @@ cudaError_t launch_fwd_splitkv(const CUtensorMap& tq, const CUtensorMap& tk, con
                                const CUtensorMap& top, const float* o_part, float* lse_part, void* o, float* lse,
                                const Shape& s, int Nk, int n_splits, int kt_per_split, const WaitCfg& wc,
                                cudaStream_t st) {
-  return kernel_dim(s.d) == 128
-             ? launch_fwd_splitkv_t<128>(tq, tk, tv, top, o_part, lse_part, o, lse, s, Nk, n_splits, kt_per_split, wc,
-                                         st)
-             : launch_fwd_splitkv_t<64>(tq, tk, tv, top, o_part, lse_part, o, lse, s, Nk, n_splits, kt_per_split, wc,
-                                        st);
+  switch (kernel_dim(s.d)) {
+    case 256:
+      return launch_fwd_splitkv_t<256>(tq, tk, tv, top, o_part, lse_part, o, lse, s, Nk, n_splits, kt_per_split, wc,
+                                       st);
+    case 128:
+      return launch_fwd_splitkv_t<128>(tq, tk, tv, top, o_part, lse_part, o, lse, s, Nk, n_splits, kt_per_split, wc,
+                                       st);
+    default:
+      return launch_fwd_splitkv_t<64>(tq, tk, tv, top, o_part, lse_part, o, lse, s, Nk, n_splits, kt_per_split, wc,
+                                      st);
+  }
 }
 
 // Issue strategy (measured on GB300): at d = 128 one warp's issue loop (two

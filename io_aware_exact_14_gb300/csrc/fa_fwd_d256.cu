@@ -25,6 +25,9 @@
 // Lazy rescaling as in fa_fwd.cu: a row keeps its reference max until a block
 // exceeds it by more than 2^8; O is rescaled in TMEM only when some row of
 // the warp moves, after the previous P V product has completed.
+// Split-KV launches (non-causal): a CTA takes one query tile and one chunk of
+// key tiles and writes the chunk's normalised O in fp32 (staged across the
+// then idle Q buffer and ring) and its LSE; fa_fwd.cu's merge combines them.
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
 
@@ -76,20 +79,38 @@ __device__ __forceinline__ void stream_tile(int t, int n, bool& is_v, int& j) {
 __device__ __forceinline__ int pos_k(int j) { return j == 0 ? 0 : 2 * j - 1; }
 __device__ __forceinline__ int pos_v(int j, int n) { return j == n - 1 ? 2 * n - 1 : 2 * j + 2; }
 
-// A CTA's work: head bh (hc for the 4-D maps), query tile qt, key tiles 0..n-1.
+// A CTA's work: head bh (hc for the 4-D maps), query tile qt, key tiles
+// kt0 .. kt0 + n - 1; split is the key chunk of a split-KV launch (else 0).
 struct W256 {
-  int bh, qt, n;
+  int bh, qt, n, kt0, split;
   HeadCoord hc;
 };
 
-__device__ __forceinline__ W256 w256_work(int N, int n_qt, int BH, int H, int band, bool causal) {
+__device__ __forceinline__ W256 w256_work(int n_qt, int BH, int H, int band, bool causal) {
   W256 w;
   int rank;
   banded_order(blockIdx.x, n_qt, BH, band, w.bh, rank);
   w.hc = head_coord(w.bh, H);
   w.qt = causal ? n_qt - 1 - rank : rank;   // causal: heavy (long-row) tiles first
   w.n = causal ? w.qt + 1 : n_qt;
-  (void)N;
+  w.kt0 = 0;
+  w.split = 0;
+  return w;
+}
+
+// Split-KV: CTA u takes query tile u % n_qt of one head and one chunk of
+// kt_per_split key tiles (the last chunk may be shorter, never empty); CTAs
+// of one (head, chunk) are adjacent, so they share the chunk's K/V in L2.
+__device__ __forceinline__ W256 w256_split_work(int n_qt, int n_splits, int kt_per_split, int n_kt, int H) {
+  W256 w;
+  const int u = static_cast<int>(blockIdx.x);
+  w.qt = u % n_qt;
+  const int rest = u / n_qt;
+  w.split = rest % n_splits;
+  w.bh = rest / n_splits;
+  w.hc = head_coord(w.bh, H);
+  w.kt0 = w.split * kt_per_split;
+  w.n = min(kt_per_split, n_kt - w.kt0);
   return w;
 }
 
@@ -115,7 +136,7 @@ __device__ void f256_producer(const W256& w, uint8_t* smem, uint64_t* full, uint
     mbar_arrive_expect_tx(&full[slot], C::kUnitBytes);
 #pragma unroll
     for (int b = 0; b < 2; ++b)
-      tma_load_hd(dst + b * C::kBoxBytes, is_v ? tmV : tmK, &full[slot], 128 * h + 64 * b, 128 * j, w.hc);
+      tma_load_hd(dst + b * C::kBoxBytes, is_v ? tmV : tmK, &full[slot], 128 * h + 64 * b, 128 * (w.kt0 + j), w.hc);
     issued = u + 1;
   }
   if (issued < units) {   // unwinding: let the copies in flight land before shared memory is released
@@ -192,10 +213,14 @@ __device__ void f256_mma(const W256& w, uint32_t tmem, uint32_t sbase, uint64_t*
 // DROPOUT: dropout on the probabilities that feed O += P V (the keep mask of
 // the shared counter-based contract, drawn on chip; the row sum l, hence
 // LSE, uses the plain ones, and 1/(1-p) goes into the epilogue).
-template <bool CAUSAL, bool DROPOUT>
+// SPLIT: O goes out in fp32 through the partial-output map (z = split * BH +
+// bh) and the LSE to lse[(split * BH + bh) * N + row].  N is the query
+// length, Nk the key length.
+template <bool CAUSAL, bool SPLIT, bool DROPOUT>
 __device__ void f256_softmax(const W256& w, uint32_t tmem, uint8_t* smem, uint64_t* s_full, uint64_t* p_full,
                              uint64_t* o_ready, uint64_t* staged, const CUtensorMap* tmO, float* __restrict__ lse,
-                             int N, int d, float scale_log2, const DropArgs& drop, const CtaGuard& g) {
+                             int N, int Nk, int BH, int d, float scale_log2, const DropArgs& drop,
+                             const CtaGuard& g) {
   using C = F256;
   const int r = threadIdx.x & 127;
   const int row = w.qt * 128 + r;
@@ -229,8 +254,8 @@ __device__ void f256_softmax(const W256& w, uint32_t tmem, uint8_t* smem, uint64
     tmem_ld_fence(s[2]);
     tmem_ld_fence(s[3]);
 
-    const int kv0 = j * 128;
-    int lim = N - kv0;
+    const int kv0 = (w.kt0 + j) * 128;
+    int lim = Nk - kv0;
     if (CAUSAL) lim = min(lim, row - kv0 + 1);
     if (lim < 128) {
 #pragma unroll
@@ -315,39 +340,76 @@ __device__ void f256_softmax(const W256& w, uint32_t tmem, uint8_t* smem, uint64
   tc_fence_after();
   const float inv_l = l > 0.f ? (DROPOUT ? drop.scale : 1.f) / l : 0.f;
   const uint32_t stage = smem_u32(smem + C::kQOff);
+  if constexpr (SPLIT) {
+    // fp32 staging: 8 boxes of 128 rows x 32 floats (128-byte rows, swizzled)
+    // over the Q buffer and the ring, whose last readers (S(n-1) and P V(n-1))
+    // have completed and which no copy refills
+    static_assert(C::kSlotOff + C::kSlots * C::kUnitBytes >= 128u * 256u * 4u, "fp32 staging fits");
 #pragma unroll 1
-  for (int c = 0; c < 256; c += 32) {
-    uint32_t o[32];
-    tmem_ld32(tO + c, o);
-    tmem_ld_wait(o);
-    const uint32_t box = stage + (c / 64) * C::kBoxBytes + r * 128;
+    for (int c = 0; c < 256; c += 32) {
+      if (c >= d) break;   // the columns past d are not stored
+      uint32_t o[32];
+      tmem_ld32(tO + c, o);
+      tmem_ld_wait(o);
+      const uint32_t box = stage + (c / 32) * 16384u + r * 128;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int chunk = (c % 64) / 8 + q;
-      float f[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(o[8 * q + e]) * inv_l;
-      st_shared_v4(box + ((chunk ^ (r & 7)) << 4), pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
-                   pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+      for (int q = 0; q < 8; ++q)
+        st_shared_v4(box + ((q ^ (r & 7)) << 4), __float_as_uint(__uint_as_float(o[4 * q]) * inv_l),
+                     __float_as_uint(__uint_as_float(o[4 * q + 1]) * inv_l),
+                     __float_as_uint(__uint_as_float(o[4 * q + 2]) * inv_l),
+                     __float_as_uint(__uint_as_float(o[4 * q + 3]) * inv_l));
     }
+    fence_proxy_async_smem();
+    mbar_arrive(staged);
+    if (r == 0 && mbar_wait(staged, 0, g, kSiteFwd256 | 8u)) {
+      for (int b = 0; b < 8; ++b)
+        if (32 * b < d) tma_store_3d(tmO, smem + C::kQOff + b * 16384u, 32 * b, w.qt * 128, w.split * BH + w.bh);
+      tma_store_commit();
+      tma_store_wait_read_all();
+    }
+    if (row < N)
+      lse[static_cast<size_t>(w.split * BH + w.bh) * N + row] = l > 0.f ? (m_use + __log2f(l)) * kLn2 : -INFINITY;
+  } else {
+#pragma unroll 1
+    for (int c = 0; c < 256; c += 32) {
+      uint32_t o[32];
+      tmem_ld32(tO + c, o);
+      tmem_ld_wait(o);
+      const uint32_t box = stage + (c / 64) * C::kBoxBytes + r * 128;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int chunk = (c % 64) / 8 + q;
+        float f[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(o[8 * q + e]) * inv_l;
+        st_shared_v4(box + ((chunk ^ (r & 7)) << 4), pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                     pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+      }
+    }
+    fence_proxy_async_smem();
+    mbar_arrive(staged);
+    if (r == 0 && mbar_wait(staged, 0, g, kSiteFwd256 | 8u)) {
+      for (int b = 0; b < 4; ++b)
+        if (64 * b < d) tma_store_hd(tmO, smem + C::kQOff + b * C::kBoxBytes, 64 * b, w.qt * 128, w.hc);
+      tma_store_commit();
+      tma_store_wait_read_all();
+    }
+    if (row < N) lse[static_cast<size_t>(w.bh) * N + row] = l > 0.f ? (m_use + __log2f(l)) * kLn2 : -INFINITY;
   }
-  fence_proxy_async_smem();
-  mbar_arrive(staged);
-  if (r == 0 && mbar_wait(staged, 0, g, kSiteFwd256 | 8u)) {
-    for (int b = 0; b < 4; ++b)
-      if (64 * b < d) tma_store_hd(tmO, smem + C::kQOff + b * C::kBoxBytes, 64 * b, w.qt * 128, w.hc);
-    tma_store_commit();
-    tma_store_wait_read_all();
-  }
-  if (row < N) lse[static_cast<size_t>(w.bh) * N + row] = l > 0.f ? (m_use + __log2f(l)) * kLn2 : -INFINITY;
 }
 
-template <bool CAUSAL, bool FD, bool DROPOUT>
+// SPLIT: a split-KV launch (non-causal, no dropout): n_kt key tiles in
+// n_splits chunks of kt_per_split; tmO is then the fp32 partial-output map
+// and lse the partial LSE.  N is the query length and Nk the key length
+// (equal outside split-KV launches).
+template <bool CAUSAL, bool FD, bool DROPOUT, bool SPLIT>
 __global__ void __launch_bounds__(192, 1)
     fa_fwd_d256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                       float* __restrict__ lse, int N, int d, int n_qt, int BH, int H, int band, float scale_log2,
-                       int ks, uint32_t idesc_pv1, const __grid_constant__ DropArgs drop, const WaitCfg wc) {
+                       float* __restrict__ lse, int N, int Nk, int d, int n_qt, int BH, int H, int band,
+                       float scale_log2, int ks, uint32_t idesc_pv1, int n_kt, int n_splits, int kt_per_split,
+                       const __grid_constant__ DropArgs drop, const WaitCfg wc) {
+  static_assert(!SPLIT || (!CAUSAL && !DROPOUT), "split-KV launches are non-causal without dropout");
   using C = F256;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -363,7 +425,7 @@ __global__ void __launch_bounds__(192, 1)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kMiscOff + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const W256 w = w256_work(N, n_qt, BH, H, band, CAUSAL);
+  const W256 w = SPLIT ? w256_split_work(n_qt, n_splits, kt_per_split, n_kt, H) : w256_work(n_qt, BH, H, band, CAUSAL);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kSlots; ++i) mbar_init(&full[i], 1);
@@ -406,8 +468,8 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   } else {
-    f256_softmax<CAUSAL, DROPOUT>(w, tmem, smem, s_full, p_full, o_ready, staged, &tmO, lse, N, d, scale_log2, drop,
-                                  g);
+    f256_softmax<CAUSAL, SPLIT, DROPOUT>(w, tmem, smem, s_full, p_full, o_ready, staged, &tmO, lse, N, Nk, BH, d,
+                                         scale_log2, drop, g);
     __syncwarp();
     tc_fence_before();
     named_bar_sync(1, 160);
@@ -418,15 +480,17 @@ template <bool CAUSAL, bool DROPOUT>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
                      float* lse, const Shape& s, const DropArgs& drop, const WaitCfg& wc, cudaStream_t st) {
   using C = F256;
-  auto kern = s.d == 256 ? fa_fwd_d256_kernel<CAUSAL, true, DROPOUT> : fa_fwd_d256_kernel<CAUSAL, false, DROPOUT>;
+  auto kern = s.d == 256 ? fa_fwd_d256_kernel<CAUSAL, true, DROPOUT, false>
+                         : fa_fwd_d256_kernel<CAUSAL, false, DROPOUT, false>;
   const cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), C::kSmemBytes, C::kThreads, 0);
   if (e != cudaSuccess) return e;
   const int n_qt = (s.N + 127) / 128;
   const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
   const dim3 grid(static_cast<unsigned>(s.B) * s.H * n_qt);
-  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, to, lse, s.N, s.d, n_qt, s.B * s.H, s.H,
+  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, to, lse, s.N, s.N, s.d, n_qt, s.B * s.H, s.H,
                                                  head_band(s.N, s.d), scale_log2, score_ksteps(s.d),
-                                                 idesc_bf16(128, out_cols(s.d) - 128, false, true), drop, wc);
+                                                 idesc_bf16(128, out_cols(s.d) - 128, false, true), n_qt, 1, n_qt,
+                                                 drop, wc);
   return cudaGetLastError();
 }
 
@@ -440,6 +504,23 @@ cudaError_t launch_fwd_d256(const CUtensorMap& tq, const CUtensorMap& tk, const 
                     : launch_t<false, true>(tq, tk, tv, to, lse, s, drop, wc, st);
   return s.causal ? launch_t<true, false>(tq, tk, tv, to, lse, s, drop, wc, st)
                   : launch_t<false, false>(tq, tk, tv, to, lse, s, drop, wc, st);
+}
+
+cudaError_t launch_fwd_d256_split(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                  const CUtensorMap& top, float* lse_part, const Shape& s, int Nk, int n_splits,
+                                  int kt_per_split, const WaitCfg& wc, cudaStream_t st) {
+  using C = F256;
+  auto kern = s.d == 256 ? fa_fwd_d256_kernel<false, true, false, true> : fa_fwd_d256_kernel<false, false, false, true>;
+  const cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), C::kSmemBytes, C::kThreads, 0);
+  if (e != cudaSuccess) return e;
+  const int n_qt = (s.N + 127) / 128, n_kt = (Nk + 127) / 128;
+  const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
+  const dim3 grid(static_cast<unsigned>(s.B) * s.H * n_splits * n_qt);
+  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, top, lse_part, s.N, Nk, s.d, n_qt, s.B * s.H, s.H, 1,
+                                                 scale_log2, score_ksteps(s.d),
+                                                 idesc_bf16(128, out_cols(s.d) - 128, false, true), n_kt, n_splits,
+                                                 kt_per_split, no_drop_args(), wc);
+  return cudaGetLastError();
 }
 
 cudaError_t fwd_d256_status(uint32_t* out, bool reset) {

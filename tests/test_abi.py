@@ -191,7 +191,7 @@ def _splitkv_ws(B, H, Nq, Nk, d, splits):
     per = -(-n_kt // w)
     n_used = -(-n_kt // per)
     rows = B * H * Nq * n_used
-    kd = 64 if d <= 64 else 128
+    kd = 64 if d <= 64 else (128 if d <= 128 else 256)
     r256 = lambda x: (x + 255) // 256 * 256
     return r256(rows * kd * 4) + r256(rows * 4)
 
@@ -201,8 +201,10 @@ def test_splitkv_workspace_sizes(lib):
     fp32 partial outputs (padded to the kernel's head width) plus the partial
     LSE of the chunks actually used, each rounded to 256 bytes."""
     for args in [(1, 1, 1, 1000, 128, 3), (2, 3, 5, 4097, 64, 7), (1, 2, 16, 129, 96, 4),
-                 (1, 1, 1, 128, 40, 8), (2, 1, 33, 70000, 128, 300)]:
+                 (1, 1, 1, 128, 40, 8), (2, 1, 33, 70000, 128, 300), (1, 4, 1, 9000, 256, 6),
+                 (2, 2, 130, 300, 200, 2)]:
         assert lib.fa_fwd_splitkv_workspace_bytes(*args) == _splitkv_ws(*args), args
     assert lib.fa_fwd_splitkv_workspace_bytes(1, 1, 1, 0, 128, 4) == 0     # no keys
     assert lib.fa_fwd_splitkv_workspace_bytes(1, 1, 0, 100, 128, 4) == 0   # no queries
     assert lib.fa_fwd_splitkv_workspace_bytes(1, 1, 1, 100, 100, 4) == 0   # d not a multiple of 8
+    assert lib.fa_fwd_splitkv_workspace_bytes(1, 1, 1, 100, 264, 4) == 0   # above the widest head

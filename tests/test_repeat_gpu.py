@@ -71,7 +71,9 @@ CASES = {
     "bwd_d256_causal": lambda: _bwd(2, 4, 2048, 256, True, 909),
     "bwd_d192": lambda: _bwd(1, 4, 1100, 192, False, 910),
     "dropout_d128_causal": lambda: _dropout(2, 4, 1024, 128, True, 911),
+    "dropout_d256_causal": lambda: _dropout(1, 4, 1024, 256, True, 914),
     "splitkv_d128": lambda: _splitkv(2, 8, 128, 8192, 128, 912),
+    "splitkv_d256": lambda: _splitkv(2, 8, 64, 8192, 256, 915),
     "fp8_d128_causal": lambda: _fp8(2, 8, 2048, 128, True, 913),
 }
 

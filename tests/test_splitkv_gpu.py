@@ -20,6 +20,12 @@ CASES = [
     (1, 4, 64, 128, 64, 5),         # more splits wanted than key tiles
     (1, 1, 17, 129, 128, 2),        # a one-key last chunk
     (3, 2, 33, 700, 64, 1),         # one chunk: the plain kernel plus the merge
+    # wide heads (the d = 256 kernel's split mode)
+    (1, 1, 1, 3000, 256, 0),
+    (2, 2, 200, 3000, 256, 7),      # two query tiles, ragged key tail
+    (1, 3, 17, 129, 160, 2),        # a one-key last chunk, d below the box width
+    (1, 2, 40, 1500, 192, 1),       # one chunk
+    (1, 2, 64, 128, 200, 5),        # more splits wanted than key tiles, d not a multiple of 32
 ]
 
 
@@ -41,10 +47,11 @@ def test_splitkv_parity(B, H, Nq, Nk, d, splits):
     assert oracle.lse_max_abs_err(f64(lse), lse_ref) <= TOL_LSE
 
 
-def test_splitkv_split_counts_agree():
+@pytest.mark.parametrize("d", [128, 256])
+def test_splitkv_split_counts_agree(d):
     """Every chunking reaches the same exact result, within the forward tolerance
     of the oracle, and the same chunking twice is bitwise the same."""
-    B, H, Nq, Nk, d = 2, 2, 40, 2500, 128
+    B, H, Nq, Nk = 2, 2, 40, 2500
     x = make_splitkv_inputs(B, H, Nq, Nk, d, 77)
     g = {k: t.cuda() for k, t in x.items()}
     o_ref, lse_ref = oracle.attn_fwd_ref(f64(x["q"]), f64(x["k"]), f64(x["v"]), 0.1, False)
@@ -71,18 +78,19 @@ def test_splitkv_matches_plain_forward_when_lengths_agree():
     assert (lse_s - lse_p).abs().max().item() <= 2 * TOL_LSE
 
 
-def test_splitkv_empty_keys_and_queries():
+@pytest.mark.parametrize("d", [64, 256])
+def test_splitkv_empty_keys_and_queries(d):
     """Nk == 0: every row has no key, O = 0 and LSE = -inf; Nq == 0 is a no-op."""
-    q = torch.randn(2, 2, 9, 64, device="cuda").to(torch.bfloat16)
-    kv = torch.empty(2, 2, 0, 64, device="cuda", dtype=torch.bfloat16)
+    q = torch.randn(2, 2, 9, d, device="cuda").to(torch.bfloat16)
+    kv = torch.empty(2, 2, 0, d, device="cuda", dtype=torch.bfloat16)
     o = torch.full_like(q, 7.0)
     lse = torch.zeros(2, 2, 9, device="cuda")
     fa.fa_fwd_splitkv(q, kv, kv, None, 0, out=o, lse=lse)
     torch.cuda.synchronize()
     assert_no_timeout()
     assert torch.all(o == 0) and torch.all(torch.isneginf(lse))
-    q0 = torch.empty(2, 2, 0, 64, device="cuda", dtype=torch.bfloat16)
-    k = torch.randn(2, 2, 300, 64, device="cuda").to(torch.bfloat16)
+    q0 = torch.empty(2, 2, 0, d, device="cuda", dtype=torch.bfloat16)
+    k = torch.randn(2, 2, 300, d, device="cuda").to(torch.bfloat16)
     o0, lse0 = fa.fa_fwd_splitkv(q0, k, k, None, 0)
     assert o0.numel() == 0 and lse0.numel() == 0
 

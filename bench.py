@@ -649,7 +649,7 @@ def run_splitkv(args, dist: Dist):
                    "d": d, "causal": False, "num_splits": ns if ns > 0 else "library choice (0)",
                    "l2": f"inputs larger than L2: K and V are {2 * B * H * Nk * d * 2 / 1e6:.0f} MB together",
                    "step": "fa_fwd_splitkv (split forward kernel + merge kernel)"},
-        "roofline": {"kernel": ("fa_fwd_d256_kernel<split>" if d > 128 else "fa_fwd_kernel<split>")
+        "roofline": {"kernel": "fa_fwd_d256_kernel<split>"
                      + " + fa_fwd_merge_kernel", "bound": "hbm",
                      "achieved": round(algo / (ms * 1e-3) / 1e9, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(algo / (ms * 1e-3) / 1e9 / hbm, 3), "peak_source": f"{peak_src} HBM copy",

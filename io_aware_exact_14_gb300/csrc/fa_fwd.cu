@@ -80,17 +80,14 @@ struct FwdCfg {
 };
 
 // A CTA's work: head bh, query tiles qt0 (and qt0 + 1 when n1 > 0), key
-// tiles kt0 .. kt0 + n - 1 (n0 / n1 of them for tile 0 / 1), and the key
-// split whose partial result it writes (split-KV launches only).
+// tiles 0 .. n - 1 (n0 / n1 of them for tile 0 / 1).
 struct FwdWork {
-  int bh, qt0, n0, n1, n, kt0, split;
+  int bh, qt0, n0, n1, n;
   HeadCoord hc;   // bh as (h, b) for the 4-D tensor maps
 };
 
 __device__ __forceinline__ FwdWork fwd_work(int N, int n_pairs, int BH, int H, int band, bool causal) {
   FwdWork w;
-  w.kt0 = 0;
-  w.split = 0;
   int rank;
   banded_order(blockIdx.x, n_pairs, BH, band, w.bh, rank);
   w.hc = head_coord(w.bh, H);
@@ -101,24 +98,6 @@ __device__ __forceinline__ FwdWork fwd_work(int N, int n_pairs, int BH, int H, i
   w.n0 = causal ? min(w.qt0 + 1, n_qt) : n_qt;
   w.n1 = qt1 < n_qt ? (causal ? min(qt1 + 1, n_qt) : n_qt) : 0;
   w.n = max(w.n0, w.n1);
-  return w;
-}
-
-// Split-KV: CTA u takes one query tile of one head and one chunk of
-// kt_per_split key tiles (the last chunk may be shorter, never empty).  CTAs
-// of one (head, chunk) are adjacent, so they share the chunk's K/V in L2.
-__device__ __forceinline__ FwdWork fwd_split_work(int u, int n_qt, int n_splits, int kt_per_split, int n_kt,
-                                                 int H) {
-  FwdWork w;
-  w.qt0 = u % n_qt;
-  const int rest = u / n_qt;
-  w.split = rest % n_splits;
-  w.bh = rest / n_splits;
-  w.hc = head_coord(w.bh, H);
-  w.kt0 = w.split * kt_per_split;
-  w.n0 = min(kt_per_split, n_kt - w.kt0);
-  w.n1 = 0;
-  w.n = w.n0;
   return w;
 }
 
@@ -161,12 +140,12 @@ __device__ __forceinline__ void fwd_producer(const FwdWork& w, uint8_t* smem, ui
       if (j + kL2Ahead < w.n) {   // the same tile kL2Ahead steps on, into L2 while this one lands
 #pragma unroll
         for (int b = 0; b < C::kBoxes; ++b)
-          tma_prefetch_l2_hd(kind ? tmV : tmK, 64 * b, 128 * (w.kt0 + j + kL2Ahead), w.hc);
+          tma_prefetch_l2_hd(kind ? tmV : tmK, 64 * b, 128 * (j + kL2Ahead), w.hc);
       }
       uint8_t* dst = smem + C::kSlotOff + (idx % C::kSlots) * C::kTileBytes;
 #pragma unroll
       for (int b = 0; b < C::kBoxes; ++b)
-        tma_load_hd(dst + b * C::kBoxBytes, kind ? tmV : tmK, &full[grp % C::kGroups], 64 * b, 128 * (w.kt0 + j),
+        tma_load_hd(dst + b * C::kBoxBytes, kind ? tmV : tmK, &full[grp % C::kGroups], 64 * b, 128 * j,
                     w.hc);
       issued = idx + 1;
     }
@@ -322,18 +301,13 @@ __device__ __forceinline__ void fwd_mma_both(const FwdWork& w, uint32_t tmem, ui
   }
 }
 
-// SPLIT: a split-KV CTA (one query tile, one chunk of keys): O of the chunk
-// is stored in fp32 to the partial-output map (z = split * BH + bh) and the
-// chunk's LSE to lse[(split * BH + bh) * N + row]; otherwise O goes out in
-// bf16 and z = bh, split = 0.  N is the query length, Nk the key length.
 // DROPOUT: the probabilities that feed O += P V are multiplied by the keep
 // mask and the scale (the row sum l, hence LSE, uses the plain ones).
-template <int D, bool CAUSAL, bool SPLIT, bool DROPOUT>
+template <int D, bool CAUSAL, bool DROPOUT>
 __device__ __forceinline__ void fwd_softmax(const FwdWork& w, int tile, uint32_t tmem, uint8_t* smem,
                                             uint64_t* s_full, uint64_t* p_full, uint64_t* o_done,
                                             uint64_t* staged, const CUtensorMap* tmO, float* __restrict__ lse, int N,
-                                            int Nk, int BH, float scale_log2, const DropArgs& drop,
-                                            const CtaGuard& g) {
+                                            float scale_log2, const DropArgs& drop, const CtaGuard& g) {
   using C = FwdCfg<D>;
   const int n_i = tile ? w.n1 : w.n0;
   if (n_i == 0) return;
@@ -353,7 +327,7 @@ __device__ __forceinline__ void fwd_softmax(const FwdWork& w, int tile, uint32_t
     uint32_t kp[DROPOUT ? 8 : 1];
     if constexpr (DROPOUT) {
       uint32_t ge[32];
-      dropout_rows<8>(drop, w.bh, row, (w.kt0 + j) * 128, ge);
+      dropout_rows<8>(drop, w.bh, row, j * 128, ge);
 #pragma unroll
       for (int g = 0; g < 8; ++g) kp[g] = pack_keep4(ge[4 * g], ge[4 * g + 1], ge[4 * g + 2], ge[4 * g + 3]);
     }
@@ -371,8 +345,8 @@ __device__ __forceinline__ void fwd_softmax(const FwdWork& w, int tile, uint32_t
     tmem_ld_fence(s[3]);
 
     // keys kv0 .. kv0+lim-1 are visible to this row
-    const int kv0 = (w.kt0 + j) * 128;
-    int lim = Nk - kv0;
+    const int kv0 = j * 128;
+    int lim = N - kv0;
     if (CAUSAL) lim = min(lim, row - kv0 + 1);
     if (lim < 128) {
 #pragma unroll
@@ -448,82 +422,44 @@ __device__ __forceinline__ void fwd_softmax(const FwdWork& w, int tile, uint32_t
   __syncwarp();
   tc_fence_after();
   const float inv_l = l > 0.f ? (DROPOUT ? drop.scale : 1.f) / l : 0.f;
-  if constexpr (SPLIT) {
-    // fp32 staging: D/32 boxes of 128 rows x 32 floats (128-byte rows, swizzled)
-    // across both Q buffers; a split-KV CTA has one query tile, and its last
-    // S product (the Q buffer's last reader) finished before o_done
-    static_assert(2 * C::kTileBytes >= 128u * D * 4u, "fp32 staging fits the two Q buffers");
-    const uint32_t stage = smem_u32(smem + C::kQOff);
+  const uint32_t stage = smem_u32(smem + C::kQOff + tile * C::kTileBytes);
 #pragma unroll
-    for (int c = 0; c < D; c += 32) {
-      uint32_t o[32];
-      tmem_ld32(tO + c, o);
-      tmem_ld_wait(o);
-      const uint32_t box = stage + (c / 32) * 16384u + r * 128;
+  for (int c = 0; c < D; c += 32) {
+    uint32_t o[32];
+    tmem_ld32(tO + c, o);
+    tmem_ld_wait(o);
+    const uint32_t box = stage + (c / 64) * C::kBoxBytes + r * 128;
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        st_shared_v4(box + ((q ^ (r & 7)) << 4), __float_as_uint(__uint_as_float(o[4 * q]) * inv_l),
-                     __float_as_uint(__uint_as_float(o[4 * q + 1]) * inv_l),
-                     __float_as_uint(__uint_as_float(o[4 * q + 2]) * inv_l),
-                     __float_as_uint(__uint_as_float(o[4 * q + 3]) * inv_l));
-    }
-    fence_proxy_async_smem();
-    mbar_arrive(&staged[tile]);
-    if (r == 0 && mbar_wait(&staged[tile], 0, g, kSiteFwd | 8u)) {
+    for (int q = 0; q < 4; ++q) {
+      const int chunk = (c % 64) / 8 + q;
+      float f[8];
 #pragma unroll
-      for (int b = 0; b < D / 32; ++b)
-        tma_store_3d(tmO, smem + C::kQOff + b * 16384u, 32 * b, qt * 128, w.split * BH + w.bh);
-      tma_store_commit();
-      tma_store_wait_read_all();
-    }
-  } else {
-    const uint32_t stage = smem_u32(smem + C::kQOff + tile * C::kTileBytes);
-#pragma unroll
-    for (int c = 0; c < D; c += 32) {
-      uint32_t o[32];
-      tmem_ld32(tO + c, o);
-      tmem_ld_wait(o);
-      const uint32_t box = stage + (c / 64) * C::kBoxBytes + r * 128;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int chunk = (c % 64) / 8 + q;
-        float f[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(o[8 * q + e]) * inv_l;
-        st_shared_v4(box + ((chunk ^ (r & 7)) << 4), pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
-                     pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
-      }
-    }
-    fence_proxy_async_smem();
-    mbar_arrive(&staged[tile]);
-    if (r == 0 && mbar_wait(&staged[tile], 0, g, kSiteFwd | 8u)) {
-#pragma unroll
-      for (int b = 0; b < C::kBoxes; ++b)
-        tma_store_hd(tmO, smem + C::kQOff + tile * C::kTileBytes + b * C::kBoxBytes, 64 * b, qt * 128, w.hc);
-      tma_store_commit();
-      tma_store_wait_read_all();
+      for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(o[8 * q + e]) * inv_l;
+      st_shared_v4(box + ((chunk ^ (r & 7)) << 4), pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                   pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
     }
   }
-  if (row < N)
-    lse[static_cast<size_t>(w.split * BH + w.bh) * N + row] = l > 0.f ? (m_use + __log2f(l)) * kLn2 : -INFINITY;
+  fence_proxy_async_smem();
+  mbar_arrive(&staged[tile]);
+  if (r == 0 && mbar_wait(&staged[tile], 0, g, kSiteFwd | 8u)) {
+#pragma unroll
+    for (int b = 0; b < C::kBoxes; ++b)
+      tma_store_hd(tmO, smem + C::kQOff + tile * C::kTileBytes + b * C::kBoxBytes, 64 * b, qt * 128, w.hc);
+    tma_store_commit();
+    tma_store_wait_read_all();
+  }
+  if (row < N) lse[static_cast<size_t>(w.bh) * N + row] = l > 0.f ? (m_use + __log2f(l)) * kLn2 : -INFINITY;
 }
 
 // ISSUERS: MMA-issuing warps, 1 (warp 9 issues both tiles) or 2 (one per tile).
-// SPLIT: a split-KV launch (non-causal, one issuer): CTA u takes query tile
-// u % n_qt of one head and one chunk of kt_per_split of the n_kt key tiles;
-// tmO is then the fp32 partial-output map and lse the partial LSE.  N is the
-// query length and Nk the key length (equal outside split-KV launches).
 // DROPOUT: dropout on the probabilities (mask from `drop`, see fwd_softmax).
 // FD: d == D (compile-time K steps and output width of the products).
-template <int D, bool CAUSAL, int ISSUERS, bool SPLIT, bool DROPOUT, bool FD>
+template <int D, bool CAUSAL, int ISSUERS, bool DROPOUT, bool FD>
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                  float* __restrict__ lse, int N, int n_pairs, int BH, int H, int band, float scale_log2, int Nk,
-                  int n_qt, int n_kt, int n_splits, int kt_per_split, int ks, uint32_t idesc_pv,
-                  const __grid_constant__ DropArgs drop, const WaitCfg wc) {
-  static_assert(!SPLIT || (!CAUSAL && ISSUERS == 1), "split-KV launches are non-causal with one issuer");
-  static_assert(!(SPLIT && DROPOUT), "split-KV launches have no dropout");
+                  float* __restrict__ lse, int N, int n_pairs, int BH, int H, int band, float scale_log2, int ks,
+                  uint32_t idesc_pv, const __grid_constant__ DropArgs drop, const WaitCfg wc) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -541,8 +477,7 @@ __global__ void __launch_bounds__(384, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const FwdWork w = SPLIT ? fwd_split_work(static_cast<int>(blockIdx.x), n_qt, n_splits, kt_per_split, n_kt, H)
-                          : fwd_work(N, n_pairs, BH, H, band, CAUSAL);
+  const FwdWork w = fwd_work(N, n_pairs, BH, H, band, CAUSAL);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kGroups; ++i) {
@@ -599,8 +534,8 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else {
     regs_inc<C::kRegsSoftmax>();
-    fwd_softmax<D, CAUSAL, SPLIT, DROPOUT>(w, warp >> 2, tmem, smem, s_full, p_full, o_done, staged, &tmO, lse, N,
-                                           Nk, BH, scale_log2, drop, g);
+    fwd_softmax<D, CAUSAL, DROPOUT>(w, warp >> 2, tmem, smem, s_full, p_full, o_done, staged, &tmO, lse, N,
+                                    scale_log2, drop, g);
     __syncwarp();
     tc_fence_before();
     named_bar_sync(1, 256 + 32 * ISSUERS);
@@ -613,8 +548,7 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
                          const WaitCfg& wc, cudaStream_t st) {
   using C = FwdCfg<D>;
   // d == D: the compile-time instantiation; two issuing warps only there
-  auto kern = s.d == D ? fa_fwd_kernel<D, CAUSAL, ISSUERS, false, DROPOUT, true>
-                       : fa_fwd_kernel<D, CAUSAL, 1, false, DROPOUT, false>;
+  auto kern = s.d == D ? fa_fwd_kernel<D, CAUSAL, ISSUERS, DROPOUT, true> : fa_fwd_kernel<D, CAUSAL, 1, DROPOUT, false>;
   // opt-in shared memory; the softmax warpgroups' setmaxnreg split must fit the launch allocation
   const cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), C::kSmemBytes, C::kThreads, C::kRegsNeeded);
   if (e != cudaSuccess) return e;
@@ -623,9 +557,8 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
   const dim3 grid(static_cast<unsigned>(s.B) * s.H * n_pairs);
   kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, to, lse, s.N, n_pairs, s.B * s.H, s.H,
-                                                 head_band(s.N, s.d), scale_log2, s.N, n_qt, n_qt, 1, n_qt,
-                                                 score_ksteps(s.d), idesc_bf16(128, out_cols(s.d), false, true),
-                                                 drop, wc);
+                                                 head_band(s.N, s.d), scale_log2, score_ksteps(s.d),
+                                                 idesc_bf16(128, out_cols(s.d), false, true), drop, wc);
   return cudaGetLastError();
 }
 
@@ -692,27 +625,9 @@ cudaError_t launch_fwd_splitkv_t(const CUtensorMap& tq, const CUtensorMap& tk, c
                                  const Shape& s, int Nk, int n_splits, int kt_per_split, const WaitCfg& wc,
                                  cudaStream_t st) {
   const int BH = s.B * s.H;
-  cudaError_t e;
-  if (n_splits > 0) {
-    if constexpr (D == 256) {   // wide heads: their own kernel's split mode
-      e = launch_fwd_d256_split(tq, tk, tv, top, lse_part, s, Nk, n_splits, kt_per_split, wc, st);
-      if (e != cudaSuccess) return e;
-    } else {
-      using C = FwdCfg<D>;
-      const int n_qt = (s.N + 127) / 128;
-      const int n_kt = (Nk + 127) / 128;
-      auto kern = s.d == D ? fa_fwd_kernel<D, false, 1, true, false, true>
-                           : fa_fwd_kernel<D, false, 1, true, false, false>;
-      e = prepare_kernel(reinterpret_cast<const void*>(kern), C::kSmemBytes, C::kThreads, C::kRegsNeeded);
-      if (e != cudaSuccess) return e;
-      const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
-      const dim3 grid(static_cast<unsigned>(BH) * n_splits * n_qt);
-      kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, top, lse_part, s.N, n_qt, BH, s.H, 1, scale_log2,
-                                                     Nk, n_qt, n_kt, n_splits, kt_per_split, score_ksteps(s.d),
-                                                     idesc_bf16(128, out_cols(s.d), false, true), no_drop_args(),
-                                                     wc);
-      if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
+  if (n_splits > 0) {   // the chunks: the one-query-tile kernel's split mode
+    const cudaError_t e = launch_fwd_onetile_split(tq, tk, tv, top, lse_part, s, Nk, n_splits, kt_per_split, wc, st);
+    if (e != cudaSuccess) return e;
   }
   const long long rows = static_cast<long long>(BH) * s.N;
   const long long blocks = (rows + 7) / 8;   // 8 warps (rows) per block

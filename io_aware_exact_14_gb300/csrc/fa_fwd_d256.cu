@@ -1,33 +1,39 @@
-// Forward pass for wide heads (128 < d <= 256, kernel built for D = 256) on
-// sm_103a: the same method as fa_fwd.cu -- query tile on chip, K/V tiles
+// One-query-tile forward on sm_103a: wide heads (128 < d <= 256, kernel
+// width DK = 256) and every split-KV launch (DK = 64, 128 or 256, the
+// kernel width of d).  The same method as fa_fwd.cu -- query tile on chip, K/V tiles
 // streamed, running (m, l, acc) with one division by l at the end
 // ("为什么Flash Attention能将注意力计算提速数倍而不损失精度", sections
 // "分块计算（Tiling）" and "在线Softmax技巧"; "FlashAttention的Triton实现：
 // IO-aware注意力机制底层原理", section "分块策略：SRAM容量限制下的精打细算", which
 // sizes the blocks from the on-chip budget and the head dim).
 //
-// Why a kernel of its own: at D = 256 one query tile's O accumulator takes
+// Why a kernel of its own: at DK = 256 one query tile's O accumulator takes
 // 256 of the 512 TMEM columns, so a CTA holds one query tile (not two), and a
 // 128 x 256 bf16 K or V tile is 64 KB, so the ring moves d-halves.
 //
 // GB300 design (one CTA per SM, 192 threads):
 //   warps 0-3  softmax (thread = query row = TMEM lane)
-//   warp  4    TMA producer: Q once (4 boxes), then K/V d-halves ("units",
-//              128 rows x 128 columns = 32 KB) through a 5-slot ring
+//   warp  4    TMA producer: Q once (DK / 64 boxes), then K/V "units"
+//              (DK = 256: d-halves of 128 rows x 128 columns = 32 KB; else
+//              whole tiles) through the ring
 //   warp  5    TMEM owner and tcgen05.mma issuer (elect.sync in a converged warp)
 // TMEM: S buffers [0,128) and [128,256) (key step j uses buffer j & 1, so
-// S(j+1) is computed while the softmax works on S(j)); O [256, 512).
+// S(j+1) is computed while the softmax works on S(j)); O [256, 256 + DK).
 // P (bf16) overwrites the first 64 columns of its S buffer and feeds
-// O += P V from TMEM, one 128-column half of O per V unit.
+// O += P V from TMEM, one 128-column part of O per V unit.
 // Tiles stream in the order the products need them: K_0 K_1 V_0 K_2 V_1 ...
-// K_{n-1} V_{n-2} V_{n-1}; each tile is two units (d-halves), each unit lands
-// on its slot's barrier, and one commit per tile releases both units.
+// K_{n-1} V_{n-2} V_{n-1}; each unit lands on its slot's barrier, and one
+// commit per tile releases its units.
 // Lazy rescaling as in fa_fwd.cu: a row keeps its reference max until a block
 // exceeds it by more than 2^8; O is rescaled in TMEM only when some row of
 // the warp moves, after the previous P V product has completed.
 // Split-KV launches (non-causal): a CTA takes one query tile and one chunk of
 // key tiles and writes the chunk's normalised O in fp32 (staged across the
 // then idle Q buffer and ring) and its LSE; fa_fwd.cu's merge combines them.
+// For a decode-shaped call (a few query rows against many keys) this layout
+// streams K/V best: S is double-buffered, so the next tile's scores overlap
+// the softmax, and the ring holds every byte shared memory leaves beside Q
+// (DK = 64: 13 tiles of 16 KB; DK = 128: 6 of 32 KB; DK = 256: 5 d-halves).
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
 
@@ -42,19 +48,33 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint32_t kSiteFwd256 = 0x400;
 
+// DK: the kernel's head width (256 for wide heads; split-KV launches also
+// run it at 64 and 128).  A K or V tile moves as kHalves units of
+// kUnitBoxes 64-column boxes; the ring takes what shared memory leaves
+// beside Q.  Each tile's release is one commit on empty[tile % kTileBars],
+// and kTileBars * kHalves >= kSlots, so a release barrier is never reused
+// before the producer has waited on it.
+template <int DK>
 struct F256 {
+  static_assert(DK == 64 || DK == 128 || DK == 256, "kernel head width");
+  static constexpr int kHalves = DK == 256 ? 2 : 1;                // units per tile
+  static constexpr int kUnitBoxes = DK == 64 ? 1 : 2;              // boxes per unit
+  static constexpr int kUnitSteps = 4 * kUnitBoxes;                // 16-column K steps per unit
   static constexpr uint32_t kBoxBytes = 128u * 128u;       // 128 rows x 64 bf16 (128 B, swizzled)
-  static constexpr uint32_t kUnitBytes = 2 * kBoxBytes;    // 128 rows x 128 bf16: one d-half
-  static constexpr int kSlots = 5;
-  static constexpr int kTileBars = 4;
-  static constexpr uint32_t kQOff = 0;                     // 4 boxes; O staging at the end
-  static constexpr uint32_t kSlotOff = 4 * kBoxBytes;
+  static constexpr uint32_t kUnitBytes = kUnitBoxes * kBoxBytes;
+  static constexpr int kQBoxes = DK / 64;
+  static constexpr int kSlots = DK == 256 ? 5 : (DK == 128 ? 6 : 13);
+  static constexpr int kTileBars = DK == 256 ? 4 : 16;
+  static_assert(kTileBars * kHalves >= kSlots, "release barriers outlast the ring");
+  static constexpr uint32_t kQOff = 0;                     // Q boxes; O staging at the end
+  static constexpr uint32_t kSlotOff = kQBoxes * kBoxBytes;
   static constexpr uint32_t kBarOff = kSlotOff + kSlots * kUnitBytes;
   // full[kSlots], empty[kTileBars], q_full, s_full[2], p_full, o_ready, staged, drain
   static constexpr int kBars = kSlots + kTileBars + 7;
   static constexpr uint32_t kMiscOff = kBarOff + kBars * 8;   // tmem holder, abort flag
   static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;   // + alignment slack
   static_assert(kSmemBytes <= 232448, "shared-memory budget");
+  static_assert(kBarOff >= 128u * DK * 4u, "fp32 staging of O fits the Q buffer and the ring");
   static constexpr int kThreads = 192;
   static constexpr uint32_t kColO = 256;
 };
@@ -114,19 +134,21 @@ __device__ __forceinline__ W256 w256_split_work(int n_qt, int n_splits, int kt_p
   return w;
 }
 
+template <int DK>
 __device__ void f256_producer(const W256& w, uint8_t* smem, uint64_t* full, uint64_t* empty, uint64_t* q_full,
                               const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
                               const CtaGuard& g) {
-  using C = F256;
-  mbar_arrive_expect_tx(q_full, 4 * C::kBoxBytes);
+  using C = F256<DK>;
+  mbar_arrive_expect_tx(q_full, C::kQBoxes * C::kBoxBytes);
 #pragma unroll
-  for (int b = 0; b < 4; ++b) tma_load_hd(smem + C::kQOff + b * C::kBoxBytes, tmQ, q_full, 64 * b, 128 * w.qt, w.hc);
-  const int units = 4 * w.n;
+  for (int b = 0; b < C::kQBoxes; ++b)
+    tma_load_hd(smem + C::kQOff + b * C::kBoxBytes, tmQ, q_full, 64 * b, 128 * w.qt, w.hc);
+  const int units = 2 * C::kHalves * w.n;
   int issued = 0;
   for (int u = 0; u < units; ++u) {
-    const int t = u >> 1, h = u & 1, slot = u % C::kSlots;
-    if (u >= C::kSlots) {   // the slot's previous unit belongs to tile (u - kSlots) / 2: wait for its release
-      const int pt = (u - C::kSlots) >> 1;
+    const int t = u / C::kHalves, h = u % C::kHalves, slot = u % C::kSlots;
+    if (u >= C::kSlots) {   // the slot's previous unit belongs to tile (u - kSlots) / kHalves: wait for its release
+      const int pt = (u - C::kSlots) / C::kHalves;
       if (!mbar_wait(&empty[pt % C::kTileBars], (pt / C::kTileBars) & 1, g, kSiteFwd256 | 1u)) break;
     }
     bool is_v;
@@ -135,7 +157,7 @@ __device__ void f256_producer(const W256& w, uint8_t* smem, uint64_t* full, uint
     uint8_t* dst = smem + C::kSlotOff + slot * C::kUnitBytes;
     mbar_arrive_expect_tx(&full[slot], C::kUnitBytes);
 #pragma unroll
-    for (int b = 0; b < 2; ++b)
+    for (int b = 0; b < C::kUnitBoxes; ++b)
       tma_load_hd(dst + b * C::kBoxBytes, is_v ? tmV : tmK, &full[slot], 128 * h + 64 * b, 128 * (w.kt0 + j), w.hc);
     issued = u + 1;
   }
@@ -146,24 +168,24 @@ __device__ void f256_producer(const W256& w, uint8_t* smem, uint64_t* full, uint
   }
 }
 
-// Descriptor offset of K step kk (16 columns) inside a 2-box unit (K-major).
+// Descriptor offset of K step kk (16 columns) inside a unit (K-major).
 __device__ __forceinline__ uint64_t kstep_off(int kk) {
-  return static_cast<uint64_t>(((kk / 4) * F256::kBoxBytes + (kk % 4) * 32) >> 4);
+  return static_cast<uint64_t>(((kk / 4) * (128u * 128u) + (kk % 4) * 32) >> 4);
 }
 
 // The MMA warp: S(0) S(1) | PV(0) S(2) | PV(1) S(3) | ... | PV(n-1).
-// ks = ceil(d / 16) steps of 16 columns hold data (9..16 here); the second
-// half of O is idesc_pv1 wide (N = ceil(d / 16) * 16 - 128).  FD (d = 256):
-// compile-time steps and widths; otherwise the steps are predicated.
-template <bool FD>
+// ks = ceil(d / 16) steps of 16 columns hold data; the last unit's part of O
+// is idesc_pvl wide (N = ceil(d / 16) * 16 - 128 (kHalves - 1)).  FD
+// (d = DK): compile-time steps and widths; otherwise the steps are
+// predicated.
+template <int DK, bool FD>
 __device__ void f256_mma(const W256& w, uint32_t tmem, uint32_t sbase, uint64_t* full, uint64_t* empty,
                          uint64_t* q_full, uint64_t* s_full, uint64_t* p_full, uint64_t* o_ready, int ks,
-                         uint32_t idesc_pv1, const CtaGuard& g) {
-  using C = F256;
+                         uint32_t idesc_pvl, const CtaGuard& g) {
+  using C = F256<DK>;
   constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
-  constexpr uint32_t idesc_pv = idesc_bf16(128, 128, false, true);
+  constexpr uint32_t idesc_pv = idesc_bf16(128, 64 * C::kUnitBoxes, false, true);
   const uint64_t qd0 = sdesc_sw128(sbase + C::kQOff, 16, 1024);
-  const uint64_t qd1 = sdesc_sw128(sbase + C::kQOff + C::kUnitBytes, 16, 1024);
   const uint64_t kd0 = sdesc_sw128(sbase + C::kSlotOff, 16, 1024);            // slot 0, K-major
   const uint64_t vd0 = sdesc_sw128(sbase + C::kSlotOff, C::kBoxBytes, 1024);  // slot 0, MN-major
   auto slot_off = [](int u) { return static_cast<uint64_t>((u % C::kSlots) * (C::kUnitBytes >> 4)); };
@@ -172,16 +194,17 @@ __device__ void f256_mma(const W256& w, uint32_t tmem, uint32_t sbase, uint64_t*
   };
   auto issue_s = [&](int buf, int t) -> bool {   // S into buffer `buf` from the K tile at stream position t
     const uint32_t ts = tmem + 128u * buf;
-    for (int h = 0; h < 2; ++h) {
-      if (!unit_wait(2 * t + h)) return false;
-      const uint64_t q = h ? qd1 : qd0, k = kd0 + slot_off(2 * t + h);
+    for (int h = 0; h < C::kHalves; ++h) {
+      if (!unit_wait(C::kHalves * t + h)) return false;
+      const uint64_t q = qd0 + static_cast<uint64_t>((h * C::kUnitBytes) >> 4);
+      const uint64_t k = kd0 + slot_off(C::kHalves * t + h);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
+      for (int kk = 0; kk < C::kUnitSteps; ++kk)
         if constexpr (FD)
           tc_mma_ss_w(ts, q + kstep_off(kk), k + kstep_off(kk), idesc_s, (h | kk) ? 1u : 0u);
         else
           tc_mma_ss_w_if(ts, q + kstep_off(kk), k + kstep_off(kk), idesc_s, (h | kk) ? 1u : 0u,
-                         8 * h + kk < ks ? 1u : 0u);
+                         C::kUnitSteps * h + kk < ks ? 1u : 0u);
     }
     tc_commit_w(&s_full[buf]);
     tc_commit_w(&empty[t % C::kTileBars]);
@@ -192,16 +215,18 @@ __device__ void f256_mma(const W256& w, uint32_t tmem, uint32_t sbase, uint64_t*
   if (w.n > 1 && !issue_s(1, pos_k(1))) return;
   for (int j = 0; j < w.n; ++j) {
     const int t = pos_v(j, w.n), buf = j & 1;
-    if (!unit_wait(2 * t) || !unit_wait(2 * t + 1)) return;
+    for (int h = 0; h < C::kHalves; ++h)
+      if (!unit_wait(C::kHalves * t + h)) return;
     if (!mbar_wait_w(p_full, j & 1, g, kSiteFwd256 | 4u)) return;
     tc_fence_after();
     const uint32_t tp = tmem + 128u * buf;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint64_t v = vd0 + slot_off(2 * t + h);
+    for (int h = 0; h < C::kHalves; ++h) {
+      const uint64_t v = vd0 + slot_off(C::kHalves * t + h);
+      const uint32_t idesc = (h == C::kHalves - 1 && !FD) ? idesc_pvl : idesc_pv;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)   // 128 keys, 16 per MMA; P packs 2 keys per TMEM column
-        tc_mma_ts_w(tmem + C::kColO + 128u * h, tp + kk * 8, v + ((kk * 2048) >> 4), (h && !FD) ? idesc_pv1 : idesc_pv,
+        tc_mma_ts_w(tmem + C::kColO + 128u * h, tp + kk * 8, v + ((kk * 2048) >> 4), idesc,
                     (j > 0 || kk > 0) ? 1u : 0u);
     }
     tc_commit_w(o_ready);
@@ -216,12 +241,12 @@ __device__ void f256_mma(const W256& w, uint32_t tmem, uint32_t sbase, uint64_t*
 // SPLIT: O goes out in fp32 through the partial-output map (z = split * BH +
 // bh) and the LSE to lse[(split * BH + bh) * N + row].  N is the query
 // length, Nk the key length.
-template <bool CAUSAL, bool SPLIT, bool DROPOUT>
+template <int DK, bool CAUSAL, bool SPLIT, bool DROPOUT>
 __device__ void f256_softmax(const W256& w, uint32_t tmem, uint8_t* smem, uint64_t* s_full, uint64_t* p_full,
                              uint64_t* o_ready, uint64_t* staged, const CUtensorMap* tmO, float* __restrict__ lse,
                              int N, int Nk, int BH, int d, float scale_log2, const DropArgs& drop,
                              const CtaGuard& g) {
-  using C = F256;
+  using C = F256<DK>;
   const int r = threadIdx.x & 127;
   const int row = w.qt * 128 + r;
   const uint32_t lane_base = static_cast<uint32_t>((threadIdx.x >> 5) & 3) * 32u << 16;
@@ -318,7 +343,7 @@ __device__ void f256_softmax(const W256& w, uint32_t tmem, uint8_t* smem, uint64
       tc_fence_after();
       if (rescale) {
 #pragma unroll 1
-        for (int c = 0; c < 256; c += 32) {
+        for (int c = 0; c < DK; c += 32) {
           uint32_t o[32];
           tmem_ld32(tO + c, o);
           tmem_ld_wait(o);
@@ -341,12 +366,11 @@ __device__ void f256_softmax(const W256& w, uint32_t tmem, uint8_t* smem, uint64
   const float inv_l = l > 0.f ? (DROPOUT ? drop.scale : 1.f) / l : 0.f;
   const uint32_t stage = smem_u32(smem + C::kQOff);
   if constexpr (SPLIT) {
-    // fp32 staging: 8 boxes of 128 rows x 32 floats (128-byte rows, swizzled)
-    // over the Q buffer and the ring, whose last readers (S(n-1) and P V(n-1))
-    // have completed and which no copy refills
-    static_assert(C::kSlotOff + C::kSlots * C::kUnitBytes >= 128u * 256u * 4u, "fp32 staging fits");
+    // fp32 staging: DK / 32 boxes of 128 rows x 32 floats (128-byte rows,
+    // swizzled) over the Q buffer and the ring, whose last readers (S(n-1)
+    // and P V(n-1)) have completed and which no copy refills
 #pragma unroll 1
-    for (int c = 0; c < 256; c += 32) {
+    for (int c = 0; c < DK; c += 32) {
       if (c >= d) break;   // the columns past d are not stored
       uint32_t o[32];
       tmem_ld32(tO + c, o);
@@ -362,7 +386,7 @@ __device__ void f256_softmax(const W256& w, uint32_t tmem, uint8_t* smem, uint64
     fence_proxy_async_smem();
     mbar_arrive(staged);
     if (r == 0 && mbar_wait(staged, 0, g, kSiteFwd256 | 8u)) {
-      for (int b = 0; b < 8; ++b)
+      for (int b = 0; b < DK / 32; ++b)
         if (32 * b < d) tma_store_3d(tmO, smem + C::kQOff + b * 16384u, 32 * b, w.qt * 128, w.split * BH + w.bh);
       tma_store_commit();
       tma_store_wait_read_all();
@@ -371,7 +395,7 @@ __device__ void f256_softmax(const W256& w, uint32_t tmem, uint8_t* smem, uint64
       lse[static_cast<size_t>(w.split * BH + w.bh) * N + row] = l > 0.f ? (m_use + __log2f(l)) * kLn2 : -INFINITY;
   } else {
 #pragma unroll 1
-    for (int c = 0; c < 256; c += 32) {
+    for (int c = 0; c < DK; c += 32) {
       uint32_t o[32];
       tmem_ld32(tO + c, o);
       tmem_ld_wait(o);
@@ -389,7 +413,7 @@ __device__ void f256_softmax(const W256& w, uint32_t tmem, uint8_t* smem, uint64
     fence_proxy_async_smem();
     mbar_arrive(staged);
     if (r == 0 && mbar_wait(staged, 0, g, kSiteFwd256 | 8u)) {
-      for (int b = 0; b < 4; ++b)
+      for (int b = 0; b < C::kQBoxes; ++b)
         if (64 * b < d) tma_store_hd(tmO, smem + C::kQOff + b * C::kBoxBytes, 64 * b, w.qt * 128, w.hc);
       tma_store_commit();
       tma_store_wait_read_all();
@@ -402,15 +426,16 @@ __device__ void f256_softmax(const W256& w, uint32_t tmem, uint8_t* smem, uint64
 // n_splits chunks of kt_per_split; tmO is then the fp32 partial-output map
 // and lse the partial LSE.  N is the query length and Nk the key length
 // (equal outside split-KV launches).
-template <bool CAUSAL, bool FD, bool DROPOUT, bool SPLIT>
+template <int DK, bool CAUSAL, bool FD, bool DROPOUT, bool SPLIT>
 __global__ void __launch_bounds__(192, 1)
     fa_fwd_d256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                        float* __restrict__ lse, int N, int Nk, int d, int n_qt, int BH, int H, int band,
-                       float scale_log2, int ks, uint32_t idesc_pv1, int n_kt, int n_splits, int kt_per_split,
+                       float scale_log2, int ks, uint32_t idesc_pvl, int n_kt, int n_splits, int kt_per_split,
                        const __grid_constant__ DropArgs drop, const WaitCfg wc) {
   static_assert(!SPLIT || (!CAUSAL && !DROPOUT), "split-KV launches are non-causal without dropout");
-  using C = F256;
+  static_assert(SPLIT || DK == 256, "below d = 256 only split-KV launches run this kernel");
+  using C = F256<DK>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
@@ -457,9 +482,9 @@ __global__ void __launch_bounds__(192, 1)
   const CtaGuard g{abort_flag, g_status_fwd256, wc.epoch, wc.limit_us};
 
   if (warp == 4) {
-    if (lane == 0) f256_producer(w, smem, full, empty, q_full, &tmQ, &tmK, &tmV, g);
+    if (lane == 0) f256_producer<DK>(w, smem, full, empty, q_full, &tmQ, &tmK, &tmV, g);
   } else if (warp == 5) {
-    f256_mma<FD>(w, tmem, smem_u32(smem), full, empty, q_full, s_full, p_full, o_ready, ks, idesc_pv1, g);
+    f256_mma<DK, FD>(w, tmem, smem_u32(smem), full, empty, q_full, s_full, p_full, o_ready, ks, idesc_pvl, g);
     tc_commit_w(drain);   // every MMA issued above has finished before TMEM is released
     mbar_drain(drain, 0);
     __syncwarp();
@@ -468,7 +493,7 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   } else {
-    f256_softmax<CAUSAL, SPLIT, DROPOUT>(w, tmem, smem, s_full, p_full, o_ready, staged, &tmO, lse, N, Nk, BH, d,
+    f256_softmax<DK, CAUSAL, SPLIT, DROPOUT>(w, tmem, smem, s_full, p_full, o_ready, staged, &tmO, lse, N, Nk, BH, d,
                                          scale_log2, drop, g);
     __syncwarp();
     tc_fence_before();
@@ -479,9 +504,9 @@ __global__ void __launch_bounds__(192, 1)
 template <bool CAUSAL, bool DROPOUT>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
                      float* lse, const Shape& s, const DropArgs& drop, const WaitCfg& wc, cudaStream_t st) {
-  using C = F256;
-  auto kern = s.d == 256 ? fa_fwd_d256_kernel<CAUSAL, true, DROPOUT, false>
-                         : fa_fwd_d256_kernel<CAUSAL, false, DROPOUT, false>;
+  using C = F256<256>;
+  auto kern = s.d == 256 ? fa_fwd_d256_kernel<256, CAUSAL, true, DROPOUT, false>
+                         : fa_fwd_d256_kernel<256, CAUSAL, false, DROPOUT, false>;
   const cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), C::kSmemBytes, C::kThreads, 0);
   if (e != cudaSuccess) return e;
   const int n_qt = (s.N + 127) / 128;
@@ -506,11 +531,13 @@ cudaError_t launch_fwd_d256(const CUtensorMap& tq, const CUtensorMap& tk, const 
                   : launch_t<false, false>(tq, tk, tv, to, lse, s, drop, wc, st);
 }
 
-cudaError_t launch_fwd_d256_split(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                  const CUtensorMap& top, float* lse_part, const Shape& s, int Nk, int n_splits,
-                                  int kt_per_split, const WaitCfg& wc, cudaStream_t st) {
-  using C = F256;
-  auto kern = s.d == 256 ? fa_fwd_d256_kernel<false, true, false, true> : fa_fwd_d256_kernel<false, false, false, true>;
+template <int DK>
+cudaError_t launch_split_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const CUtensorMap& top, float* lse_part, const Shape& s, int Nk, int n_splits,
+                           int kt_per_split, const WaitCfg& wc, cudaStream_t st) {
+  using C = F256<DK>;
+  auto kern = s.d == DK ? fa_fwd_d256_kernel<DK, false, true, false, true>
+                        : fa_fwd_d256_kernel<DK, false, false, false, true>;
   const cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), C::kSmemBytes, C::kThreads, 0);
   if (e != cudaSuccess) return e;
   const int n_qt = (s.N + 127) / 128, n_kt = (Nk + 127) / 128;
@@ -518,9 +545,19 @@ cudaError_t launch_fwd_d256_split(const CUtensorMap& tq, const CUtensorMap& tk, 
   const dim3 grid(static_cast<unsigned>(s.B) * s.H * n_splits * n_qt);
   kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, top, lse_part, s.N, Nk, s.d, n_qt, s.B * s.H, s.H, 1,
                                                  scale_log2, score_ksteps(s.d),
-                                                 idesc_bf16(128, out_cols(s.d) - 128, false, true), n_kt, n_splits,
-                                                 kt_per_split, no_drop_args(), wc);
+                                                 idesc_bf16(128, out_cols(s.d) - 128 * (C::kHalves - 1), false, true),
+                                                 n_kt, n_splits, kt_per_split, no_drop_args(), wc);
   return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_onetile_split(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                     const CUtensorMap& top, float* lse_part, const Shape& s, int Nk, int n_splits,
+                                     int kt_per_split, const WaitCfg& wc, cudaStream_t st) {
+  switch (kernel_dim(s.d)) {
+    case 256: return launch_split_t<256>(tq, tk, tv, top, lse_part, s, Nk, n_splits, kt_per_split, wc, st);
+    case 128: return launch_split_t<128>(tq, tk, tv, top, lse_part, s, Nk, n_splits, kt_per_split, wc, st);
+    default: return launch_split_t<64>(tq, tk, tv, top, lse_part, s, Nk, n_splits, kt_per_split, wc, st);
+  }
 }
 
 cudaError_t fwd_d256_status(uint32_t* out, bool reset) {

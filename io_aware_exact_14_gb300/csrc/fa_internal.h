@@ -129,12 +129,14 @@ cudaError_t launch_fwd_splitkv(const CUtensorMap& tq, const CUtensorMap& tk, con
                                const Shape& s, int Nk, int n_splits, int kt_per_split, const WaitCfg& wc,
                                cudaStream_t st);
 
-// The wide-head (d > 128) split-KV chunks: the fp32 partial outputs through
-// `top` ({256, Nq, n_splits*B*H}, box {32, 128, 1}; columns >= d unwritten)
-// and the partial LSE; launch_fwd_splitkv calls it and then merges.
-cudaError_t launch_fwd_d256_split(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                  const CUtensorMap& top, float* lse_part, const Shape& s, int Nk, int n_splits,
-                                  int kt_per_split, const WaitCfg& wc, cudaStream_t st);
+// The split-KV chunks (fa_fwd_d256.cu's one-query-tile kernel at the
+// kernel head width D = kernel_dim(d)): the fp32 partial outputs through
+// `top` ({D, Nq, n_splits*B*H}, box {32, 128, 1}; the 32-column boxes at or
+// past d unwritten) and the partial LSE; launch_fwd_splitkv calls it and
+// then merges.
+cudaError_t launch_fwd_onetile_split(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                     const CUtensorMap& top, float* lse_part, const Shape& s, int Nk, int n_splits,
+                                     int kt_per_split, const WaitCfg& wc, cudaStream_t st);
 
 // Split-KV chunking: `want` splits (<= 0: chosen from the SM count) of the
 // ceil(Nk/128) key tiles into chunks of kt_per_split whole tiles; n_splits is

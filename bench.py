@@ -58,7 +58,8 @@ def parse():
     ap.add_argument("--dropout", type=float, default=0.0,
                     help="drop probability p: time fa_fwd_dropout + fa_bwd_dropout instead (fwd and bwd split only)")
     ap.add_argument("--fp8", action="store_true",
-                    help="time the FP8 (e4m3) forward and its quantiser on the workload instead")
+                    help="time the FP8 (e4m3) forward and its quantiser on the workload instead; with --splitkv, "
+                         "the split-KV forward on e4m3 codes")
     ap.add_argument("--fp8-rotate", type=int, default=1, help="incoherent rotation of Q and K (1) or not (0)")
     ap.add_argument("--splitkv", action="store_true",
                     help="time the split-KV forward on --splitkv-shape instead of the training step")
@@ -597,13 +598,17 @@ def run_reference(args, dist: Dist):
 
 
 SPLITKV_METRIC = "split-KV forward GB/s (bf16 Q, K, V read, O and LSE written, 1xGB300) and % of measured HBM copy"
+SPLITKV_FP8_METRIC = ("split-KV forward on e4m3 codes GB/s (e4m3 Q, K, V^T and descales read, bf16 O and fp32 LSE "
+                      "written, 1xGB300) and % of measured HBM copy")
 
 
 def run_splitkv(args, dist: Dist):
     """Split-KV forward on a decode-shaped workload: HBM-bound (each K/V byte read
     once), so the metric is algorithmic bytes per second against the measured copy
     bandwidth.  Algorithmic bytes per call: Q, K, V read and O, LSE written; the
-    chunks' fp32 partial results in the workspace are counted as overhead, not work."""
+    chunks' fp32 partial results in the workspace are counted as overhead, not work.
+    With --fp8 the keys and values are e4m3 codes (quantised once, outside the
+    timed region, as a cache of them would be) and the call is fa_fwd_fp8_splitkv."""
     import torch
     from io_aware_exact_14_gb300 import fa
     from io_aware_exact_14_gb300.workloads import make_splitkv_inputs
@@ -617,9 +622,18 @@ def run_splitkv(args, dist: Dist):
     o = torch.empty_like(q)
     lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
     ns = args.splitkv_splits
-    ws = torch.empty(max(fa.fa_fwd_splitkv_workspace_bytes(B, H, Nq, Nk, d, ns), 1), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    call = lambda: fa.fa_fwd_splitkv(q, k, v, None, ns, out=o, lse=lse, workspace=ws)
+    if args.fp8:
+        q8, dq = fa.fa_fp8_quantize(q)
+        k8, dk = fa.fa_fp8_quantize(k)
+        vt8, dv = fa.fa_fp8_quantize(v, transpose=True)
+        ws = torch.empty(max(fa.fa_fwd_fp8_splitkv_workspace_bytes(B, H, Nq, Nk, d, ns), 1), dtype=torch.uint8,
+                         device=dev)
+        call = lambda: fa.fa_fwd_fp8_splitkv(q8, k8, vt8, dq, dk, dv, None, ns, out=o, lse=lse, workspace=ws)
+    else:
+        ws = torch.empty(max(fa.fa_fwd_splitkv_workspace_bytes(B, H, Nq, Nk, d, ns), 1), dtype=torch.uint8,
+                         device=dev)
+        call = lambda: fa.fa_fwd_splitkv(q, k, v, None, ns, out=o, lse=lse, workspace=ws)
     clocks = ClockSampler(dist.local)
     clocks.start()
     for _ in range(args.warmup):
@@ -637,26 +651,34 @@ def run_splitkv(args, dist: Dist):
     if fa.fa_debug_status(reset=True) != fa.FA_OK:
         raise RuntimeError(f"kernel pipeline timeout at site {fa.fa_debug_site():#x}")
     ms = dist.max(t0.elapsed_time(t1)) / args.steps
-    algo = 2 * B * H * (2 * Nq + 2 * Nk) * d + 4 * B * H * Nq
+    if args.fp8:   # e4m3 Q, K, V^T (its padded row pitch) and 3 descales per head; bf16 O, fp32 LSE
+        algo = B * H * (Nq * d + Nk * d + d * fa.fa_fp8_vt_ld(Nk) + 12) + B * H * Nq * (2 * d + 4)
+    else:
+        algo = 2 * B * H * (2 * Nq + 2 * Nk) * d + 4 * B * H * Nq
     value = algo * dist.world / (ms * 1e-3) / 1e9
     peaks, peak_src = load_peaks()
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     out = {
-        "metric": SPLITKV_METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": dist.world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16 q, k, v)",
-        "config": {"workload": f"decode_splitkv_B{B}_H{H}_Nq{Nq}_Nk{Nk}_d{d}", "B": B, "H": H, "Nq": Nq, "Nk": Nk,
+        "metric": SPLITKV_FP8_METRIC if args.fp8 else SPLITKV_METRIC, "value": round(value, 1), "unit": "GB/s",
+        "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if args.fp8 else "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 q, k, v" + (", quantised to e4m3 per head)" if args.fp8 else ")"),
+        "config": {"workload": f"decode_splitkv{'_fp8' if args.fp8 else ''}_B{B}_H{H}_Nq{Nq}_Nk{Nk}_d{d}",
+                   "B": B, "H": H, "Nq": Nq, "Nk": Nk,
                    "d": d, "causal": False, "num_splits": ns if ns > 0 else "library choice (0)",
-                   "l2": f"inputs larger than L2: K and V are {2 * B * H * Nk * d * 2 / 1e6:.0f} MB together",
-                   "step": "fa_fwd_splitkv (split forward kernel + merge kernel)"},
-        "roofline": {"kernel": "fa_fwd_d256_kernel<split>"
-                     + " + fa_fwd_merge_kernel", "bound": "hbm",
+                   "l2": f"inputs larger than L2: K and V are {2 * B * H * Nk * d * (1 if args.fp8 else 2) / 1e6:.0f}"
+                         " MB together" if 2 * B * H * Nk * d * (1 if args.fp8 else 2) > 129e6 else
+                         "K and V fit in L2 (no flush between calls)",
+                   "step": ("fa_fwd_fp8_splitkv" if args.fp8 else "fa_fwd_splitkv")
+                           + " (split forward kernel + merge kernel)"},
+        "roofline": {"kernel": f"fa_fwd_d256_kernel<split{', e4m3' if args.fp8 else ''}> + fa_fwd_merge_kernel",
+                     "bound": "hbm",
                      "achieved": round(algo / (ms * 1e-3) / 1e9, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(algo / (ms * 1e-3) / 1e9 / hbm, 3), "peak_source": f"{peak_src} HBM copy",
                      "work_per_launch": algo, "traffic": None},
         "gpu_launches": 2 * args.steps, "clocks": clk,
     }
-    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline and not args.fp8:
         import oracle
         from io_aware_exact_14_gb300.workloads import to_f64
         done, tb = 0, time.time()
@@ -758,11 +780,11 @@ def run_fp8(args, dist: Dist):
 def main():
     args = parse()
     dist = Dist()
-    if args.fp8 and args.impl == "ours":
-        run_fp8(args, dist)
-        return
     if args.splitkv and args.impl == "ours":
         run_splitkv(args, dist)
+        return
+    if args.fp8 and args.impl == "ours":
+        run_fp8(args, dist)
         return
     if args.impl == "reference":
         run_reference(args, dist)

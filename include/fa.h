@@ -265,6 +265,35 @@ fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const floa
                      int B, int H, int N, int d, float scale, int causal, struct CUstream_st* stream);
 
 /*
+ * Split-KV forward on e4m3 codes (non-causal), e.g. decoding against an
+ * e4m3 key/value cache: q8 [B, H, Nq, d], k8 [B, H, Nk, d], vt8
+ * [B, H, d, fa_fp8_vt_ld(Nk)] (from fa_fp8_quantize; V with transpose = 1),
+ * descales fp32 [B, H].  The keys are cut into chunks as in fa_fwd_splitkv;
+ * each chunk computes fa_fwd_fp8's arithmetic (its own reference maximum,
+ * P~ rounded to e4m3) into fp32 partials, merged by their LSE as in
+ * fa_fwd_splitkv.  The error contract of fa_fwd_fp8 holds unchanged: a
+ * chunk's P~ is the row's P~ times e^{m - m_chunk} >= 1, so its rounding is
+ * no larger relative to the row's.  o bf16 [B, H, Nq, d], lse fp32
+ * [B, H, Nq] (Nk == 0: O = 0, LSE = -inf).  workspace: at least
+ * fa_fwd_fp8_splitkv_workspace_bytes(...) bytes, 16-byte aligned (may be
+ * NULL when that is 0), else FA_ERR_WORKSPACE.  d a multiple of 16 in
+ * [16, 128]; Nq == 0 is a no-op; k8, vt8 may be NULL when Nk == 0; other
+ * errors as fa_fwd_splitkv.
+ */
+fa_status fa_fwd_fp8_splitkv(const void* q8, const void* k8, const void* vt8, const float* descale_q,
+                             const float* descale_k, const float* descale_v, void* o, float* lse,
+                             int B, int H, int Nq, int Nk, int d, float scale, int num_splits,
+                             void* workspace, size_t workspace_bytes, struct CUstream_st* stream);
+
+/*
+ * Workspace bytes fa_fwd_fp8_splitkv needs: n_used * B*H*Nq*128 fp32
+ * partial outputs plus n_used * B*H*Nq fp32 partial LSE, each rounded up
+ * to 256 bytes (n_used as in fa_fwd_splitkv_workspace_bytes).  0 for
+ * invalid sizes, Nq == 0 or Nk == 0.
+ */
+size_t fa_fwd_fp8_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int d, int num_splits);
+
+/*
  * Backward step 1: D_i = sum_c dO_ic O_ic (fp32 [B, H, N]), the row term of
  * the softmax Jacobian (derived; not on the pages).  Memory-bound.
  */

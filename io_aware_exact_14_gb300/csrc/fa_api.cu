@@ -376,12 +376,13 @@ struct SplitPlan {
   size_t o_bytes, lse_bytes;
 };
 
-fa_status split_plan(int B, int H, int Nq, int Nk, int d, int want, SplitPlan& p) {
+// width: the partial rows' floats (the kernel width of d; 128 for e4m3).
+fa_status split_plan(int B, int H, int Nq, int Nk, int width, int want, SplitPlan& p) {
   int sms = 0;
   if (want <= 0) FA_TRY(cuda_status(fa::sm_count(&sms), "reading the SM count"));
   fa::splitkv_chunks(B, H, Nq, Nk, want, sms, p.kt_per_split, p.n_splits);
   const size_t rows = static_cast<size_t>(B) * H * Nq * p.n_splits;
-  p.o_bytes = round256(rows * fa::kernel_dim(d) * 4);
+  p.o_bytes = round256(rows * width * 4);
   p.lse_bytes = round256(rows * 4);
   return FA_OK;
 }
@@ -573,7 +574,7 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, f
   if (Nk > 0) FA_TRY(check_ptrs({k, v}, {}));   // never read when there are no keys
   FA_TRY(check_scale(scale));
   SplitPlan p;
-  FA_TRY(split_plan(B, H, Nq, Nk, d, num_splits, p));
+  FA_TRY(split_plan(B, H, Nq, Nk, fa::kernel_dim(d), num_splits, p));
   if (static_cast<long long>(B) * H * p.n_splits * ((Nq + 127) / 128) > INT32_MAX) return FA_ERR_UNSUPPORTED;
   const size_t need = p.n_splits > 0 ? p.o_bytes + p.lse_bytes : 0;
   if (need > 0 && (workspace == nullptr || !aligned(workspace, 16) || workspace_bytes < need)) return FA_ERR_WORKSPACE;
@@ -604,7 +605,56 @@ size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int d, int n
       Nq <= 0 || Nk <= 0)
     return 0;
   SplitPlan p;
-  if (split_plan(B, H, Nq, Nk, d, num_splits, p) != FA_OK || p.n_splits == 0) return 0;
+  if (split_plan(B, H, Nq, Nk, fa::kernel_dim(d), num_splits, p) != FA_OK || p.n_splits == 0) return 0;
+  return p.o_bytes + p.lse_bytes;
+}
+
+fa_status fa_fwd_fp8_splitkv(const void* q8, const void* k8, const void* vt8, const float* descale_q,
+                             const float* descale_k, const float* descale_v, void* o, float* lse, int B, int H,
+                             int Nq, int Nk, int d, float scale, int num_splits, void* workspace,
+                             size_t workspace_bytes, struct CUstream_st* stream) {
+  FA_TRY(check_sizes_fp8(B, H, Nq, d));
+  FA_TRY(check_sizes_fp8(B, H, Nk, d));
+  if (Nq == 0) return FA_OK;
+  FA_TRY(check_ptrs({q8, o}, {descale_q, descale_k, descale_v, lse}));
+  if (Nk > 0) FA_TRY(check_ptrs({k8, vt8}, {}));   // never read when there are no keys
+  FA_TRY(check_scale(scale));
+  SplitPlan p;
+  FA_TRY(split_plan(B, H, Nq, Nk, 128, num_splits, p));
+  if (static_cast<long long>(B) * H * p.n_splits * ((Nq + 127) / 128) > INT32_MAX) return FA_ERR_UNSUPPORTED;
+  const size_t need = p.n_splits > 0 ? p.o_bytes + p.lse_bytes : 0;
+  if (need > 0 && (workspace == nullptr || !aligned(workspace, 16) || workspace_bytes < need)) return FA_ERR_WORKSPACE;
+  const Shape sq{B, H, Nq, d, scale, 0};
+  const size_t q_bytes = tensor_bytes(sq) / 2, k_bytes = static_cast<size_t>(B) * H * Nk * d;
+  const size_t vt_bytes = static_cast<size_t>(B) * H * d * fp8_vt_ld(Nk), ds_bytes = static_cast<size_t>(B) * H * 4;
+  FA_TRY(check_disjoint({{o, tensor_bytes(sq)}, {lse, vec_bytes(sq)}, {workspace, need}},
+                        {{q8, q_bytes}, {k8, k_bytes}, {vt8, vt_bytes}, {descale_q, ds_bytes}, {descale_k, ds_bytes},
+                         {descale_v, ds_bytes}}));
+  const float* o_part = static_cast<const float*>(workspace);
+  float* lse_part = p.n_splits > 0 ? reinterpret_cast<float*>(static_cast<char*>(workspace) + p.o_bytes) : nullptr;
+  if (p.n_splits > 0) {
+    if (!load_encoder()) return FA_ERR_CUDA;
+    const cuuint64_t dB = B, dH = H, dQ = Nq, dK = Nk, dd = d, ld = static_cast<cuuint64_t>(fp8_vt_ld(Nk));
+    const cuuint64_t q_dims[4] = {dd, dQ, dH, dB}, q_str[3] = {dd, dQ * dd, dH * dQ * dd};
+    const cuuint64_t k_dims[4] = {dd, dK, dH, dB}, k_str[3] = {dd, dK * dd, dH * dK * dd};
+    const cuuint64_t vt_dims[4] = {dK, dd, dH, dB}, vt_str[3] = {ld, dd * ld, dH * dd * ld};
+    CUtensorMap tq, tk, tvt, top;
+    FA_TRY(make_map_u8(&tq, q8, q_dims, q_str));
+    FA_TRY(make_map_u8(&tk, k8, k_dims, k_str));
+    FA_TRY(make_map_u8(&tvt, vt8, vt_dims, vt_str));
+    FA_TRY(make_map_f32(&top, workspace, 128, Nq, static_cast<long long>(p.n_splits) * B * H));
+    FA_TRY(cuda_status(fa::launch_fwd_fp8_split(tq, tk, tvt, top, descale_q, descale_k, descale_v, lse_part, sq, Nk,
+                                                p.n_splits, p.kt_per_split, fa::next_wait_cfg(), stream),
+                       "FP8 split-KV forward launch"));
+  }
+  return cuda_status(fa::launch_fwd_merge(o_part, lse_part, o, lse, sq, p.n_splits, 128, stream),
+                     "split-KV merge launch");
+}
+
+size_t fa_fwd_fp8_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int d, int num_splits) {
+  if (check_sizes_fp8(B, H, Nq, d) != FA_OK || check_sizes_fp8(B, H, Nk, d) != FA_OK || Nq <= 0 || Nk <= 0) return 0;
+  SplitPlan p;
+  if (split_plan(B, H, Nq, Nk, 128, num_splits, p) != FA_OK || p.n_splits == 0) return 0;
   return p.o_bytes + p.lse_bytes;
 }
 

@@ -64,46 +64,6 @@ struct Fp8Cfg {
 };
 static_assert(Fp8Cfg::kSmemBytes <= 227u * 1024u, "shared memory");
 
-// Instruction descriptor for kind::f8f6f4 with e4m3 A and B (format 0), fp32
-// D, both operands K-major: bits 4-5 D format (1 = f32), 7-9 A format, 10-12
-// B format, 17-22 N >> 3, 24-28 M >> 4.
-__host__ __device__ constexpr uint32_t idesc_e4m3(uint32_t M, uint32_t N) {
-  return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
-}
-
-// D (+)= A * B with A from TMEM (four e4m3 values per 32-bit column, K
-// packed along the columns of each lane) and B from shared memory.
-__device__ __forceinline__ void tc_mma_f8_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred e, p;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc_e4m3(128, 128)), "r"(accumulate)
-      : "memory");
-}
-
-// D (+)= A * B, e4m3 operands from shared memory; converged warp, one elected lane.
-__device__ __forceinline__ void tc_mma_f8_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred e, p;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc_e4m3(128, 128)), "r"(accumulate)
-      : "memory");
-}
-
-// Two fp32 values to e4m3 (round to nearest even, saturating), lo in the low byte.
-__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
-  return e4m3x2(a, b) | (e4m3x2(c, d) << 16);
-}
-
 // One 128 x 128 product: four K = 32 steps, 32 bytes apart inside the
 // 128-byte swizzle rows (descriptor start address is in 16-byte units).
 __device__ __forceinline__ void fp8_issue(uint32_t tmem_d, uint64_t a_desc, uint64_t b_desc, bool acc) {

@@ -620,16 +620,9 @@ __global__ void __launch_bounds__(256) fa_fwd_merge_kernel(const float* __restri
 }
 
 template <int D>
-cudaError_t launch_fwd_splitkv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                 const CUtensorMap& top, const float* o_part, float* lse_part, void* o, float* lse,
-                                 const Shape& s, int Nk, int n_splits, int kt_per_split, const WaitCfg& wc,
-                                 cudaStream_t st) {
-  const int BH = s.B * s.H;
-  if (n_splits > 0) {   // the chunks: the one-query-tile kernel's split mode
-    const cudaError_t e = launch_fwd_onetile_split(tq, tk, tv, top, lse_part, s, Nk, n_splits, kt_per_split, wc, st);
-    if (e != cudaSuccess) return e;
-  }
-  const long long rows = static_cast<long long>(BH) * s.N;
+cudaError_t launch_merge_t(const float* o_part, const float* lse_part, void* o, float* lse, const Shape& s,
+                           int n_splits, cudaStream_t st) {
+  const long long rows = static_cast<long long>(s.B) * s.H * s.N;
   const long long blocks = (rows + 7) / 8;   // 8 warps (rows) per block
   fa_fwd_merge_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
       o_part, lse_part, static_cast<__nv_bfloat16*>(o), lse, rows, n_splits, s.d);
@@ -638,21 +631,24 @@ cudaError_t launch_fwd_splitkv_t(const CUtensorMap& tq, const CUtensorMap& tk, c
 
 }  // namespace
 
+cudaError_t launch_fwd_merge(const float* o_part, const float* lse_part, void* o, float* lse, const Shape& s,
+                             int n_splits, int D, cudaStream_t st) {
+  switch (D) {
+    case 256: return launch_merge_t<256>(o_part, lse_part, o, lse, s, n_splits, st);
+    case 128: return launch_merge_t<128>(o_part, lse_part, o, lse, s, n_splits, st);
+    default: return launch_merge_t<64>(o_part, lse_part, o, lse, s, n_splits, st);
+  }
+}
+
 cudaError_t launch_fwd_splitkv(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                const CUtensorMap& top, const float* o_part, float* lse_part, void* o, float* lse,
                                const Shape& s, int Nk, int n_splits, int kt_per_split, const WaitCfg& wc,
                                cudaStream_t st) {
-  switch (kernel_dim(s.d)) {
-    case 256:
-      return launch_fwd_splitkv_t<256>(tq, tk, tv, top, o_part, lse_part, o, lse, s, Nk, n_splits, kt_per_split, wc,
-                                       st);
-    case 128:
-      return launch_fwd_splitkv_t<128>(tq, tk, tv, top, o_part, lse_part, o, lse, s, Nk, n_splits, kt_per_split, wc,
-                                       st);
-    default:
-      return launch_fwd_splitkv_t<64>(tq, tk, tv, top, o_part, lse_part, o, lse, s, Nk, n_splits, kt_per_split, wc,
-                                      st);
+  if (n_splits > 0) {   // the chunks: the one-query-tile kernel's split mode
+    const cudaError_t e = launch_fwd_onetile_split(tq, tk, tv, top, lse_part, s, Nk, n_splits, kt_per_split, wc, st);
+    if (e != cudaSuccess) return e;
   }
+  return launch_fwd_merge(o_part, lse_part, o, lse, s, n_splits, kernel_dim(s.d), st);
 }
 
 // Issue strategy (measured on GB300): at d = 128 one warp's issue loop (two

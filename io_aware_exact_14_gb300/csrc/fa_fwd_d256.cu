@@ -54,16 +54,21 @@ constexpr uint32_t kSiteFwd256 = 0x400;
 // beside Q.  Each tile's release is one commit on empty[tile % kTileBars],
 // and kTileBars * kHalves >= kSlots, so a release barrier is never reused
 // before the producer has waited on it.
-template <int DK>
+// F8: e4m3 Q, K and V^T (split-KV launches at DK = 128): a tile is one box
+// of 128 rows x 128 bytes, the products are kind::f8f6f4 (K = 32 per MMA),
+// V arrives transposed (d rows x key columns), so both products read K-major
+// operands, and P goes back to TMEM as e4m3, four keys per column.
+template <int DK, bool F8 = false>
 struct F256 {
   static_assert(DK == 64 || DK == 128 || DK == 256, "kernel head width");
+  static_assert(!F8 || DK == 128, "e4m3 tiles are 128 bytes wide");
   static constexpr int kHalves = DK == 256 ? 2 : 1;                // units per tile
-  static constexpr int kUnitBoxes = DK == 64 ? 1 : 2;              // boxes per unit
-  static constexpr int kUnitSteps = 4 * kUnitBoxes;                // 16-column K steps per unit
-  static constexpr uint32_t kBoxBytes = 128u * 128u;       // 128 rows x 64 bf16 (128 B, swizzled)
+  static constexpr int kUnitBoxes = (F8 || DK == 64) ? 1 : 2;      // boxes per unit
+  static constexpr int kUnitSteps = 4 * kUnitBoxes;                // 32-byte K steps per unit
+  static constexpr uint32_t kBoxBytes = 128u * 128u;       // 128 rows x 128 B (swizzled)
   static constexpr uint32_t kUnitBytes = kUnitBoxes * kBoxBytes;
-  static constexpr int kQBoxes = DK / 64;
-  static constexpr int kSlots = DK == 256 ? 5 : (DK == 128 ? 6 : 13);
+  static constexpr int kQBoxes = F8 ? 1 : DK / 64;
+  static constexpr int kSlots = DK == 256 ? 5 : ((DK == 128 && !F8) ? 6 : 13);
   static constexpr int kTileBars = DK == 256 ? 4 : 16;
   static_assert(kTileBars * kHalves >= kSlots, "release barriers outlast the ring");
   static constexpr uint32_t kQOff = 0;                     // Q boxes; O staging at the end
@@ -134,11 +139,11 @@ __device__ __forceinline__ W256 w256_split_work(int n_qt, int n_splits, int kt_p
   return w;
 }
 
-template <int DK>
+template <int DK, bool F8>
 __device__ void f256_producer(const W256& w, uint8_t* smem, uint64_t* full, uint64_t* empty, uint64_t* q_full,
                               const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
                               const CtaGuard& g) {
-  using C = F256<DK>;
+  using C = F256<DK, F8>;
   mbar_arrive_expect_tx(q_full, C::kQBoxes * C::kBoxBytes);
 #pragma unroll
   for (int b = 0; b < C::kQBoxes; ++b)
@@ -156,9 +161,14 @@ __device__ void f256_producer(const W256& w, uint8_t* smem, uint64_t* full, uint
     stream_tile(t, w.n, is_v, j);
     uint8_t* dst = smem + C::kSlotOff + slot * C::kUnitBytes;
     mbar_arrive_expect_tx(&full[slot], C::kUnitBytes);
+    if (F8 && is_v) {   // V^T: d rows x keys
+      tma_load_hd(dst, tmV, &full[slot], 128 * (w.kt0 + j), 0, w.hc);
+    } else {
 #pragma unroll
-    for (int b = 0; b < C::kUnitBoxes; ++b)
-      tma_load_hd(dst + b * C::kBoxBytes, is_v ? tmV : tmK, &full[slot], 128 * h + 64 * b, 128 * (w.kt0 + j), w.hc);
+      for (int b = 0; b < C::kUnitBoxes; ++b)
+        tma_load_hd(dst + b * C::kBoxBytes, is_v ? tmV : tmK, &full[slot], 128 * h + 64 * b, 128 * (w.kt0 + j),
+                    w.hc);
+    }
     issued = u + 1;
   }
   if (issued < units) {   // unwinding: let the copies in flight land before shared memory is released
@@ -178,11 +188,11 @@ __device__ __forceinline__ uint64_t kstep_off(int kk) {
 // is idesc_pvl wide (N = ceil(d / 16) * 16 - 128 (kHalves - 1)).  FD
 // (d = DK): compile-time steps and widths; otherwise the steps are
 // predicated.
-template <int DK, bool FD>
+template <int DK, bool FD, bool F8>
 __device__ void f256_mma(const W256& w, uint32_t tmem, uint32_t sbase, uint64_t* full, uint64_t* empty,
                          uint64_t* q_full, uint64_t* s_full, uint64_t* p_full, uint64_t* o_ready, int ks,
                          uint32_t idesc_pvl, const CtaGuard& g) {
-  using C = F256<DK>;
+  using C = F256<DK, F8>;
   constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
   constexpr uint32_t idesc_pv = idesc_bf16(128, 64 * C::kUnitBoxes, false, true);
   const uint64_t qd0 = sdesc_sw128(sbase + C::kQOff, 16, 1024);
@@ -200,7 +210,9 @@ __device__ void f256_mma(const W256& w, uint32_t tmem, uint32_t sbase, uint64_t*
       const uint64_t k = kd0 + slot_off(C::kHalves * t + h);
 #pragma unroll
       for (int kk = 0; kk < C::kUnitSteps; ++kk)
-        if constexpr (FD)
+        if constexpr (F8)   // e4m3: 32 bytes = 32 columns per step; columns past d are zero
+          tc_mma_f8_ss_w(ts, q + kstep_off(kk), k + kstep_off(kk), kk ? 1u : 0u);
+        else if constexpr (FD)
           tc_mma_ss_w(ts, q + kstep_off(kk), k + kstep_off(kk), idesc_s, (h | kk) ? 1u : 0u);
         else
           tc_mma_ss_w_if(ts, q + kstep_off(kk), k + kstep_off(kk), idesc_s, (h | kk) ? 1u : 0u,
@@ -220,14 +232,21 @@ __device__ void f256_mma(const W256& w, uint32_t tmem, uint32_t sbase, uint64_t*
     if (!mbar_wait_w(p_full, j & 1, g, kSiteFwd256 | 4u)) return;
     tc_fence_after();
     const uint32_t tp = tmem + 128u * buf;
+    if constexpr (F8) {   // 128 keys, 32 per MMA; P packs 4 keys per TMEM column; V^T K-major
+      const uint64_t vt = kd0 + slot_off(t);
 #pragma unroll
-    for (int h = 0; h < C::kHalves; ++h) {
-      const uint64_t v = vd0 + slot_off(C::kHalves * t + h);
-      const uint32_t idesc = (h == C::kHalves - 1 && !FD) ? idesc_pvl : idesc_pv;
+      for (int kk = 0; kk < 4; ++kk)
+        tc_mma_f8_ts_w(tmem + C::kColO, tp + kk * 8, vt + kstep_off(kk), (j > 0 || kk > 0) ? 1u : 0u);
+    } else {
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)   // 128 keys, 16 per MMA; P packs 2 keys per TMEM column
-        tc_mma_ts_w(tmem + C::kColO + 128u * h, tp + kk * 8, v + ((kk * 2048) >> 4), idesc,
-                    (j > 0 || kk > 0) ? 1u : 0u);
+      for (int h = 0; h < C::kHalves; ++h) {
+        const uint64_t v = vd0 + slot_off(C::kHalves * t + h);
+        const uint32_t idesc = (h == C::kHalves - 1 && !FD) ? idesc_pvl : idesc_pv;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)   // 128 keys, 16 per MMA; P packs 2 keys per TMEM column
+          tc_mma_ts_w(tmem + C::kColO + 128u * h, tp + kk * 8, v + ((kk * 2048) >> 4), idesc,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+      }
     }
     tc_commit_w(o_ready);
     tc_commit_w(&empty[t % C::kTileBars]);
@@ -241,12 +260,12 @@ __device__ void f256_mma(const W256& w, uint32_t tmem, uint32_t sbase, uint64_t*
 // SPLIT: O goes out in fp32 through the partial-output map (z = split * BH +
 // bh) and the LSE to lse[(split * BH + bh) * N + row].  N is the query
 // length, Nk the key length.
-template <int DK, bool CAUSAL, bool SPLIT, bool DROPOUT>
+template <int DK, bool CAUSAL, bool SPLIT, bool DROPOUT, bool F8>
 __device__ void f256_softmax(const W256& w, uint32_t tmem, uint8_t* smem, uint64_t* s_full, uint64_t* p_full,
                              uint64_t* o_ready, uint64_t* staged, const CUtensorMap* tmO, float* __restrict__ lse,
                              int N, int Nk, int BH, int d, float scale_log2, const DropArgs& drop,
-                             const CtaGuard& g) {
-  using C = F256<DK>;
+                             float out_mult, const CtaGuard& g) {
+  using C = F256<DK, F8>;
   const int r = threadIdx.x & 127;
   const int row = w.qt * 128 + r;
   const uint32_t lane_base = static_cast<uint32_t>((threadIdx.x >> 5) & 3) * 32u << 16;
@@ -316,22 +335,40 @@ __device__ void f256_softmax(const W256& w, uint32_t tmem, uint8_t* smem, uint64
     float2 sum[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) sum[i] = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {  // keys [64h, 64h+64) -> P columns [32h, 32h+32)
+    if constexpr (F8) {   // P~ as e4m3, four keys per column, into the first 32 columns of S
       uint32_t pk[32];
 #pragma unroll
-      for (int c = 64 * h; c < 64 * h + 64; c += 2) {
-        const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[c / 32][c % 32]),
-                                                __uint_as_float(s[(c + 1) / 32][(c + 1) % 32])),
-                                    sc2, mo2);
-        const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-        sum[(c / 2) % 4] = __fadd2_rn(sum[(c / 2) % 4], pp);
-        if constexpr (DROPOUT)   // P o M (0/1); the 1/(1-p) scale goes into the epilogue
-          pk[(c / 2) % 32] = pack_bf16x2(pp.x, pp.y) & keep_mask_pair(unpack_keep4(kp[c / 16], (c / 4) % 4), c % 4);
-        else
-          pk[(c / 2) % 32] = pack_bf16x2(pp.x, pp.y);
+      for (int c = 0; c < 128; c += 4) {
+        const float2 x0 = __ffma2_rn(make_float2(__uint_as_float(s[c / 32][c % 32]),
+                                                 __uint_as_float(s[(c + 1) / 32][(c + 1) % 32])),
+                                     sc2, mo2);
+        const float2 x1 = __ffma2_rn(make_float2(__uint_as_float(s[(c + 2) / 32][(c + 2) % 32]),
+                                                 __uint_as_float(s[(c + 3) / 32][(c + 3) % 32])),
+                                     sc2, mo2);
+        const float2 p0 = make_float2(ex2_approx(x0.x), ex2_approx(x0.y));
+        const float2 p1 = make_float2(ex2_approx(x1.x), ex2_approx(x1.y));
+        sum[(c / 4) % 4] = __fadd2_rn(sum[(c / 4) % 4], __fadd2_rn(p0, p1));
+        pk[c / 4] = e4m3x4(p0.x, p0.y, p1.x, p1.y);
       }
-      tmem_st32(tS + 32 * h, pk);
+      tmem_st32(tS, pk);
+    } else {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {  // keys [64h, 64h+64) -> P columns [32h, 32h+32)
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 64 * h; c < 64 * h + 64; c += 2) {
+          const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[c / 32][c % 32]),
+                                                  __uint_as_float(s[(c + 1) / 32][(c + 1) % 32])),
+                                      sc2, mo2);
+          const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+          sum[(c / 2) % 4] = __fadd2_rn(sum[(c / 2) % 4], pp);
+          if constexpr (DROPOUT)   // P o M (0/1); the 1/(1-p) scale goes into the epilogue
+            pk[(c / 2) % 32] = pack_bf16x2(pp.x, pp.y) & keep_mask_pair(unpack_keep4(kp[c / 16], (c / 4) % 4), c % 4);
+          else
+            pk[(c / 2) % 32] = pack_bf16x2(pp.x, pp.y);
+        }
+        tmem_st32(tS + 32 * h, pk);
+      }
     }
     const float2 s01 = __fadd2_rn(sum[0], sum[1]), s23 = __fadd2_rn(sum[2], sum[3]);
     const float2 s0123 = __fadd2_rn(s01, s23);
@@ -363,7 +400,7 @@ __device__ void f256_softmax(const W256& w, uint32_t tmem, uint8_t* smem, uint64
   if (!mbar_wait(o_ready, (w.n - 1) & 1, g, kSiteFwd256 | 7u)) return;
   __syncwarp();
   tc_fence_after();
-  const float inv_l = l > 0.f ? (DROPOUT ? drop.scale : 1.f) / l : 0.f;
+  const float inv_l = l > 0.f ? out_mult / l : 0.f;
   const uint32_t stage = smem_u32(smem + C::kQOff);
   if constexpr (SPLIT) {
     // fp32 staging: DK / 32 boxes of 128 rows x 32 floats (128-byte rows,
@@ -425,17 +462,21 @@ __device__ void f256_softmax(const W256& w, uint32_t tmem, uint8_t* smem, uint64
 // SPLIT: a split-KV launch (non-causal, no dropout): n_kt key tiles in
 // n_splits chunks of kt_per_split; tmO is then the fp32 partial-output map
 // and lse the partial LSE.  N is the query length and Nk the key length
-// (equal outside split-KV launches).
-template <int DK, bool CAUSAL, bool FD, bool DROPOUT, bool SPLIT>
+// (equal outside split-KV launches).  F8: e4m3 inputs (tmV maps V^T) with
+// per-(b, h) descales dsq, dsk, dsv (unused otherwise): S carries dsq dsk,
+// O is multiplied by dsv.
+template <int DK, bool CAUSAL, bool FD, bool DROPOUT, bool SPLIT, bool F8 = false>
 __global__ void __launch_bounds__(192, 1)
     fa_fwd_d256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                        float* __restrict__ lse, int N, int Nk, int d, int n_qt, int BH, int H, int band,
                        float scale_log2, int ks, uint32_t idesc_pvl, int n_kt, int n_splits, int kt_per_split,
+                       const float* __restrict__ dsq, const float* __restrict__ dsk, const float* __restrict__ dsv,
                        const __grid_constant__ DropArgs drop, const WaitCfg wc) {
   static_assert(!SPLIT || (!CAUSAL && !DROPOUT), "split-KV launches are non-causal without dropout");
   static_assert(SPLIT || DK == 256, "below d = 256 only split-KV launches run this kernel");
-  using C = F256<DK>;
+  static_assert(!F8 || SPLIT, "the e4m3 variant serves split-KV launches");
+  using C = F256<DK, F8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
@@ -482,9 +523,9 @@ __global__ void __launch_bounds__(192, 1)
   const CtaGuard g{abort_flag, g_status_fwd256, wc.epoch, wc.limit_us};
 
   if (warp == 4) {
-    if (lane == 0) f256_producer<DK>(w, smem, full, empty, q_full, &tmQ, &tmK, &tmV, g);
+    if (lane == 0) f256_producer<DK, F8>(w, smem, full, empty, q_full, &tmQ, &tmK, &tmV, g);
   } else if (warp == 5) {
-    f256_mma<DK, FD>(w, tmem, smem_u32(smem), full, empty, q_full, s_full, p_full, o_ready, ks, idesc_pvl, g);
+    f256_mma<DK, FD, F8>(w, tmem, smem_u32(smem), full, empty, q_full, s_full, p_full, o_ready, ks, idesc_pvl, g);
     tc_commit_w(drain);   // every MMA issued above has finished before TMEM is released
     mbar_drain(drain, 0);
     __syncwarp();
@@ -493,8 +534,13 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   } else {
-    f256_softmax<DK, CAUSAL, SPLIT, DROPOUT>(w, tmem, smem, s_full, p_full, o_ready, staged, &tmO, lse, N, Nk, BH, d,
-                                         scale_log2, drop, g);
+    float sl = scale_log2, out_mult = DROPOUT ? drop.scale : 1.f;
+    if constexpr (F8) {
+      sl *= dsq[w.bh] * dsk[w.bh];
+      out_mult = dsv[w.bh];
+    }
+    f256_softmax<DK, CAUSAL, SPLIT, DROPOUT, F8>(w, tmem, smem, s_full, p_full, o_ready, staged, &tmO, lse, N, Nk,
+                                                 BH, d, sl, drop, out_mult, g);
     __syncwarp();
     tc_fence_before();
     named_bar_sync(1, 160);
@@ -515,7 +561,7 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, to, lse, s.N, s.N, s.d, n_qt, s.B * s.H, s.H,
                                                  head_band(s.N, s.d), scale_log2, score_ksteps(s.d),
                                                  idesc_bf16(128, out_cols(s.d) - 128, false, true), n_qt, 1, n_qt,
-                                                 drop, wc);
+                                                 nullptr, nullptr, nullptr, drop, wc);
   return cudaGetLastError();
 }
 
@@ -546,7 +592,8 @@ cudaError_t launch_split_t(const CUtensorMap& tq, const CUtensorMap& tk, const C
   kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, top, lse_part, s.N, Nk, s.d, n_qt, s.B * s.H, s.H, 1,
                                                  scale_log2, score_ksteps(s.d),
                                                  idesc_bf16(128, out_cols(s.d) - 128 * (C::kHalves - 1), false, true),
-                                                 n_kt, n_splits, kt_per_split, no_drop_args(), wc);
+                                                 n_kt, n_splits, kt_per_split, nullptr, nullptr, nullptr,
+                                                 no_drop_args(), wc);
   return cudaGetLastError();
 }
 
@@ -558,6 +605,23 @@ cudaError_t launch_fwd_onetile_split(const CUtensorMap& tq, const CUtensorMap& t
     case 128: return launch_split_t<128>(tq, tk, tv, top, lse_part, s, Nk, n_splits, kt_per_split, wc, st);
     default: return launch_split_t<64>(tq, tk, tv, top, lse_part, s, Nk, n_splits, kt_per_split, wc, st);
   }
+}
+
+cudaError_t launch_fwd_fp8_split(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,
+                                 const CUtensorMap& top, const float* dsq, const float* dsk, const float* dsv,
+                                 float* lse_part, const Shape& s, int Nk, int n_splits, int kt_per_split,
+                                 const WaitCfg& wc, cudaStream_t st) {
+  using C = F256<128, true>;
+  auto kern = fa_fwd_d256_kernel<128, false, true, false, true, true>;
+  const cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), C::kSmemBytes, C::kThreads, 0);
+  if (e != cudaSuccess) return e;
+  const int n_qt = (s.N + 127) / 128, n_kt = (Nk + 127) / 128;
+  const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
+  const dim3 grid(static_cast<unsigned>(s.B) * s.H * n_splits * n_qt);
+  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tvt, top, lse_part, s.N, Nk, s.d, n_qt, s.B * s.H, s.H, 1,
+                                                 scale_log2, 8, 0u, n_kt, n_splits, kt_per_split, dsq, dsk, dsv,
+                                                 no_drop_args(), wc);
+  return cudaGetLastError();
 }
 
 cudaError_t fwd_d256_status(uint32_t* out, bool reset) {

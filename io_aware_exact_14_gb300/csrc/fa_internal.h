@@ -138,6 +138,21 @@ cudaError_t launch_fwd_onetile_split(const CUtensorMap& tq, const CUtensorMap& t
                                      const CUtensorMap& top, float* lse_part, const Shape& s, int Nk, int n_splits,
                                      int kt_per_split, const WaitCfg& wc, cudaStream_t st);
 
+// FP8 split-KV chunks: the one-query-tile kernel's e4m3 variant (d <= 128,
+// kernel width 128) on e4m3 Q, K (maps {d, Nq or Nk, H, B}, 128 x 128-byte
+// boxes) and V^T (map {Nk, d, H, B}, row pitch fp8 ldv), descales per (b, h);
+// partial outputs as launch_fwd_onetile_split at width 128.
+cudaError_t launch_fwd_fp8_split(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,
+                                 const CUtensorMap& top, const float* dsq, const float* dsk, const float* dsv,
+                                 float* lse_part, const Shape& s, int Nk, int n_splits, int kt_per_split,
+                                 const WaitCfg& wc, cudaStream_t st);
+
+// The split-KV merge (fa_fwd.cu): n_splits chunks' fp32 partial outputs
+// (rows D wide) and LSE -> o (bf16 [B, H, Nq, d]) and lse; n_splits == 0
+// writes O = 0, LSE = -inf.
+cudaError_t launch_fwd_merge(const float* o_part, const float* lse_part, void* o, float* lse, const Shape& s,
+                             int n_splits, int D, cudaStream_t st);
+
 // Split-KV chunking: `want` splits (<= 0: chosen from the SM count) of the
 // ceil(Nk/128) key tiles into chunks of kt_per_split whole tiles; n_splits is
 // the number of non-empty chunks (0 when Nk == 0).

@@ -558,6 +558,46 @@ __device__ __forceinline__ uint32_t keep_mask_one(uint32_t ge, int b) {
   return m;
 }
 
+// Instruction descriptor for kind::f8f6f4 with e4m3 A and B (format 0), fp32
+// D, both operands K-major: bits 4-5 D format (1 = f32), 7-9 A format, 10-12
+// B format, 17-22 N >> 3, 24-28 M >> 4.
+__host__ __device__ constexpr uint32_t idesc_e4m3(uint32_t M, uint32_t N) {
+  return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// D (+)= A * B with A from TMEM (four e4m3 values per 32-bit column, K
+// packed along the columns of each lane) and B from shared memory.
+__device__ __forceinline__ void tc_mma_f8_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc_e4m3(128, 128)), "r"(accumulate)
+      : "memory");
+}
+
+// D (+)= A * B, e4m3 operands from shared memory; converged warp, one elected lane.
+__device__ __forceinline__ void tc_mma_f8_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc_e4m3(128, 128)), "r"(accumulate)
+      : "memory");
+}
+
+// Two fp32 values to e4m3 (round to nearest even, saturating), lo in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+  return e4m3x2(a, b) | (e4m3x2(c, d) << 16);
+}
+
 // (M o dP) for columns c, c + 1 of keep words ge: dP where kept, else 0.
 __device__ __forceinline__ float2 keep_pair_f(float2 v, const uint32_t* ge, int c) {
   return make_float2(__uint_as_float(__float_as_uint(v.x) & keep_mask_one(ge[c / 4], c % 4)),

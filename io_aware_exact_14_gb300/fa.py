@@ -43,6 +43,8 @@ SIGNATURES = {
     "fa_fp8_quantize": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_ulonglong, _P]),
     "fa_fp8_vt_ld": (_SZ, [_I]),
     "fa_fwd_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
+    "fa_fwd_fp8_splitkv": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
+    "fa_fwd_fp8_splitkv_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "fa_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
     "fa_bwd_preprocess": (_I, [_P, _P, _P, _I, _I, _I, _I, _P]),
     "fa_bwd_dkdv": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
@@ -382,6 +384,42 @@ def fa_fwd_fp8(q8, k8, vt8, descale_q, descale_k, descale_v, scale: Optional[flo
                            descale_v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, N, d, scale,
                            int(bool(causal)), _stream_ptr(stream))
     _check("fa_fwd_fp8", st)
+    return out, lse
+
+
+def fa_fwd_fp8_splitkv_workspace_bytes(B: int, H: int, Nq: int, Nk: int, d: int, num_splits: int = 0) -> int:
+    return int(load().fa_fwd_fp8_splitkv_workspace_bytes(B, H, Nq, Nk, d, int(num_splits)))
+
+
+def fa_fwd_fp8_splitkv(q8, k8, vt8, descale_q, descale_k, descale_v, scale: Optional[float] = None,
+                       num_splits: int = 0, out=None, lse=None, workspace=None, stream=None):
+    """Non-causal split-KV forward on e4m3 codes (uint8): q8 [B, H, Nq, d], k8 [B, H, Nk, d],
+    vt8 [B, H, d, fa_fp8_vt_ld(Nk)], descales fp32 [B, H]; returns bf16 O [B, H, Nq, d] and
+    fp32 LSE [B, H, Nq]."""
+    for t, n in ((q8, "q8"), (k8, "k8"), (vt8, "vt8")):
+        if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.uint8 and t.is_contiguous()
+                and t.dim() == 4):
+            raise ValueError(f"{n} must be a contiguous 4-D uint8 CUDA tensor")
+    B, H, Nq, d = q8.shape
+    Nk = k8.shape[2]
+    if tuple(k8.shape) != (B, H, Nk, d) or tuple(vt8.shape) != (B, H, d, fa_fp8_vt_ld(Nk)):
+        raise ValueError("k8 must be [B, H, Nk, d] and vt8 [B, H, d, fa_fp8_vt_ld(Nk)]")
+    for t, n in ((descale_q, "descale_q"), (descale_k, "descale_k"), (descale_v, "descale_v")):
+        if not (t.is_cuda and t.dtype == torch.float32 and t.is_contiguous() and tuple(t.shape) == (B, H)):
+            raise ValueError(f"{n} must be a contiguous fp32 CUDA tensor [B, H]")
+    scale = default_scale(d) if scale is None else float(scale)
+    out = torch.empty((B, H, Nq, d), dtype=torch.bfloat16, device=q8.device) if out is None else out
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q8.device) if lse is None else lse
+    _same((B, H, Nq, d), out, "out")
+    _vec(lse, (B, H, Nq, d), "lse")
+    need = fa_fwd_fp8_splitkv_workspace_bytes(B, H, Nq, Nk, d, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q8.device)
+    st = load().fa_fwd_fp8_splitkv(q8.data_ptr(), k8.data_ptr(), vt8.data_ptr(), descale_q.data_ptr(),
+                                   descale_k.data_ptr(), descale_v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                   B, H, Nq, Nk, d, scale, int(num_splits), workspace.data_ptr(),
+                                   workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    _check("fa_fwd_fp8_splitkv", st)
     return out, lse
 
 

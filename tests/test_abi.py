@@ -208,3 +208,25 @@ def test_splitkv_workspace_sizes(lib):
     assert lib.fa_fwd_splitkv_workspace_bytes(1, 1, 0, 100, 128, 4) == 0   # no queries
     assert lib.fa_fwd_splitkv_workspace_bytes(1, 1, 1, 100, 100, 4) == 0   # d not a multiple of 8
     assert lib.fa_fwd_splitkv_workspace_bytes(1, 1, 1, 100, 264, 4) == 0   # above the widest head
+
+
+def test_fp8_splitkv_workspace_sizes_and_argument_checks(lib):
+    """The e4m3 split path's partial rows are 128 floats wide at every d; its
+    sizes follow the FP8 rule (d a multiple of 16 up to 128); argument errors
+    come back before any device access."""
+    for B, H, Nq, Nk, d, s in [(1, 1, 1, 1000, 128, 3), (2, 3, 5, 4097, 64, 7), (1, 2, 16, 129, 96, 4)]:
+        n_kt = (Nk + 127) // 128
+        per = -(-n_kt // min(s, n_kt))
+        rows = B * H * Nq * -(-n_kt // per)
+        r256 = lambda x: (x + 255) // 256 * 256
+        assert lib.fa_fwd_fp8_splitkv_workspace_bytes(B, H, Nq, Nk, d, s) == r256(rows * 128 * 4) + r256(rows * 4)
+    assert lib.fa_fwd_fp8_splitkv_workspace_bytes(1, 1, 1, 100, 40, 4) == 0    # d not a multiple of 16
+    assert lib.fa_fwd_fp8_splitkv_workspace_bytes(1, 1, 1, 100, 256, 4) == 0   # above the e4m3 width
+    assert lib.fa_fwd_fp8_splitkv_workspace_bytes(1, 1, 1, 0, 128, 4) == 0
+    p = [FAKE + i * 0x100000 for i in range(9)]
+    call = lambda *a: lib.fa_fwd_fp8_splitkv(*a)
+    assert call(*p[:8], 1, 1, 1, 1000, 40, 0.1, 2, p[8], 1 << 20, None) == 2     # d not a multiple of 16
+    assert call(0, *p[1:8], 1, 1, 1, 1000, 64, 0.1, 2, p[8], 1 << 20, None) == 1  # NULL q8
+    assert call(*p[:6], p[0], p[7], 1, 1, 1, 1000, 64, 0.1, 2, p[8], 1 << 20, None) == 1   # o aliases q8
+    assert call(*p[:8], 1, 1, 1, 1000, 64, 0.1, 2, p[8], 16, None) == 4          # workspace too small
+    assert call(*p[:8], 1, 1, 0, 1000, 64, 0.1, 2, None, 0, None) == 0            # Nq == 0: no-op

@@ -12,6 +12,7 @@ import torch
 import oracle
 from oracle import fp8_ref
 from io_aware_exact_14_gb300 import fa
+from io_aware_exact_14_gb300.workloads import make_splitkv_inputs
 from gpu_util import TOL_LSE, assert_no_timeout, device_inputs, f64
 
 pytestmark = pytest.mark.gpu
@@ -186,3 +187,90 @@ def test_fp8_all_zero_head():
     mean = V[0, 1].mean(axis=0)
     assert np.max(np.abs(f64(o[0, 1]) - mean[None, :]) - 2.0 ** -8 * np.abs(mean[None, :])) <= 1e-4
     assert np.allclose(f64(lse[0, 1]), math.log(N), atol=1e-4)
+
+
+# ---------------------------------------------------------------------------
+# Split-KV on e4m3 codes (decoding against an e4m3 key/value cache)
+# ---------------------------------------------------------------------------
+
+def _quantized_kv(B, H, Nq, Nk, d, seed, rotate=None):
+    x = make_splitkv_inputs(B, H, Nq, Nk, d, seed)
+    g = {k: t.cuda() for k, t in x.items()}
+    q8, dq = fa.fa_fp8_quantize(g["q"], rotate_seed=rotate)
+    k8, dk = fa.fa_fp8_quantize(g["k"], rotate_seed=rotate)
+    vt8, dv = fa.fa_fp8_quantize(g["v"], transpose=True)
+    return (q8, k8, vt8, dq, dk, dv)
+
+
+def _oracle_kv(args, Nk, scale):
+    q8, k8, vt8, dq, dk, dv = args
+    vt = _codes_np(vt8)[..., :Nk]
+    return fp8_ref.attn_fwd_fp8_ref(_codes_np(q8), _codes_np(k8), vt, dq.cpu().numpy(), dk.cpu().numpy(),
+                                    dv.cpu().numpy(), scale, False)
+
+
+def _within_bound(o, lse, O, LSE, bound):
+    excess = np.abs(f64(o) - O) - (1.1 * bound + 2.0 ** -8 * np.abs(O) + 1e-3)
+    assert np.max(excess) <= 0, f"max excess {np.max(excess):.3g}"
+    assert np.max(np.abs(f64(lse) - LSE)) <= TOL_LSE
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,d,splits,rotate", [
+    (1, 2, 1, 3000, 128, 0, None),
+    (2, 2, 200, 3000, 128, 7, 5),       # two query tiles, ragged key tail, rotated Q and K
+    (1, 3, 17, 129, 64, 2, None),       # a one-key last chunk
+    (1, 2, 40, 1500, 96, 1, None),      # one chunk
+    (1, 2, 64, 128, 32, 5, None),       # more splits wanted than key tiles
+    (2, 4, 1, 8192, 128, 0, 11)])
+def test_fp8_splitkv_within_rounding_bound(B, H, Nq, Nk, d, splits, rotate):
+    args = _quantized_kv(B, H, Nq, Nk, d, seed=880 + Nq + Nk + d, rotate=rotate)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = fa.fa_fwd_fp8_splitkv(*args, scale, splits)
+    torch.cuda.synchronize()
+    assert_no_timeout()
+    O, LSE, _, bound = _oracle_kv(args, Nk, scale)
+    _within_bound(o, lse, O, LSE, bound)
+
+
+def test_fp8_splitkv_chunkings_agree_and_match_the_fp8_forward():
+    """Every chunking stays within the bound and reruns are bitwise equal; with
+    Nq == Nk the split path lands next to fa_fwd_fp8 (same e4m3 arithmetic per
+    chunk, fp32 partials, one merge)."""
+    B, H, N, d = 1, 2, 1000, 128
+    args = _quantized_kv(B, H, N, N, d, seed=890)
+    scale = 1.0 / math.sqrt(d)
+    O, LSE, _, bound = _oracle_kv(args, N, scale)
+    for splits in (1, 3, 8, 0):
+        o, lse = fa.fa_fwd_fp8_splitkv(*args, scale, splits)
+        o2, lse2 = fa.fa_fwd_fp8_splitkv(*args, scale, splits)
+        torch.cuda.synchronize()
+        assert_no_timeout()
+        assert torch.equal(o, o2) and torch.equal(lse, lse2)
+        _within_bound(o, lse, O, LSE, bound)
+    o1, lse1 = fa.fa_fwd_fp8_splitkv(*args, scale, 1)
+    op, lsep = fa.fa_fwd_fp8(*args, scale, False)
+    torch.cuda.synchronize()
+    assert np.max(np.abs(f64(o1) - f64(op)) - 2.0 ** -7 * np.abs(f64(op))) <= 1e-3
+    assert np.max(np.abs(f64(lse1) - f64(lsep))) <= 1e-5
+
+
+def test_fp8_splitkv_empty_keys_and_short_workspace():
+    B, H, Nq, d = 2, 2, 9, 64
+    x = make_splitkv_inputs(B, H, Nq, 0, d, 895)
+    q8, dq = fa.fa_fp8_quantize(x["q"].cuda())
+    k8 = torch.empty(B, H, 0, d, dtype=torch.uint8, device="cuda")
+    vt8 = torch.empty(B, H, d, fa.fa_fp8_vt_ld(0), dtype=torch.uint8, device="cuda")
+    one = torch.ones(B, H, device="cuda")
+    o = torch.full((B, H, Nq, d), 7.0, dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros(B, H, Nq, device="cuda")
+    fa.fa_fwd_fp8_splitkv(q8, k8, vt8, dq, one, one, None, 0, out=o, lse=lse)
+    torch.cuda.synchronize()
+    assert_no_timeout()
+    assert torch.all(o == 0) and torch.all(torch.isneginf(lse))
+    args = _quantized_kv(1, 2, 16, 2048, 128, seed=896)
+    need = fa.fa_fwd_fp8_splitkv_workspace_bytes(1, 2, 16, 2048, 128, 4)
+    assert need > 0
+    ws = torch.empty(need - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(fa.FAError) as e:
+        fa.fa_fwd_fp8_splitkv(*args, None, 4, workspace=ws)
+    assert e.value.status == fa.FA_ERR_WORKSPACE

@@ -48,6 +48,15 @@ def _splitkv(B, H, Nq, Nk, d, seed):
     return lambda: fa.fa_fwd_splitkv(gq["q"], gk["k"], gk["v"])
 
 
+def _fp8_splitkv(B, H, Nq, Nk, d, seed):
+    _, gq = device_inputs(B, H, Nq, d, seed=seed)
+    _, gk = device_inputs(B, H, Nk, d, seed=seed + 1)
+    q8, dq = fa.fa_fp8_quantize(gq["q"])
+    k8, dk = fa.fa_fp8_quantize(gk["k"])
+    vt8, dv = fa.fa_fp8_quantize(gk["v"], transpose=True)
+    return lambda: fa.fa_fwd_fp8_splitkv(q8, k8, vt8, dq, dk, dv)
+
+
 def _fp8(B, H, N, d, causal, seed):
     _, g = device_inputs(B, H, N, d, seed=seed)
 
@@ -75,6 +84,7 @@ CASES = {
     "splitkv_d128": lambda: _splitkv(2, 8, 128, 8192, 128, 912),
     "splitkv_d256": lambda: _splitkv(2, 8, 64, 8192, 256, 915),
     "fp8_d128_causal": lambda: _fp8(2, 8, 2048, 128, True, 913),
+    "fp8_splitkv_d128": lambda: _fp8_splitkv(2, 8, 16, 8192, 128, 916),
 }
 
 

@@ -106,10 +106,12 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, f
 
 /*
  * Workspace bytes fa_fwd_splitkv needs for these arguments (the same
- * num_splits rule, on the current device): n_used * B*H*Nq*D fp32 partial
- * outputs (D = 64 for d <= 64, 128 for d <= 128, else 256) plus
- * n_used * B*H*Nq fp32 partial LSE, each rounded up to 256 bytes.  0 for
- * invalid sizes, Nq == 0 or Nk == 0.
+ * num_splits rule, on the current device): R * n_used * B*H*Nq*D fp32
+ * partial outputs (D = 64 for d <= 64, 128 for d <= 128, else 256) plus
+ * R * n_used * B*H*Nq fp32 partial LSE, each rounded up to 256 bytes, with
+ * R = 4 for Nq <= 32 and d <= 64 (each chunk then writes one partial result
+ * per quarter of its keys) and 1 otherwise.  0 for invalid sizes, Nq == 0
+ * or Nk == 0.
  */
 size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int d, int num_splits);
 
@@ -286,10 +288,11 @@ fa_status fa_fwd_fp8_splitkv(const void* q8, const void* k8, const void* vt8, co
                              void* workspace, size_t workspace_bytes, struct CUstream_st* stream);
 
 /*
- * Workspace bytes fa_fwd_fp8_splitkv needs: n_used * B*H*Nq*128 fp32
- * partial outputs plus n_used * B*H*Nq fp32 partial LSE, each rounded up
- * to 256 bytes (n_used as in fa_fwd_splitkv_workspace_bytes).  0 for
- * invalid sizes, Nq == 0 or Nk == 0.
+ * Workspace bytes fa_fwd_fp8_splitkv needs: R * n_used * B*H*Nq*128 fp32
+ * partial outputs plus R * n_used * B*H*Nq fp32 partial LSE, each rounded
+ * up to 256 bytes, with R = 4 for Nq <= 32 (one partial result per quarter
+ * of a chunk's keys) and 1 otherwise, n_used as in
+ * fa_fwd_splitkv_workspace_bytes.  0 for invalid sizes, Nq == 0 or Nk == 0.
  */
 size_t fa_fwd_fp8_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int d, int num_splits);
 

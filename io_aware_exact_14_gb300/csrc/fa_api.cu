@@ -6,6 +6,7 @@
 
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -337,10 +338,10 @@ fa_status cuda_status(cudaError_t e, const char* what) {
 // 3-D view {D, Nq, Z} of fp32 rows (split-KV partial outputs, Z = splits *
 // B*H, D the kernel's padded head dim); boxes of 32 floats (128 bytes) x 128
 // rows, 128-byte swizzle.
-fa_status make_map_f32(CUtensorMap* m, const void* base, int d, int Nq, long long Z) {
+fa_status make_map_f32(CUtensorMap* m, const void* base, int d, int Nq, long long Z, unsigned box_rows = 128) {
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(Nq), static_cast<cuuint64_t>(Z)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(Nq) * d * 4};
-  const cuuint32_t box[3] = {32, 128, 1};
+  const cuuint32_t box[3] = {32, box_rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box,
                               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -360,8 +361,9 @@ fa_status check_sizes_fp8(int B, int H, int N, int d) {
 
 long long fp8_vt_ld(int N) { return (static_cast<long long>(N) + 15) / 16 * 16; }
 
-fa_status make_map_u8(CUtensorMap* m, const void* base, const cuuint64_t (&dims)[4], const cuuint64_t (&strides)[3]) {
-  const cuuint32_t box[4] = {128, 128, 1, 1};
+fa_status make_map_u8(CUtensorMap* m, const void* base, const cuuint64_t (&dims)[4], const cuuint64_t (&strides)[3],
+                      unsigned box_rows = 128) {
+  const cuuint32_t box[4] = {128, box_rows, 1, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
                               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -376,12 +378,13 @@ struct SplitPlan {
   size_t o_bytes, lse_bytes;
 };
 
-// width: the partial rows' floats (the kernel width of d; 128 for e4m3).
-fa_status split_plan(int B, int H, int Nq, int Nk, int width, int want, SplitPlan& p) {
+// width: the partial rows' floats (the kernel width of d; 128 for e4m3);
+// each chunk writes `reps` partial results (fa::splitkv_replicas).
+fa_status split_plan(int B, int H, int Nq, int Nk, int width, int reps, int want, SplitPlan& p) {
   int sms = 0;
   if (want <= 0) FA_TRY(cuda_status(fa::sm_count(&sms), "reading the SM count"));
   fa::splitkv_chunks(B, H, Nq, Nk, want, sms, p.kt_per_split, p.n_splits);
-  const size_t rows = static_cast<size_t>(B) * H * Nq * p.n_splits;
+  const size_t rows = static_cast<size_t>(B) * H * Nq * p.n_splits * reps;
   p.o_bytes = round256(rows * width * 4);
   p.lse_bytes = round256(rows * 4);
   return FA_OK;
@@ -574,8 +577,10 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, f
   if (Nk > 0) FA_TRY(check_ptrs({k, v}, {}));   // never read when there are no keys
   FA_TRY(check_scale(scale));
   SplitPlan p;
-  FA_TRY(split_plan(B, H, Nq, Nk, fa::kernel_dim(d), num_splits, p));
-  if (static_cast<long long>(B) * H * p.n_splits * ((Nq + 127) / 128) > INT32_MAX) return FA_ERR_UNSUPPORTED;
+  const int reps = fa::splitkv_replicas(Nq, d, false);
+  FA_TRY(split_plan(B, H, Nq, Nk, fa::kernel_dim(d), reps, num_splits, p));
+  if (static_cast<long long>(B) * H * p.n_splits * std::max((Nq + 127) / 128, reps) > INT32_MAX)
+    return FA_ERR_UNSUPPORTED;   // the grid, and the partial results' z coordinate
   const size_t need = p.n_splits > 0 ? p.o_bytes + p.lse_bytes : 0;
   if (need > 0 && (workspace == nullptr || !aligned(workspace, 16) || workspace_bytes < need)) return FA_ERR_WORKSPACE;
   const Shape sq{B, H, Nq, d, scale, 0}, sk{B, H, Nk, d, scale, 0};
@@ -583,11 +588,13 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, f
   FA_TRY(check_disjoint({{o, qb}, {lse, vec_bytes(sq)}, {workspace, need}}, {{q, qb}, {k, kb}, {v, kb}}));
   if (!load_encoder()) return FA_ERR_CUDA;
   CUtensorMap tq, tk, tv, top;
-  FA_TRY(make_map(&tq, q, sq));
+  const unsigned rows_box = reps > 1 ? fa::kRepRows : 128;
+  FA_TRY(make_map(&tq, q, sq, fa::contiguous_strides(sq), rows_box));
   if (p.n_splits > 0) {
     FA_TRY(make_map(&tk, k, sk));
     FA_TRY(make_map(&tv, v, sk));
-    FA_TRY(make_map_f32(&top, workspace, fa::kernel_dim(d), Nq, static_cast<long long>(p.n_splits) * B * H));
+    FA_TRY(make_map_f32(&top, workspace, fa::kernel_dim(d), Nq, static_cast<long long>(p.n_splits) * reps * B * H,
+                        rows_box));
   } else {
     tk = tq;
     tv = tq;
@@ -605,7 +612,9 @@ size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int d, int n
       Nq <= 0 || Nk <= 0)
     return 0;
   SplitPlan p;
-  if (split_plan(B, H, Nq, Nk, fa::kernel_dim(d), num_splits, p) != FA_OK || p.n_splits == 0) return 0;
+  if (split_plan(B, H, Nq, Nk, fa::kernel_dim(d), fa::splitkv_replicas(Nq, d, false), num_splits, p) != FA_OK ||
+      p.n_splits == 0)
+    return 0;
   return p.o_bytes + p.lse_bytes;
 }
 
@@ -620,8 +629,10 @@ fa_status fa_fwd_fp8_splitkv(const void* q8, const void* k8, const void* vt8, co
   if (Nk > 0) FA_TRY(check_ptrs({k8, vt8}, {}));   // never read when there are no keys
   FA_TRY(check_scale(scale));
   SplitPlan p;
-  FA_TRY(split_plan(B, H, Nq, Nk, 128, num_splits, p));
-  if (static_cast<long long>(B) * H * p.n_splits * ((Nq + 127) / 128) > INT32_MAX) return FA_ERR_UNSUPPORTED;
+  const int reps = fa::splitkv_replicas(Nq, d, true);
+  FA_TRY(split_plan(B, H, Nq, Nk, 128, reps, num_splits, p));
+  if (static_cast<long long>(B) * H * p.n_splits * std::max((Nq + 127) / 128, reps) > INT32_MAX)
+    return FA_ERR_UNSUPPORTED;   // the grid, and the partial results' z coordinate
   const size_t need = p.n_splits > 0 ? p.o_bytes + p.lse_bytes : 0;
   if (need > 0 && (workspace == nullptr || !aligned(workspace, 16) || workspace_bytes < need)) return FA_ERR_WORKSPACE;
   const Shape sq{B, H, Nq, d, scale, 0};
@@ -639,22 +650,25 @@ fa_status fa_fwd_fp8_splitkv(const void* q8, const void* k8, const void* vt8, co
     const cuuint64_t k_dims[4] = {dd, dK, dH, dB}, k_str[3] = {dd, dK * dd, dH * dK * dd};
     const cuuint64_t vt_dims[4] = {dK, dd, dH, dB}, vt_str[3] = {ld, dd * ld, dH * dd * ld};
     CUtensorMap tq, tk, tvt, top;
-    FA_TRY(make_map_u8(&tq, q8, q_dims, q_str));
+    const unsigned rows_box = reps > 1 ? fa::kRepRows : 128;
+    FA_TRY(make_map_u8(&tq, q8, q_dims, q_str, rows_box));
     FA_TRY(make_map_u8(&tk, k8, k_dims, k_str));
     FA_TRY(make_map_u8(&tvt, vt8, vt_dims, vt_str));
-    FA_TRY(make_map_f32(&top, workspace, 128, Nq, static_cast<long long>(p.n_splits) * B * H));
+    FA_TRY(make_map_f32(&top, workspace, 128, Nq,
+                        static_cast<long long>(p.n_splits) * reps * B * H, rows_box));
     FA_TRY(cuda_status(fa::launch_fwd_fp8_split(tq, tk, tvt, top, descale_q, descale_k, descale_v, lse_part, sq, Nk,
                                                 p.n_splits, p.kt_per_split, fa::next_wait_cfg(), stream),
                        "FP8 split-KV forward launch"));
   }
-  return cuda_status(fa::launch_fwd_merge(o_part, lse_part, o, lse, sq, p.n_splits, 128, stream),
+  return cuda_status(fa::launch_fwd_merge(o_part, lse_part, o, lse, sq, p.n_splits * reps, 128, stream),
                      "split-KV merge launch");
 }
 
 size_t fa_fwd_fp8_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int d, int num_splits) {
   if (check_sizes_fp8(B, H, Nq, d) != FA_OK || check_sizes_fp8(B, H, Nk, d) != FA_OK || Nq <= 0 || Nk <= 0) return 0;
   SplitPlan p;
-  if (split_plan(B, H, Nq, Nk, 128, num_splits, p) != FA_OK || p.n_splits == 0) return 0;
+  if (split_plan(B, H, Nq, Nk, 128, fa::splitkv_replicas(Nq, d, true), num_splits, p) != FA_OK || p.n_splits == 0)
+    return 0;
   return p.o_bytes + p.lse_bytes;
 }
 

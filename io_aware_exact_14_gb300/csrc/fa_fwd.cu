@@ -648,7 +648,7 @@ cudaError_t launch_fwd_splitkv(const CUtensorMap& tq, const CUtensorMap& tk, con
     const cudaError_t e = launch_fwd_onetile_split(tq, tk, tv, top, lse_part, s, Nk, n_splits, kt_per_split, wc, st);
     if (e != cudaSuccess) return e;
   }
-  return launch_fwd_merge(o_part, lse_part, o, lse, s, n_splits, kernel_dim(s.d), st);
+  return launch_fwd_merge(o_part, lse_part, o, lse, s, n_splits * splitkv_replicas(s.N, s.d, false), kernel_dim(s.d), st);
 }
 
 // Issue strategy (measured on GB300): at d = 128 one warp's issue loop (two

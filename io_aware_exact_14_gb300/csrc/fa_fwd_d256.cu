@@ -139,15 +139,22 @@ __device__ __forceinline__ W256 w256_split_work(int n_qt, int n_splits, int kt_p
   return w;
 }
 
-template <int DK, bool F8>
+template <int DK, bool F8, bool REP>
 __device__ void f256_producer(const W256& w, uint8_t* smem, uint64_t* full, uint64_t* empty, uint64_t* q_full,
                               const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
                               const CtaGuard& g) {
   using C = F256<DK, F8>;
   mbar_arrive_expect_tx(q_full, C::kQBoxes * C::kBoxBytes);
+  if constexpr (REP) {   // rows 0-31 (a 32-row box map) into each 32-row quarter of the tile
 #pragma unroll
-  for (int b = 0; b < C::kQBoxes; ++b)
-    tma_load_hd(smem + C::kQOff + b * C::kBoxBytes, tmQ, q_full, 64 * b, 128 * w.qt, w.hc);
+    for (int b = 0; b < C::kQBoxes; ++b)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) tma_load_hd(smem + C::kQOff + b * C::kBoxBytes + q * 4096u, tmQ, q_full, 64 * b, 0, w.hc);
+  } else {
+#pragma unroll
+    for (int b = 0; b < C::kQBoxes; ++b)
+      tma_load_hd(smem + C::kQOff + b * C::kBoxBytes, tmQ, q_full, 64 * b, 128 * w.qt, w.hc);
+  }
   const int units = 2 * C::kHalves * w.n;
   int issued = 0;
   for (int u = 0; u < units; ++u) {
@@ -459,13 +466,157 @@ __device__ void f256_softmax(const W256& w, uint32_t tmem, uint8_t* smem, uint64
   }
 }
 
+// Split-KV with at most 32 query rows (REP): the producer loads Q's rows
+// 0-31 into all four 32-row quarters of the tile, and softmax warp q works on
+// keys [32q, 32q + 32) of every key tile for those rows, with P = 0 for the
+// other keys: four independent chunks of each key tile's softmax, a quarter
+// of the exponentials and registers per row each.  O row 32q + i then holds
+// query row i over warp q's keys; each quarter is stored as its own partial
+// result (z = (4 split + q) BH + bh, rows 0-31 through a 32-row box map), so
+// the merge, given 4 n_splits chunks, combines them like any other chunks.
+template <int DK, bool F8>
+__device__ void f256_softmax_rep(const W256& w, uint32_t tmem, uint8_t* smem, uint64_t* s_full, uint64_t* p_full,
+                                 uint64_t* o_ready, uint64_t* staged, const CUtensorMap* tmO,
+                                 float* __restrict__ lse, int N, int Nk, int BH, int d, float scale_log2,
+                                 float out_mult, const CtaGuard& g) {
+  using C = F256<DK, F8>;
+  const int r = threadIdx.x & 127;
+  const int wq = r >> 5;            // this warp's quarter of the keys (and of the TMEM lanes)
+  const int row = r & 31;           // query row (the tile is query tile 0)
+  const uint32_t lane_base = static_cast<uint32_t>(wq) * 32u << 16;
+  const uint32_t tO = tmem + lane_base + C::kColO;
+  float m_use = -INFINITY;  // reference max, base-2 units
+  float l = 0.f;
+  for (int j = 0; j < w.n; ++j) {
+    const int buf = j & 1;
+    const uint32_t tS = tmem + lane_base + 128u * buf;
+    if (!mbar_wait(&s_full[buf], (j >> 1) & 1, g, kSiteFwd256 | 6u)) return;
+    __syncwarp();
+    tc_fence_after();
+    uint32_t s[32];
+    tmem_ld32(tS + 32 * wq, s);
+    tmem_ld_wait(s);
+    const int lim = Nk - ((w.kt0 + j) * 128 + 32 * wq);   // visible keys of this quarter
+    if (lim < 32) {
+#pragma unroll
+      for (int c = 0; c < 32; ++c)
+        if (c >= lim) s[c] = __float_as_uint(-INFINITY);
+    }
+    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+    for (int c = 0; c < 32; c += 2)
+      mx[(c / 2) % 4] = max3f(mx[(c / 2) % 4], __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
+    const float row_max = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * scale_log2;
+    bool rescale = false;
+    float corr = 1.f;
+    if (j == 0) {
+      m_use = row_max;
+    } else {
+      const bool need = row_max > m_use + kRescaleThreshold;
+      rescale = __any_sync(0xffffffffu, need);
+      if (rescale) {
+        const float m_new = need ? row_max : m_use;
+        corr = (m_use == -INFINITY) ? 0.f : ex2_approx(m_use - m_new);
+        l *= corr;
+        m_use = m_new;
+      }
+    }
+    const float m_off = (m_use == -INFINITY) ? 0.f : m_use;
+    const float2 sc2 = make_float2(scale_log2, scale_log2), mo2 = make_float2(-m_off, -m_off);
+    float2 sum[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    float p[32];
+#pragma unroll
+    for (int c = 0; c < 32; c += 2) {
+      const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sc2, mo2);
+      p[c] = ex2_approx(x.x);
+      p[c + 1] = ex2_approx(x.y);
+      sum[(c / 2) % 2] = __fadd2_rn(sum[(c / 2) % 2], make_float2(p[c], p[c + 1]));
+    }
+    uint32_t pk[32];
+    if constexpr (F8) {   // e4m3, four keys per column: this quarter is columns [8 wq, 8 wq + 8)
+#pragma unroll
+      for (int i = 0; i < 32; ++i) pk[i] = 0u;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (q == wq) pk[8 * q + i] = e4m3x4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+      tmem_st32(tS, pk);
+    } else {              // bf16 pairs: this quarter is columns [16 wq, 16 wq + 16) of the 64
+#pragma unroll
+      for (int i = 0; i < 32; ++i) pk[i] = (i / 16 == (wq & 1)) ? pack_bf16x2(p[2 * (i % 16)], p[2 * (i % 16) + 1]) : 0u;
+      tmem_st32(tS + 32 * (wq >> 1), pk);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) pk[i] = 0u;
+      tmem_st32(tS + 32 * (1 - (wq >> 1)), pk);
+    }
+    const float2 s01 = __fadd2_rn(sum[0], sum[1]);
+    l += s01.x + s01.y;
+    if (j > 0) {
+      // O may be touched only once the previous P V product has completed
+      if (!mbar_wait(o_ready, (j - 1) & 1, g, kSiteFwd256 | 5u)) return;
+      __syncwarp();
+      tc_fence_after();
+      if (rescale) {
+#pragma unroll 1
+        for (int c = 0; c < DK; c += 32) {
+          uint32_t o[32];
+          tmem_ld32(tO + c, o);
+          tmem_ld_wait(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
+          tmem_st32(tO + c, o);
+        }
+      }
+    }
+    tmem_st_wait();
+    tc_fence_before();
+    mbar_arrive(p_full);
+  }
+
+  // epilogue: fp32 staging of the whole tile (as the split epilogue), then
+  // each quarter's 32 rows to its own partial result
+  if (!mbar_wait(o_ready, (w.n - 1) & 1, g, kSiteFwd256 | 7u)) return;
+  __syncwarp();
+  tc_fence_after();
+  const float inv_l = l > 0.f ? out_mult / l : 0.f;
+  const uint32_t stage = smem_u32(smem + C::kQOff);
+#pragma unroll 1
+  for (int c = 0; c < DK; c += 32) {
+    if (c >= d) break;   // the columns past d are not stored
+    uint32_t o[32];
+    tmem_ld32(tO + c, o);
+    tmem_ld_wait(o);
+    const uint32_t box = stage + (c / 32) * 16384u + r * 128;
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      st_shared_v4(box + ((q ^ (r & 7)) << 4), __float_as_uint(__uint_as_float(o[4 * q]) * inv_l),
+                   __float_as_uint(__uint_as_float(o[4 * q + 1]) * inv_l),
+                   __float_as_uint(__uint_as_float(o[4 * q + 2]) * inv_l),
+                   __float_as_uint(__uint_as_float(o[4 * q + 3]) * inv_l));
+  }
+  fence_proxy_async_smem();
+  mbar_arrive(staged);
+  if (r == 0 && mbar_wait(staged, 0, g, kSiteFwd256 | 8u)) {
+    for (int b = 0; b < DK / 32; ++b)
+      if (32 * b < d)
+        for (int q = 0; q < 4; ++q)
+          tma_store_3d(tmO, smem + C::kQOff + b * 16384u + q * 4096u, 32 * b, 0, (4 * w.split + q) * BH + w.bh);
+    tma_store_commit();
+    tma_store_wait_read_all();
+  }
+  if (row < N)
+    lse[static_cast<size_t>((4 * w.split + wq) * BH + w.bh) * N + row] =
+        l > 0.f ? (m_use + __log2f(l)) * kLn2 : -INFINITY;
+}
+
 // SPLIT: a split-KV launch (non-causal, no dropout): n_kt key tiles in
 // n_splits chunks of kt_per_split; tmO is then the fp32 partial-output map
 // and lse the partial LSE.  N is the query length and Nk the key length
 // (equal outside split-KV launches).  F8: e4m3 inputs (tmV maps V^T) with
 // per-(b, h) descales dsq, dsk, dsv (unused otherwise): S carries dsq dsk,
 // O is multiplied by dsv.
-template <int DK, bool CAUSAL, bool FD, bool DROPOUT, bool SPLIT, bool F8 = false>
+template <int DK, bool CAUSAL, bool FD, bool DROPOUT, bool SPLIT, bool F8 = false, bool REP = false>
 __global__ void __launch_bounds__(192, 1)
     fa_fwd_d256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -476,6 +627,7 @@ __global__ void __launch_bounds__(192, 1)
   static_assert(!SPLIT || (!CAUSAL && !DROPOUT), "split-KV launches are non-causal without dropout");
   static_assert(SPLIT || DK == 256, "below d = 256 only split-KV launches run this kernel");
   static_assert(!F8 || SPLIT, "the e4m3 variant serves split-KV launches");
+  static_assert(!REP || SPLIT, "row replication serves split-KV launches");
   using C = F256<DK, F8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -523,7 +675,7 @@ __global__ void __launch_bounds__(192, 1)
   const CtaGuard g{abort_flag, g_status_fwd256, wc.epoch, wc.limit_us};
 
   if (warp == 4) {
-    if (lane == 0) f256_producer<DK, F8>(w, smem, full, empty, q_full, &tmQ, &tmK, &tmV, g);
+    if (lane == 0) f256_producer<DK, F8, REP>(w, smem, full, empty, q_full, &tmQ, &tmK, &tmV, g);
   } else if (warp == 5) {
     f256_mma<DK, FD, F8>(w, tmem, smem_u32(smem), full, empty, q_full, s_full, p_full, o_ready, ks, idesc_pvl, g);
     tc_commit_w(drain);   // every MMA issued above has finished before TMEM is released
@@ -539,8 +691,12 @@ __global__ void __launch_bounds__(192, 1)
       sl *= dsq[w.bh] * dsk[w.bh];
       out_mult = dsv[w.bh];
     }
-    f256_softmax<DK, CAUSAL, SPLIT, DROPOUT, F8>(w, tmem, smem, s_full, p_full, o_ready, staged, &tmO, lse, N, Nk,
-                                                 BH, d, sl, drop, out_mult, g);
+    if constexpr (REP)
+      f256_softmax_rep<DK, F8>(w, tmem, smem, s_full, p_full, o_ready, staged, &tmO, lse, N, Nk, BH, d, sl, out_mult,
+                               g);
+    else
+      f256_softmax<DK, CAUSAL, SPLIT, DROPOUT, F8>(w, tmem, smem, s_full, p_full, o_ready, staged, &tmO, lse, N, Nk,
+                                                   BH, d, sl, drop, out_mult, g);
     __syncwarp();
     tc_fence_before();
     named_bar_sync(1, 160);
@@ -582,8 +738,11 @@ cudaError_t launch_split_t(const CUtensorMap& tq, const CUtensorMap& tk, const C
                            const CUtensorMap& top, float* lse_part, const Shape& s, int Nk, int n_splits,
                            int kt_per_split, const WaitCfg& wc, cudaStream_t st) {
   using C = F256<DK>;
-  auto kern = s.d == DK ? fa_fwd_d256_kernel<DK, false, true, false, true>
-                        : fa_fwd_d256_kernel<DK, false, false, false, true>;
+  const bool rep = splitkv_replicas(s.N, s.d, false) > 1;
+  auto kern = rep ? (s.d == DK ? fa_fwd_d256_kernel<DK, false, true, false, true, false, true>
+                               : fa_fwd_d256_kernel<DK, false, false, false, true, false, true>)
+                  : (s.d == DK ? fa_fwd_d256_kernel<DK, false, true, false, true>
+                               : fa_fwd_d256_kernel<DK, false, false, false, true>);
   const cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), C::kSmemBytes, C::kThreads, 0);
   if (e != cudaSuccess) return e;
   const int n_qt = (s.N + 127) / 128, n_kt = (Nk + 127) / 128;
@@ -612,7 +771,8 @@ cudaError_t launch_fwd_fp8_split(const CUtensorMap& tq, const CUtensorMap& tk, c
                                  float* lse_part, const Shape& s, int Nk, int n_splits, int kt_per_split,
                                  const WaitCfg& wc, cudaStream_t st) {
   using C = F256<128, true>;
-  auto kern = fa_fwd_d256_kernel<128, false, true, false, true, true>;
+  auto kern = splitkv_replicas(s.N, s.d, true) > 1 ? fa_fwd_d256_kernel<128, false, true, false, true, true, true>
+                              : fa_fwd_d256_kernel<128, false, true, false, true, true, false>;
   const cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), C::kSmemBytes, C::kThreads, 0);
   if (e != cudaSuccess) return e;
   const int n_qt = (s.N + 127) / 128, n_kt = (Nk + 127) / 128;

@@ -129,6 +129,20 @@ cudaError_t launch_fwd_splitkv(const CUtensorMap& tq, const CUtensorMap& tk, con
                                const Shape& s, int Nk, int n_splits, int kt_per_split, const WaitCfg& wc,
                                cudaStream_t st);
 
+// Split-KV calls with at most kRepRows query rows whose key tiles carry 32 KB
+// of K and V (e4m3 codes, or d <= 64) replicate those rows over the four
+// 32-row quarters of the query tile, each quarter taking a quarter of every
+// key tile's keys: the per-tile softmax is what bounds those calls (measured:
+// d = 64 decode 87% -> 97% of the copy rate, e4m3 d = 128 80% -> 87%); with
+// 64 KB or more per key tile the stream already hides it.  Each chunk then
+// writes splitkv_replicas(...) partial results: the Q map and the
+// partial-output map have 32-row boxes, and the merge sees replicas *
+// n_splits chunks.
+constexpr int kRepRows = 32;
+inline int splitkv_replicas(int Nq, int d, bool e4m3) {
+  return Nq <= kRepRows && (e4m3 || kernel_dim(d) == 64) ? 4 : 1;
+}
+
 // The split-KV chunks (fa_fwd_d256.cu's one-query-tile kernel at the
 // kernel head width D = kernel_dim(d)): the fp32 partial outputs through
 // `top` ({D, Nq, n_splits*B*H}, box {32, 128, 1}; the 32-column boxes at or

@@ -190,7 +190,7 @@ def _splitkv_ws(B, H, Nq, Nk, d, splits):
     w = min(splits, n_kt)
     per = -(-n_kt // w)
     n_used = -(-n_kt // per)
-    rows = B * H * Nq * n_used
+    rows = B * H * Nq * n_used * (4 if Nq <= 32 and d <= 64 else 1)   # four results per chunk there
     kd = 64 if d <= 64 else (128 if d <= 128 else 256)
     r256 = lambda x: (x + 255) // 256 * 256
     return r256(rows * kd * 4) + r256(rows * 4)
@@ -199,8 +199,9 @@ def _splitkv_ws(B, H, Nq, Nk, d, splits):
 def test_splitkv_workspace_sizes(lib):
     """With an explicit chunk count no device is consulted: the size is the
     fp32 partial outputs (padded to the kernel's head width) plus the partial
-    LSE of the chunks actually used, each rounded to 256 bytes."""
-    for args in [(1, 1, 1, 1000, 128, 3), (2, 3, 5, 4097, 64, 7), (1, 2, 16, 129, 96, 4),
+    LSE of the chunks actually used (four results per chunk for up to 32 query
+    rows at d <= 64), each rounded to 256 bytes."""
+    for args in [(1, 1, 1, 1000, 128, 3), (2, 3, 5, 4097, 64, 7), (1, 2, 16, 129, 96, 4), (1, 2, 33, 900, 64, 2),
                  (1, 1, 1, 128, 40, 8), (2, 1, 33, 70000, 128, 300), (1, 4, 1, 9000, 256, 6),
                  (2, 2, 130, 300, 200, 2)]:
         assert lib.fa_fwd_splitkv_workspace_bytes(*args) == _splitkv_ws(*args), args
@@ -217,7 +218,7 @@ def test_fp8_splitkv_workspace_sizes_and_argument_checks(lib):
     for B, H, Nq, Nk, d, s in [(1, 1, 1, 1000, 128, 3), (2, 3, 5, 4097, 64, 7), (1, 2, 16, 129, 96, 4)]:
         n_kt = (Nk + 127) // 128
         per = -(-n_kt // min(s, n_kt))
-        rows = B * H * Nq * -(-n_kt // per)
+        rows = B * H * Nq * -(-n_kt // per) * (4 if Nq <= 32 else 1)
         r256 = lambda x: (x + 255) // 256 * 256
         assert lib.fa_fwd_fp8_splitkv_workspace_bytes(B, H, Nq, Nk, d, s) == r256(rows * 128 * 4) + r256(rows * 4)
     assert lib.fa_fwd_fp8_splitkv_workspace_bytes(1, 1, 1, 100, 40, 4) == 0    # d not a multiple of 16

@@ -221,7 +221,9 @@ def _within_bound(o, lse, O, LSE, bound):
     (1, 3, 17, 129, 64, 2, None),       # a one-key last chunk
     (1, 2, 40, 1500, 96, 1, None),      # one chunk
     (1, 2, 64, 128, 32, 5, None),       # more splits wanted than key tiles
-    (2, 4, 1, 8192, 128, 0, 11)])
+    (2, 4, 1, 8192, 128, 0, 11),
+    (1, 2, 32, 1000, 128, 0, None),     # the replicated-row path's edge
+    (1, 2, 33, 1000, 128, 0, None)])
 def test_fp8_splitkv_within_rounding_bound(B, H, Nq, Nk, d, splits, rotate):
     args = _quantized_kv(B, H, Nq, Nk, d, seed=880 + Nq + Nk + d, rotate=rotate)
     scale = 1.0 / math.sqrt(d)

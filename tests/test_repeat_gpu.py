@@ -83,6 +83,7 @@ CASES = {
     "dropout_d256_causal": lambda: _dropout(1, 4, 1024, 256, True, 914),
     "splitkv_d128": lambda: _splitkv(2, 8, 128, 8192, 128, 912),
     "splitkv_d256": lambda: _splitkv(2, 8, 64, 8192, 256, 915),
+    "splitkv_d64_decode": lambda: _splitkv(4, 8, 1, 8192, 64, 917),
     "fp8_d128_causal": lambda: _fp8(2, 8, 2048, 128, True, 913),
     "fp8_splitkv_d128": lambda: _fp8_splitkv(2, 8, 16, 8192, 128, 916),
 }

@@ -26,6 +26,11 @@ CASES = [
     (1, 3, 17, 129, 160, 2),        # a one-key last chunk, d below the box width
     (1, 2, 40, 1500, 192, 1),       # one chunk
     (1, 2, 64, 128, 200, 5),        # more splits wanted than key tiles, d not a multiple of 32
+    # the replicated-row path (up to 32 query rows at d <= 64) at its edge and just past it
+    (2, 2, 32, 2000, 64, 0),
+    (2, 2, 33, 2000, 64, 0),
+    (1, 3, 31, 700, 40, 3),
+    (1, 2, 32, 1500, 256, 2),
 ]
 
 

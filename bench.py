@@ -711,11 +711,14 @@ def run_fp8(args, dist: Dist):
     if args.batch is not None:
         import dataclasses
         w = dataclasses.replace(w, B=args.batch, name=f"{w.name}@B={args.batch}")
+    if args.head_dim is not None:
+        import dataclasses
+        w = dataclasses.replace(w, d=args.head_dim, name=f"{w.name}@d={args.head_dim}")
     causal = w.causal[-1]
     B, H, N, d = w.shape
     x = make_inputs(B, H, N, d, w.seed + 100 * dist.rank, w.qk_mult, with_grad=False)
     q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
-    rot = 0x5EED if args.fp8_rotate else None
+    rot = 0x5EED if args.fp8_rotate and d in (64, 128, 256) else None
     stream = torch.cuda.current_stream(dev)
 
     def quantise():
@@ -759,8 +762,9 @@ def run_fp8(args, dist: Dist):
         "data": "synthetic (seeded N(0,1) bf16 q, k, v, quantised per head)",
         "config": {"workload": w.name, "B": B, "H": H, "N": N, "d": d, "causal": causal, "scale": w.scale,
                    "step": "fa_fwd_fp8", "rotation": bool(rot),
-                   "l2": "inputs larger than L2: q8, k8, vt8 are 67 MB each, O 134 MB"},
-        "roofline": {"kernel": "fa_fwd_fp8_kernel", "bound": "tensor", "achieved": round(value / dist.world, 1),
+                   "l2": f"inputs larger than L2: q8, k8, vt8 are {B * H * N * d / 1e6:.0f} MB each, "
+                         f"O {2 * B * H * N * d / 1e6:.0f} MB"},
+        "roofline": {"kernel": "fa_fwd_fp8_kernel" if d <= 128 else "fa_fwd_d256_kernel<e4m3>", "bound": "tensor", "achieved": round(value / dist.world, 1),
                      "peak": fp8_peak, "unit": "TFLOP/s", "frac": round(value / dist.world / fp8_peak, 3),
                      "peak_source": f"{peak_src} bf16 burst x 2 (nominal fp8/bf16 dense ratio)",
                      "work_per_launch": flops, "traffic": None},

@@ -12,8 +12,8 @@
  *   - Tensors are row-major, contiguous, [B, H, N, d] bf16 (d innermost);
  *     row statistics (LSE, D) are [B, H, N] fp32.  Q, K, V share one N.
  *   - d must be a multiple of 8 from 8 to 256 for every entry point but
- *     the FP8 ones and the deadlock-guard test hook (d up to 128, see
- *     there); else FA_ERR_UNSUPPORTED.  d <= 64 runs the d = 64 kernels,
+ *     the FP8 ones (a multiple of 16) and the deadlock-guard test hook (d up
+ *     to 128, see there); else FA_ERR_UNSUPPORTED.  d <= 64 runs the d = 64 kernels,
  *     64 < d <= 128 the d = 128 ones and 128 < d <= 256 the wide-head
  *     (d = 256) ones: the missing columns are zero-filled on chip, never
  *     read from or written to memory, and the products that contract over d
@@ -238,9 +238,10 @@ fa_status fa_bwd_dropout(const void* q, const void* k, const void* v, const void
  *   rotate != 0: x is first multiplied along d by diag(sigma) H_d / sqrt(d)
  *                (Sylvester-Hadamard; sigma_c = +-1 from bit c of
  *                Philox4x32-10(counter 0, key = seed)); apply it to Q and to
- *                K with the same seed (Q K^T is unchanged).  d must be 64 or
- *                128 (FA_ERR_UNSUPPORTED otherwise).
- * d must be a multiple of 16 in [16, 128] (FA_ERR_UNSUPPORTED).  descale is
+ *                K with the same seed (Q K^T is unchanged).  d must be 64,
+ *                128 or 256 (FA_ERR_UNSUPPORTED otherwise); sigma_c for
+ *                c >= 128 comes from counter block c / 128 (bit c mod 128).
+ * d must be a multiple of 16 in [16, 256] (FA_ERR_UNSUPPORTED).  descale is
  * fp32 [B, H] device memory; x, out 16-byte aligned.  One kernel on
  * `stream` (a cluster launch: one 8-CTA cluster per (b, h)).
  */
@@ -259,8 +260,9 @@ size_t fa_fp8_vt_ld(int N);
  * [B, H, N, d]; lse fp32 [B, H, N] of S.  Error contract (derived, not on
  * the pages): against the exact attention of the dequantised inputs,
  * |O - O_exact| <= sum_j max(2^-4 P~_ij, 2^-10) |V_jc| / l_i plus fp32
- * and bf16 output rounding.  d a multiple of 16 in [16, 128]; causal as in
- * fa_fwd; other errors as fa_fwd.
+ * and bf16 output rounding.  d a multiple of 16 in [16, 256] (d > 128 runs
+ * the one-query-tile kernel's e4m3 variant); causal as in fa_fwd; other
+ * errors as fa_fwd.
  */
 fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* descale_q,
                      const float* descale_k, const float* descale_v, void* o, float* lse,
@@ -279,7 +281,7 @@ fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const floa
  * [B, H, Nq] (Nk == 0: O = 0, LSE = -inf).  workspace: at least
  * fa_fwd_fp8_splitkv_workspace_bytes(...) bytes, 16-byte aligned (may be
  * NULL when that is 0), else FA_ERR_WORKSPACE.  d a multiple of 16 in
- * [16, 128]; Nq == 0 is a no-op; k8, vt8 may be NULL when Nk == 0; other
+ * [16, 256]; Nq == 0 is a no-op; k8, vt8 may be NULL when Nk == 0; other
  * errors as fa_fwd_splitkv.
  */
 fa_status fa_fwd_fp8_splitkv(const void* q8, const void* k8, const void* vt8, const float* descale_q,
@@ -288,10 +290,11 @@ fa_status fa_fwd_fp8_splitkv(const void* q8, const void* k8, const void* vt8, co
                              void* workspace, size_t workspace_bytes, struct CUstream_st* stream);
 
 /*
- * Workspace bytes fa_fwd_fp8_splitkv needs: R * n_used * B*H*Nq*128 fp32
- * partial outputs plus R * n_used * B*H*Nq fp32 partial LSE, each rounded
- * up to 256 bytes, with R = 4 for Nq <= 32 (one partial result per quarter
- * of a chunk's keys) and 1 otherwise, n_used as in
+ * Workspace bytes fa_fwd_fp8_splitkv needs: R * n_used * B*H*Nq*W fp32
+ * partial outputs (W = 128 for d <= 128, else 256) plus R * n_used * B*H*Nq
+ * fp32 partial LSE, each rounded up to 256 bytes, with R = 4 for Nq <= 32
+ * and d <= 128 (one partial result per quarter of a chunk's keys) and 1
+ * otherwise, n_used as in
  * fa_fwd_splitkv_workspace_bytes.  0 for invalid sizes, Nq == 0 or Nk == 0.
  */
 size_t fa_fwd_fp8_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int d, int num_splits);

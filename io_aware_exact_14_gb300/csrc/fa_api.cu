@@ -351,11 +351,11 @@ fa_status make_map_f32(CUtensorMap* m, const void* base, int d, int Nq, long lon
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// FP8: sizes (d a multiple of 16 in [16, 128], the copy engine's 16-byte row
+// FP8: sizes (d a multiple of 16 in [16, 256], the copy engine's 16-byte row
 // rule for 1-byte elements), the transposed-V row pitch, and 4-D maps of
 // e4m3 codes with 128 x 128 boxes.
 fa_status check_sizes_fp8(int B, int H, int N, int d) {
-  FA_TRY(check_sizes(B, H, N, d));
+  FA_TRY(check_sizes(B, H, N, d, fa::kMaxHeadDim));
   return d % 16 == 0 ? FA_OK : FA_ERR_UNSUPPORTED;
 }
 
@@ -630,7 +630,8 @@ fa_status fa_fwd_fp8_splitkv(const void* q8, const void* k8, const void* vt8, co
   FA_TRY(check_scale(scale));
   SplitPlan p;
   const int reps = fa::splitkv_replicas(Nq, d, true);
-  FA_TRY(split_plan(B, H, Nq, Nk, 128, reps, num_splits, p));
+  const int width = d > 128 ? 256 : 128;   // partial rows: the e4m3 kernel's width
+  FA_TRY(split_plan(B, H, Nq, Nk, width, reps, num_splits, p));
   if (static_cast<long long>(B) * H * p.n_splits * std::max((Nq + 127) / 128, reps) > INT32_MAX)
     return FA_ERR_UNSUPPORTED;   // the grid, and the partial results' z coordinate
   const size_t need = p.n_splits > 0 ? p.o_bytes + p.lse_bytes : 0;
@@ -654,20 +655,20 @@ fa_status fa_fwd_fp8_splitkv(const void* q8, const void* k8, const void* vt8, co
     FA_TRY(make_map_u8(&tq, q8, q_dims, q_str, rows_box));
     FA_TRY(make_map_u8(&tk, k8, k_dims, k_str));
     FA_TRY(make_map_u8(&tvt, vt8, vt_dims, vt_str));
-    FA_TRY(make_map_f32(&top, workspace, 128, Nq,
-                        static_cast<long long>(p.n_splits) * reps * B * H, rows_box));
+    FA_TRY(make_map_f32(&top, workspace, width, Nq, static_cast<long long>(p.n_splits) * reps * B * H, rows_box));
     FA_TRY(cuda_status(fa::launch_fwd_fp8_split(tq, tk, tvt, top, descale_q, descale_k, descale_v, lse_part, sq, Nk,
                                                 p.n_splits, p.kt_per_split, fa::next_wait_cfg(), stream),
                        "FP8 split-KV forward launch"));
   }
-  return cuda_status(fa::launch_fwd_merge(o_part, lse_part, o, lse, sq, p.n_splits * reps, 128, stream),
+  return cuda_status(fa::launch_fwd_merge(o_part, lse_part, o, lse, sq, p.n_splits * reps, width, stream),
                      "split-KV merge launch");
 }
 
 size_t fa_fwd_fp8_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int d, int num_splits) {
   if (check_sizes_fp8(B, H, Nq, d) != FA_OK || check_sizes_fp8(B, H, Nk, d) != FA_OK || Nq <= 0 || Nk <= 0) return 0;
   SplitPlan p;
-  if (split_plan(B, H, Nq, Nk, 128, fa::splitkv_replicas(Nq, d, true), num_splits, p) != FA_OK || p.n_splits == 0)
+  if (split_plan(B, H, Nq, Nk, d > 128 ? 256 : 128, fa::splitkv_replicas(Nq, d, true), num_splits, p) != FA_OK ||
+      p.n_splits == 0)
     return 0;
   return p.o_bytes + p.lse_bytes;
 }
@@ -753,7 +754,7 @@ size_t fa_fp8_vt_ld(int N) { return N > 0 ? static_cast<size_t>(fp8_vt_ld(N)) : 
 fa_status fa_fp8_quantize(const void* x, void* out, float* descale, int B, int H, int N, int d, int transpose,
                           int rotate, unsigned long long seed, struct CUstream_st* stream) {
   FA_TRY(check_sizes_fp8(B, H, N, d));
-  if (rotate && d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (rotate && d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
   if (N == 0) return FA_OK;
   FA_TRY(check_ptrs({x, out}, {descale}));
   const Shape s{B, H, N, d, 1.f, 0};
@@ -788,6 +789,10 @@ fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const floa
   FA_TRY(make_map_u8(&tk, k8, qk_dims, qk_str));
   FA_TRY(make_map_u8(&tvt, vt8, vt_dims, vt_str));
   FA_TRY(make_map(&to, o, s));
+  if (d > 128)   // wide heads: the one-query-tile kernel's e4m3 variant
+    return cuda_status(fa::launch_fwd_fp8_wide(tq, tk, tvt, to, descale_q, descale_k, descale_v, lse, s,
+                                               fa::next_wait_cfg(), stream),
+                       "FP8 forward launch");
   return cuda_status(fa::launch_fwd_fp8(tq, tk, tvt, to, descale_q, descale_k, descale_v, lse, s,
                                         fa::next_wait_cfg(), stream),
                      "FP8 forward launch");

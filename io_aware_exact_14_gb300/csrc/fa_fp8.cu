@@ -484,11 +484,14 @@ __device__ __forceinline__ void butterfly_row8(float (&v)[8], int sub) {
   }
 }
 
+// Columns 8 sub .. 8 sub + 7: bits of counter block sub / 16 (128 signs a
+// block), word (sub % 16) / 4, byte sub % 4.
 template <int D>
 __device__ __forceinline__ uint32_t row_signs8(const QuantArgs& a, int sub) {
   if (!a.rotate) return 0u;
-  const uint4 x = philox4x32_10(0u, 0u, 0u, 0u, a.key);   // d <= 128: counter block 0
-  const uint32_t word = (sub / 4) == 0 ? x.x : ((sub / 4) == 1 ? x.y : ((sub / 4) == 2 ? x.z : x.w));
+  const uint4 x = philox4x32_10(static_cast<uint32_t>(sub / 16), 0u, 0u, 0u, a.key);
+  const int wi = (sub % 16) / 4;
+  const uint32_t word = wi == 0 ? x.x : (wi == 1 ? x.y : (wi == 2 ? x.z : x.w));
   return (word >> (8 * (sub % 4))) & 0xFFu;
 }
 
@@ -689,8 +692,11 @@ cudaError_t launch_fp8_quantize(const void* x, void* out, float* descale, const 
   qa.key = make_drop_args(seed, 0, 0);
   qa.inv_sqrt_d = static_cast<float>(1.0 / std::sqrt(static_cast<double>(s.d)));
   qa.rotate = rotate ? 1 : 0;
-  return kernel_dim(s.d) == 128 ? launch_quant_d<128>(x, out, descale, s.B, s.H, s.N, s.d, transpose, ldv, qa, st)
-                                : launch_quant_d<64>(x, out, descale, s.B, s.H, s.N, s.d, transpose, ldv, qa, st);
+  switch (kernel_dim(s.d)) {
+    case 256: return launch_quant_d<256>(x, out, descale, s.B, s.H, s.N, s.d, transpose, ldv, qa, st);
+    case 128: return launch_quant_d<128>(x, out, descale, s.B, s.H, s.N, s.d, transpose, ldv, qa, st);
+    default: return launch_quant_d<64>(x, out, descale, s.B, s.H, s.N, s.d, transpose, ldv, qa, st);
+  }
 }
 
 cudaError_t launch_fwd_fp8(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,

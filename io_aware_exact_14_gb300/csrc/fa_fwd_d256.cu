@@ -54,22 +54,23 @@ constexpr uint32_t kSiteFwd256 = 0x400;
 // beside Q.  Each tile's release is one commit on empty[tile % kTileBars],
 // and kTileBars * kHalves >= kSlots, so a release barrier is never reused
 // before the producer has waited on it.
-// F8: e4m3 Q, K and V^T (split-KV launches at DK = 128): a tile is one box
-// of 128 rows x 128 bytes, the products are kind::f8f6f4 (K = 32 per MMA),
-// V arrives transposed (d rows x key columns), so both products read K-major
-// operands, and P goes back to TMEM as e4m3, four keys per column.
+// F8: e4m3 Q, K and V^T (DK = 128 or 256): a K tile is DK / 128 boxes of
+// 128 rows x 128 bytes side by side, a V^T tile (d rows x key columns) DK /
+// 128 boxes stacked by rows, moved as one unit; the products are
+// kind::f8f6f4 (K = 32 per MMA) on K-major operands, and P goes back to TMEM
+// as e4m3, four keys per column.
 template <int DK, bool F8 = false>
 struct F256 {
   static_assert(DK == 64 || DK == 128 || DK == 256, "kernel head width");
-  static_assert(!F8 || DK == 128, "e4m3 tiles are 128 bytes wide");
-  static constexpr int kHalves = DK == 256 ? 2 : 1;                // units per tile
-  static constexpr int kUnitBoxes = (F8 || DK == 64) ? 1 : 2;      // boxes per unit
+  static_assert(!F8 || DK >= 128, "e4m3 tiles are 128 bytes wide");
+  static constexpr int kHalves = (DK == 256 && !F8) ? 2 : 1;      // units per tile
+  static constexpr int kUnitBoxes = F8 ? DK / 128 : (DK == 64 ? 1 : 2);   // boxes per unit
   static constexpr int kUnitSteps = 4 * kUnitBoxes;                // 32-byte K steps per unit
   static constexpr uint32_t kBoxBytes = 128u * 128u;       // 128 rows x 128 B (swizzled)
   static constexpr uint32_t kUnitBytes = kUnitBoxes * kBoxBytes;
-  static constexpr int kQBoxes = F8 ? 1 : DK / 64;
-  static constexpr int kSlots = DK == 256 ? 5 : ((DK == 128 && !F8) ? 6 : 13);
-  static constexpr int kTileBars = DK == 256 ? 4 : 16;
+  static constexpr int kQBoxes = F8 ? DK / 128 : DK / 64;
+  static constexpr int kSlots = kUnitBytes == 32768u ? (DK == 256 && !F8 ? 5 : 6) : 13;
+  static constexpr int kTileBars = kHalves == 2 ? 4 : 16;
   static_assert(kTileBars * kHalves >= kSlots, "release barriers outlast the ring");
   static constexpr uint32_t kQOff = 0;                     // Q boxes; O staging at the end
   static constexpr uint32_t kSlotOff = kQBoxes * kBoxBytes;
@@ -145,15 +146,17 @@ __device__ void f256_producer(const W256& w, uint8_t* smem, uint64_t* full, uint
                               const CtaGuard& g) {
   using C = F256<DK, F8>;
   mbar_arrive_expect_tx(q_full, C::kQBoxes * C::kBoxBytes);
+  constexpr int kBoxCols = F8 ? 128 : 64;   // elements per 128-byte box row
   if constexpr (REP) {   // rows 0-31 (a 32-row box map) into each 32-row quarter of the tile
 #pragma unroll
     for (int b = 0; b < C::kQBoxes; ++b)
 #pragma unroll
-      for (int q = 0; q < 4; ++q) tma_load_hd(smem + C::kQOff + b * C::kBoxBytes + q * 4096u, tmQ, q_full, 64 * b, 0, w.hc);
+      for (int q = 0; q < 4; ++q)
+        tma_load_hd(smem + C::kQOff + b * C::kBoxBytes + q * 4096u, tmQ, q_full, kBoxCols * b, 0, w.hc);
   } else {
 #pragma unroll
     for (int b = 0; b < C::kQBoxes; ++b)
-      tma_load_hd(smem + C::kQOff + b * C::kBoxBytes, tmQ, q_full, 64 * b, 128 * w.qt, w.hc);
+      tma_load_hd(smem + C::kQOff + b * C::kBoxBytes, tmQ, q_full, kBoxCols * b, 128 * w.qt, w.hc);
   }
   const int units = 2 * C::kHalves * w.n;
   int issued = 0;
@@ -168,8 +171,14 @@ __device__ void f256_producer(const W256& w, uint8_t* smem, uint64_t* full, uint
     stream_tile(t, w.n, is_v, j);
     uint8_t* dst = smem + C::kSlotOff + slot * C::kUnitBytes;
     mbar_arrive_expect_tx(&full[slot], C::kUnitBytes);
-    if (F8 && is_v) {   // V^T: d rows x keys
-      tma_load_hd(dst, tmV, &full[slot], 128 * (w.kt0 + j), 0, w.hc);
+    if (F8 && is_v) {   // V^T: d rows x keys, boxes stacked by rows
+#pragma unroll
+      for (int b = 0; b < C::kUnitBoxes; ++b)
+        tma_load_hd(dst + b * C::kBoxBytes, tmV, &full[slot], 128 * (w.kt0 + j), 128 * b, w.hc);
+    } else if (F8) {    // K: keys x d, boxes side by side
+#pragma unroll
+      for (int b = 0; b < C::kUnitBoxes; ++b)
+        tma_load_hd(dst + b * C::kBoxBytes, tmK, &full[slot], 128 * b, 128 * (w.kt0 + j), w.hc);
     } else {
 #pragma unroll
       for (int b = 0; b < C::kUnitBoxes; ++b)
@@ -239,11 +248,15 @@ __device__ void f256_mma(const W256& w, uint32_t tmem, uint32_t sbase, uint64_t*
     if (!mbar_wait_w(p_full, j & 1, g, kSiteFwd256 | 4u)) return;
     tc_fence_after();
     const uint32_t tp = tmem + 128u * buf;
-    if constexpr (F8) {   // 128 keys, 32 per MMA; P packs 4 keys per TMEM column; V^T K-major
-      const uint64_t vt = kd0 + slot_off(t);
+    if constexpr (F8) {   // 128 keys, 32 per MMA; P packs 4 keys per TMEM column; V^T K-major,
+                          // one 128-row box per 128 columns of O
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        tc_mma_f8_ts_w(tmem + C::kColO, tp + kk * 8, vt + kstep_off(kk), (j > 0 || kk > 0) ? 1u : 0u);
+      for (int b = 0; b < C::kUnitBoxes; ++b) {
+        const uint64_t vt = kd0 + slot_off(t) + static_cast<uint64_t>((b * C::kBoxBytes) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc_mma_f8_ts_w(tmem + C::kColO + 128u * b, tp + kk * 8, vt + kstep_off(kk), (j > 0 || kk > 0) ? 1u : 0u);
+      }
     } else {
 #pragma unroll
       for (int h = 0; h < C::kHalves; ++h) {
@@ -457,7 +470,7 @@ __device__ void f256_softmax(const W256& w, uint32_t tmem, uint8_t* smem, uint64
     fence_proxy_async_smem();
     mbar_arrive(staged);
     if (r == 0 && mbar_wait(staged, 0, g, kSiteFwd256 | 8u)) {
-      for (int b = 0; b < C::kQBoxes; ++b)
+      for (int b = 0; b < DK / 64; ++b)   // bf16 O: 64-column boxes
         if (64 * b < d) tma_store_hd(tmO, smem + C::kQOff + b * C::kBoxBytes, 64 * b, w.qt * 128, w.hc);
       tma_store_commit();
       tma_store_wait_read_all();
@@ -626,7 +639,6 @@ __global__ void __launch_bounds__(192, 1)
                        const __grid_constant__ DropArgs drop, const WaitCfg wc) {
   static_assert(!SPLIT || (!CAUSAL && !DROPOUT), "split-KV launches are non-causal without dropout");
   static_assert(SPLIT || DK == 256, "below d = 256 only split-KV launches run this kernel");
-  static_assert(!F8 || SPLIT, "the e4m3 variant serves split-KV launches");
   static_assert(!REP || SPLIT, "row replication serves split-KV launches");
   using C = F256<DK, F8>;
   extern __shared__ uint8_t smem_raw[];
@@ -721,6 +733,26 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   return cudaGetLastError();
 }
 
+// The e4m3 variant at width DK: a split-KV launch (SPLIT; REP: row
+// replication) or a plain forward (grid B H n_qt, causal or not).
+template <int DK, bool CAUSAL, bool SPLIT, bool REP>
+cudaError_t launch_f8_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,
+                        const CUtensorMap& to, const float* dsq, const float* dsk, const float* dsv, float* lse,
+                        const Shape& s, int Nk, int n_splits, int kt_per_split, const WaitCfg& wc, cudaStream_t st) {
+  using C = F256<DK, true>;
+  auto kern = fa_fwd_d256_kernel<DK, CAUSAL, true, false, SPLIT, true, REP>;
+  const cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), C::kSmemBytes, C::kThreads, 0);
+  if (e != cudaSuccess) return e;
+  const int n_qt = (s.N + 127) / 128, n_kt = (Nk + 127) / 128;
+  const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
+  const dim3 grid(static_cast<unsigned>(s.B) * s.H * (SPLIT ? n_splits : 1) * n_qt);
+  // L2 band: e4m3 K and V of a head take 2 N d bytes, as bf16 ones of d / 2 columns
+  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tvt, to, lse, s.N, Nk, s.d, n_qt, s.B * s.H, s.H,
+                                                 head_band(s.N, (s.d + 1) / 2), scale_log2, 0, 0u, n_kt,
+                                                 n_splits, kt_per_split, dsq, dsk, dsv, no_drop_args(), wc);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_fwd_d256(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -738,11 +770,13 @@ cudaError_t launch_split_t(const CUtensorMap& tq, const CUtensorMap& tk, const C
                            const CUtensorMap& top, float* lse_part, const Shape& s, int Nk, int n_splits,
                            int kt_per_split, const WaitCfg& wc, cudaStream_t st) {
   using C = F256<DK>;
-  const bool rep = splitkv_replicas(s.N, s.d, false) > 1;
-  auto kern = rep ? (s.d == DK ? fa_fwd_d256_kernel<DK, false, true, false, true, false, true>
-                               : fa_fwd_d256_kernel<DK, false, false, false, true, false, true>)
-                  : (s.d == DK ? fa_fwd_d256_kernel<DK, false, true, false, true>
-                               : fa_fwd_d256_kernel<DK, false, false, false, true>);
+  auto kern = s.d == DK ? fa_fwd_d256_kernel<DK, false, true, false, true>
+                        : fa_fwd_d256_kernel<DK, false, false, false, true>;
+  if constexpr (DK == 64) {   // row replication (splitkv_replicas) applies at width 64 only
+    if (splitkv_replicas(s.N, s.d, false) > 1)
+      kern = s.d == DK ? fa_fwd_d256_kernel<DK, false, true, false, true, false, true>
+                       : fa_fwd_d256_kernel<DK, false, false, false, true, false, true>;
+  }
   const cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), C::kSmemBytes, C::kThreads, 0);
   if (e != cudaSuccess) return e;
   const int n_qt = (s.N + 127) / 128, n_kt = (Nk + 127) / 128;
@@ -770,18 +804,21 @@ cudaError_t launch_fwd_fp8_split(const CUtensorMap& tq, const CUtensorMap& tk, c
                                  const CUtensorMap& top, const float* dsq, const float* dsk, const float* dsv,
                                  float* lse_part, const Shape& s, int Nk, int n_splits, int kt_per_split,
                                  const WaitCfg& wc, cudaStream_t st) {
-  using C = F256<128, true>;
-  auto kern = splitkv_replicas(s.N, s.d, true) > 1 ? fa_fwd_d256_kernel<128, false, true, false, true, true, true>
-                              : fa_fwd_d256_kernel<128, false, true, false, true, true, false>;
-  const cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), C::kSmemBytes, C::kThreads, 0);
-  if (e != cudaSuccess) return e;
-  const int n_qt = (s.N + 127) / 128, n_kt = (Nk + 127) / 128;
-  const float scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
-  const dim3 grid(static_cast<unsigned>(s.B) * s.H * n_splits * n_qt);
-  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tvt, top, lse_part, s.N, Nk, s.d, n_qt, s.B * s.H, s.H, 1,
-                                                 scale_log2, 8, 0u, n_kt, n_splits, kt_per_split, dsq, dsk, dsv,
-                                                 no_drop_args(), wc);
-  return cudaGetLastError();
+  if (s.d > 128)
+    return launch_f8_t<256, false, true, false>(tq, tk, tvt, top, dsq, dsk, dsv, lse_part, s, Nk, n_splits,
+                                                kt_per_split, wc, st);
+  if (splitkv_replicas(s.N, s.d, true) > 1)
+    return launch_f8_t<128, false, true, true>(tq, tk, tvt, top, dsq, dsk, dsv, lse_part, s, Nk, n_splits,
+                                               kt_per_split, wc, st);
+  return launch_f8_t<128, false, true, false>(tq, tk, tvt, top, dsq, dsk, dsv, lse_part, s, Nk, n_splits,
+                                              kt_per_split, wc, st);
+}
+
+cudaError_t launch_fwd_fp8_wide(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,
+                                const CUtensorMap& to, const float* dsq, const float* dsk, const float* dsv,
+                                float* lse, const Shape& s, const WaitCfg& wc, cudaStream_t st) {
+  return s.causal ? launch_f8_t<256, true, false, false>(tq, tk, tvt, to, dsq, dsk, dsv, lse, s, s.N, 1, 0, wc, st)
+                  : launch_f8_t<256, false, false, false>(tq, tk, tvt, to, dsq, dsk, dsv, lse, s, s.N, 1, 0, wc, st);
 }
 
 cudaError_t fwd_d256_status(uint32_t* out, bool reset) {

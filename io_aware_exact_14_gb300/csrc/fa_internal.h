@@ -130,7 +130,7 @@ cudaError_t launch_fwd_splitkv(const CUtensorMap& tq, const CUtensorMap& tk, con
                                cudaStream_t st);
 
 // Split-KV calls with at most kRepRows query rows whose key tiles carry 32 KB
-// of K and V (e4m3 codes, or d <= 64) replicate those rows over the four
+// of K and V (e4m3 codes of d <= 128, or bf16 of d <= 64) replicate those rows over the four
 // 32-row quarters of the query tile, each quarter taking a quarter of every
 // key tile's keys: the per-tile softmax is what bounds those calls (measured:
 // d = 64 decode 87% -> 97% of the copy rate, e4m3 d = 128 80% -> 87%); with
@@ -140,7 +140,7 @@ cudaError_t launch_fwd_splitkv(const CUtensorMap& tq, const CUtensorMap& tk, con
 // n_splits chunks.
 constexpr int kRepRows = 32;
 inline int splitkv_replicas(int Nq, int d, bool e4m3) {
-  return Nq <= kRepRows && (e4m3 || kernel_dim(d) == 64) ? 4 : 1;
+  return Nq <= kRepRows && kernel_dim(d) <= (e4m3 ? 128 : 64) ? 4 : 1;
 }
 
 // The split-KV chunks (fa_fwd_d256.cu's one-query-tile kernel at the
@@ -152,14 +152,21 @@ cudaError_t launch_fwd_onetile_split(const CUtensorMap& tq, const CUtensorMap& t
                                      const CUtensorMap& top, float* lse_part, const Shape& s, int Nk, int n_splits,
                                      int kt_per_split, const WaitCfg& wc, cudaStream_t st);
 
-// FP8 split-KV chunks: the one-query-tile kernel's e4m3 variant (d <= 128,
-// kernel width 128) on e4m3 Q, K (maps {d, Nq or Nk, H, B}, 128 x 128-byte
+// FP8 split-KV chunks: the one-query-tile kernel's e4m3 variant (kernel
+// width 128 for d <= 128, else 256) on e4m3 Q, K (maps {d, Nq or Nk, H, B}, 128 x 128-byte
 // boxes) and V^T (map {Nk, d, H, B}, row pitch fp8 ldv), descales per (b, h);
-// partial outputs as launch_fwd_onetile_split at width 128.
+// partial outputs as launch_fwd_onetile_split at that width.
 cudaError_t launch_fwd_fp8_split(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,
                                  const CUtensorMap& top, const float* dsq, const float* dsk, const float* dsv,
                                  float* lse_part, const Shape& s, int Nk, int n_splits, int kt_per_split,
                                  const WaitCfg& wc, cudaStream_t st);
+
+// FP8 forward for 128 < d <= 256 (fa_fwd_d256.cu, the e4m3 variant at width
+// 256): maps as launch_fwd_fp8_split's with 128-row Q boxes, bf16 O map as
+// fa_fwd's; one query tile per CTA, causal or not.
+cudaError_t launch_fwd_fp8_wide(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,
+                                const CUtensorMap& to, const float* dsq, const float* dsk, const float* dsv,
+                                float* lse, const Shape& s, const WaitCfg& wc, cudaStream_t st);
 
 // The split-KV merge (fa_fwd.cu): n_splits chunks' fp32 partial outputs
 // (rows D wide) and LSE -> o (bf16 [B, H, Nq, d]) and lse; n_splits == 0

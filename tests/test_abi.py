@@ -152,13 +152,15 @@ def test_dropout_argument_checks(lib):
 def test_fp8_argument_checks(lib):
     x, out, ds = FAKE, FAKE + 0x100000, FAKE + 0x200000
     assert lib.fa_fp8_quantize(x, out, ds, 1, 1, 128, 40, 0, 0, 0, None) == 2    # d not a multiple of 16
-    assert lib.fa_fp8_quantize(x, out, ds, 1, 1, 128, 96, 0, 1, 5, None) == 2    # rotation needs d = 64 or 128
+    assert lib.fa_fp8_quantize(x, out, ds, 1, 1, 128, 96, 0, 1, 5, None) == 2    # rotation needs d = 64, 128 or 256
+    assert lib.fa_fp8_quantize(x, out, ds, 1, 1, 128, 272, 0, 0, 0, None) == 2   # above the widest head
     assert lib.fa_fp8_quantize(0, out, ds, 1, 1, 128, 64, 0, 0, 0, None) == 1
     assert lib.fa_fp8_quantize(x, x, ds, 1, 1, 128, 64, 0, 0, 0, None) == 1     # out aliases x
     assert lib.fa_fp8_quantize(x, out, ds, 1, 1, 0, 64, 0, 0, 0, None) == 0      # empty
     assert lib.fa_fp8_vt_ld(1) == 16 and lib.fa_fp8_vt_ld(32) == 32 and lib.fa_fp8_vt_ld(33) == 48
     p = [FAKE + i * 0x100000 for i in range(8)]
     assert lib.fa_fwd_fp8(*p, 1, 1, 128, 40, 0.1, 0, None) == 2
+    assert lib.fa_fwd_fp8(*p, 1, 1, 128, 272, 0.1, 0, None) == 2
     assert lib.fa_fwd_fp8(*p, 1, 1, 128, 64, 0.0, 0, None) == 1
     assert lib.fa_fwd_fp8(*p[:6], p[0], p[7], 1, 1, 128, 64, 0.1, 0, None) == 1   # o aliases q8
     assert lib.fa_fwd_fp8(0, *p[1:], 1, 1, 128, 64, 0.1, 0, None) == 1
@@ -212,17 +214,20 @@ def test_splitkv_workspace_sizes(lib):
 
 
 def test_fp8_splitkv_workspace_sizes_and_argument_checks(lib):
-    """The e4m3 split path's partial rows are 128 floats wide at every d; its
-    sizes follow the FP8 rule (d a multiple of 16 up to 128); argument errors
-    come back before any device access."""
-    for B, H, Nq, Nk, d, s in [(1, 1, 1, 1000, 128, 3), (2, 3, 5, 4097, 64, 7), (1, 2, 16, 129, 96, 4)]:
+    """The e4m3 split path's partial rows are 128 floats wide for d <= 128 and
+    256 beyond (four results per chunk for up to 32 query rows at d <= 128);
+    its sizes follow the FP8 rule (d a multiple of 16 up to 256); argument
+    errors come back before any device access."""
+    for B, H, Nq, Nk, d, s in [(1, 1, 1, 1000, 128, 3), (2, 3, 5, 4097, 64, 7), (1, 2, 16, 129, 96, 4),
+                               (1, 2, 1, 3000, 256, 5), (2, 1, 40, 900, 192, 2)]:
         n_kt = (Nk + 127) // 128
         per = -(-n_kt // min(s, n_kt))
-        rows = B * H * Nq * -(-n_kt // per) * (4 if Nq <= 32 else 1)
+        rows = B * H * Nq * -(-n_kt // per) * (4 if Nq <= 32 and d <= 128 else 1)
+        width = 128 if d <= 128 else 256
         r256 = lambda x: (x + 255) // 256 * 256
-        assert lib.fa_fwd_fp8_splitkv_workspace_bytes(B, H, Nq, Nk, d, s) == r256(rows * 128 * 4) + r256(rows * 4)
+        assert lib.fa_fwd_fp8_splitkv_workspace_bytes(B, H, Nq, Nk, d, s) == r256(rows * width * 4) + r256(rows * 4)
     assert lib.fa_fwd_fp8_splitkv_workspace_bytes(1, 1, 1, 100, 40, 4) == 0    # d not a multiple of 16
-    assert lib.fa_fwd_fp8_splitkv_workspace_bytes(1, 1, 1, 100, 256, 4) == 0   # above the e4m3 width
+    assert lib.fa_fwd_fp8_splitkv_workspace_bytes(1, 1, 1, 100, 272, 4) == 0   # above the widest head
     assert lib.fa_fwd_fp8_splitkv_workspace_bytes(1, 1, 1, 0, 128, 4) == 0
     p = [FAKE + i * 0x100000 for i in range(9)]
     call = lambda *a: lib.fa_fwd_fp8_splitkv(*a)

@@ -25,7 +25,9 @@ def _codes_np(t):
 @pytest.mark.parametrize("B,H,N,d,transpose,rotate", [
     (1, 2, 200, 128, False, None), (2, 1, 129, 64, True, None), (1, 3, 300, 96, False, None),
     (1, 1, 77, 32, True, None), (1, 2, 256, 128, False, 1234), (2, 2, 130, 64, True, 99),
-    (1, 1, 500, 128, True, 7), (1, 2, 33, 16, False, None)])
+    (1, 1, 500, 128, True, 7), (1, 2, 33, 16, False, None),
+    (1, 2, 200, 256, False, None), (1, 1, 300, 256, True, 77), (2, 1, 129, 192, True, None),
+    (1, 2, 256, 256, False, 4321)])
 def test_quantize_bit_exact(B, H, N, d, transpose, rotate):
     x, g = device_inputs(B, H, N, d, seed=800 + N + d)
     xin = g["q"] * 3.0        # a bf16 tensor; both sides quantise exactly these values
@@ -56,12 +58,12 @@ def _oracle(args, N, scale, causal):
                                     dv.cpu().numpy(), scale, causal)
 
 
-@pytest.mark.parametrize("causal", [False, True])
-def test_fp8_forward_power_of_two_probabilities_exact(causal):
+@pytest.mark.parametrize("causal,d", [(False, 128), (True, 128), (False, 256), (True, 256)])
+def test_fp8_forward_power_of_two_probabilities_exact(causal, d):
     """Q = e_0, K_j = -a_j e_0 (a_j in 0..8) and scale ln 2 make every
     probability a power of two, which e4m3 holds exactly: O must match the
     oracle to output rounding (any misplaced or misordered P byte shows)."""
-    B, H, N, d = 1, 2, 300, 128
+    B, H, N = 1, 2, 300
     rng = np.random.default_rng(11)
     q8 = np.zeros((B, H, N, d), dtype=np.uint8)
     q8[..., 0] = fp8_ref.e4m3_encode(np.array([1.0]))[0]
@@ -87,7 +89,9 @@ def test_fp8_forward_power_of_two_probabilities_exact(causal):
 
 @pytest.mark.parametrize("B,H,N,d,causal,qk", [
     (1, 2, 256, 128, False, 1.0), (2, 1, 333, 128, True, 1.0), (1, 2, 129, 64, True, 3.0),
-    (1, 1, 1000, 96, False, 1.0), (2, 2, 200, 32, True, 3.0), (1, 1, 17, 128, True, 1.0)])
+    (1, 1, 1000, 96, False, 1.0), (2, 2, 200, 32, True, 3.0), (1, 1, 17, 128, True, 1.0),
+    (1, 2, 300, 256, True, 1.0), (2, 1, 333, 192, False, 1.0), (1, 1, 1000, 256, False, 1.0),
+    (1, 2, 129, 144, True, 3.0)])
 def test_fp8_forward_within_rounding_bound(B, H, N, d, causal, qk):
     _, _, args = _quantized(B, H, N, d, seed=820 + N + d, qk_mult=qk)
     scale = 1.0 / math.sqrt(d)
@@ -223,7 +227,10 @@ def _within_bound(o, lse, O, LSE, bound):
     (1, 2, 64, 128, 32, 5, None),       # more splits wanted than key tiles
     (2, 4, 1, 8192, 128, 0, 11),
     (1, 2, 32, 1000, 128, 0, None),     # the replicated-row path's edge
-    (1, 2, 33, 1000, 128, 0, None)])
+    (1, 2, 33, 1000, 128, 0, None),
+    (1, 2, 1, 3000, 256, 0, None),      # wide heads: width-256 chunks
+    (2, 2, 200, 3000, 256, 7, 5),
+    (1, 2, 40, 1500, 192, 1, None)])
 def test_fp8_splitkv_within_rounding_bound(B, H, Nq, Nk, d, splits, rotate):
     args = _quantized_kv(B, H, Nq, Nk, d, seed=880 + Nq + Nk + d, rotate=rotate)
     scale = 1.0 / math.sqrt(d)

@@ -59,7 +59,7 @@ def pin_fwht_is_sylvester(ref):
     """fwht_f32(x) = x H_d with H_d the Sylvester-Hadamard matrix (scipy), and
     the rotation is orthogonal: it keeps q.k (fp64 products of the fp32 outputs)."""
     rng = np.random.default_rng(4)
-    for d in (8, 16, 64, 128):
+    for d in (8, 16, 64, 128, 256):
         x = rng.standard_normal((5, d)).astype(np.float32)
         want = x.astype(np.float64) @ scipy.linalg.hadamard(d)
         assert np.max(np.abs(ref.fwht_f32(x) - want)) <= 1e-5 * np.abs(want).max()
@@ -73,6 +73,10 @@ def pin_fwht_is_sylvester(ref):
         assert np.max(np.abs(qr @ kr.T - qk)) <= 1e-5 * (1 + np.abs(qk).max())
         s = ref.hadamard_signs(d, 12345)
         assert set(np.unique(s)) <= {-1.0, 1.0} and 0 < (s < 0).sum() < d
+    # past 128 columns the signs continue from the next counter block: the
+    # first 128 of d = 256 are those of d = 128, the rest a different draw
+    s256, s128 = ref.hadamard_signs(256, 777), ref.hadamard_signs(128, 777)
+    assert np.array_equal(s256[:128], s128) and not np.array_equal(s256[128:], s128)
 
 
 def pin_quantize_round_trip(ref):

@@ -81,8 +81,8 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  struct CUstream_st* stream);
 
 /*
- * Split-KV forward (non-causal) for short query blocks against long key
- * sequences, e.g. decoding: the keys are cut into num_splits chunks of whole
+ * Split-KV forward for short query blocks against long key sequences, e.g.
+ * decoding or a prefill chunk: the keys are cut into num_splits chunks of whole
  * 128-key tiles, each chunk's (O_s, LSE_s) is computed as in fa_fwd and the
  * chunks are merged with the two-block merge identity of [WHY-FAST]
  * "在线Softmax技巧" (LSE = log sum_s e^{LSE_s}, O = sum_s e^{LSE_s - LSE} O_s),
@@ -91,6 +91,13 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
  *   k, v       in : bf16 [B, H, Nk, d]
  *   o          out: bf16 [B, H, Nq, d]
  *   lse        out: fp32 [B, H, Nq]  (Nk == 0: O = 0, LSE = -inf)
+ *   causal     0: every query sees every key.  1: the query block is the
+ *              last Nq positions of the Nk-long sequence (query i at
+ *              position Nk - Nq + i, aligned to the end of the keys), and
+ *              sees keys 0 .. Nk - Nq + i; a query with no such key (Nq >
+ *              Nk) gets O = 0, LSE = -inf.  Nq == Nk is fa_fwd's causal mask.
+ *              (The library's reading: the pages define the mask only for
+ *              equal lengths.)
  *   num_splits  chunks wanted (<= 0: chosen from the SM count); the count
  *               used is at most ceil(Nk / 128), every chunk non-empty
  *   workspace   scratch for the chunks' fp32 (O_s, LSE_s), owned by the
@@ -101,7 +108,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
  * and overlap rules as for fa_fwd, with Nq and Nk each in place of N.
  */
 fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
-                         int B, int H, int Nq, int Nk, int d, float scale, int num_splits,
+                         int B, int H, int Nq, int Nk, int d, float scale, int causal, int num_splits,
                          void* workspace, size_t workspace_bytes, struct CUstream_st* stream);
 
 /*
@@ -269,8 +276,8 @@ fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const floa
                      int B, int H, int N, int d, float scale, int causal, struct CUstream_st* stream);
 
 /*
- * Split-KV forward on e4m3 codes (non-causal), e.g. decoding against an
- * e4m3 key/value cache: q8 [B, H, Nq, d], k8 [B, H, Nk, d], vt8
+ * Split-KV forward on e4m3 codes (causal as in fa_fwd_splitkv), e.g.
+ * decoding against an e4m3 key/value cache: q8 [B, H, Nq, d], k8 [B, H, Nk, d], vt8
  * [B, H, d, fa_fp8_vt_ld(Nk)] (from fa_fp8_quantize; V with transpose = 1),
  * descales fp32 [B, H].  The keys are cut into chunks as in fa_fwd_splitkv;
  * each chunk computes fa_fwd_fp8's arithmetic (its own reference maximum,
@@ -286,7 +293,7 @@ fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const floa
  */
 fa_status fa_fwd_fp8_splitkv(const void* q8, const void* k8, const void* vt8, const float* descale_q,
                              const float* descale_k, const float* descale_v, void* o, float* lse,
-                             int B, int H, int Nq, int Nk, int d, float scale, int num_splits,
+                             int B, int H, int Nq, int Nk, int d, float scale, int causal, int num_splits,
                              void* workspace, size_t workspace_bytes, struct CUstream_st* stream);
 
 /*

@@ -568,8 +568,8 @@ fa_status fa_fwd_strided(const void* q, const fa_strides* q_st, const void* k, c
 }
 
 fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
-                         int Nk, int d, float scale, int num_splits, void* workspace, size_t workspace_bytes,
-                         struct CUstream_st* stream) {
+                         int Nk, int d, float scale, int causal, int num_splits, void* workspace,
+                         size_t workspace_bytes, struct CUstream_st* stream) {
   FA_TRY(check_sizes(B, H, Nq, d, fa::kMaxHeadDim));
   FA_TRY(check_sizes(B, H, Nk, d, fa::kMaxHeadDim));
   if (Nq == 0) return FA_OK;
@@ -583,7 +583,7 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, f
     return FA_ERR_UNSUPPORTED;   // the grid, and the partial results' z coordinate
   const size_t need = p.n_splits > 0 ? p.o_bytes + p.lse_bytes : 0;
   if (need > 0 && (workspace == nullptr || !aligned(workspace, 16) || workspace_bytes < need)) return FA_ERR_WORKSPACE;
-  const Shape sq{B, H, Nq, d, scale, 0}, sk{B, H, Nk, d, scale, 0};
+  const Shape sq{B, H, Nq, d, scale, causal ? 1 : 0}, sk{B, H, Nk, d, scale, 0};
   const size_t qb = tensor_bytes(sq), kb = tensor_bytes(sk);
   FA_TRY(check_disjoint({{o, qb}, {lse, vec_bytes(sq)}, {workspace, need}}, {{q, qb}, {k, kb}, {v, kb}}));
   if (!load_encoder()) return FA_ERR_CUDA;
@@ -620,7 +620,7 @@ size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int d, int n
 
 fa_status fa_fwd_fp8_splitkv(const void* q8, const void* k8, const void* vt8, const float* descale_q,
                              const float* descale_k, const float* descale_v, void* o, float* lse, int B, int H,
-                             int Nq, int Nk, int d, float scale, int num_splits, void* workspace,
+                             int Nq, int Nk, int d, float scale, int causal, int num_splits, void* workspace,
                              size_t workspace_bytes, struct CUstream_st* stream) {
   FA_TRY(check_sizes_fp8(B, H, Nq, d));
   FA_TRY(check_sizes_fp8(B, H, Nk, d));
@@ -636,7 +636,7 @@ fa_status fa_fwd_fp8_splitkv(const void* q8, const void* k8, const void* vt8, co
     return FA_ERR_UNSUPPORTED;   // the grid, and the partial results' z coordinate
   const size_t need = p.n_splits > 0 ? p.o_bytes + p.lse_bytes : 0;
   if (need > 0 && (workspace == nullptr || !aligned(workspace, 16) || workspace_bytes < need)) return FA_ERR_WORKSPACE;
-  const Shape sq{B, H, Nq, d, scale, 0};
+  const Shape sq{B, H, Nq, d, scale, causal ? 1 : 0};
   const size_t q_bytes = tensor_bytes(sq) / 2, k_bytes = static_cast<size_t>(B) * H * Nk * d;
   const size_t vt_bytes = static_cast<size_t>(B) * H * d * fp8_vt_ld(Nk), ds_bytes = static_cast<size_t>(B) * H * 4;
   FA_TRY(check_disjoint({{o, tensor_bytes(sq)}, {lse, vec_bytes(sq)}, {workspace, need}},

@@ -127,7 +127,11 @@ __device__ __forceinline__ W256 w256_work(int n_qt, int BH, int H, int band, boo
 // Split-KV: CTA u takes query tile u % n_qt of one head and one chunk of
 // kt_per_split key tiles (the last chunk may be shorter, never empty); CTAs
 // of one (head, chunk) are adjacent, so they share the chunk's K/V in L2.
-__device__ __forceinline__ W256 w256_split_work(int n_qt, int n_splits, int kt_per_split, int n_kt, int H) {
+// Causal (query i at position Nk - Nq + i): the CTA stops at the last key
+// tile its rows can see, but keeps one tile where it sees none, so that it
+// still writes its (empty) partial result.
+__device__ __forceinline__ W256 w256_split_work(int n_qt, int n_splits, int kt_per_split, int n_kt, int H,
+                                                bool causal, int Nq, int Nk) {
   W256 w;
   const int u = static_cast<int>(blockIdx.x);
   w.qt = u % n_qt;
@@ -137,6 +141,12 @@ __device__ __forceinline__ W256 w256_split_work(int n_qt, int n_splits, int kt_p
   w.hc = head_coord(w.bh, H);
   w.kt0 = w.split * kt_per_split;
   w.n = min(kt_per_split, n_kt - w.kt0);
+  if (causal) {
+    const long long last_key = static_cast<long long>(w.qt) * 128 + 127 + (Nk - Nq);
+    const long long tiles = last_key < 0 ? 0 : last_key / 128 + 1;   // key tiles the rows can see
+    const long long seen = (tiles < n_kt ? tiles : n_kt) - w.kt0;
+    if (seen < w.n) w.n = seen < 1 ? 1 : static_cast<int>(seen);
+  }
   return w;
 }
 
@@ -320,7 +330,7 @@ __device__ void f256_softmax(const W256& w, uint32_t tmem, uint8_t* smem, uint64
 
     const int kv0 = (w.kt0 + j) * 128;
     int lim = Nk - kv0;
-    if (CAUSAL) lim = min(lim, row - kv0 + 1);
+    if (CAUSAL) lim = min(lim, row + (Nk - N) - kv0 + 1);   // query row at position Nk - N + row
     if (lim < 128) {
 #pragma unroll
       for (int c = 0; c < 128; ++c)
@@ -487,7 +497,7 @@ __device__ void f256_softmax(const W256& w, uint32_t tmem, uint8_t* smem, uint64
 // query row i over warp q's keys; each quarter is stored as its own partial
 // result (z = (4 split + q) BH + bh, rows 0-31 through a 32-row box map), so
 // the merge, given 4 n_splits chunks, combines them like any other chunks.
-template <int DK, bool F8>
+template <int DK, bool CAUSAL, bool F8>
 __device__ void f256_softmax_rep(const W256& w, uint32_t tmem, uint8_t* smem, uint64_t* s_full, uint64_t* p_full,
                                  uint64_t* o_ready, uint64_t* staged, const CUtensorMap* tmO,
                                  float* __restrict__ lse, int N, int Nk, int BH, int d, float scale_log2,
@@ -509,7 +519,9 @@ __device__ void f256_softmax_rep(const W256& w, uint32_t tmem, uint8_t* smem, ui
     uint32_t s[32];
     tmem_ld32(tS + 32 * wq, s);
     tmem_ld_wait(s);
-    const int lim = Nk - ((w.kt0 + j) * 128 + 32 * wq);   // visible keys of this quarter
+    const int kq0 = (w.kt0 + j) * 128 + 32 * wq;   // first key of this quarter
+    int lim = Nk - kq0;                            // visible keys of this quarter
+    if (CAUSAL) lim = min(lim, row + (Nk - N) - kq0 + 1);   // query row at position Nk - N + row
     if (lim < 32) {
 #pragma unroll
       for (int c = 0; c < 32; ++c)
@@ -637,7 +649,7 @@ __global__ void __launch_bounds__(192, 1)
                        float scale_log2, int ks, uint32_t idesc_pvl, int n_kt, int n_splits, int kt_per_split,
                        const float* __restrict__ dsq, const float* __restrict__ dsk, const float* __restrict__ dsv,
                        const __grid_constant__ DropArgs drop, const WaitCfg wc) {
-  static_assert(!SPLIT || (!CAUSAL && !DROPOUT), "split-KV launches are non-causal without dropout");
+  static_assert(!SPLIT || !DROPOUT, "split-KV launches have no dropout");
   static_assert(SPLIT || DK == 256, "below d = 256 only split-KV launches run this kernel");
   static_assert(!REP || SPLIT, "row replication serves split-KV launches");
   using C = F256<DK, F8>;
@@ -655,7 +667,8 @@ __global__ void __launch_bounds__(192, 1)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kMiscOff + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const W256 w = SPLIT ? w256_split_work(n_qt, n_splits, kt_per_split, n_kt, H) : w256_work(n_qt, BH, H, band, CAUSAL);
+  const W256 w = SPLIT ? w256_split_work(n_qt, n_splits, kt_per_split, n_kt, H, CAUSAL, N, Nk)
+                       : w256_work(n_qt, BH, H, band, CAUSAL);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kSlots; ++i) mbar_init(&full[i], 1);
@@ -704,8 +717,8 @@ __global__ void __launch_bounds__(192, 1)
       out_mult = dsv[w.bh];
     }
     if constexpr (REP)
-      f256_softmax_rep<DK, F8>(w, tmem, smem, s_full, p_full, o_ready, staged, &tmO, lse, N, Nk, BH, d, sl, out_mult,
-                               g);
+      f256_softmax_rep<DK, CAUSAL, F8>(w, tmem, smem, s_full, p_full, o_ready, staged, &tmO, lse, N, Nk, BH, d, sl,
+                                       out_mult, g);
     else
       f256_softmax<DK, CAUSAL, SPLIT, DROPOUT, F8>(w, tmem, smem, s_full, p_full, o_ready, staged, &tmO, lse, N, Nk,
                                                    BH, d, sl, drop, out_mult, g);
@@ -765,17 +778,17 @@ cudaError_t launch_fwd_d256(const CUtensorMap& tq, const CUtensorMap& tk, const 
                   : launch_t<false, false>(tq, tk, tv, to, lse, s, drop, wc, st);
 }
 
-template <int DK>
+template <int DK, bool CAUSAL>
 cudaError_t launch_split_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            const CUtensorMap& top, float* lse_part, const Shape& s, int Nk, int n_splits,
                            int kt_per_split, const WaitCfg& wc, cudaStream_t st) {
   using C = F256<DK>;
-  auto kern = s.d == DK ? fa_fwd_d256_kernel<DK, false, true, false, true>
-                        : fa_fwd_d256_kernel<DK, false, false, false, true>;
+  auto kern = s.d == DK ? fa_fwd_d256_kernel<DK, CAUSAL, true, false, true>
+                        : fa_fwd_d256_kernel<DK, CAUSAL, false, false, true>;
   if constexpr (DK == 64) {   // row replication (splitkv_replicas) applies at width 64 only
     if (splitkv_replicas(s.N, s.d, false) > 1)
-      kern = s.d == DK ? fa_fwd_d256_kernel<DK, false, true, false, true, false, true>
-                       : fa_fwd_d256_kernel<DK, false, false, false, true, false, true>;
+      kern = s.d == DK ? fa_fwd_d256_kernel<DK, CAUSAL, true, false, true, false, true>
+                       : fa_fwd_d256_kernel<DK, CAUSAL, false, false, true, false, true>;
   }
   const cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), C::kSmemBytes, C::kThreads, 0);
   if (e != cudaSuccess) return e;
@@ -793,10 +806,17 @@ cudaError_t launch_split_t(const CUtensorMap& tq, const CUtensorMap& tk, const C
 cudaError_t launch_fwd_onetile_split(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                      const CUtensorMap& top, float* lse_part, const Shape& s, int Nk, int n_splits,
                                      int kt_per_split, const WaitCfg& wc, cudaStream_t st) {
+  if (s.causal) {
+    switch (kernel_dim(s.d)) {
+      case 256: return launch_split_t<256, true>(tq, tk, tv, top, lse_part, s, Nk, n_splits, kt_per_split, wc, st);
+      case 128: return launch_split_t<128, true>(tq, tk, tv, top, lse_part, s, Nk, n_splits, kt_per_split, wc, st);
+      default: return launch_split_t<64, true>(tq, tk, tv, top, lse_part, s, Nk, n_splits, kt_per_split, wc, st);
+    }
+  }
   switch (kernel_dim(s.d)) {
-    case 256: return launch_split_t<256>(tq, tk, tv, top, lse_part, s, Nk, n_splits, kt_per_split, wc, st);
-    case 128: return launch_split_t<128>(tq, tk, tv, top, lse_part, s, Nk, n_splits, kt_per_split, wc, st);
-    default: return launch_split_t<64>(tq, tk, tv, top, lse_part, s, Nk, n_splits, kt_per_split, wc, st);
+    case 256: return launch_split_t<256, false>(tq, tk, tv, top, lse_part, s, Nk, n_splits, kt_per_split, wc, st);
+    case 128: return launch_split_t<128, false>(tq, tk, tv, top, lse_part, s, Nk, n_splits, kt_per_split, wc, st);
+    default: return launch_split_t<64, false>(tq, tk, tv, top, lse_part, s, Nk, n_splits, kt_per_split, wc, st);
   }
 }
 
@@ -804,14 +824,23 @@ cudaError_t launch_fwd_fp8_split(const CUtensorMap& tq, const CUtensorMap& tk, c
                                  const CUtensorMap& top, const float* dsq, const float* dsk, const float* dsv,
                                  float* lse_part, const Shape& s, int Nk, int n_splits, int kt_per_split,
                                  const WaitCfg& wc, cudaStream_t st) {
+  const bool rep = splitkv_replicas(s.N, s.d, true) > 1;
+  if (s.causal) {
+    if (s.d > 128)
+      return launch_f8_t<256, true, true, false>(tq, tk, tvt, top, dsq, dsk, dsv, lse_part, s, Nk, n_splits,
+                                                 kt_per_split, wc, st);
+    return rep ? launch_f8_t<128, true, true, true>(tq, tk, tvt, top, dsq, dsk, dsv, lse_part, s, Nk, n_splits,
+                                                    kt_per_split, wc, st)
+               : launch_f8_t<128, true, true, false>(tq, tk, tvt, top, dsq, dsk, dsv, lse_part, s, Nk, n_splits,
+                                                     kt_per_split, wc, st);
+  }
   if (s.d > 128)
     return launch_f8_t<256, false, true, false>(tq, tk, tvt, top, dsq, dsk, dsv, lse_part, s, Nk, n_splits,
                                                 kt_per_split, wc, st);
-  if (splitkv_replicas(s.N, s.d, true) > 1)
-    return launch_f8_t<128, false, true, true>(tq, tk, tvt, top, dsq, dsk, dsv, lse_part, s, Nk, n_splits,
-                                               kt_per_split, wc, st);
-  return launch_f8_t<128, false, true, false>(tq, tk, tvt, top, dsq, dsk, dsv, lse_part, s, Nk, n_splits,
-                                              kt_per_split, wc, st);
+  return rep ? launch_f8_t<128, false, true, true>(tq, tk, tvt, top, dsq, dsk, dsv, lse_part, s, Nk, n_splits,
+                                                   kt_per_split, wc, st)
+             : launch_f8_t<128, false, true, false>(tq, tk, tvt, top, dsq, dsk, dsv, lse_part, s, Nk, n_splits,
+                                                    kt_per_split, wc, st);
 }
 
 cudaError_t launch_fwd_fp8_wide(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,

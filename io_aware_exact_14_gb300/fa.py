@@ -34,7 +34,7 @@ SIGNATURES = {
     "fa_fwd_strided": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
     "fa_bwd_strided": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                             _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
-    "fa_fwd_splitkv": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
+    "fa_fwd_splitkv": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P]),
     "fa_fwd_splitkv_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "fa_bwd_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
@@ -43,7 +43,7 @@ SIGNATURES = {
     "fa_fp8_quantize": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_ulonglong, _P]),
     "fa_fp8_vt_ld": (_SZ, [_I]),
     "fa_fwd_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
-    "fa_fwd_fp8_splitkv": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
+    "fa_fwd_fp8_splitkv": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P]),
     "fa_fwd_fp8_splitkv_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "fa_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
     "fa_bwd_preprocess": (_I, [_P, _P, _P, _I, _I, _I, _I, _P]),
@@ -236,9 +236,10 @@ def fa_fwd_splitkv_workspace_bytes(B: int, H: int, Nq: int, Nk: int, d: int, num
 
 
 def fa_fwd_splitkv(q, k, v, scale: Optional[float] = None, num_splits: int = 0, out=None, lse=None,
-                   workspace=None, stream=None):
-    """Non-causal O, LSE for q [B, H, Nq, d] against k, v [B, H, Nk, d], the keys cut
-    into `num_splits` chunks (<= 0: the library's choice) merged by their LSE."""
+                   workspace=None, stream=None, causal: bool = False):
+    """O, LSE for q [B, H, Nq, d] against k, v [B, H, Nk, d], the keys cut into
+    `num_splits` chunks (<= 0: the library's choice) merged by their LSE; causal:
+    query i sits at position Nk - Nq + i and sees the keys up to it."""
     qs = _bhnd(q, "q")
     ks = _bhnd(k, "k")
     _same(ks, v, "v")
@@ -257,7 +258,7 @@ def fa_fwd_splitkv(q, k, v, scale: Optional[float] = None, num_splits: int = 0, 
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     st = load().fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                               B, H, Nq, Nk, d, scale, int(num_splits), workspace.data_ptr(),
+                               B, H, Nq, Nk, d, scale, int(bool(causal)), int(num_splits), workspace.data_ptr(),
                                workspace.numel() * workspace.element_size(), _stream_ptr(stream))
     _check("fa_fwd_splitkv", st)
     return out, lse
@@ -392,10 +393,10 @@ def fa_fwd_fp8_splitkv_workspace_bytes(B: int, H: int, Nq: int, Nk: int, d: int,
 
 
 def fa_fwd_fp8_splitkv(q8, k8, vt8, descale_q, descale_k, descale_v, scale: Optional[float] = None,
-                       num_splits: int = 0, out=None, lse=None, workspace=None, stream=None):
-    """Non-causal split-KV forward on e4m3 codes (uint8): q8 [B, H, Nq, d], k8 [B, H, Nk, d],
+                       num_splits: int = 0, out=None, lse=None, workspace=None, stream=None, causal: bool = False):
+    """Split-KV forward on e4m3 codes (uint8): q8 [B, H, Nq, d], k8 [B, H, Nk, d],
     vt8 [B, H, d, fa_fp8_vt_ld(Nk)], descales fp32 [B, H]; returns bf16 O [B, H, Nq, d] and
-    fp32 LSE [B, H, Nq]."""
+    fp32 LSE [B, H, Nq]; causal as in fa_fwd_splitkv."""
     for t, n in ((q8, "q8"), (k8, "k8"), (vt8, "vt8")):
         if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.uint8 and t.is_contiguous()
                 and t.dim() == 4):
@@ -417,7 +418,7 @@ def fa_fwd_fp8_splitkv(q8, k8, vt8, descale_q, descale_k, descale_v, scale: Opti
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q8.device)
     st = load().fa_fwd_fp8_splitkv(q8.data_ptr(), k8.data_ptr(), vt8.data_ptr(), descale_q.data_ptr(),
                                    descale_k.data_ptr(), descale_v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                                   B, H, Nq, Nk, d, scale, int(num_splits), workspace.data_ptr(),
+                                   B, H, Nq, Nk, d, scale, int(bool(causal)), int(num_splits), workspace.data_ptr(),
                                    workspace.numel() * workspace.element_size(), _stream_ptr(stream))
     _check("fa_fwd_fp8_splitkv", st)
     return out, lse

@@ -231,8 +231,8 @@ def test_fp8_splitkv_workspace_sizes_and_argument_checks(lib):
     assert lib.fa_fwd_fp8_splitkv_workspace_bytes(1, 1, 1, 0, 128, 4) == 0
     p = [FAKE + i * 0x100000 for i in range(9)]
     call = lambda *a: lib.fa_fwd_fp8_splitkv(*a)
-    assert call(*p[:8], 1, 1, 1, 1000, 40, 0.1, 2, p[8], 1 << 20, None) == 2     # d not a multiple of 16
-    assert call(0, *p[1:8], 1, 1, 1, 1000, 64, 0.1, 2, p[8], 1 << 20, None) == 1  # NULL q8
-    assert call(*p[:6], p[0], p[7], 1, 1, 1, 1000, 64, 0.1, 2, p[8], 1 << 20, None) == 1   # o aliases q8
-    assert call(*p[:8], 1, 1, 1, 1000, 64, 0.1, 2, p[8], 16, None) == 4          # workspace too small
-    assert call(*p[:8], 1, 1, 0, 1000, 64, 0.1, 2, None, 0, None) == 0            # Nq == 0: no-op
+    assert call(*p[:8], 1, 1, 1, 1000, 40, 0.1, 0, 2, p[8], 1 << 20, None) == 2     # d not a multiple of 16
+    assert call(0, *p[1:8], 1, 1, 1, 1000, 64, 0.1, 0, 2, p[8], 1 << 20, None) == 1  # NULL q8
+    assert call(*p[:6], p[0], p[7], 1, 1, 1, 1000, 64, 0.1, 1, 2, p[8], 1 << 20, None) == 1   # o aliases q8
+    assert call(*p[:8], 1, 1, 1, 1000, 64, 0.1, 1, 2, p[8], 16, None) == 4          # workspace too small
+    assert call(*p[:8], 1, 1, 0, 1000, 64, 0.1, 0, 2, None, 0, None) == 0            # Nq == 0: no-op

@@ -283,3 +283,21 @@ def test_fp8_splitkv_empty_keys_and_short_workspace():
     with pytest.raises(fa.FAError) as e:
         fa.fa_fwd_fp8_splitkv(*args, None, 4, workspace=ws)
     assert e.value.status == fa.FA_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,d,splits", [
+    (1, 2, 200, 3000, 128, 7), (1, 2, 17, 1000, 128, 0), (1, 2, 40, 1500, 256, 1), (2, 1, 300, 300, 64, 2)])
+def test_fp8_causal_splitkv_within_rounding_bound(B, H, Nq, Nk, d, splits):
+    """Causal: query i at position Nk - Nq + i; the oracle runs the FP8
+    reference on query codes placed at those positions of an Nk-row array."""
+    args = _quantized_kv(B, H, Nq, Nk, d, seed=990 + Nq + Nk + d)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = fa.fa_fwd_fp8_splitkv(*args, scale, splits, causal=True)
+    torch.cuda.synchronize()
+    assert_no_timeout()
+    q8, k8, vt8, dq, dk, dv = args
+    qp = np.zeros((B, H, Nk, d), dtype=np.uint8)
+    qp[:, :, Nk - Nq:] = _codes_np(q8)
+    O, LSE, _, bound = fp8_ref.attn_fwd_fp8_ref(qp, _codes_np(k8), _codes_np(vt8)[..., :Nk], dq.cpu().numpy(),
+                                                dk.cpu().numpy(), dv.cpu().numpy(), scale, True)
+    _within_bound(o, lse, O[:, :, Nk - Nq:], LSE[:, :, Nk - Nq:], bound[:, :, Nk - Nq:])

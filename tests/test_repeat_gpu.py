@@ -42,10 +42,10 @@ def _dropout(B, H, N, d, causal, seed):
     return run
 
 
-def _splitkv(B, H, Nq, Nk, d, seed):
+def _splitkv(B, H, Nq, Nk, d, seed, causal=False):
     _, gq = device_inputs(B, H, Nq, d, seed=seed)
     _, gk = device_inputs(B, H, Nk, d, seed=seed + 1)
-    return lambda: fa.fa_fwd_splitkv(gq["q"], gk["k"], gk["v"])
+    return lambda: fa.fa_fwd_splitkv(gq["q"], gk["k"], gk["v"], causal=causal)
 
 
 def _fp8_splitkv(B, H, Nq, Nk, d, seed):
@@ -84,6 +84,7 @@ CASES = {
     "splitkv_d128": lambda: _splitkv(2, 8, 128, 8192, 128, 912),
     "splitkv_d256": lambda: _splitkv(2, 8, 64, 8192, 256, 915),
     "splitkv_d64_decode": lambda: _splitkv(4, 8, 1, 8192, 64, 917),
+    "splitkv_d128_causal_chunk": lambda: _splitkv(2, 8, 256, 8192, 128, 918, True),
     "fp8_d128_causal": lambda: _fp8(2, 8, 2048, 128, True, 913),
     "fp8_splitkv_d128": lambda: _fp8_splitkv(2, 8, 16, 8192, 128, 916),
 }

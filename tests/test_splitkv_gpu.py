@@ -111,3 +111,72 @@ def test_splitkv_rejects_short_workspace():
     with pytest.raises(fa.FAError) as e:
         fa.fa_fwd_splitkv(g["q"], g["k"], g["v"], None, 4, workspace=ws)
     assert e.value.status == fa.FA_ERR_WORKSPACE
+
+
+# Causal split-KV: the query block is the last Nq positions of the Nk-long
+# sequence (query i at position Nk - Nq + i), so the oracle is the plain
+# definition evaluated at those positions of a query array of Nk rows.
+def _causal_ref(x, scale):
+    q, k, v = f64(x["q"]), f64(x["k"]), f64(x["v"])
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    qp = np.zeros((B, H, Nk, d))
+    qp[:, :, Nk - Nq:] = q
+    rows = np.broadcast_to(np.arange(Nk - Nq, Nk), (B, H, Nq))
+    return oracle.attn_fwd_ref_rows(qp, k, v, scale, True, rows)
+
+
+CAUSAL_CASES = [
+    # B, H, Nq, Nk, d, num_splits
+    (1, 2, 1, 3000, 128, 0),        # one query row: sees every key
+    (2, 2, 200, 3000, 128, 7),      # two query tiles, early chunks past some rows' positions
+    (1, 3, 17, 129, 64, 2),         # replicated rows, a one-key last chunk
+    (2, 2, 32, 2000, 64, 0),        # replicated rows at their edge
+    (1, 2, 64, 128, 200, 5),        # more splits wanted than key tiles
+    (1, 2, 40, 1500, 256, 1),       # wide heads, one chunk
+    (1, 1, 500, 700, 96, 0),
+]
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,d,splits", CAUSAL_CASES)
+def test_causal_splitkv_parity(B, H, Nq, Nk, d, splits):
+    x = make_splitkv_inputs(B, H, Nq, Nk, d, 900 + Nq + Nk + d)
+    g = {k: t.cuda() for k, t in x.items()}
+    scale = 1.0 / np.sqrt(d)
+    o, lse = fa.fa_fwd_splitkv(g["q"], g["k"], g["v"], scale, splits, causal=True)
+    torch.cuda.synchronize()
+    assert_no_timeout()
+    o_ref, lse_ref = _causal_ref(x, scale)
+    assert o_excess_err(f64(o), o_ref) <= TOL_O
+    assert oracle.lse_max_abs_err(f64(lse), lse_ref) <= TOL_LSE
+
+
+def test_causal_splitkv_equal_lengths_is_the_square_mask():
+    """Nq == Nk: the same result as fa_fwd's causal forward (both within the
+    tolerance of the oracle)."""
+    B, H, N, d = 1, 2, 700, 128
+    x = make_splitkv_inputs(B, H, N, N, d, 950)
+    g = {k: t.cuda() for k, t in x.items()}
+    o_s, lse_s = fa.fa_fwd_splitkv(g["q"], g["k"], g["v"], None, 3, causal=True)
+    o_p, lse_p = fa.fa_fwd(g["q"], g["k"], g["v"], None, True)
+    torch.cuda.synchronize()
+    assert_no_timeout()
+    assert (o_s.float() - o_p.float()).abs().max().item() <= 2 * TOL_O
+    assert (lse_s - lse_p).abs().max().item() <= 2 * TOL_LSE
+
+
+def test_causal_splitkv_queries_before_the_first_key():
+    """Nq > Nk: the first Nq - Nk queries sit before position 0 and see no key
+    (O = 0, LSE = -inf); the rest match the oracle at their positions."""
+    B, H, Nq, Nk, d = 1, 2, 300, 200, 64
+    x = make_splitkv_inputs(B, H, Nq, Nk, d, 960)
+    g = {k: t.cuda() for k, t in x.items()}
+    o, lse = fa.fa_fwd_splitkv(g["q"], g["k"], g["v"], None, 2, causal=True)
+    torch.cuda.synchronize()
+    assert_no_timeout()
+    cut = Nq - Nk
+    assert torch.all(o[:, :, :cut] == 0) and torch.all(torch.isneginf(lse[:, :, :cut]))
+    tail = {"q": x["q"][:, :, cut:], "k": x["k"], "v": x["v"]}
+    o_ref, lse_ref = _causal_ref(tail, 1.0 / np.sqrt(d))
+    assert o_excess_err(f64(o[:, :, cut:]), o_ref) <= TOL_O
+    assert oracle.lse_max_abs_err(f64(lse[:, :, cut:]), lse_ref) <= TOL_LSE

@@ -63,7 +63,9 @@ def parse():
     ap.add_argument("--fp8-rotate", type=int, default=1, help="incoherent rotation of Q and K (1) or not (0)")
     ap.add_argument("--splitkv", action="store_true",
                     help="time the split-KV forward on --splitkv-shape instead of the training step")
-    ap.add_argument("--splitkv-shape", default="8,32,1,16384,128", help="B,H,Nq,Nk,d (non-causal)")
+    ap.add_argument("--splitkv-shape", default="8,32,1,16384,128", help="B,H,Nq,Nk,d")
+    ap.add_argument("--splitkv-causal", action="store_true",
+                    help="causal split-KV (the query block is the last Nq positions of the keys' sequence)")
     ap.add_argument("--splitkv-splits", type=int, default=0, help="key chunks (0: the library's choice)")
     return ap.parse_args()
 
@@ -629,11 +631,12 @@ def run_splitkv(args, dist: Dist):
         vt8, dv = fa.fa_fp8_quantize(v, transpose=True)
         ws = torch.empty(max(fa.fa_fwd_fp8_splitkv_workspace_bytes(B, H, Nq, Nk, d, ns), 1), dtype=torch.uint8,
                          device=dev)
-        call = lambda: fa.fa_fwd_fp8_splitkv(q8, k8, vt8, dq, dk, dv, None, ns, out=o, lse=lse, workspace=ws)
+        call = lambda: fa.fa_fwd_fp8_splitkv(q8, k8, vt8, dq, dk, dv, None, ns, out=o, lse=lse, workspace=ws,
+                                             causal=args.splitkv_causal)
     else:
         ws = torch.empty(max(fa.fa_fwd_splitkv_workspace_bytes(B, H, Nq, Nk, d, ns), 1), dtype=torch.uint8,
                          device=dev)
-        call = lambda: fa.fa_fwd_splitkv(q, k, v, None, ns, out=o, lse=lse, workspace=ws)
+        call = lambda: fa.fa_fwd_splitkv(q, k, v, None, ns, out=o, lse=lse, workspace=ws, causal=args.splitkv_causal)
     clocks = ClockSampler(dist.local)
     clocks.start()
     for _ in range(args.warmup):
@@ -663,9 +666,10 @@ def run_splitkv(args, dist: Dist):
         "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if args.fp8 else "bf16",
         "data": "synthetic (seeded N(0,1) bf16 q, k, v" + (", quantised to e4m3 per head)" if args.fp8 else ")"),
-        "config": {"workload": f"decode_splitkv{'_fp8' if args.fp8 else ''}_B{B}_H{H}_Nq{Nq}_Nk{Nk}_d{d}",
+        "config": {"workload": f"decode_splitkv{'_fp8' if args.fp8 else ''}{'_causal' if args.splitkv_causal else ''}"
+                               f"_B{B}_H{H}_Nq{Nq}_Nk{Nk}_d{d}",
                    "B": B, "H": H, "Nq": Nq, "Nk": Nk,
-                   "d": d, "causal": False, "num_splits": ns if ns > 0 else "library choice (0)",
+                   "d": d, "causal": bool(args.splitkv_causal), "num_splits": ns if ns > 0 else "library choice (0)",
                    "l2": f"inputs larger than L2: K and V are {2 * B * H * Nk * d * (1 if args.fp8 else 2) / 1e6:.0f}"
                          " MB together" if 2 * B * H * Nk * d * (1 if args.fp8 else 2) > 129e6 else
                          "K and V fit in L2 (no flush between calls)",
@@ -678,7 +682,7 @@ def run_splitkv(args, dist: Dist):
                      "work_per_launch": algo, "traffic": None},
         "gpu_launches": 2 * args.steps, "clocks": clk,
     }
-    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline and not args.fp8:
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline and not args.fp8 and not args.splitkv_causal:
         import oracle
         from io_aware_exact_14_gb300.workloads import to_f64
         done, tb = 0, time.time()

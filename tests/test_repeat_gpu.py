@@ -87,6 +87,8 @@ CASES = {
     "splitkv_d128_causal_chunk": lambda: _splitkv(2, 8, 256, 8192, 128, 918, True),
     "fp8_d128_causal": lambda: _fp8(2, 8, 2048, 128, True, 913),
     "fp8_splitkv_d128": lambda: _fp8_splitkv(2, 8, 16, 8192, 128, 916),
+    "fp8_d256_causal": lambda: _fp8(2, 4, 2048, 256, True, 919),
+    "fp8_splitkv_d256": lambda: _fp8_splitkv(2, 8, 1, 8192, 256, 920),
 }
 
 

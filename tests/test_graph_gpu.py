@@ -6,7 +6,9 @@ parameters, so a captured forward + backward replays on whatever the static
 buffers hold at replay time.  Each replay, with fresh inputs copied into the
 captured buffers, must equal the same calls made eagerly, bit for bit (the
 kernels are deterministic).  Covered: the three kernel families (d = 64, 128,
-256), both masks, the workspace and the no-allocation backward.
+256), both masks, the workspace and the no-allocation backward; and a
+decode step (split-KV on bf16 or e4m3 keys and values, the latter with the
+query's quantisation inside the graph).
 """
 import pytest
 import torch
@@ -62,3 +64,52 @@ def test_graph_replay_equals_eager_calls(d, causal, noalloc):
         assert_no_timeout()
         for n in ("o", "lse", "dq", "dk", "dv"):
             assert torch.equal(static[n], eager[n]), f"{n} differs on replay {rep}"
+
+
+@pytest.mark.parametrize("d,e4m3,causal", [(128, False, False), (64, False, True), (128, True, False),
+                                            (256, True, True)])
+def test_graph_replay_of_decode_steps(d, e4m3, causal):
+    """A decode loop's split-KV call (bf16 or e4m3 keys and values, one
+    query row per head) captured once and replayed with new queries equals
+    the eager call bit for bit."""
+    B, H, Nq, Nk = 2, 4, 4, 3000
+    _, kv = device_inputs(B, H, Nk, d, seed=7300 + d)
+    q_static = torch.empty((B, H, Nq, d), dtype=torch.bfloat16, device="cuda")
+    outs = {n: (torch.empty((B, H, Nq, d), dtype=torch.bfloat16, device="cuda"),
+                torch.empty((B, H, Nq), dtype=torch.float32, device="cuda")) for n in ("static", "eager")}
+    if e4m3:
+        k8, dk = fa.fa_fp8_quantize(kv["k"])
+        vt8, dv = fa.fa_fp8_quantize(kv["v"], transpose=True)
+        q8 = torch.empty((B, H, Nq, d), dtype=torch.uint8, device="cuda")
+        dq = torch.empty((B, H), dtype=torch.float32, device="cuda")
+        ws = torch.empty(max(fa.fa_fwd_fp8_splitkv_workspace_bytes(B, H, Nq, Nk, d, 0), 1), dtype=torch.uint8,
+                         device="cuda")
+
+        def step(q, out):
+            fa.fa_fp8_quantize(q, out=q8, descale=dq)
+            fa.fa_fwd_fp8_splitkv(q8, k8, vt8, dq, dk, dv, None, 0, out=out[0], lse=out[1], workspace=ws,
+                                  causal=causal)
+    else:
+        ws = torch.empty(max(fa.fa_fwd_splitkv_workspace_bytes(B, H, Nq, Nk, d, 0), 1), dtype=torch.uint8,
+                         device="cuda")
+
+        def step(q, out):
+            fa.fa_fwd_splitkv(q, kv["k"], kv["v"], None, 0, out=out[0], lse=out[1], workspace=ws, causal=causal)
+    _, first = device_inputs(B, H, Nq, d, seed=7400 + d)
+    q_static.copy_(first["q"])
+    step(q_static, outs["static"])
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step(q_static, outs["static"])
+    torch.cuda.synchronize()
+    for rep in range(3):
+        _, g = device_inputs(B, H, Nq, d, seed=7500 + 10 * d + rep)
+        q_static.copy_(g["q"])
+        graph.replay()
+        torch.cuda.synchronize()
+        step(g["q"], outs["eager"])
+        torch.cuda.synchronize()
+        assert_no_timeout()
+        for i in range(2):
+            assert torch.equal(outs["static"][i], outs["eager"][i]), f"output {i} differs on replay {rep}"

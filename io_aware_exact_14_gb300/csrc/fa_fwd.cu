@@ -586,25 +586,44 @@ __global__ void __launch_bounds__(256) fa_fwd_merge_kernel(const float* __restri
   for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
   float wsum = 0.f;
   if (m != -INFINITY) {
-    for (int s = 0; s < n_splits; ++s) {
-      const long long idx = static_cast<long long>(s) * rows + row;
-      const float ls = lse_part[idx];
-      const float wgt = ls == -INFINITY ? 0.f : __expf(ls - m);
-      wsum += wgt;
-      const float* src = o_part + idx * D + lane * kPer;
-      if constexpr (kPer >= 4) {
+    // chunks in order s = 0, 1, ...; the loads of kBatch chunks go out
+    // together (independent of the sums), the sums then run in order
+    constexpr int kBatch = 4;
+    for (int s0 = 0; s0 < n_splits; s0 += kBatch) {
+      float ls[kBatch];
+      float x[kBatch][kPer];
 #pragma unroll
-        for (int e = 0; e < kPer; e += 4) {
-          const float4 x = *reinterpret_cast<const float4*>(src + e);
-          acc[e] = fmaf(wgt, x.x, acc[e]);
-          acc[e + 1] = fmaf(wgt, x.y, acc[e + 1]);
-          acc[e + 2] = fmaf(wgt, x.z, acc[e + 2]);
-          acc[e + 3] = fmaf(wgt, x.w, acc[e + 3]);
+      for (int u = 0; u < kBatch; ++u) {
+        ls[u] = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) x[u][e] = 0.f;
+        if (s0 + u < n_splits) {
+          const long long idx = static_cast<long long>(s0 + u) * rows + row;
+          ls[u] = lse_part[idx];
+          const float* src = o_part + idx * D + lane * kPer;
+#pragma unroll
+          for (int e = 0; e < kPer; e += (kPer >= 4 ? 4 : 2)) {
+            if constexpr (kPer >= 4) {
+              const float4 v = *reinterpret_cast<const float4*>(src + e);
+              x[u][e] = v.x;
+              x[u][e + 1] = v.y;
+              x[u][e + 2] = v.z;
+              x[u][e + 3] = v.w;
+            } else {
+              const float2 v = *reinterpret_cast<const float2*>(src + e);
+              x[u][e] = v.x;
+              x[u][e + 1] = v.y;
+            }
+          }
         }
-      } else {
-        const float2 x = *reinterpret_cast<const float2*>(src);
-        acc[0] = fmaf(wgt, x.x, acc[0]);
-        acc[1] = fmaf(wgt, x.y, acc[1]);
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        if (s0 + u >= n_splits) break;
+        const float wgt = ls[u] == -INFINITY ? 0.f : __expf(ls[u] - m);
+        wsum += wgt;
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) acc[e] = fmaf(wgt, x[u][e], acc[e]);
       }
     }
   }

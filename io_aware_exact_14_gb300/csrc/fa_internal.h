@@ -119,11 +119,13 @@ cudaError_t launch_fwd_q4(const CUtensorMap& tq, const CUtensorMap& tk64, const 
                           const CUtensorMap& to, float* lse, const Shape& s, const WaitCfg& wc, cudaStream_t st);
 
 // Split-KV forward for short query blocks against long key sequences
-// (non-causal): Q maps {d, Nq, H, B} (s.N = Nq), K/V maps {d, Nk, H, B}; each
-// chunk of key tiles writes its normalised O (fp32, map `top` {d, Nq,
-// n_splits*B*H}, box {32, 128, 1}) and its LSE (lse_part, fp32
-// [n_splits, B*H, Nq]); a merge kernel then writes o (bf16 [B, H, Nq, d]) and
-// lse (fp32 [B, H, Nq]).  n_splits and kt_per_split come from splitkv_chunks.
+// (s.causal: the block is the last Nq positions of the keys' sequence): Q
+// maps {d, Nq, H, B} (s.N = Nq; 32-row boxes with replicated rows), K/V maps
+// {d, Nk, H, B}; each chunk of key tiles writes its normalised O (fp32, map
+// `top` {D, Nq, R*n_splits*B*H}, 32-column boxes of 128 rows, or 32 with
+// replicated rows) and its LSE (lse_part, fp32 [R*n_splits, B*H, Nq]; R =
+// splitkv_replicas); the merge then writes o (bf16 [B, H, Nq, d]) and lse
+// (fp32 [B, H, Nq]).  n_splits and kt_per_split come from splitkv_chunks.
 cudaError_t launch_fwd_splitkv(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                const CUtensorMap& top, const float* o_part, float* lse_part, void* o, float* lse,
                                const Shape& s, int Nk, int n_splits, int kt_per_split, const WaitCfg& wc,
@@ -145,9 +147,8 @@ inline int splitkv_replicas(int Nq, int d, bool e4m3) {
 
 // The split-KV chunks (fa_fwd_d256.cu's one-query-tile kernel at the
 // kernel head width D = kernel_dim(d)): the fp32 partial outputs through
-// `top` ({D, Nq, n_splits*B*H}, box {32, 128, 1}; the 32-column boxes at or
-// past d unwritten) and the partial LSE; launch_fwd_splitkv calls it and
-// then merges.
+// `top` (the 32-column boxes at or past d unwritten) and the partial LSE, as
+// launch_fwd_splitkv describes; launch_fwd_splitkv calls it and then merges.
 cudaError_t launch_fwd_onetile_split(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                      const CUtensorMap& top, float* lse_part, const Shape& s, int Nk, int n_splits,
                                      int kt_per_split, const WaitCfg& wc, cudaStream_t st);

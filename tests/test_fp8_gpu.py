@@ -104,10 +104,10 @@ def test_fp8_forward_within_rounding_bound(B, H, N, d, causal, qk):
     assert np.max(np.abs(f64(lse) - LSE)) <= TOL_LSE
 
 
-@pytest.mark.parametrize("B,H,N,causal", [(1, 2, 4096, False), (1, 1, 6400, True)])
-def test_fp8_long_rows(B, H, N, causal):
-    """Rows of 25-50 key steps per CTA: the ring and barrier phases wrap many times."""
-    d = 128
+@pytest.mark.parametrize("B,H,N,causal,d", [(1, 2, 4096, False, 128), (1, 1, 6400, True, 128),
+                                             (1, 1, 3000, True, 256)])
+def test_fp8_long_rows(B, H, N, causal, d):
+    """Rows of 24-50 key steps per CTA: the ring and barrier phases wrap many times."""
     _, _, args = _quantized(B, H, N, d, seed=870 + N)
     scale = 1.0 / math.sqrt(d)
     o, lse = fa.fa_fwd_fp8(*args, scale, causal)
@@ -159,9 +159,10 @@ def test_incoherent_rotation_helps_with_outlier_channels():
     assert errs[4321] <= 0.1, errs
 
 
-@pytest.mark.parametrize("N,causal", [(1, False), (1, True), (130, True)])
-def test_fp8_short_and_ragged_rows(N, causal):
-    B, H, d = 2, 2, 64
+@pytest.mark.parametrize("N,causal,d", [(1, False, 64), (1, True, 64), (130, True, 64), (1, True, 256),
+                                         (130, False, 256), (257, True, 160)])
+def test_fp8_short_and_ragged_rows(N, causal, d):
+    B, H = 2, 2
     _, _, args = _quantized(B, H, N, d, seed=850 + N)
     scale = 1.0 / math.sqrt(d)
     o, lse = fa.fa_fwd_fp8(*args, scale, causal)

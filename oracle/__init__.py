@@ -6,6 +6,7 @@ benchmark's CPU-baseline / reference arm.  The product path never imports it.
 from .attention_ref import (  # noqa: F401
     attn_fwd_ref,
     attn_fwd_ref_rows,
+    attn_fwd_ref_end_aligned,
     attn_bwd_ref,
     attn_bwd_ref_sampled,
     attn_fwd_dropout_ref,

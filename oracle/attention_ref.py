@@ -135,6 +135,31 @@ def attn_fwd_ref_rows(q, k, v, scale: float, causal: bool,
     return O, LSE
 
 
+def attn_fwd_ref_end_aligned(q, k, v, scale: float) -> Tuple[np.ndarray, np.ndarray]:
+    """Causal attention of a query block against a longer (or shorter) key
+    sequence: O [B,H,Nq,d] and LSE [B,H,Nq] for q [B,H,Nq,d], k, v [B,H,Nk,d].
+
+    The pages define the causal mask only for equal lengths.  Reading used
+    here (and by the library's causal split-KV): the block is the last Nq
+    positions of the Nk-long sequence, so query i sits at position
+    Nk - Nq + i and sees the keys up to it; Nq == Nk is the square mask, a
+    query before position 0 sees no key (O = 0, LSE = -inf, as any empty row).
+    """
+    q, k, v = _as64(q), _as64(k), _as64(v)
+    B, H, Nq, _ = q.shape
+    Nk = k.shape[2]
+    O = np.zeros((B, H, Nq, v.shape[-1]))
+    LSE = np.zeros((B, H, Nq))
+    pos = np.arange(Nq) + (Nk - Nq)
+    for b in range(B):
+        for h in range(H):
+            S = _apply_causal(_scores(q[b, h], k[b, h], scale), pos)
+            P, m, l = _softmax_stats(S)
+            O[b, h] = P @ v[b, h]
+            LSE[b, h] = _lse(m, l)
+    return O, LSE
+
+
 def _grad_v(P: np.ndarray, doh: np.ndarray) -> np.ndarray:
     """dV = P^T dO."""
     return P.T @ doh

@@ -335,6 +335,33 @@ def pin_unequal_lengths(ref):
     assert np.abs(lse - math.log(23)).max() <= 1e-13
 
 
+def pin_causal_end_aligned(ref):
+    """Causal blocks aligned to the end of the keys (query i at position
+    Nk - Nq + i): Nq == Nk is the square causal mask; a block is the last Nq
+    rows of the square problem; one row sees every key; with Q = 0 row i is
+    the mean of V[0 .. Nk - Nq + i] with LSE = ln(Nk - Nq + i + 1); queries
+    before position 0 are empty rows (O = 0, LSE = -inf)."""
+    qf, k, v = _rand((2, 2, 23, 4), 161), _rand((2, 2, 23, 4), 162), _rand((2, 2, 23, 4), 163)
+    o_sq, l_sq = ref.attn_fwd_ref(qf, k, v, 0.4, True)
+    o, lse = ref.attn_fwd_ref_end_aligned(qf, k, v, 0.4)
+    assert np.abs(o - o_sq).max() <= 1e-14 and np.abs(lse - l_sq).max() <= 1e-14
+    o5, l5 = ref.attn_fwd_ref_end_aligned(qf[:, :, -5:], k, v, 0.4)
+    assert np.abs(o5 - o_sq[:, :, -5:]).max() <= 1e-14 and np.abs(l5 - l_sq[:, :, -5:]).max() <= 1e-14
+    o1, l1 = ref.attn_fwd_ref_end_aligned(qf[:, :, :1], k, v, 0.4)
+    o1n, l1n = ref.attn_fwd_ref(qf[:, :, :1], k, v, 0.4, False)
+    assert np.abs(o1 - o1n).max() <= 1e-14 and np.abs(l1 - l1n).max() <= 1e-14
+    oz, lz = ref.attn_fwd_ref_end_aligned(np.zeros((1, 1, 6, 4)), k[:1, :1], v[:1, :1], 0.4)
+    for i in range(6):
+        n = 23 - 6 + i + 1
+        assert np.abs(oz[0, 0, i] - v[0, 0, :n].mean(axis=0)).max() <= 1e-13
+        assert abs(lz[0, 0, i] - math.log(n)) <= 1e-13
+    q30 = _rand((1, 1, 30, 4), 164)
+    o30, l30 = ref.attn_fwd_ref_end_aligned(q30, k[:1, :1], v[:1, :1], 0.4)
+    assert np.all(o30[:, :, :7] == 0) and np.all(np.isneginf(l30[:, :, :7]))
+    o23, l23 = ref.attn_fwd_ref(q30[:, :, 7:], k[:1, :1], v[:1, :1], 0.4, True)
+    assert np.abs(o30[:, :, 7:] - o23).max() <= 1e-14 and np.abs(l30[:, :, 7:] - l23).max() <= 1e-14
+
+
 # ---------------------------------------------------------------------------
 # Dropout: the counter-based generator and the dropout algebra
 # ---------------------------------------------------------------------------
@@ -427,6 +454,7 @@ ALL_PINS = [
     pin_causal_row0_and_n1,
     pin_invariances,
     pin_rows_equals_full,
+    pin_causal_end_aligned,
     pin_finite_differences,
     pin_sampled_gradients,
     pin_gradient_identities,

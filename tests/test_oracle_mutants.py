@@ -73,6 +73,26 @@ def _sampled_drop_last_group(q, k, v, do, s, causal, rows, cols, group=1024):
     return dq, dk, dv
 
 
+def _end_aligned_shifted(shift):
+    """The end-aligned causal block with query i at position Nk - Nq + i + shift
+    (shift = -(Nk - Nq): top-left alignment instead)."""
+    def f(q, k, v, scale):
+        mod = _fresh_oracle()
+        q, k, v = (np.asarray(x, dtype=np.float64) for x in (q, k, v))
+        B, H, Nq, _ = q.shape
+        Nk = k.shape[2]
+        pos = np.arange(Nq) + (Nk - Nq) + (shift if shift is not None else -(Nk - Nq))
+        O = np.zeros((B, H, Nq, v.shape[-1]))
+        L = np.zeros((B, H, Nq))
+        for b in range(B):
+            for h in range(H):
+                P, m, l = mod._softmax_stats(mod._apply_causal(mod._scores(q[b, h], k[b, h], scale), pos))
+                O[b, h] = P @ v[b, h]
+                L[b, h] = mod._lse(m, l)
+        return O, L
+    return f
+
+
 MUTANTS = {
     "scores_without_scale": {"_scores": lambda q, k, s: q @ k.T},
     "scores_transposed": {"_scores": lambda q, k, s: s * (k @ q.T)},
@@ -95,6 +115,8 @@ MUTANTS = {
     "philox_nine_rounds": {"philox4x32_10": _philox_rounds(9)},
     "sampled_cols_off_by_one": {"attn_bwd_ref_sampled": _sampled_shifted_cols},
     "sampled_last_group_dropped": {"attn_bwd_ref_sampled": _sampled_drop_last_group},
+    "end_aligned_top_left": {"attn_fwd_ref_end_aligned": _end_aligned_shifted(None)},
+    "end_aligned_off_by_one": {"attn_fwd_ref_end_aligned": _end_aligned_shifted(-1)},
 }
 
 

@@ -114,16 +114,9 @@ def test_splitkv_rejects_short_workspace():
 
 
 # Causal split-KV: the query block is the last Nq positions of the Nk-long
-# sequence (query i at position Nk - Nq + i), so the oracle is the plain
-# definition evaluated at those positions of a query array of Nk rows.
+# sequence (query i at position Nk - Nq + i), the oracle's end-aligned mask.
 def _causal_ref(x, scale):
-    q, k, v = f64(x["q"]), f64(x["k"]), f64(x["v"])
-    B, H, Nq, d = q.shape
-    Nk = k.shape[2]
-    qp = np.zeros((B, H, Nk, d))
-    qp[:, :, Nk - Nq:] = q
-    rows = np.broadcast_to(np.arange(Nk - Nq, Nk), (B, H, Nq))
-    return oracle.attn_fwd_ref_rows(qp, k, v, scale, True, rows)
+    return oracle.attn_fwd_ref_end_aligned(f64(x["q"]), f64(x["k"]), f64(x["v"]), scale)
 
 
 CAUSAL_CASES = [
